@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs for the MoE decode block.
+
+This module holds no arithmetic of the method: it only draws random tensors with the
+shapes and distributions of the pages' workload (a Qwen3-30B-A3B-shaped MoE layer:
+H=2048, I=768, E=128 experts, top-8) and of the large-batch case (H=4096, I=1536), and
+converts them to the bit patterns the CPU oracle takes.  Both the CUDA path and the oracle
+receive the very same tensors from here.
+
+Recipe (every tensor has its own sub-seed, a CRC32 of "<workload>/<layer>/<tensor>" mixed
+with the run seed, so any tensor can be regenerated alone):
+
+* h ~ N(0, 1) rounded to bf16, shape [M, H];
+* router W_r ~ N(0, 0.02) bf16 [H, E]; optional per-expert router bias ~ N(0, 1) fp32 [E];
+* dense W_gate, W_up ~ N(0, 0.02) bf16 [E, H, I]; W_down ~ N(0, 0.02) bf16 [E, I, H];
+* blockwise VQ gate/up: index maps J uniform in [0, K) uint8 [E, H/d, I]; layer-shared code
+  books ~ N(0, 0.02) bf16 [K, d] (one for gate, one for up); down stays dense bf16.
+"""
+from __future__ import annotations
+
+import dataclasses
+import zlib
+from typing import Optional
+
+import numpy as np
+import torch
+
+W_DENSE = 0
+W_VQ = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    H: int
+    I: int
+    E: int
+    k: int
+    b: int
+    M: int
+    kind: int = W_DENSE
+    d: int = 4
+    K: int = 256
+    router_bias: bool = False
+    layers: int = 1
+    residual: bool = False
+    w_std: float = 0.02
+    h_std: float = 1.0
+
+
+# The five workloads: a single decode layer at one token, the same layer at 21 tokens (the
+# route-block page's fixture size), a 48-layer MoE-only residual stack, a VQ gate/up layer,
+# and a large-batch layer with a biased router.
+WORKLOADS = {
+    "layer_m1": Workload("layer_m1", H=2048, I=768, E=128, k=8, b=8, M=1),
+    "layer_m21": Workload("layer_m21", H=2048, I=768, E=128, k=8, b=8, M=21),
+    "stack48": Workload("stack48", H=2048, I=768, E=128, k=8, b=8, M=1, layers=48,
+                        residual=True),
+    "vq_d4": Workload("vq_d4", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=4, K=256),
+    "large_m256": Workload("large_m256", H=4096, I=1536, E=128, k=8, b=64, M=256,
+                           router_bias=True),
+}
+
+
+def workload(name: str, **overrides) -> Workload:
+    return dataclasses.replace(WORKLOADS[name], **overrides)
+
+
+def sub_seed(seed: int, wl_name: str, layer: int, tensor: str) -> int:
+    tag = ("%s/%d/%s" % (wl_name, layer, tensor)).encode()
+    return (zlib.crc32(tag) ^ (seed * 0x9E3779B1)) & 0x7FFFFFFFFFFF
+
+
+def _gen(device, s):
+    g = torch.Generator(device=device)
+    g.manual_seed(s)
+    return g
+
+
+def _normal_bf16(shape, std, device, s):
+    t = torch.randn(*shape, generator=_gen(device, s), device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
+
+
+def make_hidden(wl: Workload, M: Optional[int] = None, seed: int = 0, device="cpu",
+                tag: str = "h") -> torch.Tensor:
+    M = wl.M if M is None else M
+    return _normal_bf16((M, wl.H), wl.h_std, device, sub_seed(seed, wl.name, 0, tag))
+
+
+def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu") -> dict:
+    """All parameters of one MoE layer as torch tensors on ``device``."""
+    H, I, E = wl.H, wl.I, wl.E
+    s = lambda t: sub_seed(seed, wl.name, layer, t)  # noqa: E731
+    p = {"kind": wl.kind, "H": H, "I": I, "E": E, "d": wl.d, "K": wl.K}
+    p["w_router"] = _normal_bf16((H, E), wl.w_std, device, s("w_router"))
+    if wl.router_bias:
+        p["bias"] = torch.randn(E, generator=_gen(device, s("bias")), device=device,
+                                dtype=torch.float32)
+    else:
+        p["bias"] = None
+    if wl.kind == W_DENSE:
+        p["w_gate"] = _normal_bf16((E, H, I), wl.w_std, device, s("w_gate"))
+        p["w_up"] = _normal_bf16((E, H, I), wl.w_std, device, s("w_up"))
+    else:
+        if H % wl.d:
+            raise ValueError("H must be a multiple of d")
+        p["j_gate"] = torch.randint(0, wl.K, (E, H // wl.d, I), generator=_gen(device, s("j_gate")),
+                                    device=device, dtype=torch.int32).to(torch.uint8)
+        p["j_up"] = torch.randint(0, wl.K, (E, H // wl.d, I), generator=_gen(device, s("j_up")),
+                                  device=device, dtype=torch.int32).to(torch.uint8)
+        p["cb_gate"] = _normal_bf16((wl.K, wl.d), wl.w_std, device, s("cb_gate"))
+        p["cb_up"] = _normal_bf16((wl.K, wl.d), wl.w_std, device, s("cb_up"))
+    p["w_down"] = _normal_bf16((E, I, H), wl.w_std, device, s("w_down"))
+    return p
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> C-contiguous numpy uint16 bit patterns (on the host)."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected a bf16 tensor")
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_weights(layer: dict, experts=None) -> dict:
+    """Host copies of a layer's expert weights in the oracle's dict form.
+
+    ``experts`` (optional, sorted list of expert ids) restricts the copy to those experts
+    and renumbers them 0..len-1; the caller must renumber routes the same way.
+    """
+    def sel(t):
+        if t is None:
+            return None
+        if experts is not None:
+            t = t[torch.as_tensor(experts, device=t.device, dtype=torch.long)]
+        return t
+
+    w = {"kind": layer["kind"], "H": layer["H"], "I": layer["I"],
+         "E": layer["E"] if experts is None else len(experts),
+         "d": layer.get("d", 0), "K": layer.get("K", 0)}
+    if layer["kind"] == W_DENSE:
+        w["w_gate"] = bits(sel(layer["w_gate"]))
+        w["w_up"] = bits(sel(layer["w_up"]))
+    else:
+        w["j_gate"] = sel(layer["j_gate"]).cpu().numpy()
+        w["j_up"] = sel(layer["j_up"]).cpu().numpy()
+        w["cb_gate"] = bits(layer["cb_gate"])
+        w["cb_up"] = bits(layer["cb_up"])
+    w["w_down"] = bits(sel(layer["w_down"]))
+    return w
