@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE decode block (one JSON line on stdout, rank 0).
+
+A step is one pass of the whole block -- router GEMV + softmax top-k, alignment, gate/up +
+SiLU, down + weighted combine -- over one batch of seeded synthetic input, through the C ABI
+(moe_decode_block).  Default workload: one Qwen3-30B-A3B-shaped MoE layer (H=2048, I=768,
+E=128, k=8, b=8) at M=21 decode tokens.  Successive steps cycle through several
+independently drawn weight sets, so every step reads its experts from HBM, not from L2.
+
+value   = decode tokens/s over all ranks (M * steps * ranks / max-over-ranks time);
+e2e     = the same metric through moe_decode_block_host (host h in, host out back, the
+          copies inside the timed region);
+roofline= the gate/up kernel (the dominant one): algorithmic bytes per launch / its mean
+          duration from CUDA events recorded around it on its stream, over a traced pass of
+          the same steps right after the timed region;
+cpu_baseline = the fp64 CPU oracle on a bounded sample of the same workload.
+
+`--impl reference` times the oracle alone (the reference arm: there is no other
+implementation of this block to run) and prints the same line with "impl": "reference".
+Under torchrun every rank runs its own replica of the workload on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routed_expert_ffn_top_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "MoE-block decode µs/layer, tokens/s & HBM GB/s vs ~8 TB/s peak, M=1..256"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="layer_m21", choices=sorted(syn.WORKLOADS))
+    p.add_argument("--M", type=int, default=None, help="override the token count")
+    p.add_argument("--weight-sets", type=int, default=8,
+                   help="independent weight sets cycled by single-layer workloads")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-extras", action="store_true",
+                   help="time the block only (no trace, e2e, CPU baseline): for profilers")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------ ranks
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemv.cu", "ptx.cuh", "moe_internal.cuh"):
+        with open(os.path.join(ROOT, "routed_expert_ffn_top_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source; otherwise None."""
+    path = os.path.join(PROFILES, "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d[kernel][workload]
+        if ent.get("source_hash") != kernel_source_hash():
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+def expert_bytes(wl):
+    """Bytes of one expert's weights that the block streams (gate/up representation + down)."""
+    if wl.kind == syn.W_DENSE:
+        gu = 2 * wl.H * wl.I * 2
+    else:
+        gu = 2 * (wl.H // wl.d) * wl.I
+    return gu, wl.I * wl.H * 2
+
+
+# ------------------------------------------------------------------------------ ours
+def run_ours(args, world, rank, local):
+    from routed_expert_ffn_top_gb300 import build as lib_build
+    from routed_expert_ffn_top_gb300 import moe
+
+    lib_build.build()
+    dev = torch.device("cuda", local)
+    wl = syn.workload(args.workload, **({"M": args.M} if args.M else {}))
+    M = wl.M
+    stack = wl.layers > 1
+    n_sets = wl.layers if stack else max(1, args.weight_sets)
+    layers = [syn.make_layer(wl, layer=i, seed=1 + rank, device=dev) for i in range(n_sets)]
+    h0 = syn.make_hidden(wl, seed=1 + rank, device=dev)
+    ws = moe.alloc_workspace(layers[0], M, wl.k, wl.b, dev)
+    out = [torch.empty_like(h0) for _ in range(2)]
+    ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
+    wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_block = 4
+
+    def step(i):
+        """One step: a single layer, or all L layers of the residual stack."""
+        if stack:
+            h = h0
+            for li in range(n_sets):
+                o = out[li % 2]
+                moe.moe_decode_block(h, layers[li], wl.k, wl.b, residual=h, out=o, topk_ids=ids,
+                                     topk_weights=wts, workspace=ws, stream=stream)
+                h = o
+        else:
+            moe.moe_decode_block(h0, layers[i % n_sets], wl.k, wl.b, out=out[0], topk_ids=ids,
+                                 topk_weights=wts, workspace=ws, stream=stream)
+
+    blocks_per_step = n_sets if stack else 1
+
+    # unique experts each weight set routes to (bytes actually streamed per block)
+    gu_b, dn_b = expert_bytes(wl)
+    per_set_unique = []
+    if stack:
+        h = h0
+        for li in range(n_sets):
+            o = out[li % 2]
+            moe.moe_decode_block(h, layers[li], wl.k, wl.b, residual=h, out=o, topk_ids=ids,
+                                 topk_weights=wts, workspace=ws)
+            per_set_unique.append(int(torch.unique(ids).numel()))
+            h = o
+    else:
+        for li in range(n_sets):
+            moe.moe_decode_block(h0, layers[li], wl.k, wl.b, out=out[0], topk_ids=ids,
+                                 topk_weights=wts, workspace=ws)
+            per_set_unique.append(int(torch.unique(ids).numel()))
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if moe.moe_read_device_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    t_ms = ev0.elapsed_time(ev1)
+    t_ms = max_over_ranks(t_ms, world)
+    clocks = clk.summary()
+    status = moe.moe_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %#x after the timed region" % status)
+
+    ms_per_step = t_ms / args.steps
+    tokens = M * args.steps * world
+    value = tokens / (t_ms / 1e3)
+    # unique routed-expert bytes of the steps that ran
+    if stack:
+        step_bytes = sum(per_set_unique) * (gu_b + dn_b)
+    else:
+        step_bytes = statistics.mean(per_set_unique[i % n_sets] for i in range(args.steps)) * (gu_b + dn_b)
+    router_bytes = wl.H * wl.E * 2 * blocks_per_step
+    hbm_gbs = (step_bytes + router_bytes) / (ms_per_step * 1e-3) / 1e9
+    us_per_layer = ms_per_step * 1e3 / blocks_per_step
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) hidden states, N(0,0.02) bf16 weights)",
+        "config": {"workload": wl.name, "M": M, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "b": wl.b, "layers_per_step": blocks_per_step,
+                   "weight_kind": "dense_bf16" if wl.kind == syn.W_DENSE else "vq_d%d" % wl.d,
+                   "l2": ("inputs larger than L2: %d independent weight sets of %.2f GB cycled"
+                          % (n_sets, wl.E * (gu_b + dn_b) / 1e9)),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "us_per_layer": round(us_per_layer, 3),
+        "hbm_gbs_unique_expert_bytes": round(hbm_gbs, 1),
+        "unique_experts_per_layer": round(statistics.mean(per_set_unique), 2),
+        "gpu_launches": launches_per_block * blocks_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if args.no_extras:
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        return
+
+    # --- traced pass: per-kernel durations from events recorded around the kernels
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    dur = {"router": [], "align": [], "gateup": [], "down": []}
+
+    def traced_block(h, li, res, o):
+        moe.moe_set_trace_events(evs)
+        try:
+            moe.moe_decode_block(h, layers[li], wl.k, wl.b, residual=res, out=o, topk_ids=ids,
+                                 topk_weights=wts, workspace=ws, stream=stream)
+        finally:
+            moe.moe_set_trace_events(None)
+        evs[4].synchronize()
+        dur["router"].append(evs[0].elapsed_time(evs[1]))
+        dur["align"].append(evs[1].elapsed_time(evs[2]))
+        dur["gateup"].append(evs[2].elapsed_time(evs[3]))
+        dur["down"].append(evs[3].elapsed_time(evs[4]))
+
+    for i in range(args.steps):
+        if stack:
+            h = h0
+            for li in range(n_sets):
+                traced_block(h, li, h, out[li % 2])
+                h = out[li % 2]
+        else:
+            traced_block(h0, i % n_sets, None, out[0])
+    mean_ms = {k: statistics.mean(v) for k, v in dur.items()}
+    peak, peak_kind = measured_peaks()
+    u_mean = statistics.mean(per_set_unique)
+    gu_alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * 4
+    achieved = gu_alg / (mean_ms["gateup"] * 1e-3) / 1e9
+    traffic = recorded_traffic("gateup_dense_kernel", wl.name)
+    result["roofline"] = {
+        "kernel": "gateup_dense_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+        "traffic": traffic, "algorithmic_bytes_per_launch": int(gu_alg),
+        "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
+    }
+    dn_alg = u_mean * dn_b + M * wl.k * wl.I * 4
+    result["down_kernel_gbs"] = round(dn_alg / (mean_ms["down"] * 1e-3) / 1e9, 1)
+
+    # --- e2e: host h in, host out back, copies inside the timed region
+    h_host = h0.cpu().pin_memory()
+    out_host = torch.empty_like(h_host).pin_memory()
+    h_dev = torch.empty_like(h0)
+
+    def e2e_step(i):
+        if stack:  # one host round trip around the whole L-layer stack
+            h_dev.copy_(h_host, non_blocking=True)
+            h = h_dev
+            for li in range(n_sets):
+                moe.moe_decode_block(h, layers[li], wl.k, wl.b, residual=h, out=out[li % 2],
+                                     topk_ids=ids, topk_weights=wts, workspace=ws, stream=stream)
+                h = out[li % 2]
+            out_host.copy_(h, non_blocking=True)
+            stream.synchronize()
+        else:  # the C ABI's host entry point: copy in, block, copy out, synchronise
+            moe.moe_decode_block_host(h_host, layers[i % n_sets], wl.k, wl.b, h_dev, out[0],
+                                      out_host, ids, wts, ws, stream=stream)
+
+    for i in range(max(1, args.warmup)):
+        e2e_step(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+    result["e2e"] = {"value": round(M * args.steps * world / t_e2e, 3), "unit": UNIT,
+                     "h2d_bytes_per_step": M * wl.H * 2, "d2h_bytes_per_step": M * wl.H * 2}
+
+    # --- CPU baseline: the oracle on a bounded sample (rank 0 only, N = 1 only)
+    if rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(wl, layers[0], h0, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def _oracle_block_sample(wl, layer, h, tokens):
+    """Host copies for the oracle: full router, and only the experts the sample uses."""
+    import oracle
+    bias = layer.get("bias")
+    bias = None if bias is None else bias.detach().cpu().numpy()
+    hb = syn.bits(h[:tokens])
+    wr = syn.bits(layer["w_router"])
+    logits = oracle.router_logits(hb, wr, bias, tokens, wl.H, wl.E)
+    ids, _, _ = oracle.topk_softmax(logits, wl.k)
+    used = sorted(set(ids.reshape(-1).tolist()))
+    w = syn.oracle_weights(layer, used)
+    remap = {e: i for i, e in enumerate(used)}
+    return hb, wr, bias, w, remap
+
+
+def _time_oracle_block(wl, hb, wr, bias, w, remap, tokens):
+    """One timed oracle pass over the sample: routing + expert FFN + combine."""
+    import oracle
+    t0 = time.perf_counter()
+    logits = oracle.router_logits(hb, wr, bias, tokens, wl.H, wl.E)
+    ids, wts, _ = oracle.topk_softmax(logits, wl.k)
+    local = np.vectorize(remap.get)(ids).astype(np.int32)
+    oracle.expert_ffn(hb, w, local, wts)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, layer, h, seconds):
+    import oracle
+    oracle.build()
+    tokens = h.shape[0]
+    hb, wr, bias, w, remap = _oracle_block_sample(wl, layer, h, tokens)
+    total, n = 0.0, 0
+    while total < seconds or n == 0:
+        total += _time_oracle_block(wl, hb, wr, bias, w, remap, tokens)
+        n += 1
+    return {"value": round(tokens * n / total, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d full passes of the %s block (%d tokens, all routed experts), "
+                      "single-threaded fp64 C oracle, %.1f s" % (n, wl.name, tokens, total)}
+
+
+# ------------------------------------------------------------------------- reference
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = syn.workload(args.workload, **({"M": args.M} if args.M else {}))
+    layer = syn.make_layer(wl, layer=0, seed=1, device="cpu")
+    h = syn.make_hidden(wl, seed=1, device="cpu")
+    # each step: the oracle's full block on a sample of at most 8 tokens of the batch
+    tokens = min(wl.M, 8)
+    hb, wr, bias, w, remap = _oracle_block_sample(wl, layer, h, tokens)
+    for _ in range(args.warmup):
+        _time_oracle_block(wl, hb, wr, bias, w, remap, tokens)
+    times = [_time_oracle_block(wl, hb, wr, bias, w, remap, tokens) for _ in range(args.steps)]
+    total = sum(times)
+    value = tokens * args.steps / total
+    blocks = wl.layers if wl.layers > 1 else 1
+    sample = ("%d of the %d tokens of the %s batch per step (one layer), single-threaded fp64 "
+              "C oracle" % (tokens, wl.M, wl.name))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "b": wl.b, "layers_per_step": blocks},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) small-batch MoE decode block.
+ *
+ * The block, as the pages define it:
+ *   * router: logits = h W_r (+ bias), softmax, top-k experts, affinities a renormalised
+ *     over the k selected experts ("A Multi-Engine Dataflow for MoE Decoding on
+ *     Scratchpad-Based Tensor Accelerators", MoE block background around Figure 2);
+ *   * alignment: the M x k expert ids flattened row-major into route ids r = m*k + j,
+ *     valid routes grouped by expert in ascending route id, each expert padded to a
+ *     multiple of b rows, plus a parallel expert-per-block vector ("Route-Block Membership
+ *     Selects Packed-AWQ Arithmetic", Sections 2.1 and 5.3);
+ *   * expert FFN: p = SiLU(h W_gate[e]) * (h W_up[e]), y = p W_down[e] (Multi-Engine
+ *     Dataflow page, stage-3 activation and Section 4.3; "Channel Selection for
+ *     Mixture-of-Experts Decoding Needs No Calibration Data", Background);
+ *   * combine: out[m] = residual[m] + sum_j a_{m,j} y_{m,j} (Multi-Engine Dataflow page,
+ *     Section 4.3, "accumulated summation");
+ *   * optional blockwise-VQ gate/up: column i of W_e cut into length-d blocks along H,
+ *     block q replaced by code word J_e[q][i] of a layer-shared code book
+ *     (Multi-Engine Dataflow page, Section 2.3).
+ *
+ * Conventions shared by every entry point
+ *   * Pointers named h, w_*, j_*, cb_*, bias, topk_*, sorted_route_ids, expert_block_ids,
+ *     num_padded, residual, out and workspace are DEVICE pointers, row-major and
+ *     contiguous, each 16-byte aligned.  The caller owns and allocates every buffer;
+ *     the library allocates no device or host memory.
+ *   * bf16 tensors are IEEE bfloat16 (uint16 storage).  Accumulation is fp32.
+ *   * `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Calls are stream-ordered and asynchronous: they never synchronise, except
+ *     moe_read_device_status and the *_host entry point, which say so.
+ *   * Argument errors are reported synchronously, before anything is launched.  Shapes
+ *     the kernels do not support fail closed with MOE_ERR_UNSUPPORTED.
+ *   * Conditions found on the device (an expert id outside [0, E), a bounded device wait
+ *     that gave up) never trap: they set bits in a status word inside the workspace, read
+ *     back with moe_read_device_status.
+ *   * Every reduction runs in an order fixed by tile indices only (never by grid size,
+ *     block position or atomic arrival order), so results are bitwise reproducible run
+ *     to run, and a route's output bits do not depend on which aligned block it lands in.
+ *
+ * Supported shapes: 1 <= k <= min(E, 32); 8 <= E <= 512, E % 8 == 0; H % 128 == 0 and
+ * 128 <= H <= 8192; I % 128 == 0 and 128 <= I <= 8192; (H/8) * E * 2 <= 131072 bytes
+ * (router slice); b >= 1 and (b <= 8 or b % 8 == 0); 0 <= M; M * k < 2^24.
+ * VQ: d == 4, K == 256.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL or misaligned pointer, negative size, bad enum */
+    MOE_ERR_UNSUPPORTED = 2,   /* a shape outside the supported range (fails closed) */
+    MOE_ERR_WORKSPACE = 3,     /* workspace or alignment capacity smaller than required */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
+    MOE_ERR_DEVICE = 5         /* moe_read_device_status: the device set a status bit */
+} moe_status_t;
+
+/* Bits of the device status word. */
+#define MOE_DEV_INVALID_EXPERT 0x1  /* a route's expert id was outside [0, E): excluded */
+#define MOE_DEV_WAIT_TIMEOUT   0x2  /* a bounded device wait gave up; outputs undefined */
+#define MOE_DEV_BAD_ALIGNMENT  0x4  /* an aligned row disagreed with topk_ids: skipped */
+
+/* Weight representations of the gate/up projections. */
+#define MOE_W_DENSE_BF16 0
+#define MOE_W_VQ_GATEUP  1
+
+/*
+ * One MoE layer's expert weights (all device pointers).
+ *   kind == MOE_W_DENSE_BF16: w_gate, w_up [E,H,I] bf16 (row h of expert e holds I
+ *     contiguous values); j_*, cb_* unused.
+ *   kind == MOE_W_VQ_GATEUP: j_gate, j_up [E,H/d,I] uint8 index maps (expert-private);
+ *     cb_gate, cb_up [K,d] bf16 code books (layer-shared), W[e][d*q+t][i] =
+ *     cb[J[e][q][i]][t]; w_gate, w_up unused.
+ *   w_down [E,I,H] bf16 in both cases (the down projection stays dense).
+ */
+typedef struct moe_expert_weights {
+    int32_t kind;
+    int32_t H, I, E;
+    const void *w_gate;
+    const void *w_up;
+    const uint8_t *j_gate;
+    const uint8_t *j_up;
+    const void *cb_gate;
+    const void *cb_up;
+    int32_t d, K;
+    const void *w_down;
+} moe_expert_weights_t;
+
+/* A short static description of a status code (never NULL). */
+const char *moe_status_string(int status);
+
+/*
+ * Router: logits = h W_r (+ bias), top-k, affinities.
+ *   h [M,H] bf16; w_router [H,E] bf16; bias [E] fp32 or NULL (added to the logits, used
+ *   for both selection and affinities).
+ *   Outputs topk_ids [M,k] int32 (slot j = j-th largest logit, ties to the lower expert
+ *   id) and topk_weights [M,k] fp32: renormalize != 0 gives softmax over the k selected
+ *   logits; renormalize == 0 gives the full softmax over E at the selected experts.
+ *   Logits accumulate in fp32 in a fixed order (independent of M).
+ */
+int moe_route_topk(const void *h, const void *w_router, const float *bias, int M, int H,
+                   int E, int k, int renormalize, int32_t *topk_ids, float *topk_weights,
+                   void *stream);
+
+/* Rows the alignment can need: M*k + min(E, M*k) * (b - 1).  Returns 0 on bad sizes. */
+size_t moe_align_capacity(int M, int k, int E, int b);
+
+/*
+ * Stable block alignment ("Route-Block Membership ...", Sections 2.1, 3.1, 5.3).
+ *   topk_ids [M,k] int32.  Route r = m*k + j is valid when 0 <= topk_ids[r] < E; invalid
+ *   routes are excluded.  For each expert e in ascending order with n_e > 0 routes:
+ *   its routes in ascending r, then ceil(n_e/b)*b - n_e sentinel rows (value M*k).
+ *   Outputs: sorted_route_ids [cap] int32, expert_block_ids [cap/b] int32 (expert of each
+ *   b-row block, -1 past the last block), num_padded [1] int32 (rows used).  Rows past
+ *   num_padded are sentinels.  cap must be >= moe_align_capacity(M, k, E, b), else
+ *   MOE_ERR_WORKSPACE.  Atomic-free ordering: bitwise identical on every run.
+ */
+int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
+                         int32_t *sorted_route_ids, int32_t *expert_block_ids,
+                         int32_t *num_padded, size_t cap, void *stream);
+
+/*
+ * Workspace bytes that moe_expert_ffn / moe_decode_block need for (weights shape, M, k, b).
+ * The workspace must be zero-filled before its first use; every call that completes
+ * without a device wait timeout leaves its counters zero again, so it can be reused by
+ * stream-ordered calls without clearing.  Returns 0 on unsupported arguments.
+ */
+size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b);
+
+/*
+ * Expert FFN + affinity-weighted combine for given routes.
+ *   h [M,H] bf16; topk_ids [M,k] int32; topk_weights [M,k] fp32; residual [M,H] bf16 or
+ *   NULL; out [M,H] bf16 = bf16(residual + sum_j a_j y_j) (tokens with no valid route get
+ *   the residual, or zero).
+ *   Alignment: either all three of sorted_route_ids / expert_block_ids / num_padded as
+ *   produced by moe_align_block_size for (topk_ids, E, b) -- every valid route exactly
+ *   once -- or all three NULL, in which case the alignment is computed into the workspace.
+ *   workspace: ws_bytes >= moe_workspace_bytes(w, M, k, b), zero-filled before first use.
+ */
+int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
+                   const int32_t *topk_ids, const float *topk_weights,
+                   const int32_t *sorted_route_ids, const int32_t *expert_block_ids,
+                   const int32_t *num_padded, int b, const void *residual, void *out,
+                   void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * The whole block: router (renormalised softmax top-k) -> alignment -> expert FFN ->
+ * combine.  Same arguments as above; topk_ids [M,k] and topk_weights [M,k] are outputs.
+ */
+int moe_decode_block(const void *h, const void *w_router, const float *bias,
+                     const moe_expert_weights_t *w, int M, int k, int b,
+                     const void *residual, void *out, int32_t *topk_ids,
+                     float *topk_weights, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * moe_decode_block with HOST input and output: copies h_host [M,H] bf16 (and residual_host
+ * if not NULL) into the caller's device staging buffers h_dev / residual_dev, runs the
+ * block, copies out_dev [M,H] back to out_host, and synchronises `stream` before returning.
+ * Host buffers should be pinned (page-locked) for asynchronous copies.
+ */
+int moe_decode_block_host(const void *h_host, const void *residual_host, void *out_host,
+                          void *h_dev, void *residual_dev, void *out_dev,
+                          const void *w_router, const float *bias,
+                          const moe_expert_weights_t *w, int M, int k, int b,
+                          int32_t *topk_ids, float *topk_weights, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+/*
+ * Tracing.  When `events` is not NULL, each later moe_decode_block / moe_expert_ffn call
+ * made from this host thread records the caller's CUDA events (cudaEvent_t passed as
+ * void*) on its stream: events[0] before its first kernel, events[1] after the router,
+ * events[2] after the alignment, events[3] after the gate/up kernel, events[4] after the
+ * down kernel (stages a call does not run are not recorded; n must be 5).  An event
+ * between two kernels removes the launch overlap the kernels otherwise get, so traced
+ * calls run slightly slower.  Pass NULL (n = 0) to stop tracing.
+ */
+int moe_set_trace_events(void *const *events, int n);
+
+/*
+ * Synchronises `stream`, reads the workspace's device status word into *status_out and
+ * clears it.  Returns MOE_OK when the word was zero, MOE_ERR_DEVICE when any bit was set.
+ */
+int moe_read_device_status(void *workspace, void *stream, int32_t *status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

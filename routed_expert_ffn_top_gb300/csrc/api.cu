@@ -1,0 +1,420 @@
+// api.cu -- the C ABI (include/moe.h): argument validation, workspace layout, TMA tensor
+// maps and the stream-ordered orchestration of the kernels.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+Dims make_dims(int M, int k, int E, int H, int I, int b) {
+    Dims d;
+    d.M = M;
+    d.k = k;
+    d.E = E;
+    d.H = H;
+    d.I = I;
+    d.b = b;
+    d.rsub = (b <= kNT) ? b : kNT;
+    d.R = (int64_t)M * k;
+    d.cap = d.R + (int64_t)(d.R < E ? d.R : E) * (b - 1);
+    d.max_sub = d.cap / d.rsub;
+    d.n_it = I / kTI;
+    d.n_hg = H / kHG;
+    d.n_ht = H / kTN;
+    d.n_ig = I / kIG;
+    return d;
+}
+
+WsLayout ws_layout(const Dims &d) {
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.status = take(64);
+    L.sorted = take((size_t)d.cap * 4);
+    L.blocks = take((size_t)(d.cap / d.b) * 4);
+    L.npad = take(16);
+    L.cnt_gu = take((size_t)d.max_sub * d.n_it * 4);
+    L.cnt_dn = take((size_t)d.M * d.n_ht * 4);
+    L.p = take((size_t)d.R * d.I * 4);
+    L.part_gu = take((size_t)d.n_hg * d.R * d.I * 8);
+    L.part_dn = take((size_t)d.n_ig * d.R * d.H * 4);
+    L.total = off;
+    return L;
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 cudaLaunchAttribute *attrs, int cluster_x) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int n = 0;
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 0) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = cluster_x;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cfg;
+}
+
+// --------------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [outer][inner] of `elem` bytes, box [box_outer][box_inner].
+static bool make_tmap_2d(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int elem,
+                         uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (uint64_t)elem};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+// ------------------------------------------------------------------------------ tracing
+static thread_local cudaEvent_t g_trace[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+static thread_local bool g_tracing = false;
+
+static void trace(int i, cudaStream_t s) {
+    if (g_tracing && g_trace[i]) cudaEventRecord(g_trace[i], s);
+}
+
+extern "C" int moe_set_trace_events(void *const *events, int n) {
+    if (events == nullptr) {
+        g_tracing = false;
+        for (int i = 0; i < 5; ++i) g_trace[i] = nullptr;
+        return MOE_OK;
+    }
+    if (n != 5) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+    g_tracing = true;
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------------ validation
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static int check_router_shape(int M, int H, int E, int k) {
+    if (M < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (E < 8 || E > 512 || E % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (k > E || k > 32) return MOE_ERR_UNSUPPORTED;
+    if (H % 128 != 0 || H < 128 || H > 8192) return MOE_ERR_UNSUPPORTED;
+    if ((size_t)(H / kRouterCluster) * E * 2 > 131072) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)M * k >= (1 << 24)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+static int check_block(int b) {
+    if (b <= 0) return MOE_ERR_INVALID_ARG;
+    if (b > kNT && b % kNT != 0) return MOE_ERR_UNSUPPORTED;
+    if (b > 4096) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+static int check_weights(const moe_expert_weights_t *w) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    if (w->H <= 0 || w->I <= 0 || w->E <= 0) return MOE_ERR_INVALID_ARG;
+    if (w->I % 128 != 0 || w->I < 128 || w->I > 8192) return MOE_ERR_UNSUPPORTED;
+    if (w->H % 128 != 0 || w->H < 128 || w->H > 8192) return MOE_ERR_UNSUPPORTED;
+    if (w->E < 8 || w->E > 512 || w->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!w->w_down || !aligned(w->w_down, 16)) return MOE_ERR_INVALID_ARG;
+    if (w->kind == MOE_W_DENSE_BF16) {
+        if (!w->w_gate || !w->w_up || !aligned(w->w_gate, 16) || !aligned(w->w_up, 16))
+            return MOE_ERR_INVALID_ARG;
+        return MOE_OK;
+    }
+    if (w->kind == MOE_W_VQ_GATEUP) {
+        if (!w->j_gate || !w->j_up || !w->cb_gate || !w->cb_up) return MOE_ERR_INVALID_ARG;
+        if (w->d != 4 || w->K != 256) return MOE_ERR_UNSUPPORTED;
+        return MOE_ERR_UNSUPPORTED;  // the VQ expert kernels are not part of this build
+    }
+    return MOE_ERR_INVALID_ARG;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+extern "C" const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+        case MOE_ERR_WORKSPACE: return "workspace or capacity too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE: return "device status flag set";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int moe_route_topk(const void *h, const void *w_router, const float *bias, int M,
+                              int H, int E, int k, int renormalize, int32_t *topk_ids,
+                              float *topk_weights, void *stream) {
+    int rc = check_router_shape(M, H, E, k);
+    if (rc != MOE_OK) return rc;
+    if (M == 0) return MOE_OK;
+    if (!h || !w_router || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w_router, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_router(static_cast<const __nv_bfloat16 *>(h),
+                                     static_cast<const __nv_bfloat16 *>(w_router), bias, M, H, E, k,
+                                     renormalize, topk_ids, topk_weights,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t moe_align_capacity(int M, int k, int E, int b) {
+    if (M < 0 || k <= 0 || E <= 0 || b <= 0) return 0;
+    const int64_t R = (int64_t)M * k;
+    return (size_t)(R + (int64_t)(R < E ? R : E) * (b - 1));
+}
+
+extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
+                                    int32_t *sorted_route_ids, int32_t *expert_block_ids,
+                                    int32_t *num_padded, size_t cap, void *stream) {
+    if (M < 0 || k <= 0 || E <= 0 || b <= 0) return MOE_ERR_INVALID_ARG;
+    if (E > 4096 || (int64_t)M * k >= (1 << 24)) return MOE_ERR_UNSUPPORTED;
+    if (cap < moe_align_capacity(M, k, E, b)) return MOE_ERR_WORKSPACE;
+    if (!num_padded || (M > 0 && !topk_ids) || (cap > 0 && !sorted_route_ids) ||
+        (cap / b > 0 && !expert_block_ids))
+        return MOE_ERR_INVALID_ARG;
+    if ((topk_ids && !aligned(topk_ids, 4)) || (sorted_route_ids && !aligned(sorted_route_ids, 4)) ||
+        (expert_block_ids && !aligned(expert_block_ids, 4)) || !aligned(num_padded, 4))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_align(topk_ids, M, k, E, b, sorted_route_ids, expert_block_ids,
+                                    num_padded, (int64_t)cap, nullptr, 0, nullptr, 0, nullptr,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b) {
+    if (!w || M < 0 || k <= 0 || k > 32 || k > w->E || check_block(b) != MOE_OK) return 0;
+    if (w->H <= 0 || w->I <= 0 || w->E <= 0) return 0;
+    if ((int64_t)M * k >= (1 << 24)) return 0;
+    return ws_layout(make_dims(M, k, w->E, w->H, w->I, b)).total;
+}
+
+// Runs gate/up and down for aligned routes (alignment pointers already resolved).
+static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims &d,
+                       const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
+                       const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
+                       unsigned char *ws, const WsLayout &L, cudaStream_t stream) {
+    CUtensorMap tm_gate, tm_up, tm_down;
+    if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                      (uint64_t)d.E * d.H, kTI, kHG) ||
+        !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                      (uint64_t)d.E * d.H, kTI, kHG) ||
+        !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
+                      (uint64_t)d.E * d.I, kTN, kIG))
+        return MOE_ERR_CUDA;
+    GemvArgs a;
+    a.h = static_cast<const __nv_bfloat16 *>(h);
+    a.topk_ids = topk_ids;
+    a.topk_wts = topk_weights;
+    a.sorted = sorted;
+    a.blocks = blocks;
+    a.npad = npad;
+    a.residual = static_cast<const __nv_bfloat16 *>(residual);
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.p = reinterpret_cast<float *>(ws + L.p);
+    a.part_gu = reinterpret_cast<float2 *>(ws + L.part_gu);
+    a.part_dn = reinterpret_cast<float *>(ws + L.part_dn);
+    a.cnt_gu = reinterpret_cast<int32_t *>(ws + L.cnt_gu);
+    a.cnt_dn = reinterpret_cast<int32_t *>(ws + L.cnt_dn);
+    a.status = reinterpret_cast<int32_t *>(ws + L.status);
+    a.M = d.M;
+    a.k = d.k;
+    a.E = d.E;
+    a.H = d.H;
+    a.I = d.I;
+    a.b = d.b;
+    a.rsub = d.rsub;
+    a.n_it = d.n_it;
+    a.n_hg = d.n_hg;
+    a.n_ht = d.n_ht;
+    a.n_ig = d.n_ig;
+    cudaError_t err = launch_gateup_dense(tm_gate, tm_up, a, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(3, stream);
+    err = launch_down(tm_down, a, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(4, stream);
+    return MOE_OK;
+}
+
+static int check_ffn_common(const void *h, const moe_expert_weights_t *w, int M, int k, int b,
+                            const void *residual, const void *out, const void *workspace,
+                            size_t ws_bytes) {
+    int rc = check_weights(w);
+    if (rc != MOE_OK) return rc;
+    rc = check_block(b);
+    if (rc != MOE_OK) return rc;
+    if (M < 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || k > w->E || (int64_t)M * k >= (1 << 24)) return MOE_ERR_UNSUPPORTED;
+    if (M == 0) return MOE_OK;
+    if (!h || !out || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
+        (residual && !aligned(residual, 16)))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_workspace_bytes(w, M, k, b)) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
+                              const int32_t *topk_ids, const float *topk_weights,
+                              const int32_t *sorted_route_ids, const int32_t *expert_block_ids,
+                              const int32_t *num_padded, int b, const void *residual, void *out,
+                              void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace, ws_bytes);
+    if (rc != MOE_OK || M == 0) return rc;
+    if (!topk_ids || !topk_weights || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+        return MOE_ERR_INVALID_ARG;
+    const int given = (sorted_route_ids != nullptr) + (expert_block_ids != nullptr) +
+                      (num_padded != nullptr);
+    if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
+    const Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    const WsLayout L = ws_layout(d);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int32_t *sorted = sorted_route_ids, *blocks = expert_block_ids, *npad = num_padded;
+    trace(0, s);
+    if (given == 0) {
+        int32_t *ws_sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+        int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
+        int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
+        cudaError_t err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                                       reinterpret_cast<int32_t *>(ws + L.cnt_gu), d.max_sub * d.n_it,
+                                       reinterpret_cast<int32_t *>(ws + L.cnt_dn), (int64_t)M * d.n_ht,
+                                       reinterpret_cast<int32_t *>(ws + L.status), s);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        trace(2, s);
+        sorted = ws_sorted;
+        blocks = ws_blocks;
+        npad = ws_npad;
+    } else if (!aligned(sorted, 4) || !aligned(blocks, 4) || !aligned(npad, 4)) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    return run_experts(h, w, d, topk_ids, topk_weights, sorted, blocks, npad, residual, out, ws, L, s);
+}
+
+extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,
+                                const moe_expert_weights_t *w, int M, int k, int b,
+                                const void *residual, void *out, int32_t *topk_ids,
+                                float *topk_weights, void *workspace, size_t ws_bytes,
+                                void *stream) {
+    int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace, ws_bytes);
+    if (rc != MOE_OK) return rc;
+    rc = check_router_shape(M, w->H, w->E, k);
+    if (rc != MOE_OK || M == 0) return rc;
+    if (!w_router || !topk_ids || !topk_weights || !aligned(w_router, 16) ||
+        !aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    const Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    const WsLayout L = ws_layout(d);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    trace(0, s);
+    cudaError_t err = launch_router(static_cast<const __nv_bfloat16 *>(h),
+                                    static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H,
+                                    w->E, k, 1, topk_ids, topk_weights, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(1, s);
+    int32_t *ws_sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
+    int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
+    err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                       reinterpret_cast<int32_t *>(ws + L.cnt_gu), d.max_sub * d.n_it,
+                       reinterpret_cast<int32_t *>(ws + L.cnt_dn), (int64_t)M * d.n_ht,
+                       reinterpret_cast<int32_t *>(ws + L.status), s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(2, s);
+    return run_experts(h, w, d, topk_ids, topk_weights, ws_sorted, ws_blocks, ws_npad, residual,
+                       out, ws, L, s);
+}
+
+extern "C" int moe_decode_block_host(const void *h_host, const void *residual_host,
+                                     void *out_host, void *h_dev, void *residual_dev,
+                                     void *out_dev, const void *w_router, const float *bias,
+                                     const moe_expert_weights_t *w, int M, int k, int b,
+                                     int32_t *topk_ids, float *topk_weights, void *workspace,
+                                     size_t ws_bytes, void *stream) {
+    if (!w || M < 0) return MOE_ERR_INVALID_ARG;
+    if (M > 0 && (!h_host || !out_host || !h_dev || !out_dev)) return MOE_ERR_INVALID_ARG;
+    if ((residual_host != nullptr) != (residual_dev != nullptr)) return MOE_ERR_INVALID_ARG;
+    // Validate everything before the first copy, so an error leaves nothing enqueued.
+    int rc = check_ffn_common(h_dev, w, M, k, b, residual_dev, out_dev, workspace, ws_bytes);
+    if (rc != MOE_OK) return rc;
+    rc = check_router_shape(M, w->H, w->E, k);
+    if (rc != MOE_OK || M == 0) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)M * w->H * 2;
+    if (cudaMemcpyAsync(h_dev, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (residual_host &&
+        cudaMemcpyAsync(residual_dev, residual_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    rc = moe_decode_block(h_dev, w_router, bias, w, M, k, b, residual_dev, out_dev, topk_ids,
+                          topk_weights, workspace, ws_bytes, stream);
+    if (rc != MOE_OK) return rc;
+    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+extern "C" int moe_read_device_status(void *workspace, void *stream, int32_t *status_out) {
+    if (!workspace || !status_out || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof v, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    *status_out = v;
+    return v == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}

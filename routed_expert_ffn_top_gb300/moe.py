@@ -1,0 +1,318 @@
+"""Thin ctypes binding of the C ABI in ``include/moe.h`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no arithmetic of
+its own: it checks dtypes/devices/contiguity of torch tensors, allocates outputs the
+caller did not pass, hands raw device pointers and the current CUDA stream to the library,
+and raises :class:`MoeError` on a non-zero status.  The library must have been built
+(``python -m routed_expert_ffn_top_gb300.build`` or ``__graft_entry__.build()``); there is
+no fallback of any kind when it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE = 5
+
+MOE_DEV_INVALID_EXPERT = 0x1
+MOE_DEV_WAIT_TIMEOUT = 0x2
+MOE_DEV_BAD_ALIGNMENT = 0x4
+
+MOE_W_DENSE_BF16 = 0
+MOE_W_VQ_GATEUP = 1
+
+# Every symbol include/moe.h declares (checked against the header by the tests).
+EXPORTS = (
+    "moe_status_string", "moe_route_topk", "moe_align_capacity", "moe_align_block_size",
+    "moe_workspace_bytes", "moe_expert_ffn", "moe_decode_block", "moe_decode_block_host",
+    "moe_read_device_status", "moe_set_trace_events",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, moe_status_string(status), status))
+
+
+class ExpertWeights(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+        ("E", ctypes.c_int32),
+        ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+        ("j_gate", ctypes.c_void_p), ("j_up", ctypes.c_void_p),
+        ("cb_gate", ctypes.c_void_p), ("cb_up", ctypes.c_void_p),
+        ("d", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("w_down", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded CDLL (raises if the library has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "CUDA library %s is missing: build it with "
+                    "`python -m routed_expert_ffn_top_gb300.build`" % path)
+            L = ctypes.CDLL(path)
+            vp, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            wp = ctypes.POINTER(ExpertWeights)
+            L.moe_status_string.argtypes = [ci]
+            L.moe_status_string.restype = ctypes.c_char_p
+            L.moe_route_topk.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp]
+            L.moe_align_capacity.argtypes = [ci, ci, ci, ci]
+            L.moe_align_capacity.restype = sz
+            L.moe_align_block_size.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, sz, vp]
+            L.moe_workspace_bytes.argtypes = [wp, ci, ci, ci]
+            L.moe_workspace_bytes.restype = sz
+            L.moe_expert_ffn.argtypes = [vp, wp, ci, ci, vp, vp, vp, vp, vp, ci, vp, vp, vp, sz, vp]
+            L.moe_decode_block.argtypes = [vp, vp, vp, wp, ci, ci, ci, vp, vp, vp, vp, vp, sz, vp]
+            L.moe_decode_block_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, wp, ci, ci, ci,
+                                                vp, vp, vp, sz, vp]
+            L.moe_read_device_status.argtypes = [vp, vp, vp]
+            L.moe_set_trace_events.argtypes = [vp, ci]
+            for f in ("moe_route_topk", "moe_align_block_size", "moe_expert_ffn",
+                      "moe_decode_block", "moe_decode_block_host", "moe_read_device_status",
+                      "moe_set_trace_events"):
+                getattr(L, f).restype = ci
+            _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------------------- marshalling
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t, dtype, name, device=None):
+    if t is None:
+        raise ValueError("%s is required" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s must be on %s, got %s" % (name, device, t.device))
+    return t
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def expert_weights(layer: dict) -> ExpertWeights:
+    """C weight descriptor for a layer dict (as made by :mod:`.synthetic`).
+
+    The descriptor holds raw pointers; the caller keeps ``layer``'s tensors alive.
+    """
+    w = ExpertWeights()
+    w.kind = int(layer.get("kind", MOE_W_DENSE_BF16))
+    w.H, w.I, w.E = int(layer["H"]), int(layer["I"]), int(layer["E"])
+    w.d, w.K = int(layer.get("d", 0) or 0), int(layer.get("K", 0) or 0)
+    dev = layer["w_down"].device
+    _need(layer["w_down"], torch.bfloat16, "w_down", dev)
+    w.w_down = layer["w_down"].data_ptr()
+    if w.kind == MOE_W_DENSE_BF16:
+        w.w_gate = _need(layer["w_gate"], torch.bfloat16, "w_gate", dev).data_ptr()
+        w.w_up = _need(layer["w_up"], torch.bfloat16, "w_up", dev).data_ptr()
+    else:
+        w.j_gate = _need(layer["j_gate"], torch.uint8, "j_gate", dev).data_ptr()
+        w.j_up = _need(layer["j_up"], torch.uint8, "j_up", dev).data_ptr()
+        w.cb_gate = _need(layer["cb_gate"], torch.bfloat16, "cb_gate", dev).data_ptr()
+        w.cb_up = _need(layer["cb_up"], torch.bfloat16, "cb_up", dev).data_ptr()
+    return w
+
+
+# ------------------------------------------------------------------------------ entry points
+def moe_route_topk(h, w_router, bias, k, renormalize=True, topk_ids=None, topk_weights=None,
+                   stream=None):
+    dev = h.device
+    _need(h, torch.bfloat16, "h", dev)
+    _need(w_router, torch.bfloat16, "w_router", dev)
+    if bias is not None:
+        _need(bias, torch.float32, "bias", dev)
+    M, H = h.shape
+    E = w_router.shape[1]
+    if topk_ids is None:
+        topk_ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((M, k), dtype=torch.float32, device=dev)
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    _need(topk_weights, torch.float32, "topk_weights", dev)
+    _check(lib().moe_route_topk(_ptr(h), _ptr(w_router), _ptr(bias), M, H, E, k,
+                                int(bool(renormalize)), _ptr(topk_ids), _ptr(topk_weights),
+                                _stream(stream)), "moe_route_topk")
+    return topk_ids, topk_weights
+
+
+def moe_align_capacity(M, k, E, b) -> int:
+    return int(lib().moe_align_capacity(M, k, E, b))
+
+
+def moe_align_block_size(topk_ids, E, b, sorted_route_ids=None, expert_block_ids=None,
+                         num_padded=None, stream=None):
+    dev = topk_ids.device
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    M, k = topk_ids.shape
+    cap = moe_align_capacity(M, k, E, b)
+    if sorted_route_ids is None:
+        sorted_route_ids = torch.empty((cap,), dtype=torch.int32, device=dev)
+    if expert_block_ids is None:
+        expert_block_ids = torch.empty((max(cap // b, 1),), dtype=torch.int32, device=dev)
+    if num_padded is None:
+        num_padded = torch.empty((1,), dtype=torch.int32, device=dev)
+    _need(sorted_route_ids, torch.int32, "sorted_route_ids", dev)
+    _need(expert_block_ids, torch.int32, "expert_block_ids", dev)
+    _need(num_padded, torch.int32, "num_padded", dev)
+    if expert_block_ids.numel() < sorted_route_ids.numel() // b:
+        raise ValueError("expert_block_ids must hold cap // b entries")
+    _check(lib().moe_align_block_size(_ptr(topk_ids), M, k, E, b, _ptr(sorted_route_ids),
+                                      _ptr(expert_block_ids), _ptr(num_padded),
+                                      sorted_route_ids.numel(), _stream(stream)),
+           "moe_align_block_size")
+    return sorted_route_ids, expert_block_ids, num_padded
+
+
+def moe_workspace_bytes(layer: dict, M, k, b) -> int:
+    w = expert_weights(layer)
+    return int(lib().moe_workspace_bytes(ctypes.byref(w), M, k, b))
+
+
+def alloc_workspace(layer: dict, M, k, b, device=None) -> torch.Tensor:
+    """A zero-filled workspace of the size the library asks for (256-byte aligned)."""
+    n = moe_workspace_bytes(layer, M, k, b)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED, "moe_workspace_bytes")
+    device = layer["w_down"].device if device is None else device
+    return torch.zeros((n,), dtype=torch.uint8, device=device)
+
+
+def moe_expert_ffn(h, layer, topk_ids, topk_weights, b, alignment=None, residual=None,
+                   out=None, workspace=None, stream=None):
+    dev = h.device
+    _need(h, torch.bfloat16, "h", dev)
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    _need(topk_weights, torch.float32, "topk_weights", dev)
+    M, k = topk_ids.shape
+    w = expert_weights(layer)
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual", dev)
+    if out is None:
+        out = torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)
+    _need(out, torch.bfloat16, "out", dev)
+    if workspace is None:
+        workspace = alloc_workspace(layer, M, k, b, dev)
+    srt = blk = npad = None
+    if alignment is not None:
+        srt, blk, npad = alignment
+    _check(lib().moe_expert_ffn(_ptr(h), ctypes.byref(w), M, k, _ptr(topk_ids),
+                                _ptr(topk_weights), _ptr(srt), _ptr(blk), _ptr(npad), b,
+                                _ptr(residual), _ptr(out), _ptr(workspace), workspace.numel(),
+                                _stream(stream)), "moe_expert_ffn")
+    return out
+
+
+def moe_decode_block(h, layer, k, b, residual=None, out=None, topk_ids=None, topk_weights=None,
+                     workspace=None, stream=None):
+    dev = h.device
+    _need(h, torch.bfloat16, "h", dev)
+    M = h.shape[0]
+    w = expert_weights(layer)
+    w_router = _need(layer["w_router"], torch.bfloat16, "w_router", dev)
+    bias = layer.get("bias")
+    if bias is not None:
+        _need(bias, torch.float32, "bias", dev)
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual", dev)
+    if out is None:
+        out = torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((M, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(layer, M, k, b, dev)
+    _need(out, torch.bfloat16, "out", dev)
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    _need(topk_weights, torch.float32, "topk_weights", dev)
+    _check(lib().moe_decode_block(_ptr(h), _ptr(w_router), _ptr(bias), ctypes.byref(w), M, k, b,
+                                  _ptr(residual), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
+                                  _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_decode_block")
+    return out, topk_ids, topk_weights
+
+
+def moe_decode_block_host(h_host, layer, k, b, h_dev, out_dev, out_host, topk_ids, topk_weights,
+                          workspace, residual_host=None, residual_dev=None, stream=None):
+    """Host in, host out: the library copies h to the device and the result back, and
+    synchronises the stream before returning."""
+    w = expert_weights(layer)
+    bias = layer.get("bias")
+    M = h_host.shape[0]
+    _check(lib().moe_decode_block_host(_ptr(h_host), _ptr(residual_host), _ptr(out_host),
+                                       _ptr(h_dev), _ptr(residual_dev), _ptr(out_dev),
+                                       _ptr(layer["w_router"]), _ptr(bias), ctypes.byref(w), M, k,
+                                       b, _ptr(topk_ids), _ptr(topk_weights), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)),
+           "moe_decode_block_host")
+    return out_host
+
+
+def moe_read_device_status(workspace, stream=None) -> int:
+    """Synchronises the stream, returns the device status bits and clears them."""
+    out = ctypes.c_int32(0)
+    rc = lib().moe_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(out))
+    if rc not in (MOE_OK, MOE_ERR_DEVICE):
+        raise MoeError(rc, "moe_read_device_status")
+    return int(out.value)
+
+
+def moe_set_trace_events(events=None):
+    """Record the given five torch.cuda.Event objects around the block's kernels on every
+    later call from this thread (see include/moe.h); ``None`` stops tracing."""
+    if events is None:
+        _check(lib().moe_set_trace_events(None, 0), "moe_set_trace_events")
+        return
+    events = list(events)
+    for e in events:  # torch creates the CUDA event lazily, on first record
+        if e.cuda_event == 0:
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib().moe_set_trace_events(arr, len(events)), "moe_set_trace_events")

@@ -1,0 +1,118 @@
+"""The C-ABI library builds, loads and exports what include/moe.h declares; host-side
+validation answers without touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as entry
+from routed_expert_ffn_top_gb300 import moe, synthetic as syn
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    entry.build()
+    return moe.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_binding_exports():
+    assert sorted(moe.EXPORTS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert moe.moe_status_string(code)
+    assert moe.moe_status_string(99) == "unknown status"
+
+
+def test_align_capacity_host(lib):
+    assert moe.moe_align_capacity(21, 8, 128, 8) == 168 + 128 * 7
+    assert moe.moe_align_capacity(1, 8, 128, 8) == 8 + 8 * 7
+    assert moe.moe_align_capacity(256, 8, 128, 64) == 2048 + 128 * 63
+    assert moe.moe_align_capacity(0, 8, 128, 8) == 0
+    assert moe.moe_align_capacity(-1, 8, 128, 8) == 0
+
+
+def _weights(kind=0, H=2048, I=768, E=128):
+    w = moe.ExpertWeights()
+    w.kind, w.H, w.I, w.E, w.d, w.K = kind, H, I, E, 4, 256
+    fake = 1 << 20  # a 16-byte aligned non-null address; never dereferenced by validation
+    w.w_gate = w.w_up = w.w_down = fake
+    w.j_gate = w.j_up = w.cb_gate = w.cb_up = fake
+    return w
+
+
+def test_workspace_bytes_host(lib):
+    for name in ("layer_m1", "layer_m21", "large_m256"):
+        wl = syn.WORKLOADS[name]
+        w = _weights(H=wl.H, I=wl.I, E=wl.E)
+        assert lib.moe_workspace_bytes(ctypes.byref(w), wl.M, wl.k, wl.b) > 0
+    w = _weights()
+    assert lib.moe_workspace_bytes(ctypes.byref(w), 4, 0, 8) == 0      # k = 0
+    assert lib.moe_workspace_bytes(ctypes.byref(w), 4, 8, 12) == 0     # b > 8 not a multiple of 8
+    assert lib.moe_workspace_bytes(None, 4, 8, 8) == 0
+
+
+def test_validation_fails_closed_without_gpu(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    ids = vp(1 << 20)
+    # unsupported E (not a multiple of 8), k > E, H not a multiple of 128
+    assert lib.moe_route_topk(fake, fake, None, 1, 2048, 7, 2, 1, ids, ids, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route_topk(fake, fake, None, 1, 2048, 8, 9, 1, ids, ids, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route_topk(fake, fake, None, 1, 2000, 8, 2, 1, ids, ids, None) == moe.MOE_ERR_UNSUPPORTED
+    # NULL and misaligned pointers
+    assert lib.moe_route_topk(None, fake, None, 1, 2048, 128, 8, 1, ids, ids, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_topk(vp((1 << 20) + 2), fake, None, 1, 2048, 128, 8, 1, ids, ids, None) == moe.MOE_ERR_INVALID_ARG
+    # M == 0 is a no-op
+    assert lib.moe_route_topk(None, None, None, 0, 2048, 128, 8, 1, None, None, None) == moe.MOE_OK
+    # alignment capacity too small
+    assert lib.moe_align_block_size(ids, 21, 8, 128, 8, ids, ids, ids, 100, None) == moe.MOE_ERR_WORKSPACE
+    # workspace too small
+    w = _weights()
+    assert lib.moe_expert_ffn(fake, ctypes.byref(w), 4, 8, ids, ids, None, None, None, 8, None,
+                              fake, vp(1 << 20), 16, None) == moe.MOE_ERR_WORKSPACE
+    # half-given alignment
+    need = lib.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8)
+    assert lib.moe_expert_ffn(fake, ctypes.byref(w), 4, 8, ids, ids, ids, None, None, 8, None,
+                              fake, vp(1 << 20), need, None) == moe.MOE_ERR_INVALID_ARG
+    # VQ with unsupported d
+    wv = _weights(kind=1)
+    wv.d = 8
+    assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wv), 1, 8, 8, None, fake, ids, ids,
+                                vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    # unknown weight kind
+    wk = _weights(kind=7)
+    assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wk), 1, 8, 8, None, fake, ids, ids,
+                                vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_oracle_and_product_are_separate():
+    """The product package never imports the oracle (and vice versa)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "routed_expert_ffn_top_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "moe_oracle" not in text, f
+    for f in os.listdir(os.path.join(root, "oracle")):
+        if f.endswith((".py", ".c")):
+            text = open(os.path.join(root, "oracle", f)).read()
+            assert not re.search(r"^\s*(import|from)\s+routed_expert_ffn_top_gb300", text, re.M), f
+            assert not re.search(r'#\s*include\s*"moe', text), f

@@ -1,0 +1,319 @@
+"""CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_ref as G
+import oracle
+import oracle_pins
+from routed_expert_ffn_top_gb300 import moe, synthetic as syn
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as entry
+    entry.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def _random_ids(rng, M, k, E, distinct=True):
+    if distinct and k <= E:
+        return np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32).reshape(M, k)
+    return rng.integers(0, E, size=(M, k)).astype(np.int32)
+
+
+def _random_affinities(rng, M, k):
+    a = rng.random((M, k)) + 0.05
+    return (a / a.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------- router
+@pytest.mark.parametrize("E,k,H,M,bias,renorm", [
+    (128, 8, 2048, 1, False, True), (128, 8, 2048, 21, False, True),
+    (128, 8, 4096, 256, True, True), (8, 1, 128, 5, False, True), (64, 2, 256, 13, True, False),
+    (512, 32, 1024, 3, False, True), (24, 5, 384, 9, True, True), (128, 8, 2048, 64, False, True),
+])
+def test_route_topk(E, k, H, M, bias, renorm):
+    wl = syn.Workload("router_t", H=H, I=128, E=E, k=k, b=8, M=M, router_bias=bias)
+    g = torch.Generator(device=DEV).manual_seed(E * 1000 + M)
+    h = torch.randn(M, H, generator=g, device=DEV).to(torch.bfloat16)
+    layer = {"H": H, "E": E,
+             "w_router": (torch.randn(H, E, generator=g, device=DEV) * 0.02).to(torch.bfloat16),
+             "bias": torch.randn(E, generator=g, device=DEV) if bias else None}
+    ids, wts = moe.moe_route_topk(h, layer["w_router"], layer["bias"], k, renormalize=renorm)
+    torch.cuda.synchronize()
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, k, renorm)
+    _, _, near = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts, logits, k, renorm)
+    assert near <= max(1, M // 50)
+
+
+# --------------------------------------------------------------------------- alignment
+def _gpu_align(ids_np, E, b):
+    ids = torch.as_tensor(ids_np, dtype=torch.int32, device=DEV).reshape(ids_np.shape)
+    srt, blk, npad = moe.moe_align_block_size(ids, E, b)
+    torch.cuda.synchronize()
+    return srt.cpu().numpy(), blk.cpu().numpy(), int(npad.item())
+
+
+def test_align_random_cases_bit_exact():
+    rng = np.random.default_rng(104)
+    n = 0
+    for trial in range(128):
+        M = int(rng.integers(0, 65))
+        k = int(rng.integers(1, 9))
+        E = int(rng.integers(1, 300))
+        b = int(rng.choice([1, 2, 3, 4, 8, 16, 64]))
+        ids = _random_ids(rng, M, k, E, distinct=(trial % 2 == 0)).reshape(M, k)
+        if trial % 4 == 1 and ids.size:
+            mask = rng.random(ids.shape) < 0.15
+            ids[mask] = rng.choice([-1, E, E + 7, -100], size=int(mask.sum()))
+        if M == 0:
+            continue
+        o_srt, o_blk, o_np = oracle.align(ids, E, b)
+        g_srt, g_blk, g_np = _gpu_align(ids, E, b)
+        assert g_np == o_np, trial
+        assert np.array_equal(g_srt, o_srt), trial
+        assert np.array_equal(g_blk[:o_blk.size], o_blk), trial
+        n += 1
+    assert n >= 104
+
+
+def test_align_page_fixture():
+    fx = oracle_pins.load_fixture()
+    ids = oracle_pins.fixture_topk_ids(fx)
+    g_srt, g_blk, g_np = _gpu_align(ids, fx["E"], fx["b"])
+    o_srt, o_blk, o_np = oracle.align(ids, fx["E"], fx["b"])
+    assert g_np == o_np == fx["aligned_rows"]
+    assert int((g_blk >= 0).sum()) == fx["active_blocks"]
+    assert np.array_equal(g_srt, o_srt) and np.array_equal(g_blk, o_blk)
+
+
+def test_align_large_and_deterministic():
+    rng = np.random.default_rng(7)
+    ids = _random_ids(rng, 1024, 8, 256)
+    ref = oracle.align(ids, 256, 16)
+    for run in range(20):
+        g = _gpu_align(ids, 256, 16)
+        assert g[2] == ref[2] and np.array_equal(g[0], ref[0]) and np.array_equal(g[1], ref[1]), run
+
+
+# ------------------------------------------------------------------- expert FFN, small
+SMALL = [
+    # M, k, E, H, I, b
+    (1, 1, 8, 128, 128, 1), (5, 2, 8, 256, 128, 3), (13, 8, 16, 384, 256, 8),
+    (3, 4, 32, 128, 384, 16), (37, 6, 64, 256, 128, 64), (64, 8, 128, 512, 256, 8),
+    (2, 8, 8, 1024, 640, 2), (9, 3, 40, 640, 128, 5),
+]
+
+
+def _small_layer(M, k, E, H, I, b, seed=0, bias=False):
+    wl = syn.Workload("small_%d_%d_%d_%d_%d_%d" % (M, k, E, H, I, b), H=H, I=I, E=E, k=k, b=b,
+                      M=M, router_bias=bias)
+    return wl, syn.make_layer(wl, seed=seed, device=DEV), syn.make_hidden(wl, seed=seed, device=DEV)
+
+
+@pytest.mark.parametrize("M,k,E,H,I,b", SMALL)
+def test_expert_ffn_small(M, k, E, H, I, b):
+    wl, layer, h = _small_layer(M, k, E, H, I, b)
+    rng = np.random.default_rng(M * 31 + E)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    res = syn.make_hidden(wl, seed=5, device=DEV, tag="res")
+    t_ids = torch.as_tensor(ids, device=DEV)
+    t_a = torch.as_tensor(a, device=DEV)
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = G.oracle_ffn(layer, h, ids, a, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "expert_ffn %s" % (SMALL,))
+    # the same call with the caller's own alignment buffers gives the same bits
+    srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
+    out2 = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad), residual=res,
+                              workspace=ws)
+    assert torch.equal(out, out2)
+
+
+def test_expert_ffn_invalid_ids_and_status():
+    M, k, E, H, I, b = 6, 3, 16, 256, 128, 4
+    wl, layer, h = _small_layer(M, k, E, H, I, b, seed=3)
+    ids = np.array([[0, -1, 5], [16, 2, 3], [-5, -1, 99], [7, 7, 1], [15, 0, 4], [9, 10, 11]],
+                   np.int32)
+    a = _random_affinities(np.random.default_rng(1), M, k)
+    res = syn.make_hidden(wl, seed=8, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, torch.as_tensor(ids, device=DEV),
+                             torch.as_tensor(a, device=DEV), b, residual=res, workspace=ws)
+    st = moe.moe_read_device_status(ws)
+    assert st & moe.MOE_DEV_INVALID_EXPERT
+    assert moe.moe_read_device_status(ws) == 0  # read clears
+    ref = G.oracle_ffn(layer, h, ids, a, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "invalid ids")
+    # token 2 has no valid route: its output is exactly the residual
+    assert torch.equal(out[2], res[2])
+
+
+def test_expert_ffn_bad_alignment_is_flagged():
+    M, k, E, H, I, b = 4, 2, 8, 128, 128, 2
+    wl, layer, h = _small_layer(M, k, E, H, I, b, seed=4)
+    ids = np.array([[0, 1], [1, 2], [2, 3], [3, 0]], np.int32)
+    t_ids = torch.as_tensor(ids, device=DEV)
+    a = torch.full((M, k), 0.5, device=DEV)
+    srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
+    srt_bad = srt.clone()
+    s = srt_bad.cpu().numpy()
+    s[0], s[2] = s[2], s[0]  # move a route of expert 1 into expert 0's block
+    srt_bad.copy_(torch.as_tensor(s))
+    ws = moe.alloc_workspace(layer, M, k, b)
+    moe.moe_expert_ffn(h, layer, t_ids, a, b, alignment=(srt_bad, blk, npad), workspace=ws)
+    assert moe.moe_read_device_status(ws) & moe.MOE_DEV_BAD_ALIGNMENT
+
+
+def test_membership_invariance_bitwise():
+    """A route's output bits do not depend on which aligned block it occupies: the
+    route-block page's within-block permutation and boundary exchange both preserve them."""
+    M, k, E, H, I, b = 24, 2, 8, 512, 256, 4
+    wl, layer, h = _small_layer(M, k, E, H, I, b, seed=6)
+    ids = np.stack([[m % 3, 3 + m % 5] for m in range(M)]).astype(np.int32)  # experts with many routes
+    a = _random_affinities(np.random.default_rng(2), M, k)
+    t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
+    srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
+    ws = moe.alloc_workspace(layer, M, k, b)
+    base = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad), workspace=ws)
+    s = srt.cpu().numpy()
+    bl = blk.cpu().numpy()
+    e0_rows = [i for i in range(int(npad.item())) if bl[i // b] == 0 and s[i] < M * k]
+    assert len(e0_rows) >= b + 1  # spans at least two blocks
+    within = s.copy()
+    within[e0_rows[0]], within[e0_rows[1]] = within[e0_rows[1]], within[e0_rows[0]]
+    boundary = s.copy()
+    boundary[e0_rows[b - 1]], boundary[e0_rows[b]] = boundary[e0_rows[b]], boundary[e0_rows[b - 1]]
+    shuffled = s.copy()
+    shuffled[e0_rows] = np.random.default_rng(0).permutation(s[e0_rows])
+    for variant in (within, boundary, shuffled):
+        alt = torch.as_tensor(variant, device=DEV)
+        out = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(alt, blk, npad), workspace=ws)
+        assert torch.equal(out, base)
+    assert moe.moe_read_device_status(ws) == 0
+
+
+def test_expert_ffn_m0_is_noop():
+    wl, layer, h = _small_layer(1, 2, 8, 128, 128, 8)
+    out = torch.zeros(0, 128, dtype=torch.bfloat16, device=DEV)
+    ids = torch.zeros(0, 2, dtype=torch.int32, device=DEV)
+    a = torch.zeros(0, 2, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(1024, dtype=torch.uint8, device=DEV)
+    moe.moe_expert_ffn(h[:0], layer, ids, a, 8, out=out, workspace=ws)
+
+
+# ----------------------------------------------------------------- the five workloads
+_cache = {}
+
+
+def _workload_layer(name, layer_idx=0, seed=0):
+    key = (name, layer_idx, seed)
+    if key not in _cache:
+        _cache.clear()
+        torch.cuda.empty_cache()
+        wl = syn.WORKLOADS[name]
+        _cache[key] = syn.make_layer(wl, layer=layer_idx, seed=seed, device=DEV)
+    return _cache[key]
+
+
+def _check_block(name, M=None, tokens=None, seed=0):
+    wl = syn.WORKLOADS[name]
+    layer = _workload_layer(name, seed=seed)
+    M = wl.M if M is None else M
+    h = syn.make_hidden(wl, M=M, seed=seed, device=DEV)
+    ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
+    out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+    use_ids, use_wts, near = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
+                                             logits, wl.k)
+    ref = G.oracle_ffn(layer, h, use_ids, use_wts, tokens=tokens)
+    got = G.to_f64(out) if tokens is None else G.to_f64(out)[tokens]
+    G.assert_close_block(got, ref, name)
+    return layer, h, ws, out, ids, wts
+
+
+def test_layer_m1():
+    _check_block("layer_m1")
+
+
+def test_layer_m21_alignment_and_20_run_determinism():
+    wl = syn.WORKLOADS["layer_m21"]
+    layer, h, ws, out, ids, wts = _check_block("layer_m21")
+    # alignment of the router's ids: bit-exact against the oracle
+    srt, blk, npad = moe.moe_align_block_size(ids, wl.E, wl.b)
+    o_srt, o_blk, o_np = oracle.align(ids.cpu().numpy(), wl.E, wl.b)
+    assert int(npad.item()) == o_np
+    assert np.array_equal(srt.cpu().numpy(), o_srt)
+    assert np.array_equal(blk.cpu().numpy()[:o_blk.size], o_blk)
+    for run in range(20):
+        out2, ids2, wts2 = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+        assert torch.equal(out2, out) and torch.equal(ids2, ids) and torch.equal(wts2, wts), run
+
+
+def test_batch_invariance_bitwise():
+    wl = syn.WORKLOADS["layer_m21"]
+    layer = _workload_layer("layer_m21")
+    h = syn.make_hidden(wl, seed=0, device=DEV)
+    out, ids, _ = moe.moe_decode_block(h, layer, wl.k, wl.b)
+    for m in (0, 7, 20):
+        o1, i1, _ = moe.moe_decode_block(h[m:m + 1].contiguous(), layer, wl.k, wl.b)
+        assert torch.equal(i1[0], ids[m]) and torch.equal(o1[0], out[m]), m
+    o5, _, _ = moe.moe_decode_block(h[3:8].contiguous(), layer, wl.k, wl.b)
+    assert torch.equal(o5, out[3:8])
+
+
+def test_host_entry_point_matches_device():
+    wl = syn.WORKLOADS["layer_m21"]
+    layer = _workload_layer("layer_m21")
+    h = syn.make_hidden(wl, seed=0, device=DEV)
+    ws = moe.alloc_workspace(layer, wl.M, wl.k, wl.b)
+    out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+    h_host = h.cpu().pin_memory()
+    out_host = torch.empty_like(h_host).pin_memory()
+    h_dev, out_dev = torch.empty_like(h), torch.empty_like(h)
+    moe.moe_decode_block_host(h_host, layer, wl.k, wl.b, h_dev, out_dev, out_host,
+                              torch.empty_like(ids), torch.empty_like(wts), ws)
+    assert torch.equal(out_host, out.cpu())
+
+
+def test_large_m256_sampled_tokens():
+    _check_block("large_m256", tokens=np.array([0, 1, 77, 128, 200, 254, 255]))
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+def test_stack48_teacher_forced(M):
+    """48-layer MoE-only residual stack h <- bf16(h + moe(h)); each sampled layer is checked
+    against the oracle fed with that layer's GPU input (teacher forcing)."""
+    wl = syn.WORKLOADS["stack48"]
+    L = wl.layers
+    rng = np.random.default_rng(M)
+    sampled = sorted({0, 23, L - 1} | set(rng.choice(L, 3, replace=False).tolist()))
+    h = syn.make_hidden(wl, M=M, seed=0, device=DEV)
+    ws = None
+    tokens = None if M <= 16 else np.array([0, 5, 31, 63])
+    for layer_idx in range(L):
+        if layer_idx not in sampled:
+            # unsampled layers still run, on the same seeded weights recipe
+            pass
+        layer = syn.make_layer(wl, layer=layer_idx, seed=0, device=DEV)
+        if ws is None:
+            ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
+        out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, residual=h, workspace=ws)
+        if layer_idx in sampled:
+            o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+            use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids,
+                                                  o_wts, logits, wl.k)
+            ref = G.oracle_ffn(layer, h, use_ids, use_wts, residual=h, tokens=tokens)
+            got = G.to_f64(out) if tokens is None else G.to_f64(out)[tokens]
+            G.assert_close_block(got, ref, "stack layer %d M=%d" % (layer_idx, M))
+        del layer
+        h = out
+    assert moe.moe_read_device_status(ws) == 0
