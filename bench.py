@@ -210,7 +210,7 @@ def run_ours(args, world, rank, local):
     ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
     wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_block = 4
+    launches_per_block = 5
 
     def step(i):
         """One step: a single layer, or all L layers of the residual stack."""
@@ -303,8 +303,8 @@ def run_ours(args, world, rank, local):
         return
 
     # --- traced pass: per-kernel durations from events recorded around the kernels
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    dur = {"router": [], "align": [], "gateup": [], "down": []}
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    dur = {"router": [], "align": [], "gateup": [], "down": [], "combine": []}
 
     def traced_block(h, li, res, o):
         moe.moe_set_trace_events(evs)
@@ -313,11 +313,12 @@ def run_ours(args, world, rank, local):
                                  topk_weights=wts, workspace=ws, stream=stream)
         finally:
             moe.moe_set_trace_events(None)
-        evs[4].synchronize()
+        evs[5].synchronize()
         dur["router"].append(evs[0].elapsed_time(evs[1]))
         dur["align"].append(evs[1].elapsed_time(evs[2]))
         dur["gateup"].append(evs[2].elapsed_time(evs[3]))
         dur["down"].append(evs[3].elapsed_time(evs[4]))
+        dur["combine"].append(evs[4].elapsed_time(evs[5]))
 
     for i in range(args.steps):
         if stack:
@@ -339,7 +340,7 @@ def run_ours(args, world, rank, local):
         "traffic": traffic, "algorithmic_bytes_per_launch": int(gu_alg),
         "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
     }
-    dn_alg = u_mean * dn_b + M * wl.k * wl.I * 4
+    dn_alg = u_mean * dn_b + M * wl.k * (wl.I + wl.H) * 4
     result["down_kernel_gbs"] = round(dn_alg / (mean_ms["down"] * 1e-3) / 1e9, 1)
 
     # --- e2e: host h in, host out back, copies inside the timed region

@@ -126,9 +126,11 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
 
 /*
  * Workspace bytes that moe_expert_ffn / moe_decode_block need for (weights shape, M, k, b).
- * The workspace must be zero-filled before its first use; every call that completes
- * without a device wait timeout leaves its counters zero again, so it can be reused by
- * stream-ordered calls without clearing.  Returns 0 on unsupported arguments.
+ * The workspace holds the alignment (when the library computes it), the per-route
+ * intermediate p [M*k, I] fp32 and expert outputs y [M*k, H] fp32, and the device status
+ * word (its first 4 bytes), which must be zero before the first call (allocate it
+ * zero-filled).  Calls that share a workspace must be ordered on one stream.
+ * Returns 0 on unsupported arguments.
  */
 size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b);
 
@@ -140,7 +142,7 @@ size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b);
  *   Alignment: either all three of sorted_route_ids / expert_block_ids / num_padded as
  *   produced by moe_align_block_size for (topk_ids, E, b) -- every valid route exactly
  *   once -- or all three NULL, in which case the alignment is computed into the workspace.
- *   workspace: ws_bytes >= moe_workspace_bytes(w, M, k, b), zero-filled before first use.
+ *   workspace: ws_bytes >= moe_workspace_bytes(w, M, k, b).
  */
 int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
                    const int32_t *topk_ids, const float *topk_weights,
@@ -175,9 +177,9 @@ int moe_decode_block_host(const void *h_host, const void *residual_host, void *o
  * made from this host thread records the caller's CUDA events (cudaEvent_t passed as
  * void*) on its stream: events[0] before its first kernel, events[1] after the router,
  * events[2] after the alignment, events[3] after the gate/up kernel, events[4] after the
- * down kernel (stages a call does not run are not recorded; n must be 5).  An event
- * between two kernels removes the launch overlap the kernels otherwise get, so traced
- * calls run slightly slower.  Pass NULL (n = 0) to stop tracing.
+ * down kernel, events[5] after the combine kernel (stages a call does not run are not
+ * recorded; n must be 6).  An event between two kernels removes the launch overlap the
+ * kernels otherwise get, so traced calls run slightly slower.  Pass NULL (n = 0) to stop.
  */
 int moe_set_trace_events(void *const *events, int n);
 

@@ -25,8 +25,7 @@ constexpr int kAlignWarps = kAlignThreads / 32;
 __global__ void __launch_bounds__(kAlignThreads)
     align_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int b,
                  int32_t *__restrict__ sorted, int32_t *__restrict__ blocks,
-                 int32_t *__restrict__ npad, int64_t cap, int32_t *zero_a, int64_t n_zero_a,
-                 int32_t *zero_b, int64_t n_zero_b, int32_t *status) {
+                 int32_t *__restrict__ npad, int64_t cap, int32_t *status) {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *cnt = sm;                  // [E]
     int32_t *off = cnt + E;             // [E] padded row offsets
@@ -44,10 +43,6 @@ __global__ void __launch_bounds__(kAlignThreads)
 
     for (int i = tid; i < (3 + kAlignWarps) * E; i += kAlignThreads) sm[i] = 0;
     if (tid == 0) s_invalid = 0;
-    // Counters of the expert kernels that follow: cleared here so that a workspace left
-    // dirty by an aborted call is usable again.
-    for (int64_t i = tid; i < n_zero_a; i += kAlignThreads) zero_a[i] = 0;
-    for (int64_t i = tid; i < n_zero_b; i += kAlignThreads) zero_b[i] = 0;
     __syncthreads();
 
     // (1) counts
@@ -129,8 +124,7 @@ __global__ void __launch_bounds__(kAlignThreads)
 }
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, int32_t *sorted,
-                         int32_t *blocks, int32_t *npad, int64_t cap, int32_t *zero_a,
-                         int64_t n_zero_a, int32_t *zero_b, int64_t n_zero_b, int32_t *status,
+                         int32_t *blocks, int32_t *npad, int64_t cap, int32_t *status,
                          cudaStream_t stream) {
     const size_t smem = (size_t)(3 + kAlignWarps) * E * sizeof(int32_t);
     cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -139,7 +133,7 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, in
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kAlignThreads), smem, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, align_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
-                              cap, zero_a, n_zero_a, zero_b, n_zero_b, status);
+                              cap, status);
 }
 
 }  // namespace moe

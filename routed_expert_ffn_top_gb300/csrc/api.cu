@@ -42,11 +42,8 @@ WsLayout ws_layout(const Dims &d) {
     L.sorted = take((size_t)d.cap * 4);
     L.blocks = take((size_t)(d.cap / d.b) * 4);
     L.npad = take(16);
-    L.cnt_gu = take((size_t)d.max_sub * d.n_it * 4);
-    L.cnt_dn = take((size_t)d.M * d.n_ht * 4);
     L.p = take((size_t)d.R * d.I * 4);
-    L.part_gu = take((size_t)d.n_hg * d.R * d.I * 8);
-    L.part_dn = take((size_t)d.n_ig * d.R * d.H * 4);
+    L.y = take((size_t)d.R * d.H * 4);
     L.total = off;
     return L;
 }
@@ -113,7 +110,7 @@ static bool make_tmap_2d(CUtensorMap *tm, const void *base, CUtensorMapDataType 
     cuuint32_t estr[2] = {1, 1};
     return fn(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace moe
@@ -121,7 +118,8 @@ static bool make_tmap_2d(CUtensorMap *tm, const void *base, CUtensorMapDataType 
 using namespace moe;
 
 // ------------------------------------------------------------------------------ tracing
-static thread_local cudaEvent_t g_trace[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+constexpr int kTracePoints = 6;
+static thread_local cudaEvent_t g_trace[kTracePoints] = {};
 static thread_local bool g_tracing = false;
 
 static void trace(int i, cudaStream_t s) {
@@ -131,11 +129,11 @@ static void trace(int i, cudaStream_t s) {
 extern "C" int moe_set_trace_events(void *const *events, int n) {
     if (events == nullptr) {
         g_tracing = false;
-        for (int i = 0; i < 5; ++i) g_trace[i] = nullptr;
+        for (int i = 0; i < kTracePoints; ++i) g_trace[i] = nullptr;
         return MOE_OK;
     }
-    if (n != 5) return MOE_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+    if (n != kTracePoints) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < kTracePoints; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
     g_tracing = true;
     return MOE_OK;
 }
@@ -229,7 +227,7 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
         (expert_block_ids && !aligned(expert_block_ids, 4)) || !aligned(num_padded, 4))
         return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_align(topk_ids, M, k, E, b, sorted_route_ids, expert_block_ids,
-                                    num_padded, (int64_t)cap, nullptr, 0, nullptr, 0, nullptr,
+                                    num_padded, (int64_t)cap, nullptr,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -263,10 +261,7 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.residual = static_cast<const __nv_bfloat16 *>(residual);
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.p = reinterpret_cast<float *>(ws + L.p);
-    a.part_gu = reinterpret_cast<float2 *>(ws + L.part_gu);
-    a.part_dn = reinterpret_cast<float *>(ws + L.part_dn);
-    a.cnt_gu = reinterpret_cast<int32_t *>(ws + L.cnt_gu);
-    a.cnt_dn = reinterpret_cast<int32_t *>(ws + L.cnt_dn);
+    a.y = reinterpret_cast<float *>(ws + L.y);
     a.status = reinterpret_cast<int32_t *>(ws + L.status);
     a.M = d.M;
     a.k = d.k;
@@ -285,6 +280,9 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     err = launch_down(tm_down, a, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(4, stream);
+    err = launch_combine(a, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(5, stream);
     return MOE_OK;
 }
 
@@ -329,8 +327,6 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
         int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
         int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
         cudaError_t err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
-                                       reinterpret_cast<int32_t *>(ws + L.cnt_gu), d.max_sub * d.n_it,
-                                       reinterpret_cast<int32_t *>(ws + L.cnt_dn), (int64_t)M * d.n_ht,
                                        reinterpret_cast<int32_t *>(ws + L.status), s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(2, s);
@@ -369,8 +365,6 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
     int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
     int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
     err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
-                       reinterpret_cast<int32_t *>(ws + L.cnt_gu), d.max_sub * d.n_it,
-                       reinterpret_cast<int32_t *>(ws + L.cnt_dn), (int64_t)M * d.n_ht,
                        reinterpret_cast<int32_t *>(ws + L.status), s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(2, s);

@@ -36,11 +36,8 @@ struct WsLayout {
     size_t sorted;   // int32[cap]
     size_t blocks;   // int32[cap / b]
     size_t npad;     // int32[4]
-    size_t cnt_gu;   // int32[max_sub * n_it]
-    size_t cnt_dn;   // int32[M * n_ht]
-    size_t p;        // float[R * I]
-    size_t part_gu;  // float2[n_hg * R * I]
-    size_t part_dn;  // float[n_ig * R * H]
+    size_t p;        // float[R * I]   SiLU(g) * u per route
+    size_t y;        // float[R * H]   down-projection output per route
     size_t total;
 };
 
@@ -57,10 +54,7 @@ struct GemvArgs {
     const __nv_bfloat16 *residual;
     __nv_bfloat16 *out;
     float *p;
-    float2 *part_gu;
-    float *part_dn;
-    int32_t *cnt_gu;
-    int32_t *cnt_dn;
+    float *y;
     int32_t *status;
     int M, k, E, H, I, b, rsub;
     int n_it, n_hg, n_ht, n_ig;
@@ -74,13 +68,14 @@ cudaError_t launch_router(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b,
                          int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
-                         int32_t *zero_a, int64_t n_zero_a, int32_t *zero_b, int64_t n_zero_b,
                          int32_t *status, cudaStream_t stream);
 
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream);
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream);
+
+cudaError_t launch_combine(const GemvArgs &a, cudaStream_t stream);
 
 // Shared launch helper: programmatic dependent launch on, optional cluster dims.
 cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

@@ -168,4 +168,37 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t v) {
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
+// c + a * b with a, b taken from the selected 16-bit halves of two registers holding bf16
+// pairs, rounded once to fp32 (a bf16 x bf16 product is exact in fp32, so this is bitwise
+// the same as fmaf on the widened values).
+#define MOE_FMA_BF16_ASM(SA, SB)                                     \
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"                        \
+        "mov.b32 {a0, a1}, %1;\n\t"                                   \
+        "mov.b32 {b0, b1}, %2;\n\t"                                   \
+        "fma.rn.f32.bf16 %0, " SA ", " SB ", %3;\n\t}"                \
+        : "=f"(d)                                                        \
+        : "r"(a), "r"(b), "f"(c))
+template <int AHI, int BHI>
+__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, float c) {
+    float d;
+    if constexpr (AHI == 0 && BHI == 0) MOE_FMA_BF16_ASM("a0", "b0");
+    else if constexpr (AHI == 0 && BHI == 1) MOE_FMA_BF16_ASM("a0", "b1");
+    else if constexpr (AHI == 1 && BHI == 0) MOE_FMA_BF16_ASM("a1", "b0");
+    else MOE_FMA_BF16_ASM("a1", "b1");
+    return d;
+}
+#undef MOE_FMA_BF16_ASM
+
+// (c0, c1) += x * (w0, w1) as one packed fp32 FMA (each lane rounds like fmaf).
+__device__ __forceinline__ void ffma2(float &c0, float &c1, float x, float w0, float w1) {
+    asm("{\n\t.reg .b64 c, w, x;\n\t"
+        "mov.b64 c, {%0, %1};\n\t"
+        "mov.b64 w, {%3, %4};\n\t"
+        "mov.b64 x, {%2, %2};\n\t"
+        "fma.rn.f32x2 c, x, w, c;\n\t"
+        "mov.b64 {%0, %1}, c;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(x), "f"(w0), "f"(w1));
+}
+
 }  // namespace moe

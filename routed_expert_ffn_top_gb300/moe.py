@@ -305,7 +305,7 @@ def moe_read_device_status(workspace, stream=None) -> int:
 
 
 def moe_set_trace_events(events=None):
-    """Record the given five torch.cuda.Event objects around the block's kernels on every
+    """Record the given six torch.cuda.Event objects around the block's kernels on every
     later call from this thread (see include/moe.h); ``None`` stops tracing."""
     if events is None:
         _check(lib().moe_set_trace_events(None, 0), "moe_set_trace_events")
