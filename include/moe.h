@@ -173,6 +173,34 @@ int moe_decode_block_host(const void *h_host, const void *residual_host, void *o
                           size_t ws_bytes, void *stream);
 
 /*
+ * Allocation-free variant of moe_decode_block.  (The papers have no counterpart; this is a
+ * deployment convenience of this library.)
+ *
+ * For callers that cannot allocate device memory for a workspace -- a host program whose
+ * GPU memory belongs entirely to another allocator (an inference server's pool, a plugin
+ * host that only passes its input and output tensors), or a deployment that forbids
+ * allocation after start-up to hold a fixed memory budget.  The caller passes the same
+ * inputs and outputs as moe_decode_block, minus the workspace: the block's scratch
+ * (alignment rows, per-route p and y, status word) lives in one fixed device array inside
+ * the library, MOE_NOALLOC_SCRATCH_BYTES per GPU, held by every GPU that loads the library
+ * until the process exits.  It calls no cudaMalloc / cudaFree.
+ *   * Sizes whose workspace (moe_workspace_bytes) exceeds MOE_NOALLOC_SCRATCH_BYTES return
+ *     MOE_ERR_WORKSPACE before anything is launched (for H=2048, I=768, k=8, b=8 that is
+ *     M > 92 tokens).
+ *   * The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   * Every call on a device uses the same array: calls that overlap on the GPU (other
+ *     streams, or unordered host threads) race.  Order them on one stream.
+ *   * The array keeps the previous call's contents; each call clears the status word
+ *     itself.  Device status cannot be read back through this entry point.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int moe_decode_block_noalloc(const void *h, const void *w_router, const float *bias,
+                             const moe_expert_weights_t *w, int M, int k, int b,
+                             const void *residual, void *out, int32_t *topk_ids,
+                             float *topk_weights, void *stream);
+
+/*
  * Tracing.  When `events` is not NULL, each later moe_decode_block / moe_expert_ffn call
  * made from this host thread records the caller's CUDA events (cudaEvent_t passed as
  * void*) on its stream: events[0] before its first kernel, events[1] after the router,

@@ -36,7 +36,7 @@ MOE_W_VQ_GATEUP = 1
 EXPORTS = (
     "moe_status_string", "moe_route_topk", "moe_align_capacity", "moe_align_block_size",
     "moe_workspace_bytes", "moe_expert_ffn", "moe_decode_block", "moe_decode_block_host",
-    "moe_read_device_status", "moe_set_trace_events",
+    "moe_read_device_status", "moe_set_trace_events", "moe_decode_block_noalloc",
 )
 
 
@@ -95,9 +95,10 @@ def lib():
                                                 vp, vp, vp, sz, vp]
             L.moe_read_device_status.argtypes = [vp, vp, vp]
             L.moe_set_trace_events.argtypes = [vp, ci]
+            L.moe_decode_block_noalloc.argtypes = [vp, vp, vp, wp, ci, ci, ci, vp, vp, vp, vp, vp]
             for f in ("moe_route_topk", "moe_align_block_size", "moe_expert_ffn",
                       "moe_decode_block", "moe_decode_block_host", "moe_read_device_status",
-                      "moe_set_trace_events"):
+                      "moe_set_trace_events", "moe_decode_block_noalloc"):
                 getattr(L, f).restype = ci
             _lib = L
     return _lib
@@ -276,6 +277,37 @@ def moe_decode_block(h, layer, k, b, residual=None, out=None, topk_ids=None, top
                                   _ptr(residual), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
                                   _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_decode_block")
+    return out, topk_ids, topk_weights
+
+
+def moe_decode_block_noalloc(h, layer, k, b, residual=None, out=None, topk_ids=None,
+                             topk_weights=None, stream=None):
+    """moe_decode_block without a workspace: for callers that cannot allocate device memory,
+    the library runs the block on its own fixed scratch array (see include/moe.h).  Outputs
+    the caller does not pass are allocated here by torch, as for the other wrappers."""
+    dev = h.device
+    _need(h, torch.bfloat16, "h", dev)
+    M = h.shape[0]
+    w = expert_weights(layer)
+    w_router = _need(layer["w_router"], torch.bfloat16, "w_router", dev)
+    bias = layer.get("bias")
+    if bias is not None:
+        _need(bias, torch.float32, "bias", dev)
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual", dev)
+    if out is None:
+        out = torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((M, k), dtype=torch.float32, device=dev)
+    _need(out, torch.bfloat16, "out", dev)
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    _need(topk_weights, torch.float32, "topk_weights", dev)
+    _check(lib().moe_decode_block_noalloc(_ptr(h), _ptr(w_router), _ptr(bias), ctypes.byref(w),
+                                          M, k, b, _ptr(residual), _ptr(out), _ptr(topk_ids),
+                                          _ptr(topk_weights), _stream(stream)),
+           "moe_decode_block_noalloc")
     return out, topk_ids, topk_weights
 
 
