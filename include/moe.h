@@ -36,9 +36,9 @@
  *     block position or atomic arrival order), so results are bitwise reproducible run
  *     to run, and a route's output bits do not depend on which aligned block it lands in.
  *
- * Supported shapes: 1 <= k <= min(E, 32); 8 <= E <= 512, E % 8 == 0; H % 128 == 0 and
- * 128 <= H <= 8192; I % 128 == 0 and 128 <= I <= 8192; (H/8) * E * 2 <= 131072 bytes
- * (router slice); b >= 1 and (b <= 8 or b % 8 == 0); 0 <= M; M * k < 2^24.
+ * Supported shapes: 1 <= k <= min(E, 32); 8 <= E <= 512, E % 8 == 0; H and I multiples of
+ * 256 up to 8192 (moe_route_topk alone: H a multiple of 128); (H/8) * E * 2 <= 131072
+ * bytes (router slice); b >= 1 and (b <= 8 or b % 8 == 0); 0 <= M; M * k < 2^24.
  * VQ: d == 4, K == 256.
  */
 #ifndef MOE_GB300_H

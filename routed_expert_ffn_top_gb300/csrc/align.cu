@@ -13,7 +13,9 @@
 // a warp, __match_any_sync groups lanes with the same expert and a popcount of the lower
 // lanes gives each route its rank, warps of the chunk are ranked through a per-warp count
 // table, and a per-expert running total carries ranks across chunks.  Every rank, hence
-// every output position, is a pure function of the input ids.
+// every output position, is a pure function of the input ids.  (5) Optionally, a table of
+// the aligned rows in groups of rsub (expert, routes, tokens) that the expert kernels read
+// one record per tile.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -25,7 +27,8 @@ constexpr int kAlignWarps = kAlignThreads / 32;
 __global__ void __launch_bounds__(kAlignThreads)
     align_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int b,
                  int32_t *__restrict__ sorted, int32_t *__restrict__ blocks,
-                 int32_t *__restrict__ npad, int64_t cap, int32_t *status) {
+                 int32_t *__restrict__ npad, int64_t cap, SubBlock *sbt, int rsub,
+                 int32_t *status) {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *cnt = sm;                  // [E]
     int32_t *off = cnt + E;             // [E] padded row offsets
@@ -121,11 +124,34 @@ __global__ void __launch_bounds__(kAlignThreads)
         npad[0] = total;
         if (status && s_invalid) atomicOr(status, MOE_DEV_INVALID_EXPERT);
     }
+    // (5) the sub-block table the expert kernels stream from
+    if (sbt) {
+        __syncthreads();
+        for (int64_t sb = tid; sb < total / rsub; sb += kAlignThreads)
+            build_subblock(sorted, blocks, ids, sb, rsub, b, E, R, k, false, nullptr, sbt + sb);
+    }
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+    plan_kernel(const int32_t *__restrict__ ids, const int32_t *__restrict__ sorted,
+                const int32_t *__restrict__ blocks, const int32_t *__restrict__ npad, int M,
+                int k, int E, int b, int rsub, int64_t max_sub, SubBlock *sbt, int32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t R = (int64_t)M * k;
+    int64_t nsub = npad[0] / rsub;
+    if (nsub > max_sub) {  // a num_padded larger than the capacity: use what fits
+        nsub = max_sub;
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, MOE_DEV_BAD_ALIGNMENT);
+    }
+    for (int64_t sb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; sb < nsub;
+         sb += (int64_t)gridDim.x * blockDim.x)
+        build_subblock(sorted, blocks, ids, sb, rsub, b, E, R, k, true, status, sbt + sb);
 }
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, int32_t *sorted,
-                         int32_t *blocks, int32_t *npad, int64_t cap, int32_t *status,
-                         cudaStream_t stream) {
+                         int32_t *blocks, int32_t *npad, int64_t cap, SubBlock *sbt, int rsub,
+                         int32_t *status, cudaStream_t stream) {
     const size_t smem = (size_t)(3 + kAlignWarps) * E * sizeof(int32_t);
     cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
@@ -133,7 +159,18 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, in
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kAlignThreads), smem, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, align_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
-                              cap, status);
+                              cap, sbt, rsub, status);
+}
+
+cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const int32_t *blocks,
+                        const int32_t *npad, int M, int k, int E, int b, int rsub,
+                        int64_t max_sub, SubBlock *sbt, int32_t *status, cudaStream_t stream) {
+    cudaLaunchAttribute attrs[2];
+    const int64_t blocks_needed = (max_sub + kAlignThreads - 1) / kAlignThreads;
+    const int grid = (int)(blocks_needed < 1 ? 1 : (blocks_needed > 1024 ? 1024 : blocks_needed));
+    cudaLaunchConfig_t cfg = launch_config(dim3(grid), dim3(kAlignThreads), 0, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, plan_kernel, topk_ids, sorted, blocks, npad, M, k, E, b, rsub,
+                              max_sub, sbt, status);
 }
 
 }  // namespace moe

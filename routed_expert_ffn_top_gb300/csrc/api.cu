@@ -24,9 +24,9 @@ Dims make_dims(int M, int k, int E, int H, int I, int b) {
     d.cap = d.R + (int64_t)(d.R < E ? d.R : E) * (b - 1);
     d.max_sub = d.cap / d.rsub;
     d.n_it = I / kTI;
-    d.n_hg = H / kHG;
+    d.n_hb = H / kBoxRows;
     d.n_ht = H / kTN;
-    d.n_ig = I / kIG;
+    d.n_ib = I / kBoxRows;
     return d;
 }
 
@@ -42,6 +42,7 @@ WsLayout ws_layout(const Dims &d) {
     L.sorted = take((size_t)d.cap * 4);
     L.blocks = take((size_t)(d.cap / d.b) * 4);
     L.npad = take(16);
+    L.sbt = take((size_t)d.max_sub * sizeof(SubBlock));
     L.p = take((size_t)d.R * d.I * 4);
     L.y = take((size_t)d.R * d.H * 4);
     L.total = off;
@@ -161,8 +162,8 @@ static int check_block(int b) {
 static int check_weights(const moe_expert_weights_t *w) {
     if (!w) return MOE_ERR_INVALID_ARG;
     if (w->H <= 0 || w->I <= 0 || w->E <= 0) return MOE_ERR_INVALID_ARG;
-    if (w->I % 128 != 0 || w->I < 128 || w->I > 8192) return MOE_ERR_UNSUPPORTED;
-    if (w->H % 128 != 0 || w->H < 128 || w->H > 8192) return MOE_ERR_UNSUPPORTED;
+    if (w->I % kBoxRows != 0 || w->I > 8192) return MOE_ERR_UNSUPPORTED;
+    if (w->H % kBoxRows != 0 || w->H > 8192) return MOE_ERR_UNSUPPORTED;
     if (w->E < 8 || w->E > 512 || w->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (!w->w_down || !aligned(w->w_down, 16)) return MOE_ERR_INVALID_ARG;
     if (w->kind == MOE_W_DENSE_BF16) {
@@ -227,7 +228,7 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
         (expert_block_ids && !aligned(expert_block_ids, 4)) || !aligned(num_padded, 4))
         return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_align(topk_ids, M, k, E, b, sorted_route_ids, expert_block_ids,
-                                    num_padded, (int64_t)cap, nullptr,
+                                    num_padded, (int64_t)cap, nullptr, 0, nullptr,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -240,23 +241,22 @@ extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int 
 
 // Runs gate/up and down for aligned routes (alignment pointers already resolved).
 static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims &d,
-                       const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
-                       const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
-                       unsigned char *ws, const WsLayout &L, cudaStream_t stream) {
+                       const int32_t *topk_ids, const float *topk_weights, const int32_t *npad,
+                       const void *residual, void *out, unsigned char *ws, const WsLayout &L,
+                       cudaStream_t stream) {
     CUtensorMap tm_gate, tm_up, tm_down;
     if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, kTI, kHG) ||
+                      (uint64_t)d.E * d.H, kTI, kBoxRows) ||
         !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, kTI, kHG) ||
+                      (uint64_t)d.E * d.H, kTI, kBoxRows) ||
         !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
-                      (uint64_t)d.E * d.I, kTN, kIG))
+                      (uint64_t)d.E * d.I, kTN, kBoxRows))
         return MOE_ERR_CUDA;
     GemvArgs a;
     a.h = static_cast<const __nv_bfloat16 *>(h);
     a.topk_ids = topk_ids;
     a.topk_wts = topk_weights;
-    a.sorted = sorted;
-    a.blocks = blocks;
+    a.sbt = reinterpret_cast<const SubBlock *>(ws + L.sbt);
     a.npad = npad;
     a.residual = static_cast<const __nv_bfloat16 *>(residual);
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -271,9 +271,10 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.b = d.b;
     a.rsub = d.rsub;
     a.n_it = d.n_it;
-    a.n_hg = d.n_hg;
+    a.n_hb = d.n_hb;
     a.n_ht = d.n_ht;
-    a.n_ig = d.n_ig;
+    a.n_ib = d.n_ib;
+    a.max_sub = d.max_sub;
     cudaError_t err = launch_gateup_dense(tm_gate, tm_up, a, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
@@ -320,23 +321,26 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int32_t *sorted = sorted_route_ids, *blocks = expert_block_ids, *npad = num_padded;
     trace(0, s);
+    const int32_t *npad = num_padded;
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    SubBlock *sbt = reinterpret_cast<SubBlock *>(ws + L.sbt);
+    cudaError_t err;
     if (given == 0) {
-        int32_t *ws_sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
-        int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
         int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
-        cudaError_t err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
-                                       reinterpret_cast<int32_t *>(ws + L.status), s);
-        if (err != cudaSuccess) return MOE_ERR_CUDA;
-        trace(2, s);
-        sorted = ws_sorted;
-        blocks = ws_blocks;
+        err = launch_align(topk_ids, M, k, w->E, b, reinterpret_cast<int32_t *>(ws + L.sorted),
+                           reinterpret_cast<int32_t *>(ws + L.blocks), ws_npad, d.cap, sbt, d.rsub,
+                           status, s);
         npad = ws_npad;
-    } else if (!aligned(sorted, 4) || !aligned(blocks, 4) || !aligned(npad, 4)) {
-        return MOE_ERR_INVALID_ARG;
+    } else {
+        if (!aligned(sorted_route_ids, 4) || !aligned(expert_block_ids, 4) || !aligned(num_padded, 4))
+            return MOE_ERR_INVALID_ARG;
+        err = launch_plan(topk_ids, sorted_route_ids, expert_block_ids, num_padded, M, k, w->E, b,
+                          d.rsub, d.max_sub, sbt, status, s);
     }
-    return run_experts(h, w, d, topk_ids, topk_weights, sorted, blocks, npad, residual, out, ws, L, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(2, s);
+    return run_experts(h, w, d, topk_ids, topk_weights, npad, residual, out, ws, L, s);
 }
 
 extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,
@@ -365,11 +369,11 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
     int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
     int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
     err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                       reinterpret_cast<SubBlock *>(ws + L.sbt), d.rsub,
                        reinterpret_cast<int32_t *>(ws + L.status), s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(2, s);
-    return run_experts(h, w, d, topk_ids, topk_weights, ws_sorted, ws_blocks, ws_npad, residual,
-                       out, ws, L, s);
+    return run_experts(h, w, d, topk_ids, topk_weights, ws_npad, residual, out, ws, L, s);
 }
 
 extern "C" int moe_decode_block_host(const void *h_host, const void *residual_host,

@@ -8,65 +8,62 @@
 // and, channel by channel, "Channel Selection for Mixture-of-Experts Decoding Needs No
 // Calibration Data" (Background: channel j owns row j of gate/up and column j of down).
 //
-// At decode batch sizes every weight byte serves only a handful of tokens, so the kernels
-// are HBM streams.  The work is cut into tiles over the aligned rows:
+// At decode batch sizes every weight byte serves only a handful of tokens, so both expert
+// kernels are HBM streams, and what bounds them is how many bytes each SM keeps in flight.
+// An SM's tensor-memory-access unit works on only a few copies at a time, so every weight
+// copy here is one large box (256 rows x 64 columns of bf16 = 32 KB), and the small
+// activation slices travel separately through 16-byte cp.async copies.
+//
+// Work is cut into tiles over the aligned rows:
 //   * a sub-block is `rsub` consecutive aligned rows: at most 8 routes of ONE expert (the
-//     alignment pads every expert to a multiple of b and rsub divides b);
+//     alignment pads every expert to a multiple of b and rsub divides b); its record
+//     (expert, routes, tokens) comes from the sub-block table the alignment step wrote;
 //   * gate/up tile = (sub-block, 64-column I tile): all H rows of W_gate[e] and W_up[e] in
-//     that column range, streamed as H/128 boxes of 128x64 bf16 per projection;
-//   * down tile = (sub-block, 64-column H tile): all I rows of W_down[e] in that range, as
-//     I/128 boxes of 128x64 bf16.
-// Persistent CTAs (one per SM) own contiguous ranges of whole tiles.  Warp 0 is the
-// producer: one thread issues TMA tensor loads of the boxes, plus bulk copies of the
-// sub-block's activation slices, into a ring of shared-memory stages guarded by full/empty
-// mbarriers.  Warps 1..8 consume: warp w owns rows [16w, 16w+16) of every box, lane l the
-// 8 rows [16w + 8(l/16), +8) and the 4 columns [4(l%16), +4), and keeps fp32 accumulators
-// for up to 8 tokens in registers across all boxes of the tile (gate/up multiplies the
-// bf16 h and weight values directly into fp32; down uses packed fp32 FMAs on fp32 p).  Only at the end of a tile do the 8 warps combine their partial
-// sums (shared memory, fixed warp order), and the epilogue writes p (gate/up) or y (down).
-// A third small kernel forms out = residual + sum_j a_j y_j in slot order j = 0..k-1.
+//     that column range, as H/256 boxes of each projection, alternating gate and up;
+//   * down tile = (sub-block, 64-column H tile): all I rows of W_down[e], I/256 boxes.
+// Persistent CTAs (one per SM) own tiles c, c + G, c + 2G ... (G = grid size); tiles are
+// numbered column tile fastest, so neighbouring SMs stream neighbouring column ranges of
+// the same rows.  Warp 0 (one thread) issues the TMA box copies into a ring of stages;
+// warp 1 copies each stage's activation slices (h rows for gate/up, p rows for down) with
+// cp.async and hangs them on the same full barrier; warps 2..9 consume.  Consumer warp w
+// owns rows [32w, 32w+32) of every box; lane l the 16 rows [32w + 16(l/16), +16) and the 4
+// columns [4(l%16), +4); fp32 accumulators for up to 8 tokens live in registers across all
+// boxes of the tile (gate/up multiplies bf16 h and weights straight into fp32; down uses
+// packed fp32 FMAs on fp32 p).  At the end of a tile the two lane halves and then the 8
+// warps are summed, and the epilogue writes p (gate/up) or y (down).  A third small kernel
+// forms out = residual + sum_j a_j y_j in slot order j = 0..k-1.
 //
 // Reduction order, fixed by tile indices only (never by grid size, CTA, block position,
 // batch size or arrival order): per thread, boxes ascending and rows ascending inside its
-// 8-row slice; then the two lane halves; then warps 0..7; then, for the combine, slots
-// 0..k-1.  So the results are
-// bitwise reproducible, a route's bits do not depend on the block it sits in or on the
-// other routes of its block, and a token's output does not depend on M.
+// 16-row slice; then the two lane halves; then warps 0..7; then, for the combine, slots
+// 0..k-1.  So the results are bitwise reproducible, a route's bits do not depend on the
+// block it sits in or on the other routes of its block, and a token's output does not
+// depend on M.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
-constexpr int kStagesGU = 5;
-constexpr int kStagesDN = 8;
+constexpr int kStages = 5;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kRowsPerWarp = 16;  // of every 128-row box
-static_assert(kHG == kConsumerWarps * kRowsPerWarp && kIG == kConsumerWarps * kRowsPerWarp, "rows");
+constexpr int kRowsPerWarp = kBoxRows / kConsumerWarps;  // 32
+constexpr int kRowsPerThread = kRowsPerWarp / 2;         // 16
+constexpr int kFirstConsumerWarp = 2;
 
-constexpr int kBoxBytesGU = kHG * kTI * 2;                      // 16 KB per projection
-constexpr int kStageBytesGU = 2 * kBoxBytesGU + kNT * kHG * 2;  // + h slices (bf16)
-constexpr int kBoxBytesDN = kIG * kTN * 2;                      // 16 KB
-constexpr int kStageBytesDN = kBoxBytesDN + kNT * kIG * 4;      // + p slices (fp32)
+constexpr int kBoxBytes = kBoxRows * kTI * 2;                 // 32 KB (also kTN == kTI)
+constexpr int kStageBytesGU = kBoxBytes + kNT * kBoxRows * 2;  // + h slices (bf16)
+constexpr int kStageBytesDN = kBoxBytes + kNT * kBoxRows * 4;  // + p slices (fp32)
 constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 2 * 4;
 constexpr int kRedBytesDN = kConsumerWarps * kNT * kTN * 4;
+static_assert(kTI == kTN, "one box shape for both kernels");
 static_assert(kStageBytesGU % 1024 == 0 && kStageBytesDN % 1024 == 0, "stage alignment");
 
-struct StageMeta {
-    int ntok;
-    int e;
-    int routes[kNT];
-};
-
 struct Ctl {
-    uint64_t full[8];
-    uint64_t empty[8];
-    StageMeta meta[8];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    SubBlock meta[kStages];  // the sub-block record of the tile each stage belongs to
     volatile int abort;
 };
-
-// CTA c owns tiles c, c + G, c + 2G, ... (G = grid size).  Tiles are numbered column
-// tile fastest, so at any moment neighbouring CTAs stream neighbouring column ranges of the
-// same weight rows, and the DRAM pages those rows live in are read while open.
 
 // Bounded wait that also gives up as soon as another thread of the CTA has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ctl &ctl) {
@@ -82,73 +79,62 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ct
     }
 }
 
-// Routes of sub-block sb: the valid entries among its rsub aligned rows whose top-k id is
-// the block's expert.  Anything else is padding (a mismatch is flagged as a bad alignment).
-__device__ void decode_subblock(const GemvArgs &a, int64_t sb, StageMeta &s) {
-    const int64_t row0 = sb * a.rsub;
-    const int e = a.blocks[row0 / a.b];
-    const int64_t R = (int64_t)a.M * a.k;
-    s.e = e;
-    int n = 0;
-    if (e >= 0 && e < a.E) {
-        for (int q = 0; q < a.rsub; ++q) {
-            const int r = a.sorted[row0 + q];
-            if (r < 0 || r >= R) continue;
-            if (a.topk_ids[r] != e) {
-                atomicOr(a.status, MOE_DEV_BAD_ALIGNMENT);
-                continue;
-            }
-            s.routes[n++] = r;
-        }
+__device__ __forceinline__ void advance(int &stage, uint32_t &phase) {
+    if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
     }
-    s.ntok = n;
 }
 
-// Producer (one thread).  A tile with no route is announced by a single stage with
-// ntok == 0 and no copies; otherwise `boxes` stages, one per box of the tile.
-struct NoFlush {
-    __device__ void operator()() const {}
-};
+__device__ __forceinline__ void load_record(const SubBlock *src, uint4 (&dst)[5]) {
+    const uint4 *s = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) dst[i] = s[i];
+}
 
-// `flush` runs before the producer could block on a stage it issued itself (once every
-// stage of the ring has been issued) and after the last stage: the down kernel uses it to
-// copy the activations it held back until its dependency wait.
-template <int kStages, typename IssueFn, typename FlushFn = NoFlush>
-__device__ void producer_loop(const GemvArgs &a, Ctl &ctl, int64_t T, int tiles_per_sub,
-                              int boxes, IssueFn issue, FlushFn flush = NoFlush()) {
+__device__ __forceinline__ void init_ring(Ctl &ctl) {
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(&ctl.full[s], 2);  // the box producer and the activation loader
+        mbar_init(&ctl.empty[s], kConsumerWarps);
+    }
+    ctl.abort = 0;
+    fence_mbar_init();
+}
+
+// Box producer (one thread).  A tile with no route is announced by a single stage that
+// carries no copies; otherwise `stages_per_tile` stages.  `issue(stage, tile, j, e)` issues
+// the TMA copy of stage j of the tile and arms the stage's full barrier.
+template <typename IssueFn>
+__device__ void box_producer(const GemvArgs &a, Ctl &ctl, int64_t T, int tiles_per_sub,
+                             int stages_per_tile, IssueFn issue) {
     int stage = 0;
     uint32_t phase = 0;
-    int64_t cur_sb = -1;
-    StageMeta cur;
-    cur.ntok = 0;
-    cur.e = -1;
     uint32_t issued = 0, parity_bits = 0;
-    int64_t n_issued = 0;
-    for (int64_t t = blockIdx.x; t < T && !ctl.abort; t += gridDim.x) {
-        const int64_t sb = t / tiles_per_sub;
-        if (sb != cur_sb) {
-            decode_subblock(a, sb, cur);
-            cur_sb = sb;
-        }
-        const int nst = cur.ntok > 0 ? boxes : 1;
-        for (int bx = 0; bx < nst; ++bx) {
-            if (n_issued == kStages) flush();
+    // The record of the next tile is loaded while the current tile streams.
+    uint4 cur[5], nxt[5];
+    const int64_t G = gridDim.x;
+    if ((int64_t)blockIdx.x < T) load_record(a.sbt + blockIdx.x / tiles_per_sub, nxt);
+    for (int64_t t = blockIdx.x; t < T && !ctl.abort; t += G) {
+#pragma unroll
+        for (int i = 0; i < 5; ++i) cur[i] = nxt[i];
+        if (t + G < T) load_record(a.sbt + (t + G) / tiles_per_sub, nxt);
+        const int e = (int)cur[0].x;
+        const int ntok = (int)cur[0].y;
+        const int nst = ntok > 0 ? stages_per_tile : 1;
+        for (int j = 0; j < nst; ++j) {
             if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) break;
-            ++n_issued;
-            ctl.meta[stage] = cur;
-            if (cur.ntok > 0)
-                issue(stage, t, bx, cur);
+            uint4 *m = reinterpret_cast<uint4 *>(&ctl.meta[stage]);
+#pragma unroll
+            for (int i = 0; i < 5; ++i) m[i] = cur[i];
+            if (ntok > 0)
+                issue(stage, t, j, e);
             else
                 mbar_arrive(&ctl.full[stage]);
             issued |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
+            advance(stage, phase);
         }
     }
-    flush();
     // Never leave the CTA while copies may still be landing in its shared memory.
     for (int s = 0; s < kStages; ++s)
         if ((issued >> s) & 1u)
@@ -156,11 +142,280 @@ __device__ void producer_loop(const GemvArgs &a, Ctl &ctl, int64_t T, int tiles_
     if (ctl.abort) atomicOr(a.status, MOE_DEV_WAIT_TIMEOUT);
 }
 
-template <int kStages>
-__device__ __forceinline__ void advance(int &stage, uint32_t &phase) {
-    if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+// Activation loader (one warp).  For every stage the box producer fills, lane l copies
+// `chunks` 16-byte pieces per route: src(route, token, tile, j, piece) -> the stage's slice
+// area.  Its arrival on the stage's full barrier completes only when its copies have landed.
+template <typename SrcFn>
+__device__ void slice_loader(const GemvArgs &a, Ctl &ctl, unsigned char *stages, int stage_bytes,
+                             int slice_bytes, int chunks, int64_t T, int tiles_per_sub,
+                             int stages_per_tile, SrcFn src) {
+    const int lane = threadIdx.x & 31;
+    int stage = 0;
+    uint32_t phase = 0;
+    const int64_t G = gridDim.x;
+    for (int64_t t = blockIdx.x; t < T && !ctl.abort; t += G) {
+        const SubBlock *rec = a.sbt + t / tiles_per_sub;
+        const int ntok = rec->ntok;
+        // lane q (< 8) holds route q and its token
+        const int my_route = rec->routes[lane & (kNT - 1)];
+        const int my_token = rec->tokens[lane & (kNT - 1)];
+        const int nst = ntok > 0 ? stages_per_tile : 1;
+        for (int j = 0; j < nst; ++j) {
+            if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) return;
+            if (ntok > 0) {
+                unsigned char *dst = stages + stage * stage_bytes + kBoxBytes;
+                for (int q = 0; q < ntok; ++q) {
+                    const int route = __shfl_sync(0xffffffffu, my_route, q);
+                    const int token = __shfl_sync(0xffffffffu, my_token, q);
+                    for (int c = 0; c < chunks; ++c)
+                        cp_async_16(dst + q * slice_bytes + (lane * chunks + c) * 16,
+                                    src(route, token, t, j, lane * chunks + c));
+                }
+                cp_async_mbar_arrive(&ctl.full[stage]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.full[stage]);
+            advance(stage, phase);
+        }
+    }
+}
+
+// Per-thread position inside the consumer warps.
+struct Lane {
+    int ctid;   // 0..255
+    int cw;     // consumer warp 0..7
+    int lane;
+    int half;   // which 16 rows of the warp's 32
+    int c4;     // first of the 4 columns
+    int rbase;  // first of the 16 rows
+};
+
+// acc[q][c] += sum over this thread's 16 rows of x_q[row] * W[row][c4 + c] for NT tokens
+// (bf16 x bf16 -> fp32, rows ascending).  `st` is the stage: the box, then the h slices.
+template <int NT>
+__device__ __forceinline__ void accumulate_bf16_box(const unsigned char *st, const Lane &ln,
+                                                    float (&acc)[NT][4]) {
+    const unsigned char *xs = st + kBoxBytes + ln.rbase * 2;
+#pragma unroll
+    for (int r8 = 0; r8 < kRowsPerThread; r8 += 8) {
+        uint2 w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = *reinterpret_cast<const uint2 *>(st + (ln.rbase + r8 + i) * (kTI * 2) + ln.c4 * 2);
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xs + q * kBoxRows * 2 + r8 * 2);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t x2 = xw[i >> 1];
+                if (i & 1) {
+                    acc[q][0] = fma_bf16<1, 0>(x2, w[i].x, acc[q][0]);
+                    acc[q][1] = fma_bf16<1, 1>(x2, w[i].x, acc[q][1]);
+                    acc[q][2] = fma_bf16<1, 0>(x2, w[i].y, acc[q][2]);
+                    acc[q][3] = fma_bf16<1, 1>(x2, w[i].y, acc[q][3]);
+                } else {
+                    acc[q][0] = fma_bf16<0, 0>(x2, w[i].x, acc[q][0]);
+                    acc[q][1] = fma_bf16<0, 1>(x2, w[i].x, acc[q][1]);
+                    acc[q][2] = fma_bf16<0, 0>(x2, w[i].y, acc[q][2]);
+                    acc[q][3] = fma_bf16<0, 1>(x2, w[i].y, acc[q][3]);
+                }
+            }
+        }
+    }
+}
+
+// acc[q][c] += sum over this thread's 16 rows of p_q[row] * W[row][c4 + c] for NT routes
+// (fp32 p, bf16 weights, packed fp32 FMAs, rows ascending).
+template <int NT>
+__device__ __forceinline__ void accumulate_f32_box(const unsigned char *st, const Lane &ln,
+                                                   float (&acc)[NT][4]) {
+    const float *xs = reinterpret_cast<const float *>(st + kBoxBytes) + ln.rbase;
+#pragma unroll
+    for (int r8 = 0; r8 < kRowsPerThread; r8 += 8) {
+        float w[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint2 w2 = *reinterpret_cast<const uint2 *>(st + (ln.rbase + r8 + i) * (kTN * 2) + ln.c4 * 2);
+            w[i][0] = bf16_lo(w2.x);
+            w[i][1] = bf16_hi(w2.x);
+            w[i][2] = bf16_lo(w2.y);
+            w[i][3] = bf16_hi(w2.y);
+        }
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const float4 p0 = *reinterpret_cast<const float4 *>(xs + q * kBoxRows + r8);
+            const float4 p1 = *reinterpret_cast<const float4 *>(xs + q * kBoxRows + r8 + 4);
+            const float x[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ffma2(acc[q][0], acc[q][1], x[i], w[i][0], w[i][1]);
+                ffma2(acc[q][2], acc[q][3], x[i], w[i][2], w[i][3]);
+            }
+        }
+    }
+}
+
+// Releases the stage to the box producer and the loader once this warp is done with it.
+__device__ __forceinline__ void release_stage(Ctl &ctl, const Lane &ln, int &stage, uint32_t &phase) {
+    __syncwarp();
+    if (ln.lane == 0) mbar_arrive(&ctl.empty[stage]);
+    advance(stage, phase);
+}
+
+// One gate/up tile with NT routes; its first stage has already been waited for.  Returns
+// false when the CTA must stop (a bounded wait gave up somewhere in the CTA).
+template <int NT>
+__device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
+                            const Lane &ln, int it, int r0, int r1, int &stage, uint32_t &phase) {
+    float ag[NT][4], au[NT][4];
+#pragma unroll
+    for (int q = 0; q < NT; ++q)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ag[q][c] = au[q][c] = 0.0f;
+    bool failed = false;
+    // stages of a tile: gate box, up box for rows [0, 256), then for [256, 512), ...
+    for (int j = 0; j < 2 * a.n_hb; ++j) {
+        if (j > 0 && !wait_or_abort(&ctl.full[stage], phase, ctl)) {
+            failed = true;
+            break;
+        }
+        const unsigned char *st = stages + stage * kStageBytesGU;
+        if (j & 1)
+            accumulate_bf16_box<NT>(st, ln, au);
+        else
+            accumulate_bf16_box<NT>(st, ln, ag);
+        release_stage(ctl, ln, stage, phase);
+    }
+    if (named_bar_or(1, kConsumerThreads, failed)) return false;
+    // the two lane halves (rows), then the warps; the same bits on both lanes
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        float g4[4], u4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            g4[c] = ag[q][c] + __shfl_xor_sync(0xffffffffu, ag[q][c], 16);
+            u4[c] = au[q][c] + __shfl_xor_sync(0xffffffffu, au[q][c], 16);
+        }
+        if (ln.half == 0) {
+            float *dst = &red[((ln.cw * kNT + q) * kTI + ln.c4) * 2];
+            *reinterpret_cast<float4 *>(dst) = make_float4(g4[0], u4[0], g4[1], u4[1]);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(g4[2], u4[2], g4[3], u4[3]);
+        }
+    }
+    named_bar_sync(1, kConsumerThreads);
+    const int col0 = it * kTI;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int idx = ln.ctid + pass * kConsumerThreads;
+        const int q = idx / kTI, c = idx % kTI;
+        if (q < NT) {
+            float2 sum = *reinterpret_cast<const float2 *>(&red[(q * kTI + c) * 2]);
+#pragma unroll
+            for (int w = 1; w < kConsumerWarps; ++w) {
+                const float2 v = *reinterpret_cast<const float2 *>(&red[((w * kNT + q) * kTI + c) * 2]);
+                sum.x += v.x;
+                sum.y += v.y;
+            }
+            a.p[(int64_t)(pass ? r1 : r0) * a.I + col0 + c] = silu_f32(sum.x) * sum.y;
+        }
+    }
+    named_bar_sync(1, kConsumerThreads);
+    return true;
+}
+
+// One down tile with NT routes (first stage already waited for); see gateup_tile.
+template <int NT>
+__device__ bool down_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
+                          const Lane &ln, int ht, int r0, int r1, int &stage, uint32_t &phase) {
+    float acc[NT][4];
+#pragma unroll
+    for (int q = 0; q < NT; ++q)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[q][c] = 0.0f;
+    bool failed = false;
+    for (int j = 0; j < a.n_ib; ++j) {
+        if (j > 0 && !wait_or_abort(&ctl.full[stage], phase, ctl)) {
+            failed = true;
+            break;
+        }
+        accumulate_f32_box<NT>(stages + stage * kStageBytesDN, ln, acc);
+        release_stage(ctl, ln, stage, phase);
+    }
+    if (named_bar_or(1, kConsumerThreads, failed)) return false;
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        float v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = acc[q][c] + __shfl_xor_sync(0xffffffffu, acc[q][c], 16);
+        if (ln.half == 0)
+            *reinterpret_cast<float4 *>(&red[(ln.cw * kNT + q) * kTN + ln.c4]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    named_bar_sync(1, kConsumerThreads);
+    const int col0 = ht * kTN;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int idx = ln.ctid + pass * kConsumerThreads;
+        const int q = idx / kTN, c = idx % kTN;
+        if (q < NT) {
+            float sum = red[q * kTN + c];
+#pragma unroll
+            for (int w = 1; w < kConsumerWarps; ++w) sum += red[(w * kNT + q) * kTN + c];
+            a.y[(int64_t)(pass ? r1 : r0) * a.H + col0 + c] = sum;
+        }
+    }
+    named_bar_sync(1, kConsumerThreads);
+    return true;
+}
+
+// Consumer loop shared by both kernels: waits for a tile's first stage, reads how many routes
+// it has, and runs the tile body specialised for that count.
+template <bool kGateUp>
+__device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
+                              int64_t T, int tiles_per_sub) {
+    const int warp = threadIdx.x >> 5;
+    Lane ln;
+    ln.ctid = threadIdx.x - 32 * kFirstConsumerWarp;
+    ln.cw = warp - kFirstConsumerWarp;
+    ln.lane = threadIdx.x & 31;
+    ln.half = ln.lane >> 4;
+    ln.c4 = (ln.lane & 15) * 4;
+    ln.rbase = ln.cw * kRowsPerWarp + ln.half * kRowsPerThread;
+    const int cols = kGateUp ? kTI : kTN;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const int ct = (int)(t % tiles_per_sub);
+        if (!wait_or_abort(&ctl.full[stage], phase, ctl)) {
+            named_bar_or(1, kConsumerThreads, true);
+            break;
+        }
+        const SubBlock &mt = ctl.meta[stage];
+        const int ntok = mt.ntok;
+        const int q0 = ln.ctid / cols, q1 = (ln.ctid + kConsumerThreads) / cols;
+        const int r0 = (q0 < ntok) ? mt.routes[q0] : -1;
+        const int r1 = (q1 < ntok) ? mt.routes[q1] : -1;
+        bool go = true;
+#define MOE_TILE(N)                                                                          \
+    case N:                                                                                  \
+        go = kGateUp ? gateup_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase)     \
+                     : down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);      \
+        break;
+        switch (ntok) {
+            MOE_TILE(1)
+            MOE_TILE(2)
+            MOE_TILE(3)
+            MOE_TILE(4)
+            MOE_TILE(5)
+            MOE_TILE(6)
+            MOE_TILE(7)
+            MOE_TILE(8)
+            default:  // an empty tile is announced by a single stage
+                release_stage(ctl, ln, stage, phase);
+                go = !named_bar_or(1, kConsumerThreads, false);
+        }
+#undef MOE_TILE
+        if (!go) break;
     }
 }
 
@@ -172,17 +427,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
-    float *red = reinterpret_cast<float *>(base + kStagesGU * kStageBytesGU);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStagesGU * kStageBytesGU + kRedBytesGU);
+    float *red = reinterpret_cast<float *>(base + kStages * kStageBytesGU);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesGU + kRedBytesGU);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStagesGU; ++s) {
-            mbar_init(&ctl.full[s], 1);
-            mbar_init(&ctl.empty[s], kConsumerWarps);
-        }
-        ctl.abort = 0;
-        fence_mbar_init();
+        init_ring(ctl);
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
     }
@@ -190,144 +440,34 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
 
-    const int64_t T = (a.npad[0] / a.rsub) * a.n_it;
+    const int64_t T = num_subblocks(a) * a.n_it;
+    const int per_tile = 2 * a.n_hb;  // gate box, up box, for every 256 rows of H
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
-            producer_loop<kStagesGU>(a, ctl, T, a.n_it, a.n_hg,
-                                     [&](int stage, int64_t t, int hg, const StageMeta &m) {
+            box_producer(a, ctl, T, a.n_it, per_tile, [&](int stage, int64_t t, int j, int e) {
                 const int it = (int)(t % a.n_it);
-                unsigned char *st = stages + stage * kStageBytesGU;
                 uint64_t *bar = &ctl.full[stage];
-                mbar_arrive_expect_tx(bar, 2 * kBoxBytesGU + m.ntok * kHG * 2);
-                const int32_t y = m.e * a.H + hg * kHG;
-                tma_load_2d(st, &tm_gate, it * kTI, y, bar, pol_w);
-                tma_load_2d(st + kBoxBytesGU, &tm_up, it * kTI, y, bar, pol_w);
-                for (int q = 0; q < m.ntok; ++q) {
-                    const int tok = m.routes[q] / a.k;
-                    bulk_load(st + 2 * kBoxBytesGU + q * kHG * 2,
-                              a.h + (size_t)tok * a.H + (size_t)hg * kHG, kHG * 2, bar);
-                }
+                mbar_arrive_expect_tx(bar, kBoxBytes);
+                tma_load_2d(stages + stage * kStageBytesGU,
+                            (j & 1) ? (const void *)&tm_up : (const void *)&tm_gate, it * kTI,
+                            e * a.H + (j >> 1) * kBoxRows, bar, pol_w);
             });
         }
         return;
     }
-
-    // ---------------------------------------------------------------- consumers
-    // Lane l of consumer warp w: columns 4*(l%16) .. +3 of the tile, rows 16w + 8*(l/16)
-    // .. +7 of every box (8 consecutive rows: one 16-byte load of each token's h slice).
-    const int ctid = threadIdx.x - 32;
-    const int cw = warp - 1;
-    const int half = lane >> 4;
-    const int c4 = (lane & 15) * 4;
-    const int rbase = cw * kRowsPerWarp + half * 8;
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        const int it = (int)(t % a.n_it);
-        float ag[kNT][4], au[kNT][4];
-#pragma unroll
-        for (int q = 0; q < kNT; ++q)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ag[q][j] = au[q][j] = 0.0f;
-        int ntok = 0, r0 = -1, r1 = -1;
-        bool failed = false;
-        for (int hg = 0; hg < a.n_hg; ++hg) {
-            if (failed || !wait_or_abort(&ctl.full[stage], phase, ctl)) {
-                failed = true;
-                break;
-            }
-            const StageMeta &mt = ctl.meta[stage];
-            if (hg == 0) {
-                ntok = mt.ntok;
-                const int q0 = ctid / kTI, q1 = (ctid + kConsumerThreads) / kTI;
-                r0 = (q0 < ntok) ? mt.routes[q0] : -1;
-                r1 = (q1 < ntok) ? mt.routes[q1] : -1;
-            }
-            if (ntok > 0) {
-                const unsigned char *st = stages + stage * kStageBytesGU;
-                uint2 gw[8], uw[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    gw[i] = *reinterpret_cast<const uint2 *>(st + (rbase + i) * (kTI * 2) + c4 * 2);
-                    uw[i] = *reinterpret_cast<const uint2 *>(st + kBoxBytesGU + (rbase + i) * (kTI * 2) + c4 * 2);
-                }
-                const unsigned char *xs = st + 2 * kBoxBytesGU + rbase * 2;
-#pragma unroll
-                for (int q = 0; q < kNT; ++q) {
-                    if (q < ntok) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + q * kHG * 2);
-                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint32_t x2 = xw[i >> 1];
-                            if (i & 1) {
-                                ag[q][0] = fma_bf16<1, 0>(x2, gw[i].x, ag[q][0]);
-                                ag[q][1] = fma_bf16<1, 1>(x2, gw[i].x, ag[q][1]);
-                                ag[q][2] = fma_bf16<1, 0>(x2, gw[i].y, ag[q][2]);
-                                ag[q][3] = fma_bf16<1, 1>(x2, gw[i].y, ag[q][3]);
-                                au[q][0] = fma_bf16<1, 0>(x2, uw[i].x, au[q][0]);
-                                au[q][1] = fma_bf16<1, 1>(x2, uw[i].x, au[q][1]);
-                                au[q][2] = fma_bf16<1, 0>(x2, uw[i].y, au[q][2]);
-                                au[q][3] = fma_bf16<1, 1>(x2, uw[i].y, au[q][3]);
-                            } else {
-                                ag[q][0] = fma_bf16<0, 0>(x2, gw[i].x, ag[q][0]);
-                                ag[q][1] = fma_bf16<0, 1>(x2, gw[i].x, ag[q][1]);
-                                ag[q][2] = fma_bf16<0, 0>(x2, gw[i].y, ag[q][2]);
-                                ag[q][3] = fma_bf16<0, 1>(x2, gw[i].y, ag[q][3]);
-                                au[q][0] = fma_bf16<0, 0>(x2, uw[i].x, au[q][0]);
-                                au[q][1] = fma_bf16<0, 1>(x2, uw[i].x, au[q][1]);
-                                au[q][2] = fma_bf16<0, 0>(x2, uw[i].y, au[q][2]);
-                                au[q][3] = fma_bf16<0, 1>(x2, uw[i].y, au[q][3]);
-                            }
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.empty[stage]);
-            advance<kStagesGU>(stage, phase);
-            if (ntok == 0) break;  // an empty tile is announced by a single stage
-        }
-        if (named_bar_or(1, kConsumerThreads, failed)) break;
-        if (ntok == 0) continue;
-        // rows of the two lane halves: half 0 + half 1 (the same bits on both lanes)
-#pragma unroll
-        for (int q = 0; q < kNT; ++q)
-            if (q < ntok) {
-                float g4[4], u4[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    g4[j] = ag[q][j] + __shfl_xor_sync(0xffffffffu, ag[q][j], 16);
-                    u4[j] = au[q][j] + __shfl_xor_sync(0xffffffffu, au[q][j], 16);
-                }
-                if (half == 0) {
-                    float *dst = &red[((cw * kNT + q) * kTI + c4) * 2];
-                    *reinterpret_cast<float4 *>(dst) = make_float4(g4[0], u4[0], g4[1], u4[1]);
-                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(g4[2], u4[2], g4[3], u4[3]);
-                }
-            }
-        named_bar_sync(1, kConsumerThreads);
-        const int col0 = it * kTI;
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int idx = ctid + pass * kConsumerThreads;
-            const int q = idx / kTI, c = idx % kTI;
-            const int r = pass ? r1 : r0;
-            if (q < ntok) {
-                float2 s = *reinterpret_cast<const float2 *>(&red[(q * kTI + c) * 2]);
-#pragma unroll
-                for (int w = 1; w < kConsumerWarps; ++w) {
-                    const float2 v = *reinterpret_cast<const float2 *>(&red[((w * kNT + q) * kTI + c) * 2]);
-                    s.x += v.x;
-                    s.y += v.y;
-                }
-                a.p[(int64_t)r * a.I + col0 + c] = silu_f32(s.x) * s.y;
-            }
-        }
-        named_bar_sync(1, kConsumerThreads);
+    if (warp == 1) {
+        // h rows [256 (j/2), +256) of each token: 512 bytes = one 16-byte piece per lane
+        slice_loader(a, ctl, stages, kStageBytesGU, kBoxRows * 2, 1, T, a.n_it, per_tile,
+                     [&](int route, int token, int64_t t, int j, int piece) {
+                         return reinterpret_cast<const unsigned char *>(a.h) +
+                                ((size_t)token * a.H + (size_t)(j >> 1) * kBoxRows) * 2 + piece * 16;
+                     });
+        return;
     }
+
+    consume_tiles<true>(a, ctl, stages, red, T, a.n_it);
 }
 
 // ------------------------------------------------------------------------------- down
@@ -337,156 +477,47 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
-    float *red = reinterpret_cast<float *>(base + kStagesDN * kStageBytesDN);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStagesDN * kStageBytesDN + kRedBytesDN);
+    float *red = reinterpret_cast<float *>(base + kStages * kStageBytesDN);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesDN + kRedBytesDN);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStagesDN; ++s) {
-            mbar_init(&ctl.full[s], 1);
-            mbar_init(&ctl.empty[s], kConsumerWarps);
-        }
-        ctl.abort = 0;
-        fence_mbar_init();
+        init_ring(ctl);
         prefetch_tensormap(&tm_down);
     }
     __syncthreads();
     // The routing and the alignment were complete before the gate/up kernel (the grid this
     // one depends on) started its work, so which down weights to read is already known
-    // ("A Multi-Engine Dataflow ...", overlap window of the down-projection DMA): the
-    // producer streams W_down boxes into the ring right away and waits for the gate/up
-    // grid only before it copies p, which that grid writes.
-    const int64_t T = (a.npad[0] / a.rsub) * a.n_ht;
+    // ("A Multi-Engine Dataflow ...", overlap window of the down-projection DMA): the box
+    // producer streams W_down right away; only the loader of p, which the gate/up grid
+    // writes, waits for that grid.
+    const int64_t T = num_subblocks(a) * a.n_ht;
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
-            bool waited = false;
-            int npend = 0;
-            int pend_stage[kStagesDN];
-            int pend_ig[kStagesDN];
-            StageMeta pend_meta[kStagesDN];
-            auto copy_p = [&](int stage, int ig, const StageMeta &m) {
-                unsigned char *st = stages + stage * kStageBytesDN;
-                for (int q = 0; q < m.ntok; ++q)
-                    bulk_load(st + kBoxBytesDN + q * kIG * 4,
-                              a.p + (size_t)m.routes[q] * a.I + (size_t)ig * kIG, kIG * 4,
-                              &ctl.full[stage]);
-            };
-            auto flush = [&]() {
-                pdl_wait();
-                waited = true;
-                for (int i = 0; i < npend; ++i) copy_p(pend_stage[i], pend_ig[i], pend_meta[i]);
-                npend = 0;
-            };
-            producer_loop<kStagesDN>(a, ctl, T, a.n_ht, a.n_ig,
-                                     [&](int stage, int64_t t, int ig, const StageMeta &m) {
+            box_producer(a, ctl, T, a.n_ht, a.n_ib, [&](int stage, int64_t t, int j, int e) {
                 const int ht = (int)(t % a.n_ht);
-                unsigned char *st = stages + stage * kStageBytesDN;
                 uint64_t *bar = &ctl.full[stage];
-                mbar_arrive_expect_tx(bar, kBoxBytesDN + m.ntok * kIG * 4);
-                tma_load_2d(st, &tm_down, ht * kTN, m.e * a.I + ig * kIG, bar, pol_w);
-                if (waited) {
-                    copy_p(stage, ig, m);
-                } else {
-                    pend_stage[npend] = stage;
-                    pend_ig[npend] = ig;
-                    pend_meta[npend] = m;
-                    ++npend;
-                }
-            }, [&]() { if (!waited) flush(); });
+                mbar_arrive_expect_tx(bar, kBoxBytes);
+                tma_load_2d(stages + stage * kStageBytesDN, &tm_down, ht * kTN,
+                            e * a.I + j * kBoxRows, bar, pol_w);
+            });
         }
         return;
     }
-    pdl_launch_dependents();
-
-    // Same lane layout as gate/up: 4 columns x 8 consecutive rows of every box.
-    const int ctid = threadIdx.x - 32;
-    const int cw = warp - 1;
-    const int half = lane >> 4;
-    const int c4 = (lane & 15) * 4;
-    const int rbase = cw * kRowsPerWarp + half * 8;
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        const int ht = (int)(t % a.n_ht);
-        float acc[kNT][4];
-#pragma unroll
-        for (int q = 0; q < kNT; ++q)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[q][j] = 0.0f;
-        int ntok = 0, r0 = -1, r1 = -1;
-        bool failed = false;
-        for (int ig = 0; ig < a.n_ig; ++ig) {
-            if (failed || !wait_or_abort(&ctl.full[stage], phase, ctl)) {
-                failed = true;
-                break;
-            }
-            const StageMeta &mt = ctl.meta[stage];
-            if (ig == 0) {
-                ntok = mt.ntok;
-                const int q0 = ctid / kTN, q1 = (ctid + kConsumerThreads) / kTN;
-                r0 = (q0 < ntok) ? mt.routes[q0] : -1;
-                r1 = (q1 < ntok) ? mt.routes[q1] : -1;
-            }
-            if (ntok > 0) {
-                const unsigned char *st = stages + stage * kStageBytesDN;
-                float w[8][4];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint2 w2 = *reinterpret_cast<const uint2 *>(st + (rbase + i) * (kTN * 2) + c4 * 2);
-                    w[i][0] = bf16_lo(w2.x);
-                    w[i][1] = bf16_hi(w2.x);
-                    w[i][2] = bf16_lo(w2.y);
-                    w[i][3] = bf16_hi(w2.y);
-                }
-                const float *xs = reinterpret_cast<const float *>(st + kBoxBytesDN) + rbase;
-#pragma unroll
-                for (int q = 0; q < kNT; ++q) {
-                    if (q < ntok) {
-                        const float4 p0 = *reinterpret_cast<const float4 *>(xs + q * kIG);
-                        const float4 p1 = *reinterpret_cast<const float4 *>(xs + q * kIG + 4);
-                        const float x[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            ffma2(acc[q][0], acc[q][1], x[i], w[i][0], w[i][1]);
-                            ffma2(acc[q][2], acc[q][3], x[i], w[i][2], w[i][3]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.empty[stage]);
-            advance<kStagesDN>(stage, phase);
-            if (ntok == 0) break;
-        }
-        if (named_bar_or(1, kConsumerThreads, failed)) break;
-        if (ntok == 0) continue;
-#pragma unroll
-        for (int q = 0; q < kNT; ++q)
-            if (q < ntok) {
-                float v[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) v[j] = acc[q][j] + __shfl_xor_sync(0xffffffffu, acc[q][j], 16);
-                if (half == 0)
-                    *reinterpret_cast<float4 *>(&red[(cw * kNT + q) * kTN + c4]) = make_float4(v[0], v[1], v[2], v[3]);
-            }
-        named_bar_sync(1, kConsumerThreads);
-        const int col0 = ht * kTN;
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int idx = ctid + pass * kConsumerThreads;
-            const int q = idx / kTN, c = idx % kTN;
-            const int r = pass ? r1 : r0;
-            if (q < ntok) {
-                float sum = red[q * kTN + c];
-#pragma unroll
-                for (int w2 = 1; w2 < kConsumerWarps; ++w2) sum += red[(w2 * kNT + q) * kTN + c];
-                a.y[(int64_t)r * a.H + col0 + c] = sum;
-            }
-        }
-        named_bar_sync(1, kConsumerThreads);
+    if (warp == 1) {
+        pdl_wait();
+        // p rows [256 j, +256) of each route: 1 KB = two 16-byte pieces per lane
+        slice_loader(a, ctl, stages, kStageBytesDN, kBoxRows * 4, 2, T, a.n_ht, a.n_ib,
+                     [&](int route, int token, int64_t t, int j, int piece) {
+                         return reinterpret_cast<const unsigned char *>(a.p) +
+                                ((size_t)route * a.I + (size_t)j * kBoxRows) * 4 + piece * 16;
+                     });
+        return;
     }
+    pdl_launch_dependents();
+    consume_tiles<false>(a, ctl, stages, red, T, a.n_ht);
 }
 
 // ---------------------------------------------------------------------------- combine
@@ -528,8 +559,8 @@ __global__ void __launch_bounds__(kCombineThreads)
     *reinterpret_cast<uint2 *>(out + o) = ov;
 }
 
-static size_t gateup_smem() { return 1024 + kStagesGU * kStageBytesGU + kRedBytesGU + sizeof(Ctl); }
-static size_t down_smem() { return 1024 + kStagesDN * kStageBytesDN + kRedBytesDN + sizeof(Ctl); }
+static size_t gateup_smem() { return 1024 + kStages * kStageBytesGU + kRedBytesGU + sizeof(Ctl); }
+static size_t down_smem() { return 1024 + kStages * kStageBytesDN + kRedBytesDN + sizeof(Ctl); }
 
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream) {

@@ -14,11 +14,10 @@ namespace moe {
 // GEMV-regime tiling (fixed, so every reduction order depends on tile indices only).
 constexpr int kNT = 8;          // tokens per sub-block (register tile of the GEMV kernels)
 constexpr int kTI = 64;         // gate/up: I columns per tile (128-byte rows in shared memory)
-constexpr int kHG = 128;        // gate/up: H rows per unit
 constexpr int kTN = 64;         // down: H columns per tile
-constexpr int kIG = 128;        // down: I rows per unit
+constexpr int kBoxRows = 256;   // rows (of H for gate/up, of I for down) per weight box
 constexpr int kConsumerWarps = 8;
-constexpr int kGemvThreads = 32 * (1 + kConsumerWarps);
+constexpr int kGemvThreads = 32 * (2 + kConsumerWarps);  // producer, loader, consumers
 constexpr int kRouterCluster = 8;  // CTAs per router cluster (split of H)
 constexpr int kRouterThreads = 256;
 
@@ -28,14 +27,26 @@ struct Dims {
     int64_t R;        // routes M*k (also the sentinel value)
     int64_t cap;      // alignment capacity in rows
     int64_t max_sub;  // cap / rsub
-    int n_it, n_hg, n_ht, n_ig;
+    int n_it, n_hb, n_ht, n_ib;  // column tiles and 256-row boxes of gate/up and down
 };
+
+// One sub-block of the alignment (rsub consecutive aligned rows of one expert), as the
+// expert kernels consume it: the expert, its valid routes in row order, and their tokens.
+struct __align__(16) SubBlock {
+    int e;
+    int ntok;
+    int routes[kNT];
+    int tokens[kNT];
+    int pad[2];
+};
+static_assert(sizeof(SubBlock) == 80, "SubBlock layout");
 
 struct WsLayout {
     size_t status;   // int32[16]
     size_t sorted;   // int32[cap]
     size_t blocks;   // int32[cap / b]
     size_t npad;     // int32[4]
+    size_t sbt;      // SubBlock[max_sub]
     size_t p;        // float[R * I]   SiLU(g) * u per route
     size_t y;        // float[R * H]   down-projection output per route
     size_t total;
@@ -48,8 +59,7 @@ struct GemvArgs {
     const __nv_bfloat16 *h;
     const int32_t *topk_ids;
     const float *topk_wts;
-    const int32_t *sorted;
-    const int32_t *blocks;
+    const SubBlock *sbt;
     const int32_t *npad;
     const __nv_bfloat16 *residual;
     __nv_bfloat16 *out;
@@ -57,18 +67,64 @@ struct GemvArgs {
     float *y;
     int32_t *status;
     int M, k, E, H, I, b, rsub;
-    int n_it, n_hg, n_ht, n_ig;
+    int n_it, n_hb, n_ht, n_ib;
+    int64_t max_sub;  // rows of the sub-block table
 };
 
+// Sub-blocks to process: num_padded / rsub, never more than the table holds.
+__device__ __forceinline__ int64_t num_subblocks(const GemvArgs &a) {
+    const int64_t n = a.npad[0] / a.rsub;
+    return n < 0 ? 0 : (n > a.max_sub ? a.max_sub : n);
+}
+
 int num_sms();
+
+// Record of sub-block sb: expert of its block, valid routes (0 <= r < R) of its rsub rows in
+// row order, token of each route.  With `check`, a route whose top-k id is not the block's
+// expert is left out and flagged as a bad alignment.
+__device__ __forceinline__ void build_subblock(const int32_t *sorted, const int32_t *blocks,
+                                               const int32_t *topk_ids, int64_t sb, int rsub,
+                                               int b, int E, int64_t R, int k, bool check,
+                                               int32_t *status, SubBlock *out) {
+    const int64_t row0 = sb * rsub;
+    const int e = blocks[row0 / b];
+    SubBlock rec;
+    rec.e = e;
+    int n = 0;
+#pragma unroll 1
+    for (int q = 0; q < kNT; ++q) rec.routes[q] = rec.tokens[q] = -1;
+    rec.pad[0] = rec.pad[1] = 0;
+    if (e >= 0 && e < E) {
+#pragma unroll 1
+        for (int q = 0; q < rsub; ++q) {
+            const int r = sorted[row0 + q];
+            if (r < 0 || r >= R) continue;
+            if (check && topk_ids[r] != e) {
+                if (status) atomicOr(status, MOE_DEV_BAD_ALIGNMENT);
+                continue;
+            }
+            rec.routes[n] = r;
+            rec.tokens[n] = r / k;
+            ++n;
+        }
+    }
+    rec.ntok = n;
+    *out = rec;
+}
 
 cudaError_t launch_router(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                           const float *bias, int M, int H, int E, int k, int renormalize,
                           int32_t *topk_ids, float *topk_weights, cudaStream_t stream);
 
+// Alignment; when `sbt` is not NULL it also writes the sub-block table of rsub-row blocks.
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b,
                          int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
-                         int32_t *status, cudaStream_t stream);
+                         SubBlock *sbt, int rsub, int32_t *status, cudaStream_t stream);
+
+// Sub-block table from a caller-supplied alignment, checking each row against topk_ids.
+cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const int32_t *blocks,
+                        const int32_t *npad, int M, int k, int E, int b, int rsub,
+                        int64_t max_sub, SubBlock *sbt, int32_t *status, cudaStream_t stream);
 
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream);

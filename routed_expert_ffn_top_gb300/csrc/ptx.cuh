@@ -109,6 +109,19 @@ __device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gsrc,
         : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy through L2 only (never a stale L1 line).
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc))
+                 : "memory");
+}
+
+// The mbarrier's current phase also waits for this thread's earlier cp.async copies: the
+// pending count is raised now and lowered when the copies have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---------------------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

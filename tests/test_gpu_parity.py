@@ -104,9 +104,9 @@ def test_align_large_and_deterministic():
 # ------------------------------------------------------------------- expert FFN, small
 SMALL = [
     # M, k, E, H, I, b
-    (1, 1, 8, 128, 128, 1), (5, 2, 8, 256, 128, 3), (13, 8, 16, 384, 256, 8),
-    (3, 4, 32, 128, 384, 16), (37, 6, 64, 256, 128, 64), (64, 8, 128, 512, 256, 8),
-    (2, 8, 8, 1024, 640, 2), (9, 3, 40, 640, 128, 5),
+    (1, 1, 8, 256, 256, 1), (5, 2, 8, 512, 256, 3), (13, 8, 16, 768, 512, 8),
+    (3, 4, 32, 256, 768, 16), (37, 6, 64, 256, 256, 64), (64, 8, 128, 512, 256, 8),
+    (2, 8, 8, 1024, 1280, 2), (9, 3, 40, 1280, 256, 5),
 ]
 
 
@@ -138,7 +138,7 @@ def test_expert_ffn_small(M, k, E, H, I, b):
 
 
 def test_expert_ffn_invalid_ids_and_status():
-    M, k, E, H, I, b = 6, 3, 16, 256, 128, 4
+    M, k, E, H, I, b = 6, 3, 16, 256, 256, 4
     wl, layer, h = _small_layer(M, k, E, H, I, b, seed=3)
     ids = np.array([[0, -1, 5], [16, 2, 3], [-5, -1, 99], [7, 7, 1], [15, 0, 4], [9, 10, 11]],
                    np.int32)
@@ -157,7 +157,7 @@ def test_expert_ffn_invalid_ids_and_status():
 
 
 def test_expert_ffn_bad_alignment_is_flagged():
-    M, k, E, H, I, b = 4, 2, 8, 128, 128, 2
+    M, k, E, H, I, b = 4, 2, 8, 256, 256, 2
     wl, layer, h = _small_layer(M, k, E, H, I, b, seed=4)
     ids = np.array([[0, 1], [1, 2], [2, 3], [3, 0]], np.int32)
     t_ids = torch.as_tensor(ids, device=DEV)
@@ -201,8 +201,8 @@ def test_membership_invariance_bitwise():
 
 
 def test_expert_ffn_m0_is_noop():
-    wl, layer, h = _small_layer(1, 2, 8, 128, 128, 8)
-    out = torch.zeros(0, 128, dtype=torch.bfloat16, device=DEV)
+    wl, layer, h = _small_layer(1, 2, 8, 256, 256, 8)
+    out = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
     ids = torch.zeros(0, 2, dtype=torch.int32, device=DEV)
     a = torch.zeros(0, 2, dtype=torch.float32, device=DEV)
     ws = torch.zeros(1024, dtype=torch.uint8, device=DEV)
