@@ -168,19 +168,24 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    kernel source; otherwise None."""
-    path = os.path.join(PROFILES, "dram_traffic.json")
+def recorded_traffic(kernel: str, workload: str, unique_experts: float):
+    """DRAM bytes per launch of `kernel`, from the committed ncu record
+    (profiles/dram_traffic.txt: kernel, workload, kernel-source hash, unique experts of the
+    captured launch, dram read+write bytes of that launch), scaled to `unique_experts`
+    routed experts.  None when there is no record taken on the current kernel source."""
+    path = os.path.join(PROFILES, "dram_traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        ent = d[kernel][workload]
-        if ent.get("source_hash") != kernel_source_hash():
-            return None
-        return float(ent["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError, TypeError):
+            for line in f:
+                parts = line.split()
+                if len(parts) != 5 or line.startswith("#"):
+                    continue
+                k, wl, src, u, b = parts
+                if k == kernel and wl == workload and src == kernel_source_hash():
+                    return float(b) / float(u) * unique_experts
+    except (OSError, ValueError):
         return None
+    return None
 
 
 def expert_bytes(wl):
@@ -294,6 +299,7 @@ def run_ours(args, world, rank, local):
         "us_per_layer": round(us_per_layer, 3),
         "hbm_gbs_unique_expert_bytes": round(hbm_gbs, 1),
         "unique_experts_per_layer": round(statistics.mean(per_set_unique), 2),
+        "unique_experts_per_set": per_set_unique,
         "gpu_launches": launches_per_block * blocks_per_step * args.steps,
         "clocks": clocks,
     }
@@ -333,11 +339,12 @@ def run_ours(args, world, rank, local):
     u_mean = statistics.mean(per_set_unique)
     gu_alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * 4
     achieved = gu_alg / (mean_ms["gateup"] * 1e-3) / 1e9
-    traffic = recorded_traffic("gateup_dense_kernel", wl.name)
+    traffic = recorded_traffic("gateup_dense_kernel", wl.name, u_mean)
     result["roofline"] = {
         "kernel": "gateup_dense_kernel", "bound": "hbm", "achieved": round(achieved, 1),
         "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-        "traffic": traffic, "algorithmic_bytes_per_launch": int(gu_alg),
+        "traffic": None if traffic is None else int(traffic),
+        "algorithmic_bytes_per_launch": int(gu_alg),
         "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
     }
     dn_alg = u_mean * dn_b + M * wl.k * (wl.I + wl.H) * 4
@@ -408,15 +415,17 @@ def _time_oracle_block(wl, hb, wr, bias, w, remap, tokens):
 def cpu_baseline(wl, layer, h, seconds):
     import oracle
     oracle.build()
-    tokens = h.shape[0]
+    # a bounded sample: whole passes over at most 32 tokens of the batch
+    tokens = min(h.shape[0], 32)
     hb, wr, bias, w, remap = _oracle_block_sample(wl, layer, h, tokens)
     total, n = 0.0, 0
     while total < seconds or n == 0:
         total += _time_oracle_block(wl, hb, wr, bias, w, remap, tokens)
         n += 1
     return {"value": round(tokens * n / total, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d full passes of the %s block (%d tokens, all routed experts), "
-                      "single-threaded fp64 C oracle, %.1f s" % (n, wl.name, tokens, total)}
+            "sample": "%d passes of the %s block over %d of its %d tokens (router, all their "
+                      "routed experts, combine), single-threaded fp64 C oracle, %.1f s"
+                      % (n, wl.name, tokens, h.shape[0], total)}
 
 
 # ------------------------------------------------------------------------- reference
