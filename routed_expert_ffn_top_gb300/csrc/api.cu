@@ -173,8 +173,12 @@ static int check_weights(const moe_expert_weights_t *w) {
     }
     if (w->kind == MOE_W_VQ_GATEUP) {
         if (!w->j_gate || !w->j_up || !w->cb_gate || !w->cb_up) return MOE_ERR_INVALID_ARG;
+        if (!aligned(w->j_gate, 16) || !aligned(w->j_up, 16) || !aligned(w->cb_gate, 16) ||
+            !aligned(w->cb_up, 16))
+            return MOE_ERR_INVALID_ARG;
         if (w->d != 4 || w->K != 256) return MOE_ERR_UNSUPPORTED;
-        return MOE_ERR_UNSUPPORTED;  // the VQ expert kernels are not part of this build
+        if (w->H % (4 * kBoxRows) != 0) return MOE_ERR_UNSUPPORTED;  // 1024-row index boxes
+        return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;
 }
@@ -244,13 +248,21 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
                        const int32_t *topk_ids, const float *topk_weights, const int32_t *npad,
                        const void *residual, void *out, unsigned char *ws, const WsLayout &L,
                        cudaStream_t stream) {
+    const bool vq = w->kind == MOE_W_VQ_GATEUP;
     CUtensorMap tm_gate, tm_up, tm_down;
-    if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, kTI, kBoxRows) ||
-        !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, kTI, kBoxRows) ||
-        !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
-                      (uint64_t)d.E * d.I, kTN, kBoxRows))
+    bool ok;
+    if (vq)  // index maps [E * H/4 rows][I] uint8, boxes of 256 rows x 64 columns
+        ok = make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                          (uint64_t)d.E * (d.H / 4), kTI, kBoxRows) &&
+             make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                          (uint64_t)d.E * (d.H / 4), kTI, kBoxRows);
+    else
+        ok = make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                          (uint64_t)d.E * d.H, kTI, kBoxRows) &&
+             make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                          (uint64_t)d.E * d.H, kTI, kBoxRows);
+    if (!ok || !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
+                             (uint64_t)d.E * d.I, kTN, kBoxRows))
         return MOE_ERR_CUDA;
     GemvArgs a;
     a.h = static_cast<const __nv_bfloat16 *>(h);
@@ -275,7 +287,11 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.n_ht = d.n_ht;
     a.n_ib = d.n_ib;
     a.max_sub = d.max_sub;
-    cudaError_t err = launch_gateup_dense(tm_gate, tm_up, a, stream);
+    a.cb_gate = vq ? static_cast<const uint2 *>(w->cb_gate) : nullptr;
+    a.cb_up = vq ? static_cast<const uint2 *>(w->cb_up) : nullptr;
+    a.n_qb = d.H / (4 * kBoxRows);
+    cudaError_t err = vq ? launch_gateup_vq(tm_gate, tm_up, a, stream)
+                         : launch_gateup_dense(tm_gate, tm_up, a, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
     err = launch_down(tm_down, a, stream);

@@ -54,9 +54,20 @@ constexpr int kBoxBytes = kBoxRows * kTI * 2;                 // 32 KB (also kTN
 constexpr int kStageBytesGU = kBoxBytes + kNT * kBoxRows * 2;  // + h slices (bf16)
 constexpr int kStageBytesDN = kBoxBytes + kNT * kBoxRows * 4;  // + p slices (fp32)
 constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 2 * 4;
+// VQ gate/up: a box is 256 rows x 64 columns of uint8 code indices (16 KB), i.e. 1024 rows of
+// H; its activation slices are those 1024 h values of each route's token.
+constexpr int kVQRows = 256;
+constexpr int kVQHRows = 4 * kVQRows;
+constexpr int kVQBoxBytes = kVQRows * kTI;
+constexpr int kStageBytesVQ = kVQBoxBytes + kNT * kVQHRows * 2;
+constexpr int kCodeBookBytes = 256 * 8;
 constexpr int kRedBytesDN = kConsumerWarps * kNT * kTN * 4;
 static_assert(kTI == kTN, "one box shape for both kernels");
-static_assert(kStageBytesGU % 1024 == 0 && kStageBytesDN % 1024 == 0, "stage alignment");
+static_assert(kStageBytesGU % 1024 == 0 && kStageBytesDN % 1024 == 0 && kStageBytesVQ % 1024 == 0,
+              "stage alignment");
+static_assert(kVQRows == kBoxRows, "the consumer lanes own 16 of the 256 rows of every box");
+
+enum TileKind { kDenseGateUp = 0, kDown = 1, kVQGateUp = 2 };
 
 struct Ctl {
     uint64_t full[kStages];
@@ -147,8 +158,8 @@ __device__ void box_producer(const GemvArgs &a, Ctl &ctl, int64_t T, int tiles_p
 // area.  Its arrival on the stage's full barrier completes only when its copies have landed.
 template <typename SrcFn>
 __device__ void slice_loader(const GemvArgs &a, Ctl &ctl, unsigned char *stages, int stage_bytes,
-                             int slice_bytes, int chunks, int64_t T, int tiles_per_sub,
-                             int stages_per_tile, SrcFn src) {
+                             int box_bytes, int slice_bytes, int chunks, int64_t T,
+                             int tiles_per_sub, int stages_per_tile, SrcFn src) {
     const int lane = threadIdx.x & 31;
     int stage = 0;
     uint32_t phase = 0;
@@ -163,7 +174,7 @@ __device__ void slice_loader(const GemvArgs &a, Ctl &ctl, unsigned char *stages,
         for (int j = 0; j < nst; ++j) {
             if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) return;
             if (ntok > 0) {
-                unsigned char *dst = stages + stage * stage_bytes + kBoxBytes;
+                unsigned char *dst = stages + stage * stage_bytes + box_bytes;
                 for (int q = 0; q < ntok; ++q) {
                     const int route = __shfl_sync(0xffffffffu, my_route, q);
                     const int token = __shfl_sync(0xffffffffu, my_token, q);
@@ -256,6 +267,36 @@ __device__ __forceinline__ void accumulate_f32_box(const unsigned char *st, cons
     }
 }
 
+// VQ box ("A Multi-Engine Dataflow ...", Section 2.3: column i of W_e is cut into length-4
+// blocks along H, block q holding code word J[e][q][i] of the layer-shared code book):
+// acc[q][c] += sum over this thread's 16 index rows r of sum_t x_q[4r + t] * cb[J[r][c]][t]
+// (bf16 x bf16 -> fp32, H rows ascending).  `cb` is the code book in shared memory.
+template <int NT>
+__device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const uint2 *cb,
+                                                  const Lane &ln, float (&acc)[NT][4]) {
+    const unsigned char *xs = st + kVQBoxBytes + ln.rbase * 8;
+#pragma unroll 4
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const uint32_t jw = *reinterpret_cast<const uint32_t *>(st + (ln.rbase + i) * kTI + ln.c4);
+        uint2 cw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cw[c] = cb[(jw >> (8 * c)) & 0xffu];
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const uint2 xv = *reinterpret_cast<const uint2 *>(xs + q * kVQHRows * 2 + i * 8);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v = acc[q][c];
+                v = fma_bf16<0, 0>(xv.x, cw[c].x, v);
+                v = fma_bf16<1, 1>(xv.x, cw[c].x, v);
+                v = fma_bf16<0, 0>(xv.y, cw[c].y, v);
+                v = fma_bf16<1, 1>(xv.y, cw[c].y, v);
+                acc[q][c] = v;
+            }
+        }
+    }
+}
+
 // Releases the stage to the box producer and the loader once this warp is done with it.
 __device__ __forceinline__ void release_stage(Ctl &ctl, const Lane &ln, int &stage, uint32_t &phase) {
     __syncwarp();
@@ -265,26 +306,36 @@ __device__ __forceinline__ void release_stage(Ctl &ctl, const Lane &ln, int &sta
 
 // One gate/up tile with NT routes; its first stage has already been waited for.  Returns
 // false when the CTA must stop (a bounded wait gave up somewhere in the CTA).
-template <int NT>
+template <int NT, bool kVQ>
 __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
-                            const Lane &ln, int it, int r0, int r1, int &stage, uint32_t &phase) {
+                            const uint2 *cbs, const Lane &ln, int it, int r0, int r1, int &stage,
+                            uint32_t &phase) {
     float ag[NT][4], au[NT][4];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ag[q][c] = au[q][c] = 0.0f;
     bool failed = false;
-    // stages of a tile: gate box, up box for rows [0, 256), then for [256, 512), ...
-    for (int j = 0; j < 2 * a.n_hb; ++j) {
+    // stages of a tile: gate box, up box for the first rows of H, then the next rows, ...
+    const int nst = kVQ ? 2 * a.n_qb : 2 * a.n_hb;
+    for (int j = 0; j < nst; ++j) {
         if (j > 0 && !wait_or_abort(&ctl.full[stage], phase, ctl)) {
             failed = true;
             break;
         }
-        const unsigned char *st = stages + stage * kStageBytesGU;
-        if (j & 1)
-            accumulate_bf16_box<NT>(st, ln, au);
-        else
-            accumulate_bf16_box<NT>(st, ln, ag);
+        if constexpr (kVQ) {
+            const unsigned char *st = stages + stage * kStageBytesVQ;
+            if (j & 1)
+                accumulate_vq_box<NT>(st, cbs + 256, ln, au);
+            else
+                accumulate_vq_box<NT>(st, cbs, ln, ag);
+        } else {
+            const unsigned char *st = stages + stage * kStageBytesGU;
+            if (j & 1)
+                accumulate_bf16_box<NT>(st, ln, au);
+            else
+                accumulate_bf16_box<NT>(st, ln, ag);
+        }
         release_stage(ctl, ln, stage, phase);
     }
     if (named_bar_or(1, kConsumerThreads, failed)) return false;
@@ -370,9 +421,9 @@ __device__ bool down_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, fl
 
 // Consumer loop shared by both kernels: waits for a tile's first stage, reads how many routes
 // it has, and runs the tile body specialised for that count.
-template <bool kGateUp>
+template <int kKind>
 __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
-                              int64_t T, int tiles_per_sub) {
+                              const uint2 *cbs, int64_t T, int tiles_per_sub) {
     const int warp = threadIdx.x >> 5;
     Lane ln;
     ln.ctid = threadIdx.x - 32 * kFirstConsumerWarp;
@@ -381,7 +432,7 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
     ln.half = ln.lane >> 4;
     ln.c4 = (ln.lane & 15) * 4;
     ln.rbase = ln.cw * kRowsPerWarp + ln.half * kRowsPerThread;
-    const int cols = kGateUp ? kTI : kTN;
+    const int cols = kKind == kDown ? kTN : kTI;
     int stage = 0;
     uint32_t phase = 0;
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -398,8 +449,11 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
         bool go = true;
 #define MOE_TILE(N)                                                                          \
     case N:                                                                                  \
-        go = kGateUp ? gateup_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase)     \
-                     : down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);      \
+        if constexpr (kKind == kDown)                                                        \
+            go = down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);            \
+        else                                                                                 \
+            go = gateup_tile<N, kKind == kVQGateUp>(a, ctl, stages, red, cbs, ln, ct, r0, r1, \
+                                                    stage, phase);                           \
         break;
         switch (ntok) {
             MOE_TILE(1)
@@ -459,7 +513,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     if (warp == 1) {
         // h rows [256 (j/2), +256) of each token: 512 bytes = one 16-byte piece per lane
-        slice_loader(a, ctl, stages, kStageBytesGU, kBoxRows * 2, 1, T, a.n_it, per_tile,
+        slice_loader(a, ctl, stages, kStageBytesGU, kBoxBytes, kBoxRows * 2, 1, T, a.n_it, per_tile,
                      [&](int route, int token, int64_t t, int j, int piece) {
                          return reinterpret_cast<const unsigned char *>(a.h) +
                                 ((size_t)token * a.H + (size_t)(j >> 1) * kBoxRows) * 2 + piece * 16;
@@ -467,7 +521,61 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         return;
     }
 
-    consume_tiles<true>(a, ctl, stages, red, T, a.n_it);
+    consume_tiles<kDenseGateUp>(a, ctl, stages, red, nullptr, T, a.n_it);
+}
+
+// ------------------------------------------------------------------------- VQ gate/up
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    gateup_vq_kernel(const __grid_constant__ CUtensorMap tm_jgate,
+                     const __grid_constant__ CUtensorMap tm_jup, const GemvArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *stages = base;
+    float *red = reinterpret_cast<float *>(base + kStages * kStageBytesVQ);
+    uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kStageBytesVQ + kRedBytesGU);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesVQ + kRedBytesGU + 2 * kCodeBookBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        init_ring(ctl);
+        prefetch_tensormap(&tm_jgate);
+        prefetch_tensormap(&tm_jup);
+    }
+    // the layer-shared code books (weights, not produced by an earlier kernel)
+    for (int i = threadIdx.x; i < 512; i += blockDim.x)
+        cbs[i] = i < 256 ? a.cb_gate[i] : a.cb_up[i - 256];
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int64_t T = num_subblocks(a) * a.n_it;
+    const int per_tile = 2 * a.n_qb;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            box_producer(a, ctl, T, a.n_it, per_tile, [&](int stage, int64_t t, int j, int e) {
+                const int it = (int)(t % a.n_it);
+                uint64_t *bar = &ctl.full[stage];
+                mbar_arrive_expect_tx(bar, kVQBoxBytes);
+                tma_load_2d(stages + stage * kStageBytesVQ,
+                            (j & 1) ? (const void *)&tm_jup : (const void *)&tm_jgate, it * kTI,
+                            e * (a.H / 4) + (j >> 1) * kVQRows, bar, pol_w);
+            });
+        }
+        return;
+    }
+    if (warp == 1) {
+        // h rows [1024 (j/2), +1024) of each token: 2 KB = four 16-byte pieces per lane
+        slice_loader(a, ctl, stages, kStageBytesVQ, kVQBoxBytes, kVQHRows * 2, 4, T, a.n_it, per_tile,
+                     [&](int route, int token, int64_t t, int j, int piece) {
+                         return reinterpret_cast<const unsigned char *>(a.h) +
+                                ((size_t)token * a.H + (size_t)(j >> 1) * kVQHRows) * 2 + piece * 16;
+                     });
+        return;
+    }
+    consume_tiles<kVQGateUp>(a, ctl, stages, red, cbs, T, a.n_it);
 }
 
 // ------------------------------------------------------------------------------- down
@@ -509,7 +617,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     if (warp == 1) {
         pdl_wait();
         // p rows [256 j, +256) of each route: 1 KB = two 16-byte pieces per lane
-        slice_loader(a, ctl, stages, kStageBytesDN, kBoxRows * 4, 2, T, a.n_ht, a.n_ib,
+        slice_loader(a, ctl, stages, kStageBytesDN, kBoxBytes, kBoxRows * 4, 2, T, a.n_ht, a.n_ib,
                      [&](int route, int token, int64_t t, int j, int piece) {
                          return reinterpret_cast<const unsigned char *>(a.p) +
                                 ((size_t)route * a.I + (size_t)j * kBoxRows) * 4 + piece * 16;
@@ -517,7 +625,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         return;
     }
     pdl_launch_dependents();
-    consume_tiles<false>(a, ctl, stages, red, T, a.n_ht);
+    consume_tiles<kDown>(a, ctl, stages, red, nullptr, T, a.n_ht);
 }
 
 // ---------------------------------------------------------------------------- combine
@@ -571,6 +679,21 @@ cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &t
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, gateup_dense_kernel, tm_gate, tm_up, a);
+}
+
+static size_t gateup_vq_smem() {
+    return 1024 + kStages * kStageBytesVQ + kRedBytesGU + 2 * kCodeBookBytes + sizeof(Ctl);
+}
+
+cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                             const GemvArgs &a, cudaStream_t stream) {
+    const size_t smem = gateup_vq_smem();
+    cudaError_t err = cudaFuncSetAttribute(gateup_vq_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, gateup_vq_kernel, tm_jgate, tm_jup, a);
 }
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream) {

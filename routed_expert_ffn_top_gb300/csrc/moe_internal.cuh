@@ -66,9 +66,12 @@ struct GemvArgs {
     float *p;
     float *y;
     int32_t *status;
+    const uint2 *cb_gate;  // VQ code books [256] code words of 4 bf16 (NULL when dense)
+    const uint2 *cb_up;
     int M, k, E, H, I, b, rsub;
     int n_it, n_hb, n_ht, n_ib;
-    int64_t max_sub;  // rows of the sub-block table
+    int n_qb;              // VQ: index-map boxes of 256 rows (1024 rows of H) per projection
+    int64_t max_sub;       // rows of the sub-block table
 };
 
 // Sub-blocks to process: num_padded / rsub, never more than the table holds.
@@ -128,6 +131,10 @@ cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const in
 
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream);
+
+// Blockwise-VQ gate/up (d = 4, K = 256): index maps through TMA, code books in shared memory.
+cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                             const GemvArgs &a, cudaStream_t stream);
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream);
 

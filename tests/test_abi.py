@@ -95,6 +95,14 @@ def test_validation_fails_closed_without_gpu(lib):
     wv.d = 8
     assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wv), 1, 8, 8, None, fake, ids, ids,
                                 vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    # VQ with H not a multiple of 1024 (index boxes cover 1024 rows of H)
+    wv = _weights(kind=1, H=1536)
+    assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wv), 1, 8, 8, None, fake, ids, ids,
+                                vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    # dense H, I not multiples of 256
+    wd = _weights(H=2048 + 128)
+    assert lib.moe_expert_ffn(fake, ctypes.byref(wd), 4, 8, ids, ids, None, None, None, 8, None,
+                              fake, vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
     # unknown weight kind
     wk = _weights(kind=7)
     assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wk), 1, 8, 8, None, fake, ids, ids,

@@ -284,6 +284,51 @@ def test_host_entry_point_matches_device():
     assert torch.equal(out_host, out.cpu())
 
 
+VQ_SMALL = [
+    # M, k, E, H, I, b
+    (5, 2, 8, 1024, 256, 3), (13, 4, 16, 2048, 512, 8), (2, 8, 8, 1024, 768, 1), (30, 3, 24, 1024, 256, 16),
+]
+
+
+@pytest.mark.parametrize("M,k,E,H,I,b", VQ_SMALL)
+def test_vq_expert_ffn_small(M, k, E, H, I, b):
+    wl = syn.Workload("vq_small_%d_%d_%d" % (M, k, E), H=H, I=I, E=E, k=k, b=b, M=M,
+                      kind=syn.W_VQ, d=4, K=256)
+    layer = syn.make_layer(wl, seed=2, device=DEV)
+    h = syn.make_hidden(wl, seed=2, device=DEV)
+    rng = np.random.default_rng(M + E)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    res = syn.make_hidden(wl, seed=4, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, torch.as_tensor(ids, device=DEV),
+                             torch.as_tensor(a, device=DEV), b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = G.oracle_ffn(layer, h, ids, a, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "vq expert_ffn")
+
+
+def test_vq_block_every_m_1_to_16():
+    """The blockwise-VQ workload: parity at every M from 1 to 16 (one weight set)."""
+    wl = syn.WORKLOADS["vq_d4"]
+    layer = _workload_layer("vq_d4")
+    for M in range(1, 17):
+        h = syn.make_hidden(wl, M=M, seed=M, device=DEV)
+        ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
+        out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+        assert moe.moe_read_device_status(ws) == 0
+        o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+        use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
+                                              logits, wl.k)
+        ref = G.oracle_ffn(layer, h, use_ids, use_wts)
+        G.assert_close_block(G.to_f64(out), ref, "vq_d4 M=%d" % M)
+    # bitwise determinism and batch invariance of the VQ path
+    out2, _, _ = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+    assert torch.equal(out2, out)
+    o1, _, _ = moe.moe_decode_block(h[3:4].contiguous(), layer, wl.k, wl.b)
+    assert torch.equal(o1[0], out[3])
+
+
 def test_large_m256_sampled_tokens():
     _check_block("large_m256", tokens=np.array([0, 1, 77, 128, 200, 254, 255]))
 
