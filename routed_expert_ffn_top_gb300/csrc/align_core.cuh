@@ -1,0 +1,144 @@
+// align_core.cuh -- the stable alignment as a device function for one 256-thread CTA, shared
+// by the stand-alone alignment kernel and the router (which runs it when one cluster holds
+// every token).
+//
+// "Route-Block Membership Selects Packed-AWQ Arithmetic", Section 2.1: route r = m*k + j;
+// valid routes grouped by expert, each expert padded to a multiple of b, and a parallel
+// expert-per-block vector.  Section 5.3: valid routes ordered by (expert id, route id).
+//
+// (1) per-expert counts in shared memory (integer atomics commute, so the counts do not
+// depend on arrival order); (2) one warp scans the padded counts into row offsets; (3) the
+// routes are scattered chunk by chunk in ascending r: inside a warp __match_any_sync groups
+// the lanes of one expert and a popcount of the lower lanes ranks them, a per-warp count
+// table ranks the warps of a chunk, and per-expert running totals carry ranks across chunks;
+// (4) padding rows, the block vector, the tail, and the sub-block records (expert, routes in
+// row order, their tokens) that the expert kernels read one per tile.  Every position is a
+// pure function of the input ids.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr int kAlignThreads = 256;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+// Shared-memory ints align_core needs for E experts.
+__host__ __device__ constexpr int align_smem_ints(int E) { return (3 + kAlignWarps) * E + 4; }
+
+// ids: M*k expert ids (global or shared memory); outputs may be NULL except npad.
+// Requires blockDim.x == kAlignThreads and every thread of the CTA to call it.
+__device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, int b, int rsub,
+                                  int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
+                                  SubBlock *sbt, int32_t *status, int32_t *sm) {
+    int32_t *cnt = sm;                          // [E]
+    int32_t *off = cnt + E;                     // [E] padded row offsets
+    int32_t *running = off + E;                 // [E]
+    int32_t *warp_cnt = running + E;            // [kAlignWarps][E]
+    int32_t *misc = warp_cnt + kAlignWarps * E;  // [0] total, [1] invalid flag
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t sentinel = (int32_t)R;
+
+    for (int i = tid; i < (3 + kAlignWarps) * E; i += kAlignThreads) sm[i] = 0;
+    if (tid == 0) misc[1] = 0;
+    __syncthreads();
+
+    // (1) counts
+    int local_invalid = 0;
+    for (int64_t r = tid; r < R; r += kAlignThreads) {
+        const int e = ids[r];
+        if (e >= 0 && e < E)
+            atomicAdd(&cnt[e], 1);
+        else
+            local_invalid = 1;
+    }
+    if (local_invalid) atomicOr(&misc[1], 1);
+    __syncthreads();
+
+    // (2) exclusive scan of padded counts (warp 0; lane owns a contiguous run of experts)
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per, e1 = min(E, e0 + per);
+        int s = 0;
+        for (int e = e0; e < e1; ++e) s += (cnt[e] + b - 1) / b * b;
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - s;
+        for (int e = e0; e < e1; ++e) {
+            off[e] = run;
+            run += (cnt[e] + b - 1) / b * b;
+        }
+        if (lane == 31) misc[0] = incl;
+    }
+    __syncthreads();
+    const int total = misc[0];
+
+    // (3) stable scatter in ascending route id
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t base = 0; base < R; base += kAlignThreads) {
+        const int64_t r = base + tid;
+        const int e = (r < R) ? ids[r] : -1;
+        const bool valid = (e >= 0 && e < E);
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int lower = __popc(peers & lt_mask);
+        const int wcount = __popc(peers);
+        const bool leader = lower == 0;
+        if (valid && leader) warp_cnt[warp * E + e] = wcount;
+        __syncthreads();
+        if (valid) {
+            int rank = running[e] + lower;
+            for (int w = 0; w < warp; ++w) rank += warp_cnt[w * E + e];
+            const int64_t pos = (int64_t)off[e] + rank;
+            if (pos < cap) {
+                if (sorted) sorted[pos] = (int32_t)r;
+                if (sbt) {
+                    SubBlock *rec = sbt + pos / rsub;
+                    rec->routes[pos % rsub] = (int32_t)r;
+                    rec->tokens[pos % rsub] = (int32_t)(r / k);
+                }
+            }
+        }
+        __syncthreads();
+        if (valid && leader) {
+            // several warps may hold routes of expert e: integer adds commute
+            atomicAdd(&running[e], wcount);
+            warp_cnt[warp * E + e] = 0;
+        }
+        __syncthreads();
+    }
+
+    // (4) padding rows, block vector, sub-block records, tail
+    for (int e = tid; e < E; e += kAlignThreads) {
+        const int n = cnt[e];
+        if (n == 0) continue;
+        const int padded = (n + b - 1) / b * b;
+        if (sorted)
+            for (int q = n; q < padded; ++q)
+                if (off[e] + q < cap) sorted[off[e] + q] = sentinel;
+        if (blocks)
+            for (int q = 0; q < padded / b; ++q) blocks[off[e] / b + q] = e;
+        if (sbt)
+            for (int s = off[e] / rsub; s < (off[e] + padded) / rsub; ++s) {
+                const int first = s * rsub - off[e];
+                const int ntok = max(0, min(rsub, n - first));
+                SubBlock *rec = sbt + s;
+                rec->e = e;
+                rec->ntok = ntok;
+                for (int q = ntok; q < kNT; ++q) rec->routes[q] = rec->tokens[q] = -1;
+            }
+    }
+    if (sorted)
+        for (int64_t pos = (int64_t)total + tid; pos < cap; pos += kAlignThreads) sorted[pos] = sentinel;
+    if (blocks)
+        for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += kAlignThreads) blocks[q] = -1;
+    if (tid == 0) {
+        npad[0] = total;
+        if (status && misc[1]) atomicOr(status, MOE_DEV_INVALID_EXPERT);
+    }
+}
+
+}  // namespace moe

@@ -376,18 +376,29 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     trace(0, s);
-    cudaError_t err = launch_router(static_cast<const __nv_bfloat16 *>(h),
-                                    static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H,
-                                    w->E, k, 1, topk_ids, topk_weights, s);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
-    trace(1, s);
     int32_t *ws_sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
     int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
     int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
-    err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
-                       reinterpret_cast<SubBlock *>(ws + L.sbt), d.rsub,
-                       reinterpret_cast<int32_t *>(ws + L.status), s);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    SubBlock *ws_sbt = reinterpret_cast<SubBlock *>(ws + L.sbt);
+    int32_t *ws_status = reinterpret_cast<int32_t *>(ws + L.status);
+    cudaError_t err;
+    if (router_can_align(M, k)) {  // one launch routes and aligns
+        err = launch_router_align(static_cast<const __nv_bfloat16 *>(h),
+                                  static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H, w->E,
+                                  k, 1, topk_ids, topk_weights, b, d.rsub, ws_sorted, ws_blocks,
+                                  ws_npad, d.cap, ws_sbt, ws_status, s);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        trace(1, s);
+    } else {
+        err = launch_router(static_cast<const __nv_bfloat16 *>(h),
+                            static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H, w->E, k, 1,
+                            topk_ids, topk_weights, s);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        trace(1, s);
+        err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap, ws_sbt,
+                           d.rsub, ws_status, s);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+    }
     trace(2, s);
     return run_experts(h, w, d, topk_ids, topk_weights, ws_npad, residual, out, ws, L, s);
 }

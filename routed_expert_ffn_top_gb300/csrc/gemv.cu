@@ -642,16 +642,30 @@ __global__ void __launch_bounds__(kCombineThreads)
     const int n = (blockIdx.x * kCombineThreads + threadIdx.x) * 4;
     if (m >= M || n >= H) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-        const int64_t r = (int64_t)m * k + j;
-        const int e = topk_ids[r];
-        if (e < 0 || e >= E) continue;
-        const float aw = topk_wts[r];
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(y + r * H + n));
-        acc.x = fmaf(aw, v.x, acc.x);
-        acc.y = fmaf(aw, v.y, acc.y);
-        acc.z = fmaf(aw, v.z, acc.z);
-        acc.w = fmaf(aw, v.w, acc.w);
+    // 8 slots at a time: ids, affinities and y rows are all loaded before any is used (every
+    // route has a y row in the workspace; the rows of invalid routes are simply not added)
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        int e[8];
+        float aw[8];
+        float4 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int64_t r = (int64_t)m * k + j0 + jj;
+            if (j0 + jj < k) {
+                e[jj] = topk_ids[r];
+                aw[jj] = topk_wts[r];
+                v[jj] = __ldcg(reinterpret_cast<const float4 *>(y + r * H + n));
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            if (j0 + jj < k && e[jj] >= 0 && e[jj] < E) {
+                acc.x = fmaf(aw[jj], v[jj].x, acc.x);
+                acc.y = fmaf(aw[jj], v[jj].y, acc.y);
+                acc.z = fmaf(aw[jj], v[jj].z, acc.z);
+                acc.w = fmaf(aw[jj], v[jj].w, acc.w);
+            }
+        }
     }
     const size_t o = (size_t)m * H + n;
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);

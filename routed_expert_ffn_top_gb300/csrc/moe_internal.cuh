@@ -119,6 +119,15 @@ cudaError_t launch_router(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                           const float *bias, int M, int H, int E, int k, int renormalize,
                           int32_t *topk_ids, float *topk_weights, cudaStream_t stream);
 
+// Router that also aligns the routes (and writes the sub-block table) in the same launch;
+// possible when one router cluster holds every token.
+bool router_can_align(int M, int k);
+cudaError_t launch_router_align(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
+                                const float *bias, int M, int H, int E, int k, int renormalize,
+                                int32_t *topk_ids, float *topk_weights, int b, int rsub,
+                                int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
+                                SubBlock *sbt, int32_t *status, cudaStream_t stream);
+
 // Alignment; when `sbt` is not NULL it also writes the sub-block table of rsub-row blocks.
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b,
                          int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
