@@ -45,9 +45,12 @@ WsLayout ws_layout(const Dims &d) {
     L.sbt = take((size_t)d.max_sub * sizeof(SubBlock));
     L.p = take((size_t)d.R * d.I * 4);
     L.y = take((size_t)d.R * d.H * 4);
+    L.p_rows = take((d.b == kGemmBlock) ? (size_t)d.cap * d.I * 2 : 0);
     L.total = off;
     return L;
 }
+
+bool gemm_regime(int kind, int b) { return kind == MOE_W_DENSE_BF16 && b == kGemmBlock; }
 
 int num_sms() {
     static int cache[64] = {0};
@@ -102,7 +105,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D row-major tensor [outer][inner] of `elem` bytes, box [box_outer][box_inner].
 static bool make_tmap_2d(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int elem,
-                         uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+                         uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -110,8 +114,8 @@ static bool make_tmap_2d(CUtensorMap *tm, const void *base, CUtensorMapDataType 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     return fn(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace moe
@@ -244,10 +248,69 @@ extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int 
 }
 
 // Runs gate/up and down for aligned routes (alignment pointers already resolved).
+// The large-batch regime: tcgen05 grouped GEMMs over the 64-row aligned blocks, then the
+// fixed-order combine.
+static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
+                    const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
+                    const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
+                    unsigned char *ws, const WsLayout &L, cudaStream_t stream) {
+    CUtensorMap tm_gate, tm_up, tm_down;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                      (uint64_t)d.E * d.H, 64, 128, sw) ||
+        !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                      (uint64_t)d.E * d.H, 64, 128, sw) ||
+        !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
+                      (uint64_t)d.E * d.I, 64, 128, sw))
+        return MOE_ERR_CUDA;
+    GemmArgs g;
+    g.x = static_cast<const __nv_bfloat16 *>(h);
+    g.ids = topk_ids;
+    g.sorted = sorted;
+    g.blocks = blocks;
+    g.npad = npad;
+    g.p_rows = reinterpret_cast<__nv_bfloat16 *>(ws + L.p_rows);
+    g.y = reinterpret_cast<float *>(ws + L.y);
+    g.status = reinterpret_cast<int32_t *>(ws + L.status);
+    g.M = d.M;
+    g.k = d.k;
+    g.E = d.E;
+    g.H = d.H;
+    g.I = d.I;
+    g.R = d.R;
+    g.cap = d.cap;
+    cudaError_t err = launch_gemm_gateup(tm_gate, tm_up, g, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(3, stream);
+    GemmArgs gd = g;
+    gd.x = g.p_rows;
+    err = launch_gemm_down(tm_down, gd, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(4, stream);
+    GemvArgs c;
+    memset(&c, 0, sizeof c);
+    c.topk_ids = topk_ids;
+    c.topk_wts = topk_weights;
+    c.residual = static_cast<const __nv_bfloat16 *>(residual);
+    c.out = static_cast<__nv_bfloat16 *>(out);
+    c.y = g.y;
+    c.M = d.M;
+    c.k = d.k;
+    c.E = d.E;
+    c.H = d.H;
+    err = launch_combine(c, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace(5, stream);
+    return MOE_OK;
+}
+
 static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims &d,
-                       const int32_t *topk_ids, const float *topk_weights, const int32_t *npad,
-                       const void *residual, void *out, unsigned char *ws, const WsLayout &L,
-                       cudaStream_t stream) {
+                       const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
+                       const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
+                       unsigned char *ws, const WsLayout &L, cudaStream_t stream) {
+    if (gemm_regime(w->kind, d.b))
+        return run_gemm(h, w, d, topk_ids, topk_weights, sorted, blocks, npad, residual, out, ws,
+                        L, stream);
     const bool vq = w->kind == MOE_W_VQ_GATEUP;
     CUtensorMap tm_gate, tm_up, tm_down;
     bool ok;
@@ -351,12 +414,16 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     } else {
         if (!aligned(sorted_route_ids, 4) || !aligned(expert_block_ids, 4) || !aligned(num_padded, 4))
             return MOE_ERR_INVALID_ARG;
-        err = launch_plan(topk_ids, sorted_route_ids, expert_block_ids, num_padded, M, k, w->E, b,
-                          d.rsub, d.max_sub, sbt, status, s);
+        err = gemm_regime(w->kind, b)
+                  ? cudaSuccess
+                  : launch_plan(topk_ids, sorted_route_ids, expert_block_ids, num_padded, M, k,
+                                w->E, b, d.rsub, d.max_sub, sbt, status, s);
     }
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(2, s);
-    return run_experts(h, w, d, topk_ids, topk_weights, npad, residual, out, ws, L, s);
+    const int32_t *srt = given ? sorted_route_ids : reinterpret_cast<const int32_t *>(ws + L.sorted);
+    const int32_t *blk = given ? expert_block_ids : reinterpret_cast<const int32_t *>(ws + L.blocks);
+    return run_experts(h, w, d, topk_ids, topk_weights, srt, blk, npad, residual, out, ws, L, s);
 }
 
 extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,
@@ -400,7 +467,8 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
         if (err != cudaSuccess) return MOE_ERR_CUDA;
     }
     trace(2, s);
-    return run_experts(h, w, d, topk_ids, topk_weights, ws_npad, residual, out, ws, L, s);
+    return run_experts(h, w, d, topk_ids, topk_weights, ws_sorted, ws_blocks, ws_npad, residual, out,
+                       ws, L, s);
 }
 
 extern "C" int moe_decode_block_host(const void *h_host, const void *residual_host,

@@ -49,10 +49,12 @@ struct WsLayout {
     size_t sbt;      // SubBlock[max_sub]
     size_t p;        // float[R * I]   SiLU(g) * u per route
     size_t y;        // float[R * H]   down-projection output per route
+    size_t p_rows;   // bf16[cap * I]  large-batch regime: p per aligned row
     size_t total;
 };
 
 Dims make_dims(int M, int k, int E, int H, int I, int b);
+bool gemm_regime(int kind, int b);
 WsLayout ws_layout(const Dims &d);
 
 struct GemvArgs {
@@ -73,6 +75,26 @@ struct GemvArgs {
     int n_qb;              // VQ: index-map boxes of 256 rows (1024 rows of H) per projection
     int64_t max_sub;       // rows of the sub-block table
 };
+
+// Large-batch regime (aligned blocks of 64 rows, dense weights): grouped GEMMs on tcgen05.
+constexpr int kGemmBlock = 64;
+
+struct GemmArgs {
+    const __nv_bfloat16 *x;   // B rows: gate/up reads h [M,H]; down reads p_rows [cap,I]
+    const int32_t *ids;       // topk_ids [M*k]: a row whose route disagrees is skipped
+    const int32_t *sorted;    // aligned rows (route ids, sentinel = M*k)
+    const int32_t *blocks;    // expert of each 64-row block
+    const int32_t *npad;
+    __nv_bfloat16 *p_rows;    // gate/up output: SiLU(g) * u per aligned row, bf16 [cap, I]
+    float *y;                 // down output per route [M*k, H]
+    int32_t *status;
+    int M, k, E, H, I;
+    int64_t R, cap;
+};
+
+cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                               const GemmArgs &a, cudaStream_t stream);
+cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
 
 // Sub-blocks to process: num_padded / rsub, never more than the table holds.
 __device__ __forceinline__ int64_t num_subblocks(const GemvArgs &a) {

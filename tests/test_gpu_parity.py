@@ -107,6 +107,10 @@ SMALL = [
     (1, 1, 8, 256, 256, 1), (5, 2, 8, 512, 256, 3), (13, 8, 16, 768, 512, 8),
     (3, 4, 32, 256, 768, 16), (37, 6, 64, 256, 256, 64), (64, 8, 128, 512, 256, 8),
     (2, 8, 8, 1024, 1280, 2), (9, 3, 40, 1280, 256, 5),
+    # b = 64 with dense weights: the tcgen05 grouped-GEMM regime (several blocks per expert,
+    # ragged last blocks, single-route blocks, K and channel counts over several tiles)
+    (1, 1, 8, 256, 256, 64), (300, 2, 8, 512, 768, 64), (64, 8, 16, 1024, 512, 64),
+    (129, 4, 8, 256, 1536, 64), (300, 8, 128, 768, 256, 64),
 ]
 
 
@@ -156,8 +160,9 @@ def test_expert_ffn_invalid_ids_and_status():
     assert torch.equal(out[2], res[2])
 
 
-def test_expert_ffn_bad_alignment_is_flagged():
-    M, k, E, H, I, b = 4, 2, 8, 256, 256, 2
+@pytest.mark.parametrize("b", [2, 64])
+def test_expert_ffn_bad_alignment_is_flagged(b):
+    M, k, E, H, I = 4, 2, 8, 256, 256
     wl, layer, h = _small_layer(M, k, E, H, I, b, seed=4)
     ids = np.array([[0, 1], [1, 2], [2, 3], [3, 0]], np.int32)
     t_ids = torch.as_tensor(ids, device=DEV)
@@ -165,7 +170,7 @@ def test_expert_ffn_bad_alignment_is_flagged():
     srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
     srt_bad = srt.clone()
     s = srt_bad.cpu().numpy()
-    s[0], s[2] = s[2], s[0]  # move a route of expert 1 into expert 0's block
+    s[0], s[b] = s[b], s[0]  # move a route of expert 1 into expert 0's block
     srt_bad.copy_(torch.as_tensor(s))
     ws = moe.alloc_workspace(layer, M, k, b)
     moe.moe_expert_ffn(h, layer, t_ids, a, b, alignment=(srt_bad, blk, npad), workspace=ws)
@@ -330,7 +335,31 @@ def test_vq_block_every_m_1_to_16():
 
 
 def test_large_m256_sampled_tokens():
-    _check_block("large_m256", tokens=np.array([0, 1, 77, 128, 200, 254, 255]))
+    layer, h, ws, out, ids, wts = _check_block("large_m256",
+                                               tokens=np.array([0, 1, 77, 128, 200, 254, 255]))
+    wl = syn.WORKLOADS["large_m256"]
+    out2, _, _ = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+    assert torch.equal(out, out2)
+
+
+def test_gemm_regime_batch_and_membership_invariance():
+    """In the grouped-GEMM regime a route is one column of its block's MMA: its bits do not
+    depend on the other routes of the block, on the block's position or on M."""
+    M, k, E, H, I, b = 96, 4, 8, 512, 512, 64
+    wl, layer, h = _small_layer(M, k, E, H, I, b, seed=3)
+    rng = np.random.default_rng(11)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    t_ids = torch.as_tensor(ids, device=DEV)
+    t_a = torch.as_tensor(a, device=DEV)
+    out = moe.moe_expert_ffn(h, layer, t_ids, t_a, b)
+    for sub in ([5], [0, 95], list(range(40, 71)), list(range(95, -1, -3))):
+        sel = torch.as_tensor(sub, device=DEV)
+        o = moe.moe_expert_ffn(h[sel].contiguous(), layer, t_ids[sel].contiguous(),
+                               t_a[sel].contiguous(), b)
+        assert torch.equal(o, out[sel]), sub
+    ref = G.oracle_ffn(layer, h, ids, a)
+    G.assert_close_block(G.to_f64(out), ref, "gemm regime")
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
