@@ -45,7 +45,9 @@ WsLayout ws_layout(const Dims &d) {
     L.sbt = take((size_t)d.max_sub * sizeof(SubBlock));
     L.p = take((size_t)d.R * d.I * 4);
     L.y = take((size_t)d.R * d.H * 4);
-    L.p_rows = take((d.b == kGemmBlock) ? (size_t)d.cap * d.I * 2 : 0);
+    const size_t tile_rows = (d.b == kGemmBlock) ? (size_t)(d.cap / kGemmBlock) * kGemmBlock : 0;
+    L.x_tiles = take(tile_rows * d.H * 2);
+    L.p_tiles = take(tile_rows * d.I * 2);
     L.total = off;
     return L;
 }
@@ -257,11 +259,11 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     CUtensorMap tm_gate, tm_up, tm_down;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
     if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, 64, 128, sw) ||
+                      (uint64_t)d.E * d.H, 64, 256, sw) ||
         !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, 64, 128, sw) ||
+                      (uint64_t)d.E * d.H, 64, 256, sw) ||
         !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
-                      (uint64_t)d.E * d.I, 64, 128, sw))
+                      (uint64_t)d.E * d.I, 64, 256, sw))
         return MOE_ERR_CUDA;
     GemmArgs g;
     g.x = static_cast<const __nv_bfloat16 *>(h);
@@ -269,7 +271,8 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     g.sorted = sorted;
     g.blocks = blocks;
     g.npad = npad;
-    g.p_rows = reinterpret_cast<__nv_bfloat16 *>(ws + L.p_rows);
+    g.x_tiles = reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles);
+    g.p_tiles = reinterpret_cast<__nv_bfloat16 *>(ws + L.p_tiles);
     g.y = reinterpret_cast<float *>(ws + L.y);
     g.status = reinterpret_cast<int32_t *>(ws + L.status);
     g.M = d.M;
@@ -279,12 +282,12 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     g.I = d.I;
     g.R = d.R;
     g.cap = d.cap;
-    cudaError_t err = launch_gemm_gateup(tm_gate, tm_up, g, stream);
+    cudaError_t err = launch_gather_rows(g, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    err = launch_gemm_gateup(tm_gate, tm_up, g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
-    GemmArgs gd = g;
-    gd.x = g.p_rows;
-    err = launch_gemm_down(tm_down, gd, stream);
+    err = launch_gemm_down(tm_down, g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(4, stream);
     GemvArgs c;

@@ -12,16 +12,26 @@
 //   gate/up:  D[128][64] = [W_gate[e][:, i0:i0+64] | W_up[e][:, i0:i0+64]]^T  x  X^T
 //             (lanes 0-63 accumulate g, lanes 64-127 accumulate u, of channels i0..i0+63)
 //   down:     D[128][64] = W_down[e][:, h0:h0+128]^T  x  P^T
-// A comes straight from the [E,H,I] / [E,I,H] weights: TMA boxes of 64 columns x 128 rows
-// with 128-byte swizzle form the MN-major canonical layout (one 64-wide M half per box).
-// B (the block's token rows of h, or of p) is gathered by a loader warp with 16-byte
-// cp.async copies into the K-major 128-byte-swizzle layout; sentinel rows become zeros.
-// Per CTA: warp 0 issues the weight TMA, warp 1 loads B, one thread of warp 2 issues the
-// MMAs (K = 16 each) into one of two tensor-memory accumulators, and warps 4-7 drain the
-// finished accumulator: gate/up computes p = SiLU(g) * u and writes it as bf16 rows for the
-// down GEMM; down writes y per route for the fixed-order combine.  Persistent CTAs take
-// units (block, channel tile) round-robin, channel tile fastest, so the units of one block
-// and of neighbouring blocks of the same expert run side by side and share weight reads.
+// A comes straight from the [E,H,I] / [E,I,H] weights: TMA boxes of 64 columns x 256 rows
+// (32 KB) with 128-byte swizzle form the MN-major canonical layout, one 64-wide M half per
+// box.  One SM's TMA unit keeps only a few copies in flight, so copies are made as large
+// as the swizzled layout allows.
+//
+// B is read from "tiled" row buffers: for every aligned block, K is cut into 64-wide
+// chunks and each chunk is stored as the 8 KB K-major 128-byte-swizzle image of its 64
+// rows (row n at n*128 bytes, 16-byte piece j at (j ^ n%8)*16).  A stage of 256 K is then
+// one contiguous 32 KB bulk copy that lands in shared memory already in the MMA layout.
+//   x tiles: the token rows of h, gathered per aligned row by gather_rows_kernel;
+//   p tiles: p = SiLU(g) * u in bf16, written by the gate/up epilogue, read by down.
+// Rows of padding are never written: their columns of D are independent of the others
+// and are dropped by the epilogues, so whatever the memory holds there cannot reach a
+// result.
+//
+// Per CTA (6 warps): warp 0 issues the copies, one thread of warp 1 issues the MMAs
+// (K = 16 each) into one of two tensor-memory accumulators, and warps 2-5 drain the
+// finished accumulator (a warp reads the TMEM lanes of its rank modulo 4).  Persistent CTAs
+// take units (block, channel tile) round-robin, channel tile fastest, so the units of one
+// block run side by side and share its row tiles in L2.
 //
 // Each output element is one K-ordered chain of MMAs into its accumulator, independent of
 // the other columns of the block, of the grid and of M: the results are bitwise
@@ -31,17 +41,18 @@
 
 namespace moe {
 
-constexpr int kGN = 64;                              // routes per MMA (one aligned block)
+constexpr int kGN = kGemmBlock;                      // routes per MMA (one aligned block)
 constexpr int kGM = 128;                             // output channels per MMA
-constexpr int kGK = 128;                             // K per stage
-constexpr int kGStages = 4;
-constexpr int kGHalfBytes = 64 * kGK * 2;            // one 64-wide M half: 16 KB
-constexpr int kGABytes = 2 * kGHalfBytes;            // 32 KB
-constexpr int kGBBytes = kGN * kGK * 2;              // 16 KB
-constexpr int kGStageBytes = kGABytes + kGBBytes;    // 48 KB
-constexpr int kGThreads = 256;                       // 8 warps
+constexpr int kGK = 256;                             // K per stage
+constexpr int kGStages = 2;
+constexpr int kGHalfBytes = 64 * kGK * 2;            // one 64-wide M half: 32 KB
+constexpr int kGABytes = 2 * kGHalfBytes;            // 64 KB
+constexpr int kGBBytes = kGN * kGK * 2;              // 32 KB
+constexpr int kGStageBytes = kGABytes + kGBBytes;    // 96 KB
+constexpr int kGChunkBytes = kGN * 64 * 2;           // one 64-wide K chunk of a block: 8 KB
+constexpr int kGThreads = 192;                       // 6 warps
+constexpr int kGEpiWarp0 = 2;
 constexpr uint32_t kGTmemCols = 2 * kGN;             // two 128 x 64 fp32 accumulators
-constexpr int kGEpiWarp0 = 4;
 
 struct GCtl {
     uint64_t full[kGStages];
@@ -51,8 +62,7 @@ struct GCtl {
     uint64_t done;
     uint32_t tmem;
     volatile int abort;
-    int rows[kGN];        // loader: source row of each block row (-1: zeros)
-    int route[2][kGN];    // epilogue: route of each block row, per accumulator
+    int route[2][kGN];    // down epilogue: route of each block row, per accumulator
 };
 
 __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, GCtl &ctl) {
@@ -80,7 +90,7 @@ __device__ __forceinline__ void gadvance(int &stage, uint32_t &phase) {
 __device__ __forceinline__ int gemm_route(const GemmArgs &a, int64_t pos, int e, bool flag) {
     const int r = a.sorted[pos];
     if (r < 0 || r >= a.R) return -1;
-    if (a.ids[r] != e) {
+    if (e < 0 || e >= a.E || a.ids[r] != e) {
         if (flag) atomicOr(a.status, MOE_DEV_BAD_ALIGNMENT);
         return -1;
     }
@@ -93,92 +103,100 @@ __device__ __forceinline__ int64_t gemm_blocks(const GemmArgs &a) {
     return n < 0 ? 0 : (n > cap_blocks ? cap_blocks : n);
 }
 
-// Weight boxes of one unit: `issue(stage_smem, bar, e, ct, s)` copies the A tile of K-step s.
-template <typename IssueFn>
-__device__ void gemm_producer(const GemmArgs &a, GCtl &ctl, unsigned char *stages, int64_t T,
-                              int n_ct, int nks, IssueFn issue) {
+// Byte offset of (row n, 16-byte piece j) inside a block's 8 KB K chunk.
+__device__ __forceinline__ uint32_t tile_offset(int n, int j) {
+    return (uint32_t)(n * 128 + ((j ^ (n & 7)) << 4));
+}
+
+// ------------------------------------------------------------------------ row gather
+// x tiles of every valid aligned row: one warp per row, 8 lanes per 64-wide K chunk.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const GemmArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nrows = gemm_blocks(a) * kGN;
+    const int nchunk = a.H / 64;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t pos = warp0; pos < nrows; pos += nwarps) {
+        const int64_t blk = pos / kGN;
+        const int n = (int)(pos % kGN);
+        const int r = gemm_route(a, pos, a.blocks[blk], lane == 0);
+        if (r < 0) continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)(r / a.k) * a.H);
+        unsigned char *dst = reinterpret_cast<unsigned char *>(a.x_tiles) +
+                             blk * (int64_t)nchunk * kGChunkBytes;
+        const int j = lane & 7;
+        const uint32_t off = tile_offset(n, j);
+        for (int c = lane >> 3; c < nchunk; c += 4)
+            *reinterpret_cast<uint4 *>(dst + (int64_t)c * kGChunkBytes + off) = src[c * 8 + j];
+    }
+}
+
+// ------------------------------------------------------------------- pipeline roles
+// Copies of one unit: per stage the two 32 KB weight boxes (issue_a) and the 32 KB row
+// tile of the block (btiles + (blk * nks + s) * 32 KB).  The weights depend only on the
+// alignment, which was complete before this grid started; the row tiles are written by
+// the previous grid, so the first stages' tile copies wait for it (griddepcontrol) while
+// their weight copies are already in flight.
+template <typename IssueA>
+__device__ void gemm_producer(const GemmArgs &a, GCtl &ctl, unsigned char *stages,
+                              const unsigned char *btiles, int64_t T, int n_ct, int nks,
+                              IssueA issue_a) {
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, parity_bits = 0;
+    bool waited = false;
+    int npend = 0;
+    const unsigned char *pend_src[kGStages];
+    int pend_stage[kGStages];
     for (int64_t u = blockIdx.x; u < T && !ctl.abort; u += gridDim.x) {
         const int64_t blk = u / n_ct;
         const int ct = (int)(u % n_ct);
         int e = a.blocks[blk];
         if (e < 0 || e >= a.E) {
             atomicOr(a.status, MOE_DEV_BAD_ALIGNMENT);
-            e = 0;  // keep the pipeline in step; the rows of such a block are all padding
+            e = 0;  // keep the pipeline in step; every row of such a block is dropped
         }
         for (int s = 0; s < nks; ++s) {
             if (!gwait(&ctl.empty[stage], phase ^ 1u, ctl)) break;
             uint64_t *bar = &ctl.full[stage];
-            mbar_arrive_expect_tx(bar, kGABytes);
-            issue(stages + stage * kGStageBytes, bar, e, ct, s);
+            unsigned char *st = stages + stage * kGStageBytes;
+            mbar_arrive_expect_tx(bar, kGStageBytes);
+            issue_a(st, bar, e, ct, s);
+            const unsigned char *src = btiles + (blk * nks + s) * (int64_t)kGBBytes;
+            if (waited) {
+                bulk_load(st + kGABytes, src, kGBBytes, bar);
+            } else {
+                pend_src[npend] = src;
+                pend_stage[npend] = stage;
+                if (++npend == kGStages) {
+                    pdl_wait();
+                    waited = true;
+                    for (int q = 0; q < npend; ++q)
+                        bulk_load(stages + pend_stage[q] * kGStageBytes + kGABytes, pend_src[q],
+                                  kGBBytes, &ctl.full[pend_stage[q]]);
+                    npend = 0;
+                }
+            }
             issued |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
             gadvance(stage, phase);
         }
     }
+    if (!waited) {
+        pdl_wait();
+        for (int q = 0; q < npend; ++q)
+            bulk_load(stages + pend_stage[q] * kGStageBytes + kGABytes, pend_src[q], kGBBytes,
+                      &ctl.full[pend_stage[q]]);
+    }
+    // every copy has landed before the CTA can exit
     for (int s = 0; s < kGStages; ++s)
         if ((issued >> s) & 1u)
             if (!mbar_wait_bounded(&ctl.full[s], (parity_bits >> s) & 1u)) ctl.abort = 1;
 }
 
-// B tiles: the 64 rows of the unit's block, K-step s, into the K-major swizzled layout
-// (element (n, k): 8 KB per 64-wide K half, 1 KB per 8 rows, 16-byte chunk c of row n at
-// position c ^ (n % 8)).  Row n comes from src + rows[n] * ld, or is zero when rows[n] < 0.
-template <bool kDownB>
-__device__ void gemm_loader(const GemmArgs &a, GCtl &ctl, unsigned char *stages, int64_t T,
-                            int n_ct, int nks) {
-    const int lane = threadIdx.x & 31;
-    const __nv_bfloat16 *src = a.x;
-    const int64_t ld = kDownB ? a.I : a.H;
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int64_t u = blockIdx.x; u < T && !ctl.abort; u += gridDim.x) {
-        const int64_t blk = u / n_ct;
-        const int e = a.blocks[blk];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int n = lane + 32 * h;
-            int row;
-            if (kDownB) {
-                row = (int)(blk * kGN + n);  // p rows are stored in aligned-row order
-            } else {
-                const int r = gemm_route(a, blk * kGN + n, e, u % n_ct == 0);
-                row = r >= 0 ? r / a.k : -1;
-            }
-            ctl.rows[n] = row;
-        }
-        __syncwarp();
-        for (int s = 0; s < nks; ++s) {
-            bool ok = true;
-            if (lane == 0) ok = gwait(&ctl.empty[stage], phase ^ 1u, ctl);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                cp_async_wait_all();
-                return;
-            }
-            unsigned char *B = stages + stage * kGStageBytes + kGABytes;
-#pragma unroll 4
-            for (int j = 0; j < (kGN * kGK * 2 / 16) / 32; ++j) {
-                const int id = j * 32 + lane;
-                const int n = id >> 4, c = id & 15;
-                const int row = ctl.rows[n];
-                const __nv_bfloat16 *g = src + (int64_t)(row >= 0 ? row : 0) * ld + s * kGK + c * 8;
-                unsigned char *dst = B + (c >> 3) * 8192 + (n >> 3) * 1024 + (n & 7) * 128 +
-                                     (((c & 7) ^ (n & 7)) << 4);
-                cp_async_16_zfill(dst, g, row >= 0 ? 16u : 0u);
-            }
-            cp_async_mbar_arrive(&ctl.full[stage]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.full[stage]);
-            gadvance(stage, phase);
-        }
-        __syncwarp();
-    }
-    cp_async_wait_all();
-}
-
-// MMA issuer (one thread): for each unit, nks stages x 8 MMAs of K = 16 into accumulator
+// MMA issuer (one thread): for each unit, nks stages x 16 MMAs of K = 16 into accumulator
 // buffer (unit parity); each stage is released when its MMAs complete.
 __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
     constexpr uint32_t idesc = umma_idesc_bf16(kGM, kGN, true, false);
@@ -198,15 +216,15 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
                 break;
             }
             tc_fence_after();
-            fence_proxy_async_smem();  // the B rows arrived through cp.async (generic proxy)
             const uint32_t A = smem_u32(stages + stage * kGStageBytes);
             const uint32_t B = A + kGABytes;
 #pragma unroll
             for (int ks = 0; ks < kGK / 16; ++ks) {
-                // A: MN-major, M halves 16 KB apart, 8-row K atoms 1 KB apart, 16 K rows per MMA
+                // A: MN-major, M halves 32 KB apart, 8-row K atoms 1 KB apart, 16 K rows per MMA
                 const uint64_t ad = umma_smem_desc(A + ks * 2048, kGHalfBytes, 1024, 2);
-                // B: K-major, 64-wide K halves 8 KB apart, 32 bytes per K step, 8-row atoms 1 KB
-                const uint64_t bd = umma_smem_desc(B + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2);
+                // B: K-major, 64-wide K chunks 8 KB apart, 32 bytes per K step, 8-row atoms 1 KB
+                const uint64_t bd =
+                    umma_smem_desc(B + (ks >> 2) * kGChunkBytes + (ks & 3) * 32, 16, 1024, 2);
                 umma_bf16(d, ad, bd, idesc, s > 0 || ks > 0);
             }
             umma_commit(&ctl.empty[stage]);
@@ -223,7 +241,7 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
 __device__ __forceinline__ void gemm_init(GCtl &ctl, int warp) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGStages; ++s) {
-            mbar_init(&ctl.full[s], 2);  // weight TMA + B loader
+            mbar_init(&ctl.full[s], 1);   // the producer's expect_tx arrival
             mbar_init(&ctl.empty[s], 1);  // MMA completion
         }
         for (int b = 0; b < 2; ++b) {
@@ -234,7 +252,7 @@ __device__ __forceinline__ void gemm_init(GCtl &ctl, int warp) {
         ctl.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 2) tmem_alloc(&ctl.tmem, kGTmemCols);
+    if (warp == 1) tmem_alloc(&ctl.tmem, kGTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -244,8 +262,24 @@ __device__ __forceinline__ void gemm_finish(GCtl &ctl, int warp, int32_t *status
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 2) tmem_dealloc(ctl.tmem, kGTmemCols);
+    if (warp == 1) tmem_dealloc(ctl.tmem, kGTmemCols);
     if (threadIdx.x == 0 && ctl.abort) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+}
+
+// Epilogue warp: the 64 fp32 columns of its 32 TMEM lanes of accumulator `buf`, then the
+// accumulator is handed back to the MMA issuer.
+__device__ __forceinline__ void drain_accumulator(GCtl &ctl, int quad, int buf, float (&v)[kGN]) {
+    tc_fence_after();
+#pragma unroll
+    for (int c0 = 0; c0 < kGN; c0 += 16) {
+        float t16[16];
+        tmem_ld16(ctl.tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(buf * kGN + c0), t16);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[c0 + i] = t16[i];
+    }
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.tempty[buf]);
 }
 
 // ---------------------------------------------------------------------------- gate/up
@@ -257,14 +291,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
     float *gbuf = reinterpret_cast<float *>(base + kGStages * kGStageBytes);  // [64 rows][64 ch]
-    GCtl &ctl = *reinterpret_cast<GCtl *>(base + kGStages * kGStageBytes + 64 * 64 * 4);
+    unsigned char *pst = base + kGStages * kGStageBytes + kGN * 64 * 4;       // one p chunk
+    GCtl &ctl = *reinterpret_cast<GCtl *>(pst + kGChunkBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
     }
     gemm_init(ctl, warp);
-    pdl_wait();
     pdl_launch_dependents();
 
     const int n_ct = a.I / 64;
@@ -274,8 +308,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            gemm_producer(a, ctl, stages, T, n_ct, nks,
-                          [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
+            gemm_producer(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles), T,
+                          n_ct, nks, [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
                 const int32_t y = e * a.H + s * kGK;
                 tma_load_2d(st, &tm_gate, ct * 64, y, bar, pol);
                 tma_load_2d(st + kGHalfBytes, &tm_up, ct * 64, y, bar, pol);
@@ -283,46 +317,41 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        gemm_loader<false>(a, ctl, stages, T, n_ct, nks);
-    } else if (warp == 2) {
         if (lane == 0) gemm_mma(ctl, stages, T, nks);
         __syncwarp();
-    } else if (warp >= kGEpiWarp0) {
-        const int ew = warp - kGEpiWarp0;  // TMEM lanes [32 ew, 32 ew + 32)
-        const int row = 32 * ew + lane;    // accumulator row: gate channel (< 64) or up channel
+    } else {
+        const int quad = warp & 3;           // TMEM lanes [32 quad, 32 quad + 32)
+        const int row = 32 * quad + lane;    // accumulator row: gate channel (< 64) or up channel
+        const int tid = threadIdx.x - 32 * kGEpiWarp0;
         int local = 0;
         for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
             const int64_t blk = u / n_ct;
             const int ct = (int)(u % n_ct);
             const int buf = local & 1;
-            const uint32_t tph = (uint32_t)(local >> 1) & 1u;
-            const bool ok = gwait(&ctl.tfull[buf], tph, ctl);
-            if (named_bar_or(2, 128, !ok)) break;
-            tc_fence_after();
+            const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
+            if (named_bar_or(1, 128, !ok)) break;
             float v[kGN];
-#pragma unroll
-            for (int c0 = 0; c0 < kGN; c0 += 16) {
-                float t16[16];
-                tmem_ld16(ctl.tmem + ((uint32_t)(32 * ew) << 16) + (uint32_t)(buf * kGN + c0), t16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[c0 + i] = t16[i];
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.tempty[buf]);  // accumulator free for the next unit
-            if (ew < 2) {
+            drain_accumulator(ctl, quad, buf, v);
+            if (quad < 2) {
 #pragma unroll
                 for (int n = 0; n < kGN; ++n) gbuf[n * 64 + row] = v[n];
             }
-            named_bar_sync(2, 128);
-            if (ew >= 2) {
+            named_bar_sync(1, 128);
+            if (quad >= 2) {
                 const int ch = row - 64;
-                __nv_bfloat16 *dst = a.p_rows + (blk * kGN) * a.I + ct * 64 + ch;
 #pragma unroll
-                for (int n = 0; n < kGN; ++n)
-                    dst[(int64_t)n * a.I] = __float2bfloat16(silu_f32(gbuf[n * 64 + ch]) * v[n]);
+                for (int n = 0; n < kGN; ++n) {
+                    const float p = silu_f32(gbuf[n * 64 + ch]) * v[n];
+                    *reinterpret_cast<__nv_bfloat16 *>(pst + tile_offset(n, ch >> 3) + (ch & 7) * 2) =
+                        __float2bfloat16(p);
+                }
             }
-            named_bar_sync(2, 128);
+            named_bar_sync(1, 128);
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(a.p_tiles) +
+                                                   (blk * n_ct + ct) * (int64_t)kGChunkBytes);
+            const uint4 *srcv = reinterpret_cast<const uint4 *>(pst);
+#pragma unroll
+            for (int i = 0; i < kGChunkBytes / 16 / 128; ++i) dst[tid + 128 * i] = srcv[tid + 128 * i];
         }
     }
     gemm_finish(ctl, warp, a.status);
@@ -339,9 +368,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) prefetch_tensormap(&tm_down);
     gemm_init(ctl, warp);
-    // The weights of each unit are known from the alignment, which was complete before the
-    // gate/up grid started: the weight producer streams right away, the p loader and the
-    // epilogue wait for the gate/up grid.
+    pdl_launch_dependents();
+
     const int n_ct = a.H / kGM;
     const int nks = a.I / kGK;
     const int64_t T = gemm_blocks(a) * n_ct;
@@ -349,8 +377,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            gemm_producer(a, ctl, stages, T, n_ct, nks,
-                          [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
+            gemm_producer(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.p_tiles), T,
+                          n_ct, nks, [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
                 const int32_t y = e * a.I + s * kGK;
                 tma_load_2d(st, &tm_down, ct * kGM, y, bar, pol);
                 tma_load_2d(st + kGHalfBytes, &tm_down, ct * kGM + 64, y, bar, pol);
@@ -358,51 +386,45 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        pdl_wait();
-        gemm_loader<true>(a, ctl, stages, T, n_ct, nks);
-    } else if (warp == 2) {
         if (lane == 0) gemm_mma(ctl, stages, T, nks);
         __syncwarp();
-    } else if (warp >= kGEpiWarp0) {
-        pdl_wait();
-        pdl_launch_dependents();
-        const int ew = warp - kGEpiWarp0;
-        const int ch = 32 * ew + lane;  // output channel within the 128-channel tile
+    } else {
+        const int quad = warp & 3;
+        const int ch = 32 * quad + lane;  // output channel within the 128-channel tile
         int local = 0;
         for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
             const int64_t blk = u / n_ct;
             const int ct = (int)(u % n_ct);
             const int buf = local & 1;
-            const uint32_t tph = (uint32_t)(local >> 1) & 1u;
             if (ch < kGN) ctl.route[buf][ch] = gemm_route(a, blk * kGN + ch, a.blocks[blk], false);
-            const bool ok = gwait(&ctl.tfull[buf], tph, ctl);
-            if (named_bar_or(2, 128, !ok)) break;
-            tc_fence_after();
+            const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
+            if (named_bar_or(1, 128, !ok)) break;
             float v[kGN];
-#pragma unroll
-            for (int c0 = 0; c0 < kGN; c0 += 16) {
-                float t16[16];
-                tmem_ld16(ctl.tmem + ((uint32_t)(32 * ew) << 16) + (uint32_t)(buf * kGN + c0), t16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[c0 + i] = t16[i];
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
+            drain_accumulator(ctl, quad, buf, v);
             float *ybase = a.y + ct * kGM + ch;
 #pragma unroll
             for (int n = 0; n < kGN; ++n) {
                 const int r = ctl.route[buf][n];
                 if (r >= 0) ybase[(int64_t)r * a.H] = v[n];
             }
-            named_bar_sync(2, 128);  // route[buf] may be refilled two units later
         }
     }
     gemm_finish(ctl, warp, a.status);
 }
 
-static size_t gemm_gateup_smem() { return 1024 + kGStages * kGStageBytes + 64 * 64 * 4 + sizeof(GCtl); }
+static size_t gemm_gateup_smem() {
+    return 1024 + kGStages * kGStageBytes + kGN * 64 * 4 + kGChunkBytes + sizeof(GCtl);
+}
 static size_t gemm_down_smem() { return 1024 + kGStages * kGStageBytes + sizeof(GCtl); }
+
+cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream) {
+    cudaLaunchAttribute attrs[2];
+    const int64_t want = (a.cap + 7) / 8;  // 8 rows (warps) per CTA
+    const int64_t most = 4 * (int64_t)num_sms();
+    const int grid = (int)(want < 1 ? 1 : (want > most ? most : want));
+    cudaLaunchConfig_t cfg = launch_config(dim3(grid), dim3(256), 0, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, gather_rows_kernel, a);
+}
 
 cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                const GemmArgs &a, cudaStream_t stream) {

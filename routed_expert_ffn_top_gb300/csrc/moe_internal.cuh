@@ -49,7 +49,8 @@ struct WsLayout {
     size_t sbt;      // SubBlock[max_sub]
     size_t p;        // float[R * I]   SiLU(g) * u per route
     size_t y;        // float[R * H]   down-projection output per route
-    size_t p_rows;   // bf16[cap * I]  large-batch regime: p per aligned row
+    size_t x_tiles;  // bf16[cap * H]  large-batch regime: token rows per aligned row
+    size_t p_tiles;  // bf16[cap * I]  large-batch regime: p per aligned row
     size_t total;
 };
 
@@ -80,18 +81,20 @@ struct GemvArgs {
 constexpr int kGemmBlock = 64;
 
 struct GemmArgs {
-    const __nv_bfloat16 *x;   // B rows: gate/up reads h [M,H]; down reads p_rows [cap,I]
+    const __nv_bfloat16 *x;   // h [M,H] (read by the row gather)
     const int32_t *ids;       // topk_ids [M*k]: a row whose route disagrees is skipped
     const int32_t *sorted;    // aligned rows (route ids, sentinel = M*k)
     const int32_t *blocks;    // expert of each 64-row block
     const int32_t *npad;
-    __nv_bfloat16 *p_rows;    // gate/up output: SiLU(g) * u per aligned row, bf16 [cap, I]
+    __nv_bfloat16 *x_tiles;   // token rows of h per aligned row, tiled [cap/64][H/64][8 KB]
+    __nv_bfloat16 *p_tiles;   // SiLU(g) * u per aligned row, bf16, tiled [cap/64][I/64][8 KB]
     float *y;                 // down output per route [M*k, H]
     int32_t *status;
     int M, k, E, H, I;
     int64_t R, cap;
 };
 
+cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
