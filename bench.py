@@ -53,6 +53,10 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="layer_m21", choices=sorted(syn.WORKLOADS))
     p.add_argument("--M", type=int, default=None, help="override the token count")
+    p.add_argument("--graph", action="store_true",
+                   help="time CUDA-graph replays of the block instead of direct calls")
+    p.add_argument("--E", type=int, default=None,
+                   help="override the expert count (smaller captures of the same kernels)")
     p.add_argument("--weight-sets", type=int, default=8,
                    help="independent weight sets cycled by single-layer workloads")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -160,9 +164,30 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def overrides(args) -> dict:
+    out = {}
+    if args.M:
+        out["M"] = args.M
+    if args.E:
+        out["E"] = args.E
+    return out
+
+
+def gemm_regime(wl) -> bool:
+    """Dense weights with 64-row aligned blocks run as tcgen05 grouped GEMMs."""
+    return wl.kind == syn.W_DENSE and wl.b == 64
+
+
+def gateup_kernel_name(wl) -> str:
+    if gemm_regime(wl):
+        return "gemm_gateup_kernel"
+    return "gateup_dense_kernel" if wl.kind == syn.W_DENSE else "gateup_vq_kernel"
+
+
+def kernel_source_hash(kernel: str = "gateup_dense_kernel"):
     h = hashlib.sha256()
-    for name in ("gemv.cu", "ptx.cuh", "moe_internal.cuh"):
+    src = "gemm_tc05.cu" if kernel.startswith("gemm_") else "gemv.cu"
+    for name in (src, "ptx.cuh", "moe_internal.cuh"):
         with open(os.path.join(ROOT, "routed_expert_ffn_top_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -181,7 +206,7 @@ def recorded_traffic(kernel: str, workload: str, unique_experts: float):
                 if len(parts) != 5 or line.startswith("#"):
                     continue
                 k, wl, src, u, b = parts
-                if k == kernel and wl == workload and src == kernel_source_hash():
+                if k == kernel and wl == workload and src == kernel_source_hash(kernel):
                     return float(b) / float(u) * unique_experts
     except (OSError, ValueError):
         return None
@@ -204,7 +229,7 @@ def run_ours(args, world, rank, local):
 
     lib_build.build()
     dev = torch.device("cuda", local)
-    wl = syn.workload(args.workload, **({"M": args.M} if args.M else {}))
+    wl = syn.workload(args.workload, **overrides(args))
     M = wl.M
     stack = wl.layers > 1
     n_sets = wl.layers if stack else max(1, args.weight_sets)
@@ -215,39 +240,68 @@ def run_ours(args, world, rank, local):
     ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
     wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_block = 5
+    # router (+ alignment when one router cluster holds every token), alignment otherwise,
+    # [row gather in the grouped-GEMM regime], gate/up, down, combine
+    fused_align = 1 <= M <= 8 and M * wl.k <= 256
+    gemm = gemm_regime(wl)
+    launches_per_block = (4 if fused_align else 5) + (1 if gemm else 0)
 
-    def step(i):
+    def eager_step(i, s):
         """One step: a single layer, or all L layers of the residual stack."""
         if stack:
             h = h0
             for li in range(n_sets):
                 o = out[li % 2]
                 moe.moe_decode_block(h, layers[li], wl.k, wl.b, residual=h, out=o, topk_ids=ids,
-                                     topk_weights=wts, workspace=ws, stream=stream)
+                                     topk_weights=wts, workspace=ws, stream=s)
                 h = o
         else:
             moe.moe_decode_block(h0, layers[i % n_sets], wl.k, wl.b, out=out[0], topk_ids=ids,
-                                 topk_weights=wts, workspace=ws, stream=stream)
+                                 topk_weights=wts, workspace=ws, stream=s)
+
+    # The timed steps call moe_decode_block directly.  With --graph they replay CUDA graphs
+    # of the same calls (one per weight set, or one of the whole stack) instead; the other
+    # form is timed after the main region for comparison.
+    graphs = []
+    if args.graph:
+        if stack:
+            graphs.append(moe.capture_graph(lambda s: eager_step(0, s)))
+        else:
+            for li in range(n_sets):
+                graphs.append(moe.capture_graph(lambda s, li=li: eager_step(li, s)))
+        torch.cuda.synchronize()
+
+    def step(i):
+        if graphs:
+            graphs[i % len(graphs)].replay()
+        else:
+            eager_step(i, stream)
 
     blocks_per_step = n_sets if stack else 1
 
     # unique experts each weight set routes to (bytes actually streamed per block)
     gu_b, dn_b = expert_bytes(wl)
     per_set_unique = []
+    padded_rows = []  # aligned rows sum_e ceil(n_e / b) * b of each probe
+
+    def note_routing():
+        per_set_unique.append(int(torch.unique(ids).numel()))
+        n_e = torch.bincount(ids.flatten().long(), minlength=wl.E)
+        padded_rows.append(int(((n_e + wl.b - 1) // wl.b * wl.b).sum().item()))
+
     if stack:
         h = h0
         for li in range(n_sets):
             o = out[li % 2]
             moe.moe_decode_block(h, layers[li], wl.k, wl.b, residual=h, out=o, topk_ids=ids,
                                  topk_weights=wts, workspace=ws)
-            per_set_unique.append(int(torch.unique(ids).numel()))
+            note_routing()
             h = o
     else:
         for li in range(n_sets):
             moe.moe_decode_block(h0, layers[li], wl.k, wl.b, out=out[0], topk_ids=ids,
                                  topk_weights=wts, workspace=ws)
-            per_set_unique.append(int(torch.unique(ids).numel()))
+            note_routing()
     torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -273,6 +327,28 @@ def run_ours(args, world, rank, local):
     if status != 0:
         raise RuntimeError("device status %#x after the timed region" % status)
 
+    # the other launch form over the same steps, for comparison
+    other_ms = None
+    if not args.no_extras:
+        other = graphs
+        if not graphs:
+            if stack:
+                other = [moe.capture_graph(lambda s: eager_step(0, s))]
+            else:
+                other = [moe.capture_graph(lambda s, li=li: eager_step(li, s))
+                         for li in range(n_sets)]
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            if graphs:
+                eager_step(i, stream)
+            else:
+                other[i % len(other)].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        other_ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
+        del other
+
     ms_per_step = t_ms / args.steps
     tokens = M * args.steps * world
     value = tokens / (t_ms / 1e3)
@@ -297,6 +373,9 @@ def run_ours(args, world, rank, local):
                           % (n_sets, wl.E * (gu_b + dn_b) / 1e9)),
                    "parallelism": "replicas" if world > 1 else "single"},
         "us_per_layer": round(us_per_layer, 3),
+        "launch": "cuda_graph_replay" if graphs else "direct_calls",
+        ("direct_call_us_per_layer" if graphs else "graph_replay_us_per_layer"):
+            None if other_ms is None else round(other_ms * 1e3 / blocks_per_step, 3),
         "hbm_gbs_unique_expert_bytes": round(hbm_gbs, 1),
         "unique_experts_per_layer": round(statistics.mean(per_set_unique), 2),
         "unique_experts_per_set": per_set_unique,
@@ -337,18 +416,28 @@ def run_ours(args, world, rank, local):
     mean_ms = {k: statistics.mean(v) for k, v in dur.items()}
     peak, peak_kind = measured_peaks()
     u_mean = statistics.mean(per_set_unique)
-    gu_alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * 4
+    # weights of the routed experts + h read once + p written (fp32 per route in the GEMV
+    # regime, bf16 per route in the GEMM regime)
+    gu_kernel = gateup_kernel_name(wl)
+    p_bytes = 2 if gemm else 4
+    gu_alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * p_bytes
     achieved = gu_alg / (mean_ms["gateup"] * 1e-3) / 1e9
-    traffic = recorded_traffic("gateup_dense_kernel", wl.name, u_mean)
+    traffic = recorded_traffic(gu_kernel, wl.name, u_mean)
     result["roofline"] = {
-        "kernel": "gateup_dense_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "kernel": gu_kernel, "bound": "hbm", "achieved": round(achieved, 1),
         "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
         "traffic": None if traffic is None else int(traffic),
         "algorithmic_bytes_per_launch": int(gu_alg),
         "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
     }
-    dn_alg = u_mean * dn_b + M * wl.k * (wl.I + wl.H) * 4
+    dn_alg = u_mean * dn_b + M * wl.k * (wl.I * p_bytes + wl.H * 4)
     result["down_kernel_gbs"] = round(dn_alg / (mean_ms["down"] * 1e-3) / 1e9, 1)
+    if gemm:
+        # tensor work actually issued: every aligned row, valid or padding, x 2 flops per MAC
+        npad = float(sum(padded_rows) / len(padded_rows))
+        result["roofline"]["tensor_tflops_issued"] = round(
+            2 * npad * 2 * wl.H * wl.I / (mean_ms["gateup"] * 1e-3) / 1e12, 1)
+        result["roofline"]["gather_in_gateup_interval"] = True
 
     # --- e2e: host h in, host out back, copies inside the timed region
     h_host = h0.cpu().pin_memory()
@@ -434,7 +523,7 @@ def run_reference(args, world, rank):
         return
     import oracle
     oracle.build()
-    wl = syn.workload(args.workload, **({"M": args.M} if args.M else {}))
+    wl = syn.workload(args.workload, **overrides(args))
     layer = syn.make_layer(wl, layer=0, seed=1, device="cpu")
     h = syn.make_hidden(wl, seed=1, device="cpu")
     # each step: the oracle's full block on a sample of at most 8 tokens of the batch

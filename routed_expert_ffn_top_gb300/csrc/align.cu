@@ -42,8 +42,7 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, in
                          int32_t *blocks, int32_t *npad, int64_t cap, SubBlock *sbt, int rsub,
                          int32_t *status, cudaStream_t stream) {
     const size_t smem = (size_t)align_smem_ints(E) * sizeof(int32_t);
-    cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(align_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kAlignThreads), smem, stream, attrs, 0);

@@ -141,4 +141,78 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
     }
 }
 
+// The same alignment for at most kAlignThreads routes whose ids are already in shared
+// memory, with one thread per route and no per-expert tables: thread r counts the routes of
+// its expert (n_e) and those of them before r, the first route of each expert publishes
+// ceil(n_e / b) * b, and the padded offset of an expert is the sum published by the experts
+// below it.  Positions, padding, block vector, sub-block records and tail are the same
+// function of the ids as in align_core.
+__host__ __device__ constexpr int align_small_smem_ints() { return kAlignThreads + 4; }
+
+__device__ inline void align_small(const int32_t *ids, int R, int k, int E, int b, int rsub,
+                                   int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
+                                   SubBlock *sbt, int32_t *status, int32_t *sm) {
+    int32_t *pub = sm;  // [kAlignThreads] padded count published by each expert's first route
+    const int tid = threadIdx.x;
+    const int32_t sentinel = R;
+    int e = -1, n = 0, lower = 0;
+    bool valid = false;
+    if (tid < R) {
+        e = ids[tid];
+        valid = e >= 0 && e < E;
+        if (valid)
+            for (int q = 0; q < R; ++q)
+                if (ids[q] == e) {
+                    ++n;
+                    lower += q < tid;
+                }
+    }
+    const int padded = valid ? (n + b - 1) / b * b : 0;
+    const bool leader = valid && lower == 0;
+    pub[tid] = leader ? padded : 0;
+    const int any_invalid = __syncthreads_or(tid < R && !valid);
+
+    int off = 0, total = 0;
+    for (int q = 0; q < R; ++q) {
+        const int p = pub[q];
+        total += p;
+        if (p != 0 && ids[q] < e) off += p;
+    }
+    if (valid) {
+        const int64_t pos = (int64_t)off + lower;
+        if (pos < cap) {
+            if (sorted) sorted[pos] = tid;
+            if (sbt) {
+                SubBlock *rec = sbt + pos / rsub;
+                rec->routes[pos % rsub] = tid;
+                rec->tokens[pos % rsub] = tid / k;
+            }
+        }
+    }
+    if (leader) {
+        if (sorted)
+            for (int q = n; q < padded; ++q)
+                if (off + q < cap) sorted[off + q] = sentinel;
+        if (blocks)
+            for (int q = 0; q < padded / b; ++q) blocks[off / b + q] = e;
+        if (sbt)
+            for (int s = off / rsub; s < (off + padded) / rsub; ++s) {
+                const int first = s * rsub - off;
+                const int ntok = max(0, min(rsub, n - first));
+                SubBlock *rec = sbt + s;
+                rec->e = e;
+                rec->ntok = ntok;
+                for (int q = ntok; q < kNT; ++q) rec->routes[q] = rec->tokens[q] = -1;
+            }
+    }
+    if (sorted)
+        for (int64_t pos = (int64_t)total + tid; pos < cap; pos += kAlignThreads) sorted[pos] = sentinel;
+    if (blocks)
+        for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += kAlignThreads) blocks[q] = -1;
+    if (tid == 0) {
+        npad[0] = total;
+        if (status && any_invalid) atomicOr(status, MOE_DEV_INVALID_EXPERT);
+    }
+}
+
 }  // namespace moe

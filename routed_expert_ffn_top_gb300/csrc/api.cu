@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -64,6 +65,20 @@ int num_sms() {
         cache[dev] = n > 0 ? n : 1;
     }
     return cache[dev];
+}
+
+cudaError_t ensure_smem(const void *func, size_t bytes) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> done;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({func, dev});
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess) done[{func, dev}] = bytes;
+    return err;
 }
 
 cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

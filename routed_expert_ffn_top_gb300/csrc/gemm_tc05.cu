@@ -429,8 +429,7 @@ cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream) {
 cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                const GemmArgs &a, cudaStream_t stream) {
     const size_t smem = gemm_gateup_smem();
-    cudaError_t err = cudaFuncSetAttribute(gemm_gateup_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_gateup_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);
@@ -439,8 +438,7 @@ cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm
 
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream) {
     const size_t smem = gemm_down_smem();
-    cudaError_t err = cudaFuncSetAttribute(gemm_down_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_down_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);

@@ -687,8 +687,7 @@ static size_t down_smem() { return 1024 + kStages * kStageBytesDN + kRedBytesDN 
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream) {
     const size_t smem = gateup_smem();
-    cudaError_t err = cudaFuncSetAttribute(gateup_dense_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gateup_dense_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
@@ -702,8 +701,7 @@ static size_t gateup_vq_smem() {
 cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
                              const GemvArgs &a, cudaStream_t stream) {
     const size_t smem = gateup_vq_smem();
-    cudaError_t err = cudaFuncSetAttribute(gateup_vq_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gateup_vq_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
@@ -712,8 +710,7 @@ cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream) {
     const size_t smem = down_smem();
-    cudaError_t err = cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(down_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);

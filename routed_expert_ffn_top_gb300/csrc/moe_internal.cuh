@@ -174,6 +174,11 @@ cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStrea
 
 cudaError_t launch_combine(const GemvArgs &a, cudaStream_t stream);
 
+// Raises `func`'s dynamic shared-memory limit to at least `bytes` on the current device.
+// The attribute is set once per (kernel, device) and remembered: repeating the runtime call
+// on every launch costs host time that small decode blocks cannot hide.
+cudaError_t ensure_smem(const void *func, size_t bytes);
+
 // Shared launch helper: programmatic dependent launch on, optional cluster dims.
 cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attrs, int cluster_x);

@@ -36,15 +36,19 @@ struct FusedAlign {
 };
 
 // Generic address of `p` (a shared variable of this CTA) in CTA `rank` of the cluster.
-__device__ __forceinline__ const float *cluster_peer(const float *p, uint32_t rank) {
+template <typename T>
+__device__ __forceinline__ T *cluster_peer_mut(T *p, uint32_t rank) {
     uint64_t out;
     asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
-    return reinterpret_cast<const float *>(out);
+    return reinterpret_cast<T *>(out);
 }
-__device__ __forceinline__ const int32_t *cluster_peer(const int32_t *p, uint32_t rank) {
-    uint64_t out;
-    asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
-    return reinterpret_cast<const int32_t *>(out);
+
+// fp32 -> uint32 with the same order (larger float, larger key; -0 and +0 both map to the
+// key of +0, so they tie as floats do).  Every non-NaN float maps above 0.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 template <int TM>
@@ -62,7 +66,8 @@ __global__ void __launch_bounds__(kRouterThreads)
     const int RG = kRouterThreads / npairs;  // row groups (>= 1 since E <= 512)
 
     // shared layout: w_s [HS][E] bf16 | x_s [TM][HS] bf16 | red [RG][TM][E] f32 |
-    //                part [TM][E] f32 | ids_s [k] | bar | align scratch
+    //                gath [8][E] f32 (this CTA's token: the partial logits of every rank) |
+    //                ids_s [8 * 32] | bar | align scratch
     unsigned char *ptr = smem_raw;
     __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(ptr);
     ptr += (size_t)HS * E * 2;
@@ -70,8 +75,8 @@ __global__ void __launch_bounds__(kRouterThreads)
     ptr += (size_t)TM * HS * 2;
     float *red = reinterpret_cast<float *>(ptr);
     ptr += (size_t)RG * TM * E * 4;
-    float *part = reinterpret_cast<float *>(ptr);
-    ptr += (size_t)TM * E * 4;
+    float *gath = reinterpret_cast<float *>(ptr);
+    ptr += (size_t)kRouterCluster * E * 4;
     int32_t *ids_s = reinterpret_cast<int32_t *>(ptr);  // [8 * 32] gathered ids (rank 0)
     ptr += 8 * 32 * 4;
     uint64_t *bar = reinterpret_cast<uint64_t *>(ptr);
@@ -144,10 +149,14 @@ __global__ void __launch_bounds__(kRouterThreads)
         }
     }
     __syncthreads();
+    // Row groups summed in order, then pushed to the CTA that finalises the token: rank t
+    // receives every rank's partial logits of token t in its own shared memory, so after the
+    // cluster barrier all reads are local.
     for (int idx = tid; idx < TM * E; idx += kRouterThreads) {
         float s = red[idx];
         for (int g = 1; g < RG; ++g) s += red[(size_t)g * TM * E + idx];
-        part[idx] = s;
+        const int t = idx / E, e = idx - t * E;
+        if (tile * TM + t < M) cluster_peer_mut(gath, (uint32_t)t)[(size_t)rank * E + e] = s;
     }
     cluster_sync();
 
@@ -158,53 +167,51 @@ __global__ void __launch_bounds__(kRouterThreads)
     if (warp == 0 && t < TM && m < M) {
         constexpr int kPerLane = 16;  // E <= 512
         float vals[kPerLane];
+        uint32_t key[kPerLane];
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
             const int e = lane + 32 * i;
             float v = -FLT_MAX;
+            key[i] = 0u;  // no candidate
             if (e < E) {
-                // the 8 partials are loaded together, then summed in rank order
-                float pv[kRouterCluster];
-#pragma unroll
-                for (uint32_t q = 0; q < kRouterCluster; ++q)
-                    pv[q] = *cluster_peer(part + (size_t)t * E + e, q);
                 v = 0.0f;
 #pragma unroll
-                for (int q = 0; q < kRouterCluster; ++q) v += pv[q];
+                for (int q = 0; q < kRouterCluster; ++q) v += gath[(size_t)q * E + e];
                 if (bias) v += bias[e];
                 if (!ok) v = -FLT_MAX;
+                key[i] = order_key(v);
             }
             vals[i] = v;
         }
-        uint32_t taken = 0;
+        // k rounds of a warp arg-max: the largest key, ties to the lower expert id (each lane
+        // scans its experts in ascending id, then the lowest id among the lanes at the max)
         int my_e = -1;
         float my_v = -FLT_MAX;
         for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
+            uint32_t bk = 0u;
+            int bi = -1;
 #pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u)) {
-                    const float v = vals[i];
-                    if (v > bv || (v == bv && e < be)) {
-                        bv = v;
-                        be = e;
+            for (int i = 0; i < kPerLane; ++i)
+                if (key[i] > bk) {
+                    bk = key[i];
+                    bi = i;
+                }
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t cand = (bi >= 0 && bk == mk) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+            const uint32_t be = __reduce_min_sync(0xffffffffu, cand);
+            float bv = -FLT_MAX;
+            if (be != 0xffffffffu && (int)(be & 31) == lane) {
+                const int i = (int)(be >> 5);
+#pragma unroll
+                for (int q = 0; q < kPerLane; ++q)
+                    if (q == i) {
+                        bv = vals[q];
+                        key[q] = 0u;  // taken
                     }
-                }
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if (be >= 0 && be < E && (be & 31) == lane) taken |= 1u << (be >> 5);
+            bv = __shfl_sync(0xffffffffu, bv, (int)(be & 31));
             if (lane == j) {
-                my_e = be;
+                my_e = be == 0xffffffffu ? -1 : (int)be;
                 my_v = bv;
             }
         }
@@ -228,28 +235,25 @@ __global__ void __launch_bounds__(kRouterThreads)
             const int id = ok ? my_e : -1;
             topk_ids[(size_t)m * k + lane] = id;
             topk_wts[(size_t)m * k + lane] = ok ? ex / denom : 0.0f;
-            ids_s[lane] = id;
+            // every token's ids go to rank 0, which aligns them when one cluster holds all
+            if (fa.enabled) cluster_peer_mut(ids_s, 0u)[t * k + lane] = id;
         }
     }
     if (fa.enabled) {
-        // every token's ids are in the cluster: rank 0 gathers them and aligns
         cluster_sync();
-        if (rank == 0) {
-            for (int idx = tid; idx < M * k; idx += kRouterThreads)
-                ids_s[idx] = *cluster_peer(ids_s + idx % k, (uint32_t)(idx / k));
-            __syncthreads();
-            align_core(ids_s, (int64_t)M * k, k, E, fa.b, fa.rsub, fa.sorted, fa.blocks, fa.npad,
-                       fa.cap, fa.sbt, fa.status, align_sm);
-        }
+        if (rank == 0)
+            align_small(ids_s, M * k, k, E, fa.b, fa.rsub, fa.sorted, fa.blocks, fa.npad, fa.cap,
+                        fa.sbt, fa.status, align_sm);
     }
-    cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+    // No CTA touches another's shared memory after the last cluster barrier.
 }
 
 static size_t router_smem(int TM, int H, int E, bool fuse) {
     const int HS = H / kRouterCluster;
     const int RG = kRouterThreads / (E / 2);
     return (size_t)HS * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
-           (size_t)TM * E * 4 + 8 * 32 * 4 + 16 + (fuse ? (size_t)align_smem_ints(E) * 4 : 0);
+           (size_t)kRouterCluster * E * 4 + 8 * 32 * 4 + 16 +
+           (fuse ? (size_t)align_small_smem_ints() * 4 : 0);
 }
 
 template <int TM>
@@ -258,8 +262,7 @@ static cudaError_t launch_router_tm(const __nv_bfloat16 *h, const __nv_bfloat16 
                                     int32_t *ids, float *wts, const FusedAlign &fa,
                                     cudaStream_t stream) {
     const size_t smem = router_smem(TM, H, E, fa.enabled != 0);
-    cudaError_t err = cudaFuncSetAttribute(router_topk_kernel<TM>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(router_topk_kernel<TM>), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     dim3 grid(kRouterCluster, (M + TM - 1) / TM, 1);

@@ -348,3 +348,28 @@ def moe_set_trace_events(events=None):
             e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib().moe_set_trace_events(arr, len(events)), "moe_set_trace_events")
+
+
+# ------------------------------------------------------------------------------ CUDA graphs
+def capture_graph(fn, stream: Optional[torch.cuda.Stream] = None) -> torch.cuda.CUDAGraph:
+    """Capture ``fn(stream)`` -- one or more calls of the entry points above on ``stream`` --
+    into a CUDA graph, after one eager run of it on the same stream.
+
+    Decoding repeats the same block shapes step after step.  Replaying the captured
+    launches (programmatic dependent launches included) skips the per-call host work:
+    argument checks, marshalling, tensor-map encoding and one launch per kernel.  At small
+    M that host work takes longer than the block's GPU time.  The graph keeps the raw
+    pointers of the tensors ``fn`` used: a replay reads the inputs that are in those same
+    tensors at that time and writes the same outputs.  Its workspace must not be shared
+    with calls that run at the same time.
+    """
+    if stream is None:
+        stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        fn(stream)  # eager run: one-time kernel attributes are set outside the capture
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn(stream)
+    torch.cuda.current_stream().wait_stream(stream)
+    return graph

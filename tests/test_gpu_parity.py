@@ -391,3 +391,25 @@ def test_stack48_teacher_forced(M):
         del layer
         h = out
     assert moe.moe_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("b", [1, 8, 64])
+def test_decode_block_router_fused_alignment(M, b):
+    """M <= 8: the router cluster also aligns the routes; every block size and regime."""
+    k, E, H, I = 4, 16, 512, 256
+    wl = syn.Workload("fused_%d_%d" % (M, b), H=H, I=I, E=E, k=k, b=b, M=M, router_bias=True)
+    layer = syn.make_layer(wl, seed=M + b, device=DEV)
+    h = syn.make_hidden(wl, seed=M + b, device=DEV)
+    res = syn.make_hidden(wl, seed=7, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out, ids, wts = moe.moe_decode_block(h, layer, k, b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, k)
+    use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
+                                          logits, k)
+    ref = G.oracle_ffn(layer, h, use_ids, use_wts, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "fused alignment M=%d b=%d" % (M, b))
+    # the same routes through the stand-alone alignment give the same bits
+    out2 = moe.moe_expert_ffn(h, layer, ids, wts, b, residual=res)
+    assert torch.equal(out, out2)
