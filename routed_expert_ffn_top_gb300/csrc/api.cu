@@ -368,6 +368,7 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.n_ht = d.n_ht;
     a.n_ib = d.n_ib;
     a.max_sub = d.max_sub;
+    a.w_down = static_cast<const unsigned char *>(w->w_down);
     a.cb_gate = vq ? static_cast<const uint2 *>(w->cb_gate) : nullptr;
     a.cb_up = vq ? static_cast<const uint2 *>(w->cb_up) : nullptr;
     a.n_qb = d.H / (4 * kBoxRows);

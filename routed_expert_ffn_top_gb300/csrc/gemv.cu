@@ -473,6 +473,28 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
     }
 }
 
+// A VQ gate/up CTA with no tile (small batches: fewer tiles than SMs) warms the routed
+// experts' W_down in L2 for the down kernel: the index maps are a quarter of the dense
+// gate/up bytes, so HBM has room during gate/up (with dense weights it has not, and the
+// prefetch would only slow gate/up down).  Every thread of the idle
+// CTAs prefetches 128-byte lines (load-store path, so no copy engine queue is held), the
+// lines of each expert's first sub-block dealt out round-robin.
+__device__ void prefetch_down_weights(const GemvArgs &a, int64_t T) {
+    const int64_t idle = (int64_t)gridDim.x - T;
+    if ((int64_t)blockIdx.x < T || idle <= 0) return;
+    const int64_t n_sub = num_subblocks(a);
+    const int64_t lines = (int64_t)a.I * a.H * 2 / 128;  // per expert
+    const int64_t stride = idle * blockDim.x;
+    for (int64_t sb = 0; sb < n_sub; ++sb) {
+        const int e = a.sbt[sb].e;
+        if (e < 0 || e >= a.E || a.sbt[sb].ntok == 0) continue;
+        if (sb > 0 && a.sbt[sb - 1].e == e) continue;  // not the expert's first sub-block
+        const unsigned char *base = a.w_down + (int64_t)e * lines * 128;
+        for (int64_t l = ((int64_t)blockIdx.x - T) * blockDim.x + threadIdx.x; l < lines; l += stride)
+            prefetch_l2_line(base + l * 128);
+    }
+}
+
 // ---------------------------------------------------------------------------- gate/up
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gateup_dense_kernel(const __grid_constant__ CUtensorMap tm_gate,
@@ -551,6 +573,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
     const int64_t T = num_subblocks(a) * a.n_it;
     const int per_tile = 2 * a.n_qb;
+    prefetch_down_weights(a, T);
 
     if (warp == 0) {
         if (lane == 0) {

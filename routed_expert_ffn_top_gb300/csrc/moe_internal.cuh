@@ -69,6 +69,7 @@ struct GemvArgs {
     float *p;
     float *y;
     int32_t *status;
+    const unsigned char *w_down;  // W_down [E, I, H] bf16 (idle gate/up CTAs warm it in L2)
     const uint2 *cb_gate;  // VQ code books [256] code words of 4 bf16 (NULL when dense)
     const uint2 *cb_up;
     int M, k, E, H, I, b, rsub;

@@ -109,6 +109,11 @@ __device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gsrc,
         : "memory");
 }
 
+// Prefetch of one line into L2 through the load-store path.
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // 16-byte asynchronous global -> shared copy through L2 only (never a stale L1 line).
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
