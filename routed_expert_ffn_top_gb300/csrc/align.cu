@@ -18,7 +18,17 @@ __global__ void __launch_bounds__(kAlignThreads)
     extern __shared__ __align__(16) int32_t sm[];
     pdl_wait();
     pdl_launch_dependents();
-    align_core(ids, (int64_t)M * k, k, E, b, rsub, sorted, blocks, npad, cap, sbt, status, sm);
+    const int64_t R = (int64_t)M * k;
+    const int32_t *src = ids;
+    if (R <= kAlignStagedRoutes) {
+        // every id read once, all loads in flight together, then shared-memory reads only
+        int32_t *ids_s = sm + align_smem_ints(E);
+#pragma unroll 8
+        for (int64_t r = threadIdx.x; r < R; r += kAlignThreads) ids_s[r] = ids[r];
+        __syncthreads();
+        src = ids_s;
+    }
+    align_core(src, R, k, E, b, rsub, sorted, blocks, npad, cap, sbt, status, sm);
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
@@ -41,7 +51,9 @@ __global__ void __launch_bounds__(kAlignThreads)
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, int32_t *sorted,
                          int32_t *blocks, int32_t *npad, int64_t cap, SubBlock *sbt, int rsub,
                          int32_t *status, cudaStream_t stream) {
-    const size_t smem = (size_t)align_smem_ints(E) * sizeof(int32_t);
+    const int64_t R = (int64_t)M * k;
+    const size_t smem =
+        (size_t)(align_smem_ints(E) + (R <= kAlignStagedRoutes ? R : 0)) * sizeof(int32_t);
     cudaError_t err = ensure_smem(reinterpret_cast<const void *>(align_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];

@@ -22,6 +22,8 @@ namespace moe {
 
 constexpr int kAlignThreads = 256;
 constexpr int kAlignWarps = kAlignThreads / 32;
+// The stand-alone alignment stages up to this many route ids in shared memory (128 KB).
+constexpr int kAlignStagedRoutes = 32768;
 
 // Shared-memory ints align_core needs for E experts.
 __host__ __device__ constexpr int align_smem_ints(int E) { return (3 + kAlignWarps) * E + 4; }
@@ -141,18 +143,19 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
     }
 }
 
-// The same alignment for at most kAlignThreads routes whose ids are already in shared
+// The same alignment for at most 256 routes (and at most blockDim.x) whose ids are already in shared
 // memory, with one thread per route and no per-expert tables: thread r counts the routes of
 // its expert (n_e) and those of them before r, the first route of each expert publishes
 // ceil(n_e / b) * b, and the padded offset of an expert is the sum published by the experts
 // below it.  Positions, padding, block vector, sub-block records and tail are the same
 // function of the ids as in align_core.
-__host__ __device__ constexpr int align_small_smem_ints() { return kAlignThreads + 4; }
+__host__ __device__ constexpr int align_small_smem_ints(int nthreads) { return nthreads + 4; }
 
 __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int b, int rsub,
                                    int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
                                    SubBlock *sbt, int32_t *status, int32_t *sm) {
-    int32_t *pub = sm;  // [kAlignThreads] padded count published by each expert's first route
+    int32_t *pub = sm;  // [blockDim.x] padded count published by each expert's first route
+    const int nthr = blockDim.x;
     const int tid = threadIdx.x;
     const int32_t sentinel = R;
     int e = -1, n = 0, lower = 0;
@@ -206,9 +209,9 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
             }
     }
     if (sorted)
-        for (int64_t pos = (int64_t)total + tid; pos < cap; pos += kAlignThreads) sorted[pos] = sentinel;
+        for (int64_t pos = (int64_t)total + tid; pos < cap; pos += nthr) sorted[pos] = sentinel;
     if (blocks)
-        for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += kAlignThreads) blocks[q] = -1;
+        for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += nthr) blocks[q] = -1;
     if (tid == 0) {
         npad[0] = total;
         if (status && any_invalid) atomicOr(status, MOE_DEV_INVALID_EXPERT);

@@ -427,8 +427,8 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     if (given == 0) {
         int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
         err = launch_align(topk_ids, M, k, w->E, b, reinterpret_cast<int32_t *>(ws + L.sorted),
-                           reinterpret_cast<int32_t *>(ws + L.blocks), ws_npad, d.cap, sbt, d.rsub,
-                           status, s);
+                           reinterpret_cast<int32_t *>(ws + L.blocks), ws_npad, d.cap,
+                           gemm_regime(w->kind, b) ? nullptr : sbt, d.rsub, status, s);
         npad = ws_npad;
     } else {
         if (!aligned(sorted_route_ids, 4) || !aligned(expert_block_ids, 4) || !aligned(num_padded, 4))
@@ -481,8 +481,8 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
                             topk_ids, topk_weights, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
-        err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap, ws_sbt,
-                           d.rsub, ws_status, s);
+        err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                           gemm_regime(w->kind, b) ? nullptr : ws_sbt, d.rsub, ws_status, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
     }
     trace(2, s);

@@ -19,7 +19,7 @@ constexpr int kBoxRows = 256;   // rows (of H for gate/up, of I for down) per we
 constexpr int kConsumerWarps = 8;
 constexpr int kGemvThreads = 32 * (2 + kConsumerWarps);  // producer, loader, consumers
 constexpr int kRouterCluster = 8;  // CTAs per router cluster (split of H)
-constexpr int kRouterThreads = 256;
+constexpr int kRouterThreads = 512;
 
 struct Dims {
     int M, k, E, H, I, b;

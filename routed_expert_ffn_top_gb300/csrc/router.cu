@@ -51,7 +51,8 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int TM>
+// TM tokens per cluster tile; kPerLane experts per lane in the top-k warp (E <= 32 kPerLane).
+template <int TM, int kPerLane>
 __global__ void __launch_bounds__(kRouterThreads)
     router_topk_kernel(const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ wr,
                        const float *__restrict__ bias, int M, int H, int E, int k, int renorm,
@@ -165,7 +166,6 @@ __global__ void __launch_bounds__(kRouterThreads)
     const int t = (int)rank;
     const int m = tile * TM + t;
     if (warp == 0 && t < TM && m < M) {
-        constexpr int kPerLane = 16;  // E <= 512
         float vals[kPerLane];
         uint32_t key[kPerLane];
 #pragma unroll
@@ -253,23 +253,42 @@ static size_t router_smem(int TM, int H, int E, bool fuse) {
     const int RG = kRouterThreads / (E / 2);
     return (size_t)HS * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
            (size_t)kRouterCluster * E * 4 + 8 * 32 * 4 + 16 +
-           (fuse ? (size_t)align_small_smem_ints() * 4 : 0);
+           (fuse ? (size_t)align_small_smem_ints(kRouterThreads) * 4 : 0);
 }
 
-template <int TM>
+template <int TM, int kPerLane>
 static cudaError_t launch_router_tm(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                                     const float *bias, int M, int H, int E, int k, int renorm,
                                     int32_t *ids, float *wts, const FusedAlign &fa,
                                     cudaStream_t stream) {
     const size_t smem = router_smem(TM, H, E, fa.enabled != 0);
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(router_topk_kernel<TM>), smem);
+    cudaError_t err =
+        ensure_smem(reinterpret_cast<const void *>(router_topk_kernel<TM, kPerLane>), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     dim3 grid(kRouterCluster, (M + TM - 1) / TM, 1);
     cudaLaunchConfig_t cfg = launch_config(grid, dim3(kRouterThreads), smem, stream, attrs,
                                            kRouterCluster);
-    return cudaLaunchKernelEx(&cfg, router_topk_kernel<TM>, h, w_router, bias, M, H, E, k,
+    return cudaLaunchKernelEx(&cfg, router_topk_kernel<TM, kPerLane>, h, w_router, bias, M, H, E, k,
                               renorm, ids, wts, fa);
+}
+
+template <int kPerLane>
+static cudaError_t launch_router_lanes(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
+                                       const float *bias, int M, int H, int E, int k, int renorm,
+                                       int32_t *topk_ids, float *topk_weights,
+                                       const FusedAlign &fa, cudaStream_t stream) {
+    if (M <= 1)
+        return launch_router_tm<1, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
+                                             topk_weights, fa, stream);
+    if (M <= 2)
+        return launch_router_tm<2, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
+                                             topk_weights, fa, stream);
+    if (M <= 4)
+        return launch_router_tm<4, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
+                                             topk_weights, fa, stream);
+    return launch_router_tm<8, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
+                                         topk_weights, fa, stream);
 }
 
 static cudaError_t launch_router_any(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
@@ -278,17 +297,14 @@ static cudaError_t launch_router_any(const __nv_bfloat16 *h, const __nv_bfloat16
                                      const FusedAlign &fa, cudaStream_t stream) {
     if (M <= 0) return cudaSuccess;
     const int renorm = renormalize ? 1 : 0;
-    if (M <= 1)
-        return launch_router_tm<1>(h, w_router, bias, M, H, E, k, renorm, topk_ids, topk_weights,
+    if (E <= 128)
+        return launch_router_lanes<4>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
+                                      topk_weights, fa, stream);
+    if (E <= 256)
+        return launch_router_lanes<8>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
+                                      topk_weights, fa, stream);
+    return launch_router_lanes<16>(h, w_router, bias, M, H, E, k, renorm, topk_ids, topk_weights,
                                    fa, stream);
-    if (M <= 2)
-        return launch_router_tm<2>(h, w_router, bias, M, H, E, k, renorm, topk_ids, topk_weights,
-                                   fa, stream);
-    if (M <= 4)
-        return launch_router_tm<4>(h, w_router, bias, M, H, E, k, renorm, topk_ids, topk_weights,
-                                   fa, stream);
-    return launch_router_tm<8>(h, w_router, bias, M, H, E, k, renorm, topk_ids, topk_weights, fa,
-                               stream);
 }
 
 cudaError_t launch_router(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
