@@ -10,25 +10,47 @@
 
 namespace moe {
 
+// Shared-memory ints the alignment kernel uses for (E, R, cap, b): align_core's tables, the
+// staged ids, and the aligned rows and block vector built in shared memory.  Returns 0 when
+// they do not fit (then ids and rows stay in global memory).
+static int64_t align_kernel_ints(int E, int64_t R, int64_t cap, int b) {
+    const int64_t n = align_smem_ints(E) + R + cap + cap / b + 4;
+    return (R <= kAlignStagedRoutes && n * 4 <= kAlignSmemBytes) ? n : 0;
+}
+
 __global__ void __launch_bounds__(kAlignThreads)
     align_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int b,
                  int32_t *__restrict__ sorted, int32_t *__restrict__ blocks,
                  int32_t *__restrict__ npad, int64_t cap, SubBlock *sbt, int rsub,
-                 int32_t *status) {
+                 int32_t *status, int staged) {
     extern __shared__ __align__(16) int32_t sm[];
     pdl_wait();
     pdl_launch_dependents();
     const int64_t R = (int64_t)M * k;
-    const int32_t *src = ids;
-    if (R <= kAlignStagedRoutes) {
-        // every id read once, all loads in flight together, then shared-memory reads only
-        int32_t *ids_s = sm + align_smem_ints(E);
-#pragma unroll 8
-        for (int64_t r = threadIdx.x; r < R; r += kAlignThreads) ids_s[r] = ids[r];
-        __syncthreads();
-        src = ids_s;
+    if (!staged) {
+        align_core(ids, R, k, E, b, rsub, sorted, blocks, npad, cap, sbt, status, sm);
+        return;
     }
-    align_core(src, R, k, E, b, rsub, sorted, blocks, npad, cap, sbt, status, sm);
+    // Everything in shared memory: the ids are read once with all loads in flight, the rows
+    // and the block vector are built there, then leave with coalesced stores; the sub-block
+    // records are formed one per thread from the finished rows.
+    int32_t *ids_s = sm + align_smem_ints(E);
+    int32_t *rows_s = ids_s + R;
+    int32_t *blocks_s = rows_s + cap;
+#pragma unroll 8
+    for (int64_t r = threadIdx.x; r < R; r += kAlignThreads) ids_s[r] = ids[r];
+    __syncthreads();
+    align_core(ids_s, R, k, E, b, rsub, rows_s, blocks_s, npad, cap, nullptr, status, sm);
+    __syncthreads();
+    if (sorted)
+        for (int64_t i = threadIdx.x; i < cap; i += kAlignThreads) sorted[i] = rows_s[i];
+    if (blocks)
+        for (int64_t i = threadIdx.x; i < cap / b; i += kAlignThreads) blocks[i] = blocks_s[i];
+    if (sbt) {
+        const int64_t total = sm[(3 + kAlignWarps) * E];  // align_core's padded row count
+        for (int64_t sb = threadIdx.x; sb < total / rsub; sb += kAlignThreads)
+            build_subblock(rows_s, blocks_s, ids_s, sb, rsub, b, E, R, k, false, status, sbt + sb);
+    }
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
@@ -52,14 +74,14 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, in
                          int32_t *blocks, int32_t *npad, int64_t cap, SubBlock *sbt, int rsub,
                          int32_t *status, cudaStream_t stream) {
     const int64_t R = (int64_t)M * k;
-    const size_t smem =
-        (size_t)(align_smem_ints(E) + (R <= kAlignStagedRoutes ? R : 0)) * sizeof(int32_t);
+    const int64_t staged_ints = align_kernel_ints(E, R, cap, b);
+    const size_t smem = (size_t)(staged_ints ? staged_ints : align_smem_ints(E)) * sizeof(int32_t);
     cudaError_t err = ensure_smem(reinterpret_cast<const void *>(align_kernel), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kAlignThreads), smem, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, align_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
-                              cap, sbt, rsub, status);
+                              cap, sbt, rsub, status, staged_ints ? 1 : 0);
 }
 
 cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const int32_t *blocks,

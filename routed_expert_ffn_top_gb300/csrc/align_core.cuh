@@ -22,14 +22,21 @@ namespace moe {
 
 constexpr int kAlignThreads = 256;
 constexpr int kAlignWarps = kAlignThreads / 32;
-// The stand-alone alignment stages up to this many route ids in shared memory (128 KB).
+// The stand-alone alignment works in shared memory (ids, aligned rows, block vector) when
+// they fit in kAlignSmemBytes.
 constexpr int kAlignStagedRoutes = 32768;
+constexpr int kAlignSmemBytes = 200 * 1024;
 
 // Shared-memory ints align_core needs for E experts.
 __host__ __device__ constexpr int align_smem_ints(int E) { return (3 + kAlignWarps) * E + 4; }
 
 // ids: M*k expert ids (global or shared memory); outputs may be NULL except npad.
 // Requires blockDim.x == kAlignThreads and every thread of the CTA to call it.
+// n rounded up to a multiple of b (mask arithmetic when b is a power of two).
+__device__ __forceinline__ int pad_to(int n, int b) {
+    return (b & (b - 1)) == 0 ? (n + b - 1) & ~(b - 1) : (n + b - 1) / b * b;
+}
+
 __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, int b, int rsub,
                                   int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
                                   SubBlock *sbt, int32_t *status, int32_t *sm) {
@@ -62,7 +69,7 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
         const int per = (E + 31) / 32;
         const int e0 = lane * per, e1 = min(E, e0 + per);
         int s = 0;
-        for (int e = e0; e < e1; ++e) s += (cnt[e] + b - 1) / b * b;
+        for (int e = e0; e < e1; ++e) s += pad_to(cnt[e], b);
         int incl = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -72,12 +79,18 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
         int run = incl - s;
         for (int e = e0; e < e1; ++e) {
             off[e] = run;
-            run += (cnt[e] + b - 1) / b * b;
+            run += pad_to(cnt[e], b);
         }
         if (lane == 31) misc[0] = incl;
     }
     __syncthreads();
     const int total = misc[0];
+    // Every row starts as a sentinel (coalesced, all threads); the scatter below overwrites
+    // the rows of valid routes, so the padding rows and the tail need no per-expert loops.
+    if (sorted) {
+        for (int64_t pos = tid; pos < cap; pos += kAlignThreads) sorted[pos] = sentinel;
+        __syncthreads();
+    }
 
     // (3) stable scatter in ascending route id
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -113,14 +126,11 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
         __syncthreads();
     }
 
-    // (4) padding rows, block vector, sub-block records, tail
+    // (4) block vector, sub-block records, tail of the block vector
     for (int e = tid; e < E; e += kAlignThreads) {
         const int n = cnt[e];
         if (n == 0) continue;
-        const int padded = (n + b - 1) / b * b;
-        if (sorted)
-            for (int q = n; q < padded; ++q)
-                if (off[e] + q < cap) sorted[off[e] + q] = sentinel;
+        const int padded = pad_to(n, b);
         if (blocks)
             for (int q = 0; q < padded / b; ++q) blocks[off[e] / b + q] = e;
         if (sbt)
@@ -133,8 +143,6 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
                 for (int q = ntok; q < kNT; ++q) rec->routes[q] = rec->tokens[q] = -1;
             }
     }
-    if (sorted)
-        for (int64_t pos = (int64_t)total + tid; pos < cap; pos += kAlignThreads) sorted[pos] = sentinel;
     if (blocks)
         for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += kAlignThreads) blocks[q] = -1;
     if (tid == 0) {
@@ -170,9 +178,12 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
                     lower += q < tid;
                 }
     }
-    const int padded = valid ? (n + b - 1) / b * b : 0;
+    const int padded = valid ? pad_to(n, b) : 0;
     const bool leader = valid && lower == 0;
     pub[tid] = leader ? padded : 0;
+    // every row starts as a sentinel; the routes' rows are written after the barrier
+    if (sorted)
+        for (int64_t pos = tid; pos < cap; pos += nthr) sorted[pos] = sentinel;
     const int any_invalid = __syncthreads_or(tid < R && !valid);
 
     int off = 0, total = 0;
@@ -193,9 +204,6 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
         }
     }
     if (leader) {
-        if (sorted)
-            for (int q = n; q < padded; ++q)
-                if (off + q < cap) sorted[off + q] = sentinel;
         if (blocks)
             for (int q = 0; q < padded / b; ++q) blocks[off / b + q] = e;
         if (sbt)
@@ -208,8 +216,6 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
                 for (int q = ntok; q < kNT; ++q) rec->routes[q] = rec->tokens[q] = -1;
             }
     }
-    if (sorted)
-        for (int64_t pos = (int64_t)total + tid; pos < cap; pos += nthr) sorted[pos] = sentinel;
     if (blocks)
         for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += nthr) blocks[q] = -1;
     if (tid == 0) {
