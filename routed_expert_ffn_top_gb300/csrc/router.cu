@@ -35,6 +35,13 @@ struct FusedAlign {
     int32_t *status;
 };
 
+// Passes over a CTA's W_r slice of HS rows: one when the slice fits kRouterPassBytes, else
+// two (the supported shapes keep the slice within 2 kRouterPassBytes).
+constexpr int kRouterPassBytes = 64 * 1024;
+__host__ __device__ inline int router_passes(int HS, int E) {
+    return (HS * E * 2 > kRouterPassBytes) ? 2 : 1;
+}
+
 // Generic address of `p` (a shared variable of this CTA) in CTA `rank` of the cluster.
 template <typename T>
 __device__ __forceinline__ T *cluster_peer_mut(T *p, uint32_t rank) {
@@ -66,12 +73,20 @@ __global__ void __launch_bounds__(kRouterThreads)
     const int npairs = E / 2;
     const int RG = kRouterThreads / npairs;  // row groups (>= 1 since E <= 512)
 
-    // shared layout: w_s [HS][E] bf16 | x_s [TM][HS] bf16 | red [RG][TM][E] f32 |
+    // W_r rows of this CTA stream through shared memory in npass passes of HP rows (one
+    // pass when the slice is at most kRouterPassBytes), so that two CTAs fit on an SM at
+    // every supported shape.  Row group g of pass p is rows p*HP + [g*HP/RG, (g+1)*HP/RG);
+    // a thread sums its rows in ascending order over the passes.  The split depends on
+    // (H, E) only, never on M.
+    const int npass = router_passes(HS, E);
+    const int HP = HS / npass;
+
+    // shared layout: w_s [HP][E] bf16 | x_s [TM][HS] bf16 | red [RG][TM][E] f32 |
     //                gath [8][E] f32 (this CTA's token: the partial logits of every rank) |
     //                ids_s [8 * 32] | bar | align scratch
     unsigned char *ptr = smem_raw;
     __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(ptr);
-    ptr += (size_t)HS * E * 2;
+    ptr += (size_t)HP * E * 2;
     __nv_bfloat16 *x_s = reinterpret_cast<__nv_bfloat16 *>(ptr);
     ptr += (size_t)TM * HS * 2;
     float *red = reinterpret_cast<float *>(ptr);
@@ -84,7 +99,8 @@ __global__ void __launch_bounds__(kRouterThreads)
     ptr += 16;
     int32_t *align_sm = reinterpret_cast<int32_t *>(ptr);
 
-    const uint32_t w_bytes = (uint32_t)HS * E * 2;
+    const uint32_t w_bytes = (uint32_t)HP * E * 2;
+    const __nv_bfloat16 *w_cta = wr + (size_t)rank * HS * E;
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -92,7 +108,7 @@ __global__ void __launch_bounds__(kRouterThreads)
     __syncthreads();
     if (tid == 0) {
         mbar_arrive_expect_tx(bar, w_bytes);
-        bulk_load(w_s, wr + (size_t)rank * HS * E, w_bytes, bar);
+        bulk_load(w_s, w_cta, w_bytes, bar);
     }
     pdl_wait();  // h may come from the previous kernel in the stream
     pdl_launch_dependents();
@@ -107,19 +123,30 @@ __global__ void __launch_bounds__(kRouterThreads)
         *reinterpret_cast<uint4 *>(x_s + (size_t)t * HS + pc * 8) = v;
     }
     __syncthreads();
-    const bool ok = mbar_wait_bounded(bar, 0);
 
     const int pair = tid % npairs, rg = tid / npairs;
-    if (ok && rg < RG) {
-        const int r0 = rg * HS / RG, r1 = (rg + 1) * HS / RG;
-        float acc0[TM], acc1[TM];
+    float acc0[TM], acc1[TM];
 #pragma unroll
-        for (int t = 0; t < TM; ++t) acc0[t] = acc1[t] = 0.0f;
-        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(w_s) + pair;
-        const uint32_t *x32 = reinterpret_cast<const uint32_t *>(x_s);
+    for (int t = 0; t < TM; ++t) acc0[t] = acc1[t] = 0.0f;
+    const uint32_t *wrow = reinterpret_cast<const uint32_t *>(w_s) + pair;
+    const uint32_t *x32 = reinterpret_cast<const uint32_t *>(x_s);
+    bool ok = true;
+    for (int pass = 0; pass < npass; ++pass) {
+        if (pass > 0) {
+            __syncthreads();  // every thread is done with the previous pass's rows
+            if (tid == 0 && ok) {  // (after a wait that gave up, no further copy is issued)
+                mbar_arrive_expect_tx(bar, w_bytes);
+                bulk_load(w_s, w_cta + (size_t)pass * HP * E, w_bytes, bar);
+            }
+        }
+        ok = ok && mbar_wait_bounded(bar, (uint32_t)pass & 1u);
+        if (!ok || rg >= RG) continue;
+        const int base = pass * HP;  // first row of the pass within the CTA's slice
+        const int r0 = base + rg * HP / RG, r1 = base + (rg + 1) * HP / RG;
         int r = r0;
         for (; r + 1 < r1 && (r & 1) == 0; r += 2) {  // two rows per step (one bf16 pair of h)
-            const uint32_t wa = wrow[(size_t)r * npairs], wb = wrow[(size_t)(r + 1) * npairs];
+            const uint32_t wa = wrow[(size_t)(r - base) * npairs];
+            const uint32_t wb = wrow[(size_t)(r + 1 - base) * npairs];
 #pragma unroll
             for (int t = 0; t < TM; ++t) {
                 const uint32_t xv = x32[((size_t)t * HS + r) >> 1];
@@ -130,7 +157,7 @@ __global__ void __launch_bounds__(kRouterThreads)
             }
         }
         for (; r < r1; ++r) {  // an odd tail row (row groups of odd length)
-            const uint32_t wa = wrow[(size_t)r * npairs];
+            const uint32_t wa = wrow[(size_t)(r - base) * npairs];
 #pragma unroll
             for (int t = 0; t < TM; ++t) {
                 const uint32_t xv = x32[((size_t)t * HS + r) >> 1];
@@ -143,6 +170,8 @@ __global__ void __launch_bounds__(kRouterThreads)
                 }
             }
         }
+    }
+    if (ok && rg < RG) {
 #pragma unroll
         for (int t = 0; t < TM; ++t) {
             red[((size_t)rg * TM + t) * E + 2 * pair] = acc0[t];
@@ -251,7 +280,7 @@ __global__ void __launch_bounds__(kRouterThreads)
 static size_t router_smem(int TM, int H, int E, bool fuse) {
     const int HS = H / kRouterCluster;
     const int RG = kRouterThreads / (E / 2);
-    return (size_t)HS * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
+    return (size_t)(HS / router_passes(HS, E)) * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
            (size_t)kRouterCluster * E * 4 + 8 * 32 * 4 + 16 +
            (fuse ? (size_t)align_small_smem_ints(kRouterThreads) * 4 : 0);
 }
