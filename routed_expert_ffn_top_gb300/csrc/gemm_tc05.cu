@@ -128,8 +128,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmArgs a) {
                              blk * (int64_t)nchunk * kGChunkBytes;
         const int j = lane & 7;
         const uint32_t off = tile_offset(n, j);
-        for (int c = lane >> 3; c < nchunk; c += 4)
-            *reinterpret_cast<uint4 *>(dst + (int64_t)c * kGChunkBytes + off) = src[c * 8 + j];
+        // 8 pieces per lane in flight at once (chunks c, c+4, ..., c+28), then their stores
+        for (int c0 = lane >> 3; c0 < nchunk; c0 += 32) {
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (c0 + 4 * i < nchunk) v[i] = src[(c0 + 4 * i) * 8 + j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (c0 + 4 * i < nchunk)
+                    *reinterpret_cast<uint4 *>(dst + (int64_t)(c0 + 4 * i) * kGChunkBytes + off) = v[i];
+        }
     }
 }
 
