@@ -37,6 +37,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
 
 W_DENSE = 0
 W_VQ = 1
+W_VQLR = 2
 
 _lock = threading.RLock()
 _lib = None
@@ -66,6 +67,9 @@ class _Weights(ctypes.Structure):
         ("cb_gate", ctypes.c_void_p), ("cb_up", ctypes.c_void_p),
         ("d", ctypes.c_int), ("K", ctypes.c_int),
         ("w_down", ctypes.c_void_p),
+        ("d_gate", ctypes.c_void_p), ("d_up", ctypes.c_void_p),
+        ("c_gate", ctypes.c_void_p), ("c_up", ctypes.c_void_p),
+        ("r", ctypes.c_int),
     ]
 
 
@@ -198,6 +202,11 @@ def _weights_struct(w, keep):
     s.cb_gate = put("cb_gate", w.get("cb_gate"), _bits)
     s.cb_up = put("cb_up", w.get("cb_up"), _bits)
     s.w_down = put("w_down", w.get("w_down"), _bits)
+    s.d_gate = put("d_gate", w.get("d_gate"), _bits)
+    s.d_up = put("d_up", w.get("d_up"), _bits)
+    s.c_gate = put("c_gate", w.get("c_gate"), _bits)
+    s.c_up = put("c_up", w.get("c_up"), _bits)
+    s.r = w.get("r", 0) or 0
     return s
 
 

@@ -40,7 +40,10 @@
  *     and it contributes nothing to the output;
  *   - padding rows carry the sentinel value M*k; an expert with no route gets no block;
  *     rows past num_padded are sentinels and block entries past the last block are -1;
- *   - VQ (d-length column blocks along H): W[e][d*q + t][i] = B[J[e][q][i]][t].
+ *   - VQ (d-length column blocks along H): W[e][d*q + t][i] = B[J[e][q][i]][t];
+ *   - VQ+LR (the hybrid representation; the page's Eq. (1) is garbled, its text describes a
+ *     sum): per projection W_e = Q_B(J_e) + D C_e, with D [H, r] shared by all experts of the
+ *     layer and projection and C_e [r, I] private to the expert; down stays dense bf16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -220,9 +223,10 @@ int oracle_align(const int32_t *topk_ids, int M, int k, int E, int b,
 /* Weight representations for the gate/up projections. */
 #define ORACLE_W_DENSE 0
 #define ORACLE_W_VQ 1
+#define ORACLE_W_VQLR 2
 
 typedef struct {
-    int kind;                 /* ORACLE_W_DENSE or ORACLE_W_VQ */
+    int kind;                 /* ORACLE_W_DENSE, ORACLE_W_VQ or ORACLE_W_VQLR */
     int H, I, E;
     const uint16_t *w_gate;   /* dense: [E,H,I] bf16 */
     const uint16_t *w_up;     /* dense: [E,H,I] bf16 */
@@ -232,6 +236,11 @@ typedef struct {
     const uint16_t *cb_up;    /* VQ: [K,d] bf16 code book, layer-shared */
     int d, K;
     const uint16_t *w_down;   /* [E,I,H] bf16 */
+    const uint16_t *d_gate;   /* VQ+LR: [H,r] bf16 low-rank basis, layer-shared */
+    const uint16_t *d_up;     /* VQ+LR: [H,r] bf16 */
+    const uint16_t *c_gate;   /* VQ+LR: [E,r,I] bf16 low-rank coefficients, per expert */
+    const uint16_t *c_up;     /* VQ+LR: [E,r,I] bf16 */
+    int r;
 } oracle_weights_t;
 
 /*
@@ -258,6 +267,37 @@ static void accumulate_row(const oracle_weights_t *w, const uint16_t *dense, con
 }
 
 /*
+ * Low-rank half of the hybrid gate/up representation [MED, the hybrid-representation
+ * paragraph around its Eq. (1), and "Reuse of shared projections"]: each projection's weight is
+ * W_e = Q_B(J_e) + D C_e with the layer-shared basis D [H, r] and the expert's coefficients
+ * C_e [r, I], so h^T W_e = h^T Q_B(J_e) + (D^T h)^T C_e.  The product is taken in that
+ * factored order: z = D^T h once per token and projection, then acc[i] += sum_rho z[rho]
+ * C_e[rho][i] (the same value as h^T (D C_e) in exact arithmetic).
+ */
+static void add_low_rank(const oracle_weights_t *w, const uint16_t *hrow, int e, double *zg,
+                         double *zu, double *g, double *u)
+{
+    const int H = w->H, I = w->I, R = w->r;
+    for (int rho = 0; rho < R; ++rho)
+        zg[rho] = zu[rho] = 0.0;
+    for (int hh = 0; hh < H; ++hh) {
+        const double x = bf16_bits_to_double(hrow[hh]);
+        for (int rho = 0; rho < R; ++rho) {
+            zg[rho] += x * bf16_bits_to_double(w->d_gate[(size_t)hh * R + rho]);
+            zu[rho] += x * bf16_bits_to_double(w->d_up[(size_t)hh * R + rho]);
+        }
+    }
+    for (int rho = 0; rho < R; ++rho) {
+        const uint16_t *cg = w->c_gate + ((size_t)e * R + rho) * I;
+        const uint16_t *cu = w->c_up + ((size_t)e * R + rho) * I;
+        for (int i = 0; i < I; ++i) {
+            g[i] += zg[rho] * bf16_bits_to_double(cg[i]);
+            u[i] += zu[rho] * bf16_bits_to_double(cu[i]);
+        }
+    }
+}
+
+/*
  * Expert FFN and weighted combine [MED, MoE block background, stage-3 activation, Section
  * 4.3; CSM, channel view]:
  *   g = h W_gate[e], u = h W_up[e], p = silu(g) * u, y = p W_down[e],
@@ -277,9 +317,12 @@ int oracle_expert_ffn(const uint16_t *h, const oracle_weights_t *w, int M, int k
     if (w->kind == ORACLE_W_DENSE) {
         if (!w->w_gate || !w->w_up)
             return ORACLE_ERR_ARG;
-    } else if (w->kind == ORACLE_W_VQ) {
+    } else if (w->kind == ORACLE_W_VQ || w->kind == ORACLE_W_VQLR) {
         if (!w->j_gate || !w->j_up || !w->cb_gate || !w->cb_up || w->d <= 0 || w->K <= 0 ||
             w->H % w->d != 0)
+            return ORACLE_ERR_ARG;
+        if (w->kind == ORACLE_W_VQLR &&
+            (!w->d_gate || !w->d_up || !w->c_gate || !w->c_up || w->r <= 0))
             return ORACLE_ERR_ARG;
     } else {
         return ORACLE_ERR_ARG;
@@ -289,8 +332,11 @@ int oracle_expert_ffn(const uint16_t *h, const oracle_weights_t *w, int M, int k
     double *u = (double *)malloc(sizeof(double) * (size_t)I);
     double *p = (double *)malloc(sizeof(double) * (size_t)I);
     double *y = (double *)malloc(sizeof(double) * (size_t)H);
-    if (!g || !u || !p || !y) {
-        free(g); free(u); free(p); free(y);
+    const int R = w->kind == ORACLE_W_VQLR ? w->r : 0;
+    double *zg = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+    double *zu = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+    if (!g || !u || !p || !y || !zg || !zu) {
+        free(g); free(u); free(p); free(y); free(zg); free(zu);
         return ORACLE_ERR_NOMEM;
     }
     for (int m = 0; m < M; ++m) {
@@ -314,6 +360,8 @@ int oracle_expert_ffn(const uint16_t *h, const oracle_weights_t *w, int M, int k
                 accumulate_row(w, w->w_gate, w->j_gate, w->cb_gate, e, hh, x, g);
                 accumulate_row(w, w->w_up, w->j_up, w->cb_up, e, hh, x, u);
             }
+            if (R > 0)
+                add_low_rank(w, h + (size_t)m * H, e, zg, zu, g, u);
             for (int i = 0; i < I; ++i)
                 p[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
             for (int n = 0; n < H; ++n)
@@ -331,7 +379,7 @@ int oracle_expert_ffn(const uint16_t *h, const oracle_weights_t *w, int M, int k
                 memcpy(y_out + r * H, y, sizeof(double) * (size_t)H);
         }
     }
-    free(g); free(u); free(p); free(y);
+    free(g); free(u); free(p); free(y); free(zg); free(zu);
     return ORACLE_OK;
 }
 

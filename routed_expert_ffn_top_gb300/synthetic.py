@@ -13,7 +13,9 @@ with the run seed, so any tensor can be regenerated alone):
 * router W_r ~ N(0, 0.02) bf16 [H, E]; optional per-expert router bias ~ N(0, 1) fp32 [E];
 * dense W_gate, W_up ~ N(0, 0.02) bf16 [E, H, I]; W_down ~ N(0, 0.02) bf16 [E, I, H];
 * blockwise VQ gate/up: index maps J uniform in [0, K) uint8 [E, H/d, I]; layer-shared code
-  books ~ N(0, 0.02) bf16 [K, d] (one for gate, one for up); down stays dense bf16.
+  books ~ N(0, 0.02) bf16 [K, d] (one for gate, one for up); down stays dense bf16;
+* VQ + low-rank gate/up: the VQ tensors above plus, per projection, a layer-shared basis
+  D ~ N(0, 0.02) bf16 [H, r] and per-expert coefficients C ~ N(0, 0.02) bf16 [E, r, I].
 """
 from __future__ import annotations
 
@@ -26,6 +28,7 @@ import torch
 
 W_DENSE = 0
 W_VQ = 1
+W_VQLR = 2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -40,6 +43,7 @@ class Workload:
     kind: int = W_DENSE
     d: int = 4
     K: int = 256
+    r: int = 0
     router_bias: bool = False
     layers: int = 1
     residual: bool = False
@@ -56,6 +60,8 @@ WORKLOADS = {
     "stack48": Workload("stack48", H=2048, I=768, E=128, k=8, b=8, M=1, layers=48,
                         residual=True),
     "vq_d4": Workload("vq_d4", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=4, K=256),
+    "vqlr_d4_r256": Workload("vqlr_d4_r256", H=2048, I=768, E=128, k=8, b=8, M=1,
+                             kind=W_VQLR, d=4, K=256, r=256),
     "large_m256": Workload("large_m256", H=4096, I=1536, E=128, k=8, b=64, M=256,
                            router_bias=True),
 }
@@ -93,7 +99,7 @@ def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu") -> dic
     """All parameters of one MoE layer as torch tensors on ``device``."""
     H, I, E = wl.H, wl.I, wl.E
     s = lambda t: sub_seed(seed, wl.name, layer, t)  # noqa: E731
-    p = {"kind": wl.kind, "H": H, "I": I, "E": E, "d": wl.d, "K": wl.K}
+    p = {"kind": wl.kind, "H": H, "I": I, "E": E, "d": wl.d, "K": wl.K, "r": wl.r}
     p["w_router"] = _normal_bf16((H, E), wl.w_std, device, s("w_router"))
     if wl.router_bias:
         p["bias"] = torch.randn(E, generator=_gen(device, s("bias")), device=device,
@@ -112,6 +118,11 @@ def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu") -> dic
                                   device=device, dtype=torch.int32).to(torch.uint8)
         p["cb_gate"] = _normal_bf16((wl.K, wl.d), wl.w_std, device, s("cb_gate"))
         p["cb_up"] = _normal_bf16((wl.K, wl.d), wl.w_std, device, s("cb_up"))
+    if wl.kind == W_VQLR:
+        p["d_gate"] = _normal_bf16((H, wl.r), wl.w_std, device, s("d_gate"))
+        p["d_up"] = _normal_bf16((H, wl.r), wl.w_std, device, s("d_up"))
+        p["c_gate"] = _normal_bf16((E, wl.r, I), wl.w_std, device, s("c_gate"))
+        p["c_up"] = _normal_bf16((E, wl.r, I), wl.w_std, device, s("c_up"))
     p["w_down"] = _normal_bf16((E, I, H), wl.w_std, device, s("w_down"))
     return p
 
@@ -147,5 +158,11 @@ def oracle_weights(layer: dict, experts=None) -> dict:
         w["j_up"] = sel(layer["j_up"]).cpu().numpy()
         w["cb_gate"] = bits(layer["cb_gate"])
         w["cb_up"] = bits(layer["cb_up"])
+    if layer["kind"] == W_VQLR:
+        w["r"] = layer["r"]
+        w["d_gate"] = bits(layer["d_gate"])
+        w["d_up"] = bits(layer["d_up"])
+        w["c_gate"] = bits(sel(layer["c_gate"]))
+        w["c_up"] = bits(sel(layer["c_up"]))
     w["w_down"] = bits(sel(layer["w_down"]))
     return w

@@ -66,6 +66,12 @@ def dense_numpy(layer):
         # W[e, d*q + t, i] = B[J[e, q, i], t]: gather the code words, then move t next to q.
         wg = cbg[jg].transpose(0, 1, 3, 2).reshape(E, Q * d, I)
         wu = cbu[ju].transpose(0, 1, 3, 2).reshape(E, Q * d, I)
+        if layer["kind"] == syn.W_VQLR:
+            # the low-rank half materialised: D [H, r] times C_e [r, I], per expert
+            dg, du = f64(syn.bits(layer["d_gate"])), f64(syn.bits(layer["d_up"]))
+            cg, cu = f64(syn.bits(layer["c_gate"])), f64(syn.bits(layer["c_up"]))
+            wg = wg + np.einsum("hr,eri->ehi", dg, cg)
+            wu = wu + np.einsum("hr,eri->ehi", du, cu)
     wd = f64(syn.bits(layer["w_down"]))
     return wg, wu, wd
 
@@ -466,6 +472,85 @@ def pin_vq_constant_index_is_dense():
     ref = np.stack([(silu(x[m] @ wg[ids[m, 0]]) * (x[m] @ wu[ids[m, 0]])) @ wd[ids[m, 0]]
                     for m in range(2)])
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------------------------- VQ + LR
+def vqlr_workload(**kw):
+    base = dict(name="pin_vqlr", H=32, I=12, E=5, k=2, b=4, M=3, kind=syn.W_VQLR, d=4, K=16, r=6)
+    base.update(kw)
+    return syn.Workload(**base)
+
+
+def pin_vqlr_equals_materialised_dense():
+    # "A Multi-Engine Dataflow ...", hybrid representation (text around its Eq. (1)):
+    # W_e = Q_B(J_e) + D C_e.  The oracle multiplies in the factored order (D^T h first); the
+    # reference materialises W_e in numpy (einsum) and multiplies h by it directly.
+    wl = vqlr_workload()
+    layer, h = small_layer(wl, seed=21)
+    wg, wu, wd = dense_numpy(layer)
+    x = f64(syn.bits(h))
+    ids = np.array([[0, 4], [3, 1], [2, 0]], np.int32)
+    a = np.array([[0.6, 0.4], [0.5, 0.5], [0.25, 0.75]])
+    ref = np.zeros((wl.M, wl.H))
+    for m in range(wl.M):
+        for j in range(wl.k):
+            e = ids[m, j]
+            ref[m] += a[m, j] * ((silu(x[m] @ wg[e]) * (x[m] @ wu[e])) @ wd[e])
+    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    assert np.allclose(out, ref, rtol=1e-11, atol=1e-13)
+
+
+def pin_vqlr_zero_coefficients_is_vq():
+    # C_e = 0 removes the low-rank half exactly: the result is the VQ-only block, bit for bit.
+    wl = vqlr_workload(E=3, M=2, r=5)
+    layer, h = small_layer(wl, seed=22)
+    layer = dict(layer)
+    layer["c_gate"] = torch.zeros_like(layer["c_gate"])
+    layer["c_up"] = torch.zeros_like(layer["c_up"])
+    vq = dict(layer)
+    vq["kind"] = syn.W_VQ
+    ids = np.array([[2, 0], [1, 2]], np.int32)
+    a = np.array([[0.3, 0.7], [0.8, 0.2]])
+    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out_vq = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(vq), ids, a)
+    assert np.array_equal(out, out_vq)
+
+
+def pin_vqlr_zero_codebook_is_low_rank_swiglu():
+    # All code words zero: the expert is the textbook low-rank SwiGLU
+    # (silu(h D_g C_g) * (h D_u C_u)) W_down, computed here with numpy matmuls.
+    wl = vqlr_workload(E=2, M=2, H=24, I=10, r=4, k=1)
+    layer, h = small_layer(wl, seed=23)
+    layer = dict(layer)
+    layer["cb_gate"] = torch.zeros_like(layer["cb_gate"])
+    layer["cb_up"] = torch.zeros_like(layer["cb_up"])
+    x = f64(syn.bits(h))
+    dg, du = f64(syn.bits(layer["d_gate"])), f64(syn.bits(layer["d_up"]))
+    cg, cu = f64(syn.bits(layer["c_gate"])), f64(syn.bits(layer["c_up"]))
+    wd = f64(syn.bits(layer["w_down"]))
+    ids = np.array([[1], [0]], np.int32)
+    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, np.ones((2, 1)))
+    ref = np.stack([(silu((x[m] @ dg) @ cg[ids[m, 0]]) * ((x[m] @ du) @ cu[ids[m, 0]]))
+                    @ wd[ids[m, 0]] for m in range(2)])
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
+
+
+def pin_vqlr_projections_are_separate():
+    # Gate and up keep their own basis and coefficients: swapping the up pair for the gate
+    # pair makes u equal g, so p = silu(g) * g, checked against that closed form.
+    wl = vqlr_workload(E=2, M=1, H=16, I=6, r=3, k=1)
+    layer, h = small_layer(wl, seed=24)
+    layer = dict(layer)
+    layer["d_up"] = layer["d_gate"].clone()
+    layer["c_up"] = layer["c_gate"].clone()
+    layer["j_up"] = layer["j_gate"].clone()
+    layer["cb_up"] = layer["cb_gate"].clone()
+    wg, _, wd = dense_numpy(layer)
+    x = f64(syn.bits(h))
+    ids = np.array([[1]], np.int32)
+    g = x[0] @ wg[1]
+    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, np.ones((1, 1)))
+    assert np.allclose(out[0], (silu(g) * g) @ wd[1], rtol=1e-12, atol=1e-14)
 
 
 # -------------------------------------------------------------------------- whole block

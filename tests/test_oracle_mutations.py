@@ -47,6 +47,14 @@ MUTANTS = [
     ("routes_descending", [("for (int64_t r = 0; r < R; ++r) {\n            if (topk_ids[r] == e)",
                             "for (int64_t r = R - 1; r >= 0; --r) {\n            if (topk_ids[r] == e)")]),
     ("tail_blocks_zero", [("expert_block_ids[q] = -1;", "expert_block_ids[q] = 0;")]),
+    ("low_rank_dropped", [("                add_low_rank(w, h + (size_t)m * H, e, zg, zu, g, u);",
+                           "                (void)zg;")]),
+    ("low_rank_basis_permuted", [("zg[rho] += x * bf16_bits_to_double(w->d_gate[(size_t)hh * R + rho]);",
+                                    "zg[rho] += x * bf16_bits_to_double(w->d_gate[(size_t)(hh % R) * R + (rho * 7 + hh) % R]);")]),
+    ("low_rank_gate_basis_for_up", [("zu[rho] += x * bf16_bits_to_double(w->d_up[(size_t)hh * R + rho]);",
+                                     "zu[rho] += x * bf16_bits_to_double(w->d_gate[(size_t)hh * R + rho]);")]),
+    ("low_rank_wrong_expert", [("const uint16_t *cg = w->c_gate + ((size_t)e * R + rho) * I;",
+                                "const uint16_t *cg = w->c_gate + ((size_t)((e + 1) % w->E) * R + rho) * I;")]),
 ]
 
 
