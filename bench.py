@@ -218,8 +218,18 @@ def expert_bytes(wl):
     if wl.kind == syn.W_DENSE:
         gu = 2 * wl.H * wl.I * 2
     else:
-        gu = 2 * (wl.H // wl.d) * wl.I
+        gu = 2 * (wl.H // wl.d) * wl.I          # uint8 index maps of gate and up
+        if wl.kind == syn.W_VQLR:
+            gu += 2 * wl.r * wl.I * 2          # bf16 low-rank coefficients C_gate, C_up
     return gu, wl.I * wl.H * 2
+
+
+def shared_bytes(wl):
+    """Layer-shared weights read once per block: the router (and the low-rank bases)."""
+    b = wl.H * wl.E * 2
+    if wl.kind == syn.W_VQLR:
+        b += 2 * wl.H * wl.r * 2
+    return b
 
 
 # ------------------------------------------------------------------------------ ours
@@ -357,7 +367,7 @@ def run_ours(args, world, rank, local):
         step_bytes = sum(per_set_unique) * (gu_b + dn_b)
     else:
         step_bytes = statistics.mean(per_set_unique[i % n_sets] for i in range(args.steps)) * (gu_b + dn_b)
-    router_bytes = wl.H * wl.E * 2 * blocks_per_step
+    router_bytes = shared_bytes(wl) * blocks_per_step
     hbm_gbs = (step_bytes + router_bytes) / (ms_per_step * 1e-3) / 1e9
     us_per_layer = ms_per_step * 1e3 / blocks_per_step
 

@@ -68,15 +68,22 @@ typedef enum moe_status {
 /* Weight representations of the gate/up projections. */
 #define MOE_W_DENSE_BF16 0
 #define MOE_W_VQ_GATEUP  1
+#define MOE_W_VQLR_GATEUP 2
 
 /*
  * One MoE layer's expert weights (all device pointers).
  *   kind == MOE_W_DENSE_BF16: w_gate, w_up [E,H,I] bf16 (row h of expert e holds I
- *     contiguous values); j_*, cb_* unused.
+ *     contiguous values); j_*, cb_*, d_*, c_* unused.
  *   kind == MOE_W_VQ_GATEUP: j_gate, j_up [E,H/d,I] uint8 index maps (expert-private);
  *     cb_gate, cb_up [K,d] bf16 code books (layer-shared), W[e][d*q+t][i] =
  *     cb[J[e][q][i]][t]; w_gate, w_up unused.
- *   w_down [E,I,H] bf16 in both cases (the down projection stays dense).
+ *   kind == MOE_W_VQLR_GATEUP: the VQ fields above plus a low-rank term per projection
+ *     ("A Multi-Engine Dataflow ...", the hybrid representation around its Eq. (1)):
+ *     W_e = Q_B(J_e) + D C_e with d_gate, d_up [H,r] bf16 (layer-shared basis) and c_gate,
+ *     c_up [E,r,I] bf16 (expert-private coefficients).  z = D^T h is computed once per
+ *     token and projection (in the router's launch), then accumulated with the VQ sum.
+ *   w_down [E,I,H] bf16 in every case (the down projection stays dense).
+ * Fields after w_down were added for MOE_W_VQLR_GATEUP; zero them for the other kinds.
  */
 typedef struct moe_expert_weights {
     int32_t kind;
@@ -89,6 +96,11 @@ typedef struct moe_expert_weights {
     const void *cb_up;
     int32_t d, K;
     const void *w_down;
+    const void *d_gate;
+    const void *d_up;
+    const void *c_gate;
+    const void *c_up;
+    int32_t r;
 } moe_expert_weights_t;
 
 /* A short static description of a status code (never NULL). */

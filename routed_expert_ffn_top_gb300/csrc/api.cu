@@ -46,6 +46,7 @@ WsLayout ws_layout(const Dims &d) {
     L.sbt = take((size_t)d.max_sub * sizeof(SubBlock));
     L.p = take((size_t)d.R * d.I * 4);
     L.y = take((size_t)d.R * d.H * 4);
+    L.z = take((size_t)d.M * 2 * d.r * 4);
     const size_t tile_rows = (d.b == kGemmBlock) ? (size_t)(d.cap / kGemmBlock) * kGemmBlock : 0;
     L.x_tiles = take(tile_rows * d.H * 2);
     L.p_tiles = take(tile_rows * d.I * 2);
@@ -120,6 +121,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// 3-D row-major bf16 tensor [d2][d1][d0], box [b2][b1][b0], no swizzle; out-of-range box
+// elements read as zeros.
+static bool make_tmap_3d_bf16(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1,
+                              uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D row-major tensor [outer][inner] of `elem` bytes, box [box_outer][box_inner].
 static bool make_tmap_2d(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int elem,
                          uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
@@ -192,16 +208,28 @@ static int check_weights(const moe_expert_weights_t *w) {
             return MOE_ERR_INVALID_ARG;
         return MOE_OK;
     }
-    if (w->kind == MOE_W_VQ_GATEUP) {
+    if (w->kind == MOE_W_VQ_GATEUP || w->kind == MOE_W_VQLR_GATEUP) {
         if (!w->j_gate || !w->j_up || !w->cb_gate || !w->cb_up) return MOE_ERR_INVALID_ARG;
         if (!aligned(w->j_gate, 16) || !aligned(w->j_up, 16) || !aligned(w->cb_gate, 16) ||
             !aligned(w->cb_up, 16))
             return MOE_ERR_INVALID_ARG;
         if (w->d != 4 || w->K != 256) return MOE_ERR_UNSUPPORTED;
         if (w->H % (4 * kBoxRows) != 0) return MOE_ERR_UNSUPPORTED;  // 1024-row index boxes
+        if (w->kind == MOE_W_VQ_GATEUP) return MOE_OK;
+        if (!w->d_gate || !w->d_up || !w->c_gate || !w->c_up || !aligned(w->d_gate, 16) ||
+            !aligned(w->d_up, 16) || !aligned(w->c_gate, 16) || !aligned(w->c_up, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (w->r <= 0) return MOE_ERR_INVALID_ARG;
+        // r in multiples of 128 up to 512 (the router's column split; 256-row boxes of C)
+        if (w->r % 128 != 0 || w->r > 512) return MOE_ERR_UNSUPPORTED;
         return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;
+}
+
+// Rank of the low-rank term (0 unless the weights are VQ + low rank).
+static int lr_rank(const moe_expert_weights_t *w) {
+    return (w && w->kind == MOE_W_VQLR_GATEUP) ? w->r : 0;
 }
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -230,7 +258,7 @@ extern "C" int moe_route_topk(const void *h, const void *w_router, const float *
         return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_router(static_cast<const __nv_bfloat16 *>(h),
                                      static_cast<const __nv_bfloat16 *>(w_router), bias, M, H, E, k,
-                                     renormalize, topk_ids, topk_weights,
+                                     renormalize, topk_ids, topk_weights, nullptr,
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -261,10 +289,24 @@ extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int 
     if (!w || M < 0 || k <= 0 || k > 32 || k > w->E || check_block(b) != MOE_OK) return 0;
     if (w->H <= 0 || w->I <= 0 || w->E <= 0) return 0;
     if ((int64_t)M * k >= (1 << 24)) return 0;
-    return ws_layout(make_dims(M, k, w->E, w->H, w->I, b)).total;
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    d.r = lr_rank(w);
+    return ws_layout(d).total;
 }
 
 // Runs gate/up and down for aligned routes (alignment pointers already resolved).
+// The low-rank projections of VQ + low-rank weights (z in the workspace), or NULL.
+static const LowRankProj *lowrank_proj(const moe_expert_weights_t *w, const Dims &d,
+                                       unsigned char *ws, const WsLayout &L, LowRankProj *out) {
+    if (w->kind != MOE_W_VQLR_GATEUP) return nullptr;
+    out->d_gate = static_cast<const __nv_bfloat16 *>(w->d_gate);
+    out->d_up = static_cast<const __nv_bfloat16 *>(w->d_up);
+    out->r = d.r;
+    out->first = 0;
+    out->z = reinterpret_cast<float *>(ws + L.z);
+    return out;
+}
+
 // The large-batch regime: tcgen05 grouped GEMMs over the 64-row aligned blocks, then the
 // fixed-order combine.
 static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
@@ -329,7 +371,14 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     if (gemm_regime(w->kind, d.b))
         return run_gemm(h, w, d, topk_ids, topk_weights, sorted, blocks, npad, residual, out, ws,
                         L, stream);
-    const bool vq = w->kind == MOE_W_VQ_GATEUP;
+    const bool vq = w->kind == MOE_W_VQ_GATEUP || w->kind == MOE_W_VQLR_GATEUP;
+    const bool lowrank = w->kind == MOE_W_VQLR_GATEUP;
+    CUtensorMap tm_cgate, tm_cup;  // C [E][r][I]: boxes of 64 columns x 256 rows of r
+    if (lowrank && (!make_tmap_3d_bf16(&tm_cgate, w->c_gate, (uint64_t)d.I, (uint64_t)d.r,
+                                       (uint64_t)d.E, kTI, kBoxRows, 1) ||
+                    !make_tmap_3d_bf16(&tm_cup, w->c_up, (uint64_t)d.I, (uint64_t)d.r,
+                                       (uint64_t)d.E, kTI, kBoxRows, 1)))
+        return MOE_ERR_CUDA;
     CUtensorMap tm_gate, tm_up, tm_down;
     bool ok;
     if (vq)  // index maps [E * H/4 rows][I] uint8, boxes of 256 rows x 64 columns
@@ -372,7 +421,11 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.cb_gate = vq ? static_cast<const uint2 *>(w->cb_gate) : nullptr;
     a.cb_up = vq ? static_cast<const uint2 *>(w->cb_up) : nullptr;
     a.n_qb = d.H / (4 * kBoxRows);
-    cudaError_t err = vq ? launch_gateup_vq(tm_gate, tm_up, a, stream)
+    a.z = lowrank ? reinterpret_cast<const float *>(ws + L.z) : nullptr;
+    a.r = lowrank ? d.r : 0;
+    a.n_rb = lowrank ? (d.r + kBoxRows - 1) / kBoxRows : 0;
+    cudaError_t err = vq ? launch_gateup_vq(tm_gate, tm_up, lowrank ? &tm_cgate : nullptr,
+                                            lowrank ? &tm_cup : nullptr, a, stream)
                          : launch_gateup_dense(tm_gate, tm_up, a, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
@@ -415,7 +468,8 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     const int given = (sorted_route_ids != nullptr) + (expert_block_ids != nullptr) +
                       (num_padded != nullptr);
     if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
-    const Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    d.r = lr_rank(w);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -439,6 +493,13 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
                                 w->E, b, d.rsub, d.max_sub, sbt, status, s);
     }
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    LowRankProj lr_store;
+    if (const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store)) {
+        // without a router launch to ride along, the projections get one of their own
+        if (launch_lowrank_proj(static_cast<const __nv_bfloat16 *>(h), M, w->H, *lr, s) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     trace(2, s);
     const int32_t *srt = given ? sorted_route_ids : reinterpret_cast<const int32_t *>(ws + L.sorted);
     const int32_t *blk = given ? expert_block_ids : reinterpret_cast<const int32_t *>(ws + L.blocks);
@@ -457,7 +518,8 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
     if (!w_router || !topk_ids || !topk_weights || !aligned(w_router, 16) ||
         !aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
-    const Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    d.r = lr_rank(w);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -467,18 +529,20 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
     int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
     SubBlock *ws_sbt = reinterpret_cast<SubBlock *>(ws + L.sbt);
     int32_t *ws_status = reinterpret_cast<int32_t *>(ws + L.status);
+    LowRankProj lr_store;
+    const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store);  // rides in the router launch
     cudaError_t err;
     if (router_can_align(M, k)) {  // one launch routes and aligns
         err = launch_router_align(static_cast<const __nv_bfloat16 *>(h),
                                   static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H, w->E,
                                   k, 1, topk_ids, topk_weights, b, d.rsub, ws_sorted, ws_blocks,
-                                  ws_npad, d.cap, ws_sbt, ws_status, s);
+                                  ws_npad, d.cap, ws_sbt, ws_status, lr, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
     } else {
         err = launch_router(static_cast<const __nv_bfloat16 *>(h),
                             static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H, w->E, k, 1,
-                            topk_ids, topk_weights, s);
+                            topk_ids, topk_weights, lr, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
         err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,

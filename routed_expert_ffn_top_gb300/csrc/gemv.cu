@@ -53,13 +53,16 @@ constexpr int kFirstConsumerWarp = 2;
 constexpr int kBoxBytes = kBoxRows * kTI * 2;                 // 32 KB (also kTN == kTI)
 constexpr int kStageBytesGU = kBoxBytes + kNT * kBoxRows * 2;  // + h slices (bf16)
 constexpr int kStageBytesDN = kBoxBytes + kNT * kBoxRows * 4;  // + p slices (fp32)
-constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 2 * 4;
+constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 4;  // g, then u, through one buffer
 // VQ gate/up: a box is 256 rows x 64 columns of uint8 code indices (16 KB), i.e. 1024 rows of
 // H; its activation slices are those 1024 h values of each route's token.
 constexpr int kVQRows = 256;
 constexpr int kVQHRows = 4 * kVQRows;
 constexpr int kVQBoxBytes = kVQRows * kTI;
 constexpr int kStageBytesVQ = kVQBoxBytes + kNT * kVQHRows * 2;
+// VQ + low-rank gate/up: the ring also carries C boxes (256 rows of r x 64 columns, bf16)
+// with fp32 z slices, the shape of a down stage.
+constexpr int kStageBytesLR = kStageBytesDN;
 constexpr int kCodeBookBytes = 256 * 8;
 constexpr int kRedBytesDN = kConsumerWarps * kNT * kTN * 4;
 static_assert(kTI == kTN, "one box shape for both kernels");
@@ -67,7 +70,7 @@ static_assert(kStageBytesGU % 1024 == 0 && kStageBytesDN % 1024 == 0 && kStageBy
               "stage alignment");
 static_assert(kVQRows == kBoxRows, "the consumer lanes own 16 of the 256 rows of every box");
 
-enum TileKind { kDenseGateUp = 0, kDown = 1, kVQGateUp = 2 };
+enum TileKind { kDenseGateUp = 0, kDown = 1, kVQGateUp = 2, kVQLRGateUp = 3 };
 
 struct Ctl {
     uint64_t full[kStages];
@@ -153,13 +156,20 @@ __device__ void box_producer(const GemvArgs &a, Ctl &ctl, int64_t T, int tiles_p
     if (ctl.abort) atomicOr(a.status, MOE_DEV_WAIT_TIMEOUT);
 }
 
-// Activation loader (one warp).  For every stage the box producer fills, lane l copies
-// `chunks` 16-byte pieces per route: src(route, token, tile, j, piece) -> the stage's slice
-// area.  Its arrival on the stage's full barrier completes only when its copies have landed.
-template <typename SrcFn>
+// Where a stage's activation slices go: after the stage's box (box_bytes), one slice of
+// slice_bytes per route, chunks 16-byte pieces per lane.
+struct SliceLayout {
+    int box_bytes, slice_bytes, chunks;
+};
+
+// Activation loader (one warp).  For every stage j the box producer fills, lane l copies
+// its pieces of each route's slice, src(route, token, tile, j, piece) -> the stage's slice
+// area (a NULL source writes zeros).  Its arrival on the stage's full barrier completes only
+// when its copies have landed.
+template <typename LayoutFn, typename SrcFn>
 __device__ void slice_loader(const GemvArgs &a, Ctl &ctl, unsigned char *stages, int stage_bytes,
-                             int box_bytes, int slice_bytes, int chunks, int64_t T,
-                             int tiles_per_sub, int stages_per_tile, SrcFn src) {
+                             int64_t T, int tiles_per_sub, int stages_per_tile, LayoutFn layout,
+                             SrcFn src) {
     const int lane = threadIdx.x & 31;
     int stage = 0;
     uint32_t phase = 0;
@@ -172,15 +182,22 @@ __device__ void slice_loader(const GemvArgs &a, Ctl &ctl, unsigned char *stages,
         const int my_token = rec->tokens[lane & (kNT - 1)];
         const int nst = ntok > 0 ? stages_per_tile : 1;
         for (int j = 0; j < nst; ++j) {
-            if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) return;
+            if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) {
+                cp_async_wait_all();
+                return;
+            }
             if (ntok > 0) {
-                unsigned char *dst = stages + stage * stage_bytes + box_bytes;
+                const SliceLayout L = layout(j);
+                unsigned char *dst = stages + stage * stage_bytes + L.box_bytes;
                 for (int q = 0; q < ntok; ++q) {
                     const int route = __shfl_sync(0xffffffffu, my_route, q);
                     const int token = __shfl_sync(0xffffffffu, my_token, q);
-                    for (int c = 0; c < chunks; ++c)
-                        cp_async_16(dst + q * slice_bytes + (lane * chunks + c) * 16,
-                                    src(route, token, t, j, lane * chunks + c));
+                    for (int c = 0; c < L.chunks; ++c) {
+                        const unsigned char *g = src(route, token, t, j, lane * L.chunks + c);
+                        cp_async_16_zfill(dst + q * L.slice_bytes + (lane * L.chunks + c) * 16,
+                                          g ? g : reinterpret_cast<const unsigned char *>(a.h),
+                                          g ? 16u : 0u);
+                    }
                 }
                 cp_async_mbar_arrive(&ctl.full[stage]);
             }
@@ -189,6 +206,7 @@ __device__ void slice_loader(const GemvArgs &a, Ctl &ctl, unsigned char *stages,
             advance(stage, phase);
         }
     }
+    cp_async_wait_all();
 }
 
 // Per-thread position inside the consumer warps.
@@ -304,33 +322,65 @@ __device__ __forceinline__ void release_stage(Ctl &ctl, const Lane &ln, int &sta
     advance(stage, phase);
 }
 
+// Sums the 8 warps' partials of (route q, column c) in warp order; `red` holds, per warp,
+// route and column, the value the warp's two lane halves summed.
+__device__ __forceinline__ float sum_warps(const float *red, int q, int c) {
+    float v = red[q * kTI + c];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) v += red[(w * kNT + q) * kTI + c];
+    return v;
+}
+
+// Writes this thread's lane-half sums of acc into red (lanes of the lower half only).
+template <int NT>
+__device__ __forceinline__ void stage_partials(float *red, const Lane &ln, float (&acc)[NT][4]) {
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        float v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = acc[q][c] + __shfl_xor_sync(0xffffffffu, acc[q][c], 16);
+        if (ln.half == 0)
+            *reinterpret_cast<float4 *>(&red[(ln.cw * kNT + q) * kTI + ln.c4]) =
+                make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 // One gate/up tile with NT routes; its first stage has already been waited for.  Returns
 // false when the CTA must stop (a bounded wait gave up somewhere in the CTA).
-template <int NT, bool kVQ>
+// Stages: dense, a gate box and an up box for every 256 rows of H; VQ, a gate and an up
+// index box for every 1024 rows of H; with kLR, then a C_gate and a C_up box for every 256
+// rows of r, multiplied by z = D^T h into the same accumulators ([MED]'s joint
+// accumulation of the VQ and low-rank terms).
+template <int NT, bool kVQ, bool kLR>
 __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                             const uint2 *cbs, const Lane &ln, int it, int r0, int r1, int &stage,
                             uint32_t &phase) {
+    constexpr int kSt = kLR ? kStageBytesLR : (kVQ ? kStageBytesVQ : kStageBytesGU);
     float ag[NT][4], au[NT][4];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ag[q][c] = au[q][c] = 0.0f;
     bool failed = false;
-    // stages of a tile: gate box, up box for the first rows of H, then the next rows, ...
-    const int nst = kVQ ? 2 * a.n_qb : 2 * a.n_hb;
+    const int nvq = kVQ ? 2 * a.n_qb : 2 * a.n_hb;
+    const int nst = nvq + (kLR ? 2 * a.n_rb : 0);
     for (int j = 0; j < nst; ++j) {
         if (j > 0 && !wait_or_abort(&ctl.full[stage], phase, ctl)) {
             failed = true;
             break;
         }
-        if constexpr (kVQ) {
-            const unsigned char *st = stages + stage * kStageBytesVQ;
+        const unsigned char *st = stages + stage * kSt;
+        if (kLR && j >= nvq) {
+            if ((j - nvq) & 1)
+                accumulate_f32_box<NT>(st, ln, au);
+            else
+                accumulate_f32_box<NT>(st, ln, ag);
+        } else if constexpr (kVQ) {
             if (j & 1)
                 accumulate_vq_box<NT>(st, cbs + 256, ln, au);
             else
                 accumulate_vq_box<NT>(st, cbs, ln, ag);
         } else {
-            const unsigned char *st = stages + stage * kStageBytesGU;
             if (j & 1)
                 accumulate_bf16_box<NT>(st, ln, au);
             else
@@ -339,37 +389,25 @@ __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, 
         release_stage(ctl, ln, stage, phase);
     }
     if (named_bar_or(1, kConsumerThreads, failed)) return false;
-    // the two lane halves (rows), then the warps; the same bits on both lanes
+    // the two lane halves (rows), then the warps in order: g first, then u
+    float g[2];
+    stage_partials<NT>(red, ln, ag);
+    named_bar_sync(1, kConsumerThreads);
 #pragma unroll
-    for (int q = 0; q < NT; ++q) {
-        float g4[4], u4[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            g4[c] = ag[q][c] + __shfl_xor_sync(0xffffffffu, ag[q][c], 16);
-            u4[c] = au[q][c] + __shfl_xor_sync(0xffffffffu, au[q][c], 16);
-        }
-        if (ln.half == 0) {
-            float *dst = &red[((ln.cw * kNT + q) * kTI + ln.c4) * 2];
-            *reinterpret_cast<float4 *>(dst) = make_float4(g4[0], u4[0], g4[1], u4[1]);
-            *reinterpret_cast<float4 *>(dst + 4) = make_float4(g4[2], u4[2], g4[3], u4[3]);
-        }
+    for (int pass = 0; pass < 2; ++pass) {
+        const int idx = ln.ctid + pass * kConsumerThreads;
+        g[pass] = (idx / kTI < NT) ? sum_warps(red, idx / kTI, idx % kTI) : 0.0f;
     }
+    named_bar_sync(1, kConsumerThreads);
+    stage_partials<NT>(red, ln, au);
     named_bar_sync(1, kConsumerThreads);
     const int col0 = it * kTI;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
         const int idx = ln.ctid + pass * kConsumerThreads;
         const int q = idx / kTI, c = idx % kTI;
-        if (q < NT) {
-            float2 sum = *reinterpret_cast<const float2 *>(&red[(q * kTI + c) * 2]);
-#pragma unroll
-            for (int w = 1; w < kConsumerWarps; ++w) {
-                const float2 v = *reinterpret_cast<const float2 *>(&red[((w * kNT + q) * kTI + c) * 2]);
-                sum.x += v.x;
-                sum.y += v.y;
-            }
-            a.p[(int64_t)(pass ? r1 : r0) * a.I + col0 + c] = silu_f32(sum.x) * sum.y;
-        }
+        if (q < NT)
+            a.p[(int64_t)(pass ? r1 : r0) * a.I + col0 + c] = silu_f32(g[pass]) * sum_warps(red, q, c);
     }
     named_bar_sync(1, kConsumerThreads);
     return true;
@@ -452,8 +490,8 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
         if constexpr (kKind == kDown)                                                        \
             go = down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);            \
         else                                                                                 \
-            go = gateup_tile<N, kKind == kVQGateUp>(a, ctl, stages, red, cbs, ln, ct, r0, r1, \
-                                                    stage, phase);                           \
+            go = gateup_tile<N, kKind != kDenseGateUp, kKind == kVQLRGateUp>(                 \
+                a, ctl, stages, red, cbs, ln, ct, r0, r1, stage, phase);                     \
         break;
         switch (ntok) {
             MOE_TILE(1)
@@ -535,7 +573,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     if (warp == 1) {
         // h rows [256 (j/2), +256) of each token: 512 bytes = one 16-byte piece per lane
-        slice_loader(a, ctl, stages, kStageBytesGU, kBoxBytes, kBoxRows * 2, 1, T, a.n_it, per_tile,
+        slice_loader(a, ctl, stages, kStageBytesGU, T, a.n_it, per_tile,
+                     [](int) { return SliceLayout{kBoxBytes, kBoxRows * 2, 1}; },
                      [&](int route, int token, int64_t t, int j, int piece) {
                          return reinterpret_cast<const unsigned char *>(a.h) +
                                 ((size_t)token * a.H + (size_t)(j >> 1) * kBoxRows) * 2 + piece * 16;
@@ -547,22 +586,33 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 }
 
 // ------------------------------------------------------------------------- VQ gate/up
+// tm_jgate / tm_jup: index maps [E*H/4 rows][I] uint8, boxes of 256 index rows x 64
+// columns.  With kLR also tm_cgate / tm_cup: C [E][r][I] bf16 as 3-D maps (I, r, E), boxes
+// of 64 columns x 256 rows of r x 1 expert (rows past r are read as zeros).
+template <bool kLR>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gateup_vq_kernel(const __grid_constant__ CUtensorMap tm_jgate,
-                     const __grid_constant__ CUtensorMap tm_jup, const GemvArgs a) {
+                     const __grid_constant__ CUtensorMap tm_jup,
+                     const __grid_constant__ CUtensorMap tm_cgate,
+                     const __grid_constant__ CUtensorMap tm_cup, const GemvArgs a) {
+    constexpr int kSt = kLR ? kStageBytesLR : kStageBytesVQ;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
-    float *red = reinterpret_cast<float *>(base + kStages * kStageBytesVQ);
-    uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kStageBytesVQ + kRedBytesGU);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesVQ + kRedBytesGU + 2 * kCodeBookBytes);
+    float *red = reinterpret_cast<float *>(base + kStages * kSt);
+    uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kSt + kRedBytesGU);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kSt + kRedBytesGU + 2 * kCodeBookBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         init_ring(ctl);
         prefetch_tensormap(&tm_jgate);
         prefetch_tensormap(&tm_jup);
+        if (kLR) {
+            prefetch_tensormap(&tm_cgate);
+            prefetch_tensormap(&tm_cup);
+        }
     }
     // the layer-shared code books (weights, not produced by an earlier kernel)
     for (int i = threadIdx.x; i < 512; i += blockDim.x)
@@ -572,7 +622,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     pdl_launch_dependents();
 
     const int64_t T = num_subblocks(a) * a.n_it;
-    const int per_tile = 2 * a.n_qb;
+    const int nvq = 2 * a.n_qb;
+    const int per_tile = nvq + (kLR ? 2 * a.n_rb : 0);
     prefetch_down_weights(a, T);
 
     if (warp == 0) {
@@ -581,24 +632,44 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             box_producer(a, ctl, T, a.n_it, per_tile, [&](int stage, int64_t t, int j, int e) {
                 const int it = (int)(t % a.n_it);
                 uint64_t *bar = &ctl.full[stage];
-                mbar_arrive_expect_tx(bar, kVQBoxBytes);
-                tma_load_2d(stages + stage * kStageBytesVQ,
-                            (j & 1) ? (const void *)&tm_jup : (const void *)&tm_jgate, it * kTI,
-                            e * (a.H / 4) + (j >> 1) * kVQRows, bar, pol_w);
+                unsigned char *dst = stages + stage * kSt;
+                if (kLR && j >= nvq) {
+                    const int jj = j - nvq;
+                    mbar_arrive_expect_tx(bar, kBoxBytes);
+                    tma_load_3d(dst, (jj & 1) ? (const void *)&tm_cup : (const void *)&tm_cgate,
+                                it * kTI, (jj >> 1) * kBoxRows, e, bar, pol_w);
+                } else {
+                    mbar_arrive_expect_tx(bar, kVQBoxBytes);
+                    tma_load_2d(dst, (j & 1) ? (const void *)&tm_jup : (const void *)&tm_jgate,
+                                it * kTI, e * (a.H / 4) + (j >> 1) * kVQRows, bar, pol_w);
+                }
             });
         }
         return;
     }
     if (warp == 1) {
-        // h rows [1024 (j/2), +1024) of each token: 2 KB = four 16-byte pieces per lane
-        slice_loader(a, ctl, stages, kStageBytesVQ, kVQBoxBytes, kVQHRows * 2, 4, T, a.n_it, per_tile,
-                     [&](int route, int token, int64_t t, int j, int piece) {
+        // VQ stages: h rows [1024 (j/2), +1024) of each token, 2 KB = four 16-byte pieces per
+        // lane.  Low-rank stages: z rows [256 (jj/2), +256) of the token's gate or up
+        // projection, 1 KB = two pieces per lane; rows past r are zeros.
+        slice_loader(a, ctl, stages, kSt, T, a.n_it, per_tile,
+                     [&](int j) {
+                         return (kLR && j >= nvq) ? SliceLayout{kBoxBytes, kBoxRows * 4, 2}
+                                                  : SliceLayout{kVQBoxBytes, kVQHRows * 2, 4};
+                     },
+                     [&](int route, int token, int64_t t, int j, int piece) -> const unsigned char * {
+                         if (kLR && j >= nvq) {
+                             const int jj = j - nvq;
+                             const int row = (jj >> 1) * kBoxRows + piece * 4;
+                             if (row >= a.r) return nullptr;
+                             return reinterpret_cast<const unsigned char *>(
+                                 a.z + (size_t)token * 2 * a.r + (size_t)(jj & 1) * a.r + row);
+                         }
                          return reinterpret_cast<const unsigned char *>(a.h) +
                                 ((size_t)token * a.H + (size_t)(j >> 1) * kVQHRows) * 2 + piece * 16;
                      });
         return;
     }
-    consume_tiles<kVQGateUp>(a, ctl, stages, red, cbs, T, a.n_it);
+    consume_tiles<kLR ? kVQLRGateUp : kVQGateUp>(a, ctl, stages, red, cbs, T, a.n_it);
 }
 
 // ------------------------------------------------------------------------------- down
@@ -640,7 +711,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     if (warp == 1) {
         pdl_wait();
         // p rows [256 j, +256) of each route: 1 KB = two 16-byte pieces per lane
-        slice_loader(a, ctl, stages, kStageBytesDN, kBoxBytes, kBoxRows * 4, 2, T, a.n_ht, a.n_ib,
+        slice_loader(a, ctl, stages, kStageBytesDN, T, a.n_ht, a.n_ib,
+                     [](int) { return SliceLayout{kBoxBytes, kBoxRows * 4, 2}; },
                      [&](int route, int token, int64_t t, int j, int piece) {
                          return reinterpret_cast<const unsigned char *>(a.p) +
                                 ((size_t)route * a.I + (size_t)j * kBoxRows) * 4 + piece * 16;
@@ -717,18 +789,27 @@ cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &t
     return cudaLaunchKernelEx(&cfg, gateup_dense_kernel, tm_gate, tm_up, a);
 }
 
-static size_t gateup_vq_smem() {
-    return 1024 + kStages * kStageBytesVQ + kRedBytesGU + 2 * kCodeBookBytes + sizeof(Ctl);
+static size_t gateup_vq_smem(bool lr) {
+    return 1024 + kStages * (lr ? kStageBytesLR : kStageBytesVQ) + kRedBytesGU +
+           2 * kCodeBookBytes + sizeof(Ctl);
 }
 
 cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                             const CUtensorMap *tm_cgate, const CUtensorMap *tm_cup,
                              const GemvArgs &a, cudaStream_t stream) {
-    const size_t smem = gateup_vq_smem();
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gateup_vq_kernel), smem);
+    const bool lr = a.r > 0;
+    const size_t smem = gateup_vq_smem(lr);
+    const void *fn = lr ? reinterpret_cast<const void *>(gateup_vq_kernel<true>)
+                        : reinterpret_cast<const void *>(gateup_vq_kernel<false>);
+    cudaError_t err = ensure_smem(fn, smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, gateup_vq_kernel, tm_jgate, tm_jup, a);
+    if (lr)
+        return cudaLaunchKernelEx(&cfg, gateup_vq_kernel<true>, tm_jgate, tm_jup, *tm_cgate,
+                                  *tm_cup, a);
+    // the low-rank maps are unused without the term: pass the index maps in their place
+    return cudaLaunchKernelEx(&cfg, gateup_vq_kernel<false>, tm_jgate, tm_jup, tm_jgate, tm_jup, a);
 }
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream) {

@@ -28,6 +28,7 @@ struct Dims {
     int64_t cap;      // alignment capacity in rows
     int64_t max_sub;  // cap / rsub
     int n_it, n_hb, n_ht, n_ib;  // column tiles and 256-row boxes of gate/up and down
+    int r = 0;        // rank of the low-rank gate/up term (0: none)
 };
 
 // One sub-block of the alignment (rsub consecutive aligned rows of one expert), as the
@@ -49,6 +50,7 @@ struct WsLayout {
     size_t sbt;      // SubBlock[max_sub]
     size_t p;        // float[R * I]   SiLU(g) * u per route
     size_t y;        // float[R * H]   down-projection output per route
+    size_t z;        // float[M * 2r]  low-rank projections z = D^T h (gate, then up)
     size_t x_tiles;  // bf16[cap * H]  large-batch regime: token rows per aligned row
     size_t p_tiles;  // bf16[cap * I]  large-batch regime: p per aligned row
     size_t total;
@@ -70,6 +72,8 @@ struct GemvArgs {
     float *y;
     int32_t *status;
     const unsigned char *w_down;  // W_down [E, I, H] bf16 (idle gate/up CTAs warm it in L2)
+    const float *z;        // VQ + low rank: z = D^T h [M, 2r] (gate, then up); else NULL
+    int r, n_rb;           // rank of the low-rank term (0: none); its 256-row boxes
     const uint2 *cb_gate;  // VQ code books [256] code words of 4 bf16 (NULL when dense)
     const uint2 *cb_up;
     int M, k, E, H, I, b, rsub;
@@ -141,9 +145,23 @@ __device__ __forceinline__ void build_subblock(const int32_t *sorted, const int3
     *out = rec;
 }
 
+// Low-rank projections z = D^T h of VQ + low-rank gate/up weights, computed by extra
+// clusters of the router's launch (see router.cu).
+struct LowRankProj {
+    const __nv_bfloat16 *d_gate, *d_up;  // [H, r] bf16, layer-shared
+    int r;                               // 0: no projection
+    int first;                           // set by the launcher
+    float *z;                            // [M, 2r] fp32: gate then up
+};
+
 cudaError_t launch_router(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                           const float *bias, int M, int H, int E, int k, int renormalize,
-                          int32_t *topk_ids, float *topk_weights, cudaStream_t stream);
+                          int32_t *topk_ids, float *topk_weights, const LowRankProj *lr,
+                          cudaStream_t stream);
+
+// The projections alone (callers that bring their own routing).
+cudaError_t launch_lowrank_proj(const __nv_bfloat16 *h, int M, int H, const LowRankProj &lr,
+                                cudaStream_t stream);
 
 // Router that also aligns the routes (and writes the sub-block table) in the same launch;
 // possible when one router cluster holds every token.
@@ -152,7 +170,8 @@ cudaError_t launch_router_align(const __nv_bfloat16 *h, const __nv_bfloat16 *w_r
                                 const float *bias, int M, int H, int E, int k, int renormalize,
                                 int32_t *topk_ids, float *topk_weights, int b, int rsub,
                                 int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
-                                SubBlock *sbt, int32_t *status, cudaStream_t stream);
+                                SubBlock *sbt, int32_t *status, const LowRankProj *lr,
+                                cudaStream_t stream);
 
 // Alignment; when `sbt` is not NULL it also writes the sub-block table of rsub-row blocks.
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b,
@@ -167,8 +186,10 @@ cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const in
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream);
 
-// Blockwise-VQ gate/up (d = 4, K = 256): index maps through TMA, code books in shared memory.
+// Blockwise-VQ gate/up (d = 4, K = 256): index maps through TMA, code books in shared memory;
+// with a.r > 0 also the low-rank term (C maps through TMA, z slices from a.z).
 cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                             const CUtensorMap *tm_cgate, const CUtensorMap *tm_cup,
                              const GemvArgs &a, cudaStream_t stream);
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream);

@@ -35,11 +35,18 @@ struct FusedAlign {
     int32_t *status;
 };
 
-// Passes over a CTA's W_r slice of HS rows: one when the slice fits kRouterPassBytes, else
-// two (the supported shapes keep the slice within 2 kRouterPassBytes).
+// Low-rank projections computed in the router's launch (VQ + low-rank gate/up weights):
+// clusters blockIdx.y >= lr.first compute z[m][p*r + c] = sum_h h[m][h] D_p[h][c] for
+// projection p (0 gate, 1 up) of their token tile, with the same split of H over the
+// cluster, the same fixed summation order and no top-k.
+
+// Passes over a CTA's slice of HS weight rows with E columns: the smallest power of two
+// that keeps one pass within kRouterPassBytes.
 constexpr int kRouterPassBytes = 64 * 1024;
 __host__ __device__ inline int router_passes(int HS, int E) {
-    return (HS * E * 2 > kRouterPassBytes) ? 2 : 1;
+    int n = 1;
+    while ((int64_t)(HS / n) * E * 2 > kRouterPassBytes && n < HS) n *= 2;
+    return n;
 }
 
 // Generic address of `p` (a shared variable of this CTA) in CTA `rank` of the cluster.
@@ -64,12 +71,19 @@ __global__ void __launch_bounds__(kRouterThreads)
     router_topk_kernel(const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ wr,
                        const float *__restrict__ bias, int M, int H, int E, int k, int renorm,
                        int32_t *__restrict__ topk_ids, float *__restrict__ topk_wts,
-                       const FusedAlign fa) {
+                       const FusedAlign fa, const LowRankProj lr) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int tid = threadIdx.x;
     const uint32_t rank = cluster_ctarank();
     const int HS = H / kRouterCluster;
-    const int tile = blockIdx.y;
+    // A cluster either routes its token tile (columns: the E experts of W_r) or computes one
+    // low-rank projection of it (columns: the r basis vectors of D_gate or D_up).
+    const bool zmode = lr.r > 0 && (int)blockIdx.y >= lr.first;
+    const int zi = (int)blockIdx.y - lr.first;
+    const int tile = zmode ? zi >> 1 : (int)blockIdx.y;
+    const int proj = zi & 1;
+    if (zmode) E = lr.r;
+    const __nv_bfloat16 *wsrc = zmode ? (proj ? lr.d_up : lr.d_gate) : wr;
     const int npairs = E / 2;
     const int RG = kRouterThreads / npairs;  // row groups (>= 1 since E <= 512)
 
@@ -100,7 +114,7 @@ __global__ void __launch_bounds__(kRouterThreads)
     int32_t *align_sm = reinterpret_cast<int32_t *>(ptr);
 
     const uint32_t w_bytes = (uint32_t)HP * E * 2;
-    const __nv_bfloat16 *w_cta = wr + (size_t)rank * HS * E;
+    const __nv_bfloat16 *w_cta = wsrc + (size_t)rank * HS * E;
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -194,6 +208,16 @@ __global__ void __launch_bounds__(kRouterThreads)
     const int warp = tid >> 5, lane = tid & 31;
     const int t = (int)rank;
     const int m = tile * TM + t;
+    if (zmode) {  // the projection: the 8 partials summed in rank order
+        if (t < TM && m < M)
+            for (int c = tid; c < E; c += kRouterThreads) {
+                float v = 0.0f;
+#pragma unroll
+                for (int q = 0; q < kRouterCluster; ++q) v += gath[(size_t)q * E + c];
+                lr.z[(size_t)m * 2 * lr.r + (size_t)proj * lr.r + c] = ok ? v : 0.0f;
+            }
+        return;  // no CTA touches another's shared memory after the cluster barrier
+    }
     if (warp == 0 && t < TM && m < M) {
         float vals[kPerLane];
         uint32_t key[kPerLane];
@@ -289,59 +313,75 @@ template <int TM, int kPerLane>
 static cudaError_t launch_router_tm(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                                     const float *bias, int M, int H, int E, int k, int renorm,
                                     int32_t *ids, float *wts, const FusedAlign &fa,
-                                    cudaStream_t stream) {
-    const size_t smem = router_smem(TM, H, E, fa.enabled != 0);
+                                    LowRankProj lr, bool route, cudaStream_t stream) {
+    const int ntiles = (M + TM - 1) / TM;
+    const int cols = (lr.r > E || !route) ? lr.r : E;
+    const size_t smem = router_smem(TM, H, cols, route && fa.enabled != 0);
     cudaError_t err =
         ensure_smem(reinterpret_cast<const void *>(router_topk_kernel<TM, kPerLane>), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
-    dim3 grid(kRouterCluster, (M + TM - 1) / TM, 1);
+    lr.first = route ? ntiles : 0;
+    dim3 grid(kRouterCluster, lr.first + (lr.r > 0 ? 2 * ntiles : 0), 1);
     cudaLaunchConfig_t cfg = launch_config(grid, dim3(kRouterThreads), smem, stream, attrs,
                                            kRouterCluster);
     return cudaLaunchKernelEx(&cfg, router_topk_kernel<TM, kPerLane>, h, w_router, bias, M, H, E, k,
-                              renorm, ids, wts, fa);
+                              renorm, ids, wts, fa, lr);
 }
 
 template <int kPerLane>
 static cudaError_t launch_router_lanes(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                                        const float *bias, int M, int H, int E, int k, int renorm,
                                        int32_t *topk_ids, float *topk_weights,
-                                       const FusedAlign &fa, cudaStream_t stream) {
+                                       const FusedAlign &fa, const LowRankProj &lr, bool route,
+                                       cudaStream_t stream) {
     if (M <= 1)
         return launch_router_tm<1, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
-                                             topk_weights, fa, stream);
+                                             topk_weights, fa, lr, route, stream);
     if (M <= 2)
         return launch_router_tm<2, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
-                                             topk_weights, fa, stream);
+                                             topk_weights, fa, lr, route, stream);
     if (M <= 4)
         return launch_router_tm<4, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
-                                             topk_weights, fa, stream);
+                                             topk_weights, fa, lr, route, stream);
     return launch_router_tm<8, kPerLane>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
-                                         topk_weights, fa, stream);
+                                         topk_weights, fa, lr, route, stream);
 }
 
 static cudaError_t launch_router_any(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                                      const float *bias, int M, int H, int E, int k,
                                      int renormalize, int32_t *topk_ids, float *topk_weights,
-                                     const FusedAlign &fa, cudaStream_t stream) {
+                                     const FusedAlign &fa, const LowRankProj *lr_in,
+                                     cudaStream_t stream) {
     if (M <= 0) return cudaSuccess;
     const int renorm = renormalize ? 1 : 0;
+    LowRankProj lr{};
+    if (lr_in) lr = *lr_in;
     if (E <= 128)
         return launch_router_lanes<4>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
-                                      topk_weights, fa, stream);
+                                      topk_weights, fa, lr, true, stream);
     if (E <= 256)
         return launch_router_lanes<8>(h, w_router, bias, M, H, E, k, renorm, topk_ids,
-                                      topk_weights, fa, stream);
+                                      topk_weights, fa, lr, true, stream);
     return launch_router_lanes<16>(h, w_router, bias, M, H, E, k, renorm, topk_ids, topk_weights,
-                                   fa, stream);
+                                   fa, lr, true, stream);
 }
 
 cudaError_t launch_router(const __nv_bfloat16 *h, const __nv_bfloat16 *w_router,
                           const float *bias, int M, int H, int E, int k, int renormalize,
-                          int32_t *topk_ids, float *topk_weights, cudaStream_t stream) {
+                          int32_t *topk_ids, float *topk_weights, const LowRankProj *lr,
+                          cudaStream_t stream) {
     FusedAlign fa{};
     return launch_router_any(h, w_router, bias, M, H, E, k, renormalize, topk_ids, topk_weights,
-                             fa, stream);
+                             fa, lr, stream);
+}
+
+cudaError_t launch_lowrank_proj(const __nv_bfloat16 *h, int M, int H, const LowRankProj &lr,
+                                cudaStream_t stream) {
+    if (M <= 0 || lr.r <= 0) return cudaSuccess;
+    FusedAlign fa{};
+    return launch_router_lanes<4>(h, nullptr, nullptr, M, H, lr.r, 0, 0, nullptr, nullptr, fa, lr,
+                                  false, stream);
 }
 
 bool router_can_align(int M, int k) { return M >= 1 && M <= kRouterCluster && M * k <= 8 * 32; }
@@ -350,7 +390,8 @@ cudaError_t launch_router_align(const __nv_bfloat16 *h, const __nv_bfloat16 *w_r
                                 const float *bias, int M, int H, int E, int k, int renormalize,
                                 int32_t *topk_ids, float *topk_weights, int b, int rsub,
                                 int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
-                                SubBlock *sbt, int32_t *status, cudaStream_t stream) {
+                                SubBlock *sbt, int32_t *status, const LowRankProj *lr,
+                                cudaStream_t stream) {
     FusedAlign fa;
     fa.enabled = 1;
     fa.b = b;
@@ -362,7 +403,7 @@ cudaError_t launch_router_align(const __nv_bfloat16 *h, const __nv_bfloat16 *w_r
     fa.sbt = sbt;
     fa.status = status;
     return launch_router_any(h, w_router, bias, M, H, E, k, renormalize, topk_ids, topk_weights,
-                             fa, stream);
+                             fa, lr, stream);
 }
 
 }  // namespace moe

@@ -31,6 +31,7 @@ MOE_DEV_BAD_ALIGNMENT = 0x4
 
 MOE_W_DENSE_BF16 = 0
 MOE_W_VQ_GATEUP = 1
+MOE_W_VQLR_GATEUP = 2
 
 # Every symbol include/moe.h declares (checked against the header by the tests).
 EXPORTS = (
@@ -55,6 +56,9 @@ class ExpertWeights(ctypes.Structure):
         ("cb_gate", ctypes.c_void_p), ("cb_up", ctypes.c_void_p),
         ("d", ctypes.c_int32), ("K", ctypes.c_int32),
         ("w_down", ctypes.c_void_p),
+        ("d_gate", ctypes.c_void_p), ("d_up", ctypes.c_void_p),
+        ("c_gate", ctypes.c_void_p), ("c_up", ctypes.c_void_p),
+        ("r", ctypes.c_int32),
     ]
 
 
@@ -158,6 +162,12 @@ def expert_weights(layer: dict) -> ExpertWeights:
         w.j_up = _need(layer["j_up"], torch.uint8, "j_up", dev).data_ptr()
         w.cb_gate = _need(layer["cb_gate"], torch.bfloat16, "cb_gate", dev).data_ptr()
         w.cb_up = _need(layer["cb_up"], torch.bfloat16, "cb_up", dev).data_ptr()
+    if w.kind == MOE_W_VQLR_GATEUP:
+        w.r = int(layer["r"])
+        w.d_gate = _need(layer["d_gate"], torch.bfloat16, "d_gate", dev).data_ptr()
+        w.d_up = _need(layer["d_up"], torch.bfloat16, "d_up", dev).data_ptr()
+        w.c_gate = _need(layer["c_gate"], torch.bfloat16, "c_gate", dev).data_ptr()
+        w.c_up = _need(layer["c_up"], torch.bfloat16, "c_up", dev).data_ptr()
     return w
 
 

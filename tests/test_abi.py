@@ -103,6 +103,24 @@ def test_validation_fails_closed_without_gpu(lib):
     wd = _weights(H=2048 + 128)
     assert lib.moe_expert_ffn(fake, ctypes.byref(wd), 4, 8, ids, ids, None, None, None, 8, None,
                               fake, vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    # VQ + low rank: rank not a multiple of 128, rank too large, missing basis
+    for r, expect in ((200, moe.MOE_ERR_UNSUPPORTED), (640, moe.MOE_ERR_UNSUPPORTED),
+                      (0, moe.MOE_ERR_INVALID_ARG)):
+        wl_ = _weights(kind=2)
+        wl_.r = r
+        wl_.d_gate = wl_.d_up = wl_.c_gate = wl_.c_up = 1 << 20
+        assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wl_), 1, 8, 8, None, fake, ids,
+                                    ids, vp(1 << 20), 1 << 30, None) == expect, r
+    wl_ = _weights(kind=2)
+    wl_.r = 256
+    wl_.d_gate = wl_.c_gate = wl_.c_up = 1 << 20  # d_up missing
+    assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wl_), 1, 8, 8, None, fake, ids, ids,
+                                vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    # the workspace grows by the projections z [M, 2r] fp32
+    wl_.d_up = 1 << 20
+    wv_ = _weights(kind=1)
+    assert (lib.moe_workspace_bytes(ctypes.byref(wl_), 4, 8, 8)
+            >= lib.moe_workspace_bytes(ctypes.byref(wv_), 4, 8, 8) + 4 * 2 * 256 * 4)
     # unknown weight kind
     wk = _weights(kind=7)
     assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wk), 1, 8, 8, None, fake, ids, ids,

@@ -334,6 +334,64 @@ def test_vq_block_every_m_1_to_16():
     assert torch.equal(o1[0], out[3])
 
 
+VQLR_SMALL = [
+    # M, k, E, H, I, b, r
+    (5, 2, 8, 1024, 256, 3, 128), (13, 4, 16, 2048, 512, 8, 256), (2, 8, 8, 1024, 768, 1, 384),
+    (30, 3, 24, 1024, 256, 16, 512), (1, 1, 8, 1024, 256, 8, 256),
+]
+
+
+@pytest.mark.parametrize("M,k,E,H,I,b,r", VQLR_SMALL)
+def test_vqlr_expert_ffn_small(M, k, E, H, I, b, r):
+    """VQ + low-rank gate/up through moe_expert_ffn (the projections get their own launch)."""
+    wl = syn.Workload("vqlr_small_%d_%d_%d_%d" % (M, k, E, r), H=H, I=I, E=E, k=k, b=b, M=M,
+                      kind=syn.W_VQLR, d=4, K=256, r=r)
+    layer = syn.make_layer(wl, seed=3, device=DEV)
+    h = syn.make_hidden(wl, seed=3, device=DEV)
+    rng = np.random.default_rng(M + E + r)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    res = syn.make_hidden(wl, seed=5, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, torch.as_tensor(ids, device=DEV),
+                             torch.as_tensor(a, device=DEV), b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = G.oracle_ffn(layer, h, ids, a, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "vqlr expert_ffn r=%d" % r)
+    # the low-rank term matters: without it the output misses the bar by a wide margin
+    # (the unit-scale residual dominates the relative error, hence 3x rather than more)
+    vq = dict(layer)
+    vq["kind"] = syn.W_VQ
+    out_vq = moe.moe_expert_ffn(h, vq, torch.as_tensor(ids, device=DEV),
+                                torch.as_tensor(a, device=DEV), b, residual=res)
+    assert G.rel_l2(G.to_f64(out_vq), ref) > 3 * G.REL_L2
+
+
+def test_vqlr_block_every_m_1_to_16():
+    """The VQ + low-rank workload (d=4, r=256): the projections ride in the router launch;
+    parity at every M from 1 to 16, bitwise determinism and batch invariance."""
+    wl = syn.WORKLOADS["vqlr_d4_r256"]
+    layer = _workload_layer("vqlr_d4_r256")
+    for M in range(1, 17):
+        h = syn.make_hidden(wl, M=M, seed=M, device=DEV)
+        ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
+        out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+        assert moe.moe_read_device_status(ws) == 0
+        o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+        use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
+                                              logits, wl.k)
+        ref = G.oracle_ffn(layer, h, use_ids, use_wts)
+        G.assert_close_block(G.to_f64(out), ref, "vqlr_d4_r256 M=%d" % M)
+    out2, _, _ = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+    assert torch.equal(out2, out)
+    o1, _, _ = moe.moe_decode_block(h[3:4].contiguous(), layer, wl.k, wl.b)
+    assert torch.equal(o1[0], out[3])
+    # the decode block (projections in the router launch) and the expert entry point
+    # (projections in a launch of their own) agree bit for bit
+    o3 = moe.moe_expert_ffn(h, layer, ids, wts, wl.b)
+    assert torch.equal(o3, out)
+
+
 def test_large_m256_sampled_tokens():
     layer, h, ws, out, ids, wts = _check_block("large_m256",
                                                tokens=np.array([0, 1, 77, 128, 200, 254, 255]))
