@@ -54,6 +54,7 @@ constexpr int kBoxBytes = kBoxRows * kTI * 2;                 // 32 KB (also kTN
 constexpr int kStageBytesGU = kBoxBytes + kNT * kBoxRows * 2;  // + h slices (bf16)
 constexpr int kStageBytesDN = kBoxBytes + kNT * kBoxRows * 4;  // + p slices (fp32)
 constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 4;  // g, then u, through one buffer
+constexpr int kXwBytes = kConsumerWarps * kNT * kRowsPerWarp * 4;  // dense: per-warp fp32 h rows
 // VQ gate/up: a box is 256 rows x 64 columns of uint8 code indices (16 KB), i.e. 1024 rows of
 // H; its activation slices are those 1024 h values of each route's token.
 constexpr int kVQRows = 256;
@@ -254,6 +255,47 @@ __device__ __forceinline__ void accumulate_bf16_box(const unsigned char *st, con
     }
 }
 
+// The same sums for tiles with 3 or more routes, with fewer instructions: the warp first
+// widens its 32 rows of every route's h slice to fp32 in its own scratch xw [NT][32] (a
+// bf16 -> fp32 widening is exact), then each lane multiplies with packed fp32 FMAs.  Every
+// product of two bf16 values is exact in fp32 and each FMA rounds once, as the mixed-
+// precision FMA does, in the same row order: the bits are those of accumulate_bf16_box.
+template <int NT>
+__device__ __forceinline__ void accumulate_bf16_box_x32(const unsigned char *st, const Lane &ln,
+                                                        float *xw, float (&acc)[NT][4]) {
+    const __nv_bfloat16 *xs = reinterpret_cast<const __nv_bfloat16 *>(st + kBoxBytes);
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+        xw[i * kRowsPerWarp + ln.lane] =
+            __bfloat162float(xs[i * kBoxRows + ln.cw * kRowsPerWarp + ln.lane]);
+    __syncwarp();
+    const float *xr = xw + ln.half * kRowsPerThread;  // this lane's 16 rows of every route
+#pragma unroll
+    for (int r8 = 0; r8 < kRowsPerThread; r8 += 8) {
+        float w[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint2 w2 = *reinterpret_cast<const uint2 *>(st + (ln.rbase + r8 + i) * (kTI * 2) + ln.c4 * 2);
+            w[i][0] = bf16_lo(w2.x);
+            w[i][1] = bf16_hi(w2.x);
+            w[i][2] = bf16_lo(w2.y);
+            w[i][3] = bf16_hi(w2.y);
+        }
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(xr + q * kRowsPerWarp + r8);
+            const float4 x1 = *reinterpret_cast<const float4 *>(xr + q * kRowsPerWarp + r8 + 4);
+            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ffma2(acc[q][0], acc[q][1], x[i], w[i][0], w[i][1]);
+                ffma2(acc[q][2], acc[q][3], x[i], w[i][2], w[i][3]);
+            }
+        }
+    }
+    __syncwarp();  // the scratch is refilled for the next box
+}
+
 // acc[q][c] += sum over this thread's 16 rows of p_q[row] * W[row][c4 + c] for NT routes
 // (fp32 p, bf16 weights, packed fp32 FMAs, rows ascending).
 template <int NT>
@@ -313,6 +355,12 @@ __device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const
             }
         }
     }
+}
+
+// The tile bodies take one extra shared-memory pointer: the VQ kernels pass their code
+// books, the dense gate/up kernel its per-warp fp32 scratch (kConsumerWarps x [kNT][32]).
+__device__ __forceinline__ float *cbs_or_xw_as_floats(const uint2 *p) {
+    return const_cast<float *>(reinterpret_cast<const float *>(p));
 }
 
 // Releases the stage to the box producer and the loader once this warp is done with it.
@@ -380,6 +428,12 @@ __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, 
                 accumulate_vq_box<NT>(st, cbs + 256, ln, au);
             else
                 accumulate_vq_box<NT>(st, cbs, ln, ag);
+        } else if (NT >= 3) {
+            float *xw = cbs_or_xw_as_floats(cbs) + ln.cw * (kNT * kRowsPerWarp);
+            if (j & 1)
+                accumulate_bf16_box_x32<NT>(st, ln, xw, au);
+            else
+                accumulate_bf16_box_x32<NT>(st, ln, xw, ag);
         } else {
             if (j & 1)
                 accumulate_bf16_box<NT>(st, ln, au);
@@ -542,7 +596,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
     float *red = reinterpret_cast<float *>(base + kStages * kStageBytesGU);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesGU + kRedBytesGU);
+    float *xw = reinterpret_cast<float *>(base + kStages * kStageBytesGU + kRedBytesGU);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesGU + kRedBytesGU + kXwBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -582,7 +637,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         return;
     }
 
-    consume_tiles<kDenseGateUp>(a, ctl, stages, red, nullptr, T, a.n_it);
+    consume_tiles<kDenseGateUp>(a, ctl, stages, red, reinterpret_cast<const uint2 *>(xw), T,
+                                a.n_it);
 }
 
 // ------------------------------------------------------------------------- VQ gate/up
@@ -776,7 +832,9 @@ __global__ void __launch_bounds__(kCombineThreads)
     *reinterpret_cast<uint2 *>(out + o) = ov;
 }
 
-static size_t gateup_smem() { return 1024 + kStages * kStageBytesGU + kRedBytesGU + sizeof(Ctl); }
+static size_t gateup_smem() {
+    return 1024 + kStages * kStageBytesGU + kRedBytesGU + kXwBytes + sizeof(Ctl);
+}
 static size_t down_smem() { return 1024 + kStages * kStageBytesDN + kRedBytesDN + sizeof(Ctl); }
 
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
