@@ -213,8 +213,8 @@ static int check_weights(const moe_expert_weights_t *w) {
         if (!aligned(w->j_gate, 16) || !aligned(w->j_up, 16) || !aligned(w->cb_gate, 16) ||
             !aligned(w->cb_up, 16))
             return MOE_ERR_INVALID_ARG;
-        if (w->d != 4 || w->K != 256) return MOE_ERR_UNSUPPORTED;
-        if (w->H % (4 * kBoxRows) != 0) return MOE_ERR_UNSUPPORTED;  // 1024-row index boxes
+        if ((w->d != 4 && w->d != 8) || w->K != 256) return MOE_ERR_UNSUPPORTED;
+        if (w->H % 1024 != 0) return MOE_ERR_UNSUPPORTED;  // index boxes cover 1024 rows of H
         if (w->kind == MOE_W_VQ_GATEUP) return MOE_OK;
         if (!w->d_gate || !w->d_up || !w->c_gate || !w->c_up || !aligned(w->d_gate, 16) ||
             !aligned(w->d_up, 16) || !aligned(w->c_gate, 16) || !aligned(w->c_up, 16))
@@ -381,11 +381,11 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
         return MOE_ERR_CUDA;
     CUtensorMap tm_gate, tm_up, tm_down;
     bool ok;
-    if (vq)  // index maps [E * H/4 rows][I] uint8, boxes of 256 rows x 64 columns
+    if (vq)  // index maps [E * H/d rows][I] uint8, boxes of 1024/d rows x 64 columns
         ok = make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
-                          (uint64_t)d.E * (d.H / 4), kTI, kBoxRows) &&
+                          (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d) &&
              make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
-                          (uint64_t)d.E * (d.H / 4), kTI, kBoxRows);
+                          (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d);
     else
         ok = make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
                           (uint64_t)d.E * d.H, kTI, kBoxRows) &&
@@ -425,7 +425,7 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.r = lowrank ? d.r : 0;
     a.n_rb = lowrank ? (d.r + kBoxRows - 1) / kBoxRows : 0;
     cudaError_t err = vq ? launch_gateup_vq(tm_gate, tm_up, lowrank ? &tm_cgate : nullptr,
-                                            lowrank ? &tm_cup : nullptr, a, stream)
+                                            lowrank ? &tm_cup : nullptr, a, w->d, stream)
                          : launch_gateup_dense(tm_gate, tm_up, a, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);

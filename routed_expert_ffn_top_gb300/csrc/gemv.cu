@@ -57,19 +57,23 @@ constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 4;  // g, then u, throu
 constexpr int kXwBytes = kConsumerWarps * kNT * kRowsPerWarp * 4;  // dense: per-warp fp32 h rows
 // VQ gate/up: a box is 256 rows x 64 columns of uint8 code indices (16 KB), i.e. 1024 rows of
 // H; its activation slices are those 1024 h values of each route's token.
-constexpr int kVQRows = 256;
-constexpr int kVQHRows = 4 * kVQRows;
-constexpr int kVQBoxBytes = kVQRows * kTI;
-constexpr int kStageBytesVQ = kVQBoxBytes + kNT * kVQHRows * 2;
+// VQ gate/up with code words of kD elements (d = 4 or 8): a box is 1024/kD index rows x 64
+// columns of uint8 (16 KB at d = 4, 8 KB at d = 8), i.e. 1024 rows of H either way; its
+// activation slices are those 1024 h values of each route's token.
+constexpr int kVQHRows = 1024;
+__host__ __device__ constexpr int vq_rows(int d) { return kVQHRows / d; }
+__host__ __device__ constexpr int vq_box_bytes(int d) { return vq_rows(d) * kTI; }
+__host__ __device__ constexpr int vq_stage_bytes(int d) { return vq_box_bytes(d) + kNT * kVQHRows * 2; }
+__host__ __device__ constexpr int vq_codebook_bytes(int d) { return 256 * d * 2; }  // one projection
+constexpr int kStageBytesVQ = vq_stage_bytes(4);
 // VQ + low-rank gate/up: the ring also carries C boxes (256 rows of r x 64 columns, bf16)
 // with fp32 z slices, the shape of a down stage.
 constexpr int kStageBytesLR = kStageBytesDN;
-constexpr int kCodeBookBytes = 256 * 8;
 constexpr int kRedBytesDN = kConsumerWarps * kNT * kTN * 4;
 static_assert(kTI == kTN, "one box shape for both kernels");
 static_assert(kStageBytesGU % 1024 == 0 && kStageBytesDN % 1024 == 0 && kStageBytesVQ % 1024 == 0,
               "stage alignment");
-static_assert(kVQRows == kBoxRows, "the consumer lanes own 16 of the 256 rows of every box");
+static_assert(vq_rows(4) == kBoxRows && vq_rows(8) * 2 == kBoxRows, "VQ boxes of 256 or 128 rows");
 
 enum TileKind { kDenseGateUp = 0, kDown = 1, kVQGateUp = 2, kVQLRGateUp = 3 };
 
@@ -327,31 +331,58 @@ __device__ __forceinline__ void accumulate_f32_box(const unsigned char *st, cons
     }
 }
 
-// VQ box ("A Multi-Engine Dataflow ...", Section 2.3: column i of W_e is cut into length-4
+// VQ box ("A Multi-Engine Dataflow ...", Section 2.3: column i of W_e is cut into length-d
 // blocks along H, block q holding code word J[e][q][i] of the layer-shared code book):
-// acc[q][c] += sum over this thread's 16 index rows r of sum_t x_q[4r + t] * cb[J[r][c]][t]
-// (bf16 x bf16 -> fp32, H rows ascending).  `cb` is the code book in shared memory.
-template <int NT>
-__device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const uint2 *cb,
+// acc[q][c] += sum over this thread's index rows r of sum_t x_q[d r + t] * cb[J[r][c]][t]
+// (bf16 x bf16 -> fp32, H rows ascending).  `cb` is the code book in shared memory, one
+// kD-element code word per 8 (d = 4) or 16 (d = 8) bytes.  A warp owns 1/8 of the box's
+// index rows, a lane half 1/16 of them.
+template <int NT, int kD>
+__device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const void *cb,
                                                   const Lane &ln, float (&acc)[NT][4]) {
-    const unsigned char *xs = st + kVQBoxBytes + ln.rbase * 8;
-#pragma unroll 4
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const uint32_t jw = *reinterpret_cast<const uint32_t *>(st + (ln.rbase + i) * kTI + ln.c4);
-        uint2 cw[4];
+    constexpr int kRows = vq_rows(kD) / 16;  // index rows per thread: 16 (d = 4), 8 (d = 8)
+    const int rb = ln.cw * (2 * kRows) + ln.half * kRows;
+    const unsigned char *xs = st + vq_box_bytes(kD) + rb * kD * 2;
+#pragma unroll(kD == 4 ? 2 : 1)  // (deeper unrolling spills registers)
+    for (int i = 0; i < kRows; ++i) {
+        const uint32_t jw = *reinterpret_cast<const uint32_t *>(st + (rb + i) * kTI + ln.c4);
+        if constexpr (kD == 4) {
+            uint2 cw[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cw[c] = cb[(jw >> (8 * c)) & 0xffu];
+            for (int c = 0; c < 4; ++c) cw[c] = static_cast<const uint2 *>(cb)[(jw >> (8 * c)) & 0xffu];
 #pragma unroll
-        for (int q = 0; q < NT; ++q) {
-            const uint2 xv = *reinterpret_cast<const uint2 *>(xs + q * kVQHRows * 2 + i * 8);
+            for (int q = 0; q < NT; ++q) {
+                const uint2 xv = *reinterpret_cast<const uint2 *>(xs + q * kVQHRows * 2 + i * 8);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v = acc[q][c];
-                v = fma_bf16<0, 0>(xv.x, cw[c].x, v);
-                v = fma_bf16<1, 1>(xv.x, cw[c].x, v);
-                v = fma_bf16<0, 0>(xv.y, cw[c].y, v);
-                v = fma_bf16<1, 1>(xv.y, cw[c].y, v);
-                acc[q][c] = v;
+                for (int c = 0; c < 4; ++c) {
+                    float v = acc[q][c];
+                    v = fma_bf16<0, 0>(xv.x, cw[c].x, v);
+                    v = fma_bf16<1, 1>(xv.x, cw[c].x, v);
+                    v = fma_bf16<0, 0>(xv.y, cw[c].y, v);
+                    v = fma_bf16<1, 1>(xv.y, cw[c].y, v);
+                    acc[q][c] = v;
+                }
+            }
+        } else {
+            uint4 cw[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) cw[c] = static_cast<const uint4 *>(cb)[(jw >> (8 * c)) & 0xffu];
+#pragma unroll
+            for (int q = 0; q < NT; ++q) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + q * kVQHRows * 2 + i * 16);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v = acc[q][c];
+                    v = fma_bf16<0, 0>(xv.x, cw[c].x, v);
+                    v = fma_bf16<1, 1>(xv.x, cw[c].x, v);
+                    v = fma_bf16<0, 0>(xv.y, cw[c].y, v);
+                    v = fma_bf16<1, 1>(xv.y, cw[c].y, v);
+                    v = fma_bf16<0, 0>(xv.z, cw[c].z, v);
+                    v = fma_bf16<1, 1>(xv.z, cw[c].z, v);
+                    v = fma_bf16<0, 0>(xv.w, cw[c].w, v);
+                    v = fma_bf16<1, 1>(xv.w, cw[c].w, v);
+                    acc[q][c] = v;
+                }
             }
         }
     }
@@ -399,11 +430,11 @@ __device__ __forceinline__ void stage_partials(float *red, const Lane &ln, float
 // index box for every 1024 rows of H; with kLR, then a C_gate and a C_up box for every 256
 // rows of r, multiplied by z = D^T h into the same accumulators ([MED]'s joint
 // accumulation of the VQ and low-rank terms).
-template <int NT, bool kVQ, bool kLR>
+template <int NT, bool kVQ, bool kLR, int kD>
 __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                             const uint2 *cbs, const Lane &ln, int it, int r0, int r1, int &stage,
                             uint32_t &phase) {
-    constexpr int kSt = kLR ? kStageBytesLR : (kVQ ? kStageBytesVQ : kStageBytesGU);
+    constexpr int kSt = kLR ? kStageBytesLR : (kVQ ? vq_stage_bytes(kD) : kStageBytesGU);
     float ag[NT][4], au[NT][4];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
@@ -424,10 +455,11 @@ __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, 
             else
                 accumulate_f32_box<NT>(st, ln, ag);
         } else if constexpr (kVQ) {
+            const unsigned char *cb = reinterpret_cast<const unsigned char *>(cbs);
             if (j & 1)
-                accumulate_vq_box<NT>(st, cbs + 256, ln, au);
+                accumulate_vq_box<NT, kD>(st, cb + vq_codebook_bytes(kD), ln, au);
             else
-                accumulate_vq_box<NT>(st, cbs, ln, ag);
+                accumulate_vq_box<NT, kD>(st, cb, ln, ag);
         } else if (NT >= 3) {
             float *xw = cbs_or_xw_as_floats(cbs) + ln.cw * (kNT * kRowsPerWarp);
             if (j & 1)
@@ -513,7 +545,7 @@ __device__ bool down_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, fl
 
 // Consumer loop shared by both kernels: waits for a tile's first stage, reads how many routes
 // it has, and runs the tile body specialised for that count.
-template <int kKind>
+template <int kKind, int kD = 4>
 __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                               const uint2 *cbs, int64_t T, int tiles_per_sub) {
     const int warp = threadIdx.x >> 5;
@@ -544,7 +576,7 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
         if constexpr (kKind == kDown)                                                        \
             go = down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);            \
         else                                                                                 \
-            go = gateup_tile<N, kKind != kDenseGateUp, kKind == kVQLRGateUp>(                 \
+            go = gateup_tile<N, kKind != kDenseGateUp, kKind == kVQLRGateUp, kD>(             \
                 a, ctl, stages, red, cbs, ln, ct, r0, r1, stage, phase);                     \
         break;
         switch (ntok) {
@@ -645,20 +677,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 // tm_jgate / tm_jup: index maps [E*H/4 rows][I] uint8, boxes of 256 index rows x 64
 // columns.  With kLR also tm_cgate / tm_cup: C [E][r][I] bf16 as 3-D maps (I, r, E), boxes
 // of 64 columns x 256 rows of r x 1 expert (rows past r are read as zeros).
-template <bool kLR>
+template <bool kLR, int kD>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gateup_vq_kernel(const __grid_constant__ CUtensorMap tm_jgate,
                      const __grid_constant__ CUtensorMap tm_jup,
                      const __grid_constant__ CUtensorMap tm_cgate,
                      const __grid_constant__ CUtensorMap tm_cup, const GemvArgs a) {
-    constexpr int kSt = kLR ? kStageBytesLR : kStageBytesVQ;
+    constexpr int kSt = kLR ? kStageBytesLR : vq_stage_bytes(kD);
+    constexpr int kBox = vq_box_bytes(kD);
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
     float *red = reinterpret_cast<float *>(base + kStages * kSt);
     uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kSt + kRedBytesGU);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kSt + kRedBytesGU + 2 * kCodeBookBytes);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kSt + kRedBytesGU +
+                                        2 * vq_codebook_bytes(kD));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -670,9 +704,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             prefetch_tensormap(&tm_cup);
         }
     }
-    // the layer-shared code books (weights, not produced by an earlier kernel)
-    for (int i = threadIdx.x; i < 512; i += blockDim.x)
-        cbs[i] = i < 256 ? a.cb_gate[i] : a.cb_up[i - 256];
+    // the layer-shared code books (weights, not produced by an earlier kernel), 8 bytes at
+    // a time: gate's K d-element words, then up's
+    constexpr int kCbWords = vq_codebook_bytes(kD) / 8;
+    for (int i = threadIdx.x; i < 2 * kCbWords; i += blockDim.x)
+        cbs[i] = i < kCbWords ? a.cb_gate[i] : a.cb_up[i - kCbWords];
     __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
@@ -695,9 +731,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                     tma_load_3d(dst, (jj & 1) ? (const void *)&tm_cup : (const void *)&tm_cgate,
                                 it * kTI, (jj >> 1) * kBoxRows, e, bar, pol_w);
                 } else {
-                    mbar_arrive_expect_tx(bar, kVQBoxBytes);
+                    mbar_arrive_expect_tx(bar, kBox);
                     tma_load_2d(dst, (j & 1) ? (const void *)&tm_jup : (const void *)&tm_jgate,
-                                it * kTI, e * (a.H / 4) + (j >> 1) * kVQRows, bar, pol_w);
+                                it * kTI, e * (a.H / kD) + (j >> 1) * vq_rows(kD), bar, pol_w);
                 }
             });
         }
@@ -710,7 +746,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         slice_loader(a, ctl, stages, kSt, T, a.n_it, per_tile,
                      [&](int j) {
                          return (kLR && j >= nvq) ? SliceLayout{kBoxBytes, kBoxRows * 4, 2}
-                                                  : SliceLayout{kVQBoxBytes, kVQHRows * 2, 4};
+                                                  : SliceLayout{kBox, kVQHRows * 2, 4};
                      },
                      [&](int route, int token, int64_t t, int j, int piece) -> const unsigned char * {
                          if (kLR && j >= nvq) {
@@ -725,7 +761,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                      });
         return;
     }
-    consume_tiles<kLR ? kVQLRGateUp : kVQGateUp>(a, ctl, stages, red, cbs, T, a.n_it);
+    consume_tiles<kLR ? kVQLRGateUp : kVQGateUp, kD>(a, ctl, stages, red, cbs, T, a.n_it);
 }
 
 // ------------------------------------------------------------------------------- down
@@ -847,27 +883,34 @@ cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &t
     return cudaLaunchKernelEx(&cfg, gateup_dense_kernel, tm_gate, tm_up, a);
 }
 
-static size_t gateup_vq_smem(bool lr) {
-    return 1024 + kStages * (lr ? kStageBytesLR : kStageBytesVQ) + kRedBytesGU +
-           2 * kCodeBookBytes + sizeof(Ctl);
+static size_t gateup_vq_smem(bool lr, int d) {
+    return 1024 + kStages * (lr ? kStageBytesLR : vq_stage_bytes(d)) + kRedBytesGU +
+           2 * vq_codebook_bytes(d) + sizeof(Ctl);
+}
+
+template <bool kLR, int kD>
+static cudaError_t launch_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                             const CUtensorMap &tm_cgate, const CUtensorMap &tm_cup,
+                             const GemvArgs &a, cudaStream_t stream) {
+    const size_t smem = gateup_vq_smem(kLR, kD);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gateup_vq_kernel<kLR, kD>), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, gateup_vq_kernel<kLR, kD>, tm_jgate, tm_jup, tm_cgate, tm_cup, a);
 }
 
 cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
                              const CUtensorMap *tm_cgate, const CUtensorMap *tm_cup,
-                             const GemvArgs &a, cudaStream_t stream) {
-    const bool lr = a.r > 0;
-    const size_t smem = gateup_vq_smem(lr);
-    const void *fn = lr ? reinterpret_cast<const void *>(gateup_vq_kernel<true>)
-                        : reinterpret_cast<const void *>(gateup_vq_kernel<false>);
-    cudaError_t err = ensure_smem(fn, smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attrs[2];
-    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
-    if (lr)
-        return cudaLaunchKernelEx(&cfg, gateup_vq_kernel<true>, tm_jgate, tm_jup, *tm_cgate,
-                                  *tm_cup, a);
-    // the low-rank maps are unused without the term: pass the index maps in their place
-    return cudaLaunchKernelEx(&cfg, gateup_vq_kernel<false>, tm_jgate, tm_jup, tm_jgate, tm_jup, a);
+                             const GemvArgs &a, int d, cudaStream_t stream) {
+    // without the low-rank term its maps are unused: the index maps stand in for them
+    const CUtensorMap &cg = tm_cgate ? *tm_cgate : tm_jgate;
+    const CUtensorMap &cu = tm_cup ? *tm_cup : tm_jup;
+    if (a.r > 0)
+        return d == 8 ? launch_vq<true, 8>(tm_jgate, tm_jup, cg, cu, a, stream)
+                      : launch_vq<true, 4>(tm_jgate, tm_jup, cg, cu, a, stream);
+    return d == 8 ? launch_vq<false, 8>(tm_jgate, tm_jup, cg, cu, a, stream)
+                  : launch_vq<false, 4>(tm_jgate, tm_jup, cg, cu, a, stream);
 }
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream) {

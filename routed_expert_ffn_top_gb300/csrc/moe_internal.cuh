@@ -74,7 +74,7 @@ struct GemvArgs {
     const unsigned char *w_down;  // W_down [E, I, H] bf16 (idle gate/up CTAs warm it in L2)
     const float *z;        // VQ + low rank: z = D^T h [M, 2r] (gate, then up); else NULL
     int r, n_rb;           // rank of the low-rank term (0: none); its 256-row boxes
-    const uint2 *cb_gate;  // VQ code books [256] code words of 4 bf16 (NULL when dense)
+    const uint2 *cb_gate;  // VQ code books [256][d] bf16 read 8 bytes at a time (NULL: dense)
     const uint2 *cb_up;
     int M, k, E, H, I, b, rsub;
     int n_it, n_hb, n_ht, n_ib;
@@ -186,11 +186,12 @@ cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const in
 cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                 const GemvArgs &a, cudaStream_t stream);
 
-// Blockwise-VQ gate/up (d = 4, K = 256): index maps through TMA, code books in shared memory;
-// with a.r > 0 also the low-rank term (C maps through TMA, z slices from a.z).
+// Blockwise-VQ gate/up (d = 4 or 8, K = 256): index maps through TMA (boxes of 1024/d index
+// rows x 64 columns), code books in shared memory; with a.r > 0 also the low-rank term (C
+// maps through TMA, z slices from a.z).
 cudaError_t launch_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
                              const CUtensorMap *tm_cgate, const CUtensorMap *tm_cup,
-                             const GemvArgs &a, cudaStream_t stream);
+                             const GemvArgs &a, int d, cudaStream_t stream);
 
 cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStream_t stream);
 

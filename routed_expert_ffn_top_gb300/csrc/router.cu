@@ -315,8 +315,14 @@ static cudaError_t launch_router_tm(const __nv_bfloat16 *h, const __nv_bfloat16 
                                     int32_t *ids, float *wts, const FusedAlign &fa,
                                     LowRankProj lr, bool route, cudaStream_t stream) {
     const int ntiles = (M + TM - 1) / TM;
-    const int cols = (lr.r > E || !route) ? lr.r : E;
-    const size_t smem = router_smem(TM, H, cols, route && fa.enabled != 0);
+    // the routing clusters and the projection clusters carve shared memory for their own
+    // column counts (E, r); the launch gets the larger of the two layouts (not the layout of
+    // the larger count: more columns take more, smaller passes)
+    size_t smem = route ? router_smem(TM, H, E, fa.enabled != 0) : 0;
+    if (lr.r > 0) {
+        const size_t zs = router_smem(TM, H, lr.r, false);
+        if (zs > smem) smem = zs;
+    }
     cudaError_t err =
         ensure_smem(reinterpret_cast<const void *>(router_topk_kernel<TM, kPerLane>), smem);
     if (err != cudaSuccess) return err;

@@ -62,6 +62,9 @@ WORKLOADS = {
     "vq_d4": Workload("vq_d4", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=4, K=256),
     "vqlr_d4_r256": Workload("vqlr_d4_r256", H=2048, I=768, E=128, k=8, b=8, M=1,
                              kind=W_VQLR, d=4, K=256, r=256),
+    "vq_d8": Workload("vq_d8", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=8, K=256),
+    "vqlr_d8_r384": Workload("vqlr_d8_r384", H=2048, I=768, E=128, k=8, b=8, M=1,
+                             kind=W_VQLR, d=8, K=256, r=384),
     "large_m256": Workload("large_m256", H=4096, I=1536, E=128, k=8, b=64, M=256,
                            router_bias=True),
 }

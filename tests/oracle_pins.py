@@ -429,6 +429,20 @@ def pin_vq_equals_decoded_dense():
     assert np.array_equal(out_vq, out_dense)
 
 
+def pin_vq_d8_equals_decoded_dense():
+    # The same definition with 8-element code words (the pages' deployed d = 8).
+    wl = vq_workload(d=8, H=64, K=16)
+    layer, h = small_layer(wl, seed=16)
+    wg, wu, wd = dense_numpy(layer)
+    dense = {"kind": syn.W_DENSE, "H": wl.H, "I": wl.I, "E": wl.E,
+             "w_gate": bf16_bits(wg), "w_up": bf16_bits(wu), "w_down": syn.bits(layer["w_down"])}
+    ids = np.array([[1, 3], [4, 0], [2, 2]], np.int32)
+    a = np.array([[0.7, 0.3], [0.5, 0.5], [0.4, 0.6]])
+    out_vq = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out_dense = oracle.expert_ffn(syn.bits(h), dense, ids, a)
+    assert np.array_equal(out_vq, out_dense)
+
+
 def pin_vq_projection_codebook():
     # "A Multi-Engine Dataflow ...", Section 4.2 (reuse of shared projections): with
     # T[q, c] = h_q . B_c for every length-d block q of h, the projection output is

@@ -90,9 +90,9 @@ def test_validation_fails_closed_without_gpu(lib):
     need = lib.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8)
     assert lib.moe_expert_ffn(fake, ctypes.byref(w), 4, 8, ids, ids, ids, None, None, 8, None,
                               fake, vp(1 << 20), need, None) == moe.MOE_ERR_INVALID_ARG
-    # VQ with unsupported d
+    # VQ with unsupported d (4 and 8 are supported)
     wv = _weights(kind=1)
-    wv.d = 8
+    wv.d = 2
     assert lib.moe_decode_block(fake, fake, None, ctypes.byref(wv), 1, 8, 8, None, fake, ids, ids,
                                 vp(1 << 20), 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
     # VQ with H not a multiple of 1024 (index boxes cover 1024 rows of H)

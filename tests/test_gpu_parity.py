@@ -290,15 +290,17 @@ def test_host_entry_point_matches_device():
 
 
 VQ_SMALL = [
-    # M, k, E, H, I, b
-    (5, 2, 8, 1024, 256, 3), (13, 4, 16, 2048, 512, 8), (2, 8, 8, 1024, 768, 1), (30, 3, 24, 1024, 256, 16),
+    # M, k, E, H, I, b, d
+    (5, 2, 8, 1024, 256, 3, 4), (13, 4, 16, 2048, 512, 8, 4), (2, 8, 8, 1024, 768, 1, 4),
+    (30, 3, 24, 1024, 256, 16, 4), (5, 2, 8, 1024, 256, 3, 8), (13, 4, 16, 2048, 512, 8, 8),
+    (30, 3, 24, 3072, 256, 16, 8),
 ]
 
 
-@pytest.mark.parametrize("M,k,E,H,I,b", VQ_SMALL)
-def test_vq_expert_ffn_small(M, k, E, H, I, b):
-    wl = syn.Workload("vq_small_%d_%d_%d" % (M, k, E), H=H, I=I, E=E, k=k, b=b, M=M,
-                      kind=syn.W_VQ, d=4, K=256)
+@pytest.mark.parametrize("M,k,E,H,I,b,d", VQ_SMALL)
+def test_vq_expert_ffn_small(M, k, E, H, I, b, d):
+    wl = syn.Workload("vq_small_%d_%d_%d_%d" % (M, k, E, d), H=H, I=I, E=E, k=k, b=b, M=M,
+                      kind=syn.W_VQ, d=d, K=256)
     layer = syn.make_layer(wl, seed=2, device=DEV)
     h = syn.make_hidden(wl, seed=2, device=DEV)
     rng = np.random.default_rng(M + E)
@@ -335,17 +337,18 @@ def test_vq_block_every_m_1_to_16():
 
 
 VQLR_SMALL = [
-    # M, k, E, H, I, b, r
-    (5, 2, 8, 1024, 256, 3, 128), (13, 4, 16, 2048, 512, 8, 256), (2, 8, 8, 1024, 768, 1, 384),
-    (30, 3, 24, 1024, 256, 16, 512), (1, 1, 8, 1024, 256, 8, 256),
+    # M, k, E, H, I, b, r, d
+    (5, 2, 8, 1024, 256, 3, 128, 4), (13, 4, 16, 2048, 512, 8, 256, 4),
+    (2, 8, 8, 1024, 768, 1, 384, 4), (30, 3, 24, 1024, 256, 16, 512, 4),
+    (1, 1, 8, 1024, 256, 8, 256, 4), (13, 4, 16, 2048, 512, 8, 384, 8), (3, 2, 8, 1024, 256, 1, 128, 8),
 ]
 
 
-@pytest.mark.parametrize("M,k,E,H,I,b,r", VQLR_SMALL)
-def test_vqlr_expert_ffn_small(M, k, E, H, I, b, r):
+@pytest.mark.parametrize("M,k,E,H,I,b,r,d", VQLR_SMALL)
+def test_vqlr_expert_ffn_small(M, k, E, H, I, b, r, d):
     """VQ + low-rank gate/up through moe_expert_ffn (the projections get their own launch)."""
-    wl = syn.Workload("vqlr_small_%d_%d_%d_%d" % (M, k, E, r), H=H, I=I, E=E, k=k, b=b, M=M,
-                      kind=syn.W_VQLR, d=4, K=256, r=r)
+    wl = syn.Workload("vqlr_small_%d_%d_%d_%d_%d" % (M, k, E, r, d), H=H, I=I, E=E, k=k, b=b,
+                      M=M, kind=syn.W_VQLR, d=d, K=256, r=r)
     layer = syn.make_layer(wl, seed=3, device=DEV)
     h = syn.make_hidden(wl, seed=3, device=DEV)
     rng = np.random.default_rng(M + E + r)
@@ -367,11 +370,13 @@ def test_vqlr_expert_ffn_small(M, k, E, H, I, b, r):
     assert G.rel_l2(G.to_f64(out_vq), ref) > 3 * G.REL_L2
 
 
-def test_vqlr_block_every_m_1_to_16():
-    """The VQ + low-rank workload (d=4, r=256): the projections ride in the router launch;
-    parity at every M from 1 to 16, bitwise determinism and batch invariance."""
-    wl = syn.WORKLOADS["vqlr_d4_r256"]
-    layer = _workload_layer("vqlr_d4_r256")
+@pytest.mark.parametrize("name", ["vqlr_d4_r256", "vqlr_d8_r384"])
+def test_vqlr_block_every_m_1_to_16(name):
+    """The VQ + low-rank workloads ((d, r) = (4, 256) and the pages' deployed (8, 384)): the
+    projections ride in the router launch; parity at every M from 1 to 16, bitwise
+    determinism and batch invariance."""
+    wl = syn.WORKLOADS[name]
+    layer = _workload_layer(name)
     for M in range(1, 17):
         h = syn.make_hidden(wl, M=M, seed=M, device=DEV)
         ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
@@ -381,7 +386,7 @@ def test_vqlr_block_every_m_1_to_16():
         use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
                                               logits, wl.k)
         ref = G.oracle_ffn(layer, h, use_ids, use_wts)
-        G.assert_close_block(G.to_f64(out), ref, "vqlr_d4_r256 M=%d" % M)
+        G.assert_close_block(G.to_f64(out), ref, "%s M=%d" % (name, M))
     out2, _, _ = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
     assert torch.equal(out2, out)
     o1, _, _ = moe.moe_decode_block(h[3:4].contiguous(), layer, wl.k, wl.b)
