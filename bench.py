@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--M", type=int, default=None, help="override the token count")
     p.add_argument("--graph", action="store_true",
                    help="time CUDA-graph replays of the block instead of direct calls")
+    p.add_argument("--b", type=int, default=None,
+                   help="override the alignment block size (64 selects the tcgen05 regime)")
     p.add_argument("--E", type=int, default=None,
                    help="override the expert count (smaller captures of the same kernels)")
     p.add_argument("--weight-sets", type=int, default=8,
@@ -170,12 +172,15 @@ def overrides(args) -> dict:
         out["M"] = args.M
     if args.E:
         out["E"] = args.E
+    if args.b:
+        out["b"] = args.b
     return out
 
 
 def gemm_regime(wl) -> bool:
-    """Dense weights with 64-row aligned blocks run as tcgen05 grouped GEMMs."""
-    return wl.kind == syn.W_DENSE and wl.b == 64
+    """Dense weights with 64-row aligned blocks, or with at least 4 routes per expert on
+    average (the library then aligns in 64-row blocks itself), run as tcgen05 grouped GEMMs."""
+    return wl.kind == syn.W_DENSE and (wl.b == 64 or wl.M * wl.k >= 4 * wl.E)
 
 
 def gateup_kernel_name(wl) -> str:

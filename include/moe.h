@@ -165,6 +165,12 @@ int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
 /*
  * The whole block: router (renormalised softmax top-k) -> alignment -> expert FFN ->
  * combine.  Same arguments as above; topk_ids [M,k] and topk_weights [M,k] are outputs.
+ * Regimes: with b == 64 and dense weights the experts run as grouped GEMMs on the tensor
+ * cores, otherwise as GEMV streams.  When the library aligns the routes itself (here, and
+ * in moe_expert_ffn without a caller alignment), dense weights with at least 4 routes per
+ * expert on average (M*k >= 4E) also take the grouped-GEMM regime whatever b is: b only
+ * shapes the internal alignment.  Results are bitwise reproducible and independent of M
+ * within a regime; across regimes they agree within the parity tolerance.
  */
 int moe_decode_block(const void *h, const void *w_router, const float *bias,
                      const moe_expert_weights_t *w, int M, int k, int b,

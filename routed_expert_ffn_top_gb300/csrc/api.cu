@@ -285,13 +285,34 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
                                     static_cast<cudaStream_t>(stream)));
 }
 
-extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b) {
+// The block size the library aligns with when it aligns the routes itself: the caller's b,
+// except that dense weights with at least 4 routes per expert on average run the grouped-
+// GEMM regime, whose aligned blocks are 64 rows.  (Measured at H=2048, I=768, E=128, k=8:
+// M=64 takes 253 us per layer as GEMV streams and 228 us as tcgen05 GEMMs, M=128 414 and
+// 239 us; at M=32 the GEMV streams are ahead, 189 against 205 us.)
+static int effective_block(const moe_expert_weights_t *w, int M, int k, int b) {
+    if (w && w->kind == MOE_W_DENSE_BF16 && b != kGemmBlock &&
+        (int64_t)M * k >= 4 * (int64_t)w->E)
+        return kGemmBlock;
+    return b;
+}
+
+size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, int b) {
     if (!w || M < 0 || k <= 0 || k > 32 || k > w->E || check_block(b) != MOE_OK) return 0;
     if (w->H <= 0 || w->I <= 0 || w->E <= 0) return 0;
     if ((int64_t)M * k >= (1 << 24)) return 0;
     Dims d = make_dims(M, k, w->E, w->H, w->I, b);
     d.r = lr_rank(w);
     return ws_layout(d).total;
+}
+
+extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b) {
+    // enough for the caller's b (a caller-supplied alignment) and for the block size the
+    // library picks when it aligns itself
+    const size_t a = workspace_bytes_fixed(w, M, k, b);
+    if (a == 0) return 0;
+    const size_t e = workspace_bytes_fixed(w, M, k, effective_block(w, M, k, b));
+    return a > e ? a : e;
 }
 
 // Runs gate/up and down for aligned routes (alignment pointers already resolved).
@@ -468,6 +489,7 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     const int given = (sorted_route_ids != nullptr) + (expert_block_ids != nullptr) +
                       (num_padded != nullptr);
     if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
+    if (given == 0) b = effective_block(w, M, k, b);
     Dims d = make_dims(M, k, w->E, w->H, w->I, b);
     d.r = lr_rank(w);
     const WsLayout L = ws_layout(d);
@@ -506,18 +528,22 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     return run_experts(h, w, d, topk_ids, topk_weights, srt, blk, npad, residual, out, ws, L, s);
 }
 
-extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,
-                                const moe_expert_weights_t *w, int M, int k, int b,
-                                const void *residual, void *out, int32_t *topk_ids,
-                                float *topk_weights, void *workspace, size_t ws_bytes,
-                                void *stream) {
-    int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace, ws_bytes);
+int moe::decode_block(const void *h, const void *w_router, const float *bias,
+                      const moe_expert_weights_t *w, int M, int k, int b, const void *residual,
+                      void *out, int32_t *topk_ids, float *topk_weights, void *workspace,
+                      size_t ws_bytes, void *stream, bool pick_regime) {
+    // with a fixed b the workspace only needs that b's layout
+    int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace,
+                              pick_regime ? ws_bytes : (size_t)-1);
+    if (rc == MOE_OK && !pick_regime && ws_bytes < workspace_bytes_fixed(w, M, k, b))
+        rc = MOE_ERR_WORKSPACE;
     if (rc != MOE_OK) return rc;
     rc = check_router_shape(M, w->H, w->E, k);
     if (rc != MOE_OK || M == 0) return rc;
     if (!w_router || !topk_ids || !topk_weights || !aligned(w_router, 16) ||
         !aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
+    if (pick_regime) b = effective_block(w, M, k, b);
     Dims d = make_dims(M, k, w->E, w->H, w->I, b);
     d.r = lr_rank(w);
     const WsLayout L = ws_layout(d);
@@ -552,6 +578,15 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
     trace(2, s);
     return run_experts(h, w, d, topk_ids, topk_weights, ws_sorted, ws_blocks, ws_npad, residual, out,
                        ws, L, s);
+}
+
+extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,
+                                const moe_expert_weights_t *w, int M, int k, int b,
+                                const void *residual, void *out, int32_t *topk_ids,
+                                float *topk_weights, void *workspace, size_t ws_bytes,
+                                void *stream) {
+    return decode_block(h, w_router, bias, w, M, k, b, residual, out, topk_ids, topk_weights,
+                        workspace, ws_bytes, stream, true);
 }
 
 extern "C" int moe_decode_block_host(const void *h_host, const void *residual_host,

@@ -197,6 +197,15 @@ cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStrea
 
 cudaError_t launch_combine(const GemvArgs &a, cudaStream_t stream);
 
+// The decode block with the block size fixed to the caller's b (no switch to the grouped-
+// GEMM regime) and the workspace size that needs: the allocation-free entry, whose scratch
+// has a fixed size, runs through these.
+int decode_block(const void *h, const void *w_router, const float *bias,
+                 const moe_expert_weights_t *w, int M, int k, int b, const void *residual,
+                 void *out, int32_t *topk_ids, float *topk_weights, void *workspace,
+                 size_t ws_bytes, void *stream, bool pick_regime);
+size_t workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, int b);
+
 // Raises `func`'s dynamic shared-memory limit to at least `bytes` on the current device.
 // The attribute is set once per (kernel, device) and remembered: repeating the runtime call
 // on every launch costs host time that small decode blocks cannot hide.

@@ -134,11 +134,15 @@ def test_expert_ffn_small(M, k, E, H, I, b):
     assert moe.moe_read_device_status(ws) == 0
     ref = G.oracle_ffn(layer, h, ids, a, residual=res)
     G.assert_close_block(G.to_f64(out), ref, "expert_ffn %s" % (SMALL,))
-    # the same call with the caller's own alignment buffers gives the same bits
+    # the same call with the caller's own alignment buffers: the same bits when both run the
+    # same regime (the library's own alignment takes 64-row blocks at 4+ routes per expert)
     srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
     out2 = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad), residual=res,
                               workspace=ws)
-    assert torch.equal(out, out2)
+    if b == 64 or M * k < 4 * E:
+        assert torch.equal(out, out2)
+    else:
+        G.assert_close_block(G.to_f64(out2), ref, "expert_ffn, caller alignment")
 
 
 def test_expert_ffn_invalid_ids_and_status():
@@ -403,6 +407,30 @@ def test_large_m256_sampled_tokens():
     wl = syn.WORKLOADS["large_m256"]
     out2, _, _ = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
     assert torch.equal(out, out2)
+
+
+def test_decode_block_picks_the_gemm_regime_for_large_batches():
+    """At 4+ routes per expert the library aligns in 64-row blocks and runs the tcgen05
+    kernels whatever b is; below that, b's GEMV streams run."""
+    wl = syn.workload("layer_m21", M=64)
+    layer = _workload_layer("layer_m21")
+    h = syn.make_hidden(wl, M=64, seed=64, device=DEV)
+    out8, ids, wts = moe.moe_decode_block(h, layer, wl.k, 8)
+    out64, _, _ = moe.moe_decode_block(h, layer, wl.k, 64)
+    assert torch.equal(out8, out64)  # the same regime, the same bits
+    assert torch.equal(moe.moe_expert_ffn(h, layer, ids, wts, 8), out8)
+    tokens = np.array([0, 17, 63])
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+    use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
+                                          logits, wl.k)
+    ref = G.oracle_ffn(layer, h, use_ids, use_wts, tokens=tokens)
+    G.assert_close_block(G.to_f64(out8)[tokens], ref, "M=64 grouped-GEMM regime")
+    # below the threshold (M=32: 2 routes per expert) the GEMV regime keeps b = 8
+    h32 = h[:32].contiguous()
+    o32, ids32, wts32 = moe.moe_decode_block(h32, layer, wl.k, 8)
+    srt, blk, npad = moe.moe_align_block_size(ids32, wl.E, 8)
+    assert torch.equal(moe.moe_expert_ffn(h32, layer, ids32, wts32, 8, alignment=(srt, blk, npad)),
+                       o32)
 
 
 def test_gemm_regime_batch_and_membership_invariance():
