@@ -235,6 +235,22 @@ int moe_set_trace_events(void *const *events, int n);
  */
 int moe_read_device_status(void *workspace, void *stream, int32_t *status_out);
 
+/*
+ * Failure-detection self-test.  Launches, on `stream`, one CTA shaped like the grouped-GEMM
+ * kernels that takes its tensor memory and then waits on an mbarrier that nothing ever
+ * completes.  The kernels' own bounded wait gives up after about one second of %globaltimer.
+ * The CTA then stops its other warps, frees its tensor memory and sets MOE_DEV_WAIT_TIMEOUT
+ * in the workspace's status word.  No copy, MMA or memory access besides the status word
+ * is ever issued, so the CUDA context stays usable.
+ *
+ * workspace: a device pointer, 256-byte aligned, with ws_bytes >= 4.  Only its status word
+ * (the first int32) is written.
+ * Returns MOE_ERR_INVALID_ARG for a NULL, misaligned or too small workspace, MOE_ERR_CUDA if
+ * the launch fails, else MOE_OK once the launch is enqueued (asynchronous, like every
+ * entry point; read the bit back with moe_read_device_status).
+ */
+int moe_selftest_wait_timeout(void *workspace, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -629,3 +629,10 @@ extern "C" int moe_read_device_status(void *workspace, void *stream, int32_t *st
     *status_out = v;
     return v == 0 ? MOE_OK : MOE_ERR_DEVICE;
 }
+
+extern "C" int moe_selftest_wait_timeout(void *workspace, size_t ws_bytes, void *stream) {
+    if (!workspace || ws_bytes < sizeof(int32_t) || !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_wait_selftest(static_cast<int32_t *>(workspace),
+                                                 static_cast<cudaStream_t>(stream)));
+}

@@ -421,6 +421,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
     gemm_finish(ctl, warp, a.status);
 }
 
+// ------------------------------------------------------------------ bounded-wait self-test
+// One CTA shaped like the GEMM kernels takes its tensor memory and then waits on the first
+// accumulator's "full" barrier, which no MMA commit ever completes.  The waits and the
+// teardown are the GEMM kernels' own: the first elected lane whose wait runs out raises the
+// abort flag, the other warps see it and stop waiting, the CTA frees its tensor memory and
+// MOE_DEV_WAIT_TIMEOUT lands in the status word.  No copy or MMA is ever in flight.
+__global__ void __launch_bounds__(kGThreads, 1) wait_selftest_kernel(int32_t *status) {
+    __shared__ GCtl ctl;
+    const int warp = threadIdx.x >> 5;
+    gemm_init(ctl, warp);
+    if ((threadIdx.x & 31) == 0) gwait(&ctl.tfull[0], 0, ctl);
+    __syncwarp();
+    gemm_finish(ctl, warp, status);
+}
+
 static size_t gemm_gateup_smem() {
     return 1024 + kGStages * kGStageBytes + kGN * 64 * 4 + kGChunkBytes + sizeof(GCtl);
 }
@@ -452,6 +467,11 @@ cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cuda
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, gemm_down_kernel, tm_down, a);
+}
+
+cudaError_t launch_wait_selftest(int32_t *status, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, kGThreads, 0, stream>>>(status);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -103,6 +103,8 @@ cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
+// One CTA whose bounded wait runs out on purpose (sets MOE_DEV_WAIT_TIMEOUT in *status).
+cudaError_t launch_wait_selftest(int32_t *status, cudaStream_t stream);
 
 // Sub-blocks to process: num_padded / rsub, never more than the table holds.
 __device__ __forceinline__ int64_t num_subblocks(const GemvArgs &a) {

@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_status_string", "moe_route_topk", "moe_align_capacity", "moe_align_block_size",
     "moe_workspace_bytes", "moe_expert_ffn", "moe_decode_block", "moe_decode_block_host",
     "moe_read_device_status", "moe_set_trace_events", "moe_decode_block_noalloc",
+    "moe_selftest_wait_timeout",
 )
 
 
@@ -100,9 +101,11 @@ def lib():
             L.moe_read_device_status.argtypes = [vp, vp, vp]
             L.moe_set_trace_events.argtypes = [vp, ci]
             L.moe_decode_block_noalloc.argtypes = [vp, vp, vp, wp, ci, ci, ci, vp, vp, vp, vp, vp]
+            L.moe_selftest_wait_timeout.argtypes = [vp, sz, vp]
             for f in ("moe_route_topk", "moe_align_block_size", "moe_expert_ffn",
                       "moe_decode_block", "moe_decode_block_host", "moe_read_device_status",
-                      "moe_set_trace_events", "moe_decode_block_noalloc"):
+                      "moe_set_trace_events", "moe_decode_block_noalloc",
+                      "moe_selftest_wait_timeout"):
                 getattr(L, f).restype = ci
             _lib = L
     return _lib
@@ -344,6 +347,13 @@ def moe_read_device_status(workspace, stream=None) -> int:
     if rc not in (MOE_OK, MOE_ERR_DEVICE):
         raise MoeError(rc, "moe_read_device_status")
     return int(out.value)
+
+
+def moe_selftest_wait_timeout(workspace, stream=None):
+    """Enqueue the failure-detection self-test (include/moe.h): one CTA whose bounded wait
+    runs out after about a second and sets MOE_DEV_WAIT_TIMEOUT in the workspace's status."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_set_trace_events(events=None):

@@ -142,3 +142,12 @@ def test_oracle_and_product_are_separate():
             text = open(os.path.join(root, "oracle", f)).read()
             assert not re.search(r"^\s*(import|from)\s+routed_expert_ffn_top_gb300", text, re.M), f
             assert not re.search(r'#\s*include\s*"moe', text), f
+
+
+def test_selftest_wait_timeout_validates_before_launch(lib):
+    L = moe.lib()
+    assert L.moe_selftest_wait_timeout(None, 256, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_wait_timeout(ctypes.c_void_p((1 << 20) + 16), 256, None) == \
+        moe.MOE_ERR_INVALID_ARG  # not 256-byte aligned
+    assert L.moe_selftest_wait_timeout(ctypes.c_void_p(1 << 20), 0, None) == \
+        moe.MOE_ERR_INVALID_ARG  # no room for the status word
