@@ -178,18 +178,23 @@ def overrides(args) -> dict:
 
 
 def gemm_regime(wl) -> bool:
-    """Dense weights with 64-row aligned blocks, or with at least 4 routes per expert on
-    average (the library then aligns in 64-row blocks itself), run as tcgen05 grouped GEMMs."""
-    return wl.kind == syn.W_DENSE and (wl.b == 64 or wl.M * wl.k >= 4 * wl.E)
+    """Dense weights run as tcgen05 grouped GEMMs over tiles of the aligned blocks."""
+    return wl.kind == syn.W_DENSE
+
+
+def library_block(wl) -> int:
+    """The block size moe_decode_block aligns with: for dense weights 64 rows from 4 routes
+    per expert on average, else 16; VQ weights keep the workload's b."""
+    if wl.kind == syn.W_DENSE:
+        return 64 if wl.M * wl.k >= 4 * wl.E else 16
+    return wl.b
 
 
 def gateup_kernel_name(wl) -> str:
-    if gemm_regime(wl):
-        return "gemm_gateup_kernel"
-    return "gateup_dense_kernel" if wl.kind == syn.W_DENSE else "gateup_vq_kernel"
+    return "gemm_gateup_kernel" if gemm_regime(wl) else "gateup_vq_kernel"
 
 
-def kernel_source_hash(kernel: str = "gateup_dense_kernel"):
+def kernel_source_hash(kernel: str = "gemm_gateup_kernel"):
     h = hashlib.sha256()
     src = "gemm_tc05.cu" if kernel.startswith("gemm_") else "gemv.cu"
     for name in (src, "ptx.cuh", "moe_internal.cuh"):
@@ -255,11 +260,12 @@ def run_ours(args, world, rank, local):
     ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
     wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    # router (+ alignment when one router cluster holds every token), alignment otherwise,
-    # [row gather in the grouped-GEMM regime], gate/up, down, combine
+    # router (+ alignment, and the row tiles of the grouped GEMMs, when one router cluster
+    # holds every token), else alignment [+ row gather for dense weights]; gate/up, down,
+    # combine
     fused_align = 1 <= M <= 8 and M * wl.k <= 256
     gemm = gemm_regime(wl)
-    launches_per_block = (4 if fused_align else 5) + (1 if gemm else 0)
+    launches_per_block = (4 if fused_align else 5) + (1 if gemm and not fused_align else 0)
 
     def eager_step(i, s):
         """One step: a single layer, or all L layers of the residual stack."""
@@ -298,11 +304,12 @@ def run_ours(args, world, rank, local):
     gu_b, dn_b = expert_bytes(wl)
     per_set_unique = []
     padded_rows = []  # aligned rows sum_e ceil(n_e / b) * b of each probe
+    b_lib = library_block(wl)
 
     def note_routing():
         per_set_unique.append(int(torch.unique(ids).numel()))
         n_e = torch.bincount(ids.flatten().long(), minlength=wl.E)
-        padded_rows.append(int(((n_e + wl.b - 1) // wl.b * wl.b).sum().item()))
+        padded_rows.append(int(((n_e + b_lib - 1) // b_lib * b_lib).sum().item()))
 
     if stack:
         h = h0
@@ -431,8 +438,8 @@ def run_ours(args, world, rank, local):
     mean_ms = {k: statistics.mean(v) for k, v in dur.items()}
     peak, peak_kind = measured_peaks()
     u_mean = statistics.mean(per_set_unique)
-    # weights of the routed experts + h read once + p written (fp32 per route in the GEMV
-    # regime, bf16 per route in the GEMM regime)
+    # weights of the routed experts + h read once + p written (fp32 per route from the VQ
+    # kernel, bf16 per route from the tcgen05 one)
     gu_kernel = gateup_kernel_name(wl)
     p_bytes = 2 if gemm else 4
     gu_alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * p_bytes

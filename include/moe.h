@@ -139,7 +139,8 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
 /*
  * Workspace bytes that moe_expert_ffn / moe_decode_block need for (weights shape, M, k, b).
  * The workspace holds the alignment (when the library computes it), the per-route
- * intermediate p [M*k, I] fp32 and expert outputs y [M*k, H] fp32, and the device status
+ * intermediates (dense weights: tiles of token rows and of p in bf16; VQ weights: p [M*k, I]
+ * fp32), the expert outputs y [M*k, H] fp32, and the device status
  * word (its first 4 bytes), which must be zero before the first call (allocate it
  * zero-filled).  Calls that share a workspace must be ordered on one stream.
  * Returns 0 on unsupported arguments.
@@ -165,12 +166,15 @@ int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
 /*
  * The whole block: router (renormalised softmax top-k) -> alignment -> expert FFN ->
  * combine.  Same arguments as above; topk_ids [M,k] and topk_weights [M,k] are outputs.
- * Regimes: with b == 64 and dense weights the experts run as grouped GEMMs on the tensor
- * cores, otherwise as GEMV streams.  When the library aligns the routes itself (here, and
- * in moe_expert_ffn without a caller alignment), dense weights with at least 4 routes per
- * expert on average (M*k >= 4E) also take the grouped-GEMM regime whatever b is: b only
- * shapes the internal alignment.  Results are bitwise reproducible and independent of M
- * within a regime; across regimes they agree within the parity tolerance.
+ * Dense weights run as grouped GEMMs on the tensor cores over tiles of the aligned blocks:
+ * 16-row tiles for blocks of up to 16 rows, 64-row tiles otherwise.  When the library
+ * aligns the routes itself (here, and in moe_expert_ffn without a caller alignment) it
+ * picks the block size for dense weights: 64 rows from 4 routes per expert on average
+ * (M*k >= 4E), 16 rows below; b only matters for a caller's own alignment.  Every route of
+ * dense weights is one K-ordered chain of MMAs per projection, so a token's output bits do
+ * not depend on M, on the other tokens, on its block or its position in it, on b or on the
+ * tile width.  VQ gate/up weights run as GEMV streams on the CUDA cores with the caller's b;
+ * their results are bitwise reproducible and independent of M and of block membership.
  */
 int moe_decode_block(const void *h, const void *w_router, const float *bias,
                      const moe_expert_weights_t *w, int M, int k, int b,
@@ -203,8 +207,8 @@ int moe_decode_block_host(const void *h_host, const void *residual_host, void *o
  * the library, MOE_NOALLOC_SCRATCH_BYTES per GPU, held by every GPU that loads the library
  * until the process exits.  It calls no cudaMalloc / cudaFree.
  *   * Sizes whose workspace (moe_workspace_bytes) exceeds MOE_NOALLOC_SCRATCH_BYTES return
- *     MOE_ERR_WORKSPACE before anything is launched (for H=2048, I=768, k=8, b=8 that is
- *     M > 92 tokens).
+ *     MOE_ERR_WORKSPACE before anything is launched (for H=2048, I=768, E=128, k=8 that is
+ *     M > 150 tokens at b=8, M > 205 at b=16).
  *   * The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
  *   * Every call on a device uses the same array: calls that overlap on the GPU (other
@@ -212,7 +216,7 @@ int moe_decode_block_host(const void *h_host, const void *residual_host, void *o
  *   * The array keeps the previous call's contents; each call clears the status word
  *     itself.  Device status cannot be read back through this entry point.
  */
-#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 int moe_decode_block_noalloc(const void *h, const void *w_router, const float *bias,
                              const moe_expert_weights_t *w, int M, int k, int b,
                              const void *residual, void *out, int32_t *topk_ids,
@@ -222,7 +226,8 @@ int moe_decode_block_noalloc(const void *h, const void *w_router, const float *b
  * Tracing.  When `events` is not NULL, each later moe_decode_block / moe_expert_ffn call
  * made from this host thread records the caller's CUDA events (cudaEvent_t passed as
  * void*) on its stream: events[0] before its first kernel, events[1] after the router,
- * events[2] after the alignment, events[3] after the gate/up kernel, events[4] after the
+ * events[2] after the alignment (and the row gather of dense weights), events[3] after the
+ * gate/up kernel, events[4] after the
  * down kernel, events[5] after the combine kernel (stages a call does not run are not
  * recorded; n must be 6).  An event between two kernels removes the launch overlap the
  * kernels otherwise get, so traced calls run slightly slower.  Pass NULL (n = 0) to stop.

@@ -156,12 +156,14 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
 // its expert (n_e) and those of them before r, the first route of each expert publishes
 // ceil(n_e / b) * b, and the padded offset of an expert is the sum published by the experts
 // below it.  Positions, padding, block vector, sub-block records and tail are the same
-// function of the ids as in align_core.
+// function of the ids as in align_core.  Every output may be NULL; pos_out (shared memory,
+// R entries) receives each route's aligned row, -1 for an invalid route.
 __host__ __device__ constexpr int align_small_smem_ints(int nthreads) { return nthreads + 4; }
 
 __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int b, int rsub,
                                    int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
-                                   SubBlock *sbt, int32_t *status, int32_t *sm) {
+                                   SubBlock *sbt, int32_t *status, int32_t *sm,
+                                   int32_t *pos_out = nullptr) {
     int32_t *pub = sm;  // [blockDim.x] padded count published by each expert's first route
     const int nthr = blockDim.x;
     const int tid = threadIdx.x;
@@ -192,6 +194,7 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
         total += p;
         if (p != 0 && ids[q] < e) off += p;
     }
+    if (pos_out && tid < R) pos_out[tid] = (valid && off + lower < cap) ? off + lower : -1;
     if (valid) {
         const int64_t pos = (int64_t)off + lower;
         if (pos < cap) {
@@ -219,7 +222,7 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
     if (blocks)
         for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += nthr) blocks[q] = -1;
     if (tid == 0) {
-        npad[0] = total;
+        if (npad) npad[0] = total;
         if (status && any_invalid) atomicOr(status, MOE_DEV_INVALID_EXPERT);
     }
 }

@@ -12,7 +12,7 @@ namespace moe {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-Dims make_dims(int M, int k, int E, int H, int I, int b) {
+Dims make_dims(int M, int k, int E, int H, int I, int b, int kind) {
     Dims d;
     d.M = M;
     d.k = k;
@@ -20,6 +20,9 @@ Dims make_dims(int M, int k, int E, int H, int I, int b) {
     d.H = H;
     d.I = I;
     d.b = b;
+    d.gemm = kind == MOE_W_DENSE_BF16;
+    d.kn = gemm_tile_width(b);
+    d.tpb = gemm_tiles_per_block(b);
     d.rsub = (b <= kNT) ? b : kNT;
     d.R = (int64_t)M * k;
     d.cap = d.R + (int64_t)(d.R < E ? d.R : E) * (b - 1);
@@ -43,18 +46,17 @@ WsLayout ws_layout(const Dims &d) {
     L.sorted = take((size_t)d.cap * 4);
     L.blocks = take((size_t)(d.cap / d.b) * 4);
     L.npad = take(16);
-    L.sbt = take((size_t)d.max_sub * sizeof(SubBlock));
-    L.p = take((size_t)d.R * d.I * 4);
+    // the sub-block table and fp32 p serve the GEMV kernels, the row tiles the tcgen05 ones
+    L.sbt = take(d.gemm ? 0 : (size_t)d.max_sub * sizeof(SubBlock));
+    L.p = take(d.gemm ? 0 : (size_t)d.R * d.I * 4);
     L.y = take((size_t)d.R * d.H * 4);
     L.z = take((size_t)d.M * 2 * d.r * 4);
-    const size_t tile_rows = (d.b == kGemmBlock) ? (size_t)(d.cap / kGemmBlock) * kGemmBlock : 0;
+    const size_t tile_rows = d.gemm ? (size_t)(d.cap / d.b) * d.tpb * d.kn : 0;
     L.x_tiles = take(tile_rows * d.H * 2);
     L.p_tiles = take(tile_rows * d.I * 2);
     L.total = off;
     return L;
 }
-
-bool gemm_regime(int kind, int b) { return kind == MOE_W_DENSE_BF16 && b == kGemmBlock; }
 
 int num_sms() {
     static int cache[64] = {0};
@@ -285,15 +287,14 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
                                     static_cast<cudaStream_t>(stream)));
 }
 
-// The block size the library aligns with when it aligns the routes itself: the caller's b,
-// except that dense weights with at least 4 routes per expert on average run the grouped-
-// GEMM regime, whose aligned blocks are 64 rows.  (Measured at H=2048, I=768, E=128, k=8:
-// M=64 takes 253 us per layer as GEMV streams and 228 us as tcgen05 GEMMs, M=128 414 and
-// 239 us; at M=32 the GEMV streams are ahead, 189 against 205 us.)
+// The block size the library aligns with when it aligns the routes itself.  Dense weights run
+// as tcgen05 tiles whatever b is, so the library picks the tile width: 64-row blocks from 4
+// routes per expert on average (the routes of an expert fill the MMA's N side), 16-row blocks
+// below that (an expert's weights stream once for up to 16 of its routes).  VQ weights keep
+// the caller's b.
 static int effective_block(const moe_expert_weights_t *w, int M, int k, int b) {
-    if (w && w->kind == MOE_W_DENSE_BF16 && b != kGemmBlock &&
-        (int64_t)M * k >= 4 * (int64_t)w->E)
-        return kGemmBlock;
+    if (w && w->kind == MOE_W_DENSE_BF16)
+        return (int64_t)M * k >= 4 * (int64_t)w->E ? kGemmBlock : kGemmNarrow;
     return b;
 }
 
@@ -301,7 +302,7 @@ size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, i
     if (!w || M < 0 || k <= 0 || k > 32 || k > w->E || check_block(b) != MOE_OK) return 0;
     if (w->H <= 0 || w->I <= 0 || w->E <= 0) return 0;
     if ((int64_t)M * k >= (1 << 24)) return 0;
-    Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
     d.r = lr_rank(w);
     return ws_layout(d).total;
 }
@@ -328,20 +329,21 @@ static const LowRankProj *lowrank_proj(const moe_expert_weights_t *w, const Dims
     return out;
 }
 
-// The large-batch regime: tcgen05 grouped GEMMs over the 64-row aligned blocks, then the
-// fixed-order combine.
+// Dense weights: the row gather (unless the router wrote the rows), tcgen05 grouped GEMMs
+// over the tiles of the aligned blocks, then the fixed-order combine.
 static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
                     const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
                     const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
-                    unsigned char *ws, const WsLayout &L, cudaStream_t stream) {
+                    unsigned char *ws, const WsLayout &L, bool rows_ready, cudaStream_t stream) {
     CUtensorMap tm_gate, tm_up, tm_down;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const int box_rows = kGemmStageK;  // K rows per weight box: one stage's depth
     if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, 64, 256, sw) ||
+                      (uint64_t)d.E * d.H, 64, box_rows, sw) ||
         !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, 64, 256, sw) ||
+                      (uint64_t)d.E * d.H, 64, box_rows, sw) ||
         !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
-                      (uint64_t)d.E * d.I, 64, 256, sw))
+                      (uint64_t)d.E * d.I, 64, box_rows, sw))
         return MOE_ERR_CUDA;
     GemmArgs g;
     g.x = static_cast<const __nv_bfloat16 *>(h);
@@ -358,10 +360,15 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     g.E = d.E;
     g.H = d.H;
     g.I = d.I;
+    g.b = d.b;
+    g.kn = d.kn;
+    g.tpb = d.tpb;
+    g.wait_first = rows_ready ? 1 : 0;
     g.R = d.R;
     g.cap = d.cap;
-    cudaError_t err = launch_gather_rows(g, stream);
+    cudaError_t err = rows_ready ? cudaSuccess : launch_gather_rows(g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (!rows_ready) trace(2, stream);  // the row gather counts with the alignment
     err = launch_gemm_gateup(tm_gate, tm_up, g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
@@ -385,14 +392,16 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     return MOE_OK;
 }
 
+// rows_ready: the router already wrote the x tiles of the grouped GEMMs.
 static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims &d,
                        const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
                        const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
-                       unsigned char *ws, const WsLayout &L, cudaStream_t stream) {
-    if (gemm_regime(w->kind, d.b))
+                       unsigned char *ws, const WsLayout &L, cudaStream_t stream,
+                       bool rows_ready = false) {
+    if (d.gemm)
         return run_gemm(h, w, d, topk_ids, topk_weights, sorted, blocks, npad, residual, out, ws,
-                        L, stream);
-    const bool vq = w->kind == MOE_W_VQ_GATEUP || w->kind == MOE_W_VQLR_GATEUP;
+                        L, rows_ready, stream);
+    // VQ (and VQ + low-rank) gate/up: GEMV streams on the CUDA cores
     const bool lowrank = w->kind == MOE_W_VQLR_GATEUP;
     CUtensorMap tm_cgate, tm_cup;  // C [E][r][I]: boxes of 64 columns x 256 rows of r
     if (lowrank && (!make_tmap_3d_bf16(&tm_cgate, w->c_gate, (uint64_t)d.I, (uint64_t)d.r,
@@ -401,17 +410,12 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
                                        (uint64_t)d.E, kTI, kBoxRows, 1)))
         return MOE_ERR_CUDA;
     CUtensorMap tm_gate, tm_up, tm_down;
-    bool ok;
-    if (vq)  // index maps [E * H/d rows][I] uint8, boxes of 1024/d rows x 64 columns
-        ok = make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
-                          (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d) &&
-             make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
-                          (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d);
-    else
-        ok = make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                          (uint64_t)d.E * d.H, kTI, kBoxRows) &&
-             make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                          (uint64_t)d.E * d.H, kTI, kBoxRows);
+    // index maps [E * H/d rows][I] uint8, boxes of 1024/d rows x 64 columns
+    const bool ok =
+        make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                     (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d) &&
+        make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                     (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d);
     if (!ok || !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
                              (uint64_t)d.E * d.I, kTN, kBoxRows))
         return MOE_ERR_CUDA;
@@ -439,15 +443,14 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.n_ib = d.n_ib;
     a.max_sub = d.max_sub;
     a.w_down = static_cast<const unsigned char *>(w->w_down);
-    a.cb_gate = vq ? static_cast<const uint2 *>(w->cb_gate) : nullptr;
-    a.cb_up = vq ? static_cast<const uint2 *>(w->cb_up) : nullptr;
+    a.cb_gate = static_cast<const uint2 *>(w->cb_gate);
+    a.cb_up = static_cast<const uint2 *>(w->cb_up);
     a.n_qb = d.H / (4 * kBoxRows);
     a.z = lowrank ? reinterpret_cast<const float *>(ws + L.z) : nullptr;
     a.r = lowrank ? d.r : 0;
     a.n_rb = lowrank ? (d.r + kBoxRows - 1) / kBoxRows : 0;
-    cudaError_t err = vq ? launch_gateup_vq(tm_gate, tm_up, lowrank ? &tm_cgate : nullptr,
-                                            lowrank ? &tm_cup : nullptr, a, w->d, stream)
-                         : launch_gateup_dense(tm_gate, tm_up, a, stream);
+    cudaError_t err = launch_gateup_vq(tm_gate, tm_up, lowrank ? &tm_cgate : nullptr,
+                                       lowrank ? &tm_cup : nullptr, a, w->d, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
     err = launch_down(tm_down, a, stream);
@@ -490,7 +493,7 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
                       (num_padded != nullptr);
     if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
     if (given == 0) b = effective_block(w, M, k, b);
-    Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
     d.r = lr_rank(w);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -504,12 +507,12 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
         int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
         err = launch_align(topk_ids, M, k, w->E, b, reinterpret_cast<int32_t *>(ws + L.sorted),
                            reinterpret_cast<int32_t *>(ws + L.blocks), ws_npad, d.cap,
-                           gemm_regime(w->kind, b) ? nullptr : sbt, d.rsub, status, s);
+                           d.gemm ? nullptr : sbt, d.rsub, status, s);
         npad = ws_npad;
     } else {
         if (!aligned(sorted_route_ids, 4) || !aligned(expert_block_ids, 4) || !aligned(num_padded, 4))
             return MOE_ERR_INVALID_ARG;
-        err = gemm_regime(w->kind, b)
+        err = d.gemm
                   ? cudaSuccess
                   : launch_plan(topk_ids, sorted_route_ids, expert_block_ids, num_padded, M, k,
                                 w->E, b, d.rsub, d.max_sub, sbt, status, s);
@@ -544,7 +547,7 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
         !aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
     if (pick_regime) b = effective_block(w, M, k, b);
-    Dims d = make_dims(M, k, w->E, w->H, w->I, b);
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
     d.r = lr_rank(w);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -558,11 +561,14 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
     LowRankProj lr_store;
     const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store);  // rides in the router launch
     cudaError_t err;
-    if (router_can_align(M, k)) {  // one launch routes and aligns
+    const bool fused = router_can_align(M, k);
+    if (fused) {  // one launch routes, aligns and (dense weights) writes the x tiles
+        RowTiles rows{nullptr, d.kn, d.tpb};
+        if (d.gemm) rows.x_tiles = reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles);
         err = launch_router_align(static_cast<const __nv_bfloat16 *>(h),
                                   static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H, w->E,
                                   k, 1, topk_ids, topk_weights, b, d.rsub, ws_sorted, ws_blocks,
-                                  ws_npad, d.cap, ws_sbt, ws_status, lr, s);
+                                  ws_npad, d.cap, d.gemm ? nullptr : ws_sbt, ws_status, lr, rows, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
     } else {
@@ -572,12 +578,12 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
         err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
-                           gemm_regime(w->kind, b) ? nullptr : ws_sbt, d.rsub, ws_status, s);
+                           d.gemm ? nullptr : ws_sbt, d.rsub, ws_status, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
     }
     trace(2, s);
     return run_experts(h, w, d, topk_ids, topk_weights, ws_sorted, ws_blocks, ws_npad, residual, out,
-                       ws, L, s);
+                       ws, L, s, fused && d.gemm);
 }
 
 extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,

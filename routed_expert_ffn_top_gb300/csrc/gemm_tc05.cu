@@ -1,68 +1,82 @@
-// gemm_tc05.cu -- expert projections of the large-batch regime as grouped GEMMs on the
-// fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory).
+// gemm_tc05.cu -- the expert projections of dense weights as grouped GEMMs on the
+// fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory), at every
+// batch size.
 //
 // The computation is the expert step of "A Multi-Engine Dataflow for MoE Decoding on
 // Scratchpad-Based Tensor Accelerators" (stage-3 activation; Section 4.3), for the rows of
-// the aligned 64-row blocks of "Route-Block Membership Selects Packed-AWQ Arithmetic"
-// (Section 2.1): every block holds routes of one expert, so a block is a dense GEMM tile.
+// the aligned blocks of "Route-Block Membership Selects Packed-AWQ Arithmetic" (Section
+// 2.1): every block holds routes of one expert, so a block is a dense GEMM tile.  A block
+// of b rows is cut into tiles of kN rows (kN = 16 for b <= 16, else 64; the MMA's N).
 //
 // Orientation ("swap AB"): the expert weights are the MMA's A operand (M = 128 output
-// channels) and the block's 64 routes are the N side, so the weights stream through HBM
-// once per block and the routes ride along:
-//   gate/up:  D[128][64] = [W_gate[e][:, i0:i0+64] | W_up[e][:, i0:i0+64]]^T  x  X^T
+// channels) and the tile's kN rows are the N side, so the weights stream through HBM once
+// per tile and the routes ride along:
+//   gate/up:  D[128][kN] = [W_gate[e][:, i0:i0+64] | W_up[e][:, i0:i0+64]]^T  x  X^T
 //             (lanes 0-63 accumulate g, lanes 64-127 accumulate u, of channels i0..i0+63)
-//   down:     D[128][64] = W_down[e][:, h0:h0+128]^T  x  P^T
+//   down:     D[128][kN] = W_down[e][:, h0:h0+128]^T  x  P^T
 // A comes straight from the [E,H,I] / [E,I,H] weights: TMA boxes of 64 columns x 256 rows
 // (32 KB) with 128-byte swizzle form the MN-major canonical layout, one 64-wide M half per
 // box.  One SM's TMA unit keeps only a few copies in flight, so copies are made as large
 // as the swizzled layout allows.
 //
-// B is read from "tiled" row buffers: for every aligned block, K is cut into 64-wide
-// chunks and each chunk is stored as the 8 KB K-major 128-byte-swizzle image of its 64
-// rows (row n at n*128 bytes, 16-byte piece j at (j ^ n%8)*16).  A stage of 256 K is then
-// one contiguous 32 KB bulk copy that lands in shared memory already in the MMA layout.
-//   x tiles: the token rows of h, gathered per aligned row by gather_rows_kernel;
+// B is read from "tiled" row buffers: for every tile, K is cut into 64-wide chunks and each
+// chunk is stored as the K-major 128-byte-swizzle image of its kN rows (row n at n*128
+// bytes, 16-byte piece j at (j ^ n%8)*16).  A stage of 256 K is then one contiguous bulk
+// copy that lands in shared memory already in the MMA layout.
+//   x tiles: the token rows of h, written per aligned row by gather_rows_kernel, or by the
+//            router when one router cluster holds every token;
 //   p tiles: p = SiLU(g) * u in bf16, written by the gate/up epilogue, read by down.
-// Rows of padding are never written: their columns of D are independent of the others
-// and are dropped by the epilogues, so whatever the memory holds there cannot reach a
-// result.
+// Rows of padding, and tile rows past their block's b rows, are never given a route: their
+// columns of D are independent of the others and are dropped by the epilogues, so whatever
+// the memory holds there cannot reach a result.
 //
 // Per CTA (6 warps): warp 0 issues the copies, one thread of warp 1 issues the MMAs
 // (K = 16 each) into one of two tensor-memory accumulators, and warps 2-5 drain the
 // finished accumulator (a warp reads the TMEM lanes of its rank modulo 4).  Persistent CTAs
-// take units (block, channel tile) round-robin, channel tile fastest, so the units of one
-// block run side by side and share its row tiles in L2.
+// take units (tile, channel tile) round-robin, channel tile fastest, so the units of one
+// tile run side by side and share its row tiles in L2.
 //
-// Each output element is one K-ordered chain of MMAs into its accumulator, independent of
-// the other columns of the block, of the grid and of M: the results are bitwise
-// reproducible and a route's bits do not depend on the block position it occupies.
+// Each output element is one K-ordered chain of MMAs into its accumulator: 16 K-steps per
+// 256-row stage, stages in ascending K, whatever kN is.  A tcgen05 MMA's element does not
+// depend on the other columns of B, on N or on its row of the tile (checked bitwise on this
+// GPU for N = 16..64, column shifts and row rotations), so a route's bits do not depend on
+// the grid, on M, on the other routes of its tile, on its block position or on kN.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
-constexpr int kGN = kGemmBlock;                      // routes per MMA (one aligned block)
 constexpr int kGM = 128;                             // output channels per MMA
-constexpr int kGK = 256;                             // K per stage
-constexpr int kGStages = 2;
-constexpr int kGHalfBytes = 64 * kGK * 2;            // one 64-wide M half: 32 KB
-constexpr int kGABytes = 2 * kGHalfBytes;            // 64 KB
-constexpr int kGBBytes = kGN * kGK * 2;              // 32 KB
-constexpr int kGStageBytes = kGABytes + kGBBytes;    // 96 KB
-constexpr int kGChunkBytes = kGN * 64 * 2;           // one 64-wide K chunk of a block: 8 KB
 constexpr int kGThreads = 192;                       // 6 warps
 constexpr int kGEpiWarp0 = 2;
-constexpr uint32_t kGTmemCols = 2 * kGN;             // two 128 x 64 fp32 accumulators
+constexpr int kGMaxStages = 3;
+
+// The shapes of one tile width kN (the MMA's N: 16 or 64 aligned rows).  A stage is the two
+// 32 KB weight boxes (64 columns x 256 rows of K, one per 64-wide M half) and the tile's
+// 256-deep slice of rows; narrow tiles keep three stages in flight, wide ones two.  (Stages
+// of 128 rows, six in flight, were slower for narrow tiles at 1 to 8 tokens.)
+template <int kN>
+struct GTile {
+    static_assert(kN == 16 || kN == 64, "tile widths: 16 or 64 rows");
+    static constexpr int kK = kGemmStageK;                    // K per stage
+    static constexpr int kHalfBytes = 64 * kK * 2;            // one M half: 32 KB
+    static constexpr int kABytes = 2 * kHalfBytes;            // 64 KB
+    static constexpr int kBBytes = kN * kK * 2;               // 8 KB or 32 KB
+    static constexpr int kStageBytes = kABytes + kBBytes;     // 72 KB or 96 KB
+    static constexpr int kStages = kN == 16 ? 3 : 2;
+    static constexpr int kChunkBytes = kN * 64 * 2;         // one 64-wide K chunk: 2 or 8 KB
+    static constexpr uint32_t kTmemCols = 2 * kN < 32 ? 32 : 2 * kN;  // two accumulators
+};
 
 struct GCtl {
-    uint64_t full[kGStages];
-    uint64_t empty[kGStages];
+    uint64_t full[kGMaxStages];
+    uint64_t empty[kGMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t done;
     uint32_t tmem;
     volatile int abort;
-    int route[2][kGN];    // down epilogue: route of each block row, per accumulator
+    int route[2][kGemmBlock];  // down epilogue: route of each tile row, per accumulator
 };
 
 __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, GCtl &ctl) {
@@ -78,8 +92,9 @@ __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, GCtl &ctl)
     }
 }
 
+template <int kN>
 __device__ __forceinline__ void gadvance(int &stage, uint32_t &phase) {
-    if (++stage == kGStages) {
+    if (++stage == GTile<kN>::kStages) {
         stage = 0;
         phase ^= 1u;
     }
@@ -97,15 +112,32 @@ __device__ __forceinline__ int gemm_route(const GemmArgs &a, int64_t pos, int e,
     return r;
 }
 
+// The block vector entry of this CTA's first unit (unit blockIdx.x), read before the unit
+// count is known so that the two loads overlap; the index is clamped into the array and
+// the value is used only when the unit exists.
+__device__ __forceinline__ int first_unit_expert(const GemmArgs &a, int n_ct) {
+    const int64_t nblk = a.cap / a.b;
+    int64_t blk = ((int64_t)blockIdx.x / n_ct) / a.tpb;
+    if (blk >= nblk) blk = nblk - 1;
+    return a.blocks[blk];
+}
+
 __device__ __forceinline__ int64_t gemm_blocks(const GemmArgs &a) {
-    const int64_t n = a.npad[0] / kGN;
-    const int64_t cap_blocks = a.cap / kGN;
+    const int64_t n = a.npad[0] / a.b;
+    const int64_t cap_blocks = a.cap / a.b;
     return n < 0 ? 0 : (n > cap_blocks ? cap_blocks : n);
 }
 
-// Byte offset of (row n, 16-byte piece j) inside a block's 8 KB K chunk.
-__device__ __forceinline__ uint32_t tile_offset(int n, int j) {
-    return (uint32_t)(n * 128 + ((j ^ (n & 7)) << 4));
+// Aligned row held by row n of tile t, or -1 when that tile row lies past its block's b rows.
+__device__ __forceinline__ int64_t tile_row(const GemmArgs &a, int64_t t, int n) {
+    const int local = (int)(t % a.tpb) * a.kn + n;
+    return local < a.b ? (t / a.tpb) * a.b + local : -1;
+}
+
+// The route of row n of tile t of expert e, or -1 (past the block, padding, or flagged).
+__device__ __forceinline__ int tile_route(const GemmArgs &a, int64_t t, int n, int e, bool flag) {
+    const int64_t pos = tile_row(a, t, n);
+    return pos < 0 ? -1 : gemm_route(a, pos, e, flag);
 }
 
 // ------------------------------------------------------------------------ row gather
@@ -114,18 +146,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmArgs a) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int64_t nrows = gemm_blocks(a) * kGN;
+    const int64_t nrows = gemm_blocks(a) * a.b;
     const int nchunk = a.H / 64;
+    const int64_t chunk_bytes = (int64_t)a.kn * 128;
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t pos = warp0; pos < nrows; pos += nwarps) {
-        const int64_t blk = pos / kGN;
-        const int n = (int)(pos % kGN);
+        const int64_t blk = pos / a.b;
+        const int local = (int)(pos % a.b);
+        const int64_t t = blk * a.tpb + local / a.kn;
+        const int n = local % a.kn;
         const int r = gemm_route(a, pos, a.blocks[blk], lane == 0);
         if (r < 0) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)(r / a.k) * a.H);
-        unsigned char *dst = reinterpret_cast<unsigned char *>(a.x_tiles) +
-                             blk * (int64_t)nchunk * kGChunkBytes;
+        unsigned char *dst = reinterpret_cast<unsigned char *>(a.x_tiles) + t * nchunk * chunk_bytes;
         const int j = lane & 7;
         const uint32_t off = tile_offset(n, j);
         // 8 pieces per lane in flight at once (chunks c, c+4, ..., c+28), then their stores
@@ -137,32 +171,35 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmArgs a) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if (c0 + 4 * i < nchunk)
-                    *reinterpret_cast<uint4 *>(dst + (int64_t)(c0 + 4 * i) * kGChunkBytes + off) = v[i];
+                    *reinterpret_cast<uint4 *>(dst + (int64_t)(c0 + 4 * i) * chunk_bytes + off) = v[i];
         }
     }
 }
 
 // ------------------------------------------------------------------- pipeline roles
-// Copies of one unit: per stage the two 32 KB weight boxes (issue_a) and the 32 KB row
-// tile of the block (btiles + (blk * nks + s) * 32 KB).  The weights depend only on the
-// alignment, which was complete before this grid started; the row tiles are written by
-// the previous grid, so the first stages' tile copies wait for it (griddepcontrol) while
-// their weight copies are already in flight.
-template <typename IssueA>
+// Copies of one unit (tile, channel tile): per stage the two 32 KB weight boxes (issue_a)
+// and the tile's K slice of rows (btiles + (tile * nks + s) * kBBytes).  After a row
+// gather the weights depend only on the alignment, which was complete before this grid
+// started; the row tiles are written by the previous grid, so the first stages' tile
+// copies wait for it (griddepcontrol) while their weight copies are already in flight.
+// already_waited: the kernel waited for the previous grid before this point (the gate/up
+// kernel when the router wrote the alignment and the x tiles).
+template <int kN, typename IssueA>
 __device__ void gemm_producer(const GemmArgs &a, GCtl &ctl, unsigned char *stages,
                               const unsigned char *btiles, int64_t T, int n_ct, int nks,
-                              IssueA issue_a) {
+                              bool already_waited, int e_first, IssueA issue_a) {
+    using G = GTile<kN>;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, parity_bits = 0;
-    bool waited = false;
+    bool waited = already_waited;
     int npend = 0;
-    const unsigned char *pend_src[kGStages];
-    int pend_stage[kGStages];
+    const unsigned char *pend_src[G::kStages];
+    int pend_stage[G::kStages];
     for (int64_t u = blockIdx.x; u < T && !ctl.abort; u += gridDim.x) {
-        const int64_t blk = u / n_ct;
+        const int64_t tile = u / n_ct;
         const int ct = (int)(u % n_ct);
-        int e = a.blocks[blk];
+        int e = u == (int64_t)blockIdx.x ? e_first : a.blocks[tile / a.tpb];
         if (e < 0 || e >= a.E) {
             atomicOr(a.status, MOE_DEV_BAD_ALIGNMENT);
             e = 0;  // keep the pipeline in step; every row of such a block is dropped
@@ -170,45 +207,47 @@ __device__ void gemm_producer(const GemmArgs &a, GCtl &ctl, unsigned char *stage
         for (int s = 0; s < nks; ++s) {
             if (!gwait(&ctl.empty[stage], phase ^ 1u, ctl)) break;
             uint64_t *bar = &ctl.full[stage];
-            unsigned char *st = stages + stage * kGStageBytes;
-            mbar_arrive_expect_tx(bar, kGStageBytes);
+            unsigned char *st = stages + stage * G::kStageBytes;
+            mbar_arrive_expect_tx(bar, G::kStageBytes);
             issue_a(st, bar, e, ct, s);
-            const unsigned char *src = btiles + (blk * nks + s) * (int64_t)kGBBytes;
+            const unsigned char *src = btiles + (tile * nks + s) * (int64_t)G::kBBytes;
             if (waited) {
-                bulk_load(st + kGABytes, src, kGBBytes, bar);
+                bulk_load(st + G::kABytes, src, G::kBBytes, bar);
             } else {
                 pend_src[npend] = src;
                 pend_stage[npend] = stage;
-                if (++npend == kGStages) {
+                if (++npend == G::kStages) {
                     pdl_wait();
                     waited = true;
                     for (int q = 0; q < npend; ++q)
-                        bulk_load(stages + pend_stage[q] * kGStageBytes + kGABytes, pend_src[q],
-                                  kGBBytes, &ctl.full[pend_stage[q]]);
+                        bulk_load(stages + pend_stage[q] * G::kStageBytes + G::kABytes, pend_src[q],
+                                  G::kBBytes, &ctl.full[pend_stage[q]]);
                     npend = 0;
                 }
             }
             issued |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
-            gadvance(stage, phase);
+            gadvance<kN>(stage, phase);
         }
     }
     if (!waited) {
         pdl_wait();
         for (int q = 0; q < npend; ++q)
-            bulk_load(stages + pend_stage[q] * kGStageBytes + kGABytes, pend_src[q], kGBBytes,
+            bulk_load(stages + pend_stage[q] * G::kStageBytes + G::kABytes, pend_src[q], G::kBBytes,
                       &ctl.full[pend_stage[q]]);
     }
     // every copy has landed before the CTA can exit
-    for (int s = 0; s < kGStages; ++s)
+    for (int s = 0; s < G::kStages; ++s)
         if ((issued >> s) & 1u)
             if (!mbar_wait_bounded(&ctl.full[s], (parity_bits >> s) & 1u)) ctl.abort = 1;
 }
 
 // MMA issuer (one thread): for each unit, nks stages x 16 MMAs of K = 16 into accumulator
 // buffer (unit parity); each stage is released when its MMAs complete.
+template <int kN>
 __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
-    constexpr uint32_t idesc = umma_idesc_bf16(kGM, kGN, true, false);
+    using G = GTile<kN>;
+    constexpr uint32_t idesc = umma_idesc_bf16(kGM, kN, true, false);
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
@@ -217,7 +256,7 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
         const uint32_t tph = (uint32_t)(local >> 1) & 1u;
         if (!gwait(&ctl.tempty[buf], tph ^ 1u, ctl)) break;
         tc_fence_after();
-        const uint32_t d = ctl.tmem + (uint32_t)(buf * kGN);
+        const uint32_t d = ctl.tmem + (uint32_t)(buf * kN);
         bool ok = true;
         for (int s = 0; s < nks; ++s) {
             if (!gwait(&ctl.full[stage], phase, ctl)) {
@@ -225,19 +264,20 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
                 break;
             }
             tc_fence_after();
-            const uint32_t A = smem_u32(stages + stage * kGStageBytes);
-            const uint32_t B = A + kGABytes;
+            const uint32_t A = smem_u32(stages + stage * G::kStageBytes);
+            const uint32_t B = A + G::kABytes;
 #pragma unroll
-            for (int ks = 0; ks < kGK / 16; ++ks) {
+            for (int ks = 0; ks < G::kK / 16; ++ks) {
                 // A: MN-major, M halves 32 KB apart, 8-row K atoms 1 KB apart, 16 K rows per MMA
-                const uint64_t ad = umma_smem_desc(A + ks * 2048, kGHalfBytes, 1024, 2);
-                // B: K-major, 64-wide K chunks 8 KB apart, 32 bytes per K step, 8-row atoms 1 KB
+                const uint64_t ad = umma_smem_desc(A + ks * 2048, G::kHalfBytes, 1024, 2);
+                // B: K-major, 64-wide K chunks kChunkBytes apart, 32 bytes per K step, 8-row
+                // atoms 1 KB apart
                 const uint64_t bd =
-                    umma_smem_desc(B + (ks >> 2) * kGChunkBytes + (ks & 3) * 32, 16, 1024, 2);
+                    umma_smem_desc(B + (ks >> 2) * G::kChunkBytes + (ks & 3) * 32, 16, 1024, 2);
                 umma_bf16(d, ad, bd, idesc, s > 0 || ks > 0);
             }
             umma_commit(&ctl.empty[stage]);
-            gadvance(stage, phase);
+            gadvance<kN>(stage, phase);
         }
         if (!ok) break;
         umma_commit(&ctl.tfull[buf]);
@@ -247,9 +287,10 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
     if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
 }
 
+template <int kN>
 __device__ __forceinline__ void gemm_init(GCtl &ctl, int warp) {
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGStages; ++s) {
+        for (int s = 0; s < GTile<kN>::kStages; ++s) {
             mbar_init(&ctl.full[s], 1);   // the producer's expect_tx arrival
             mbar_init(&ctl.empty[s], 1);  // MMA completion
         }
@@ -261,28 +302,30 @@ __device__ __forceinline__ void gemm_init(GCtl &ctl, int warp) {
         ctl.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&ctl.tmem, kGTmemCols);
+    if (warp == 1) tmem_alloc(&ctl.tmem, GTile<kN>::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 }
 
+template <int kN>
 __device__ __forceinline__ void gemm_finish(GCtl &ctl, int warp, int32_t *status) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(ctl.tmem, kGTmemCols);
+    if (warp == 1) tmem_dealloc(ctl.tmem, GTile<kN>::kTmemCols);
     if (threadIdx.x == 0 && ctl.abort) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
 }
 
-// Epilogue warp: the 64 fp32 columns of its 32 TMEM lanes of accumulator `buf`, then the
+// Epilogue warp: the kN fp32 columns of its 32 TMEM lanes of accumulator `buf`, then the
 // accumulator is handed back to the MMA issuer.
-__device__ __forceinline__ void drain_accumulator(GCtl &ctl, int quad, int buf, float (&v)[kGN]) {
+template <int kN>
+__device__ __forceinline__ void drain_accumulator(GCtl &ctl, int quad, int buf, float (&v)[kN]) {
     tc_fence_after();
 #pragma unroll
-    for (int c0 = 0; c0 < kGN; c0 += 16) {
+    for (int c0 = 0; c0 < kN; c0 += 16) {
         float t16[16];
-        tmem_ld16(ctl.tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(buf * kGN + c0), t16);
+        tmem_ld16(ctl.tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(buf * kN + c0), t16);
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[c0 + i] = t16[i];
     }
@@ -292,133 +335,146 @@ __device__ __forceinline__ void drain_accumulator(GCtl &ctl, int quad, int buf, 
 }
 
 // ---------------------------------------------------------------------------- gate/up
+template <int kN>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_gateup_kernel(const __grid_constant__ CUtensorMap tm_gate,
                        const __grid_constant__ CUtensorMap tm_up, const GemmArgs a) {
+    using G = GTile<kN>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
-    float *gbuf = reinterpret_cast<float *>(base + kGStages * kGStageBytes);  // [64 rows][64 ch]
-    unsigned char *pst = base + kGStages * kGStageBytes + kGN * 64 * 4;       // one p chunk
-    GCtl &ctl = *reinterpret_cast<GCtl *>(pst + kGChunkBytes);
+    float *gbuf = reinterpret_cast<float *>(base + G::kStages * G::kStageBytes);  // [kN][64]
+    GCtl &ctl = *reinterpret_cast<GCtl *>(base + G::kStages * G::kStageBytes + kN * 64 * 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
     }
-    gemm_init(ctl, warp);
+    gemm_init<kN>(ctl, warp);
+    // When the router wrote the alignment and the x tiles, this grid may start while it
+    // still runs: wait for it before anything reads them, and only then let the down grid
+    // start (it reads the block vector before its own wait).
+    if (a.wait_first) pdl_wait();
     pdl_launch_dependents();
 
     const int n_ct = a.I / 64;
-    const int nks = a.H / kGK;
-    const int64_t T = gemm_blocks(a) * n_ct;
+    const int nks = a.H / G::kK;
+    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
+    const int64_t T = gemm_blocks(a) * a.tpb * n_ct;
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            gemm_producer(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles), T,
-                          n_ct, nks, [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
-                const int32_t y = e * a.H + s * kGK;
+            gemm_producer<kN>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles),
+                              T, n_ct, nks, a.wait_first != 0, e_first,
+                              [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
+                const int32_t y = e * a.H + s * G::kK;
                 tma_load_2d(st, &tm_gate, ct * 64, y, bar, pol);
-                tma_load_2d(st + kGHalfBytes, &tm_up, ct * 64, y, bar, pol);
+                tma_load_2d(st + G::kHalfBytes, &tm_up, ct * 64, y, bar, pol);
             });
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) gemm_mma(ctl, stages, T, nks);
+        if (lane == 0) gemm_mma<kN>(ctl, stages, T, nks);
         __syncwarp();
     } else {
         const int quad = warp & 3;           // TMEM lanes [32 quad, 32 quad + 32)
         const int row = 32 * quad + lane;    // accumulator row: gate channel (< 64) or up channel
-        const int tid = threadIdx.x - 32 * kGEpiWarp0;
         int local = 0;
         for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
-            const int64_t blk = u / n_ct;
+            const int64_t tile = u / n_ct;
             const int ct = (int)(u % n_ct);
             const int buf = local & 1;
+            // Only rows that hold a route get p: the other columns of the tile are dropped
+            // by the down epilogue, so their p rows may keep whatever they held.
+            if (row < kN) ctl.route[buf][row] = tile_route(a, tile, row, a.blocks[tile / a.tpb], false);
             const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
             if (named_bar_or(1, 128, !ok)) break;
-            float v[kGN];
-            drain_accumulator(ctl, quad, buf, v);
+            float v[kN];
+            drain_accumulator<kN>(ctl, quad, buf, v);
             if (quad < 2) {
 #pragma unroll
-                for (int n = 0; n < kGN; ++n) gbuf[n * 64 + row] = v[n];
+                for (int n = 0; n < kN; ++n)
+                    if (ctl.route[buf][n] >= 0) gbuf[n * 64 + row] = v[n];
             }
             named_bar_sync(1, 128);
             if (quad >= 2) {
+                // p of each route row straight into the tile's swizzled chunk: a warp's 32
+                // channels are four 16-byte pieces of the row
                 const int ch = row - 64;
+                unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
+                                     (tile * n_ct + ct) * (int64_t)G::kChunkBytes + (ch & 7) * 2;
 #pragma unroll
-                for (int n = 0; n < kGN; ++n) {
+                for (int n = 0; n < kN; ++n) {
+                    if (ctl.route[buf][n] < 0) continue;
                     const float p = silu_f32(gbuf[n * 64 + ch]) * v[n];
-                    *reinterpret_cast<__nv_bfloat16 *>(pst + tile_offset(n, ch >> 3) + (ch & 7) * 2) =
-                        __float2bfloat16(p);
+                    *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, ch >> 3)) = __float2bfloat16(p);
                 }
             }
-            named_bar_sync(1, 128);
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(a.p_tiles) +
-                                                   (blk * n_ct + ct) * (int64_t)kGChunkBytes);
-            const uint4 *srcv = reinterpret_cast<const uint4 *>(pst);
-#pragma unroll
-            for (int i = 0; i < kGChunkBytes / 16 / 128; ++i) dst[tid + 128 * i] = srcv[tid + 128 * i];
         }
     }
-    gemm_finish(ctl, warp, a.status);
+    gemm_finish<kN>(ctl, warp, a.status);
 }
 
 // ------------------------------------------------------------------------------- down
+template <int kN>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap tm_down, const GemmArgs a) {
+    using G = GTile<kN>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
-    GCtl &ctl = *reinterpret_cast<GCtl *>(base + kGStages * kGStageBytes);
+    GCtl &ctl = *reinterpret_cast<GCtl *>(base + G::kStages * G::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) prefetch_tensormap(&tm_down);
-    gemm_init(ctl, warp);
+    gemm_init<kN>(ctl, warp);
     pdl_launch_dependents();
 
     const int n_ct = a.H / kGM;
-    const int nks = a.I / kGK;
-    const int64_t T = gemm_blocks(a) * n_ct;
+    const int nks = a.I / G::kK;
+    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
+    const int64_t T = gemm_blocks(a) * a.tpb * n_ct;
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            gemm_producer(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.p_tiles), T,
-                          n_ct, nks, [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
-                const int32_t y = e * a.I + s * kGK;
+            // p tiles come from the gate/up grid: always deferred to this kernel's own wait
+            gemm_producer<kN>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.p_tiles),
+                              T, n_ct, nks, false, e_first,
+                              [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
+                const int32_t y = e * a.I + s * G::kK;
                 tma_load_2d(st, &tm_down, ct * kGM, y, bar, pol);
-                tma_load_2d(st + kGHalfBytes, &tm_down, ct * kGM + 64, y, bar, pol);
+                tma_load_2d(st + G::kHalfBytes, &tm_down, ct * kGM + 64, y, bar, pol);
             });
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) gemm_mma(ctl, stages, T, nks);
+        if (lane == 0) gemm_mma<kN>(ctl, stages, T, nks);
         __syncwarp();
     } else {
         const int quad = warp & 3;
         const int ch = 32 * quad + lane;  // output channel within the 128-channel tile
         int local = 0;
         for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
-            const int64_t blk = u / n_ct;
+            const int64_t tile = u / n_ct;
             const int ct = (int)(u % n_ct);
             const int buf = local & 1;
-            if (ch < kGN) ctl.route[buf][ch] = gemm_route(a, blk * kGN + ch, a.blocks[blk], false);
+            if (ch < kN) ctl.route[buf][ch] = tile_route(a, tile, ch, a.blocks[tile / a.tpb], false);
             const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
             if (named_bar_or(1, 128, !ok)) break;
-            float v[kGN];
-            drain_accumulator(ctl, quad, buf, v);
+            float v[kN];
+            drain_accumulator<kN>(ctl, quad, buf, v);
             float *ybase = a.y + ct * kGM + ch;
 #pragma unroll
-            for (int n = 0; n < kGN; ++n) {
+            for (int n = 0; n < kN; ++n) {
                 const int r = ctl.route[buf][n];
                 if (r >= 0) ybase[(int64_t)r * a.H] = v[n];
             }
         }
     }
-    gemm_finish(ctl, warp, a.status);
+    gemm_finish<kN>(ctl, warp, a.status);
 }
 
 // ------------------------------------------------------------------ bounded-wait self-test
@@ -430,16 +486,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
 __global__ void __launch_bounds__(kGThreads, 1) wait_selftest_kernel(int32_t *status) {
     __shared__ GCtl ctl;
     const int warp = threadIdx.x >> 5;
-    gemm_init(ctl, warp);
+    gemm_init<kGemmBlock>(ctl, warp);
     if ((threadIdx.x & 31) == 0) gwait(&ctl.tfull[0], 0, ctl);
     __syncwarp();
-    gemm_finish(ctl, warp, status);
+    gemm_finish<kGemmBlock>(ctl, warp, status);
 }
 
+template <int kN>
 static size_t gemm_gateup_smem() {
-    return 1024 + kGStages * kGStageBytes + kGN * 64 * 4 + kGChunkBytes + sizeof(GCtl);
+    using G = GTile<kN>;
+    return 1024 + G::kStages * G::kStageBytes + kN * 64 * 4 + sizeof(GCtl);
 }
-static size_t gemm_down_smem() { return 1024 + kGStages * kGStageBytes + sizeof(GCtl); }
+template <int kN>
+static size_t gemm_down_smem() {
+    using G = GTile<kN>;
+    return 1024 + G::kStages * G::kStageBytes + sizeof(GCtl);
+}
 
 cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream) {
     cudaLaunchAttribute attrs[2];
@@ -450,23 +512,39 @@ cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, gather_rows_kernel, a);
 }
 
-cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
-                               const GemmArgs &a, cudaStream_t stream) {
-    const size_t smem = gemm_gateup_smem();
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_gateup_kernel), smem);
+template <int kN>
+static cudaError_t launch_gateup_tiles(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                                       const GemmArgs &a, cudaStream_t stream) {
+    const size_t smem = gemm_gateup_smem<kN>();
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_gateup_kernel<kN>), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, gemm_gateup_kernel, tm_gate, tm_up, a);
+    return cudaLaunchKernelEx(&cfg, gemm_gateup_kernel<kN>, tm_gate, tm_up, a);
+}
+
+template <int kN>
+static cudaError_t launch_down_tiles(const CUtensorMap &tm_down, const GemmArgs &a,
+                                     cudaStream_t stream) {
+    const size_t smem = gemm_down_smem<kN>();
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_down_kernel<kN>), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, gemm_down_kernel<kN>, tm_down, a);
+}
+
+cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                               const GemmArgs &a, cudaStream_t stream) {
+    if (a.kn == 16) return launch_gateup_tiles<16>(tm_gate, tm_up, a, stream);
+    if (a.kn == 64) return launch_gateup_tiles<64>(tm_gate, tm_up, a, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream) {
-    const size_t smem = gemm_down_smem();
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_down_kernel), smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attrs[2];
-    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, gemm_down_kernel, tm_down, a);
+    if (a.kn == 16) return launch_down_tiles<16>(tm_down, a, stream);
+    if (a.kn == 64) return launch_down_tiles<64>(tm_down, a, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_wait_selftest(int32_t *status, cudaStream_t stream) {

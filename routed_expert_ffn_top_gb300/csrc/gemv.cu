@@ -1,4 +1,6 @@
-// gemv.cu -- expert kernels of the small-batch (GEMV) regime.
+// gemv.cu -- expert kernels for blockwise-VQ gate/up weights (GEMV streams on CUDA cores):
+// VQ (and VQ + low-rank) gate/up, the bf16 down projection and the combine that follow it.
+// Dense weights run on the tensor cores instead (gemm_tc05.cu).
 //
 // The expert computation of "A Multi-Engine Dataflow for MoE Decoding on Scratchpad-Based
 // Tensor Accelerators" (MoE block background; stage-3 activation; Section 4.3):
@@ -18,8 +20,8 @@
 //   * a sub-block is `rsub` consecutive aligned rows: at most 8 routes of ONE expert (the
 //     alignment pads every expert to a multiple of b and rsub divides b); its record
 //     (expert, routes, tokens) comes from the sub-block table the alignment step wrote;
-//   * gate/up tile = (sub-block, 64-column I tile): all H rows of W_gate[e] and W_up[e] in
-//     that column range, as H/256 boxes of each projection, alternating gate and up;
+//   * gate/up tile = (sub-block, 64-column I tile): the index boxes of J_gate[e] and
+//     J_up[e] in that column range (each covering 1024 rows of H), alternating gate and up;
 //   * down tile = (sub-block, 64-column H tile): all I rows of W_down[e], I/256 boxes.
 // Persistent CTAs (one per SM) own tiles c, c + G, c + 2G ... (G = grid size); tiles are
 // numbered column tile fastest, so neighbouring SMs stream neighbouring column ranges of
@@ -28,7 +30,7 @@
 // cp.async and hangs them on the same full barrier; warps 2..9 consume.  Consumer warp w
 // owns rows [32w, 32w+32) of every box; lane l the 16 rows [32w + 16(l/16), +16) and the 4
 // columns [4(l%16), +4); fp32 accumulators for up to 8 tokens live in registers across all
-// boxes of the tile (gate/up multiplies bf16 h and weights straight into fp32; down uses
+// boxes of the tile (gate/up dots h with code words decoded from shared memory; down uses
 // packed fp32 FMAs on fp32 p).  At the end of a tile the two lane halves and then the 8
 // warps are summed, and the epilogue writes p (gate/up) or y (down).  A third small kernel
 // forms out = residual + sum_j a_j y_j in slot order j = 0..k-1.
@@ -51,10 +53,8 @@ constexpr int kRowsPerThread = kRowsPerWarp / 2;         // 16
 constexpr int kFirstConsumerWarp = 2;
 
 constexpr int kBoxBytes = kBoxRows * kTI * 2;                 // 32 KB (also kTN == kTI)
-constexpr int kStageBytesGU = kBoxBytes + kNT * kBoxRows * 2;  // + h slices (bf16)
 constexpr int kStageBytesDN = kBoxBytes + kNT * kBoxRows * 4;  // + p slices (fp32)
 constexpr int kRedBytesGU = kConsumerWarps * kNT * kTI * 4;  // g, then u, through one buffer
-constexpr int kXwBytes = kConsumerWarps * kNT * kRowsPerWarp * 4;  // dense: per-warp fp32 h rows
 // VQ gate/up: a box is 256 rows x 64 columns of uint8 code indices (16 KB), i.e. 1024 rows of
 // H; its activation slices are those 1024 h values of each route's token.
 // VQ gate/up with code words of kD elements (d = 4 or 8): a box is 1024/kD index rows x 64
@@ -71,11 +71,10 @@ constexpr int kStageBytesVQ = vq_stage_bytes(4);
 constexpr int kStageBytesLR = kStageBytesDN;
 constexpr int kRedBytesDN = kConsumerWarps * kNT * kTN * 4;
 static_assert(kTI == kTN, "one box shape for both kernels");
-static_assert(kStageBytesGU % 1024 == 0 && kStageBytesDN % 1024 == 0 && kStageBytesVQ % 1024 == 0,
-              "stage alignment");
+static_assert(kStageBytesDN % 1024 == 0 && kStageBytesVQ % 1024 == 0, "stage alignment");
 static_assert(vq_rows(4) == kBoxRows && vq_rows(8) * 2 == kBoxRows, "VQ boxes of 256 or 128 rows");
 
-enum TileKind { kDenseGateUp = 0, kDown = 1, kVQGateUp = 2, kVQLRGateUp = 3 };
+enum TileKind { kDown = 1, kVQGateUp = 2, kVQLRGateUp = 3 };
 
 struct Ctl {
     uint64_t full[kStages];
@@ -224,82 +223,6 @@ struct Lane {
     int rbase;  // first of the 16 rows
 };
 
-// acc[q][c] += sum over this thread's 16 rows of x_q[row] * W[row][c4 + c] for NT tokens
-// (bf16 x bf16 -> fp32, rows ascending).  `st` is the stage: the box, then the h slices.
-template <int NT>
-__device__ __forceinline__ void accumulate_bf16_box(const unsigned char *st, const Lane &ln,
-                                                    float (&acc)[NT][4]) {
-    const unsigned char *xs = st + kBoxBytes + ln.rbase * 2;
-#pragma unroll
-    for (int r8 = 0; r8 < kRowsPerThread; r8 += 8) {
-        uint2 w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = *reinterpret_cast<const uint2 *>(st + (ln.rbase + r8 + i) * (kTI * 2) + ln.c4 * 2);
-#pragma unroll
-        for (int q = 0; q < NT; ++q) {
-            const uint4 xv = *reinterpret_cast<const uint4 *>(xs + q * kBoxRows * 2 + r8 * 2);
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t x2 = xw[i >> 1];
-                if (i & 1) {
-                    acc[q][0] = fma_bf16<1, 0>(x2, w[i].x, acc[q][0]);
-                    acc[q][1] = fma_bf16<1, 1>(x2, w[i].x, acc[q][1]);
-                    acc[q][2] = fma_bf16<1, 0>(x2, w[i].y, acc[q][2]);
-                    acc[q][3] = fma_bf16<1, 1>(x2, w[i].y, acc[q][3]);
-                } else {
-                    acc[q][0] = fma_bf16<0, 0>(x2, w[i].x, acc[q][0]);
-                    acc[q][1] = fma_bf16<0, 1>(x2, w[i].x, acc[q][1]);
-                    acc[q][2] = fma_bf16<0, 0>(x2, w[i].y, acc[q][2]);
-                    acc[q][3] = fma_bf16<0, 1>(x2, w[i].y, acc[q][3]);
-                }
-            }
-        }
-    }
-}
-
-// The same sums for tiles with 3 or more routes, with fewer instructions: the warp first
-// widens its 32 rows of every route's h slice to fp32 in its own scratch xw [NT][32] (a
-// bf16 -> fp32 widening is exact), then each lane multiplies with packed fp32 FMAs.  Every
-// product of two bf16 values is exact in fp32 and each FMA rounds once, as the mixed-
-// precision FMA does, in the same row order: the bits are those of accumulate_bf16_box.
-template <int NT>
-__device__ __forceinline__ void accumulate_bf16_box_x32(const unsigned char *st, const Lane &ln,
-                                                        float *xw, float (&acc)[NT][4]) {
-    const __nv_bfloat16 *xs = reinterpret_cast<const __nv_bfloat16 *>(st + kBoxBytes);
-#pragma unroll
-    for (int i = 0; i < NT; ++i)
-        xw[i * kRowsPerWarp + ln.lane] =
-            __bfloat162float(xs[i * kBoxRows + ln.cw * kRowsPerWarp + ln.lane]);
-    __syncwarp();
-    const float *xr = xw + ln.half * kRowsPerThread;  // this lane's 16 rows of every route
-#pragma unroll
-    for (int r8 = 0; r8 < kRowsPerThread; r8 += 8) {
-        float w[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint2 w2 = *reinterpret_cast<const uint2 *>(st + (ln.rbase + r8 + i) * (kTI * 2) + ln.c4 * 2);
-            w[i][0] = bf16_lo(w2.x);
-            w[i][1] = bf16_hi(w2.x);
-            w[i][2] = bf16_lo(w2.y);
-            w[i][3] = bf16_hi(w2.y);
-        }
-#pragma unroll
-        for (int q = 0; q < NT; ++q) {
-            const float4 x0 = *reinterpret_cast<const float4 *>(xr + q * kRowsPerWarp + r8);
-            const float4 x1 = *reinterpret_cast<const float4 *>(xr + q * kRowsPerWarp + r8 + 4);
-            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                ffma2(acc[q][0], acc[q][1], x[i], w[i][0], w[i][1]);
-                ffma2(acc[q][2], acc[q][3], x[i], w[i][2], w[i][3]);
-            }
-        }
-    }
-    __syncwarp();  // the scratch is refilled for the next box
-}
-
 // acc[q][c] += sum over this thread's 16 rows of p_q[row] * W[row][c4 + c] for NT routes
 // (fp32 p, bf16 weights, packed fp32 FMAs, rows ascending).
 template <int NT>
@@ -388,12 +311,6 @@ __device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const
     }
 }
 
-// The tile bodies take one extra shared-memory pointer: the VQ kernels pass their code
-// books, the dense gate/up kernel its per-warp fp32 scratch (kConsumerWarps x [kNT][32]).
-__device__ __forceinline__ float *cbs_or_xw_as_floats(const uint2 *p) {
-    return const_cast<float *>(reinterpret_cast<const float *>(p));
-}
-
 // Releases the stage to the box producer and the loader once this warp is done with it.
 __device__ __forceinline__ void release_stage(Ctl &ctl, const Lane &ln, int &stage, uint32_t &phase) {
     __syncwarp();
@@ -426,22 +343,21 @@ __device__ __forceinline__ void stage_partials(float *red, const Lane &ln, float
 
 // One gate/up tile with NT routes; its first stage has already been waited for.  Returns
 // false when the CTA must stop (a bounded wait gave up somewhere in the CTA).
-// Stages: dense, a gate box and an up box for every 256 rows of H; VQ, a gate and an up
-// index box for every 1024 rows of H; with kLR, then a C_gate and a C_up box for every 256
-// rows of r, multiplied by z = D^T h into the same accumulators ([MED]'s joint
-// accumulation of the VQ and low-rank terms).
-template <int NT, bool kVQ, bool kLR, int kD>
+// Stages: a gate and an up index box for every 1024 rows of H; with kLR, then a C_gate and
+// a C_up box for every 256 rows of r, multiplied by z = D^T h into the same accumulators
+// ([MED]'s joint accumulation of the VQ and low-rank terms).
+template <int NT, bool kLR, int kD>
 __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                             const uint2 *cbs, const Lane &ln, int it, int r0, int r1, int &stage,
                             uint32_t &phase) {
-    constexpr int kSt = kLR ? kStageBytesLR : (kVQ ? vq_stage_bytes(kD) : kStageBytesGU);
+    constexpr int kSt = kLR ? kStageBytesLR : vq_stage_bytes(kD);
     float ag[NT][4], au[NT][4];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ag[q][c] = au[q][c] = 0.0f;
     bool failed = false;
-    const int nvq = kVQ ? 2 * a.n_qb : 2 * a.n_hb;
+    const int nvq = 2 * a.n_qb;
     const int nst = nvq + (kLR ? 2 * a.n_rb : 0);
     for (int j = 0; j < nst; ++j) {
         if (j > 0 && !wait_or_abort(&ctl.full[stage], phase, ctl)) {
@@ -454,23 +370,12 @@ __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, 
                 accumulate_f32_box<NT>(st, ln, au);
             else
                 accumulate_f32_box<NT>(st, ln, ag);
-        } else if constexpr (kVQ) {
+        } else {
             const unsigned char *cb = reinterpret_cast<const unsigned char *>(cbs);
             if (j & 1)
                 accumulate_vq_box<NT, kD>(st, cb + vq_codebook_bytes(kD), ln, au);
             else
                 accumulate_vq_box<NT, kD>(st, cb, ln, ag);
-        } else if (NT >= 3) {
-            float *xw = cbs_or_xw_as_floats(cbs) + ln.cw * (kNT * kRowsPerWarp);
-            if (j & 1)
-                accumulate_bf16_box_x32<NT>(st, ln, xw, au);
-            else
-                accumulate_bf16_box_x32<NT>(st, ln, xw, ag);
-        } else {
-            if (j & 1)
-                accumulate_bf16_box<NT>(st, ln, au);
-            else
-                accumulate_bf16_box<NT>(st, ln, ag);
         }
         release_stage(ctl, ln, stage, phase);
     }
@@ -576,7 +481,7 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
         if constexpr (kKind == kDown)                                                        \
             go = down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);            \
         else                                                                                 \
-            go = gateup_tile<N, kKind != kDenseGateUp, kKind == kVQLRGateUp, kD>(             \
+            go = gateup_tile<N, kKind == kVQLRGateUp, kD>(                                    \
                 a, ctl, stages, red, cbs, ln, ct, r0, r1, stage, phase);                     \
         break;
         switch (ntok) {
@@ -617,60 +522,6 @@ __device__ void prefetch_down_weights(const GemvArgs &a, int64_t T) {
         for (int64_t l = ((int64_t)blockIdx.x - T) * blockDim.x + threadIdx.x; l < lines; l += stride)
             prefetch_l2_line(base + l * 128);
     }
-}
-
-// ---------------------------------------------------------------------------- gate/up
-__global__ void __launch_bounds__(kGemvThreads, 1)
-    gateup_dense_kernel(const __grid_constant__ CUtensorMap tm_gate,
-                        const __grid_constant__ CUtensorMap tm_up, const GemvArgs a) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *stages = base;
-    float *red = reinterpret_cast<float *>(base + kStages * kStageBytesGU);
-    float *xw = reinterpret_cast<float *>(base + kStages * kStageBytesGU + kRedBytesGU);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kStageBytesGU + kRedBytesGU + kXwBytes);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        init_ring(ctl);
-        prefetch_tensormap(&tm_gate);
-        prefetch_tensormap(&tm_up);
-    }
-    __syncthreads();
-    pdl_wait();
-    pdl_launch_dependents();
-
-    const int64_t T = num_subblocks(a) * a.n_it;
-    const int per_tile = 2 * a.n_hb;  // gate box, up box, for every 256 rows of H
-
-    if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
-            box_producer(a, ctl, T, a.n_it, per_tile, [&](int stage, int64_t t, int j, int e) {
-                const int it = (int)(t % a.n_it);
-                uint64_t *bar = &ctl.full[stage];
-                mbar_arrive_expect_tx(bar, kBoxBytes);
-                tma_load_2d(stages + stage * kStageBytesGU,
-                            (j & 1) ? (const void *)&tm_up : (const void *)&tm_gate, it * kTI,
-                            e * a.H + (j >> 1) * kBoxRows, bar, pol_w);
-            });
-        }
-        return;
-    }
-    if (warp == 1) {
-        // h rows [256 (j/2), +256) of each token: 512 bytes = one 16-byte piece per lane
-        slice_loader(a, ctl, stages, kStageBytesGU, T, a.n_it, per_tile,
-                     [](int) { return SliceLayout{kBoxBytes, kBoxRows * 2, 1}; },
-                     [&](int route, int token, int64_t t, int j, int piece) {
-                         return reinterpret_cast<const unsigned char *>(a.h) +
-                                ((size_t)token * a.H + (size_t)(j >> 1) * kBoxRows) * 2 + piece * 16;
-                     });
-        return;
-    }
-
-    consume_tiles<kDenseGateUp>(a, ctl, stages, red, reinterpret_cast<const uint2 *>(xw), T,
-                                a.n_it);
 }
 
 // ------------------------------------------------------------------------- VQ gate/up
@@ -868,20 +719,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     *reinterpret_cast<uint2 *>(out + o) = ov;
 }
 
-static size_t gateup_smem() {
-    return 1024 + kStages * kStageBytesGU + kRedBytesGU + kXwBytes + sizeof(Ctl);
-}
 static size_t down_smem() { return 1024 + kStages * kStageBytesDN + kRedBytesDN + sizeof(Ctl); }
-
-cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
-                                const GemvArgs &a, cudaStream_t stream) {
-    const size_t smem = gateup_smem();
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gateup_dense_kernel), smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attrs[2];
-    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, gateup_dense_kernel, tm_gate, tm_up, a);
-}
 
 static size_t gateup_vq_smem(bool lr, int d) {
     return 1024 + kStages * (lr ? kStageBytesLR : vq_stage_bytes(d)) + kRedBytesGU +

@@ -23,6 +23,8 @@ constexpr int kRouterThreads = 512;
 
 struct Dims {
     int M, k, E, H, I, b;
+    bool gemm;        // dense weights: every projection runs as tcgen05 tiles of kn rows
+    int kn, tpb;      // tile width (16 or 64 aligned rows) and tiles per aligned block
     int rsub;         // rows per sub-block: b if b <= 8, else 8
     int64_t R;        // routes M*k (also the sentinel value)
     int64_t cap;      // alignment capacity in rows
@@ -51,13 +53,12 @@ struct WsLayout {
     size_t p;        // float[R * I]   SiLU(g) * u per route
     size_t y;        // float[R * H]   down-projection output per route
     size_t z;        // float[M * 2r]  low-rank projections z = D^T h (gate, then up)
-    size_t x_tiles;  // bf16[cap * H]  large-batch regime: token rows per aligned row
-    size_t p_tiles;  // bf16[cap * I]  large-batch regime: p per aligned row
+    size_t x_tiles;  // bf16[tile rows * H]  dense weights: token rows per tile row
+    size_t p_tiles;  // bf16[tile rows * I]  dense weights: p per tile row
     size_t total;
 };
 
-Dims make_dims(int M, int k, int E, int H, int I, int b);
-bool gemm_regime(int kind, int b);
+Dims make_dims(int M, int k, int E, int H, int I, int b, int kind);
 WsLayout ws_layout(const Dims &d);
 
 struct GemvArgs {
@@ -82,20 +83,43 @@ struct GemvArgs {
     int64_t max_sub;       // rows of the sub-block table
 };
 
-// Large-batch regime (aligned blocks of 64 rows, dense weights): grouped GEMMs on tcgen05.
+// Dense weights: grouped GEMMs on tcgen05 over tiles of kn aligned rows of one expert.  An
+// aligned block of b rows is cut into tpb = ceil(b / kn) tiles, kn = 16 for b <= 16, else 64.
+// The library aligns with 64-row blocks from 4 routes per expert on, else with 16-row ones.
 constexpr int kGemmBlock = 64;
+constexpr int kGemmNarrow = 16;
+
+__host__ __device__ constexpr int gemm_tile_width(int b) { return b <= kGemmNarrow ? kGemmNarrow : kGemmBlock; }
+constexpr int kGemmStageK = 256;  // K rows per pipeline stage and per weight box
+__host__ __device__ constexpr int gemm_tiles_per_block(int b) {
+    return (b + gemm_tile_width(b) - 1) / gemm_tile_width(b);
+}
+
+// Row tiles hold, for every 64-wide K chunk, the K-major 128-byte-swizzle image of the
+// tile's kn rows: row n at n * 128 bytes, its 16-byte piece j at (j ^ n % 8) * 16.
+__host__ __device__ constexpr uint32_t tile_offset(int n, int j) {
+    return (uint32_t)(n * 128 + ((j ^ (n & 7)) << 4));
+}
+
+// Where row tiles of h are written by the router when it also aligns (NULL x_tiles: not).
+struct RowTiles {
+    __nv_bfloat16 *x_tiles;
+    int kn, tpb;
+};
 
 struct GemmArgs {
     const __nv_bfloat16 *x;   // h [M,H] (read by the row gather)
     const int32_t *ids;       // topk_ids [M*k]: a row whose route disagrees is skipped
     const int32_t *sorted;    // aligned rows (route ids, sentinel = M*k)
-    const int32_t *blocks;    // expert of each 64-row block
+    const int32_t *blocks;    // expert of each b-row block
     const int32_t *npad;
-    __nv_bfloat16 *x_tiles;   // token rows of h per aligned row, tiled [cap/64][H/64][8 KB]
-    __nv_bfloat16 *p_tiles;   // SiLU(g) * u per aligned row, bf16, tiled [cap/64][I/64][8 KB]
+    __nv_bfloat16 *x_tiles;   // token rows of h per tile row, [tiles][H/64][kn * 128 B]
+    __nv_bfloat16 *p_tiles;   // SiLU(g) * u per tile row, bf16, [tiles][I/64][kn * 128 B]
     float *y;                 // down output per route [M*k, H]
     int32_t *status;
     int M, k, E, H, I;
+    int b, kn, tpb;           // aligned block rows, tile width, tiles per block
+    int wait_first;           // the previous kernel wrote the x tiles (and the alignment)
     int64_t R, cap;
 };
 
@@ -173,7 +197,7 @@ cudaError_t launch_router_align(const __nv_bfloat16 *h, const __nv_bfloat16 *w_r
                                 int32_t *topk_ids, float *topk_weights, int b, int rsub,
                                 int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
                                 SubBlock *sbt, int32_t *status, const LowRankProj *lr,
-                                cudaStream_t stream);
+                                const RowTiles &rows, cudaStream_t stream);
 
 // Alignment; when `sbt` is not NULL it also writes the sub-block table of rsub-row blocks.
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b,
@@ -185,8 +209,6 @@ cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const in
                         const int32_t *npad, int M, int k, int E, int b, int rsub,
                         int64_t max_sub, SubBlock *sbt, int32_t *status, cudaStream_t stream);
 
-cudaError_t launch_gateup_dense(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
-                                const GemvArgs &a, cudaStream_t stream);
 
 // Blockwise-VQ gate/up (d = 4 or 8, K = 256): index maps through TMA (boxes of 1024/d index
 // rows x 64 columns), code books in shared memory; with a.r > 0 also the low-rank term (C

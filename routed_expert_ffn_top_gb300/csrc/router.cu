@@ -33,6 +33,7 @@ struct FusedAlign {
     int64_t cap;
     SubBlock *sbt;
     int32_t *status;
+    RowTiles rows;  // rows.x_tiles != NULL: every CTA also writes its H slice of the row tiles
 };
 
 // Low-rank projections computed in the router's launch (VQ + low-rank gate/up weights):
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(kRouterThreads)
 
     // shared layout: w_s [HP][E] bf16 | x_s [TM][HS] bf16 | red [RG][TM][E] f32 |
     //                gath [8][E] f32 (this CTA's token: the partial logits of every rank) |
-    //                ids_s [8 * 32] | bar | align scratch
+    //                ids_s [8 * 32] | bar | align scratch | aligned row of every route
     unsigned char *ptr = smem_raw;
     __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(ptr);
     ptr += (size_t)HP * E * 2;
@@ -289,14 +290,48 @@ __global__ void __launch_bounds__(kRouterThreads)
             topk_ids[(size_t)m * k + lane] = id;
             topk_wts[(size_t)m * k + lane] = ok ? ex / denom : 0.0f;
             // every token's ids go to rank 0, which aligns them when one cluster holds all
-            if (fa.enabled) cluster_peer_mut(ids_s, 0u)[t * k + lane] = id;
+            // (to every rank when the ranks also write the row tiles)
+            if (fa.enabled) {
+                if (fa.rows.x_tiles)
+                    for (uint32_t q = 0; q < (uint32_t)kRouterCluster; ++q)
+                        cluster_peer_mut(ids_s, q)[t * k + lane] = id;
+                else
+                    cluster_peer_mut(ids_s, 0u)[t * k + lane] = id;
+            }
         }
     }
     if (fa.enabled) {
         cluster_sync();
+        int32_t *pos_s = align_sm + align_small_smem_ints(kRouterThreads);  // [M * k]
+        const int R = M * k;
         if (rank == 0)
-            align_small(ids_s, M * k, k, E, fa.b, fa.rsub, fa.sorted, fa.blocks, fa.npad, fa.cap,
-                        fa.sbt, fa.status, align_sm);
+            align_small(ids_s, R, k, E, fa.b, fa.rsub, fa.sorted, fa.blocks, fa.npad, fa.cap,
+                        fa.sbt, fa.status, align_sm, fa.rows.x_tiles ? pos_s : nullptr);
+        else if (fa.rows.x_tiles)  // the same positions, nothing else written
+            align_small(ids_s, R, k, E, fa.b, fa.rsub, nullptr, nullptr, nullptr, fa.cap, nullptr,
+                        nullptr, align_sm, pos_s);
+        if (fa.rows.x_tiles) {
+            // The x tile rows of the grouped GEMMs: this CTA's H slice of every valid route's
+            // token row (already in x_s, the cluster holds every token) goes to row n of
+            // tile t, 16-byte piece by piece in the swizzled image.
+            __syncthreads();
+            const int kn = fa.rows.kn, tpb = fa.rows.tpb, b = fa.b;
+            const int64_t chunk_bytes = (int64_t)kn * 128;
+            const int64_t tile_bytes = (int64_t)(H / 64) * chunk_bytes;
+            unsigned char *xt = reinterpret_cast<unsigned char *>(fa.rows.x_tiles);
+            for (int idx = tid; idx < R * pieces; idx += kRouterThreads) {
+                const int r = idx / pieces, q = idx - r * pieces;
+                const int pos = pos_s[r];
+                if (pos < 0) continue;
+                const int p = (int)rank * pieces + q;  // piece of the whole row (8 columns)
+                const int local = pos % b;
+                const int64_t t = (int64_t)(pos / b) * tpb + local / kn;
+                const int n = local % kn;
+                *reinterpret_cast<uint4 *>(xt + t * tile_bytes + (p >> 3) * chunk_bytes +
+                                           tile_offset(n, p & 7)) =
+                    *reinterpret_cast<const uint4 *>(x_s + (size_t)(r / k) * HS + q * 8);
+            }
+        }
     }
     // No CTA touches another's shared memory after the last cluster barrier.
 }
@@ -306,7 +341,7 @@ static size_t router_smem(int TM, int H, int E, bool fuse) {
     const int RG = kRouterThreads / (E / 2);
     return (size_t)(HS / router_passes(HS, E)) * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
            (size_t)kRouterCluster * E * 4 + 8 * 32 * 4 + 16 +
-           (fuse ? (size_t)align_small_smem_ints(kRouterThreads) * 4 : 0);
+           (fuse ? (size_t)(align_small_smem_ints(kRouterThreads) + 8 * 32) * 4 : 0);
 }
 
 template <int TM, int kPerLane>
@@ -397,8 +432,9 @@ cudaError_t launch_router_align(const __nv_bfloat16 *h, const __nv_bfloat16 *w_r
                                 int32_t *topk_ids, float *topk_weights, int b, int rsub,
                                 int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
                                 SubBlock *sbt, int32_t *status, const LowRankProj *lr,
-                                cudaStream_t stream) {
+                                const RowTiles &rows, cudaStream_t stream) {
     FusedAlign fa;
+    fa.rows = rows;
     fa.enabled = 1;
     fa.b = b;
     fa.rsub = rsub;

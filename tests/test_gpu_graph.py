@@ -21,9 +21,9 @@ def _built():
 
 
 @pytest.mark.parametrize("M,k,E,H,I,b", [
-    (1, 8, 128, 2048, 768, 8),     # router with fused alignment, GEMV expert kernels
-    (21, 8, 128, 2048, 768, 8),    # separate alignment launch
-    (96, 4, 16, 512, 512, 64),     # grouped-GEMM regime (row gather + tcgen05 kernels)
+    (1, 8, 128, 2048, 768, 8),     # router with fused alignment and row tiles, 16-row tiles
+    (21, 8, 128, 2048, 768, 8),    # separate alignment and row gather launches
+    (96, 4, 16, 512, 512, 64),     # 64-row tiles
 ])
 def test_graph_replay_bitwise(M, k, E, H, I, b):
     wl = syn.Workload("graph_%d_%d" % (M, b), H=H, I=I, E=E, k=k, b=b, M=M)

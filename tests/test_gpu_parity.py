@@ -107,10 +107,12 @@ SMALL = [
     (1, 1, 8, 256, 256, 1), (5, 2, 8, 512, 256, 3), (13, 8, 16, 768, 512, 8),
     (3, 4, 32, 256, 768, 16), (37, 6, 64, 256, 256, 64), (64, 8, 128, 512, 256, 8),
     (2, 8, 8, 1024, 1280, 2), (9, 3, 40, 1280, 256, 5),
-    # b = 64 with dense weights: the tcgen05 grouped-GEMM regime (several blocks per expert,
-    # ragged last blocks, single-route blocks, K and channel counts over several tiles)
+    # b = 64: 64-row tiles (several blocks per expert, ragged last blocks, single-route
+    # blocks, K and channel counts over several tiles); b = 24, 128: blocks that fill part
+    # of a 64-row tile, or two tiles
     (1, 1, 8, 256, 256, 64), (300, 2, 8, 512, 768, 64), (64, 8, 16, 1024, 512, 64),
     (129, 4, 8, 256, 1536, 64), (300, 8, 128, 768, 256, 64),
+    (40, 4, 16, 512, 256, 24), (90, 8, 8, 256, 512, 128),
 ]
 
 
@@ -134,15 +136,12 @@ def test_expert_ffn_small(M, k, E, H, I, b):
     assert moe.moe_read_device_status(ws) == 0
     ref = G.oracle_ffn(layer, h, ids, a, residual=res)
     G.assert_close_block(G.to_f64(out), ref, "expert_ffn %s" % (SMALL,))
-    # the same call with the caller's own alignment buffers: the same bits when both run the
-    # same regime (the library's own alignment takes 64-row blocks at 4+ routes per expert)
+    # the same call with the caller's own b-row alignment (the library aligned in 16- or
+    # 64-row blocks of its own): a route's bits do not depend on its block
     srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
     out2 = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad), residual=res,
                               workspace=ws)
-    if b == 64 or M * k < 4 * E:
-        assert torch.equal(out, out2)
-    else:
-        G.assert_close_block(G.to_f64(out2), ref, "expert_ffn, caller alignment")
+    assert torch.equal(out, out2)
 
 
 def test_expert_ffn_invalid_ids_and_status():
@@ -410,8 +409,8 @@ def test_large_m256_sampled_tokens():
 
 
 def test_decode_block_picks_the_gemm_regime_for_large_batches():
-    """At 4+ routes per expert the library aligns in 64-row blocks and runs the tcgen05
-    kernels whatever b is; below that, b's GEMV streams run."""
+    """At 4+ routes per expert the library aligns in 64-row blocks (64-row tiles) whatever b
+    is, below that in 16-row blocks; the bits are the same either way."""
     wl = syn.workload("layer_m21", M=64)
     layer = _workload_layer("layer_m21")
     h = syn.make_hidden(wl, M=64, seed=64, device=DEV)
@@ -424,17 +423,19 @@ def test_decode_block_picks_the_gemm_regime_for_large_batches():
     use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
                                           logits, wl.k)
     ref = G.oracle_ffn(layer, h, use_ids, use_wts, tokens=tokens)
-    G.assert_close_block(G.to_f64(out8)[tokens], ref, "M=64 grouped-GEMM regime")
-    # below the threshold (M=32: 2 routes per expert) the GEMV regime keeps b = 8
+    G.assert_close_block(G.to_f64(out8)[tokens], ref, "M=64, 64-row tiles")
+    # below the threshold (M=32: 2 routes per expert) 16-row tiles run: the same tokens keep
+    # their bits, and so does a caller's own 8-row alignment
     h32 = h[:32].contiguous()
     o32, ids32, wts32 = moe.moe_decode_block(h32, layer, wl.k, 8)
+    assert torch.equal(ids32, ids[:32]) and torch.equal(o32, out8[:32])
     srt, blk, npad = moe.moe_align_block_size(ids32, wl.E, 8)
     assert torch.equal(moe.moe_expert_ffn(h32, layer, ids32, wts32, 8, alignment=(srt, blk, npad)),
                        o32)
 
 
 def test_gemm_regime_batch_and_membership_invariance():
-    """In the grouped-GEMM regime a route is one column of its block's MMA: its bits do not
+    """With 64-row tiles a route is one column of its tile's MMA: its bits do not
     depend on the other routes of the block, on the block's position or on M."""
     M, k, E, H, I, b = 96, 4, 8, 512, 512, 64
     wl, layer, h = _small_layer(M, k, E, H, I, b, seed=3)
@@ -451,6 +452,69 @@ def test_gemm_regime_batch_and_membership_invariance():
         assert torch.equal(o, out[sel]), sub
     ref = G.oracle_ffn(layer, h, ids, a)
     G.assert_close_block(G.to_f64(out), ref, "gemm regime")
+
+
+def test_route_bits_independent_of_batch_block_and_tile_width():
+    """Every route of dense weights is one K-ordered chain of tcgen05 MMAs per projection
+    (the route-block page's batch- and membership-invariance as a guarantee): a token's
+    output bits are the same alone or in any batch, in blocks of 1, 8, 16, 24, 64 or 128
+    rows, in 16- or 64-row tiles, through the library's own alignment or the caller's."""
+    M, k, E, H, I = 72, 8, 16, 512, 768
+    wl, layer, h = _small_layer(M, k, E, H, I, 8, seed=21)
+    rng = np.random.default_rng(21)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
+    base = moe.moe_expert_ffn(h, layer, t_ids, t_a, 8)  # library: 64-row blocks (M*k >= 4E)
+    ref = G.oracle_ffn(layer, h, ids, a)
+    G.assert_close_block(G.to_f64(base), ref, "cross-regime base")
+    for b in (1, 8, 16, 24, 64, 128):
+        srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
+        o = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad))
+        assert torch.equal(o, base), b
+    for sub in ([3], [0, 71], list(range(10, 17)), list(range(71, -1, -5))):
+        sel = torch.as_tensor(sub, device=DEV)
+        o = moe.moe_expert_ffn(h[sel].contiguous(), layer, t_ids[sel].contiguous(),
+                               t_a[sel].contiguous(), 8)  # library: 16-row blocks
+        assert torch.equal(o, base[sel]), sub
+
+
+@pytest.mark.parametrize("M,b", [(1, 8), (2, 8), (8, 8), (21, 8), (64, 8), (3, 64)])
+def test_decode_block_on_a_dirty_workspace(M, b):
+    """Every buffer of the workspace is written before it is read: a workspace whose bytes
+    are all 0xFF (NaN in every float view) gives the same bits as a zeroed one, from the
+    first call on.  A kernel that read a buffer before its producer finished would see NaN."""
+    wl = syn.workload("layer_m21", M=M)
+    layer = _workload_layer("layer_m21")
+    h = syn.make_hidden(wl, M=M, seed=31, device=DEV)
+    res = syn.make_hidden(wl, M=M, seed=32, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, wl.k, b)
+    dirty = torch.full_like(ws, 0xFF)
+    dirty[:64] = 0  # the status word starts clear, as the entry points require
+    out_d, ids_d, _ = moe.moe_decode_block(h, layer, wl.k, b, residual=res, workspace=dirty)
+    out_z, ids_z, wts_z = moe.moe_decode_block(h, layer, wl.k, b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(dirty) == 0
+    assert torch.equal(ids_d, ids_z) and torch.equal(out_d, out_z)
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+    use_ids, use_wts, _ = G.check_routing(ids_z.cpu().numpy(), wts_z.cpu().numpy(), o_ids, o_wts,
+                                          logits, wl.k)
+    tokens = None if M <= 21 else np.array([0, M // 2, M - 1])
+    ref = G.oracle_ffn(layer, h, use_ids, use_wts, residual=res, tokens=tokens)
+    got = G.to_f64(out_z) if tokens is None else G.to_f64(out_z)[tokens]
+    G.assert_close_block(got, ref, "dirty workspace M=%d" % M)
+
+
+def test_decode_block_bits_same_in_both_tile_widths():
+    """The default layer: M=21 runs 16-row tiles, M=64 64-row tiles; the 21 shared tokens
+    keep their routing and their output bits."""
+    wl = syn.WORKLOADS["layer_m21"]
+    layer = _workload_layer("layer_m21")
+    h64 = syn.make_hidden(wl, M=64, seed=5, device=DEV)
+    o64, i64, _ = moe.moe_decode_block(h64, layer, wl.k, wl.b)
+    o21, i21, _ = moe.moe_decode_block(h64[:21].contiguous(), layer, wl.k, wl.b)
+    o1, i1, _ = moe.moe_decode_block(h64[40:41].contiguous(), layer, wl.k, wl.b)
+    assert torch.equal(i21, i64[:21]) and torch.equal(o21, o64[:21])
+    assert torch.equal(i1[0], i64[40]) and torch.equal(o1[0], o64[40])
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])

@@ -33,7 +33,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         torch.cuda.synchronize()
         assert torch.equal(ids, ref_ids), call
         assert torch.allclose(wts, ref_wts, rtol=1e-6, atol=0), call
-        G.assert_close_block(G.to_f64(out), G.to_f64(ref), "noalloc call %d" % call)
+        # the caller's 8-row blocks here, the library's 16-row blocks there: dense weights
+        # give every route the same bits whatever its block
+        assert torch.equal(out, ref), call
 
 
 def test_noalloc_refuses_sizes_beyond_its_array():
