@@ -130,6 +130,13 @@ def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu") -> dic
     return p
 
 
+def make_rotation_signs(H: int, seed: int = 0, device="cpu", tag: str = "reader/signs") -> torch.Tensor:
+    """The random signs of a block-Hadamard rotation (one +1/-1 per coordinate of H) as int8:
+    the random numbers the channel reader draws once, passed to both of its implementations."""
+    g = _gen(device, sub_seed(seed, tag, 0, "signs"))
+    return (torch.randint(0, 2, (H,), generator=g, device=device, dtype=torch.int32) * 2 - 1).to(torch.int8)
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> C-contiguous numpy uint16 bit patterns (on the host)."""
     if t.dtype != torch.bfloat16:
