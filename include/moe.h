@@ -256,6 +256,67 @@ int moe_read_device_status(void *workspace, void *stream, int32_t *status_out);
  */
 int moe_selftest_wait_timeout(void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * Channel-sparse reader ("Channel Selection for Mixture-of-Experts Decoding Needs No
+ * Calibration Data", the reader's Stages 1-3), for dense weights.  Per token, over the
+ * k * I channels of its routed experts (channel = one row of gate/up, one row of W_down):
+ *   1. x is rotated in 128-coordinate blocks by a random Hadamard transform R (signs given);
+ *      every channel's rotated gate and up rows are held as ternary sketches (two-bit codes
+ *      and one fp32 scale per block: the Ternary Weight Networks threshold 0.7 mean|r|, the
+ *      scale the mean |r| of the nonzero codes); per block only the nscan coordinates of
+ *      largest |Rx| are scanned; ahat = SiLU(ghat) * vhat;
+ *   2. score = w * ||d|| * |ahat| (w the router weight of the channel's expert); the K best
+ *      channels across all the token's experts (ties: lower slot * I + channel index) are
+ *      read exactly: a = SiLU(g . x) * (v . x);
+ *   3. out = residual + sum_{kept} w a d + U sum_{discarded} w ahat b,  b = U^T d.
+ * All sums run in fixed orders: outputs are bitwise reproducible and a token's output does
+ * not depend on the other tokens.
+ *
+ * Data (caller-allocated device buffers, 16-byte aligned):
+ *   signs   [H] int8 +1/-1;               U [H][rank] fp32 (rank <= 32), orthonormal columns
+ *   w_down  [E][I][H] bf16 (the layer's W_down, read in place)
+ *   g_rows, v_rows [E][I][H] bf16;  g_codes, v_codes [E][I][H/128][8] uint32 (code c of a
+ *   block at bits 2(c%16) of word c/16: 00 zero, 01 +1, 11 -1);  g_scales, v_scales
+ *   [E][I][H/128] fp32;  dnorm [E][I] fp32;  coef [E][I][rank] bf16 -- written by
+ *   moe_reader_build.
+ * Shapes: H a multiple of 128 up to 8192, 1 <= rank <= 32.
+ */
+typedef struct moe_reader {
+    int H, I, E, rank;
+    const int8_t *signs;
+    void *g_rows, *v_rows;
+    const void *w_down;
+    void *g_codes, *v_codes;
+    float *g_scales, *v_scales;
+    float *dnorm;
+    const float *U;
+    void *coef;
+} moe_reader_t;
+
+/*
+ * Builds the reader's data from dense weights w (kind MOE_W_DENSE_BF16, same H, I, E) and
+ * rd->signs, rd->U: channel-major gate/up rows, their sketches, the down-row norms and
+ * coef = U^T d.  Stream-ordered; MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before launching.
+ */
+int moe_reader_build(const moe_expert_weights_t *w, const moe_reader_t *rd, void *stream);
+
+/* Workspace bytes of moe_reader_ffn for (rd, M, k, K); 0 on unsupported arguments. */
+size_t moe_reader_workspace_bytes(const moe_reader_t *rd, int M, int k, int K);
+
+/*
+ * The reader's decode for M tokens with their routes: topk_ids [M,k] int32 (ids outside
+ * [0,E) are skipped), topk_weights [M,k] fp32.  K = channels read exactly per token
+ * (0 <= K <= k*I; a token with fewer valid channels reads them all), nscan = coordinates
+ * scanned per 128-block (0..128), k*I <= 16384.  residual [M,H] bf16 or NULL; out [M,H]
+ * bf16.  Optional outputs for inspection: selected [M,K] int32, the kept channels of each
+ * token (slot * I + channel, ascending, -1 past the token's count), and xr [M,H] fp32, Rx
+ * with the unscanned coordinates set to zero.  workspace: ws_bytes >=
+ * moe_reader_workspace_bytes(rd, M, k, K), 256-byte aligned.
+ */
+int moe_reader_ffn(const void *h, const moe_reader_t *rd, int M, int k, const int32_t *topk_ids,
+                   const float *topk_weights, int K, int nscan, const void *residual, void *out,
+                   int32_t *selected, float *xr, void *workspace, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -642,3 +642,92 @@ extern "C" int moe_selftest_wait_timeout(void *workspace, size_t ws_bytes, void 
     return cuda_status(moe::launch_wait_selftest(static_cast<int32_t *>(workspace),
                                                  static_cast<cudaStream_t>(stream)));
 }
+
+// ------------------------------------------------------------------------ channel reader
+static int reader_args(const moe_reader_t *rd, ReaderArgs *r) {
+    if (!rd) return MOE_ERR_INVALID_ARG;
+    if (rd->H <= 0 || rd->I <= 0 || rd->E <= 0 || rd->rank <= 0) return MOE_ERR_INVALID_ARG;
+    if (rd->H % 128 != 0 || rd->H > 8192 || rd->rank > kReaderMaxRank) return MOE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {rd->signs, rd->g_rows, rd->v_rows, rd->w_down, rd->g_codes, rd->v_codes,
+                          rd->g_scales, rd->v_scales, rd->dnorm, rd->U, rd->coef};
+    for (const void *p : ptrs)
+        if (!p || !aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+    r->H = rd->H;
+    r->I = rd->I;
+    r->E = rd->E;
+    r->rank = rd->rank;
+    r->signs = rd->signs;
+    r->g_rows = static_cast<const __nv_bfloat16 *>(rd->g_rows);
+    r->v_rows = static_cast<const __nv_bfloat16 *>(rd->v_rows);
+    r->w_down = static_cast<const __nv_bfloat16 *>(rd->w_down);
+    r->g_codes = static_cast<const uint32_t *>(rd->g_codes);
+    r->v_codes = static_cast<const uint32_t *>(rd->v_codes);
+    r->g_scales = rd->g_scales;
+    r->v_scales = rd->v_scales;
+    r->dnorm = rd->dnorm;
+    r->U = rd->U;
+    r->coef = static_cast<const __nv_bfloat16 *>(rd->coef);
+    return MOE_OK;
+}
+
+extern "C" int moe_reader_build(const moe_expert_weights_t *w, const moe_reader_t *rd, void *stream) {
+    ReaderArgs r;
+    int rc = reader_args(rd, &r);
+    if (rc != MOE_OK) return rc;
+    rc = check_weights(w);
+    if (rc != MOE_OK) return rc;
+    if (w->kind != MOE_W_DENSE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (w->H != rd->H || w->I != rd->I || w->E != rd->E || w->w_down != rd->w_down)
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_reader_build(r, static_cast<const __nv_bfloat16 *>(w->w_gate),
+                                           static_cast<const __nv_bfloat16 *>(w->w_up),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+static int check_reader_call(const ReaderArgs &r, int M, int k, int K) {
+    if (M < 0 || k <= 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || (int64_t)k * r.I > kReaderMaxCand || K > k * r.I || M > 65535)
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+extern "C" size_t moe_reader_workspace_bytes(const moe_reader_t *rd, int M, int k, int K) {
+    ReaderArgs r;
+    if (reader_args(rd, &r) != MOE_OK || check_reader_call(r, M, k, K) != MOE_OK) return 0;
+    return reader_ws_layout(r, M, k, K).total;
+}
+
+extern "C" int moe_reader_ffn(const void *h, const moe_reader_t *rd, int M, int k,
+                              const int32_t *topk_ids, const float *topk_weights, int K,
+                              int nscan, const void *residual, void *out, int32_t *selected,
+                              float *xr, void *workspace, size_t ws_bytes, void *stream) {
+    ReaderArgs r;
+    int rc = reader_args(rd, &r);
+    if (rc != MOE_OK) return rc;
+    rc = check_reader_call(r, M, k, K);
+    if (rc != MOE_OK) return rc;
+    if (nscan < 0 || nscan > 128) return MOE_ERR_UNSUPPORTED;
+    if (!h || !out || !topk_ids || !topk_weights || !workspace || !aligned(h, 16) ||
+        !aligned(out, 16) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+        !aligned(workspace, 256) || (residual && !aligned(residual, 16)) ||
+        (selected && !aligned(selected, 4)) || (xr && !aligned(xr, 4)))
+        return MOE_ERR_INVALID_ARG;
+    const ReaderWs L = reader_ws_layout(r, M, k, K);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (M == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaError_t err = launch_reader_decode(r, static_cast<const __nv_bfloat16 *>(h), M, k, topk_ids,
+                                           topk_weights, K, nscan,
+                                           static_cast<const __nv_bfloat16 *>(residual),
+                                           static_cast<__nv_bfloat16 *>(out), ws, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (selected && K > 0 &&
+        cudaMemcpyAsync(selected, ws + L.sel, (size_t)M * K * 4, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (xr && cudaMemcpyAsync(xr, ws + L.xr, (size_t)M * r.H * 4, cudaMemcpyDeviceToDevice, s) !=
+                  cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}

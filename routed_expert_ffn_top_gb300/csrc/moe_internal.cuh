@@ -127,6 +127,31 @@ cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
+constexpr int kReaderMaxCand = 16384;  // k * I candidate channels per token the selection holds
+constexpr int kReaderMaxRank = 32;
+// The channel reader's data (see reader.cu for the layout) and one call's workspace.
+struct ReaderArgs {
+    int H, I, E, rank;
+    const int8_t *signs;                    // [H] +1 / -1
+    const __nv_bfloat16 *g_rows, *v_rows;   // [E][I][H] channel-major gate / up rows
+    const __nv_bfloat16 *w_down;            // [E][I][H]
+    const uint32_t *g_codes, *v_codes;      // [E][I][H/128][8] two-bit ternary codes
+    const float *g_scales, *v_scales;       // [E][I][H/128]
+    const float *dnorm;                     // [E][I]
+    const float *U;                         // [H][rank]
+    const __nv_bfloat16 *coef;              // [E][I][rank]
+};
+struct ReaderWs {
+    size_t status, xr, ahat, score, keep, sel, nsel, partial, zpart, total;
+    int nchunk;
+};
+ReaderWs reader_ws_layout(const ReaderArgs &r, int M, int k, int K);
+cudaError_t launch_reader_build(const ReaderArgs &r, const __nv_bfloat16 *w_gate,
+                                const __nv_bfloat16 *w_up, cudaStream_t stream);
+cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, int M, int k,
+                                 const int32_t *ids, const float *wts, int K, int nscan,
+                                 const __nv_bfloat16 *residual, __nv_bfloat16 *out,
+                                 unsigned char *ws, cudaStream_t stream);
 // One CTA whose bounded wait runs out on purpose (sets MOE_DEV_WAIT_TIMEOUT in *status).
 cudaError_t launch_wait_selftest(int32_t *status, cudaStream_t stream);
 

@@ -38,7 +38,8 @@ EXPORTS = (
     "moe_status_string", "moe_route_topk", "moe_align_capacity", "moe_align_block_size",
     "moe_workspace_bytes", "moe_expert_ffn", "moe_decode_block", "moe_decode_block_host",
     "moe_read_device_status", "moe_set_trace_events", "moe_decode_block_noalloc",
-    "moe_selftest_wait_timeout",
+    "moe_selftest_wait_timeout", "moe_reader_build", "moe_reader_workspace_bytes",
+    "moe_reader_ffn",
 )
 
 
@@ -60,6 +61,17 @@ class ExpertWeights(ctypes.Structure):
         ("d_gate", ctypes.c_void_p), ("d_up", ctypes.c_void_p),
         ("c_gate", ctypes.c_void_p), ("c_up", ctypes.c_void_p),
         ("r", ctypes.c_int32),
+    ]
+
+
+class ReaderStruct(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("rank", ctypes.c_int32),
+        ("signs", ctypes.c_void_p), ("g_rows", ctypes.c_void_p), ("v_rows", ctypes.c_void_p),
+        ("w_down", ctypes.c_void_p), ("g_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+        ("g_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p), ("dnorm", ctypes.c_void_p),
+        ("U", ctypes.c_void_p), ("coef", ctypes.c_void_p),
     ]
 
 
@@ -102,10 +114,15 @@ def lib():
             L.moe_set_trace_events.argtypes = [vp, ci]
             L.moe_decode_block_noalloc.argtypes = [vp, vp, vp, wp, ci, ci, ci, vp, vp, vp, vp, vp]
             L.moe_selftest_wait_timeout.argtypes = [vp, sz, vp]
+            rp = ctypes.POINTER(ReaderStruct)
+            L.moe_reader_build.argtypes = [wp, rp, vp]
+            L.moe_reader_workspace_bytes.argtypes = [rp, ci, ci, ci]
+            L.moe_reader_workspace_bytes.restype = sz
+            L.moe_reader_ffn.argtypes = [vp, rp, ci, ci, vp, vp, ci, ci, vp, vp, vp, vp, vp, sz, vp]
             for f in ("moe_route_topk", "moe_align_block_size", "moe_expert_ffn",
                       "moe_decode_block", "moe_decode_block_host", "moe_read_device_status",
                       "moe_set_trace_events", "moe_decode_block_noalloc",
-                      "moe_selftest_wait_timeout"):
+                      "moe_selftest_wait_timeout", "moe_reader_build", "moe_reader_ffn"):
                 getattr(L, f).restype = ci
             _lib = L
     return _lib
@@ -393,3 +410,77 @@ def capture_graph(fn, stream: Optional[torch.cuda.Stream] = None) -> torch.cuda.
         fn(stream)
     torch.cuda.current_stream().wait_stream(stream)
     return graph
+
+
+# ------------------------------------------------------------------------ channel reader
+def reader_basis(w_down: torch.Tensor, rank: int = 32) -> torch.Tensor:
+    """U [H, rank] fp32 for the reader's recovery map: the top left singular vectors of the
+    H x (E I) matrix of down columns, from the eigenvectors of D^T D (an offline build step
+    done once per layer with torch's symmetric eigensolver, not part of the decode path)."""
+    D = w_down.reshape(-1, w_down.shape[-1]).to(torch.float64)
+    evals, evecs = torch.linalg.eigh(D.T @ D)
+    order = torch.argsort(evals, descending=True, stable=True)[:rank]
+    return evecs[:, order].to(torch.float32).contiguous()
+
+
+def _reader_struct(rd: dict) -> ReaderStruct:
+    s = ReaderStruct()
+    s.H, s.I, s.E, s.rank = rd["H"], rd["I"], rd["E"], rd["rank"]
+    for name in ("signs", "g_rows", "v_rows", "w_down", "g_codes", "v_codes", "g_scales",
+                 "v_scales", "dnorm", "U", "coef"):
+        setattr(s, name, rd[name].data_ptr())
+    return s
+
+
+def reader_build(layer: dict, signs: torch.Tensor, U: torch.Tensor, stream=None) -> dict:
+    """Allocate and build the reader's data for a dense layer (see include/moe.h)."""
+    E, H, I = layer["E"], layer["H"], layer["I"]
+    rank = U.shape[1]
+    dev = layer["w_down"].device
+    nb = H // 128
+    rd = {"H": H, "I": I, "E": E, "rank": rank, "signs": signs.contiguous(),
+          "U": U.to(torch.float32).contiguous(), "w_down": layer["w_down"],
+          "g_rows": torch.empty((E, I, H), dtype=torch.bfloat16, device=dev),
+          "v_rows": torch.empty((E, I, H), dtype=torch.bfloat16, device=dev),
+          "g_codes": torch.empty((E, I, nb, 8), dtype=torch.int32, device=dev),
+          "v_codes": torch.empty((E, I, nb, 8), dtype=torch.int32, device=dev),
+          "g_scales": torch.empty((E, I, nb), dtype=torch.float32, device=dev),
+          "v_scales": torch.empty((E, I, nb), dtype=torch.float32, device=dev),
+          "dnorm": torch.empty((E, I), dtype=torch.float32, device=dev),
+          "coef": torch.empty((E, I, rank), dtype=torch.bfloat16, device=dev)}
+    w = expert_weights(layer)
+    s = _reader_struct(rd)
+    _check(lib().moe_reader_build(ctypes.byref(w), ctypes.byref(s), _stream(stream)),
+           "moe_reader_build")
+    return rd
+
+
+def reader_workspace(rd: dict, M: int, k: int, K: int, device=None) -> torch.Tensor:
+    s = _reader_struct(rd)
+    n = lib().moe_reader_workspace_bytes(ctypes.byref(s), M, k, K)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED, "moe_reader_workspace_bytes")
+    return torch.zeros((n,), dtype=torch.uint8, device=rd["w_down"].device if device is None else device)
+
+
+def moe_reader_ffn(h, rd: dict, topk_ids, topk_weights, K: int, nscan: int = 80, residual=None,
+                   out=None, workspace=None, want_decisions=False, stream=None):
+    """The reader's decode (include/moe.h).  Returns out, or (out, selected [M,K] int32,
+    xr [M,H] fp32) with ``want_decisions``."""
+    M, k = topk_ids.shape
+    if out is None:
+        out = torch.empty_like(h)
+    if workspace is None:
+        workspace = reader_workspace(rd, M, k, K)
+    sel = xr = None
+    if want_decisions:
+        sel = torch.empty((M, max(K, 1)), dtype=torch.int32, device=h.device)
+        xr = torch.empty((M, rd["H"]), dtype=torch.float32, device=h.device)
+    s = _reader_struct(rd)
+    _check(lib().moe_reader_ffn(_ptr(h), ctypes.byref(s), M, k, _ptr(topk_ids), _ptr(topk_weights),
+                                K, nscan, _ptr(residual), _ptr(out), _ptr(sel), _ptr(xr),
+                                _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_reader_ffn")
+    if want_decisions:
+        return out, sel[:, :K], xr
+    return out

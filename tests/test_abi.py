@@ -151,3 +151,34 @@ def test_selftest_wait_timeout_validates_before_launch(lib):
         moe.MOE_ERR_INVALID_ARG  # not 256-byte aligned
     assert L.moe_selftest_wait_timeout(ctypes.c_void_p(1 << 20), 0, None) == \
         moe.MOE_ERR_INVALID_ARG  # no room for the status word
+
+
+def _reader(H=2048, I=768, E=128, rank=32):
+    r = moe.ReaderStruct()
+    r.H, r.I, r.E, r.rank = H, I, E, rank
+    for name in ("signs", "g_rows", "v_rows", "w_down", "g_codes", "v_codes", "g_scales",
+                 "v_scales", "dnorm", "U", "coef"):
+        setattr(r, name, 1 << 20)
+    return r
+
+
+def test_reader_validation_without_gpu(lib):
+    L = moe.lib()
+    r = _reader()
+    assert L.moe_reader_workspace_bytes(ctypes.byref(r), 1, 8, 756) > 0
+    assert L.moe_reader_workspace_bytes(ctypes.byref(r), 1, 8, 8 * 768 + 1) == 0  # K > k*I
+    assert L.moe_reader_workspace_bytes(ctypes.byref(r), 1, 32, 10) == 0  # k*I > 16384
+    assert L.moe_reader_workspace_bytes(ctypes.byref(_reader(rank=33)), 1, 8, 10) == 0
+    assert L.moe_reader_workspace_bytes(ctypes.byref(_reader(H=2000)), 1, 8, 10) == 0
+    bad = _reader()
+    bad.U = 0
+    assert L.moe_reader_workspace_bytes(ctypes.byref(bad), 1, 8, 10) == 0
+    vp = ctypes.c_void_p
+    ws = vp(1 << 21)
+    # nscan out of range and a too-small workspace fail before any launch
+    assert L.moe_reader_ffn(vp(1 << 20), ctypes.byref(r), 1, 8, vp(1 << 20), vp(1 << 20), 10, 129,
+                            None, vp(1 << 20), None, None, ws, 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_reader_ffn(vp(1 << 20), ctypes.byref(r), 1, 8, vp(1 << 20), vp(1 << 20), 10, 80,
+                            None, vp(1 << 20), None, None, ws, 16, None) == moe.MOE_ERR_WORKSPACE
+    w = _weights()
+    assert L.moe_reader_build(ctypes.byref(w), ctypes.byref(_reader(I=512)), None) == moe.MOE_ERR_INVALID_ARG
