@@ -250,6 +250,8 @@ def run_ours(args, world, rank, local):
     lib_build.build()
     dev = torch.device("cuda", local)
     wl = syn.workload(args.workload, **overrides(args))
+    if wl.reader_K > 0:
+        return run_reader(args, world, rank, local, wl)
     M = wl.M
     stack = wl.layers > 1
     n_sets = wl.layers if stack else max(1, args.weight_sets)
@@ -497,6 +499,189 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
+# ---------------------------------------------------------------------- channel reader
+def reader_bytes(wl, nvalid_channels, kept):
+    """Algorithmic bytes of one reader decode for one token: the sketch (two-bit codes and
+    fp32 scales of gate and up, the down norm) of every candidate channel, the exact rows
+    (gate, up, down) of the kept ones, the recovery coefficients of the discarded ones, U."""
+    nb = wl.H // 128
+    sketch = nvalid_channels * (2 * nb * (32 + 4) + 4)
+    exact = kept * 3 * wl.H * 2
+    recover = (nvalid_channels - kept) * wl.reader_rank * 2 + wl.H * wl.reader_rank * 4
+    return sketch, exact, recover
+
+
+def run_reader(args, world, rank, local, wl):
+    from routed_expert_ffn_top_gb300 import moe
+
+    dev = torch.device("cuda", local)
+    M, K, nscan = wl.M, wl.reader_K, wl.reader_nscan
+    n_sets = max(1, args.weight_sets)
+    layers, readers = [], []
+    for li in range(n_sets):
+        layer = syn.make_layer(wl, layer=li, seed=1 + rank, device=dev)
+        signs = syn.make_rotation_signs(wl.H, seed=li, device=dev)
+        U = moe.reader_basis(layer["w_down"], wl.reader_rank)  # offline, once per layer
+        readers.append(moe.reader_build(layer, signs, U))
+        layers.append(layer)
+    torch.cuda.synchronize()
+    h0 = syn.make_hidden(wl, seed=1 + rank, device=dev)
+    out = torch.empty_like(h0)
+    ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
+    wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
+    ws = moe.reader_workspace(readers[0], M, wl.k, K)
+    stream = torch.cuda.current_stream()
+
+    def step(i, s=None):
+        li = i % n_sets
+        moe.moe_route_topk(h0, layers[li]["w_router"], layers[li]["bias"], wl.k, topk_ids=ids,
+                           topk_weights=wts, stream=s)
+        moe.moe_reader_ffn(h0, readers[li], ids, wts, K, nscan, out=out, workspace=ws, stream=s)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record()
+        for i in range(args.steps):
+            step(i)
+        ev1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_per_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    clocks = clk.summary()
+    value = M * world / (ms_per_step * 1e-3)
+
+    # the exact block on the same weights and tokens, for comparison
+    ws_exact = moe.alloc_workspace(layers[0], M, wl.k, wl.b, dev)
+    for i in range(args.warmup):
+        moe.moe_decode_block(h0, layers[i % n_sets], wl.k, wl.b, out=out, topk_ids=ids,
+                             topk_weights=wts, workspace=ws_exact)
+    torch.cuda.synchronize()
+    ev0.record()
+    for i in range(args.steps):
+        moe.moe_decode_block(h0, layers[i % n_sets], wl.k, wl.b, out=out, topk_ids=ids,
+                             topk_weights=wts, workspace=ws_exact)
+    ev1.record()
+    torch.cuda.synchronize()
+    exact_us = ev0.elapsed_time(ev1) * 1e3 / args.steps
+
+    # traced pass: the reader's stages
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    names = ("scan_sketch", "select", "exact", "recover", "final")
+    dur = {n: [] for n in names}
+    for i in range(args.steps):
+        li = i % n_sets
+        moe.moe_route_topk(h0, layers[li]["w_router"], layers[li]["bias"], wl.k, topk_ids=ids,
+                           topk_weights=wts)
+        moe.moe_set_trace_events(evs)
+        try:
+            moe.moe_reader_ffn(h0, readers[li], ids, wts, K, nscan, out=out, workspace=ws)
+        finally:
+            moe.moe_set_trace_events(None)
+        evs[5].synchronize()
+        for q, n in enumerate(names):
+            dur[n].append(evs[q].elapsed_time(evs[q + 1]))
+    mean_ms = {n: statistics.mean(v) for n, v in dur.items()}
+    nvalid = M * wl.k * wl.I
+    kept = M * min(K, wl.k * wl.I)
+    sk_b, ex_b, rc_b = reader_bytes(wl, nvalid, kept)
+    peak, peak_kind = measured_peaks()
+    dominant = "sketch" if mean_ms["scan_sketch"] >= mean_ms["exact"] else "exact"
+    alg = sk_b if dominant == "sketch" else ex_b
+    achieved = alg / (mean_ms["scan_sketch" if dominant == "sketch" else "exact"] * 1e-3) / 1e9
+    full = M * wl.k * (2 * wl.H * wl.I * 2 + wl.I * wl.H * 2)  # the routed experts' full bytes
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) hidden states, N(0,0.02) bf16 weights)",
+        "config": {"workload": wl.name, "M": M, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "reader_K": K, "reader_nscan": nscan, "reader_rank": wl.reader_rank,
+                   "l2": "inputs larger than L2: %d independent weight sets and readers cycled"
+                         % n_sets,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "us_per_layer": round(ms_per_step * 1e3, 3),
+        "exact_block_us_per_layer": round(exact_us, 3),
+        "read_fraction_of_routed_bytes": round((sk_b + ex_b + rc_b) / full, 4),
+        "reader_bytes": {"sketch": sk_b, "exact": ex_b, "recover": rc_b},
+        "roofline": {"kernel": "reader_%s_kernel" % dominant, "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": int(alg),
+                     "kernel_ms_traced": {n: round(v, 5) for n, v in mean_ms.items()}},
+        "gpu_launches": 6 * args.steps,  # router + the reader's five kernels
+        "clocks": clocks,
+    }
+    if not args.no_extras:
+        h_host = h0.cpu().pin_memory()
+        out_host = torch.empty_like(h_host).pin_memory()
+        h_dev = torch.empty_like(h0)
+
+        def e2e_step(i):
+            li = i % n_sets
+            h_dev.copy_(h_host, non_blocking=True)
+            moe.moe_route_topk(h_dev, layers[li]["w_router"], layers[li]["bias"], wl.k,
+                               topk_ids=ids, topk_weights=wts)
+            moe.moe_reader_ffn(h_dev, readers[li], ids, wts, K, nscan, out=out, workspace=ws)
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for i in range(max(1, args.warmup)):
+            e2e_step(i)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+        result["e2e"] = {"value": round(M * args.steps * world / t_e2e, 3), "unit": UNIT,
+                         "h2d_bytes_per_step": M * wl.H * 2, "d2h_bytes_per_step": M * wl.H * 2}
+        if rank == 0 and world == 1:
+            result["cpu_baseline"] = reader_cpu_baseline(wl, layers[0], readers[0], h0,
+                                                         args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def _reader_oracle_sample(wl, layer, signs, U, h):
+    """Host data for the reader oracle: the token's routing and its experts' sketches (the
+    sketch is built once per layer, outside the timed decode)."""
+    import oracle
+    import oracle.reader as R
+    hb = syn.bits(h[:1])
+    logits = oracle.router_logits(hb, syn.bits(layer["w_router"]), None, 1, wl.H, wl.E)
+    ids, wts, _ = oracle.topk_softmax(logits, wl.k)
+    experts = sorted(set(ids.reshape(-1).tolist()))
+    sel = torch.as_tensor(experts, device=layer["w_down"].device)
+    f64 = lambda t: t[sel].to(torch.float64).cpu().numpy()  # noqa: E731
+    wg, wu, wd = f64(layer["w_gate"]), f64(layer["w_up"]), f64(layer["w_down"])
+    s64 = signs.cpu().numpy().astype(np.float64)
+    rd = R.build(wg, wu, wd, s64, rank=1)
+    rd["U"] = U.to(torch.float64).cpu().numpy()
+    rd["coef"] = wd @ rd["U"]
+    local = np.array([experts.index(e) for e in ids[0]], np.int32)
+    x = h[0].to(torch.float64).cpu().numpy()
+    return x, local, wts[0], wg, wu, wd, rd, s64
+
+
+def reader_cpu_baseline(wl, layer, reader, h, seconds):
+    import oracle.reader as R
+    x, local, a, wg, wu, wd, rd, s64 = _reader_oracle_sample(wl, layer, reader["signs"],
+                                                             reader["U"], h)
+    total, n = 0.0, 0
+    while total < seconds or n == 0:
+        t0 = time.perf_counter()
+        R.reader_token(x, local, a, wg, wu, wd, rd, s64, wl.reader_K, wl.reader_nscan)
+        total += time.perf_counter() - t0
+        n += 1
+    return {"value": round(n / total, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d decodes of one token through the fp64 numpy reader oracle (its "
+                      "experts' sketches prebuilt), %.1f s" % (n, total)}
+
+
 def _oracle_block_sample(wl, layer, h, tokens):
     """Host copies for the oracle: full router, and only the experts the sample uses."""
     import oracle
@@ -548,6 +733,8 @@ def run_reference(args, world, rank):
     wl = syn.workload(args.workload, **overrides(args))
     layer = syn.make_layer(wl, layer=0, seed=1, device="cpu")
     h = syn.make_hidden(wl, seed=1, device="cpu")
+    if wl.reader_K > 0:
+        return run_reader_reference(args, world, wl, layer, h)
     # each step: the oracle's full block on a sample of at most 8 tokens of the batch
     tokens = min(wl.M, 8)
     hb, wr, bias, w, remap = _oracle_block_sample(wl, layer, h, tokens)
@@ -566,6 +753,36 @@ def run_reference(args, world, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "b": wl.b, "layers_per_step": blocks},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_reader_reference(args, world, wl, layer, h):
+    """The reader oracle as the reference arm: one token's decode per step."""
+    import oracle.reader as R
+    signs = syn.make_rotation_signs(wl.H, seed=0)
+    U = torch.as_tensor(R.down_basis(layer["w_down"].to(torch.float64).numpy(), wl.reader_rank))
+    x, local, a, wg, wu, wd, rd, s64 = _reader_oracle_sample(wl, layer, signs, U, h)
+    for _ in range(args.warmup):
+        R.reader_token(x, local, a, wg, wu, wd, rd, s64, wl.reader_K, wl.reader_nscan)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        R.reader_token(x, local, a, wg, wu, wd, rd, s64, wl.reader_K, wl.reader_nscan)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps / total
+    sample = "one token of the %s layer per step through the fp64 numpy reader oracle" % wl.name
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "reader_K": wl.reader_K, "reader_nscan": wl.reader_nscan},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,

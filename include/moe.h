@@ -229,7 +229,10 @@ int moe_decode_block_noalloc(const void *h, const void *w_router, const float *b
  * events[2] after the alignment (and the row gather of dense weights), events[3] after the
  * gate/up kernel, events[4] after the
  * down kernel, events[5] after the combine kernel (stages a call does not run are not
- * recorded; n must be 6).  An event between two kernels removes the launch overlap the
+ * recorded; n must be 6).  moe_reader_ffn records events[0] before its first kernel, then
+ * events[1..5] after its scan and sketch scores, selection, exact reads, recovery and final
+ * sum.  An
+ * event between two kernels removes the launch overlap the
  * kernels otherwise get, so traced calls run slightly slower.  Pass NULL (n = 0) to stop.
  */
 int moe_set_trace_events(void *const *events, int n);
@@ -275,8 +278,9 @@ int moe_selftest_wait_timeout(void *workspace, size_t ws_bytes, void *stream);
  * Data (caller-allocated device buffers, 16-byte aligned):
  *   signs   [H] int8 +1/-1;               U [H][rank] fp32 (rank <= 32), orthonormal columns
  *   w_down  [E][I][H] bf16 (the layer's W_down, read in place)
- *   g_rows, v_rows [E][I][H] bf16;  g_codes, v_codes [E][I][H/128][8] uint32 (code c of a
- *   block at bits 2(c%16) of word c/16: 00 zero, 01 +1, 11 -1);  g_scales, v_scales
+ *   g_rows, v_rows [E][I][H] bf16;  g_codes, v_codes [E][I][H/128][8] uint32 (per block,
+ *   words 0-3 the mask of nonzero codes, words 4-7 the mask of negative ones; coordinate c
+ *   at bit c%32 of word c/32);  g_scales, v_scales
  *   [E][I][H/128] fp32;  dnorm [E][I] fp32;  coef [E][I][rank] bf16 -- written by
  *   moe_reader_build.
  * Shapes: H a multiple of 128 up to 8192, 1 <= rank <= 32.

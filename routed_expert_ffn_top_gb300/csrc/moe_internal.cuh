@@ -146,6 +146,8 @@ struct ReaderWs {
     int nchunk;
 };
 ReaderWs reader_ws_layout(const ReaderArgs &r, int M, int k, int K);
+// Records the caller's trace event i (moe_set_trace_events) on s, when tracing is on.
+void trace_point(int i, cudaStream_t s);
 cudaError_t launch_reader_build(const ReaderArgs &r, const __nv_bfloat16 *w_gate,
                                 const __nv_bfloat16 *w_up, cudaStream_t stream);
 cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, int M, int k,

@@ -20,12 +20,14 @@
 //
 // Layout of the reader's data (built once from the dense weights by moe_reader_build):
 //   rows g, v      [E][I][H] bf16  channel-major gate and up rows (the exact reads);
-//   codes          [E][I][H/128][8] uint32: 128 two-bit codes per block, code c of a block
-//                  at bits 2(c%16) of word c/16; 00 = 0, 01 = +1, 11 = -1;
+//   codes          [E][I][H/128][8] uint32 per block: words 0-3 the nonzero mask, words 4-7
+//                  the negative mask (coordinate c of the block at bit c%32 of word c/32);
 //   scales         [E][I][H/128] fp32;  dnorm [E][I] fp32;
 //   U              [H][r] fp32;  coef b [E][I][r] bf16.
 // Every sum has an order fixed by indices (never by the grid or by M): a token's output
 // is bitwise reproducible and independent of the other tokens.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -35,6 +37,8 @@ constexpr int kRB = 128;              // coordinates per rotation block
 constexpr int kRWords = kRB / 16;     // uint32 code words per block
 constexpr int kExactChunk = 8;        // selected channels per exact-read CTA (one per warp)
 constexpr int kSelectThreads = 1024;
+constexpr int kSketchWarps = 32;      // one 1024-thread CTA per SM: the scan and the table once
+constexpr int kTRow = 17;             // floats per 4-coordinate group of the nibble table (16 + pad)
 
 // ------------------------------------------------------------------ rotation in a warp
 // A warp holds one 128-coordinate block, lane l coordinates 4l..4l+3 in v[0..3].  The
@@ -117,23 +121,30 @@ __global__ void __launch_bounds__(256)
             fwht128_warp(v, lane);
             const float tau = 0.7f * (warp_sum(fabsf(v[0]) + fabsf(v[1]) + fabsf(v[2]) + fabsf(v[3])) /
                                       (float)kRB);
-            uint32_t bits = 0;
+            uint32_t nz = 0, ng = 0;
             float mag = 0.0f, cnt = 0.0f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (fabsf(v[q]) > tau) {
-                    bits |= (v[q] < 0.0f ? 3u : 1u) << (2 * q);
+                    nz |= 1u << q;
+                    if (v[q] < 0.0f) ng |= 1u << q;
                     mag += fabsf(v[q]);
                     cnt += 1.0f;
                 }
             }
             mag = warp_sum(mag);
             cnt = warp_sum(cnt);
-            // lane l's 8 code bits sit at bits 8 (l % 4) of word l / 4
-            uint32_t word = bits << (8 * (lane & 3));
-            word |= __shfl_xor_sync(0xffffffffu, word, 1);
-            word |= __shfl_xor_sync(0xffffffffu, word, 2);
-            if ((lane & 3) == 0) codes[b * kRWords + (lane >> 2)] = word;
+            // lane l's 4 coordinates sit at bits 4 (l % 8) of word l / 8 of each plane
+            uint32_t wz = nz << (4 * (lane & 7)), wn = ng << (4 * (lane & 7));
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                wz |= __shfl_xor_sync(0xffffffffu, wz, o);
+                wn |= __shfl_xor_sync(0xffffffffu, wn, o);
+            }
+            if ((lane & 7) == 0) {
+                codes[b * kRWords + (lane >> 3)] = wz;
+                codes[b * kRWords + 4 + (lane >> 3)] = wn;
+            }
             if (lane == 0) scales[b] = cnt > 0.0f ? mag / cnt : 0.0f;
         }
     }
@@ -172,104 +183,164 @@ cudaError_t launch_reader_build(const ReaderArgs &r, const __nv_bfloat16 *w_gate
 }
 
 // ----------------------------------------------------------------------------- decode
-// Stage 1a: x of token m rotated block by block; every coordinate outside its block's
-// nscan largest |Rx| (ties: lower coordinate) is zeroed, so the sketch products below
-// need no mask.  Grid (H/128, M), one warp per block.
-__global__ void __launch_bounds__(32)
-    reader_scan_kernel(const __nv_bfloat16 *__restrict__ h, const int8_t *__restrict__ signs,
-                       int H, int nscan, float *__restrict__ xr) {
-    __shared__ float av[kRB];
-    pdl_wait();
-    pdl_launch_dependents();
-    const int lane = threadIdx.x, b = blockIdx.x, m = blockIdx.y;
+// Stage 1a for block b of token m, by one warp: x rotated, and every coordinate outside the
+// block's nscan largest |Rx| (ties: lower coordinate) zeroed, so the sketch products need
+// no mask.  The nscan-th largest magnitude is found bit by bit from the top (its bits as
+// an unsigned integer order like the non-negative floats), counting with warp ballots; the
+// coordinates equal to it are then taken in index order.  xr: where the block's 128 values
+// go (shared memory).
+__device__ __forceinline__ void scan_block(const __nv_bfloat16 *hm, const int8_t *signs, int b,
+                                           int nscan, float *xr, int lane) {
     const int c0 = b * kRB + 4 * lane;
-    const uint2 raw = *reinterpret_cast<const uint2 *>(h + (size_t)m * H + c0);
+    const uint2 raw = *reinterpret_cast<const uint2 *>(hm + c0);
     const char4 sg = *reinterpret_cast<const char4 *>(signs + c0);
     float v[4] = {bf16_lo(raw.x) * sg.x, bf16_hi(raw.x) * sg.y, bf16_lo(raw.y) * sg.z,
                   bf16_hi(raw.y) * sg.w};
     fwht128_warp(v, lane);
+    uint32_t key[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) av[4 * lane + q] = fabsf(v[q]);
-    __syncwarp();
+    for (int q = 0; q < 4; ++q) key[q] = __float_as_uint(fabsf(v[q]));
+    bool keep[4] = {false, false, false, false};
+    if (nscan >= kRB) {
+        keep[0] = keep[1] = keep[2] = keep[3] = true;
+    } else if (nscan > 0) {
+        uint32_t t = 0;  // the largest value with at least nscan keys >= it
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = t | (1u << bit);
+            int cnt = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int c = 4 * lane + q;
-        const float a = av[c];
-        int rank = 0;
-        for (int t = 0; t < kRB; ++t) {
-            const float o = av[t];
-            rank += (o > a) || (o == a && t < c);
+            for (int q = 0; q < 4; ++q) cnt += __popc(__ballot_sync(0xffffffffu, key[q] >= cand));
+            if (cnt >= nscan) t = cand;
         }
-        xr[(size_t)m * H + c0 + q] = rank < nscan ? v[q] : 0.0f;
+        int above = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) above += __popc(__ballot_sync(0xffffffffu, key[q] > t));
+        // equal keys before this lane's (lower lanes hold lower coordinates)
+        int eq = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) eq += key[q] == t;
+        int before = eq;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, before, o);
+            if (lane >= o) before += u;
+        }
+        before -= eq;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (key[q] > t) keep[q] = true;
+            else if (key[q] == t) keep[q] = before++ < nscan - above;
+        }
     }
+    *reinterpret_cast<float4 *>(xr + 4 * lane) =
+        make_float4(keep[0] ? v[0] : 0.0f, keep[1] ? v[1] : 0.0f, keep[2] ? v[2] : 0.0f,
+                    keep[3] ? v[3] : 0.0f);
 }
 
-// sum over one half block (64 coordinates) of code * xr: lane-rotated start so that the 32
-// lanes of a warp read 32 different shared-memory banks.
-__device__ __forceinline__ float half_block_dot(uint4 cw, const float *xr, int lane) {
-    float s = 0.0f;
-#pragma unroll 4
-    for (int t = 0; t < 64; ++t) {
-        const int tt = (t + lane) & 63;
-        const int q = tt >> 4;
-        const uint32_t w = q == 0 ? cw.x : (q == 1 ? cw.y : (q == 2 ? cw.z : cw.w));
-        const uint32_t bits = (w >> (2 * (tt & 15))) & 3u;
-        const float x = xr[tt];
-        if (bits & 1u) s += (bits & 2u) ? -x : x;
-    }
-    return s;
-}
-
-// Stage 1b and the score of Stage 2: one warp per candidate channel f = slot * I + i of
-// token m.  Grid (ceil(k I / 8), M), 8 warps; xr of the token in shared memory.
-__global__ void __launch_bounds__(256)
-    reader_sketch_kernel(ReaderArgs r, const float *__restrict__ xr_all,
-                         const int32_t *__restrict__ ids, const float *__restrict__ wts, int k,
-                         float *__restrict__ ahat, float *__restrict__ score) {
-    extern __shared__ float xs[];  // [H]
+// Stage 1 and the score of Stage 2.  The CTA first rotates and scans the token's x (warp w
+// takes blocks w, w + 32, ...; every CTA of the token does the same, CTA 0 also stores the
+// result for inspection), then tabulates, for every group of 4
+// coordinates g and every 4-bit pattern n, T[g][n] = sum of the (scanned) xr of the pattern's
+// coordinates, coordinates ascending.  A code word pair (nonzero, negative masks of 32
+// coordinates) then dots with xr in 16 table reads: the positive nibbles' sums minus the
+// negative nibbles' sums.  One warp per candidate channel f = slot * I + i at a time (warps
+// stride over the token's channels); lanes take the 32-coordinate words of a block four at
+// a time, and the blocks are summed with their scales in block order.
+// Grid (G, M), 32 warps (one CTA per SM and token, so the scan and the table are built once
+// per SM); shared memory: the table, (H/4) x 17 floats (one pad float per group spreads
+// the lanes' reads over the banks) and xr (H floats).
+template <int kMaxPass>
+__global__ void __launch_bounds__(kSketchWarps * 32)
+    reader_sketch_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h, int nscan,
+                         float *__restrict__ xr_out, const int32_t *__restrict__ ids,
+                         const float *__restrict__ wts, int k, float *__restrict__ ahat,
+                         float *__restrict__ score) {
+    extern __shared__ __align__(16) float T[];  // [H/4][kTRow], then xr [H]
     pdl_wait();
     pdl_launch_dependents();
     const int m = blockIdx.y, H = r.H, I = r.I, nb = H / kRB;
     const int N = k * I;
-    for (int c = threadIdx.x; c < H; c += blockDim.x) xs[c] = xr_all[(size_t)m * H + c];
+    float *xr = T + (H / 4) * kTRow;
+    for (int b = threadIdx.x >> 5; b < nb; b += kSketchWarps)
+        scan_block(h + (size_t)m * H, r.signs, b, nscan, xr + b * kRB, threadIdx.x & 31);
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int c = threadIdx.x; c < H; c += blockDim.x) xr_out[(size_t)m * H + c] = xr[c];
+    for (int q = threadIdx.x; q < (H / 4) * 16; q += blockDim.x) {
+        const int g = q >> 4, n = q & 15;
+        float t = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (n & (1 << c)) t += xr[4 * g + c];
+        T[g * kTRow + n] = t;
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (f >= N) return;
-    const int j = f / I, i = f - j * I;
-    const int e = ids[(size_t)m * k + j];
-    const size_t o = (size_t)m * N + f;
-    if (e < 0 || e >= r.E) {
-        if (lane == 0) {
-            ahat[o] = 0.0f;
-            score[o] = -1.0f;
+    const int nwarps = gridDim.x * kSketchWarps;
+    const int nwords = 4 * nb;              // 32-coordinate words per row
+    const int npass = (nwords + 31) / 32;   // words per lane and row, at most kMaxPass
+    for (int f = blockIdx.x * kSketchWarps + (threadIdx.x >> 5); f < N; f += nwarps) {
+        const int j = f / I, i = f - j * I;
+        const int e = ids[(size_t)m * k + j];
+        const size_t o = (size_t)m * N + f;
+        if (e < 0 || e >= r.E) {
+            if (lane == 0) {
+                ahat[o] = 0.0f;
+                score[o] = -1.0f;
+            }
+            continue;
         }
-        return;
-    }
-    const int64_t ch = (int64_t)e * I + i;
-    float est[2];
+        const int64_t ch = (int64_t)e * I + i;
+        // every load of the channel first: its code words and block scales for both rows
+        uint32_t nzw[2][kMaxPass], ngw[2][kMaxPass];
+        float scw[2][kMaxPass];
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const uint32_t *codes = (p ? r.v_codes : r.g_codes) + ch * nb * kRWords;
-        const float *scales = (p ? r.v_scales : r.g_scales) + ch * nb;
-        float acc = 0.0f;
-        for (int base = 0; base < 2 * nb; base += 32) {  // half blocks, 32 per pass
-            const int idx = base + lane;
-            const bool on = idx < 2 * nb;
-            const int b = idx >> 1, half = idx & 1;
-            float s = 0.0f;
-            if (on)
-                s = half_block_dot(*reinterpret_cast<const uint4 *>(codes + b * kRWords + half * 4),
-                                   xs + b * kRB + half * 64, lane);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);  // the block's two halves
-            if (on && half == 0) acc = fmaf(scales[b], s, acc);
+        for (int p = 0; p < 2; ++p) {
+            const uint32_t *codes = (p ? r.v_codes : r.g_codes) + ch * nb * kRWords;
+            const float *scales = (p ? r.v_scales : r.g_scales) + ch * nb;
+#pragma unroll
+            for (int ps = 0; ps < kMaxPass; ++ps) {
+                const int w = ps * 32 + lane;  // word w of the row: block w / 4, quarter w % 4
+                nzw[p][ps] = ngw[p][ps] = 0u;
+                scw[p][ps] = 0.0f;
+                if (ps < npass && w < nwords) {
+                    nzw[p][ps] = codes[(w >> 2) * kRWords + (w & 3)];
+                    ngw[p][ps] = codes[(w >> 2) * kRWords + 4 + (w & 3)];
+                    scw[p][ps] = scales[w >> 2];
+                }
+            }
         }
-        est[p] = warp_sum(acc);
-    }
-    if (lane == 0) {
-        const float a = silu_f32(est[0]) * est[1];
-        ahat[o] = a;
-        score[o] = wts[(size_t)m * k + j] * r.dnorm[ch] * fabsf(a);
+        const float dn = r.dnorm[ch];
+        const float wj = wts[(size_t)m * k + j];
+        float est[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int ps = 0; ps < kMaxPass; ++ps) {
+                if (ps >= npass) break;
+                const int w = ps * 32 + lane;
+                const uint32_t pos = nzw[p][ps] & ~ngw[p][ps], neg = nzw[p][ps] & ngw[p][ps];
+                float s = 0.0f;
+                if (w < nwords) {
+                    const float *Tw = T + (size_t)(w * 8) * kTRow;  // groups 8w .. 8w+7
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        s += Tw[q * kTRow + ((pos >> (4 * q)) & 15u)] -
+                             Tw[q * kTRow + ((neg >> (4 * q)) & 15u)];
+                }
+                // the block's four words, in order, then its scale
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (w < nwords && (lane & 3) == 0) acc = fmaf(scw[p][ps], s, acc);
+            }
+            est[p] = warp_sum(acc);
+        }
+        if (lane == 0) {
+            const float a = silu_f32(est[0]) * est[1];
+            ahat[o] = a;
+            score[o] = wj * dn * fabsf(a);
+        }
     }
 }
 
@@ -306,8 +377,8 @@ __global__ void __launch_bounds__(kSelectThreads)
     reader_select_kernel(const float *__restrict__ score, int N, int K,
                          uint8_t *__restrict__ keep, int32_t *__restrict__ sel,
                          int32_t *__restrict__ nsel) {
-    extern __shared__ uint32_t keys[];  // [N]
-    __shared__ int hist[256];
+    extern __shared__ uint32_t keys[];  // [N], then 32 warp histograms of 256 bins
+    int *whist = reinterpret_cast<int *>(keys + N);
     __shared__ int warp_tot[32];
     __shared__ int s_nvalid, s_digit, s_remaining;
     pdl_wait();
@@ -328,20 +399,23 @@ __global__ void __launch_bounds__(kSelectThreads)
     uint32_t prefix = 0, mask = 0;
     int remaining = Keff;
     if (Keff > 0) {
+        const int wbase = (tid >> 5) * 256;
         for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int d = tid; d < 256; d += kSelectThreads) hist[d] = 0;
+            for (int d = tid; d < 32 * 256; d += kSelectThreads) whist[d] = 0;
             __syncthreads();
+            // each warp counts into its own histogram (integer adds commute)
             for (int f = tid; f < N; f += kSelectThreads)
-                if ((keys[f] & mask) == prefix) atomicAdd(&hist[(keys[f] >> shift) & 255u], 1);
+                if ((keys[f] & mask) == prefix) atomicAdd(&whist[wbase + ((keys[f] >> shift) & 255u)], 1);
             __syncthreads();
-            if (tid == 0) {
-                int cum = 0, d = 255;
-                for (; d > 0; --d) {
-                    if (cum + hist[d] >= remaining) break;
-                    cum += hist[d];
-                }
-                s_digit = d;
-                s_remaining = remaining - cum;
+            // thread t < 256 owns digit 255 - t: its count over the warps, then a scan in
+            // descending digit order finds the digit where the count reaches `remaining`
+            int c = 0;
+            if (tid < 256)
+                for (int w = 0; w < 32; ++w) c += whist[w * 256 + (255 - tid)];
+            const int incl = block_scan_1024(c, warp_tot);
+            if (tid < 256 && c > 0 && incl >= remaining && incl - c < remaining) {
+                s_digit = 255 - tid;
+                s_remaining = remaining - (incl - c);
             }
             __syncthreads();
             prefix |= (uint32_t)s_digit << shift;
@@ -381,6 +455,7 @@ __global__ void __launch_bounds__(kSelectThreads)
 // Stage 2 exact reads: chunk c of token m's kept channels (positions 8c .. 8c+7 of the
 // ascending list), one warp per channel for a = SiLU(g . x) (v . x), then the chunk's
 // sum of w a d in channel order into its own partial row.  Grid (nchunk, M), 256 threads.
+template <int kDPass>
 __global__ void __launch_bounds__(256)
     reader_exact_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h,
                         const int32_t *__restrict__ ids, const float *__restrict__ wts, int k,
@@ -397,49 +472,82 @@ __global__ void __launch_bounds__(256)
     uint4 *xs4 = reinterpret_cast<uint4 *>(xraw);
     for (int q = threadIdx.x; q < H / 8; q += blockDim.x) xs4[q] = hx[q];
     __syncthreads();
+    // the chunk's channels first (one per warp), so that every load below can be issued at once
     const int s = c * kExactChunk + warp;
-    int64_t ch = -1;
-    float w = 0.0f;
-    if (s < nsel[m]) {
-        const int f = sel[(size_t)m * K + s];
-        const int j = f / I, i = f - j * I;
-        const int e = ids[(size_t)m * k + j];
-        if (e >= 0 && e < r.E) {
-            ch = (int64_t)e * I + i;
-            w = wts[(size_t)m * k + j];
+    if (lane == 0) {
+        int64_t ch = -1;
+        float w = 0.0f;
+        if (s < nsel[m]) {
+            const int f = sel[(size_t)m * K + s];
+            const int j = f / I, i = f - j * I;
+            const int e = ids[(size_t)m * k + j];
+            if (e >= 0 && e < r.E) {
+                ch = (int64_t)e * I + i;
+                w = wts[(size_t)m * k + j];
+            }
         }
+        chs[warp] = ch;
+        wa[warp] = w;
     }
+    __syncthreads();
+    // this thread's pieces of the chunk's down rows are in flight while the warps form a
+    const int c0 = threadIdx.x * 8;  // 2048 columns per pass: kDPass = ceil(H / 2048)
+    uint4 dv[kDPass][kExactChunk];
+#pragma unroll
+    for (int ps = 0; ps < kDPass; ++ps)
+#pragma unroll
+        for (int q = 0; q < kExactChunk; ++q)
+            if (c0 + ps * 2048 < H && chs[q] >= 0)
+                dv[ps][q] = *reinterpret_cast<const uint4 *>(r.w_down + chs[q] * H + c0 + ps * 2048);
+    const int64_t ch = chs[warp];
     if (ch >= 0) {
         const uint4 *g = reinterpret_cast<const uint4 *>(r.g_rows + ch * H);
         const uint4 *v = reinterpret_cast<const uint4 *>(r.v_rows + ch * H);
         float gx = 0.0f, vx = 0.0f;
-        for (int q = lane; q < H / 8; q += 32) {
-            const uint4 xa = xs4[q], ga = g[q], va = v[q];
-            const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
-            const uint32_t gw[4] = {ga.x, ga.y, ga.z, ga.w};
-            const uint32_t vw[4] = {va.x, va.y, va.z, va.w};
+        // 8 pieces of each row per lane in flight, then their products in piece order
+        for (int q0 = lane; q0 < H / 8; q0 += 32 * 8) {
+            uint4 ga[8], va[8];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                gx = fmaf(bf16_lo(gw[t]), bf16_lo(xw[t]), gx);
-                gx = fmaf(bf16_hi(gw[t]), bf16_hi(xw[t]), gx);
-                vx = fmaf(bf16_lo(vw[t]), bf16_lo(xw[t]), vx);
-                vx = fmaf(bf16_hi(vw[t]), bf16_hi(xw[t]), vx);
+            for (int u = 0; u < 8; ++u) {
+                const int q = q0 + 32 * u;
+                if (q < H / 8) {
+                    ga[u] = g[q];
+                    va[u] = v[q];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = q0 + 32 * u;
+                if (q >= H / 8) break;
+                const uint4 xa = xs4[q];
+                const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
+                const uint32_t gw[4] = {ga[u].x, ga[u].y, ga[u].z, ga[u].w};
+                const uint32_t vw[4] = {va[u].x, va[u].y, va[u].z, va[u].w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    gx = fmaf(bf16_lo(gw[t]), bf16_lo(xw[t]), gx);
+                    gx = fmaf(bf16_hi(gw[t]), bf16_hi(xw[t]), gx);
+                    vx = fmaf(bf16_lo(vw[t]), bf16_lo(xw[t]), vx);
+                    vx = fmaf(bf16_hi(vw[t]), bf16_hi(xw[t]), vx);
+                }
             }
         }
         gx = warp_sum(gx);
         vx = warp_sum(vx);
-        if (lane == 0) wa[warp] = w * (silu_f32(gx) * vx);
+        __syncwarp();
+        if (lane == 0) wa[warp] = wa[warp] * (silu_f32(gx) * vx);
     }
-    if (lane == 0) chs[warp] = ch;
     __syncthreads();
     float *out = partial + ((size_t)m * nchunk + c) * H;
-    for (int c0 = threadIdx.x * 8; c0 < H; c0 += blockDim.x * 8) {
+#pragma unroll
+    for (int ps = 0; ps < kDPass; ++ps) {
+        const int cc = c0 + ps * 2048;
+        if (cc >= H) break;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
         for (int q = 0; q < kExactChunk; ++q) {
-            const int64_t cq = chs[q];
-            if (cq < 0) continue;
-            const uint4 dv = *reinterpret_cast<const uint4 *>(r.w_down + cq * H + c0);
-            const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+            if (chs[q] < 0) continue;
+            const uint32_t dw[4] = {dv[ps][q].x, dv[ps][q].y, dv[ps][q].z, dv[ps][q].w};
             const float a = wa[q];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -447,81 +555,125 @@ __global__ void __launch_bounds__(256)
                 acc[2 * t + 1] = fmaf(a, bf16_hi(dw[t]), acc[2 * t + 1]);
             }
         }
-        *reinterpret_cast<float4 *>(out + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(out + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        *reinterpret_cast<float4 *>(out + cc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(out + cc + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
 }
 
 // Stage 3: z_j = sum over the discarded channels i of slot j (ascending within a thread,
-// then threads in order) of w_j ahat b_{e,i}.  Grid (k, M), 256 threads.
+// then the lanes by a fixed xor tree, then the warps in order) of w_j ahat b_{e,i}.
+// It needs only the selection, which was complete before the exact-read grid that precedes
+// it could start, so it runs beside that grid (reading the selection from L2) and waits for
+// it only before finishing: the final grid, which waits for this one, then sees both.
+// Part p of slot j takes channels [p I/4, (p+1) I/4).  Grid (4 k, M), 256 threads.
+constexpr int kRecParts = 4;
 __global__ void __launch_bounds__(256)
     reader_recover_kernel(ReaderArgs r, const int32_t *__restrict__ ids,
                           const float *__restrict__ wts, int k, const float *__restrict__ ahat,
                           const uint8_t *__restrict__ keep, float *__restrict__ zpart) {
-    __shared__ float red[256][33];
-    pdl_wait();
+    __shared__ float red[8][kReaderMaxRank];
     pdl_launch_dependents();
-    const int j = blockIdx.x, m = blockIdx.y, I = r.I, rank = r.rank, tid = threadIdx.x;
+    const int j = blockIdx.x / kRecParts, part = blockIdx.x % kRecParts, m = blockIdx.y;
+    const int I = r.I, rank = r.rank, tid = threadIdx.x;
     const int N = k * I;
+    const int per = (I + kRecParts - 1) / kRecParts;
+    const int i0 = part * per, i1 = min(I, i0 + per);
     const int e = ids[(size_t)m * k + j];
-    float acc[32];
+    float acc[kReaderMaxRank];
 #pragma unroll
-    for (int q = 0; q < 32; ++q) acc[q] = 0.0f;
+    for (int q = 0; q < kReaderMaxRank; ++q) acc[q] = 0.0f;
     if (e >= 0 && e < r.E) {
         const float w = wts[(size_t)m * k + j];
-        for (int i = tid; i < I; i += 256) {
+        for (int i = i0 + tid; i < i1; i += 256) {
             const size_t f = (size_t)m * N + (size_t)j * I + i;
-            if (keep[f]) continue;
-            const float cw = w * ahat[f];
+            if (__ldcg(keep + f)) continue;
+            const float cw = w * __ldcg(ahat + f);
             const __nv_bfloat16 *b = r.coef + ((int64_t)e * I + i) * rank;
+            if ((rank & 7) == 0) {  // whole 16-byte pieces of 8 coefficients
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-                if (q < rank) acc[q] = fmaf(cw, __bfloat162float(b[q]), acc[q]);
+                for (int q8 = 0; q8 < kReaderMaxRank / 8; ++q8) {
+                    if (q8 * 8 >= rank) break;
+                    const uint4 pc = *reinterpret_cast<const uint4 *>(b + q8 * 8);
+                    const uint32_t pw[4] = {pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        acc[q8 * 8 + 2 * t] = fmaf(cw, bf16_lo(pw[t]), acc[q8 * 8 + 2 * t]);
+                        acc[q8 * 8 + 2 * t + 1] = fmaf(cw, bf16_hi(pw[t]), acc[q8 * 8 + 2 * t + 1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kReaderMaxRank; ++q)
+                    if (q < rank) acc[q] = fmaf(cw, __bfloat162float(b[q]), acc[q]);
+            }
         }
     }
 #pragma unroll
-    for (int q = 0; q < 32; ++q) red[tid][q] = acc[q];
+    for (int q = 0; q < kReaderMaxRank; ++q) {
+        const float v = warp_sum(acc[q]);
+        if ((tid & 31) == 0) red[tid >> 5][q] = v;
+    }
     __syncthreads();
     if (tid < rank) {
         float z = 0.0f;
-        for (int t = 0; t < 256; ++t) z += red[t][tid];
-        zpart[((size_t)m * k + j) * rank + tid] = z;
+        for (int w = 0; w < 8; ++w) z += red[w][tid];
+        zpart[(((size_t)m * k + j) * kRecParts + part) * rank + tid] = z;
     }
+    pdl_wait();  // the exact-read grid has finished before this one does
 }
 
-// out[m][n] = bf16(residual + (sum of the chunk partials in chunk order + sum_r U[n][r] z[r])),
-// z = sum over slots in order.  Grid (ceil(H / 256), M).
+// out[m][n] = bf16(residual + (ex + sum_r U[n][r] z[r])), z = sum over slots in order, ex the
+// chunk partials: warp w of the CTA sums chunks w, w + 8, ... in order for 32 columns, then
+// the 8 warps' sums are added in warp order.  Grid (ceil(H / 32), M), 256 threads.
 __global__ void __launch_bounds__(256)
     reader_final_kernel(ReaderArgs r, int k, int nchunk, const float *__restrict__ partial,
                         const float *__restrict__ zpart, const __nv_bfloat16 *__restrict__ residual,
                         __nv_bfloat16 *__restrict__ out) {
-    __shared__ float z[32];
+    __shared__ float z[kReaderMaxRank];
+    __shared__ float red[8][32];
     pdl_wait();
     pdl_launch_dependents();
     const int m = blockIdx.y, H = r.H, rank = r.rank, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     if (tid < rank) {
         float s = 0.0f;
-        for (int j = 0; j < k; ++j) s += zpart[((size_t)m * k + j) * rank + tid];
+        for (int q = 0; q < k * kRecParts; ++q) s += __ldcg(zpart + ((size_t)m * k * kRecParts + q) * rank + tid);
         z[tid] = s;
     }
-    __syncthreads();
-    const int n = blockIdx.x * 256 + tid;
-    if (n >= H) return;
-    const float *pp = partial + (size_t)m * nchunk * H + n;
+    const int n = blockIdx.x * 32 + lane;
     float ex = 0.0f;
-    int c = 0;
-    for (; c + 8 <= nchunk; c += 8) {
-        float v[8];
+    if (n < H) {
+        const float *pp = partial + (size_t)m * nchunk * H + n;
+        int c = warp;
+        for (; c + 8 * 7 < nchunk; c += 8 * 8) {  // 8 of the warp's chunks in flight
+            float v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = pp[(size_t)(c + q) * H];
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(pp + (size_t)(c + 8 * u) * H);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) ex += v[q];
+            for (int u = 0; u < 8; ++u) ex += v[u];
+        }
+        for (; c < nchunk; c += 8) ex += __ldcg(pp + (size_t)c * H);
     }
-    for (; c < nchunk; ++c) ex += pp[(size_t)c * H];
-    float rec = 0.0f;
-    for (int q = 0; q < rank; ++q) rec = fmaf(r.U[(size_t)n * rank + q], z[q], rec);
+    red[warp][lane] = ex;
+    __syncthreads();
+    // U z for the CTA's 32 columns: warp w takes columns 4w .. 4w+3, lane q the q-th
+    // coefficient of a column's U row (one coalesced row read), then a fixed xor tree
+    __shared__ float recs[32];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int col = blockIdx.x * 32 + 4 * warp + u;
+        float t = 0.0f;
+        if (col < H && lane < rank) t = r.U[(size_t)col * rank + lane] * z[lane];
+        t = warp_sum(t);
+        if (lane == 0) recs[4 * warp + u] = t;
+    }
+    __syncthreads();
+    if (warp != 0 || n >= H) return;
+    float acc = 0.0f;
+    for (int w = 0; w < 8; ++w) acc += red[w][lane];
+    acc += recs[lane];
     const float res = residual ? __bfloat162float(residual[(size_t)m * H + n]) : 0.0f;
-    out[(size_t)m * H + n] = __float2bfloat16_rn(res + (ex + rec));
+    out[(size_t)m * H + n] = __float2bfloat16_rn(res + acc);
 }
 
 // Workspace of one reader call: xr, ahat, score, keep, sel, nsel, partial, zpart.
@@ -543,7 +695,7 @@ ReaderWs reader_ws_layout(const ReaderArgs &r, int M, int k, int K) {
     L.sel = take((size_t)M * (K > 0 ? K : 1) * 4);
     L.nsel = take((size_t)M * 4);
     L.partial = take((size_t)M * (L.nchunk > 0 ? L.nchunk : 1) * r.H * 4);
-    L.zpart = take((size_t)M * k * r.rank * 4);
+    L.zpart = take((size_t)M * k * kRecParts * r.rank * 4);
     L.total = off;
     return L;
 }
@@ -564,22 +716,27 @@ cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, in
     const int N = k * r.I;
     cudaLaunchAttribute attrs[2];
     cudaError_t err;
+    // trace points: 0 before the first kernel, 1 after the scan and sketch scores, 2 after
+    // the selection, 3 after the exact reads, 4 after the recovery, 5 after the final sum
+    trace_point(0, stream);
     {
-        cudaLaunchConfig_t cfg = launch_config(dim3(r.H / kRB, M), dim3(32), 0, stream, attrs, 0);
-        err = cudaLaunchKernelEx(&cfg, reader_scan_kernel, h, r.signs, r.H, nscan, xr);
+        // the nibble table and xr
+        const size_t smem = ((size_t)(r.H / 4) * kTRow + r.H) * 4;
+        const int npass = (r.H / 32 + 31) / 32;  // 32-coordinate words per lane and row
+        auto kern = npass <= 1 ? reader_sketch_kernel<1>
+                  : npass <= 2 ? reader_sketch_kernel<2>
+                  : npass <= 4 ? reader_sketch_kernel<4> : reader_sketch_kernel<8>;
+        err = ensure_smem(reinterpret_cast<const void *>(kern), smem);
+        if (err != cudaSuccess) return err;
+        const int G = (int)std::min<int64_t>((N + kSketchWarps - 1) / kSketchWarps, num_sms());
+        cudaLaunchConfig_t cfg =
+            launch_config(dim3(G, M), dim3(kSketchWarps * 32), smem, stream, attrs, 0);
+        err = cudaLaunchKernelEx(&cfg, kern, r, h, nscan, xr, ids, wts, k, ahat, score);
         if (err != cudaSuccess) return err;
     }
+    trace_point(1, stream);
     {
-        const size_t smem = (size_t)r.H * 4;
-        err = ensure_smem(reinterpret_cast<const void *>(reader_sketch_kernel), smem);
-        if (err != cudaSuccess) return err;
-        cudaLaunchConfig_t cfg = launch_config(dim3((N + 7) / 8, M), dim3(256), smem, stream, attrs, 0);
-        err = cudaLaunchKernelEx(&cfg, reader_sketch_kernel, r, (const float *)xr, ids, wts, k,
-                                 ahat, score);
-        if (err != cudaSuccess) return err;
-    }
-    {
-        const size_t smem = (size_t)N * 4;
+        const size_t smem = (size_t)N * 4 + 32 * 256 * 4;  // keys and the warp histograms
         err = ensure_smem(reinterpret_cast<const void *>(reader_select_kernel), smem);
         if (err != cudaSuccess) return err;
         cudaLaunchConfig_t cfg = launch_config(dim3(M), dim3(kSelectThreads), smem, stream, attrs, 0);
@@ -587,25 +744,32 @@ cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, in
                                  nsel);
         if (err != cudaSuccess) return err;
     }
+    trace_point(2, stream);
     if (L.nchunk > 0) {
         const size_t smem = (size_t)r.H * 2;
+        const int dp = (r.H + 2047) / 2048;
+        auto kern = dp <= 1 ? reader_exact_kernel<1>
+                  : dp <= 2 ? reader_exact_kernel<2> : reader_exact_kernel<4>;
         cudaLaunchConfig_t cfg = launch_config(dim3(L.nchunk, M), dim3(256), smem, stream, attrs, 0);
-        err = cudaLaunchKernelEx(&cfg, reader_exact_kernel, r, h, ids, wts, k, K,
+        err = cudaLaunchKernelEx(&cfg, kern, r, h, ids, wts, k, K,
                                  (const int32_t *)sel, (const int32_t *)nsel, L.nchunk, partial);
         if (err != cudaSuccess) return err;
     }
+    trace_point(3, stream);
     {
-        cudaLaunchConfig_t cfg = launch_config(dim3(k, M), dim3(256), 0, stream, attrs, 0);
+        cudaLaunchConfig_t cfg = launch_config(dim3(k * kRecParts, M), dim3(256), 0, stream, attrs, 0);
         err = cudaLaunchKernelEx(&cfg, reader_recover_kernel, r, ids, wts, k, (const float *)ahat,
                                  (const uint8_t *)keep, zpart);
         if (err != cudaSuccess) return err;
     }
+    trace_point(4, stream);
     {
         cudaLaunchConfig_t cfg =
-            launch_config(dim3((r.H + 255) / 256, M), dim3(256), 0, stream, attrs, 0);
+            launch_config(dim3((r.H + 31) / 32, M), dim3(256), 0, stream, attrs, 0);
         err = cudaLaunchKernelEx(&cfg, reader_final_kernel, r, k, L.nchunk, (const float *)partial,
                                  (const float *)zpart, residual, out);
     }
+    trace_point(5, stream);
     return err;
 }
 

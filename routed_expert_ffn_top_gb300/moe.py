@@ -418,9 +418,9 @@ def reader_basis(w_down: torch.Tensor, rank: int = 32) -> torch.Tensor:
     H x (E I) matrix of down columns, from the eigenvectors of D^T D (an offline build step
     done once per layer with torch's symmetric eigensolver, not part of the decode path)."""
     D = w_down.reshape(-1, w_down.shape[-1]).to(torch.float64)
-    evals, evecs = torch.linalg.eigh(D.T @ D)
+    evals, evecs = torch.linalg.eigh((D.T @ D).cpu())  # H x H, solved on the host
     order = torch.argsort(evals, descending=True, stable=True)[:rank]
-    return evecs[:, order].to(torch.float32).contiguous()
+    return evecs[:, order].to(device=w_down.device, dtype=torch.float32).contiguous()
 
 
 def _reader_struct(rd: dict) -> ReaderStruct:

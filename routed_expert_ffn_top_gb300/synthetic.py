@@ -49,6 +49,11 @@ class Workload:
     residual: bool = False
     w_std: float = 0.02
     h_std: float = 1.0
+    # channel reader (dense weights): channels read exactly per token (0: not a reader
+    # workload), coordinates scanned per 128-block, rank of the recovery map
+    reader_K: int = 0
+    reader_nscan: int = 80
+    reader_rank: int = 32
 
 
 # The five workloads: a single decode layer at one token, the same layer at 21 tokens (the
@@ -67,6 +72,9 @@ WORKLOADS = {
                              kind=W_VQLR, d=8, K=256, r=384),
     "large_m256": Workload("large_m256", H=4096, I=1536, E=128, k=8, b=64, M=256,
                            router_bias=True),
+    # the decode layer at one token through the channel reader: 756 of the 8 x 768 candidate
+    # channels (12.3%) read exactly, 80 of 128 coordinates scanned, a rank-32 map
+    "reader_m1": Workload("reader_m1", H=2048, I=768, E=128, k=8, b=8, M=1, reader_K=756),
 }
 
 

@@ -28,19 +28,21 @@ def _f64(t):
 
 
 def _pack_codes(codes):
-    """int8 codes [..., nb, 128] in {-1,0,1} -> the library's uint32 words [..., nb, 8]."""
-    c = np.asarray(codes, np.int64)
-    two = np.where(c > 0, 1, np.where(c < 0, 3, 0)).astype(np.uint64)
-    two = two.reshape(c.shape[:-1] + (8, 16))
-    words = (two << (2 * np.arange(16, dtype=np.uint64))).sum(axis=-1).astype(np.uint32)
-    return words.view(np.int32)
+    """int8 codes [..., nb, 128] in {-1,0,1} -> the library's words [..., nb, 8]: words 0-3
+    the nonzero mask, 4-7 the negative mask, coordinate c at bit c%32 of word c/32."""
+    c = np.asarray(codes, np.int64).reshape(np.shape(codes)[:-1] + (4, 32))
+    bit = np.uint64(1) << np.arange(32, dtype=np.uint64)
+    nz = ((c != 0).astype(np.uint64) * bit).sum(axis=-1)
+    ng = ((c < 0).astype(np.uint64) * bit).sum(axis=-1)
+    return np.concatenate([nz, ng], axis=-1).astype(np.uint32).view(np.int32)
 
 
 def _unpack_codes(words):
     w = np.asarray(words).view(np.uint32).astype(np.uint64)
-    two = (w[..., None] >> (2 * np.arange(16, dtype=np.uint64))) & 3
-    code = np.where(two == 1, 1, np.where(two == 3, -1, 0)).astype(np.int8)
-    return code.reshape(w.shape[:-1] + (128,))
+    bits = (w[..., None] >> np.arange(32, dtype=np.uint64)) & 1
+    nz = bits[..., :4, :].reshape(w.shape[:-1] + (128,))
+    ng = bits[..., 4:, :].reshape(w.shape[:-1] + (128,))
+    return np.where(nz == 1, np.where(ng == 1, -1, 1), 0).astype(np.int8)
 
 
 def _setup(H=256, I=256, E=8, k=4, M=5, rank=16, seed=0):
