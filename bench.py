@@ -191,7 +191,9 @@ def library_block(wl) -> int:
 
 
 def gateup_kernel_name(wl) -> str:
-    return "gemm_gateup_kernel" if gemm_regime(wl) else "gateup_vq_kernel"
+    if gemm_regime(wl):
+        return "gemm_gateup_kernel"
+    return "vq_ttable_partial_kernel" if wl.vq_form == 1 else "gateup_vq_kernel"
 
 
 def kernel_source_hash(kernel: str = "gemm_gateup_kernel"):
@@ -267,7 +269,8 @@ def run_ours(args, world, rank, local):
     # combine
     fused_align = 1 <= M <= 8 and M * wl.k <= 256
     gemm = gemm_regime(wl)
-    launches_per_block = (4 if fused_align else 5) + (1 if gemm and not fused_align else 0)
+    launches_per_block = ((4 if fused_align else 5) + (1 if gemm and not fused_align else 0)
+                          + (1 if wl.vq_form == 1 else 0))  # the projected code books: 2 kernels
 
     def eager_step(i, s):
         """One step: a single layer, or all L layers of the residual stack."""

@@ -83,7 +83,14 @@ typedef enum moe_status {
  *     c_up [E,r,I] bf16 (expert-private coefficients).  z = D^T h is computed once per
  *     token and projection (in the router's launch), then accumulated with the VQ sum.
  *   w_down [E,I,H] bf16 in every case (the down projection stays dense).
- * Fields after w_down were added for MOE_W_VQLR_GATEUP; zero them for the other kinds.
+ *   vq_form (MOE_W_VQ_GATEUP only): 0 multiplies every index's code word with h in
+ *     shared memory (GEMV streams, any M); 1 uses projected code books ("A Multi-Engine
+ *     Dataflow ...", Section 2.3): per token and index row q the table
+ *     T[q][kappa] = sum_t h[d q + t] B[kappa][t], so that g_i = sum_q T[q][J[e][q][i]] (one
+ *     lookup per index instead of d products), for at most 4 tokens (M > 4:
+ *     MOE_ERR_UNSUPPORTED).  The two forms add in different orders; each is bitwise
+ *     reproducible and independent of M on its own.
+ * Fields after w_down were added later; zero them when they do not apply.
  */
 typedef struct moe_expert_weights {
     int32_t kind;
@@ -101,6 +108,7 @@ typedef struct moe_expert_weights {
     const void *c_gate;
     const void *c_up;
     int32_t r;
+    int32_t vq_form;
 } moe_expert_weights_t;
 
 /* A short static description of a status code (never NULL). */

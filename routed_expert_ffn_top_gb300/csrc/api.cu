@@ -54,6 +54,7 @@ WsLayout ws_layout(const Dims &d) {
     const size_t tile_rows = d.gemm ? (size_t)(d.cap / d.b) * d.tpb * d.kn : 0;
     L.x_tiles = take(tile_rows * d.H * 2);
     L.p_tiles = take(tile_rows * d.I * 2);
+    L.tt_part = take(d.ttable ? (size_t)vq_ttable_slices(d.H, d.vqd) * d.R * 2 * d.I * 4 : 0);
     L.total = off;
     return L;
 }
@@ -207,6 +208,8 @@ static int check_weights(const moe_expert_weights_t *w) {
     if (w->H % kBoxRows != 0 || w->H > 8192) return MOE_ERR_UNSUPPORTED;
     if (w->E < 8 || w->E > 512 || w->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (!w->w_down || !aligned(w->w_down, 16)) return MOE_ERR_INVALID_ARG;
+    if (w->vq_form != 0 && w->vq_form != 1) return MOE_ERR_INVALID_ARG;
+    if (w->vq_form == 1 && w->kind != MOE_W_VQ_GATEUP) return MOE_ERR_UNSUPPORTED;
     if (w->kind == MOE_W_DENSE_BF16) {
         if (!w->w_gate || !w->w_up || !aligned(w->w_gate, 16) || !aligned(w->w_up, 16))
             return MOE_ERR_INVALID_ARG;
@@ -234,6 +237,14 @@ static int check_weights(const moe_expert_weights_t *w) {
 // Rank of the low-rank term (0 unless the weights are VQ + low rank).
 static int lr_rank(const moe_expert_weights_t *w) {
     return (w && w->kind == MOE_W_VQLR_GATEUP) ? w->r : 0;
+}
+
+static Dims dims_for(const moe_expert_weights_t *w, int M, int k, int b) {
+    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
+    d.r = lr_rank(w);
+    d.ttable = w->kind == MOE_W_VQ_GATEUP && w->vq_form == 1;
+    d.vqd = w->d;
+    return d;
 }
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -304,8 +315,8 @@ size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, i
     if (!w || M < 0 || k <= 0 || k > 32 || k > w->E || check_block(b) != MOE_OK) return 0;
     if (w->H <= 0 || w->I <= 0 || w->E <= 0) return 0;
     if ((int64_t)M * k >= (1 << 24)) return 0;
-    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
-    d.r = lr_rank(w);
+    if (w->vq_form != 0 && (w->vq_form != 1 || w->kind != MOE_W_VQ_GATEUP)) return 0;
+    Dims d = dims_for(w, M, k, b);
     return ws_layout(d).total;
 }
 
@@ -451,8 +462,28 @@ static int run_experts(const void *h, const moe_expert_weights_t *w, const Dims 
     a.z = lowrank ? reinterpret_cast<const float *>(ws + L.z) : nullptr;
     a.r = lowrank ? d.r : 0;
     a.n_rb = lowrank ? (d.r + kBoxRows - 1) / kBoxRows : 0;
-    cudaError_t err = launch_gateup_vq(tm_gate, tm_up, lowrank ? &tm_cgate : nullptr,
-                                       lowrank ? &tm_cup : nullptr, a, w->d, stream);
+    cudaError_t err;
+    if (d.ttable) {
+        VQTableArgs t;
+        t.h = a.h;
+        t.j_gate = w->j_gate;
+        t.j_up = w->j_up;
+        t.cb_gate = static_cast<const __nv_bfloat16 *>(w->cb_gate);
+        t.cb_up = static_cast<const __nv_bfloat16 *>(w->cb_up);
+        t.ids = topk_ids;
+        t.M = d.M;
+        t.k = d.k;
+        t.E = d.E;
+        t.H = d.H;
+        t.I = d.I;
+        t.d = w->d;
+        t.partial = reinterpret_cast<float *>(ws + L.tt_part);
+        t.p = a.p;
+        err = launch_vq_ttable(t, stream);
+    } else {
+        err = launch_gateup_vq(tm_gate, tm_up, lowrank ? &tm_cgate : nullptr,
+                               lowrank ? &tm_cup : nullptr, a, w->d, stream);
+    }
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
     err = launch_down(tm_down, a, stream);
@@ -473,6 +504,7 @@ static int check_ffn_common(const void *h, const moe_expert_weights_t *w, int M,
     if (rc != MOE_OK) return rc;
     if (M < 0 || k <= 0) return MOE_ERR_INVALID_ARG;
     if (k > 32 || k > w->E || (int64_t)M * k >= (1 << 24)) return MOE_ERR_UNSUPPORTED;
+    if (w->vq_form == 1 && M > kTTMaxTokens) return MOE_ERR_UNSUPPORTED;
     if (M == 0) return MOE_OK;
     if (!h || !out || !workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned(h, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
@@ -495,8 +527,7 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
                       (num_padded != nullptr);
     if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
     if (given == 0) b = effective_block(w, M, k, b);
-    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
-    d.r = lr_rank(w);
+    Dims d = dims_for(w, M, k, b);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -549,8 +580,7 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
         !aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
     if (pick_regime) b = effective_block(w, M, k, b);
-    Dims d = make_dims(M, k, w->E, w->H, w->I, b, w->kind);
-    d.r = lr_rank(w);
+    Dims d = dims_for(w, M, k, b);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);

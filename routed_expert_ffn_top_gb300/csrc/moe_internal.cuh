@@ -31,6 +31,8 @@ struct Dims {
     int64_t max_sub;  // cap / rsub
     int n_it, n_hb, n_ht, n_ib;  // column tiles and 256-row boxes of gate/up and down
     int r = 0;        // rank of the low-rank gate/up term (0: none)
+    bool ttable = false;  // VQ gate/up through projected code books
+    int vqd = 0;          // VQ code-word length d
 };
 
 // One sub-block of the alignment (rsub consecutive aligned rows of one expert), as the
@@ -55,6 +57,7 @@ struct WsLayout {
     size_t z;        // float[M * 2r]  low-rank projections z = D^T h (gate, then up)
     size_t x_tiles;  // bf16[tile rows * H]  dense weights: token rows per tile row
     size_t p_tiles;  // bf16[tile rows * I]  dense weights: p per tile row
+    size_t tt_part;  // float[slices * M*k * 2 * I]  VQ through projected code books
     size_t total;
 };
 
@@ -129,6 +132,21 @@ cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
 constexpr int kReaderMaxCand = 16384;  // k * I candidate channels per token the selection holds
 constexpr int kReaderMaxRank = 32;
+// Blockwise VQ gate/up through projected code books (vq_ttable.cu), for at most
+// kTTMaxTokens tokens: per route the SiLU(g) * u rows p [M*k][I] fp32 the down kernel reads.
+constexpr int kTTMaxTokens = 4;
+struct VQTableArgs {
+    const __nv_bfloat16 *h;
+    const uint8_t *j_gate, *j_up;
+    const __nv_bfloat16 *cb_gate, *cb_up;
+    const int32_t *ids;
+    int M, k, E, H, I, d;
+    float *partial;  // [slices][M*k][2][I]
+    float *p;        // [M*k][I]
+};
+int vq_ttable_slices(int H, int d);
+cudaError_t launch_vq_ttable(const VQTableArgs &a, cudaStream_t stream);
+
 // The channel reader's data (see reader.cu for the layout) and one call's workspace.
 struct ReaderArgs {
     int H, I, E, rank;

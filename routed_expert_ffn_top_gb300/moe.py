@@ -61,6 +61,7 @@ class ExpertWeights(ctypes.Structure):
         ("d_gate", ctypes.c_void_p), ("d_up", ctypes.c_void_p),
         ("c_gate", ctypes.c_void_p), ("c_up", ctypes.c_void_p),
         ("r", ctypes.c_int32),
+        ("vq_form", ctypes.c_int32),
     ]
 
 
@@ -171,6 +172,7 @@ def expert_weights(layer: dict) -> ExpertWeights:
     w.kind = int(layer.get("kind", MOE_W_DENSE_BF16))
     w.H, w.I, w.E = int(layer["H"]), int(layer["I"]), int(layer["E"])
     w.d, w.K = int(layer.get("d", 0) or 0), int(layer.get("K", 0) or 0)
+    w.vq_form = int(layer.get("vq_form", 0) or 0)
     dev = layer["w_down"].device
     _need(layer["w_down"], torch.bfloat16, "w_down", dev)
     w.w_down = layer["w_down"].data_ptr()

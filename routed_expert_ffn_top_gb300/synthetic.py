@@ -54,6 +54,8 @@ class Workload:
     reader_K: int = 0
     reader_nscan: int = 80
     reader_rank: int = 32
+    # VQ gate/up form: 0 code books in shared memory, 1 projected code books (<= 4 tokens)
+    vq_form: int = 0
 
 
 # The five workloads: a single decode layer at one token, the same layer at 21 tokens (the
@@ -68,6 +70,8 @@ WORKLOADS = {
     "vqlr_d4_r256": Workload("vqlr_d4_r256", H=2048, I=768, E=128, k=8, b=8, M=1,
                              kind=W_VQLR, d=4, K=256, r=256),
     "vq_d8": Workload("vq_d8", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=8, K=256),
+    "vq_d4_tt": Workload("vq_d4_tt", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=4,
+                         K=256, vq_form=1),
     "vqlr_d8_r384": Workload("vqlr_d8_r384", H=2048, I=768, E=128, k=8, b=8, M=1,
                              kind=W_VQLR, d=8, K=256, r=384),
     "large_m256": Workload("large_m256", H=4096, I=1536, E=128, k=8, b=64, M=256,
@@ -110,7 +114,8 @@ def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu") -> dic
     """All parameters of one MoE layer as torch tensors on ``device``."""
     H, I, E = wl.H, wl.I, wl.E
     s = lambda t: sub_seed(seed, wl.name, layer, t)  # noqa: E731
-    p = {"kind": wl.kind, "H": H, "I": I, "E": E, "d": wl.d, "K": wl.K, "r": wl.r}
+    p = {"kind": wl.kind, "H": H, "I": I, "E": E, "d": wl.d, "K": wl.K, "r": wl.r,
+         "vq_form": wl.vq_form}
     p["w_router"] = _normal_bf16((H, E), wl.w_std, device, s("w_router"))
     if wl.router_bias:
         p["bias"] = torch.randn(E, generator=_gen(device, s("bias")), device=device,

@@ -182,3 +182,15 @@ def test_reader_validation_without_gpu(lib):
                             None, vp(1 << 20), None, None, ws, 16, None) == moe.MOE_ERR_WORKSPACE
     w = _weights()
     assert L.moe_reader_build(ctypes.byref(w), ctypes.byref(_reader(I=512)), None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_vq_form_validation_without_gpu(lib):
+    L = moe.lib()
+    w = _weights(kind=moe.MOE_W_VQ_GATEUP)
+    w.vq_form = 1
+    assert L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8) > 0
+    w.vq_form = 2
+    assert L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8) == 0
+    d = _weights()
+    d.vq_form = 1  # projected code books are a VQ form only
+    assert L.moe_workspace_bytes(ctypes.byref(d), 4, 8, 8) == 0

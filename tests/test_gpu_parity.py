@@ -318,6 +318,55 @@ def test_vq_expert_ffn_small(M, k, E, H, I, b, d):
     G.assert_close_block(G.to_f64(out), ref, "vq expert_ffn")
 
 
+VQ_TT = [
+    # M, k, E, H, I, b, d: projected code books (at most 4 tokens)
+    (1, 8, 16, 1024, 256, 8, 4), (3, 4, 16, 2048, 512, 1, 4), (4, 8, 8, 1024, 768, 8, 8),
+    (2, 2, 8, 3072, 256, 3, 8),
+]
+
+
+@pytest.mark.parametrize("M,k,E,H,I,b,d", VQ_TT)
+def test_vq_projected_codebooks_small(M, k, E, H, I, b, d):
+    wl = syn.Workload("vq_tt_%d_%d_%d_%d" % (M, k, E, d), H=H, I=I, E=E, k=k, b=b, M=M,
+                      kind=syn.W_VQ, d=d, K=256, vq_form=1)
+    layer = syn.make_layer(wl, seed=12, device=DEV)
+    h = syn.make_hidden(wl, seed=12, device=DEV)
+    rng = np.random.default_rng(M * 7 + E)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    res = syn.make_hidden(wl, seed=13, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, torch.as_tensor(ids, device=DEV),
+                             torch.as_tensor(a, device=DEV), b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = G.oracle_ffn(layer, h, ids, a, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "vq projected code books")
+
+
+def test_vq_projected_codebooks_block_and_invariance():
+    """The VQ layer with projected code books: parity at M = 1..4, a token's bits the same
+    alone and in a batch, within the bar of the shared-memory code-book form, and more
+    than 4 tokens refused."""
+    wl = syn.WORKLOADS["vq_d4_tt"]
+    layer = _workload_layer("vq_d4_tt")
+    h4 = syn.make_hidden(wl, M=4, seed=3, device=DEV)
+    out4, ids4, wts4 = moe.moe_decode_block(h4, layer, wl.k, wl.b)
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h4, wl.k)
+    use_ids, use_wts, _ = G.check_routing(ids4.cpu().numpy(), wts4.cpu().numpy(), o_ids, o_wts,
+                                          logits, wl.k)
+    G.assert_close_block(G.to_f64(out4), G.oracle_ffn(layer, h4, use_ids, use_wts), "tt M=4")
+    for M in (1, 2, 3):
+        o, i, _ = moe.moe_decode_block(h4[:M].contiguous(), layer, wl.k, wl.b)
+        assert torch.equal(i, ids4[:M]) and torch.equal(o, out4[:M]), M
+    smem_form = dict(layer, vq_form=0)
+    o_cb = moe.moe_expert_ffn(h4, smem_form, ids4, wts4, wl.b)
+    G.assert_close_block(G.to_f64(o_cb), G.to_f64(out4).astype(np.float64), "two VQ forms")
+    h5 = syn.make_hidden(wl, M=5, seed=3, device=DEV)
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_decode_block(h5, layer, wl.k, wl.b)
+    assert err.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
 def test_vq_block_every_m_1_to_16():
     """The blockwise-VQ workload: parity at every M from 1 to 16 (one weight set)."""
     wl = syn.WORKLOADS["vq_d4"]
