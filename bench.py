@@ -59,6 +59,9 @@ def parse_args():
                    help="override the alignment block size (64 selects the tcgen05 regime)")
     p.add_argument("--E", type=int, default=None,
                    help="override the expert count (smaller captures of the same kernels)")
+    p.add_argument("--vq-form", type=int, default=None, choices=[0, 1, 2],
+                   help="override the VQ gate/up form (VQ workloads): 0 code books in shared "
+                        "memory, 1 projected code books, 2 decoded on the tensor cores")
     p.add_argument("--weight-sets", type=int, default=8,
                    help="independent weight sets cycled by single-layer workloads")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -174,25 +177,31 @@ def overrides(args) -> dict:
         out["E"] = args.E
     if args.b:
         out["b"] = args.b
+    if args.vq_form is not None:
+        out["vq_form"] = args.vq_form
     return out
 
 
 def gemm_regime(wl) -> bool:
-    """Dense weights run as tcgen05 grouped GEMMs over tiles of the aligned blocks."""
-    return wl.kind == syn.W_DENSE
+    """Dense weights (and VQ gate/up decoded on the tensor cores) run as tcgen05 grouped
+    GEMMs over tiles of the aligned blocks."""
+    return wl.kind == syn.W_DENSE or (wl.kind == syn.W_VQ and wl.vq_form == 2)
 
 
 def library_block(wl) -> int:
     """The block size moe_decode_block aligns with: for dense weights 64 rows from 4 routes
-    per expert on average, else 16; VQ weights keep the workload's b."""
+    per expert on average, else 16; VQ weights decoded on the tensor cores 16; the other VQ
+    forms keep the workload's b."""
     if wl.kind == syn.W_DENSE:
         return 64 if wl.M * wl.k >= 4 * wl.E else 16
+    if gemm_regime(wl):
+        return 16
     return wl.b
 
 
 def gateup_kernel_name(wl) -> str:
     if gemm_regime(wl):
-        return "gemm_gateup_kernel"
+        return "gemm_gateup_vq_kernel" if wl.kind == syn.W_VQ else "gemm_gateup_kernel"
     return "vq_ttable_partial_kernel" if wl.vq_form == 1 else "gateup_vq_kernel"
 
 
@@ -396,6 +405,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": wl.name, "M": M, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "b": wl.b, "layers_per_step": blocks_per_step,
                    "weight_kind": "dense_bf16" if wl.kind == syn.W_DENSE else "vq_d%d" % wl.d,
+                   "vq_form": None if wl.kind == syn.W_DENSE else wl.vq_form,
                    "l2": ("inputs larger than L2: %d independent weight sets of %.2f GB cycled"
                           % (n_sets, wl.E * (gu_b + dn_b) / 1e9)),
                    "parallelism": "replicas" if world > 1 else "single"},

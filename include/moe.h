@@ -88,8 +88,11 @@ typedef enum moe_status {
  *     Dataflow ...", Section 2.3): per token and index row q the table
  *     T[q][kappa] = sum_t h[d q + t] B[kappa][t], so that g_i = sum_q T[q][J[e][q][i]] (one
  *     lookup per index instead of d products), for at most 4 tokens (M > 4:
- *     MOE_ERR_UNSUPPORTED).  The two forms add in different orders; each is bitwise
- *     reproducible and independent of M on its own.
+ *     MOE_ERR_UNSUPPORTED); 2 decodes the index maps through the code books into the
+ *     tensor cores' weight operand in shared memory and runs gate/up as the tcgen05 grouped
+ *     GEMM of dense weights, over 16-row tiles of the aligned blocks (any M; the library
+ *     aligns with b = 16 when it aligns itself).  The forms add in different orders; each is
+ *     bitwise reproducible and independent of M on its own.
  * Fields after w_down were added later; zero them when they do not apply.
  */
 typedef struct moe_expert_weights {

@@ -208,8 +208,8 @@ static int check_weights(const moe_expert_weights_t *w) {
     if (w->H % kBoxRows != 0 || w->H > 8192) return MOE_ERR_UNSUPPORTED;
     if (w->E < 8 || w->E > 512 || w->E % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (!w->w_down || !aligned(w->w_down, 16)) return MOE_ERR_INVALID_ARG;
-    if (w->vq_form != 0 && w->vq_form != 1) return MOE_ERR_INVALID_ARG;
-    if (w->vq_form == 1 && w->kind != MOE_W_VQ_GATEUP) return MOE_ERR_UNSUPPORTED;
+    if (w->vq_form < 0 || w->vq_form > 2) return MOE_ERR_INVALID_ARG;
+    if (w->vq_form != 0 && w->kind != MOE_W_VQ_GATEUP) return MOE_ERR_UNSUPPORTED;
     if (w->kind == MOE_W_DENSE_BF16) {
         if (!w->w_gate || !w->w_up || !aligned(w->w_gate, 16) || !aligned(w->w_up, 16))
             return MOE_ERR_INVALID_ARG;
@@ -244,6 +244,13 @@ static Dims dims_for(const moe_expert_weights_t *w, int M, int k, int b) {
     d.r = lr_rank(w);
     d.ttable = w->kind == MOE_W_VQ_GATEUP && w->vq_form == 1;
     d.vqd = w->d;
+    if (w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2) {
+        // 16-row tiles whatever b is (an aligned block is cut into ceil(b / 16) of them)
+        d.gemm = true;
+        d.vq_tc = true;
+        d.kn = kGemmNarrow;
+        d.tpb = (b + kGemmNarrow - 1) / kGemmNarrow;
+    }
     return d;
 }
 
@@ -303,11 +310,13 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
 // The block size the library aligns with when it aligns the routes itself.  Dense weights run
 // as tcgen05 tiles whatever b is, so the library picks the tile width: 64-row blocks from 4
 // routes per expert on average (the routes of an expert fill the MMA's N side), 16-row blocks
-// below that (an expert's weights stream once for up to 16 of its routes).  VQ weights keep
-// the caller's b.
+// below that (an expert's weights stream once for up to 16 of its routes).  VQ weights
+// decoded on the tensor cores run 16-row tiles only, so the library aligns with b = 16; the
+// other VQ forms keep the caller's b.
 static int effective_block(const moe_expert_weights_t *w, int M, int k, int b) {
     if (w && w->kind == MOE_W_DENSE_BF16)
         return (int64_t)M * k >= 4 * (int64_t)w->E ? kGemmBlock : kGemmNarrow;
+    if (w && w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2) return kGemmNarrow;
     return b;
 }
 
@@ -315,7 +324,8 @@ size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, i
     if (!w || M < 0 || k <= 0 || k > 32 || k > w->E || check_block(b) != MOE_OK) return 0;
     if (w->H <= 0 || w->I <= 0 || w->E <= 0) return 0;
     if ((int64_t)M * k >= (1 << 24)) return 0;
-    if (w->vq_form != 0 && (w->vq_form != 1 || w->kind != MOE_W_VQ_GATEUP)) return 0;
+    if (w->vq_form < 0 || w->vq_form > 2 || (w->vq_form != 0 && w->kind != MOE_W_VQ_GATEUP))
+        return 0;
     Dims d = dims_for(w, M, k, b);
     return ws_layout(d).total;
 }
@@ -342,8 +352,9 @@ static const LowRankProj *lowrank_proj(const moe_expert_weights_t *w, const Dims
     return out;
 }
 
-// Dense weights: the row gather (unless the router wrote the rows), tcgen05 grouped GEMMs
-// over the tiles of the aligned blocks, then the fixed-order combine.
+// Dense weights (or VQ gate/up decoded on the tensor cores): the row gather (unless the
+// router wrote the rows), tcgen05 grouped GEMMs over the tiles of the aligned blocks, then
+// the fixed-order combine.
 static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
                     const int32_t *topk_ids, const float *topk_weights, const int32_t *sorted,
                     const int32_t *blocks, const int32_t *npad, const void *residual, void *out,
@@ -351,10 +362,19 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     CUtensorMap tm_gate, tm_up, tm_down;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
     const int box_rows = kGemmStageK;  // K rows per weight box: one stage's depth
-    if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, 64, box_rows, sw) ||
-        !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
-                      (uint64_t)d.E * d.H, 64, box_rows, sw) ||
+    // VQ: the index maps [E * H/d rows][I] uint8, boxes of one stage's 256/d index rows x 64
+    // columns (unswizzled; the decoder warps write the swizzled A operand)
+    const bool maps_ok =
+        d.vq_tc
+            ? make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                           (uint64_t)d.E * (d.H / w->d), 64, box_rows / w->d) &&
+                  make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                               (uint64_t)d.E * (d.H / w->d), 64, box_rows / w->d)
+            : make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                           (uint64_t)d.E * d.H, 64, box_rows, sw) &&
+                  make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                               (uint64_t)d.E * d.H, 64, box_rows, sw);
+    if (!maps_ok ||
         !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
                       (uint64_t)d.E * d.I, 64, box_rows, sw))
         return MOE_ERR_CUDA;
@@ -377,12 +397,15 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     g.kn = d.kn;
     g.tpb = d.tpb;
     g.wait_first = rows_ready ? 1 : 0;
+    g.cb_gate = d.vq_tc ? static_cast<const __nv_bfloat16 *>(w->cb_gate) : nullptr;
+    g.cb_up = d.vq_tc ? static_cast<const __nv_bfloat16 *>(w->cb_up) : nullptr;
     g.R = d.R;
     g.cap = d.cap;
     cudaError_t err = rows_ready ? cudaSuccess : launch_gather_rows(g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (!rows_ready) trace(2, stream);  // the row gather counts with the alignment
-    err = launch_gemm_gateup(tm_gate, tm_up, g, stream);
+    err = d.vq_tc ? launch_gemm_gateup_vq(tm_gate, tm_up, g, w->d, stream)
+                  : launch_gemm_gateup(tm_gate, tm_up, g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace(3, stream);
     err = launch_gemm_down(tm_down, g, stream);

@@ -48,8 +48,7 @@ namespace moe {
 
 constexpr int kGM = 128;                             // output channels per MMA
 constexpr int kGThreads = 192;                       // 6 warps
-constexpr int kGEpiWarp0 = 2;
-constexpr int kGMaxStages = 3;
+constexpr int kGMaxStages = 8;
 
 // The shapes of one tile width kN (the MMA's N: 16 or 64 aligned rows).  A stage is the two
 // 32 KB weight boxes (64 columns x 256 rows of K, one per 64-wide M half) and the tile's
@@ -66,11 +65,54 @@ struct GTile {
     static constexpr int kStages = kN == 16 ? 3 : 2;
     static constexpr int kChunkBytes = kN * 64 * 2;         // one 64-wide K chunk: 2 or 8 KB
     static constexpr uint32_t kTmemCols = 2 * kN < 32 ? 32 : 2 * kN;  // two accumulators
+    static constexpr int kBOff = kABytes;                   // the row slice after the weights
+    static constexpr int kTxBytes = kStageBytes;            // bytes the stage's copies bring
+    static constexpr int kTileN = kN;
+    static constexpr int kDefer = kStages;  // row-slice copies held back until griddepcontrol
+    static constexpr bool kSplitB = false;  // one barrier for the weights and the row slice
+};
+
+// The VQ gate/up kernel (16-row tiles, code words of kD).  Its copy ring holds, per 256-deep
+// stage, the gate and up index boxes (256 / kD index rows x 64 columns of uint8 each, by TMA)
+// and the tile's row slice (behind a barrier of its own, so that decoding starts as soon as
+// the index boxes land); eight stages in flight.  The weight operand is decoded into
+// tensor memory instead: slots of 128 K rows (64 columns), three in flight, after the two
+// accumulators.  The code books sit in shared memory with each entry repeated kReps times
+// across the banks, so that the lanes of one wavefront, each reading its own repeat, never
+// share a bank.
+template <int kD>
+struct GTileVQ {
+    static_assert(kD == 4 || kD == 8, "code words of 4 or 8");
+    static constexpr int kK = kGemmStageK;
+    static constexpr int kJRows = kK / kD;
+    static constexpr int kJBytes = kJRows * 64;             // one projection's index box
+    static constexpr int kBOff = 2 * kJBytes;
+    static constexpr int kBBytes = 16 * kK * 2;
+    static constexpr int kStageBytes = kBOff + kBBytes;     // 16 KB (d = 4), 12 KB (d = 8)
+    static constexpr int kTxBytes = kStageBytes;
+    static constexpr int kStages = 8;
+    static constexpr int kChunkBytes = 16 * 64 * 2;
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr int kTileN = 16;
+    static constexpr int kDefer = 2;
+    static constexpr bool kSplitB = true;  // decoders wait for the index boxes only
+    static constexpr int kDecWarps = 8;    // two per TMEM lane quadrant, half a slot's K each
+    static constexpr int kSlotK = 128;                      // K rows per tensor-memory slot
+    static constexpr int kSlots = 3;
+    static constexpr uint32_t kSlotCol0 = 64;               // columns 0-31: the accumulators
+    static constexpr int kReps = kD == 4 ? 16 : 8;          // 8-byte words: 16 lanes a wavefront
+    static constexpr int kEntryBytes = kReps * kD * 2;      // 128
+    static constexpr int kCbBytes = 256 * kEntryBytes;      // one projection's code book
+    static_assert(kStageBytes % 1024 == 0 && kBOff % 1024 == 0, "stage alignment");
+    static_assert(kSlotCol0 + kSlots * 64 <= kTmemCols, "tensor memory");
 };
 
 struct GCtl {
     uint64_t full[kGMaxStages];
     uint64_t empty[kGMaxStages];
+    uint64_t bfull[kGMaxStages];  // VQ: the stage's row slice has landed
+    uint64_t afull[3];   // VQ: a tensor-memory slot of the weight operand is written
+    uint64_t aempty[3];  // VQ: the MMAs reading a slot have completed
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t done;
@@ -92,9 +134,9 @@ __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, GCtl &ctl)
     }
 }
 
-template <int kN>
+template <typename L>
 __device__ __forceinline__ void gadvance(int &stage, uint32_t &phase) {
-    if (++stage == GTile<kN>::kStages) {
+    if (++stage == L::kStages) {
         stage = 0;
         phase ^= 1u;
     }
@@ -184,11 +226,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmArgs a) {
 // copies wait for it (griddepcontrol) while their weight copies are already in flight.
 // already_waited: the kernel waited for the previous grid before this point (the gate/up
 // kernel when the router wrote the alignment and the x tiles).
-template <int kN, typename IssueA>
+template <typename G, typename IssueA>
 __device__ void gemm_producer(const GemmArgs &a, GCtl &ctl, unsigned char *stages,
                               const unsigned char *btiles, int64_t T, int n_ct, int nks,
                               bool already_waited, int e_first, IssueA issue_a) {
-    using G = GTile<kN>;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, parity_bits = 0;
@@ -208,45 +249,53 @@ __device__ void gemm_producer(const GemmArgs &a, GCtl &ctl, unsigned char *stage
             if (!gwait(&ctl.empty[stage], phase ^ 1u, ctl)) break;
             uint64_t *bar = &ctl.full[stage];
             unsigned char *st = stages + stage * G::kStageBytes;
-            mbar_arrive_expect_tx(bar, G::kStageBytes);
+            if (G::kSplitB) {
+                mbar_arrive_expect_tx(bar, G::kTxBytes - G::kBBytes);
+                mbar_arrive_expect_tx(&ctl.bfull[stage], G::kBBytes);
+            } else {
+                mbar_arrive_expect_tx(bar, G::kTxBytes);
+            }
             issue_a(st, bar, e, ct, s);
             const unsigned char *src = btiles + (tile * nks + s) * (int64_t)G::kBBytes;
             if (waited) {
-                bulk_load(st + G::kABytes, src, G::kBBytes, bar);
+                bulk_load(st + G::kBOff, src, G::kBBytes, G::kSplitB ? &ctl.bfull[stage] : bar);
             } else {
                 pend_src[npend] = src;
                 pend_stage[npend] = stage;
-                if (++npend == G::kStages) {
+                if (++npend == G::kDefer) {
                     pdl_wait();
                     waited = true;
                     for (int q = 0; q < npend; ++q)
-                        bulk_load(stages + pend_stage[q] * G::kStageBytes + G::kABytes, pend_src[q],
-                                  G::kBBytes, &ctl.full[pend_stage[q]]);
+                        bulk_load(stages + pend_stage[q] * G::kStageBytes + G::kBOff, pend_src[q],
+                                  G::kBBytes, G::kSplitB ? &ctl.bfull[pend_stage[q]] : &ctl.full[pend_stage[q]]);
                     npend = 0;
                 }
             }
             issued |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
-            gadvance<kN>(stage, phase);
+            gadvance<G>(stage, phase);
         }
     }
     if (!waited) {
         pdl_wait();
         for (int q = 0; q < npend; ++q)
-            bulk_load(stages + pend_stage[q] * G::kStageBytes + G::kABytes, pend_src[q], G::kBBytes,
-                      &ctl.full[pend_stage[q]]);
+            bulk_load(stages + pend_stage[q] * G::kStageBytes + G::kBOff, pend_src[q], G::kBBytes,
+                      G::kSplitB ? &ctl.bfull[pend_stage[q]] : &ctl.full[pend_stage[q]]);
     }
     // every copy has landed before the CTA can exit
     for (int s = 0; s < G::kStages; ++s)
-        if ((issued >> s) & 1u)
+        if ((issued >> s) & 1u) {
             if (!mbar_wait_bounded(&ctl.full[s], (parity_bits >> s) & 1u)) ctl.abort = 1;
+            if (G::kSplitB && !mbar_wait_bounded(&ctl.bfull[s], (parity_bits >> s) & 1u))
+                ctl.abort = 1;
+        }
 }
 
 // MMA issuer (one thread): for each unit, nks stages x 16 MMAs of K = 16 into accumulator
 // buffer (unit parity); each stage is released when its MMAs complete.
-template <int kN>
+template <typename G>
 __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
-    using G = GTile<kN>;
+    constexpr int kN = G::kTileN;
     constexpr uint32_t idesc = umma_idesc_bf16(kGM, kN, true, false);
     int stage = 0;
     uint32_t phase = 0;
@@ -265,7 +314,7 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
             }
             tc_fence_after();
             const uint32_t A = smem_u32(stages + stage * G::kStageBytes);
-            const uint32_t B = A + G::kABytes;
+            const uint32_t B = A + G::kBOff;
 #pragma unroll
             for (int ks = 0; ks < G::kK / 16; ++ks) {
                 // A: MN-major, M halves 32 KB apart, 8-row K atoms 1 KB apart, 16 K rows per MMA
@@ -277,7 +326,7 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
                 umma_bf16(d, ad, bd, idesc, s > 0 || ks > 0);
             }
             umma_commit(&ctl.empty[stage]);
-            gadvance<kN>(stage, phase);
+            gadvance<G>(stage, phase);
         }
         if (!ok) break;
         umma_commit(&ctl.tfull[buf]);
@@ -287,13 +336,20 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
     if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
 }
 
-template <int kN>
-__device__ __forceinline__ void gemm_init(GCtl &ctl, int warp) {
+// decoder_warps (VQ): warps that also read each stage (its index boxes) before it is free,
+// and fill the tensor-memory slots of the weight operand.
+template <typename G>
+__device__ __forceinline__ void gemm_init(GCtl &ctl, int warp, int decoder_warps = 0) {
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GTile<kN>::kStages; ++s) {
-            mbar_init(&ctl.full[s], 1);   // the producer's expect_tx arrival
-            mbar_init(&ctl.empty[s], 1);  // MMA completion
+        for (int s = 0; s < G::kStages; ++s) {
+            mbar_init(&ctl.full[s], 1);                   // the producer's expect_tx arrival
+            mbar_init(&ctl.empty[s], 1 + decoder_warps);  // MMA completion (+ decoders)
         }
+        for (int s = 0; s < 3 && decoder_warps; ++s) {
+            mbar_init(&ctl.afull[s], decoder_warps);
+            mbar_init(&ctl.aempty[s], 1);
+        }
+        for (int s = 0; s < G::kStages && G::kSplitB; ++s) mbar_init(&ctl.bfull[s], 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl.tfull[b], 1);
             mbar_init(&ctl.tempty[b], 4);  // the 4 epilogue warps
@@ -302,18 +358,18 @@ __device__ __forceinline__ void gemm_init(GCtl &ctl, int warp) {
         ctl.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&ctl.tmem, GTile<kN>::kTmemCols);
+    if (warp == 1) tmem_alloc(&ctl.tmem, G::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 }
 
-template <int kN>
+template <typename G>
 __device__ __forceinline__ void gemm_finish(GCtl &ctl, int warp, int32_t *status) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(ctl.tmem, GTile<kN>::kTmemCols);
+    if (warp == 1) tmem_dealloc(ctl.tmem, G::kTmemCols);
     if (threadIdx.x == 0 && ctl.abort) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
 }
 
@@ -351,7 +407,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
     }
-    gemm_init<kN>(ctl, warp);
+    gemm_init<G>(ctl, warp);
     // When the router wrote the alignment and the x tiles, this grid may start while it
     // still runs: wait for it before anything reads them, and only then let the down grid
     // start (it reads the block vector before its own wait).
@@ -366,7 +422,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            gemm_producer<kN>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles),
+            gemm_producer<G>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles),
                               T, n_ct, nks, a.wait_first != 0, e_first,
                               [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
                 const int32_t y = e * a.H + s * G::kK;
@@ -376,7 +432,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) gemm_mma<kN>(ctl, stages, T, nks);
+        if (lane == 0) gemm_mma<G>(ctl, stages, T, nks);
         __syncwarp();
     } else {
         const int quad = warp & 3;           // TMEM lanes [32 quad, 32 quad + 32)
@@ -414,7 +470,258 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         }
     }
-    gemm_finish<kN>(ctl, warp, a.status);
+    gemm_finish<G>(ctl, warp, a.status);
+}
+
+// ---------------------------------------------------------------------- VQ gate/up
+// Blockwise-VQ gate/up on the tensor cores (16-row tiles).  The weight operand never exists
+// in memory: four decoder warps, one TMEM lane quadrant each (lane = output channel: gate
+// channels in lanes 0-63, up in 64-127), read their channel's index of every index row q of a
+// 128-row K slot from the stage's index box, fetch its code word B[J[q][i]] (kD consecutive K
+// values of row i of the weight) from their own repeat of the code book, and write the words
+// to the slot's columns with tcgen05.st; two warps share a quadrant, each with half of the
+// slot's K, so that one's loads overlap the other's stores.  The MMA issuer takes A from
+// tensor memory and the row slice from the stage.  The chain per element is the dense
+// kernel's (K-ordered, one MMA per 16 K rows); epilogue and p tiles are the dense kernel's.
+// 14 warps: producer, MMA, 4 epilogue, 8 decoders.
+constexpr int kGVQThreads = 448;
+constexpr int kGDecWarp0 = 6;
+
+// Every lane waits; the warp goes on only if all of them got the phase (so that the
+// warp-wide tensor-memory instructions after it are never split).
+__device__ __forceinline__ bool gwait_warp(uint64_t *bar, uint32_t parity, GCtl &ctl) {
+    return __all_sync(0xffffffffu, gwait(bar, parity, ctl));
+}
+
+template <int kD>
+__device__ void gemm_mma_vq(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
+    using G = GTileVQ<kD>;
+    constexpr int kN = 16;
+    constexpr uint32_t idesc = umma_idesc_bf16(kGM, kN, false, false);
+    constexpr int kStepsPerSlot = G::kSlotK / 16;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
+    int local = 0;
+    for (int64_t u = blockIdx.x; u < T && !ctl.abort; u += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t tph = (uint32_t)(local >> 1) & 1u;
+        if (!gwait(&ctl.tempty[buf], tph ^ 1u, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = ctl.tmem + (uint32_t)(buf * kN);
+        bool ok = true;
+        for (int s = 0; s < nks && ok; ++s) {
+            if (!gwait(&ctl.bfull[stage], phase, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t B = smem_u32(stages + stage * G::kStageBytes) + G::kBOff;
+            for (int h = 0; h < G::kK / G::kSlotK; ++h) {
+                if (!gwait(&ctl.afull[slot], sphase, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t A = ctl.tmem + G::kSlotCol0 + (uint32_t)(slot * 64);
+#pragma unroll
+                for (int kk = 0; kk < kStepsPerSlot; ++kk) {
+                    const int ks = h * kStepsPerSlot + kk;  // K = 16 step within the stage
+                    const uint64_t bd =
+                        umma_smem_desc(B + (ks >> 2) * G::kChunkBytes + (ks & 3) * 32, 16, 1024, 2);
+                    umma_bf16_ts(d, A + (uint32_t)(kk * 8), bd, idesc, s > 0 || ks > 0);
+                }
+                umma_commit(&ctl.aempty[slot]);
+                if (++slot == G::kSlots) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(&ctl.empty[stage]);
+            gadvance<G>(stage, phase);
+        }
+        if (!ok) break;
+        umma_commit(&ctl.tfull[buf]);
+    }
+    umma_commit(&ctl.done);
+    if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
+}
+
+// Decoder warp (TMEM lane quadrant `quad`, half `part` of each slot's K): the weight operand
+// of every stage, slot by slot, software-pipelined -- the tensor-memory stores of slot k run
+// while the indices and code words of slot k+1 are fetched; then slot k is signalled.
+template <int kD>
+struct VQDecoder {
+    using G = GTileVQ<kD>;
+    static constexpr int kRows = G::kSlotK / kD / 2;  // index rows q per warp and slot: 16 or 8
+    GCtl &ctl;
+    const unsigned char *jbase;  // this warp's index column in stage 0 (part's rows)
+    const unsigned char *cb;     // this lane's repeat of its projection's code book
+    uint32_t taddr;              // this warp's lanes and columns in slot 0
+
+    // Slot task k (stage k / 2 of the CTA's sequence, half k % 2 of its K): waits for the
+    // stage's index boxes (first half) and for the slot to be free, then gathers the code
+    // words of the warp's rows into r; after the second half the stage's boxes are released.
+    __device__ __forceinline__ bool fetch(int64_t k, uint32_t (&r)[32]) {
+        const int64_t gs = k >> 1;
+        const int h = (int)(k & 1);
+        const int stage = (int)(gs % G::kStages);
+        if (h == 0 && !gwait_warp(&ctl.full[stage], (uint32_t)(gs / G::kStages) & 1u, ctl)) return false;
+        if (!gwait_warp(&ctl.aempty[k % G::kSlots], ((uint32_t)(k / G::kSlots) & 1u) ^ 1u, ctl))
+            return false;
+        tc_fence_after();
+        const unsigned char *jb = jbase + stage * G::kStageBytes + h * 2 * kRows * 64;
+        uint32_t idx[kRows];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) idx[q] = jb[q * 64];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            if constexpr (kD == 4) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(cb + idx[q] * G::kEntryBytes);
+                r[2 * q] = w.x;
+                r[2 * q + 1] = w.y;
+            } else {
+                const uint4 w = *reinterpret_cast<const uint4 *>(cb + idx[q] * G::kEntryBytes);
+                r[4 * q] = w.x;
+                r[4 * q + 1] = w.y;
+                r[4 * q + 2] = w.z;
+                r[4 * q + 3] = w.w;
+            }
+        }
+        if (h == 1) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.empty[stage]);  // its index boxes are read
+        }
+        return true;
+    }
+};
+
+template <int kD>
+__device__ void vq_decode(GCtl &ctl, const unsigned char *stages, const unsigned char *cbs,
+                          int64_t T, int nks, int quad, int part, int lane) {
+    using G = GTileVQ<kD>;
+    using Dec = VQDecoder<kD>;
+    const int p = quad >> 1;                      // 0: gate, 1: up
+    const int ch = 32 * (quad & 1) + lane;        // channel within the 64-column tile
+    Dec dec{ctl, stages + p * G::kJBytes + part * Dec::kRows * 64 + ch,
+            cbs + p * G::kCbBytes + (lane % G::kReps) * (kD * 2),
+            ctl.tmem + ((uint32_t)(32 * quad) << 16) + G::kSlotCol0 + (uint32_t)(32 * part)};
+    const int64_t units = T > blockIdx.x ? (T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t K = units * nks * 2;  // slot tasks of this CTA
+    // two register sets, swapped by unrolling by two (never indexed at run time)
+    uint32_t r0[32], r1[32];
+    auto step = [&](int64_t k, const uint32_t(&cur)[32], uint32_t(&next)[32]) {
+        const uint32_t ta = dec.taddr + (uint32_t)((k % G::kSlots) * 64);
+        tmem_st16(ta, cur);
+        tmem_st16(ta + 16, cur + 16);
+        const bool more = k + 1 < K && dec.fetch(k + 1, next);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.afull[k % G::kSlots]);
+        return more;
+    };
+    if (K == 0 || !dec.fetch(0, r0)) return;
+    for (int64_t k = 0; k < K; k += 2)
+        if (!step(k, r0, r1) || !step(k + 1, r1, r0)) return;
+}
+
+template <int kD>
+__global__ void __launch_bounds__(kGVQThreads, 1)
+    gemm_gateup_vq_kernel(const __grid_constant__ CUtensorMap tm_jgate,
+                          const __grid_constant__ CUtensorMap tm_jup, const GemmArgs a) {
+    using G = GTileVQ<kD>;
+    constexpr int kN = 16;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *stages = base;
+    unsigned char *cbs = base + G::kStages * G::kStageBytes;  // gate then up code book
+    float *gbuf = reinterpret_cast<float *>(cbs + 2 * G::kCbBytes);  // [16][64]
+    GCtl &ctl = *reinterpret_cast<GCtl *>(reinterpret_cast<unsigned char *>(gbuf) + kN * 64 * 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_jgate);
+        prefetch_tensormap(&tm_jup);
+    }
+    // the layer-shared code books (weights, not written by an earlier grid), each entry
+    // repeated across one 128-byte row of banks
+    constexpr int kPieces = 2 * G::kCbBytes / 16;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kPieces; i += blockDim.x) {
+        const int p = i / (kPieces / 2);
+        const int kappa = (i % (kPieces / 2)) / (G::kEntryBytes / 16);
+        const int piece = i % (G::kEntryBytes / 16);
+        const __nv_bfloat16 *src = (p ? a.cb_up : a.cb_gate) + kappa * kD;
+        uint4 v;
+        if constexpr (kD == 4) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(src);
+            v = make_uint4(w.x, w.y, w.x, w.y);
+        } else {
+            v = *reinterpret_cast<const uint4 *>(src);
+        }
+        *reinterpret_cast<uint4 *>(cbs + p * G::kCbBytes + kappa * G::kEntryBytes + piece * 16) = v;
+    }
+    gemm_init<G>(ctl, warp, G::kDecWarps);
+    if (a.wait_first) pdl_wait();
+    pdl_launch_dependents();
+
+    const int n_ct = a.I / 64;
+    const int nks = a.H / G::kK;
+    const int nrows = a.H / kD;
+    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
+    const int64_t T = gemm_blocks(a) * a.tpb * n_ct;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            gemm_producer<G>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles),
+                             T, n_ct, nks, a.wait_first != 0, e_first,
+                             [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
+                const int32_t y = e * nrows + s * G::kJRows;
+                tma_load_2d(st, &tm_jgate, ct * 64, y, bar, pol);
+                tma_load_2d(st + G::kJBytes, &tm_jup, ct * 64, y, bar, pol);
+            });
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) gemm_mma_vq<kD>(ctl, stages, T, nks);
+        __syncwarp();
+    } else if (warp >= kGDecWarp0) {
+        vq_decode<kD>(ctl, stages, cbs, T, nks, warp & 3, (warp - kGDecWarp0) >> 2, lane);
+    } else {
+        const int quad = warp & 3;
+        const int row = 32 * quad + lane;
+        int local = 0;
+        for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
+            const int64_t tile = u / n_ct;
+            const int ct = (int)(u % n_ct);
+            const int buf = local & 1;
+            if (row < kN) ctl.route[buf][row] = tile_route(a, tile, row, a.blocks[tile / a.tpb], false);
+            const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
+            if (named_bar_or(1, 128, !ok)) break;
+            float v[kN];
+            drain_accumulator<kN>(ctl, quad, buf, v);
+            if (quad < 2) {
+#pragma unroll
+                for (int n = 0; n < kN; ++n)
+                    if (ctl.route[buf][n] >= 0) gbuf[n * 64 + row] = v[n];
+            }
+            named_bar_sync(1, 128);
+            if (quad >= 2) {
+                const int ch = row - 64;
+                unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
+                                     (tile * n_ct + ct) * (int64_t)G::kChunkBytes + (ch & 7) * 2;
+#pragma unroll
+                for (int n = 0; n < kN; ++n) {
+                    if (ctl.route[buf][n] < 0) continue;
+                    const float p = silu_f32(gbuf[n * 64 + ch]) * v[n];
+                    *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, ch >> 3)) = __float2bfloat16(p);
+                }
+            }
+        }
+    }
+    gemm_finish<G>(ctl, warp, a.status);
 }
 
 // ------------------------------------------------------------------------------- down
@@ -429,7 +736,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     GCtl &ctl = *reinterpret_cast<GCtl *>(base + G::kStages * G::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) prefetch_tensormap(&tm_down);
-    gemm_init<kN>(ctl, warp);
+    gemm_init<G>(ctl, warp);
     pdl_launch_dependents();
 
     const int n_ct = a.H / kGM;
@@ -441,7 +748,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             // p tiles come from the gate/up grid: always deferred to this kernel's own wait
-            gemm_producer<kN>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.p_tiles),
+            gemm_producer<G>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.p_tiles),
                               T, n_ct, nks, false, e_first,
                               [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
                 const int32_t y = e * a.I + s * G::kK;
@@ -451,7 +758,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) gemm_mma<kN>(ctl, stages, T, nks);
+        if (lane == 0) gemm_mma<G>(ctl, stages, T, nks);
         __syncwarp();
     } else {
         const int quad = warp & 3;
@@ -474,7 +781,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         }
     }
-    gemm_finish<kN>(ctl, warp, a.status);
+    gemm_finish<G>(ctl, warp, a.status);
 }
 
 // ------------------------------------------------------------------ bounded-wait self-test
@@ -486,10 +793,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
 __global__ void __launch_bounds__(kGThreads, 1) wait_selftest_kernel(int32_t *status) {
     __shared__ GCtl ctl;
     const int warp = threadIdx.x >> 5;
-    gemm_init<kGemmBlock>(ctl, warp);
+    gemm_init<GTile<kGemmBlock>>(ctl, warp);
     if ((threadIdx.x & 31) == 0) gwait(&ctl.tfull[0], 0, ctl);
     __syncwarp();
-    gemm_finish<kGemmBlock>(ctl, warp, status);
+    gemm_finish<GTile<kGemmBlock>>(ctl, warp, status);
 }
 
 template <int kN>
@@ -539,6 +846,24 @@ cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm
     if (a.kn == 16) return launch_gateup_tiles<16>(tm_gate, tm_up, a, stream);
     if (a.kn == 64) return launch_gateup_tiles<64>(tm_gate, tm_up, a, stream);
     return cudaErrorInvalidValue;
+}
+
+template <int kD>
+static size_t gemm_gateup_vq_smem() {
+    using G = GTileVQ<kD>;
+    return 1024 + G::kStages * G::kStageBytes + 2 * G::kCbBytes + 16 * 64 * 4 + sizeof(GCtl);
+}
+
+cudaError_t launch_gemm_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                                  const GemmArgs &a, int d, cudaStream_t stream) {
+    if (a.kn != 16 || (d != 4 && d != 8)) return cudaErrorInvalidValue;
+    const size_t smem = d == 4 ? gemm_gateup_vq_smem<4>() : gemm_gateup_vq_smem<8>();
+    auto kern = d == 4 ? gemm_gateup_vq_kernel<4> : gemm_gateup_vq_kernel<8>;
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(kern), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGVQThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, kern, tm_jgate, tm_jup, a);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream) {

@@ -23,7 +23,8 @@ constexpr int kRouterThreads = 512;
 
 struct Dims {
     int M, k, E, H, I, b;
-    bool gemm;        // dense weights: every projection runs as tcgen05 tiles of kn rows
+    bool gemm;        // every projection runs as tcgen05 tiles of kn rows (dense weights,
+                      // or VQ gate/up decoded on the tensor-core path)
     int kn, tpb;      // tile width (16 or 64 aligned rows) and tiles per aligned block
     int rsub;         // rows per sub-block: b if b <= 8, else 8
     int64_t R;        // routes M*k (also the sentinel value)
@@ -33,6 +34,7 @@ struct Dims {
     int r = 0;        // rank of the low-rank gate/up term (0: none)
     bool ttable = false;  // VQ gate/up through projected code books
     int vqd = 0;          // VQ code-word length d
+    bool vq_tc = false;   // VQ gate/up on the tensor cores (16-row tiles)
 };
 
 // One sub-block of the alignment (rsub consecutive aligned rows of one expert), as the
@@ -123,6 +125,7 @@ struct GemmArgs {
     int M, k, E, H, I;
     int b, kn, tpb;           // aligned block rows, tile width, tiles per block
     int wait_first;           // the previous kernel wrote the x tiles (and the alignment)
+    const __nv_bfloat16 *cb_gate, *cb_up;  // VQ on the tensor cores: the code books
     int64_t R, cap;
 };
 
@@ -130,6 +133,10 @@ cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
                                const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
+// Blockwise-VQ gate/up on the tensor cores (16-row tiles, d = 4 or 8): index maps by TMA,
+// decoded through the code books into the MMA's A operand.
+cudaError_t launch_gemm_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                                  const GemmArgs &a, int d, cudaStream_t stream);
 constexpr int kReaderMaxCand = 16384;  // k * I candidate channels per token the selection holds
 constexpr int kReaderMaxRank = 32;
 // Blockwise VQ gate/up through projected code books (vq_ttable.cu), for at most

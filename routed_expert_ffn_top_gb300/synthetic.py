@@ -54,7 +54,8 @@ class Workload:
     reader_K: int = 0
     reader_nscan: int = 80
     reader_rank: int = 32
-    # VQ gate/up form: 0 code books in shared memory, 1 projected code books (<= 4 tokens)
+    # VQ gate/up form: 0 code books in shared memory, 1 projected code books (<= 4 tokens),
+    # 2 decoded into the tensor cores' weight operand (16-row tcgen05 tiles)
     vq_form: int = 0
 
 
@@ -72,6 +73,8 @@ WORKLOADS = {
     "vq_d8": Workload("vq_d8", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=8, K=256),
     "vq_d4_tt": Workload("vq_d4_tt", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=4,
                          K=256, vq_form=1),
+    "vq_d4_tc": Workload("vq_d4_tc", H=2048, I=768, E=128, k=8, b=8, M=1, kind=W_VQ, d=4,
+                         K=256, vq_form=2),
     "vqlr_d8_r384": Workload("vqlr_d8_r384", H=2048, I=768, E=128, k=8, b=8, M=1,
                              kind=W_VQLR, d=8, K=256, r=384),
     "large_m256": Workload("large_m256", H=4096, I=1536, E=128, k=8, b=64, M=256,

@@ -189,8 +189,21 @@ def test_vq_form_validation_without_gpu(lib):
     w = _weights(kind=moe.MOE_W_VQ_GATEUP)
     w.vq_form = 1
     assert L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8) > 0
-    w.vq_form = 2
+    w.vq_form = 3
     assert L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8) == 0
+    w.vq_form = -1
+    assert L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8) == 0
+    # the tensor-core form holds 16-row tiles: x and p tiles but no fp32 p or sub-blocks
+    w.vq_form = 0
+    smem_form = L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8)
+    w.vq_form = 2
+    tc_form = L.moe_workspace_bytes(ctypes.byref(w), 4, 8, 8)
+    assert tc_form > 0 and tc_form != smem_form
+    assert L.moe_workspace_bytes(ctypes.byref(w), 300, 8, 64) > 0  # any M
     d = _weights()
-    d.vq_form = 1  # projected code books are a VQ form only
-    assert L.moe_workspace_bytes(ctypes.byref(d), 4, 8, 8) == 0
+    for form in (1, 2):  # projected code books and tensor-core decoding are VQ forms only
+        d.vq_form = form
+        assert L.moe_workspace_bytes(ctypes.byref(d), 4, 8, 8) == 0
+    lr = _weights(kind=moe.MOE_W_VQLR_GATEUP)
+    lr.vq_form = 2
+    assert L.moe_workspace_bytes(ctypes.byref(lr), 4, 8, 8) == 0

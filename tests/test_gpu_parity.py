@@ -388,6 +388,70 @@ def test_vq_block_every_m_1_to_16():
     assert torch.equal(o1[0], out[3])
 
 
+VQ_TC = [
+    # M, k, E, H, I, b, d: index maps decoded into the tensor cores' weight operand
+    (5, 2, 8, 1024, 256, 3, 4), (13, 4, 16, 2048, 512, 8, 4), (2, 8, 8, 1024, 768, 1, 4),
+    (30, 3, 24, 1024, 256, 16, 4), (40, 4, 8, 1024, 256, 24, 4), (5, 2, 8, 1024, 256, 3, 8),
+    (13, 4, 16, 2048, 512, 8, 8), (30, 3, 24, 3072, 256, 16, 8), (64, 8, 16, 1024, 512, 64, 8),
+]
+
+
+@pytest.mark.parametrize("M,k,E,H,I,b,d", VQ_TC)
+def test_vq_tensor_core_small(M, k, E, H, I, b, d):
+    """VQ gate/up on the tcgen05 path: parity with the oracle through the library's
+    alignment and the caller's (b = 1 .. 64, so 1 to 4 sixteen-row tiles per block), the same
+    bits both ways, within the bar of the shared-memory code-book form."""
+    wl = syn.Workload("vq_tc_%d_%d_%d_%d" % (M, k, E, d), H=H, I=I, E=E, k=k, b=b, M=M,
+                      kind=syn.W_VQ, d=d, K=256, vq_form=2)
+    layer = syn.make_layer(wl, seed=14, device=DEV)
+    h = syn.make_hidden(wl, seed=14, device=DEV)
+    rng = np.random.default_rng(M * 3 + E + d)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
+    res = syn.make_hidden(wl, seed=15, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = G.oracle_ffn(layer, h, ids, a, residual=res)
+    G.assert_close_block(G.to_f64(out), ref, "vq tensor cores")
+    srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
+    o = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad), residual=res)
+    assert torch.equal(o, out)
+    o_cb = moe.moe_expert_ffn(h, dict(layer, vq_form=0), t_ids, t_a, b, residual=res)
+    G.assert_close_block(G.to_f64(o_cb), G.to_f64(out).astype(np.float64), "two VQ forms")
+
+
+def test_vq_tensor_core_block_every_m_and_invariance():
+    """The VQ decode layer on the tcgen05 path: parity at M = 1..16 (the router writes the
+    row tiles up to 8 tokens, the row gather does above), each token's bits the same alone,
+    in any batch and in a dirty workspace."""
+    wl = syn.WORKLOADS["vq_d4_tc"]
+    layer = _workload_layer("vq_d4_tc")
+    h16 = syn.make_hidden(wl, M=16, seed=9, device=DEV)
+    out16, ids16, _ = moe.moe_decode_block(h16, layer, wl.k, wl.b)
+    for M in range(1, 17):
+        h = h16[:M].contiguous()
+        ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
+        if M in (1, 7, 12):
+            ws.fill_(0xFF)
+            ws[:64] = 0
+        out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
+        assert moe.moe_read_device_status(ws) == 0
+        assert torch.equal(ids, ids16[:M]) and torch.equal(out, out16[:M]), M
+        if M in (1, 2, 5, 8, 9, 16):
+            o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+            use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids,
+                                                  o_wts, logits, wl.k)
+            G.assert_close_block(G.to_f64(out), G.oracle_ffn(layer, h, use_ids, use_wts),
+                                 "vq_d4_tc M=%d" % M)
+    for t in (0, 5, 15):
+        o1, _, _ = moe.moe_decode_block(h16[t:t + 1].contiguous(), layer, wl.k, wl.b)
+        assert torch.equal(o1[0], out16[t]), t
+    runs = [moe.moe_decode_block(h16, layer, wl.k, wl.b)[0] for _ in range(5)]
+    assert all(torch.equal(r, out16) for r in runs)
+
+
 VQLR_SMALL = [
     # M, k, E, H, I, b, r, d
     (5, 2, 8, 1024, 256, 3, 128, 4), (13, 4, 16, 2048, 512, 8, 256, 4),
