@@ -362,14 +362,14 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     CUtensorMap tm_gate, tm_up, tm_down;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
     const int box_rows = kGemmStageK;  // K rows per weight box: one stage's depth
-    // VQ: the index maps [E * H/d rows][I] uint8, boxes of one stage's 256/d index rows x 64
-    // columns (unswizzled; the decoder warps write the swizzled A operand)
+    // VQ: the index maps [E * H/d rows][I] uint8, boxes of one stage's 256/d index rows x 128
+    // columns (unswizzled; the decoder warps write the weight operand to tensor memory)
     const bool maps_ok =
         d.vq_tc
             ? make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
-                           (uint64_t)d.E * (d.H / w->d), 64, box_rows / w->d) &&
+                           (uint64_t)d.E * (d.H / w->d), 128, box_rows / w->d) &&
                   make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
-                               (uint64_t)d.E * (d.H / w->d), 64, box_rows / w->d)
+                               (uint64_t)d.E * (d.H / w->d), 128, box_rows / w->d)
             : make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
                            (uint64_t)d.E * d.H, 64, box_rows, sw) &&
                   make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,

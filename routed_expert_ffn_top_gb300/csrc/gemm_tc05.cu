@@ -72,47 +72,52 @@ struct GTile {
     static constexpr bool kSplitB = false;  // one barrier for the weights and the row slice
 };
 
-// The VQ gate/up kernel (16-row tiles, code words of kD).  Its copy ring holds, per 256-deep
-// stage, the gate and up index boxes (256 / kD index rows x 64 columns of uint8 each, by TMA)
-// and the tile's row slice (behind a barrier of its own, so that decoding starts as soon as
-// the index boxes land); eight stages in flight.  The weight operand is decoded into
-// tensor memory instead: slots of 128 K rows (64 columns), three in flight, after the two
-// accumulators.  The code books sit in shared memory with each entry repeated kReps times
-// across the banks, so that the lanes of one wavefront, each reading its own repeat, never
-// share a bank.
+// The VQ gate/up kernel (16-row tiles, code words of kD).  A unit is a tile and 128 output
+// channels of both projections: two M = 128 MMAs per K step, into a gate and an up
+// accumulator.  Its copy ring holds, per 256-deep stage, the gate and up index boxes
+// (256 / kD index rows x 128 columns of uint8 each, by TMA: 128-byte rows) and the tile's row
+// slice (behind a barrier of its own, so that decoding starts as soon as the index boxes
+// land).  The weight operand is decoded into tensor memory: slots of 64 K rows (32 columns
+// per projection), six in flight, after the accumulators.  The code books sit in shared
+// memory with each entry repeated kReps times across the banks, so that the lanes of one
+// wavefront, each reading its own repeat, never share a bank.
 template <int kD>
 struct GTileVQ {
     static_assert(kD == 4 || kD == 8, "code words of 4 or 8");
     static constexpr int kK = kGemmStageK;
+    static constexpr int kCT = 128;                         // channels per unit and projection
     static constexpr int kJRows = kK / kD;
-    static constexpr int kJBytes = kJRows * 64;             // one projection's index box
+    static constexpr int kJBytes = kJRows * kCT;            // one projection's index box
     static constexpr int kBOff = 2 * kJBytes;
     static constexpr int kBBytes = 16 * kK * 2;
-    static constexpr int kStageBytes = kBOff + kBBytes;     // 16 KB (d = 4), 12 KB (d = 8)
+    static constexpr int kStageBytes = kBOff + kBBytes;     // 24 KB (d = 4), 16 KB (d = 8)
     static constexpr int kTxBytes = kStageBytes;
-    static constexpr int kStages = 8;
+    static constexpr int kStages = kD == 4 ? 6 : 8;
     static constexpr int kChunkBytes = 16 * 64 * 2;
-    static constexpr uint32_t kTmemCols = 256;
+    static constexpr uint32_t kTmemCols = 512;
     static constexpr int kTileN = 16;
     static constexpr int kDefer = 2;
     static constexpr bool kSplitB = true;  // decoders wait for the index boxes only
-    static constexpr int kDecWarps = 8;    // two per TMEM lane quadrant, half a slot's K each
-    static constexpr int kSlotK = 128;                      // K rows per tensor-memory slot
-    static constexpr int kSlots = 3;
-    static constexpr uint32_t kSlotCol0 = 64;               // columns 0-31: the accumulators
+    static constexpr int kDecWarps = 8;    // per TMEM lane quadrant one gate and one up warp
+    static constexpr int kSlotK = 64;                       // K rows per tensor-memory slot
+    static constexpr int kSlotsPerStage = kK / kSlotK;
+    static constexpr int kSlots = 6;
+    static constexpr uint32_t kSlotCols = 64;               // gate 32 columns, then up 32
+    static constexpr uint32_t kSlotCol0 = 64;               // columns 0-63: the accumulators
     static constexpr int kReps = kD == 4 ? 16 : 8;          // 8-byte words: 16 lanes a wavefront
     static constexpr int kEntryBytes = kReps * kD * 2;      // 128
     static constexpr int kCbBytes = 256 * kEntryBytes;      // one projection's code book
     static_assert(kStageBytes % 1024 == 0 && kBOff % 1024 == 0, "stage alignment");
-    static_assert(kSlotCol0 + kSlots * 64 <= kTmemCols, "tensor memory");
+    static_assert(kSlotCol0 + kSlots * kSlotCols <= kTmemCols, "tensor memory");
+    static_assert(kSlots <= kGMaxStages, "slot barriers");
 };
 
 struct GCtl {
     uint64_t full[kGMaxStages];
     uint64_t empty[kGMaxStages];
     uint64_t bfull[kGMaxStages];  // VQ: the stage's row slice has landed
-    uint64_t afull[3];   // VQ: a tensor-memory slot of the weight operand is written
-    uint64_t aempty[3];  // VQ: the MMAs reading a slot have completed
+    uint64_t afull[kGMaxStages];   // VQ: a tensor-memory slot of the weight operand is written
+    uint64_t aempty[kGMaxStages];  // VQ: the MMAs reading a slot have completed
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t done;
@@ -345,7 +350,7 @@ __device__ __forceinline__ void gemm_init(GCtl &ctl, int warp, int decoder_warps
             mbar_init(&ctl.full[s], 1);                   // the producer's expect_tx arrival
             mbar_init(&ctl.empty[s], 1 + decoder_warps);  // MMA completion (+ decoders)
         }
-        for (int s = 0; s < 3 && decoder_warps; ++s) {
+        for (int s = 0; s < kGMaxStages && decoder_warps; ++s) {
             mbar_init(&ctl.afull[s], decoder_warps);
             mbar_init(&ctl.aempty[s], 1);
         }
@@ -475,15 +480,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
 // ---------------------------------------------------------------------- VQ gate/up
 // Blockwise-VQ gate/up on the tensor cores (16-row tiles).  The weight operand never exists
-// in memory: four decoder warps, one TMEM lane quadrant each (lane = output channel: gate
-// channels in lanes 0-63, up in 64-127), read their channel's index of every index row q of a
-// 128-row K slot from the stage's index box, fetch its code word B[J[q][i]] (kD consecutive K
-// values of row i of the weight) from their own repeat of the code book, and write the words
-// to the slot's columns with tcgen05.st; two warps share a quadrant, each with half of the
-// slot's K, so that one's loads overlap the other's stores.  The MMA issuer takes A from
-// tensor memory and the row slice from the stage.  The chain per element is the dense
-// kernel's (K-ordered, one MMA per 16 K rows); epilogue and p tiles are the dense kernel's.
-// 14 warps: producer, MMA, 4 epilogue, 8 decoders.
+// in memory: eight decoder warps, one per TMEM lane quadrant and projection (lane = output
+// channel of the unit), read their channel's index of every index row q of a 64-row K slot
+// from the stage's index box, fetch its code word B[J[q][i]] (kD consecutive K values of row
+// i of the weight) from their own repeat of the code book, and write the words to the slot's
+// columns with tcgen05.st, software-pipelined: the stores of slot k run while the words of
+// slot k+1 are fetched.  The MMA issuer takes A from tensor memory and the row slice from
+// the stage.  The chain per element is the dense kernel's (K-ordered, one MMA per 16 K
+// rows).  The epilogue thread of a channel holds its gate and up accumulators and writes
+// SiLU(g) * u to the p tiles.  14 warps: producer, MMA, 4 epilogue, 8 decoders.
+//   Bounds measured on this GPU: an M = 128, K = 16 MMA issues in about 45 cycles for any N
+// up to 64 (so the 32 MMAs of a 16-row unit's stage take about 0.7 us), and a warp's
+// tcgen05.st with its wait costs about 200 cycles whatever its size; a unit's stage runs in
+// about 1.6 us, decoding-bound.  Wider tiles cost the same MMA time per stage.
 constexpr int kGVQThreads = 448;
 constexpr int kGDecWarp0 = 6;
 
@@ -507,7 +516,7 @@ __device__ void gemm_mma_vq(GCtl &ctl, unsigned char *stages, int64_t T, int nks
         const uint32_t tph = (uint32_t)(local >> 1) & 1u;
         if (!gwait(&ctl.tempty[buf], tph ^ 1u, ctl)) break;
         tc_fence_after();
-        const uint32_t d = ctl.tmem + (uint32_t)(buf * kN);
+        const uint32_t dg = ctl.tmem + (uint32_t)(buf * 2 * kN);  // gate, then up
         bool ok = true;
         for (int s = 0; s < nks && ok; ++s) {
             if (!gwait(&ctl.bfull[stage], phase, ctl)) {
@@ -516,19 +525,21 @@ __device__ void gemm_mma_vq(GCtl &ctl, unsigned char *stages, int64_t T, int nks
             }
             tc_fence_after();
             const uint32_t B = smem_u32(stages + stage * G::kStageBytes) + G::kBOff;
-            for (int h = 0; h < G::kK / G::kSlotK; ++h) {
+            for (int h = 0; h < G::kSlotsPerStage; ++h) {
                 if (!gwait(&ctl.afull[slot], sphase, ctl)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t A = ctl.tmem + G::kSlotCol0 + (uint32_t)(slot * 64);
+                const uint32_t A = ctl.tmem + G::kSlotCol0 + (uint32_t)slot * G::kSlotCols;
 #pragma unroll
                 for (int kk = 0; kk < kStepsPerSlot; ++kk) {
                     const int ks = h * kStepsPerSlot + kk;  // K = 16 step within the stage
                     const uint64_t bd =
                         umma_smem_desc(B + (ks >> 2) * G::kChunkBytes + (ks & 3) * 32, 16, 1024, 2);
-                    umma_bf16_ts(d, A + (uint32_t)(kk * 8), bd, idesc, s > 0 || ks > 0);
+                    const bool acc = s > 0 || ks > 0;
+                    umma_bf16_ts(dg, A + (uint32_t)(kk * 8), bd, idesc, acc);
+                    umma_bf16_ts(dg + kN, A + 32 + (uint32_t)(kk * 8), bd, idesc, acc);
                 }
                 umma_commit(&ctl.aempty[slot]);
                 if (++slot == G::kSlots) {
@@ -547,33 +558,32 @@ __device__ void gemm_mma_vq(GCtl &ctl, unsigned char *stages, int64_t T, int nks
     if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
 }
 
-// Decoder warp (TMEM lane quadrant `quad`, half `part` of each slot's K): the weight operand
-// of every stage, slot by slot, software-pipelined -- the tensor-memory stores of slot k run
-// while the indices and code words of slot k+1 are fetched; then slot k is signalled.
+// Decoder warp (TMEM lane quadrant `quad`, projection `p`): the weight operand of every
+// stage, slot by slot.
 template <int kD>
 struct VQDecoder {
     using G = GTileVQ<kD>;
-    static constexpr int kRows = G::kSlotK / kD / 2;  // index rows q per warp and slot: 16 or 8
+    static constexpr int kRows = G::kSlotK / kD;  // index rows q per slot: 16 or 8
     GCtl &ctl;
-    const unsigned char *jbase;  // this warp's index column in stage 0 (part's rows)
+    const unsigned char *jbase;  // this warp's index column in stage 0
     const unsigned char *cb;     // this lane's repeat of its projection's code book
     uint32_t taddr;              // this warp's lanes and columns in slot 0
 
-    // Slot task k (stage k / 2 of the CTA's sequence, half k % 2 of its K): waits for the
-    // stage's index boxes (first half) and for the slot to be free, then gathers the code
-    // words of the warp's rows into r; after the second half the stage's boxes are released.
+    // Slot task k (stage k / 4 of the CTA's sequence, quarter k % 4 of its K): waits for the
+    // stage's index boxes (first quarter) and for the slot to be free, then gathers the code
+    // words of its rows into r; after the last quarter the stage's boxes are released.
     __device__ __forceinline__ bool fetch(int64_t k, uint32_t (&r)[32]) {
-        const int64_t gs = k >> 1;
-        const int h = (int)(k & 1);
+        const int64_t gs = k / G::kSlotsPerStage;
+        const int h = (int)(k % G::kSlotsPerStage);
         const int stage = (int)(gs % G::kStages);
         if (h == 0 && !gwait_warp(&ctl.full[stage], (uint32_t)(gs / G::kStages) & 1u, ctl)) return false;
         if (!gwait_warp(&ctl.aempty[k % G::kSlots], ((uint32_t)(k / G::kSlots) & 1u) ^ 1u, ctl))
             return false;
         tc_fence_after();
-        const unsigned char *jb = jbase + stage * G::kStageBytes + h * 2 * kRows * 64;
+        const unsigned char *jb = jbase + stage * G::kStageBytes + h * kRows * G::kCT;
         uint32_t idx[kRows];
 #pragma unroll
-        for (int q = 0; q < kRows; ++q) idx[q] = jb[q * 64];
+        for (int q = 0; q < kRows; ++q) idx[q] = jb[q * G::kCT];
 #pragma unroll
         for (int q = 0; q < kRows; ++q) {
             if constexpr (kD == 4) {
@@ -588,7 +598,7 @@ struct VQDecoder {
                 r[4 * q + 3] = w.w;
             }
         }
-        if (h == 1) {
+        if (h == G::kSlotsPerStage - 1) {
             __syncwarp();
             if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.empty[stage]);  // its index boxes are read
         }
@@ -598,20 +608,18 @@ struct VQDecoder {
 
 template <int kD>
 __device__ void vq_decode(GCtl &ctl, const unsigned char *stages, const unsigned char *cbs,
-                          int64_t T, int nks, int quad, int part, int lane) {
+                          int64_t T, int nks, int quad, int p, int lane) {
     using G = GTileVQ<kD>;
     using Dec = VQDecoder<kD>;
-    const int p = quad >> 1;                      // 0: gate, 1: up
-    const int ch = 32 * (quad & 1) + lane;        // channel within the 64-column tile
-    Dec dec{ctl, stages + p * G::kJBytes + part * Dec::kRows * 64 + ch,
-            cbs + p * G::kCbBytes + (lane % G::kReps) * (kD * 2),
-            ctl.tmem + ((uint32_t)(32 * quad) << 16) + G::kSlotCol0 + (uint32_t)(32 * part)};
+    const int ch = 32 * quad + lane;  // channel within the unit's 128
+    Dec dec{ctl, stages + p * G::kJBytes + ch, cbs + p * G::kCbBytes + (lane % G::kReps) * (kD * 2),
+            ctl.tmem + ((uint32_t)(32 * quad) << 16) + G::kSlotCol0 + (uint32_t)(32 * p)};
     const int64_t units = T > blockIdx.x ? (T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int64_t K = units * nks * 2;  // slot tasks of this CTA
+    const int64_t K = units * nks * G::kSlotsPerStage;  // slot tasks of this CTA (even)
     // two register sets, swapped by unrolling by two (never indexed at run time)
     uint32_t r0[32], r1[32];
     auto step = [&](int64_t k, const uint32_t(&cur)[32], uint32_t(&next)[32]) {
-        const uint32_t ta = dec.taddr + (uint32_t)((k % G::kSlots) * 64);
+        const uint32_t ta = dec.taddr + (uint32_t)(k % G::kSlots) * G::kSlotCols;
         tmem_st16(ta, cur);
         tmem_st16(ta + 16, cur + 16);
         const bool more = k + 1 < K && dec.fetch(k + 1, next);
@@ -637,8 +645,7 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
     unsigned char *cbs = base + G::kStages * G::kStageBytes;  // gate then up code book
-    float *gbuf = reinterpret_cast<float *>(cbs + 2 * G::kCbBytes);  // [16][64]
-    GCtl &ctl = *reinterpret_cast<GCtl *>(reinterpret_cast<unsigned char *>(gbuf) + kN * 64 * 4);
+    GCtl &ctl = *reinterpret_cast<GCtl *>(cbs + 2 * G::kCbBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_jgate);
@@ -666,7 +673,7 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
     if (a.wait_first) pdl_wait();
     pdl_launch_dependents();
 
-    const int n_ct = a.I / 64;
+    const int n_ct = a.I / G::kCT;
     const int nks = a.H / G::kK;
     const int nrows = a.H / kD;
     const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
@@ -679,8 +686,8 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
                              T, n_ct, nks, a.wait_first != 0, e_first,
                              [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
                 const int32_t y = e * nrows + s * G::kJRows;
-                tma_load_2d(st, &tm_jgate, ct * 64, y, bar, pol);
-                tma_load_2d(st + G::kJBytes, &tm_jup, ct * 64, y, bar, pol);
+                tma_load_2d(st, &tm_jgate, ct * G::kCT, y, bar, pol);
+                tma_load_2d(st + G::kJBytes, &tm_jup, ct * G::kCT, y, bar, pol);
             });
         }
         __syncwarp();
@@ -691,7 +698,9 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
         vq_decode<kD>(ctl, stages, cbs, T, nks, warp & 3, (warp - kGDecWarp0) >> 2, lane);
     } else {
         const int quad = warp & 3;
-        const int row = 32 * quad + lane;
+        const int row = 32 * quad + lane;  // channel within the unit
+        const uint32_t tl = ctl.tmem + ((uint32_t)(32 * quad) << 16);
+        const int64_t chunk_of_tile = a.I / 64;
         int local = 0;
         for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
             const int64_t tile = u / n_ct;
@@ -700,24 +709,22 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
             if (row < kN) ctl.route[buf][row] = tile_route(a, tile, row, a.blocks[tile / a.tpb], false);
             const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
             if (named_bar_or(1, 128, !ok)) break;
-            float v[kN];
-            drain_accumulator<kN>(ctl, quad, buf, v);
-            if (quad < 2) {
+            float g[kN], up[kN];
+            tc_fence_after();
+            tmem_ld16(tl + (uint32_t)(buf * 2 * kN), g);
+            tmem_ld16(tl + (uint32_t)(buf * 2 * kN + kN), up);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
+            const int c64 = row & 63;  // channel within its 64-wide chunk of p
+            unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
+                                 (tile * chunk_of_tile + 2 * ct + (row >> 6)) * (int64_t)G::kChunkBytes +
+                                 (c64 & 7) * 2;
 #pragma unroll
-                for (int n = 0; n < kN; ++n)
-                    if (ctl.route[buf][n] >= 0) gbuf[n * 64 + row] = v[n];
-            }
-            named_bar_sync(1, 128);
-            if (quad >= 2) {
-                const int ch = row - 64;
-                unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
-                                     (tile * n_ct + ct) * (int64_t)G::kChunkBytes + (ch & 7) * 2;
-#pragma unroll
-                for (int n = 0; n < kN; ++n) {
-                    if (ctl.route[buf][n] < 0) continue;
-                    const float p = silu_f32(gbuf[n * 64 + ch]) * v[n];
-                    *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, ch >> 3)) = __float2bfloat16(p);
-                }
+            for (int n = 0; n < kN; ++n) {
+                if (ctl.route[buf][n] < 0) continue;
+                const float pv = silu_f32(g[n]) * up[n];
+                *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, c64 >> 3)) = __float2bfloat16(pv);
             }
         }
     }
@@ -851,7 +858,7 @@ cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm
 template <int kD>
 static size_t gemm_gateup_vq_smem() {
     using G = GTileVQ<kD>;
-    return 1024 + G::kStages * G::kStageBytes + 2 * G::kCbBytes + 16 * 64 * 4 + sizeof(GCtl);
+    return 1024 + G::kStages * G::kStageBytes + 2 * G::kCbBytes + sizeof(GCtl);
 }
 
 cudaError_t launch_gemm_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
