@@ -159,6 +159,18 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- helpers
+NOMINAL_HBM_GBS = 8000.0  # the headline metric's "~8 TB/s"
+
+
+def bootstrap_median_ci(values, resamples=10000, seed=0):
+    """95% bootstrap interval of the median of `values` (resampled with replacement)."""
+    rng = np.random.default_rng(seed)
+    v = np.asarray(values, dtype=np.float64)
+    meds = np.median(rng.choice(v, size=(resamples, v.size), replace=True), axis=1)
+    lo, hi = np.percentile(meds, [2.5, 97.5])
+    return [round(float(lo), 3), round(float(hi), 3)]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -385,6 +397,26 @@ def run_ours(args, world, rank, local):
         other_ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
         del other
 
+    # the route-block page's protocol: 20 warm-up calls, then 7 blocks of 50 calls, each timed
+    # with CUDA events; the median block and a 10,000-resample bootstrap interval of it
+    protocol = None
+    if not args.no_extras:
+        for i in range(20):
+            step(i)
+        block_us = []
+        for blk in range(7):
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            for i in range(50):
+                step(blk * 50 + i)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            block_us.append(ev0.elapsed_time(ev1) * 1e3 / (50 * blocks_per_step))
+        protocol = {"calls_per_block": 50, "blocks": 7, "warmup_calls": 20,
+                    "median_us_per_layer": round(statistics.median(block_us), 3),
+                    "bootstrap95_us_per_layer": bootstrap_median_ci(block_us),
+                    "block_us_per_layer": [round(v, 3) for v in block_us]}
+
     ms_per_step = t_ms / args.steps
     tokens = M * args.steps * world
     value = tokens / (t_ms / 1e3)
@@ -414,11 +446,15 @@ def run_ours(args, world, rank, local):
         ("direct_call_us_per_layer" if graphs else "graph_replay_us_per_layer"):
             None if other_ms is None else round(other_ms * 1e3 / blocks_per_step, 3),
         "hbm_gbs_unique_expert_bytes": round(hbm_gbs, 1),
+        "hbm_frac": {"measured": round(hbm_gbs / measured_peaks()[0], 4),
+                     "nominal_8tbs": round(hbm_gbs / NOMINAL_HBM_GBS, 4)},
         "unique_experts_per_layer": round(statistics.mean(per_set_unique), 2),
         "unique_experts_per_set": per_set_unique,
         "gpu_launches": launches_per_block * blocks_per_step * args.steps,
         "clocks": clocks,
     }
+    if protocol is not None:
+        result["protocol"] = protocol
     if args.no_extras:
         if rank == 0:
             print(json.dumps(result), flush=True)
@@ -463,6 +499,7 @@ def run_ours(args, world, rank, local):
     result["roofline"] = {
         "kernel": gu_kernel, "bound": "hbm", "achieved": round(achieved, 1),
         "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+        "frac_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         "traffic": None if traffic is None else int(traffic),
         "algorithmic_bytes_per_launch": int(gu_alg),
         "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
@@ -624,7 +661,8 @@ def run_reader(args, world, rank, local, wl):
         "reader_bytes": {"sketch": sk_b, "exact": ex_b, "recover": rc_b},
         "roofline": {"kernel": "reader_%s_kernel" % dominant, "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4), "traffic": None,
                      "algorithmic_bytes_per_launch": int(alg),
                      "kernel_ms_traced": {n: round(v, 5) for n, v in mean_ms.items()}},
         "gpu_launches": 6 * args.steps,  # router + the reader's five kernels

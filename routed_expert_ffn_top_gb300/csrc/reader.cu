@@ -377,64 +377,103 @@ __global__ void __launch_bounds__(kSelectThreads)
     reader_select_kernel(const float *__restrict__ score, int N, int K,
                          uint8_t *__restrict__ keep, int32_t *__restrict__ sel,
                          int32_t *__restrict__ nsel) {
-    extern __shared__ uint32_t keys[];  // [N], then 32 warp histograms of 256 bins
+    extern __shared__ uint32_t keys[];  // [N], then two sets of 32 warp histograms of 256 bins
     int *whist = reinterpret_cast<int *>(keys + N);
     __shared__ int warp_tot[32];
-    __shared__ int s_nvalid, s_digit, s_remaining;
+    __shared__ int s_nvalid, s_digit, s_remaining, s_count;
+    __shared__ uint32_t s_and, s_or;
     pdl_wait();
     pdl_launch_dependents();
     const int m = blockIdx.x, tid = threadIdx.x;
-    if (tid == 0) s_nvalid = 0;
+    if (tid == 0) {
+        s_nvalid = 0;
+        s_and = ~0u;
+        s_or = 0u;
+    }
+    for (int d = tid; d < 32 * 256; d += kSelectThreads) whist[d] = 0;
     __syncthreads();
     int nv = 0;
+    uint32_t k_and = ~0u, k_or = 0u;  // over the valid keys: their common leading bits
     for (int f = tid; f < N; f += kSelectThreads) {
         const float s = score[(size_t)m * N + f];
         const uint32_t key = s >= 0.0f ? __float_as_uint(s) + 1u : 0u;  // invalid / NaN: 0
         keys[f] = key;
         nv += key != 0u;
-    }
-    atomicAdd(&s_nvalid, nv);
-    __syncthreads();
-    const int Keff = min(K, s_nvalid);
-    uint32_t prefix = 0, mask = 0;
-    int remaining = Keff;
-    if (Keff > 0) {
-        const int wbase = (tid >> 5) * 256;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int d = tid; d < 32 * 256; d += kSelectThreads) whist[d] = 0;
-            __syncthreads();
-            // each warp counts into its own histogram (integer adds commute)
-            for (int f = tid; f < N; f += kSelectThreads)
-                if ((keys[f] & mask) == prefix) atomicAdd(&whist[wbase + ((keys[f] >> shift) & 255u)], 1);
-            __syncthreads();
-            // thread t < 256 owns digit 255 - t: its count over the warps, then a scan in
-            // descending digit order finds the digit where the count reaches `remaining`
-            int c = 0;
-            if (tid < 256)
-                for (int w = 0; w < 32; ++w) c += whist[w * 256 + (255 - tid)];
-            const int incl = block_scan_1024(c, warp_tot);
-            if (tid < 256 && c > 0 && incl >= remaining && incl - c < remaining) {
-                s_digit = 255 - tid;
-                s_remaining = remaining - (incl - c);
-            }
-            __syncthreads();
-            prefix |= (uint32_t)s_digit << shift;
-            mask |= 255u << shift;
-            remaining = s_remaining;
-            __syncthreads();
+        if (key != 0u) {
+            k_and &= key;
+            k_or |= key;
         }
     }
-    // keys above the threshold are kept, and the first `remaining` keys equal to it in
-    // index order; each thread owns a contiguous run of channels
+    atomicAdd(&s_nvalid, nv);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        k_and &= __shfl_xor_sync(0xffffffffu, k_and, o);
+        k_or |= __shfl_xor_sync(0xffffffffu, k_or, o);
+    }
+    if ((tid & 31) == 0) {
+        atomicAnd(&s_and, k_and);
+        atomicOr(&s_or, k_or);
+    }
+    __syncthreads();
+    const int Keff = min(K, s_nvalid);
+    // Radix select from the first bit where the valid keys differ (the bits above it are the
+    // same in all of them: scores of one sign and a narrow exponent range), up to 8 bits a
+    // pass.  After a pass, the keys above the prefix are kept, those below dropped, and
+    // `remaining` of those under it are still to be kept.  When that is all of them, later
+    // passes cannot change the kept set: stop there.  (Invalid keys, 0, are below every
+    // valid one and never needed: Keff <= the valid count.)
+    const uint32_t diff = s_and ^ s_or;
+    int hi = diff ? 31 - __clz(diff) : -1;  // highest differing bit
+    uint32_t mask = hi < 0 ? ~0u : ~((2u << hi) - 1u);  // 2u << 31 wraps to 0: mask 0
+    uint32_t prefix = s_and & mask;
+    int remaining = Keff;
+    if (Keff > 0) {
+        int buf = 0;
+        while (hi >= 0) {
+            const int lo = hi >= 7 ? hi - 7 : 0;
+            const int nb = 1 << (hi - lo + 1);  // bins of this pass's digit
+            const uint32_t dmask = (uint32_t)nb - 1u;
+            int *hist = whist + buf * 32 * 256;
+            int *next = whist + (buf ^ 1) * 32 * 256;
+            const int wbase = (tid >> 5) * 256;
+            // each warp counts into its own histogram (integer adds commute); the other set
+            // is cleared for the next pass meanwhile
+            for (int f = tid; f < N; f += kSelectThreads)
+                if ((keys[f] & mask) == prefix) atomicAdd(&hist[wbase + ((keys[f] >> lo) & dmask)], 1);
+            for (int d = tid; d < 32 * 256; d += kSelectThreads) next[d] = 0;
+            __syncthreads();
+            // thread t < nb owns digit nb - 1 - t: its count over the warps, then a scan in
+            // descending digit order finds the digit where the count reaches `remaining`
+            int c = 0;
+            if (tid < nb)
+                for (int w = 0; w < 32; ++w) c += hist[w * 256 + (nb - 1 - tid)];
+            const int incl = block_scan_1024(c, warp_tot);
+            if (tid < nb && c > 0 && incl >= remaining && incl - c < remaining) {
+                s_digit = nb - 1 - tid;
+                s_remaining = remaining - (incl - c);
+                s_count = c;
+            }
+            __syncthreads();
+            prefix |= (uint32_t)s_digit << lo;
+            mask |= dmask << lo;
+            remaining = s_remaining;
+            const bool all_kept = remaining == s_count;
+            buf ^= 1;
+            hi = lo - 1;
+            if (all_kept) break;  // uniform: every thread read the same shared values
+        }
+    }
+    // keys above the prefix are kept, and the first `remaining` keys under it in index order;
+    // each thread owns a contiguous run of channels
     const uint32_t T = prefix;
     const int per = (N + kSelectThreads - 1) / kSelectThreads;
     const int f0 = tid * per, f1 = min(N, f0 + per);
     int eq = 0;
-    for (int f = f0; f < f1; ++f) eq += (Keff > 0 && keys[f] == T);
+    for (int f = f0; f < f1; ++f) eq += (Keff > 0 && (keys[f] & mask) == T);
     int eq_before = block_scan_1024(eq, warp_tot) - eq;
     int kc = 0;
     for (int f = f0; f < f1; ++f) {
-        const uint32_t key = keys[f];
+        const uint32_t key = keys[f] & mask;
         bool kp = false;
         if (Keff > 0) {
             if (key > T) kp = true;
@@ -736,7 +775,7 @@ cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, in
     }
     trace_point(1, stream);
     {
-        const size_t smem = (size_t)N * 4 + 32 * 256 * 4;  // keys and the warp histograms
+        const size_t smem = (size_t)N * 4 + 2 * 32 * 256 * 4;  // keys, two histogram sets
         err = ensure_smem(reinterpret_cast<const void *>(reader_select_kernel), smem);
         if (err != cudaSuccess) return err;
         cudaLaunchConfig_t cfg = launch_config(dim3(M), dim3(kSelectThreads), smem, stream, attrs, 0);
