@@ -200,17 +200,6 @@ def gemm_regime(wl) -> bool:
     return wl.kind == syn.W_DENSE or (wl.kind == syn.W_VQ and wl.vq_form == 2)
 
 
-def library_block(wl) -> int:
-    """The block size moe_decode_block aligns with: for dense weights 64 rows from 4 routes
-    per expert on average, else 16; VQ weights decoded on the tensor cores 16; the other VQ
-    forms keep the workload's b."""
-    if wl.kind == syn.W_DENSE:
-        return 64 if wl.M * wl.k >= 4 * wl.E else 16
-    if gemm_regime(wl):
-        return 16
-    return wl.b
-
-
 def gateup_kernel_name(wl) -> str:
     if gemm_regime(wl):
         return "gemm_gateup_vq_kernel" if wl.kind == syn.W_VQ else "gemm_gateup_kernel"
@@ -330,7 +319,7 @@ def run_ours(args, world, rank, local):
     gu_b, dn_b = expert_bytes(wl)
     per_set_unique = []
     padded_rows = []  # aligned rows sum_e ceil(n_e / b) * b of each probe
-    b_lib = library_block(wl)
+    b_lib = moe.moe_library_block_size(layers[0], M, wl.k, wl.b)
 
     def note_routing():
         per_set_unique.append(int(torch.unique(ids).numel()))

@@ -159,6 +159,16 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
 size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b);
 
 /*
+ * The block size moe_decode_block (and moe_expert_ffn without an alignment) aligns with for
+ * (weights, M, k, b): b itself for the VQ forms 0 and 1; for dense weights and VQ form 2 the
+ * tcgen05 tile width the library picks, 16 or 64 rows, by routes per expert and (dense) by
+ * whether one wave of 16-row units' weights fits in this device's L2.  Every route's bits
+ * are the same in both widths; the choice only affects speed.  Host-only (reads device
+ * attributes of the current device, once).  Returns 0 on invalid arguments.
+ */
+int moe_library_block_size(const moe_expert_weights_t *w, int M, int k, int b);
+
+/*
  * Expert FFN + affinity-weighted combine for given routes.
  *   h [M,H] bf16; topk_ids [M,k] int32; topk_weights [M,k] fp32; residual [M,H] bf16 or
  *   NULL; out [M,H] bf16 = bf16(residual + sum_j a_j y_j) (tokens with no valid route get

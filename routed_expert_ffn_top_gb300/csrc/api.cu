@@ -71,6 +71,18 @@ int num_sms() {
     return cache[dev];
 }
 
+int l2_bytes() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev);
+        cache[dev] = n > 0 ? n : -1;
+    }
+    return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 cudaError_t ensure_smem(const void *func, size_t bytes) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -245,11 +257,8 @@ static Dims dims_for(const moe_expert_weights_t *w, int M, int k, int b) {
     d.ttable = w->kind == MOE_W_VQ_GATEUP && w->vq_form == 1;
     d.vqd = w->d;
     if (w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2) {
-        // 16-row tiles whatever b is (an aligned block is cut into ceil(b / 16) of them)
-        d.gemm = true;
+        d.gemm = true;  // the tiles of dense weights (16 or 64 rows by b)
         d.vq_tc = true;
-        d.kn = kGemmNarrow;
-        d.tpb = (b + kGemmNarrow - 1) / kGemmNarrow;
     }
     return d;
 }
@@ -307,17 +316,31 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
                                     static_cast<cudaStream_t>(stream)));
 }
 
-// The block size the library aligns with when it aligns the routes itself.  Dense weights run
-// as tcgen05 tiles whatever b is, so the library picks the tile width: 64-row blocks from 4
-// routes per expert on average (the routes of an expert fill the MMA's N side), 16-row blocks
-// below that (an expert's weights stream once for up to 16 of its routes).  VQ weights
-// decoded on the tensor cores run 16-row tiles only, so the library aligns with b = 16; the
-// other VQ forms keep the caller's b.
+// The block size the library aligns with when it aligns the routes itself.  Dense weights,
+// and VQ weights decoded on the tensor cores, run as tcgen05 tiles whatever b is, so the
+// library picks the tile width: 16-row tiles, or 64-row ones from `per_expert` routes per
+// expert on average.  Measured on GB300 (16- against 64-row tiles):
+//   - dense weights: an expert's 16-row tiles run on neighbouring CTAs at the same time, so
+//     the second tile's weights come from L2 while one wave of units' weights fits in it
+//     (H = 2048: 16-row tiles faster up to 16 routes per expert, even at 24, slower at 32);
+//     when a wave does not fit (H = 4096, I = 1536) 64-row tiles are faster from 8;
+//   - VQ decoded on the tensor cores: a unit's MMAs and decoding cost the same for 16 or
+//     64 rows; 16-row tiles faster up to 12 routes per expert, 64-row ones from 16.
+// The other VQ forms keep the caller's b.
 static int effective_block(const moe_expert_weights_t *w, int M, int k, int b) {
-    if (w && w->kind == MOE_W_DENSE_BF16)
-        return (int64_t)M * k >= 4 * (int64_t)w->E ? kGemmBlock : kGemmNarrow;
-    if (w && w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2) return kGemmNarrow;
-    return b;
+    const bool vq_tc = w && w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2;
+    if (!w || (w->kind != MOE_W_DENSE_BF16 && !vq_tc)) return b;
+    int per_expert = 16;
+    if (!vq_tc) {
+        const int64_t wave = (int64_t)num_sms() * 2 * 64 * w->H * 2;  // 16-row units' weights
+        per_expert = wave <= (int64_t)l2_bytes() ? 24 : 4;
+    }
+    return (int64_t)M * k >= (int64_t)per_expert * w->E ? kGemmBlock : kGemmNarrow;
+}
+
+extern "C" int moe_library_block_size(const moe_expert_weights_t *w, int M, int k, int b) {
+    if (!w || M < 0 || k <= 0 || check_block(b) != MOE_OK) return 0;
+    return effective_block(w, M, k, b);
 }
 
 size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, int b) {
@@ -332,11 +355,18 @@ size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, i
 
 extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b) {
     // enough for the caller's b (a caller-supplied alignment) and for the block size the
-    // library picks when it aligns itself
+    // library picks when it aligns itself (either tile width, so that the size does not
+    // depend on the device the choice is made on)
     const size_t a = workspace_bytes_fixed(w, M, k, b);
     if (a == 0) return 0;
-    const size_t e = workspace_bytes_fixed(w, M, k, effective_block(w, M, k, b));
-    return a > e ? a : e;
+    size_t need = a;
+    const int picks[3] = {effective_block(w, M, k, b), kGemmNarrow, kGemmBlock};
+    const int npicks = effective_block(w, M, k, b) != b ? 3 : 1;
+    for (int i = 0; i < npicks; ++i) {
+        const size_t e = workspace_bytes_fixed(w, M, k, picks[i]);
+        if (e > need) need = e;
+    }
+    return need;
 }
 
 // Runs gate/up and down for aligned routes (alignment pointers already resolved).

@@ -72,44 +72,47 @@ struct GTile {
     static constexpr bool kSplitB = false;  // one barrier for the weights and the row slice
 };
 
-// The VQ gate/up kernel (16-row tiles, code words of kD).  A unit is a tile and 128 output
-// channels of both projections: two M = 128 MMAs per K step, into a gate and an up
-// accumulator.  Its copy ring holds, per 256-deep stage, the gate and up index boxes
+// The VQ gate/up kernel (tiles of kN = 16 or 64 rows, code words of kD).  A unit is a tile and
+// 128 output channels of both projections: two M = 128 MMAs per K step, into a gate and an
+// up accumulator.  Its copy ring holds, per 256-deep stage, the gate and up index boxes
 // (256 / kD index rows x 128 columns of uint8 each, by TMA: 128-byte rows) and the tile's row
 // slice (behind a barrier of its own, so that decoding starts as soon as the index boxes
 // land).  The weight operand is decoded into tensor memory: slots of 64 K rows (32 columns
-// per projection), six in flight, after the accumulators.  The code books sit in shared
-// memory with each entry repeated kReps times across the banks, so that the lanes of one
-// wavefront, each reading its own repeat, never share a bank.
-template <int kD>
+// per projection) after the accumulators, six in flight with 16-row tiles and three with
+// 64-row ones (whose accumulators take 256 columns).  The code books sit in shared memory
+// with each entry repeated kReps times across the banks, so that the lanes of one wavefront,
+// each reading its own repeat, never share a bank.
+template <int kD, int kN>
 struct GTileVQ {
     static_assert(kD == 4 || kD == 8, "code words of 4 or 8");
+    static_assert(kN == 16 || kN == 64, "tile widths: 16 or 64 rows");
     static constexpr int kK = kGemmStageK;
     static constexpr int kCT = 128;                         // channels per unit and projection
     static constexpr int kJRows = kK / kD;
     static constexpr int kJBytes = kJRows * kCT;            // one projection's index box
     static constexpr int kBOff = 2 * kJBytes;
-    static constexpr int kBBytes = 16 * kK * 2;
-    static constexpr int kStageBytes = kBOff + kBBytes;     // 24 KB (d = 4), 16 KB (d = 8)
+    static constexpr int kBBytes = kN * kK * 2;
+    static constexpr int kStageBytes = kBOff + kBBytes;     // 24/16 KB (16 rows), 48/40 KB (64)
     static constexpr int kTxBytes = kStageBytes;
-    static constexpr int kStages = kD == 4 ? 6 : 8;
-    static constexpr int kChunkBytes = 16 * 64 * 2;
+    static constexpr int kStages = kN == 16 ? (kD == 4 ? 6 : 8) : 3;
+    static constexpr int kChunkBytes = kN * 64 * 2;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kTileN = 16;
+    static constexpr int kTileN = kN;
     static constexpr int kDefer = 2;
     static constexpr bool kSplitB = true;  // decoders wait for the index boxes only
     static constexpr int kDecWarps = 8;    // per TMEM lane quadrant one gate and one up warp
     static constexpr int kSlotK = 64;                       // K rows per tensor-memory slot
     static constexpr int kSlotsPerStage = kK / kSlotK;
-    static constexpr int kSlots = 6;
+    static constexpr int kSlots = kN == 16 ? 6 : 3;
     static constexpr uint32_t kSlotCols = 64;               // gate 32 columns, then up 32
-    static constexpr uint32_t kSlotCol0 = 64;               // columns 0-63: the accumulators
+    static constexpr uint32_t kAccCols = 4 * kN;            // two buffers of gate and up
+    static constexpr uint32_t kSlotCol0 = kAccCols < 64 ? 64 : kAccCols;
     static constexpr int kReps = kD == 4 ? 16 : 8;          // 8-byte words: 16 lanes a wavefront
     static constexpr int kEntryBytes = kReps * kD * 2;      // 128
     static constexpr int kCbBytes = 256 * kEntryBytes;      // one projection's code book
     static_assert(kStageBytes % 1024 == 0 && kBOff % 1024 == 0, "stage alignment");
     static_assert(kSlotCol0 + kSlots * kSlotCols <= kTmemCols, "tensor memory");
-    static_assert(kSlots <= kGMaxStages, "slot barriers");
+    static_assert(kSlots <= kGMaxStages && kStages <= kGMaxStages, "barriers");
 };
 
 struct GCtl {
@@ -502,10 +505,9 @@ __device__ __forceinline__ bool gwait_warp(uint64_t *bar, uint32_t parity, GCtl 
     return __all_sync(0xffffffffu, gwait(bar, parity, ctl));
 }
 
-template <int kD>
+template <int kD, int kN>
 __device__ void gemm_mma_vq(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
-    using G = GTileVQ<kD>;
-    constexpr int kN = 16;
+    using G = GTileVQ<kD, kN>;
     constexpr uint32_t idesc = umma_idesc_bf16(kGM, kN, false, false);
     constexpr int kStepsPerSlot = G::kSlotK / 16;
     int stage = 0, slot = 0;
@@ -560,9 +562,9 @@ __device__ void gemm_mma_vq(GCtl &ctl, unsigned char *stages, int64_t T, int nks
 
 // Decoder warp (TMEM lane quadrant `quad`, projection `p`): the weight operand of every
 // stage, slot by slot.
-template <int kD>
+template <int kD, int kN>
 struct VQDecoder {
-    using G = GTileVQ<kD>;
+    using G = GTileVQ<kD, kN>;
     static constexpr int kRows = G::kSlotK / kD;  // index rows q per slot: 16 or 8
     GCtl &ctl;
     const unsigned char *jbase;  // this warp's index column in stage 0
@@ -606,11 +608,11 @@ struct VQDecoder {
     }
 };
 
-template <int kD>
+template <int kD, int kN>
 __device__ void vq_decode(GCtl &ctl, const unsigned char *stages, const unsigned char *cbs,
                           int64_t T, int nks, int quad, int p, int lane) {
-    using G = GTileVQ<kD>;
-    using Dec = VQDecoder<kD>;
+    using G = GTileVQ<kD, kN>;
+    using Dec = VQDecoder<kD, kN>;
     const int ch = 32 * quad + lane;  // channel within the unit's 128
     Dec dec{ctl, stages + p * G::kJBytes + ch, cbs + p * G::kCbBytes + (lane % G::kReps) * (kD * 2),
             ctl.tmem + ((uint32_t)(32 * quad) << 16) + G::kSlotCol0 + (uint32_t)(32 * p)};
@@ -634,12 +636,11 @@ __device__ void vq_decode(GCtl &ctl, const unsigned char *stages, const unsigned
         if (!step(k, r0, r1) || !step(k + 1, r1, r0)) return;
 }
 
-template <int kD>
+template <int kD, int kN>
 __global__ void __launch_bounds__(kGVQThreads, 1)
     gemm_gateup_vq_kernel(const __grid_constant__ CUtensorMap tm_jgate,
                           const __grid_constant__ CUtensorMap tm_jup, const GemmArgs a) {
-    using G = GTileVQ<kD>;
-    constexpr int kN = 16;
+    using G = GTileVQ<kD, kN>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -692,10 +693,10 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) gemm_mma_vq<kD>(ctl, stages, T, nks);
+        if (lane == 0) gemm_mma_vq<kD, kN>(ctl, stages, T, nks);
         __syncwarp();
     } else if (warp >= kGDecWarp0) {
-        vq_decode<kD>(ctl, stages, cbs, T, nks, warp & 3, (warp - kGDecWarp0) >> 2, lane);
+        vq_decode<kD, kN>(ctl, stages, cbs, T, nks, warp & 3, (warp - kGDecWarp0) >> 2, lane);
     } else {
         const int quad = warp & 3;
         const int row = 32 * quad + lane;  // channel within the unit
@@ -709,23 +710,27 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
             if (row < kN) ctl.route[buf][row] = tile_route(a, tile, row, a.blocks[tile / a.tpb], false);
             const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
             if (named_bar_or(1, 128, !ok)) break;
-            float g[kN], up[kN];
-            tc_fence_after();
-            tmem_ld16(tl + (uint32_t)(buf * 2 * kN), g);
-            tmem_ld16(tl + (uint32_t)(buf * 2 * kN + kN), up);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
             const int c64 = row & 63;  // channel within its 64-wide chunk of p
             unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
                                  (tile * chunk_of_tile + 2 * ct + (row >> 6)) * (int64_t)G::kChunkBytes +
                                  (c64 & 7) * 2;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < kN; c0 += 16) {  // 16 rows of the tile at a time
+                float g[16], up[16];
+                tmem_ld16(tl + (uint32_t)(buf * 2 * kN + c0), g);
+                tmem_ld16(tl + (uint32_t)(buf * 2 * kN + kN + c0), up);
 #pragma unroll
-            for (int n = 0; n < kN; ++n) {
-                if (ctl.route[buf][n] < 0) continue;
-                const float pv = silu_f32(g[n]) * up[n];
-                *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, c64 >> 3)) = __float2bfloat16(pv);
+                for (int n = 0; n < 16; ++n) {
+                    if (ctl.route[buf][c0 + n] < 0) continue;
+                    const float pv = silu_f32(g[n]) * up[n];
+                    *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(c0 + n, c64 >> 3)) =
+                        __float2bfloat16(pv);
+                }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
         }
     }
     gemm_finish<G>(ctl, warp, a.status);
@@ -855,22 +860,30 @@ cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm
     return cudaErrorInvalidValue;
 }
 
-template <int kD>
+template <int kD, int kN>
 static size_t gemm_gateup_vq_smem() {
-    using G = GTileVQ<kD>;
+    using G = GTileVQ<kD, kN>;
     return 1024 + G::kStages * G::kStageBytes + 2 * G::kCbBytes + sizeof(GCtl);
+}
+
+template <int kD, int kN>
+static cudaError_t launch_gemm_gateup_vq_t(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                                           const GemmArgs &a, cudaStream_t stream) {
+    const size_t smem = gemm_gateup_vq_smem<kD, kN>();
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_gateup_vq_kernel<kD, kN>), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGVQThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, gemm_gateup_vq_kernel<kD, kN>, tm_jgate, tm_jup, a);
 }
 
 cudaError_t launch_gemm_gateup_vq(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
                                   const GemmArgs &a, int d, cudaStream_t stream) {
-    if (a.kn != 16 || (d != 4 && d != 8)) return cudaErrorInvalidValue;
-    const size_t smem = d == 4 ? gemm_gateup_vq_smem<4>() : gemm_gateup_vq_smem<8>();
-    auto kern = d == 4 ? gemm_gateup_vq_kernel<4> : gemm_gateup_vq_kernel<8>;
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(kern), smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attrs[2];
-    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGVQThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, kern, tm_jgate, tm_jup, a);
+    if (d == 4 && a.kn == 16) return launch_gemm_gateup_vq_t<4, 16>(tm_jgate, tm_jup, a, stream);
+    if (d == 4 && a.kn == 64) return launch_gemm_gateup_vq_t<4, 64>(tm_jgate, tm_jup, a, stream);
+    if (d == 8 && a.kn == 16) return launch_gemm_gateup_vq_t<8, 16>(tm_jgate, tm_jup, a, stream);
+    if (d == 8 && a.kn == 64) return launch_gemm_gateup_vq_t<8, 64>(tm_jgate, tm_jup, a, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream) {

@@ -189,6 +189,7 @@ __device__ __forceinline__ int64_t num_subblocks(const GemvArgs &a) {
 }
 
 int num_sms();
+int l2_bytes();  // this device's L2 size in bytes (0 when it cannot be read)
 
 // Record of sub-block sb: expert of its block, valid routes (0 <= r < R) of its rsub rows in
 // row order, token of each route.  With `check`, a route whose top-k id is not the block's

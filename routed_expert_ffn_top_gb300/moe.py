@@ -39,7 +39,7 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_expert_ffn", "moe_decode_block", "moe_decode_block_host",
     "moe_read_device_status", "moe_set_trace_events", "moe_decode_block_noalloc",
     "moe_selftest_wait_timeout", "moe_reader_build", "moe_reader_workspace_bytes",
-    "moe_reader_ffn",
+    "moe_reader_ffn", "moe_library_block_size",
 )
 
 
@@ -107,6 +107,8 @@ def lib():
             L.moe_align_block_size.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, sz, vp]
             L.moe_workspace_bytes.argtypes = [wp, ci, ci, ci]
             L.moe_workspace_bytes.restype = sz
+            L.moe_library_block_size.argtypes = [wp, ci, ci, ci]
+            L.moe_library_block_size.restype = ci
             L.moe_expert_ffn.argtypes = [vp, wp, ci, ci, vp, vp, vp, vp, vp, ci, vp, vp, vp, sz, vp]
             L.moe_decode_block.argtypes = [vp, vp, vp, wp, ci, ci, ci, vp, vp, vp, vp, vp, sz, vp]
             L.moe_decode_block_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, wp, ci, ci, ci,
@@ -246,6 +248,12 @@ def moe_align_block_size(topk_ids, E, b, sorted_route_ids=None, expert_block_ids
 def moe_workspace_bytes(layer: dict, M, k, b) -> int:
     w = expert_weights(layer)
     return int(lib().moe_workspace_bytes(ctypes.byref(w), M, k, b))
+
+
+def moe_library_block_size(layer: dict, M, k, b) -> int:
+    """The block size moe_decode_block aligns with for these weights and sizes."""
+    w = expert_weights(layer)
+    return int(lib().moe_library_block_size(ctypes.byref(w), M, k, b))
 
 
 def alloc_workspace(layer: dict, M, k, b, device=None) -> torch.Tensor:

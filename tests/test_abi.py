@@ -184,6 +184,27 @@ def test_reader_validation_without_gpu(lib):
     assert L.moe_reader_build(ctypes.byref(w), ctypes.byref(_reader(I=512)), None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_library_block_size_without_gpu(lib):
+    """The alignment block size the library picks: the caller's b for VQ forms 0 and 1; for
+    dense weights and VQ form 2 a tile width (16 at one token; 64 for VQ form 2 from 16
+    routes per expert); 0 on invalid arguments."""
+    L = moe.lib()
+    d = _weights()
+    assert L.moe_library_block_size(ctypes.byref(d), 1, 8, 8) == 16
+    assert L.moe_library_block_size(ctypes.byref(d), 4096, 8, 8) == 64
+    assert L.moe_library_block_size(ctypes.byref(d), 1, 8, 12) == 0  # invalid b
+    assert L.moe_library_block_size(None, 1, 8, 8) == 0
+    v = _weights(kind=moe.MOE_W_VQ_GATEUP)
+    assert L.moe_library_block_size(ctypes.byref(v), 21, 8, 8) == 8
+    v.vq_form = 2
+    assert L.moe_library_block_size(ctypes.byref(v), 255, 8, 8) == 16  # 15.9 routes per expert
+    assert L.moe_library_block_size(ctypes.byref(v), 256, 8, 8) == 64
+    # the workspace covers either tile width
+    assert L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 8) >= max(
+        L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 16),
+        L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 64))
+
+
 def test_vq_form_validation_without_gpu(lib):
     L = moe.lib()
     w = _weights(kind=moe.MOE_W_VQ_GATEUP)

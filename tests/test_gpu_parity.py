@@ -422,6 +422,33 @@ def test_vq_tensor_core_small(M, k, E, H, I, b, d):
     G.assert_close_block(G.to_f64(o_cb), G.to_f64(out).astype(np.float64), "two VQ forms")
 
 
+def test_vq_tensor_core_bits_same_in_both_tile_widths():
+    """VQ on the tensor cores: 64-row tiles (the library's choice from 16 routes per expert)
+    and 16-row tiles (a caller's b = 8 alignment, or a few tokens) give every route the same
+    bits: one K-ordered MMA chain per element in both widths."""
+    M, k, E, H, I, d = 40, 4, 8, 1024, 512, 4
+    wl = syn.Workload("vq_tc_widths", H=H, I=I, E=E, k=k, b=8, M=M, kind=syn.W_VQ, d=d, K=256,
+                      vq_form=2)
+    layer = syn.make_layer(wl, seed=16, device=DEV)
+    h = syn.make_hidden(wl, seed=16, device=DEV)
+    rng = np.random.default_rng(16)
+    ids = _random_ids(rng, M, k, E)
+    a = _random_affinities(rng, M, k)
+    t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
+    assert moe.moe_library_block_size(layer, M, k, 8) == 64
+    wide = moe.moe_expert_ffn(h, layer, t_ids, t_a, 8)  # library: 64-row blocks
+    G.assert_close_block(G.to_f64(wide), G.oracle_ffn(layer, h, ids, a), "vq 64-row tiles")
+    for b in (1, 8, 16, 24, 64, 128):
+        srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
+        o = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad))
+        assert torch.equal(o, wide), b
+    for sub in ([7], [0, 39], list(range(3, 9))):
+        sel = torch.as_tensor(sub, device=DEV)
+        o = moe.moe_expert_ffn(h[sel].contiguous(), layer, t_ids[sel].contiguous(),
+                               t_a[sel].contiguous(), 8)  # library: 16-row blocks
+        assert torch.equal(o, wide[sel]), sub
+
+
 def test_vq_tensor_core_block_every_m_and_invariance():
     """The VQ decode layer on the tcgen05 path: parity at M = 1..16 (the router writes the
     row tiles up to 8 tokens, the row gather does above), each token's bits the same alone,
@@ -450,6 +477,19 @@ def test_vq_tensor_core_block_every_m_and_invariance():
         assert torch.equal(o1[0], out16[t]), t
     runs = [moe.moe_decode_block(h16, layer, wl.k, wl.b)[0] for _ in range(5)]
     assert all(torch.equal(r, out16) for r in runs)
+    # 256 tokens (16 routes per expert) run 64-row tiles: the 16 shared tokens keep their
+    # bits; sampled parity
+    assert moe.moe_library_block_size(layer, 256, wl.k, wl.b) == 64
+    h256 = torch.cat([h16, syn.make_hidden(wl, M=240, seed=10, device=DEV)])
+    out256, ids256, wts256 = moe.moe_decode_block(h256, layer, wl.k, wl.b)
+    assert torch.equal(ids256[:16], ids16) and torch.equal(out256[:16], out16)
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h256, wl.k)
+    use_ids, use_wts, _ = G.check_routing(ids256.cpu().numpy(), wts256.cpu().numpy(), o_ids,
+                                          o_wts, logits, wl.k)
+    tokens = np.array([16, 130, 255])
+    G.assert_close_block(G.to_f64(out256)[tokens],
+                         G.oracle_ffn(layer, h256, use_ids, use_wts, tokens=tokens),
+                         "vq_d4_tc M=256")
 
 
 VQLR_SMALL = [
@@ -522,29 +562,32 @@ def test_large_m256_sampled_tokens():
 
 
 def test_decode_block_picks_the_gemm_regime_for_large_batches():
-    """At 4+ routes per expert the library aligns in 64-row blocks (64-row tiles) whatever b
-    is, below that in 16-row blocks; the bits are the same either way."""
-    wl = syn.workload("layer_m21", M=64)
+    """From 24 routes per expert on the default layer (one wave of 16-row units' weights fits
+    in L2 there) the library aligns in 64-row blocks (64-row tiles) whatever b is, below
+    that in 16-row blocks; the bits are the same either way."""
+    wl = syn.workload("layer_m21", M=384)
     layer = _workload_layer("layer_m21")
-    h = syn.make_hidden(wl, M=64, seed=64, device=DEV)
+    assert moe.moe_library_block_size(layer, 384, wl.k, 8) == 64
+    assert moe.moe_library_block_size(layer, 64, wl.k, 8) == 16
+    h = syn.make_hidden(wl, M=384, seed=64, device=DEV)
     out8, ids, wts = moe.moe_decode_block(h, layer, wl.k, 8)
     out64, _, _ = moe.moe_decode_block(h, layer, wl.k, 64)
     assert torch.equal(out8, out64)  # the same regime, the same bits
     assert torch.equal(moe.moe_expert_ffn(h, layer, ids, wts, 8), out8)
-    tokens = np.array([0, 17, 63])
+    tokens = np.array([0, 170, 383])
     o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
     use_ids, use_wts, _ = G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts,
                                           logits, wl.k)
     ref = G.oracle_ffn(layer, h, use_ids, use_wts, tokens=tokens)
-    G.assert_close_block(G.to_f64(out8)[tokens], ref, "M=64, 64-row tiles")
-    # below the threshold (M=32: 2 routes per expert) 16-row tiles run: the same tokens keep
+    G.assert_close_block(G.to_f64(out8)[tokens], ref, "M=384, 64-row tiles")
+    # below the threshold (M=64: 4 routes per expert) 16-row tiles run: the same tokens keep
     # their bits, and so does a caller's own 8-row alignment
-    h32 = h[:32].contiguous()
-    o32, ids32, wts32 = moe.moe_decode_block(h32, layer, wl.k, 8)
-    assert torch.equal(ids32, ids[:32]) and torch.equal(o32, out8[:32])
-    srt, blk, npad = moe.moe_align_block_size(ids32, wl.E, 8)
-    assert torch.equal(moe.moe_expert_ffn(h32, layer, ids32, wts32, 8, alignment=(srt, blk, npad)),
-                       o32)
+    h64 = h[:64].contiguous()
+    o64, ids64, wts64 = moe.moe_decode_block(h64, layer, wl.k, 8)
+    assert torch.equal(ids64, ids[:64]) and torch.equal(o64, out8[:64])
+    srt, blk, npad = moe.moe_align_block_size(ids64, wl.E, 8)
+    assert torch.equal(moe.moe_expert_ffn(h64, layer, ids64, wts64, 8, alignment=(srt, blk, npad)),
+                       o64)
 
 
 def test_gemm_regime_batch_and_membership_invariance():
@@ -578,7 +621,8 @@ def test_route_bits_independent_of_batch_block_and_tile_width():
     ids = _random_ids(rng, M, k, E)
     a = _random_affinities(rng, M, k)
     t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
-    base = moe.moe_expert_ffn(h, layer, t_ids, t_a, 8)  # library: 64-row blocks (M*k >= 4E)
+    assert moe.moe_library_block_size(layer, M, k, 8) == 64
+    base = moe.moe_expert_ffn(h, layer, t_ids, t_a, 8)  # library: 64-row blocks
     ref = G.oracle_ffn(layer, h, ids, a)
     G.assert_close_block(G.to_f64(base), ref, "cross-regime base")
     for b in (1, 8, 16, 24, 64, 128):
@@ -618,16 +662,16 @@ def test_decode_block_on_a_dirty_workspace(M, b):
 
 
 def test_decode_block_bits_same_in_both_tile_widths():
-    """The default layer: M=21 runs 16-row tiles, M=64 64-row tiles; the 21 shared tokens
+    """The default layer: M=21 runs 16-row tiles, M=384 64-row tiles; the 21 shared tokens
     keep their routing and their output bits."""
     wl = syn.WORKLOADS["layer_m21"]
     layer = _workload_layer("layer_m21")
-    h64 = syn.make_hidden(wl, M=64, seed=5, device=DEV)
-    o64, i64, _ = moe.moe_decode_block(h64, layer, wl.k, wl.b)
-    o21, i21, _ = moe.moe_decode_block(h64[:21].contiguous(), layer, wl.k, wl.b)
-    o1, i1, _ = moe.moe_decode_block(h64[40:41].contiguous(), layer, wl.k, wl.b)
-    assert torch.equal(i21, i64[:21]) and torch.equal(o21, o64[:21])
-    assert torch.equal(i1[0], i64[40]) and torch.equal(o1[0], o64[40])
+    h384 = syn.make_hidden(wl, M=384, seed=5, device=DEV)
+    o384, i384, _ = moe.moe_decode_block(h384, layer, wl.k, wl.b)
+    o21, i21, _ = moe.moe_decode_block(h384[:21].contiguous(), layer, wl.k, wl.b)
+    o1, i1, _ = moe.moe_decode_block(h384[40:41].contiguous(), layer, wl.k, wl.b)
+    assert torch.equal(i21, i384[:21]) and torch.equal(o21, o384[:21])
+    assert torch.equal(i1[0], i384[40]) and torch.equal(o1[0], o384[40])
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
