@@ -38,7 +38,14 @@ constexpr int kRWords = kRB / 16;     // uint32 code words per block
 constexpr int kExactChunk = 8;        // selected channels per exact-read CTA (one per warp)
 constexpr int kSelectThreads = 1024;
 constexpr int kSketchWarps = 32;      // one 1024-thread CTA per SM: the scan and the table once
-constexpr int kTRow = 17;             // floats per 4-coordinate group of the nibble table (16 + pad)
+// Nibble table layout: the 16 sums of 4-coordinate group g = 8w + q (word w of a row covers
+// groups 8w .. 8w+7) for nibble n sit at nib_index(w, q, n), so that every lookup of the lane
+// that reads word w falls in bank w % 32 (one wavefront per warp-wide lookup, whatever the
+// nibbles); 4096 floats per 32 words.
+__host__ __device__ constexpr int nib_index(int w, int q, int n) {
+    return (w >> 5) * 4096 + (n * 8 + q) * 32 + (w & 31);
+}
+__host__ __device__ constexpr int nib_table_floats(int H) { return ((H / 32 + 31) / 32) * 4096; }
 
 // ------------------------------------------------------------------ rotation in a warp
 // A warp holds one 128-coordinate block, lane l coordinates 4l..4l+3 in v[0..3].  The
@@ -255,24 +262,36 @@ __global__ void __launch_bounds__(kSketchWarps * 32)
                          float *__restrict__ xr_out, const int32_t *__restrict__ ids,
                          const float *__restrict__ wts, int k, float *__restrict__ ahat,
                          float *__restrict__ score) {
-    extern __shared__ __align__(16) float T[];  // [H/4][kTRow], then xr [H]
+    extern __shared__ __align__(16) float T[];  // nibble table (nib_index), xr [H], xp [H/32][33]
     pdl_wait();
     pdl_launch_dependents();
     const int m = blockIdx.y, H = r.H, I = r.I, nb = H / kRB;
     const int N = k * I;
-    float *xr = T + (H / 4) * kTRow;
+    float *xr = T + nib_table_floats(H);
     for (int b = threadIdx.x >> 5; b < nb; b += kSketchWarps)
         scan_block(h + (size_t)m * H, r.signs, b, nscan, xr + b * kRB, threadIdx.x & 31);
     __syncthreads();
     if (blockIdx.x == 0)
         for (int c = threadIdx.x; c < H; c += blockDim.x) xr_out[(size_t)m * H + c] = xr[c];
-    for (int q = threadIdx.x; q < (H / 4) * 16; q += blockDim.x) {
-        const int g = q >> 4, n = q & 15;
-        float t = 0.0f;
+    // The table from a copy of xr padded to 33 floats per 32-coordinate word: the thread of
+    // (word w, group q) reads its 4 coordinates and writes its 16 sums, both bank-distinct
+    // across the warp's consecutive words.
+    const int W = H / 32;
+    float *xp = xr + H;  // [W][33]
+    for (int c = threadIdx.x; c < H; c += blockDim.x) xp[(c >> 5) * 33 + (c & 31)] = xr[c];
+    __syncthreads();
+    for (int t = threadIdx.x; t < 8 * W; t += blockDim.x) {
+        const int w = t % W, q = t / W;
+        const float *x4 = xp + w * 33 + 4 * q;
+        const float a[4] = {x4[0], x4[1], x4[2], x4[3]};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (n & (1 << c)) t += xr[4 * g + c];
-        T[g * kTRow + n] = t;
+        for (int n = 0; n < 16; ++n) {
+            float v = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (n & (1 << c)) v += a[c];
+            T[nib_index(w, q, n)] = v;
+        }
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -323,11 +342,11 @@ __global__ void __launch_bounds__(kSketchWarps * 32)
                 const uint32_t pos = nzw[p][ps] & ~ngw[p][ps], neg = nzw[p][ps] & ngw[p][ps];
                 float s = 0.0f;
                 if (w < nwords) {
-                    const float *Tw = T + (size_t)(w * 8) * kTRow;  // groups 8w .. 8w+7
+                    const float *Tw = T + nib_index(w, 0, 0);  // groups 8w .. 8w+7, bank w % 32
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        s += Tw[q * kTRow + ((pos >> (4 * q)) & 15u)] -
-                             Tw[q * kTRow + ((neg >> (4 * q)) & 15u)];
+                        s += Tw[(((pos >> (4 * q)) & 15u) * 8 + q) * 32] -
+                             Tw[(((neg >> (4 * q)) & 15u) * 8 + q) * 32];
                 }
                 // the block's four words, in order, then its scale
                 s += __shfl_xor_sync(0xffffffffu, s, 1);
@@ -760,7 +779,7 @@ cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, in
     trace_point(0, stream);
     {
         // the nibble table and xr
-        const size_t smem = ((size_t)(r.H / 4) * kTRow + r.H) * 4;
+        const size_t smem = ((size_t)nib_table_floats(r.H) + r.H + (size_t)(r.H / 32) * 33) * 4;
         const int npass = (r.H / 32 + 31) / 32;  // 32-coordinate words per lane and row
         auto kern = npass <= 1 ? reader_sketch_kernel<1>
                   : npass <= 2 ? reader_sketch_kernel<2>
