@@ -279,7 +279,9 @@ def run_ours(args, world, rank, local):
     # combine
     fused_align = 1 <= M <= 8 and M * wl.k <= 256
     gemm = gemm_regime(wl)
-    launches_per_block = ((4 if fused_align else 5) + (1 if gemm and not fused_align else 0)
+    # (up to 128 routes the alignment launch also writes the row tiles)
+    launches_per_block = ((4 if fused_align else 5)
+                          + (1 if gemm and not fused_align and M * wl.k > 128 else 0)
                           + (1 if wl.vq_form == 1 else 0))  # the projected code books: 2 kernels
 
     def eager_step(i, s):

@@ -6,6 +6,7 @@
 // The plan kernel turns a caller-supplied alignment into the sub-block table the expert
 // kernels read, checking every row against the top-k ids.
 #include "align_core.cuh"
+#include "moe_internal.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -82,6 +83,74 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, in
     cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kAlignThreads), smem, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, align_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
                               cap, sbt, rsub, status, staged_ints ? 1 : 0);
+}
+
+// Alignment and row tiles in one launch, for up to kAlignGatherRoutes routes (the tcgen05
+// path's tiles): every CTA aligns the routes itself (align_small, one thread per route, the
+// same stable order), CTA 0 writes the alignment, and all CTAs copy their share of the
+// valid routes' token rows into the K-major 128-byte-swizzle row tiles (16-byte pieces;
+// padding rows are left as they are: their columns are dropped by the epilogues).
+__global__ void __launch_bounds__(kAlignThreads)
+    align_gather_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int b,
+                        int32_t *__restrict__ sorted, int32_t *__restrict__ blocks,
+                        int32_t *__restrict__ npad, int64_t cap, int32_t *status,
+                        const __nv_bfloat16 *__restrict__ x, int H,
+                        __nv_bfloat16 *__restrict__ x_tiles, int kn, int tpb) {
+    __shared__ int32_t ids_s[kAlignGatherRoutes];
+    __shared__ int32_t pos_s[kAlignGatherRoutes];
+    __shared__ int32_t scratch[align_small_smem_ints(kAlignThreads)];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int R = M * k;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) ids_s[r] = ids[r];
+    __syncthreads();
+    const bool first = blockIdx.x == 0;
+    align_small(ids_s, R, k, E, b, b, first ? sorted : nullptr, first ? blocks : nullptr,
+                first ? npad : nullptr, cap, nullptr, first ? status : nullptr, scratch, pos_s);
+    __syncthreads();
+    const int pieces = H / 8;  // 16-byte pieces of a token row
+    const int64_t chunk_bytes = (int64_t)kn * 128;
+    const int64_t tile_bytes = (int64_t)(H / 64) * chunk_bytes;
+    unsigned char *xt = reinterpret_cast<unsigned char *>(x_tiles);
+    const int64_t total = (int64_t)R * pieces;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // 4 pieces per thread in flight at once, then their stores
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+        uint4 v[4];
+        int64_t dst[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t idx = i0 + u * stride;
+            dst[u] = -1;
+            if (idx >= total) continue;
+            const int r = (int)(idx / pieces), p = (int)(idx - (int64_t)r * pieces);
+            const int pos = pos_s[r];
+            if (pos < 0) continue;
+            const int local = pos % b;
+            const int64_t t = (int64_t)(pos / b) * tpb + local / kn;
+            const int n = local % kn;
+            dst[u] = t * tile_bytes + (p >> 3) * chunk_bytes + tile_offset(n, p & 7);
+            v[u] = *reinterpret_cast<const uint4 *>(x + (size_t)(r / k) * H + (size_t)p * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (dst[u] >= 0) *reinterpret_cast<uint4 *>(xt + dst[u]) = v[u];
+    }
+}
+
+cudaError_t launch_align_gather(const int32_t *topk_ids, int M, int k, int E, int b,
+                                int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
+                                int32_t *status, const __nv_bfloat16 *x, int H,
+                                const RowTiles &rows, cudaStream_t stream) {
+    const int R = M * k;
+    if (R < 1 || R > kAlignGatherRoutes || !rows.x_tiles) return cudaErrorInvalidValue;
+    const int64_t work = (int64_t)R * (H / 8);
+    int grid = (int)((work + 4 * kAlignThreads - 1) / (4 * kAlignThreads));
+    grid = grid < 1 ? 1 : (grid > num_sms() ? num_sms() : grid);
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(grid), dim3(kAlignThreads), 0, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, align_gather_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
+                              cap, status, x, H, rows.x_tiles, rows.kn, rows.tpb);
 }
 
 cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const int32_t *blocks,

@@ -589,11 +589,20 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     SubBlock *sbt = reinterpret_cast<SubBlock *>(ws + L.sbt);
     cudaError_t err;
+    bool rows_ready = false;  // the alignment launch also wrote the row tiles
     if (given == 0) {
         int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
-        err = launch_align(topk_ids, M, k, w->E, b, reinterpret_cast<int32_t *>(ws + L.sorted),
-                           reinterpret_cast<int32_t *>(ws + L.blocks), ws_npad, d.cap,
-                           d.gemm ? nullptr : sbt, d.rsub, status, s);
+        int32_t *ws_sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+        int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
+        if (d.gemm && (int64_t)M * k <= kAlignGatherRoutes) {
+            const RowTiles rows{reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles), d.kn, d.tpb};
+            err = launch_align_gather(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                                      status, static_cast<const __nv_bfloat16 *>(h), w->H, rows, s);
+            rows_ready = true;
+        } else {
+            err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                               d.gemm ? nullptr : sbt, d.rsub, status, s);
+        }
         npad = ws_npad;
     } else {
         if (!aligned(sorted_route_ids, 4) || !aligned(expert_block_ids, 4) || !aligned(num_padded, 4))
@@ -614,7 +623,8 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     trace(2, s);
     const int32_t *srt = given ? sorted_route_ids : reinterpret_cast<const int32_t *>(ws + L.sorted);
     const int32_t *blk = given ? expert_block_ids : reinterpret_cast<const int32_t *>(ws + L.blocks);
-    return run_experts(h, w, d, topk_ids, topk_weights, srt, blk, npad, residual, out, ws, L, s);
+    return run_experts(h, w, d, topk_ids, topk_weights, srt, blk, npad, residual, out, ws, L, s,
+                       rows_ready);
 }
 
 int moe::decode_block(const void *h, const void *w_router, const float *bias,
@@ -647,6 +657,7 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
     const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store);  // rides in the router launch
     cudaError_t err;
     const bool fused = router_can_align(M, k);
+    bool rows_ready = fused && d.gemm;  // x tiles written before the expert kernels
     if (fused) {  // one launch routes, aligns and (dense weights) writes the x tiles
         RowTiles rows{nullptr, d.kn, d.tpb};
         if (d.gemm) rows.x_tiles = reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles);
@@ -662,13 +673,21 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
                             topk_ids, topk_weights, lr, s);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
-        err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
-                           d.gemm ? nullptr : ws_sbt, d.rsub, ws_status, s);
+        if (d.gemm && (int64_t)M * k <= kAlignGatherRoutes) {
+            const RowTiles rows{reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles), d.kn, d.tpb};
+            err = launch_align_gather(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                                      ws_status, static_cast<const __nv_bfloat16 *>(h), w->H, rows,
+                                      s);
+            rows_ready = true;
+        } else {
+            err = launch_align(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
+                               d.gemm ? nullptr : ws_sbt, d.rsub, ws_status, s);
+        }
         if (err != cudaSuccess) return MOE_ERR_CUDA;
     }
     trace(2, s);
     return run_experts(h, w, d, topk_ids, topk_weights, ws_sorted, ws_blocks, ws_npad, residual, out,
-                       ws, L, s, fused && d.gemm);
+                       ws, L, s, rows_ready);
 }
 
 extern "C" int moe_decode_block(const void *h, const void *w_router, const float *bias,

@@ -257,6 +257,14 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b,
                          int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
                          SubBlock *sbt, int rsub, int32_t *status, cudaStream_t stream);
 
+// Alignment and the row tiles of the tcgen05 path in one launch (M * k <= 128 routes: above
+// that the per-CTA alignment, quadratic in the routes, costs more than the launch it saves).
+constexpr int kAlignGatherRoutes = 128;
+cudaError_t launch_align_gather(const int32_t *topk_ids, int M, int k, int E, int b,
+                                int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
+                                int32_t *status, const __nv_bfloat16 *x, int H,
+                                const RowTiles &rows, cudaStream_t stream);
+
 // Sub-block table from a caller-supplied alignment, checking each row against topk_ids.
 cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const int32_t *blocks,
                         const int32_t *npad, int M, int k, int E, int b, int rsub,
