@@ -187,15 +187,15 @@ int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
 /*
  * The whole block: router (renormalised softmax top-k) -> alignment -> expert FFN ->
  * combine.  Same arguments as above; topk_ids [M,k] and topk_weights [M,k] are outputs.
- * Dense weights run as grouped GEMMs on the tensor cores over tiles of the aligned blocks:
- * 16-row tiles for blocks of up to 16 rows, 64-row tiles otherwise.  When the library
- * aligns the routes itself (here, and in moe_expert_ffn without a caller alignment) it
- * picks the block size for dense weights: 64 rows from 4 routes per expert on average
- * (M*k >= 4E), 16 rows below; b only matters for a caller's own alignment.  Every route of
- * dense weights is one K-ordered chain of MMAs per projection, so a token's output bits do
- * not depend on M, on the other tokens, on its block or its position in it, on b or on the
- * tile width.  VQ gate/up weights run as GEMV streams on the CUDA cores with the caller's b;
- * their results are bitwise reproducible and independent of M and of block membership.
+ * Dense weights (and VQ weights with vq_form 2) run as grouped GEMMs on the tensor cores
+ * over tiles of the aligned blocks: 16-row tiles for blocks of up to 16 rows, 64-row tiles
+ * otherwise.  When the library aligns the routes itself (here, and in moe_expert_ffn without
+ * a caller alignment) it picks the block size, 16 or 64 rows, by routes per expert
+ * (moe_library_block_size); b only matters for a caller's own alignment.  Every route is
+ * one K-ordered chain of MMAs per projection, so a token's output bits do not depend on M,
+ * on the other tokens, on its block or its position in it, on b or on the tile width.  VQ
+ * gate/up weights with vq_form 0 or 1 run on the CUDA cores with the caller's b; their
+ * results are bitwise reproducible and independent of M and of block membership.
  */
 int moe_decode_block(const void *h, const void *w_router, const float *bias,
                      const moe_expert_weights_t *w, int M, int k, int b,

@@ -88,9 +88,10 @@ struct GemvArgs {
     int64_t max_sub;       // rows of the sub-block table
 };
 
-// Dense weights: grouped GEMMs on tcgen05 over tiles of kn aligned rows of one expert.  An
-// aligned block of b rows is cut into tpb = ceil(b / kn) tiles, kn = 16 for b <= 16, else 64.
-// The library aligns with 64-row blocks from 4 routes per expert on, else with 16-row ones.
+// Dense weights (and VQ decoded on the tensor cores): grouped GEMMs on tcgen05 over tiles
+// of kn aligned rows of one expert.  An aligned block of b rows is cut into tpb = ceil(b / kn)
+// tiles, kn = 16 for b <= 16, else 64.  The library picks 16- or 64-row blocks by routes per
+// expert (effective_block in api.cu).
 constexpr int kGemmBlock = 64;
 constexpr int kGemmNarrow = 16;
 
