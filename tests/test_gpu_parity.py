@@ -163,6 +163,27 @@ def test_expert_ffn_invalid_ids_and_status():
     assert torch.equal(out[2], res[2])
 
 
+def test_vq_tensor_core_invalid_ids_and_status():
+    """VQ decoded on the tensor cores with ids outside [0, E): those routes are dropped and
+    flagged (the one-launch alignment raises the status bit), the rest match the oracle."""
+    M, k, E, H, I, b = 6, 3, 16, 1024, 256, 4
+    wl = syn.Workload("vq_tc_invalid", H=H, I=I, E=E, k=k, b=b, M=M, kind=syn.W_VQ, d=4, K=256,
+                      vq_form=2)
+    layer = syn.make_layer(wl, seed=17, device=DEV)
+    h = syn.make_hidden(wl, seed=17, device=DEV)
+    ids = np.array([[0, -1, 5], [16, 2, 3], [-5, -1, 99], [7, 7, 1], [15, 0, 4], [9, 10, 11]],
+                   np.int32)
+    a = _random_affinities(np.random.default_rng(2), M, k)
+    res = syn.make_hidden(wl, seed=18, device=DEV, tag="res")
+    ws = moe.alloc_workspace(layer, M, k, b)
+    out = moe.moe_expert_ffn(h, layer, torch.as_tensor(ids, device=DEV),
+                             torch.as_tensor(a, device=DEV), b, residual=res, workspace=ws)
+    assert moe.moe_read_device_status(ws) & moe.MOE_DEV_INVALID_EXPERT
+    G.assert_close_block(G.to_f64(out), G.oracle_ffn(layer, h, ids, a, residual=res),
+                         "vq tensor cores, invalid ids")
+    assert torch.equal(out[2], res[2])
+
+
 @pytest.mark.parametrize("b", [2, 64])
 def test_expert_ffn_bad_alignment_is_flagged(b):
     M, k, E, H, I = 4, 2, 8, 256, 256
