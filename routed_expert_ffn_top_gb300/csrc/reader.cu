@@ -196,11 +196,10 @@ cudaError_t launch_reader_build(const ReaderArgs &r, const __nv_bfloat16 *w_gate
 // an unsigned integer order like the non-negative floats), counting with warp ballots; the
 // coordinates equal to it are then taken in index order.  xr: where the block's 128 values
 // go (shared memory).
-__device__ __forceinline__ void scan_block(const __nv_bfloat16 *hm, const int8_t *signs, int b,
-                                           int nscan, float *xr, int lane) {
+__device__ __forceinline__ void scan_block(const __nv_bfloat16 *hm, char4 sg, int b, int nscan,
+                                           float *xr, int lane) {
     const int c0 = b * kRB + 4 * lane;
     const uint2 raw = *reinterpret_cast<const uint2 *>(hm + c0);
-    const char4 sg = *reinterpret_cast<const char4 *>(signs + c0);
     float v[4] = {bf16_lo(raw.x) * sg.x, bf16_hi(raw.x) * sg.y, bf16_lo(raw.y) * sg.z,
                   bf16_hi(raw.y) * sg.w};
     fwht128_warp(v, lane);
@@ -218,6 +217,9 @@ __device__ __forceinline__ void scan_block(const __nv_bfloat16 *hm, const int8_t
 #pragma unroll
             for (int q = 0; q < 4; ++q) cnt += __popc(__ballot_sync(0xffffffffu, key[q] >= cand));
             if (cnt >= nscan) t = cand;
+            // exactly nscan keys at or above the candidate: they are the nscan largest and
+            // every other key is below them, so the lower bits cannot change the kept set
+            if (cnt == nscan) break;  // uniform across the warp (ballot counts)
         }
         int above = 0;
 #pragma unroll
@@ -263,13 +265,21 @@ __global__ void __launch_bounds__(kSketchWarps * 32)
                          const float *__restrict__ wts, int k, float *__restrict__ ahat,
                          float *__restrict__ score) {
     extern __shared__ __align__(16) float T[];  // nibble table (nib_index), xr [H], xp [H/32][33]
+    // the rotation signs of this warp's first block are weights: load them before the wait
+    const int nb0 = r.H / kRB;
+    char4 sg0 = make_char4(0, 0, 0, 0);
+    if ((int)(threadIdx.x >> 5) < nb0)
+        sg0 = *reinterpret_cast<const char4 *>(r.signs + (threadIdx.x >> 5) * kRB + 4 * (threadIdx.x & 31));
     pdl_wait();
     pdl_launch_dependents();
     const int m = blockIdx.y, H = r.H, I = r.I, nb = H / kRB;
     const int N = k * I;
     float *xr = T + nib_table_floats(H);
-    for (int b = threadIdx.x >> 5; b < nb; b += kSketchWarps)
-        scan_block(h + (size_t)m * H, r.signs, b, nscan, xr + b * kRB, threadIdx.x & 31);
+    for (int b = threadIdx.x >> 5; b < nb; b += kSketchWarps) {
+        const char4 sg = b == (int)(threadIdx.x >> 5) ? sg0 : *reinterpret_cast<const char4 *>(
+                                                               r.signs + b * kRB + 4 * (threadIdx.x & 31));
+        scan_block(h + (size_t)m * H, sg, b, nscan, xr + b * kRB, threadIdx.x & 31);
+    }
     __syncthreads();
     if (blockIdx.x == 0)
         for (int c = threadIdx.x; c < H; c += blockDim.x) xr_out[(size_t)m * H + c] = xr[c];
