@@ -277,7 +277,7 @@ def run_ours(args, world, rank, local):
     # router (+ alignment, and the row tiles of the grouped GEMMs, when one router cluster
     # holds every token), else alignment [+ row gather for dense weights]; gate/up, down,
     # combine
-    fused_align = 1 <= M <= 8 and M * wl.k <= 256
+    fused_align = 1 <= M <= 2 and M * wl.k <= 256
     gemm = gemm_regime(wl)
     # (up to 128 routes the alignment launch also writes the row tiles)
     launches_per_block = ((4 if fused_align else 5)
