@@ -16,9 +16,9 @@
 // and one warp runs the top-k (ties to the lower expert id) and the softmax.  The order
 // depends on (H, E) only, so a token's logits are the same for every M.
 //
-// When one cluster holds every token (M <= 2 on the decode path) the same kernel also runs the alignment
-// (align_core.cuh) in the CTA of rank 0 on the ids it gathers from the cluster, which saves
-// the alignment launch on the decode path.
+// When one cluster holds every token (M <= 2 on the decode path) the same kernel also runs
+// the alignment (align_core.cuh) in the CTA of rank 0 on the ids it gathers from the
+// cluster, which saves the alignment launch.
 #include <float.h>
 
 #include "align_core.cuh"
