@@ -65,6 +65,8 @@ def parse_args():
     p.add_argument("--weight-sets", type=int, default=8,
                    help="independent weight sets cycled by single-layer workloads")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per-configuration entries (the other configurations' timings)")
     p.add_argument("--no-extras", action="store_true",
                    help="time the block only (no trace, e2e, CPU baseline): for profilers")
     return p.parse_args()
@@ -206,10 +208,18 @@ def gateup_kernel_name(wl) -> str:
     return "vq_ttable_partial_kernel" if wl.vq_form == 1 else "gateup_vq_kernel"
 
 
-def kernel_source_hash(kernel: str = "gemm_gateup_kernel"):
+KERNEL_SOURCES = {
+    "decode_small_kernel": ("decode_small.cu", "gemm_core.cuh", "route_core.cuh", "align_core.cuh"),
+    "gemm_fused_kernel": ("gemm_tc05.cu", "gemm_core.cuh"),
+    "gemm_gateup_vq_kernel": ("gemm_tc05.cu", "gemm_core.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = "gemm_fused_kernel"):
+    """Hash of the sources a kernel is built from (its traffic record is void once they change)."""
     h = hashlib.sha256()
-    src = "gemm_tc05.cu" if kernel.startswith("gemm_") else "gemv.cu"
-    for name in (src, "ptx.cuh", "moe_internal.cuh"):
+    srcs = KERNEL_SOURCES.get(kernel, ("gemv.cu",))
+    for name in srcs + ("ptx.cuh", "moe_internal.cuh"):
         with open(os.path.join(ROOT, "routed_expert_ffn_top_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -254,6 +264,188 @@ def shared_bytes(wl):
     return b
 
 
+def surface_hashes(moe, layer, wl, M, h, ws, ids, out):
+    """SHA-256 of the block's surfaces after one call (the route-block page's exact-trajectory
+    record): the activation p = SiLU(g) * u (bf16) and the routed down outputs y (fp32) of the
+    valid routes in ascending route order, and the final output (bf16).  The gate/up GEMM's
+    own output (g, u) is never stored on this path: SiLU and the product are applied to the
+    accumulators."""
+    lay = moe.moe_workspace_layout(layer, M, wl.k, wl.b)
+    R, I, H = M * wl.k, wl.I, wl.H
+    idl = ids.flatten().long()
+    valid = torch.nonzero((idl >= 0) & (idl < wl.E)).flatten()
+    y = ws[lay["y"]:lay["y"] + R * H * 4].view(torch.float32).view(R, H)[valid]
+    if lay["p_rows"]:
+        p = ws[lay["p_rows"]:lay["p_rows"] + R * I * 2].view(torch.bfloat16).view(R, I)[valid]
+    else:  # the swizzled p tiles: row n of tile t, 64-wide chunk c, 16-byte piece j
+        srt, _, _ = moe.workspace_alignment(ws, lay)
+        b, kn, tpb = lay["b"], lay["kn"], lay["tpb"]
+        pos = torch.full((R,), -1, dtype=torch.long, device=ws.device)
+        srt_l = srt.long()
+        rows = torch.nonzero((srt_l >= 0) & (srt_l < R)).flatten()
+        pos[srt_l[rows]] = rows
+        pv = pos[valid]
+        t = (pv // b) * tpb + (pv % b) // kn
+        n = (pv % b) % kn
+        c = torch.arange(I // 64, device=ws.device)
+        j = torch.arange(8, device=ws.device)
+        off = (t[:, None, None] * (I // 64) * kn * 128 + c[None, :, None] * kn * 128
+               + n[:, None, None] * 128 + ((j[None, None, :] ^ (n[:, None, None] & 7)) << 4))
+        pieces = ws[lay["p_tiles"]:].view(-1)
+        byte_idx = (off[..., None] + torch.arange(16, device=ws.device)).reshape(len(pv), -1)
+        p = pieces[byte_idx].contiguous().view(torch.bfloat16).view(len(pv), I)
+    digest = lambda t: hashlib.sha256(t.contiguous().cpu().numpy().tobytes()).hexdigest()  # noqa: E731
+    return {"w13": "not stored (SiLU(g) * u formed in the gate/up epilogue)",
+            "activation": digest(p), "routed_w2": digest(y), "final": digest(out)}
+
+
+def block_launches(layer, wl, M):
+    """Kernels one moe_decode_block call launches (the library's own count)."""
+    from routed_expert_ffn_top_gb300 import moe
+    return moe.moe_workspace_layout(layer, M, wl.k, wl.b)["launches"]
+
+
+# The configurations of the headline metric, each measured in its own timed region: the
+# decode layer at 1 and 21 tokens, the 48-layer stack at 1, 4, 16 and 64 tokens, the VQ layer
+# at 1 to 16 tokens, and the large-batch layer.
+PER_CONFIG = [("layer_m1", 1), ("layer_m21", 21), ("stack48", 1), ("stack48", 4),
+              ("stack48", 16), ("stack48", 64), ("vq_d4", 1), ("vq_d4", 2), ("vq_d4", 4),
+              ("vq_d4", 8), ("vq_d4", 16), ("large_m256", 256)]
+
+
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def near_tie_counts(inputs):
+    """Tokens of each configuration whose routing is a near tie: the oracle's fp64 margin
+    between the k-th and (k+1)-th logit below 1e-4 (where fp32 rounding may legitimately pick
+    differently).  inputs: key -> (h, [layers]) as the configurations ran; the count is over
+    the tokens of h against each layer's router."""
+    import oracle
+    out = {}
+    for key, (h, layers) in inputs.items():
+        n = 0
+        for layer in layers:
+            bias = layer.get("bias")
+            bias = None if bias is None else bias.detach().cpu().numpy()
+            logits = oracle.router_logits(syn.bits(h), syn.bits(layer["w_router"]), bias,
+                                          h.shape[0], layer["H"], layer["E"])
+            k = layer.get("k", 8)
+            _, _, gap = oracle.topk_softmax(logits, k)
+            n += int((gap < 1e-4).sum())
+        out[key] = n
+    return out
+
+
+def per_config_entries(dev, local, min_seconds=0.4, near_inputs=None):
+    """µs per layer, tokens/s and HBM fractions of every configuration, each timed with CUDA
+    events over whole steps (a step = one layer, or the 48 layers of the stack) after
+    warm-up, with its own clock samples.  Single layers cycle 8 independently drawn weight
+    sets (9.7 GB, or 38.6 GB at H=4096), the stack reads 48 distinct layers (58 GB): every
+    step's expert weights come from HBM.  Blocks align with the configuration's own b."""
+    from routed_expert_ffn_top_gb300 import moe
+
+    peak, _ = measured_peaks()
+    tpeak, _ = measured_bf16_tflops()
+    stream = torch.cuda.current_stream()
+    entries = {}
+    cache = {}
+    for name, M in PER_CONFIG:
+        wl = syn.workload(name, M=M)
+        if cache.get("name") != name:
+            cache.clear()
+            torch.cuda.empty_cache()
+            n_sets = wl.layers if wl.layers > 1 else 8
+            cache["name"] = name
+            cache["layers"] = [syn.make_layer(wl, layer=i, seed=1, device=dev) for i in range(n_sets)]
+        layers = cache["layers"]
+        stack = wl.layers > 1
+        h0 = syn.make_hidden(wl, M=M, seed=1, device=dev)
+        ws = moe.alloc_workspace(layers[0], M, wl.k, wl.b, dev)
+        out = [torch.empty_like(h0) for _ in range(2)]
+        ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
+        wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
+
+        def step(i):
+            if stack:
+                h = h0
+                for li, layer in enumerate(layers):
+                    moe.moe_decode_block(h, layer, wl.k, wl.b, residual=h, out=out[li % 2],
+                                         topk_ids=ids, topk_weights=wts, workspace=ws)
+                    h = out[li % 2]
+            else:
+                moe.moe_decode_block(h0, layers[i % len(layers)], wl.k, wl.b, out=out[0],
+                                     topk_ids=ids, topk_weights=wts, workspace=ws)
+
+        # routing of every weight set, or of every layer of the stack (the bytes a step streams)
+        uniq, npad_rows = [], []
+        b_used = moe.moe_library_block_size(layers[0], M, wl.k, wl.b)
+        h = h0
+        for li, layer in enumerate(layers):
+            moe.moe_decode_block(h, layer, wl.k, wl.b, residual=h if stack else None,
+                                 out=out[li % 2], topk_ids=ids, topk_weights=wts, workspace=ws)
+            if stack:
+                h = out[li % 2]
+            uniq.append(int(torch.unique(ids).numel()))
+            n_e = torch.bincount(ids.flatten().long(), minlength=wl.E)
+            npad_rows.append(int(((n_e + b_used - 1) // b_used * b_used).sum().item()))
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step(0)
+        torch.cuda.synchronize()
+        per_step = max(time.perf_counter() - t0, 1e-6)
+        steps = int(max(10, min(20000, min_seconds / per_step)))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            for i in range(steps):
+                step(i)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+        t_ms = ev0.elapsed_time(ev1)
+        if moe.moe_read_device_status(ws) != 0:
+            raise RuntimeError("device status set in the %s M=%d entry" % (name, M))
+        layers_per_step = len(layers) if stack else 1
+        us_layer = t_ms * 1e3 / (steps * layers_per_step)
+        gu_b, dn_b = expert_bytes(wl)
+        u_mean = statistics.mean(uniq)
+        gbs = (u_mean * (gu_b + dn_b) + shared_bytes(wl)) / (us_layer * 1e-6) / 1e9
+        e = {"workload": name, "M": M, "b": wl.b, "b_effective": b_used, "steps": steps,
+             "us_per_layer": round(us_layer, 3),
+             "tokens_per_s": round(M / (us_layer * 1e-6 * layers_per_step), 2),
+             "unique_experts_per_layer": round(u_mean, 2),
+             "hbm_gbs_unique_expert_bytes": round(gbs, 1),
+             "hbm_frac": {"measured": round(gbs / peak, 4),
+                          "nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)},
+             "gpu_launches": block_launches(layers[0], wl, M) * layers_per_step * steps,
+             "clocks": clk.summary()}
+        if gemm_regime(wl):
+            npad = statistics.mean(npad_rows)
+            gu_flop = 2.0 * npad * (2 * wl.H * wl.I if wl.kind == syn.W_DENSE else 0)
+            flops = gu_flop + 2.0 * npad * wl.I * wl.H
+            e["tensor_tflops_issued"] = round(flops / (us_layer * 1e-6) / 1e12, 2)
+            e["tensor_frac_measured"] = round(flops / (us_layer * 1e-6) / 1e12 / tpeak, 4)
+        entries["%s_M%d" % (name, M)] = e
+        if near_inputs is not None:
+            router = {"H": wl.H, "E": wl.E, "k": wl.k, "w_router": layers[0]["w_router"].cpu(),
+                      "bias": None if layers[0].get("bias") is None else layers[0]["bias"].cpu()}
+            near_inputs["%s_M%d" % (name, M)] = (h0.cpu(), [router])
+        del ws, out, h0
+    cache.clear()
+    torch.cuda.empty_cache()
+    return entries
+
+
 # ------------------------------------------------------------------------------ ours
 def run_ours(args, world, rank, local):
     from routed_expert_ffn_top_gb300 import build as lib_build
@@ -277,12 +469,9 @@ def run_ours(args, world, rank, local):
     # router (+ alignment, and the row tiles of the grouped GEMMs, when one router cluster
     # holds every token), else alignment [+ row gather for dense weights]; gate/up, down,
     # combine
-    fused_align = 1 <= M <= 2 and M * wl.k <= 256
     gemm = gemm_regime(wl)
-    # (up to 128 routes the alignment launch also writes the row tiles)
-    launches_per_block = ((4 if fused_align else 5)
-                          + (1 if gemm and not fused_align and M * wl.k > 128 else 0)
-                          + (1 if wl.vq_form == 1 else 0))  # the projected code books: 2 kernels
+    launches_per_block = block_launches(layers[0], wl, M)
+    one_kernel = launches_per_block == 1
 
     def eager_step(i, s):
         """One step: a single layer, or all L layers of the residual stack."""
@@ -480,30 +669,46 @@ def run_ours(args, world, rank, local):
     mean_ms = {k: statistics.mean(v) for k, v in dur.items()}
     peak, peak_kind = measured_peaks()
     u_mean = statistics.mean(per_set_unique)
-    # weights of the routed experts + h read once + p written (fp32 per route from the VQ
-    # kernel, bf16 per route from the tcgen05 one)
-    gu_kernel = gateup_kernel_name(wl)
     p_bytes = 2 if gemm else 4
-    gu_alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * p_bytes
-    achieved = gu_alg / (mean_ms["gateup"] * 1e-3) / 1e9
-    traffic = recorded_traffic(gu_kernel, wl.name, u_mean)
+    if one_kernel:
+        # the whole block in one grid: the routed experts' weights and W_r in, h in, out back
+        kernel = "decode_small_kernel"
+        alg = u_mean * (gu_b + dn_b) + shared_bytes(wl) + 2 * M * wl.H * 2
+        k_ms = sum(mean_ms.values())
+    elif wl.kind == syn.W_DENSE:
+        # gate/up and down in one grid (its trace interval is the gate/up one): the routed
+        # experts' weights, h rows in, p out and back, y out
+        kernel = "gemm_fused_kernel"
+        alg = (u_mean * (gu_b + dn_b) + M * wl.H * 2 + 2 * M * wl.k * wl.I * p_bytes
+               + M * wl.k * wl.H * 4)
+        k_ms = mean_ms["gateup"] + mean_ms["down"]
+    else:
+        # weights of the routed experts + h read once + p written (fp32 per route from the VQ
+        # kernels on the CUDA cores, bf16 per route from the tensor-core one)
+        kernel = gateup_kernel_name(wl)
+        alg = u_mean * gu_b + M * wl.H * 2 + M * wl.k * wl.I * p_bytes
+        k_ms = mean_ms["gateup"]
+    achieved = alg / (k_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(kernel, wl.name, u_mean)
     result["roofline"] = {
-        "kernel": gu_kernel, "bound": "hbm", "achieved": round(achieved, 1),
+        "kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
         "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
         "frac_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         "traffic": None if traffic is None else int(traffic),
-        "algorithmic_bytes_per_launch": int(gu_alg),
+        "algorithmic_bytes_per_launch": int(alg),
+        "kernel_ms": round(k_ms, 5),
         "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
     }
-    dn_alg = u_mean * dn_b + M * wl.k * (wl.I * p_bytes + wl.H * 4)
-    result["down_kernel_gbs"] = round(dn_alg / (mean_ms["down"] * 1e-3) / 1e9, 1)
+    if not one_kernel and wl.kind != syn.W_DENSE:
+        dn_alg = u_mean * dn_b + M * wl.k * (wl.I * p_bytes + wl.H * 4)
+        result["down_kernel_gbs"] = round(dn_alg / (mean_ms["down"] * 1e-3) / 1e9, 1)
     if gemm:
         # tensor work actually issued: every aligned row, valid or padding, x 2 flops per MAC
         npad = float(sum(padded_rows) / len(padded_rows))
-        result["roofline"]["tensor_tflops_issued"] = round(
-            2 * npad * 2 * wl.H * wl.I / (mean_ms["gateup"] * 1e-3) / 1e12, 1)
-        # the trace point between alignment and gate/up is recorded after the row gather
-        result["roofline"]["row_gather_in_align_interval"] = not fused_align
+        flops = 2 * npad * (2 * wl.H * wl.I if wl.kind == syn.W_DENSE else 0)
+        if wl.kind == syn.W_DENSE:
+            flops += 2 * npad * wl.I * wl.H
+        result["roofline"]["tensor_tflops_issued"] = round(flops / (k_ms * 1e-3) / 1e12, 1)
 
     # --- e2e: host h in, host out back, copies inside the timed region
     h_host = h0.cpu().pin_memory()
@@ -534,9 +739,32 @@ def run_ours(args, world, rank, local):
     result["e2e"] = {"value": round(M * args.steps * world / t_e2e, 3), "unit": UNIT,
                      "h2d_bytes_per_step": M * wl.H * 2, "d2h_bytes_per_step": M * wl.H * 2}
 
-    # --- CPU baseline: the oracle on a bounded sample (rank 0 only, N = 1 only)
+    # --- the exact-trajectory record: surface hashes of two calls on the same inputs
+    hashes = []
+    for _ in range(2):
+        ws.zero_()
+        o = torch.empty_like(h0)
+        moe.moe_decode_block(h0, layers[0], wl.k, wl.b, out=o, topk_ids=ids, topk_weights=wts,
+                             workspace=ws)
+        torch.cuda.synchronize()
+        hashes.append(surface_hashes(moe, layers[0], wl, M, h0, ws, ids, o))
+    result["surface_hashes"] = dict(hashes[0], repeat_identical=hashes[0] == hashes[1])
+    result["config"]["b_effective"] = moe.moe_library_block_size(layers[0], M, wl.k, wl.b)
+    result["config"]["launches_per_layer"] = launches_per_block
+
+    # --- every configuration of the metric, each in its own timed region (N = 1 only)
+    near_inputs = {wl.name + "_M%d" % M: (h0, [dict(layers[0], k=wl.k)])}
+    if world == 1 and not args.no_per_config:
+        result["per_config"] = per_config_entries(dev, local, near_inputs=near_inputs)
+
+    # --- CPU baseline: the oracle on a bounded sample (rank 0 only, N = 1 only), and the
+    # oracle's count of near-tie tokens of each configuration's routing
     if rank == 0 and world == 1:
         result["cpu_baseline"] = cpu_baseline(wl, layers[0], h0, args.cpu_seconds)
+        nt = near_tie_counts(near_inputs)
+        result["near_tie_tokens"] = nt.get(wl.name + "_M%d" % M)
+        for key, entry in result.get("per_config", {}).items():
+            entry["near_tie_tokens"] = nt.get(key)
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -553,6 +781,17 @@ def reader_bytes(wl, nvalid_channels, kept):
     return sketch, exact, recover
 
 
+def reader_basis(w_down: torch.Tensor, rank: int = 32) -> torch.Tensor:
+    """The reader's recovery basis U [H, rank] fp32 -- model data the caller supplies, built
+    once per layer offline, not part of the decode path: the top left singular vectors of the
+    H x (E I) matrix of down columns, from the eigenvectors of D^T D (torch's symmetric
+    eigensolver on the host)."""
+    D = w_down.reshape(-1, w_down.shape[-1]).to(torch.float64)
+    evals, evecs = torch.linalg.eigh((D.T @ D).cpu())  # H x H
+    order = torch.argsort(evals, descending=True, stable=True)[:rank]
+    return evecs[:, order].to(device=w_down.device, dtype=torch.float32).contiguous()
+
+
 def run_reader(args, world, rank, local, wl):
     from routed_expert_ffn_top_gb300 import moe
 
@@ -563,7 +802,7 @@ def run_reader(args, world, rank, local, wl):
     for li in range(n_sets):
         layer = syn.make_layer(wl, layer=li, seed=1 + rank, device=dev)
         signs = syn.make_rotation_signs(wl.H, seed=li, device=dev)
-        U = moe.reader_basis(layer["w_down"], wl.reader_rank)  # offline, once per layer
+        U = reader_basis(layer["w_down"], wl.reader_rank)  # offline, once per layer
         readers.append(moe.reader_build(layer, signs, U))
         layers.append(layer)
     torch.cuda.synchronize()
@@ -735,7 +974,7 @@ def _oracle_block_sample(wl, layer, h, tokens):
     logits = oracle.router_logits(hb, wr, bias, tokens, wl.H, wl.E)
     ids, _, _ = oracle.topk_softmax(logits, wl.k)
     used = sorted(set(ids.reshape(-1).tolist()))
-    w = syn.oracle_weights(layer, used)
+    w = oracle.host_weights(layer, used)
     remap = {e: i for i, e in enumerate(used)}
     return hb, wr, bias, w, remap
 
@@ -752,19 +991,35 @@ def _time_oracle_block(wl, hb, wr, bias, w, remap, tokens):
 
 
 def cpu_baseline(wl, layer, h, seconds):
+    """The fp64 oracle on a bounded sample of the batch, timed single-threaded and on all the
+    host's cores (OpenMP over routes; the results do not depend on the thread count)."""
     import oracle
     oracle.build()
     # a bounded sample: whole passes over at most 32 tokens of the batch
     tokens = min(h.shape[0], 32)
     hb, wr, bias, w, remap = _oracle_block_sample(wl, layer, h, tokens)
-    total, n = 0.0, 0
-    while total < seconds or n == 0:
-        total += _time_oracle_block(wl, hb, wr, bias, w, remap, tokens)
-        n += 1
-    return {"value": round(tokens * n / total, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d passes of the %s block over %d of its %d tokens (router, all their "
-                      "routed experts, combine), single-threaded fp64 C oracle, %.1f s"
-                      % (n, wl.name, tokens, h.shape[0], total)}
+    ncpu = os.cpu_count() or 1
+    before = oracle.set_threads(0)
+    legs = {}
+    try:
+        for name, threads in (("single_thread", 1), ("all_cores", ncpu)):
+            used = oracle.set_threads(threads)
+            total, n = 0.0, 0
+            while total < seconds / 2 or n == 0:
+                total += _time_oracle_block(wl, hb, wr, bias, w, remap, tokens)
+                n += 1
+            legs[name] = {"value": round(tokens * n / total, 4), "threads": used, "passes": n,
+                          "seconds": round(total, 2)}
+    finally:
+        oracle.set_threads(before)
+    best = legs["all_cores"]
+    return {"value": best["value"], "unit": UNIT, "cores": best["threads"], "kind": "oracle",
+            "host_cpu_count": ncpu, "single_thread": legs["single_thread"],
+            "sample": "passes of the %s block over %d of its %d tokens (router, all their routed "
+                      "experts, combine) through the fp64 C oracle: %.1f s on %d threads (OpenMP "
+                      "over routes), %.1f s on one" % (wl.name, tokens, h.shape[0],
+                                                       best["seconds"], best["threads"],
+                                                       legs["single_thread"]["seconds"])}
 
 
 # ------------------------------------------------------------------------- reference

@@ -38,8 +38,10 @@
  *
  * Supported shapes: 1 <= k <= min(E, 32); 8 <= E <= 512, E % 8 == 0; H and I multiples of
  * 256 up to 8192 (moe_route_topk alone: H a multiple of 128); (H/8) * E * 2 <= 131072
- * bytes (router slice); b >= 1 and (b <= 8 or b % 8 == 0); 0 <= M; M * k < 2^24.
- * VQ: d == 4, K == 256.
+ * bytes (router slice); b >= 1 and (b <= 8 or b % 8 == 0), or b == 0 where an entry point
+ * says the library picks it; 0 <= M; M * k < 2^24.
+ * VQ: d in {4, 8}, K == 256, H a multiple of 1024 (vq_form 0 and 2: any M; vq_form 1: at
+ * most 4 tokens); VQ + low rank: r a multiple of 128 up to 512.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -89,10 +91,10 @@ typedef enum moe_status {
  *     T[q][kappa] = sum_t h[d q + t] B[kappa][t], so that g_i = sum_q T[q][J[e][q][i]] (one
  *     lookup per index instead of d products), for at most 4 tokens (M > 4:
  *     MOE_ERR_UNSUPPORTED); 2 decodes the index maps through the code books into the
- *     tensor cores' weight operand in shared memory and runs gate/up as the tcgen05 grouped
- *     GEMM of dense weights, over 16-row tiles of the aligned blocks (any M; the library
- *     aligns with b = 16 when it aligns itself).  The forms add in different orders; each is
- *     bitwise reproducible and independent of M on its own.
+ *     tensor cores' weight operand in tensor memory and runs gate/up as the tcgen05 grouped
+ *     GEMM of dense weights, over 16- or 64-row tiles of the aligned blocks (any M; b == 0
+ *     lets the library pick 16- or 64-row blocks).  The forms add in different orders; each
+ *     is bitwise reproducible and independent of M on its own.
  * Fields after w_down were added later; zero them when they do not apply.
  */
 typedef struct moe_expert_weights {
@@ -148,25 +150,63 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
                          int32_t *num_padded, size_t cap, void *stream);
 
 /*
- * Workspace bytes that moe_expert_ffn / moe_decode_block need for (weights shape, M, k, b).
- * The workspace holds the alignment (when the library computes it), the per-route
- * intermediates (dense weights: tiles of token rows and of p in bf16; VQ weights: p [M*k, I]
- * fp32), the expert outputs y [M*k, H] fp32, and the device status
- * word (its first 4 bytes), which must be zero before the first call (allocate it
- * zero-filled).  Calls that share a workspace must be ordered on one stream.
- * Returns 0 on unsupported arguments.
+ * Workspace bytes that moe_expert_ffn / moe_decode_block need for (weights shape, M, k, b)
+ * (b == 0: enough for any block size the library may pick).  The workspace holds the
+ * alignment (when the library computes it), the per-route intermediates (dense weights:
+ * tiles of token rows and of p in bf16, per-tile counters; VQ weights: p [M*k, I] fp32),
+ * the expert outputs y [M*k, H] fp32, and the device status word (its first 4 bytes),
+ * which must be zero before the first call (allocate it zero-filled).  Calls that share a
+ * workspace must be ordered on one stream.  Returns 0 on unsupported arguments.
  */
 size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b);
 
 /*
  * The block size moe_decode_block (and moe_expert_ffn without an alignment) aligns with for
- * (weights, M, k, b): b itself for the VQ forms 0 and 1; for dense weights and VQ form 2 the
- * tcgen05 tile width the library picks, 16 or 64 rows, by routes per expert and (dense) by
- * whether one wave of 16-row units' weights fits in this device's L2.  Every route's bits
- * are the same in both widths; the choice only affects speed.  Host-only (reads device
- * attributes of the current device, once).  Returns 0 on invalid arguments.
+ * (weights, M, k, b): b itself when b > 0; for b == 0 the library's choice -- 8 for the VQ
+ * forms 0 and 1, and for dense weights and VQ form 2 a tcgen05 tile width, 16 or 64 rows,
+ * by routes per expert and (dense) by whether one wave of 16-row units' weights fits in
+ * this device's L2.  Every route's bits are the same whatever the block size; the choice
+ * only affects speed.  Host-only (reads device attributes of the current device, once).
+ * Returns 0 on invalid arguments.
  */
 int moe_library_block_size(const moe_expert_weights_t *w, int M, int k, int b);
+
+/*
+ * Where moe_decode_block (and moe_expert_ffn without a caller alignment) keeps what it
+ * computes inside its workspace, so that a caller can read it after the call: byte offsets
+ * of sorted_route_ids [cap] int32, expert_block_ids [cap / b] int32, num_padded [1] int32
+ * and the status word, for the block size b the call aligns with (as
+ * moe_library_block_size resolves it) -- the arrays have the layout and contents that
+ * moe_align_block_size gives for the call's topk_ids, E and b -- and the per-route
+ * intermediates: y [M*k][H] fp32 (the down projection of every valid route; rows of invalid
+ * routes are not written) and, for the tensor-core paths (kn > 0), the p tiles: for each
+ * tile of kn aligned rows (tpb tiles per block, tile t of block q holding rows
+ * q*b + t*kn ...), per 64-wide chunk of I, kn rows of 128 bytes, 16-byte piece j of row n at
+ * byte n*128 + ((j ^ (n % 8)) * 16): p = SiLU(g) * u in bf16 for the rows that hold a route.
+ * Host-only; nothing is launched.  MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED on bad
+ * arguments.
+ */
+typedef struct moe_workspace_layout {
+    int32_t b;                /* block size the call aligns with */
+    int32_t kn;               /* rows per p tile (0: no p tiles, VQ forms 0 and 1) */
+    int64_t cap;              /* rows of sorted_route_ids: moe_align_capacity(M, k, E, b) */
+    size_t status;            /* byte offsets inside the workspace */
+    size_t sorted_route_ids;
+    size_t expert_block_ids;
+    size_t num_padded;
+    size_t y;
+    size_t p_tiles;
+    int32_t tpb;              /* p tiles per aligned block */
+    int32_t zero_bytes;       /* the first zero_bytes bytes (status word and counters) must be
+                                 zero before the first call; every call leaves them zero */
+    int32_t launches;         /* kernels one moe_decode_block call launches (1: the whole
+                                 block in one grid) */
+    int32_t reserved;
+    size_t p_rows;            /* the one-grid path (launches == 1): p [M*k][I] bf16 per route
+                                 instead of p tiles (0 otherwise) */
+} moe_workspace_layout_t;
+int moe_workspace_layout(const moe_expert_weights_t *w, int M, int k, int b,
+                         moe_workspace_layout_t *out);
 
 /*
  * Expert FFN + affinity-weighted combine for given routes.
@@ -175,7 +215,8 @@ int moe_library_block_size(const moe_expert_weights_t *w, int M, int k, int b);
  *   the residual, or zero).
  *   Alignment: either all three of sorted_route_ids / expert_block_ids / num_padded as
  *   produced by moe_align_block_size for (topk_ids, E, b) -- every valid route exactly
- *   once -- or all three NULL, in which case the alignment is computed into the workspace.
+ *   once, b > 0 -- or all three NULL, in which case the alignment is computed into the
+ *   workspace with block size b (b == 0: the library's choice, moe_library_block_size).
  *   workspace: ws_bytes >= moe_workspace_bytes(w, M, k, b).
  */
 int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
@@ -187,15 +228,16 @@ int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int M, int k,
 /*
  * The whole block: router (renormalised softmax top-k) -> alignment -> expert FFN ->
  * combine.  Same arguments as above; topk_ids [M,k] and topk_weights [M,k] are outputs.
- * Dense weights (and VQ weights with vq_form 2) run as grouped GEMMs on the tensor cores
- * over tiles of the aligned blocks: 16-row tiles for blocks of up to 16 rows, 64-row tiles
- * otherwise.  When the library aligns the routes itself (here, and in moe_expert_ffn without
- * a caller alignment) it picks the block size, 16 or 64 rows, by routes per expert
- * (moe_library_block_size); b only matters for a caller's own alignment.  Every route is
- * one K-ordered chain of MMAs per projection, so a token's output bits do not depend on M,
- * on the other tokens, on its block or its position in it, on b or on the tile width.  VQ
- * gate/up weights with vq_form 0 or 1 run on the CUDA cores with the caller's b; their
- * results are bitwise reproducible and independent of M and of block membership.
+ * The routes are aligned into blocks of b rows; b == 0 lets the library pick (16 or 64
+ * rows for the tensor-core paths, by routes per expert: moe_library_block_size).  Dense
+ * weights (and VQ weights with vq_form 2) run as grouped GEMMs on the tensor cores over
+ * tiles of the aligned blocks: 16-row tiles for blocks of up to 16 rows, 64-row tiles
+ * otherwise.  Dense gate/up and down run in one persistent grid whose down units stream
+ * their weights while gate/up runs.  Every route is one K-ordered chain of MMAs per
+ * projection, so a token's output bits do not depend on M, on the other tokens, on its block
+ * or its position in it, on b or on the tile width.  VQ gate/up weights with vq_form 0 or 1
+ * run on the CUDA cores; their results are bitwise reproducible and independent of M and of
+ * block membership.  The alignment stays in the workspace (moe_workspace_layout).
  */
 int moe_decode_block(const void *h, const void *w_router, const float *bias,
                      const moe_expert_weights_t *w, int M, int k, int b,

@@ -52,9 +52,11 @@ def build(force: bool = False) -> str:
     tmp = _LIB_PATH + ".tmp%d" % os.getpid()
     # -ffp-contract=off: no fused multiply-add contraction, so the rounding of every
     # product and sum is the one written in the source on every host architecture.
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-           _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    # -fopenmp: the expert loop may take whole tokens on several threads (each token's
+    # arithmetic unchanged); without an OpenMP runtime the same source builds serial.
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp]
+    if subprocess.run(base + ["-fopenmp", "-lm"], capture_output=True).returncode != 0:
+        subprocess.run(base + ["-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -84,8 +86,9 @@ def load_library(path):
                                       vp, vp, vp, vp]
     lib.oracle_decode_block.argtypes = [vp, vp, vp, ctypes.POINTER(_Weights), ci, ci,
                                         ci, vp, vp, vp, vp, vp]
+    lib.oracle_set_threads.argtypes = [ci]
     for f in ("oracle_router_logits", "oracle_topk_softmax", "oracle_align",
-              "oracle_expert_ffn", "oracle_decode_block"):
+              "oracle_expert_ffn", "oracle_decode_block", "oracle_set_threads"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -136,6 +139,12 @@ def _bits(a):
 def _check(rc, what):
     if rc != 0:
         raise RuntimeError("%s failed with oracle status %d" % (what, rc))
+
+
+def set_threads(n: int) -> int:
+    """Threads the expert loop uses (whole tokens per thread; results do not depend on it).
+    n <= 0 only reports the count.  Returns the count in effect (1 without OpenMP)."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def router_logits(h, w_router, bias, M, H, E):
@@ -249,3 +258,47 @@ def decode_block(h, w_router, bias, weights, k, renormalize=True, residual=None)
                                        k, int(bool(renormalize)), _ptr(res), _ptr(ids),
                                        _ptr(wts), _ptr(gap), _ptr(out)), "oracle_decode_block")
     return ids, wts, gap, out
+
+
+def host_weights(layer: dict, experts=None) -> dict:
+    """Host copies of a layer's expert weights (a dict of torch tensors as the seeded input
+    generator makes them) in the dict form the functions above take.  Marshalling only:
+    bf16 tensors become their uint16 bit patterns, index maps uint8 arrays.
+
+    ``experts`` (optional, sorted list of expert ids) restricts the copy to those experts
+    and renumbers them 0..len-1; the caller must renumber routes the same way.
+    """
+    import torch
+
+    def sel(t):
+        if t is None:
+            return None
+        if experts is not None:
+            t = t[torch.as_tensor(experts, device=t.device, dtype=torch.long)]
+        return t
+
+    def bits(t):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("expected a bf16 tensor")
+        return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    kind = layer["kind"]
+    w = {"kind": kind, "H": layer["H"], "I": layer["I"],
+         "E": layer["E"] if experts is None else len(experts),
+         "d": layer.get("d", 0), "K": layer.get("K", 0)}
+    if kind == W_DENSE:
+        w["w_gate"] = bits(sel(layer["w_gate"]))
+        w["w_up"] = bits(sel(layer["w_up"]))
+    else:
+        w["j_gate"] = sel(layer["j_gate"]).cpu().numpy()
+        w["j_up"] = sel(layer["j_up"]).cpu().numpy()
+        w["cb_gate"] = bits(layer["cb_gate"])
+        w["cb_up"] = bits(layer["cb_up"])
+    if kind == W_VQLR:
+        w["r"] = layer["r"]
+        w["d_gate"] = bits(layer["d_gate"])
+        w["d_up"] = bits(layer["d_up"])
+        w["c_gate"] = bits(sel(layer["c_gate"]))
+        w["c_up"] = bits(sel(layer["c_up"]))
+    w["w_down"] = bits(sel(layer["w_down"]))
+    return w

@@ -46,6 +46,9 @@
  *     layer and projection and C_e [r, I] private to the expert; down stays dense bf16.
  */
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -328,31 +331,44 @@ int oracle_expert_ffn(const uint16_t *h, const oracle_weights_t *w, int M, int k
         return ORACLE_ERR_ARG;
     }
     const int H = w->H, I = w->I, E = w->E;
-    double *g = (double *)malloc(sizeof(double) * (size_t)I);
-    double *u = (double *)malloc(sizeof(double) * (size_t)I);
-    double *p = (double *)malloc(sizeof(double) * (size_t)I);
-    double *y = (double *)malloc(sizeof(double) * (size_t)H);
     const int R = w->kind == ORACLE_W_VQLR ? w->r : 0;
-    double *zg = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
-    double *zu = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
-    if (!g || !u || !p || !y || !zg || !zu) {
-        free(g); free(u); free(p); free(y); free(zg); free(zu);
+    const int64_t routes = (int64_t)M * k;
+    /* y of every route first (routes are independent: with OpenMP each thread takes whole
+     * routes, each computed by the single-threaded loop below, unchanged), then the combine
+     * of every token in slot order. */
+    double *yall = (double *)malloc(sizeof(double) * (size_t)(routes > 0 ? routes : 1) * H);
+    if (!yall)
         return ORACLE_ERR_NOMEM;
-    }
-    for (int m = 0; m < M; ++m) {
-        double *o = out + (size_t)m * H;
-        for (int n = 0; n < H; ++n)
-            o[n] = residual ? bf16_bits_to_double(residual[(size_t)m * H + n]) : 0.0;
-        for (int j = 0; j < k; ++j) {
-            const size_t r = (size_t)m * k + j;
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *p = (double *)malloc(sizeof(double) * (size_t)I);
+        double *zg = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+        double *zu = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+        const int ok = g && u && p && zg && zu;
+        if (!ok) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = ORACLE_ERR_NOMEM;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t r = 0; r < routes; ++r) {
+            double *y = yall + (size_t)r * H;
             const int e = topk_ids[r];
-            if (e < 0 || e >= E) {
+            if (!ok || e < 0 || e >= E) {
                 if (p_out)
-                    memset(p_out + r * I, 0, sizeof(double) * (size_t)I);
-                if (y_out)
-                    memset(y_out + r * H, 0, sizeof(double) * (size_t)H);
+                    memset(p_out + (size_t)r * I, 0, sizeof(double) * (size_t)I);
+                memset(y, 0, sizeof(double) * (size_t)H);
                 continue;
             }
+            const int64_t m = r / k;
             for (int i = 0; i < I; ++i)
                 g[i] = u[i] = 0.0;
             for (int hh = 0; hh < H; ++hh) {
@@ -371,16 +387,44 @@ int oracle_expert_ffn(const uint16_t *h, const oracle_weights_t *w, int M, int k
                 for (int n = 0; n < H; ++n)
                     y[n] += p[i] * bf16_bits_to_double(drow[n]);
             }
-            for (int n = 0; n < H; ++n)
-                o[n] += a[r] * y[n];
             if (p_out)
-                memcpy(p_out + r * I, p, sizeof(double) * (size_t)I);
-            if (y_out)
-                memcpy(y_out + r * H, y, sizeof(double) * (size_t)H);
+                memcpy(p_out + (size_t)r * I, p, sizeof(double) * (size_t)I);
+        }
+        free(g); free(u); free(p); free(zg); free(zu);
+    }
+    for (int m = 0; m < M && status == ORACLE_OK; ++m) {
+        double *o = out + (size_t)m * H;
+        for (int n = 0; n < H; ++n)
+            o[n] = residual ? bf16_bits_to_double(residual[(size_t)m * H + n]) : 0.0;
+        for (int j = 0; j < k; ++j) {
+            const size_t r = (size_t)m * k + j;
+            const int e = topk_ids[r];
+            if (e < 0 || e >= E)
+                continue;
+            for (int n = 0; n < H; ++n)
+                o[n] += a[r] * yall[r * H + n];
         }
     }
-    free(g); free(u); free(p); free(y); free(zg); free(zu);
-    return ORACLE_OK;
+    if (y_out && status == ORACLE_OK)
+        memcpy(y_out, yall, sizeof(double) * (size_t)routes * H);
+    free(yall);
+    return status;
+}
+
+/*
+ * Threads the expert loop may use (OpenMP builds; 1 otherwise).  n <= 0 leaves the count
+ * as it is.  Returns the count in effect.
+ */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
 }
 
 /*

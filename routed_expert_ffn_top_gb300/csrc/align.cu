@@ -95,12 +95,14 @@ __global__ void __launch_bounds__(kAlignThreads)
                         int32_t *__restrict__ sorted, int32_t *__restrict__ blocks,
                         int32_t *__restrict__ npad, int64_t cap, int32_t *status,
                         const __nv_bfloat16 *__restrict__ x, int H,
-                        __nv_bfloat16 *__restrict__ x_tiles, int kn, int tpb) {
+                        __nv_bfloat16 *__restrict__ x_tiles, int kn, int tpb,
+                        int32_t *__restrict__ ready, int64_t nready) {
     __shared__ int32_t ids_s[kAlignGatherRoutes];
     __shared__ int32_t pos_s[kAlignGatherRoutes];
     __shared__ int32_t scratch[align_small_smem_ints(kAlignThreads)];
     pdl_wait();
     pdl_launch_dependents();
+    if (blockIdx.x == 0) zero_counts(ready, nready);  // the next grid's, read after this grid
     const int R = M * k;
     for (int r = threadIdx.x; r < R; r += blockDim.x) ids_s[r] = ids[r];
     __syncthreads();
@@ -150,7 +152,8 @@ cudaError_t launch_align_gather(const int32_t *topk_ids, int M, int k, int E, in
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(grid), dim3(kAlignThreads), 0, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, align_gather_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
-                              cap, status, x, H, rows.x_tiles, rows.kn, rows.tpb);
+                              cap, status, x, H, rows.x_tiles, rows.kn, rows.tpb, rows.ready,
+                              rows.nready);
 }
 
 cudaError_t launch_plan(const int32_t *topk_ids, const int32_t *sorted, const int32_t *blocks,

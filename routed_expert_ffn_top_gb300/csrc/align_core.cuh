@@ -174,11 +174,17 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
         e = ids[tid];
         valid = e >= 0 && e < E;
         if (valid)
-            for (int q = 0; q < R; ++q)
-                if (ids[q] == e) {
-                    ++n;
-                    lower += q < tid;
-                }
+            for (int q0 = 0; q0 < R; q0 += 8) {  // eight ids loaded before they are compared
+                int iq[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) iq[u] = q0 + u < R ? ids[q0 + u] : -1;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (iq[u] == e && q0 + u < R) {
+                        ++n;
+                        lower += q0 + u < tid;
+                    }
+            }
     }
     const int padded = valid ? pad_to(n, b) : 0;
     const bool leader = valid && lower == 0;
@@ -189,10 +195,18 @@ __device__ inline void align_small(const int32_t *ids, int R, int k, int E, int 
     const int any_invalid = __syncthreads_or(tid < R && !valid);
 
     int off = 0, total = 0;
-    for (int q = 0; q < R; ++q) {
-        const int p = pub[q];
-        total += p;
-        if (p != 0 && ids[q] < e) off += p;
+    for (int q0 = 0; q0 < R; q0 += 8) {  // eight entries loaded before they are added
+        int pq[8], iq[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            pq[u] = q0 + u < R ? pub[q0 + u] : 0;
+            iq[u] = q0 + u < R ? ids[q0 + u] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            total += pq[u];
+            if (pq[u] != 0 && iq[u] < e) off += pq[u];
+        }
     }
     if (pos_out && tid < R) pos_out[tid] = (valid && off + lower < cap) ? off + lower : -1;
     if (valid) {

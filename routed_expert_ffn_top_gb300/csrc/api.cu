@@ -43,6 +43,7 @@ WsLayout ws_layout(const Dims &d) {
         return at;
     };
     L.status = take(64);
+    L.ctl = take((size_t)kSmallCtlInts * 4);  // every layout keeps it (no other path writes it)
     L.sorted = take((size_t)d.cap * 4);
     L.blocks = take((size_t)(d.cap / d.b) * 4);
     L.npad = take(16);
@@ -54,6 +55,10 @@ WsLayout ws_layout(const Dims &d) {
     const size_t tile_rows = d.gemm ? (size_t)(d.cap / d.b) * d.tpb * d.kn : 0;
     L.x_tiles = take(tile_rows * d.H * 2);
     L.p_tiles = take(tile_rows * d.I * 2);
+    L.ready = take(d.gemm ? ((size_t)(d.cap / d.b) * d.tpb + 1) * 4 : 0);  // + the unit counter
+    const bool small = d.gemm && !d.vq_tc && small_fits(d.M, d.k, d.E, d.H, d.b);
+    L.partials = take(small ? (size_t)kRouterCluster * d.M * d.E * 4 : 0);
+    L.p_rows = take(small ? (size_t)d.R * d.I * 2 : 0);
     L.tt_part = take(d.ttable ? (size_t)vq_ttable_slices(d.H, d.vqd) * d.R * 2 * d.I * 4 : 0);
     L.total = off;
     return L;
@@ -316,9 +321,9 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
                                     static_cast<cudaStream_t>(stream)));
 }
 
-// The block size the library aligns with when it aligns the routes itself.  Dense weights,
-// and VQ weights decoded on the tensor cores, run as tcgen05 tiles whatever b is, so the
-// library picks the tile width: 16-row tiles, or 64-row ones from `per_expert` routes per
+// The block size the library aligns with when the caller leaves it to the library (b == 0).
+// Dense weights, and VQ weights decoded on the tensor cores, run as tcgen05 tiles, so the
+// library picks the tile width: 16-row blocks, or 64-row ones from `per_expert` routes per
 // expert on average.  Measured on GB300 (16- against 64-row tiles):
 //   - dense weights: an expert's 16-row tiles run on neighbouring CTAs at the same time, so
 //     the second tile's weights come from L2 while one wave of units' weights fits in it
@@ -326,10 +331,10 @@ extern "C" int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E
 //     when a wave does not fit (H = 4096, I = 1536) 64-row tiles are faster from 8;
 //   - VQ decoded on the tensor cores: a unit's MMAs and decoding cost the same for 16 or
 //     64 rows; 16-row tiles faster up to 12 routes per expert, 64-row ones from 16.
-// The other VQ forms keep the caller's b.
-static int effective_block(const moe_expert_weights_t *w, int M, int k, int b) {
+// The other VQ forms stream sub-blocks of 8 routes: they take b = 8.
+static int library_block(const moe_expert_weights_t *w, int M, int k) {
     const bool vq_tc = w && w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2;
-    if (!w || (w->kind != MOE_W_DENSE_BF16 && !vq_tc)) return b;
+    if (!w || (w->kind != MOE_W_DENSE_BF16 && !vq_tc)) return kNT;
     int per_expert = 16;
     if (!vq_tc) {
         const int64_t wave = (int64_t)num_sms() * 2 * 64 * w->H * 2;  // 16-row units' weights
@@ -338,9 +343,20 @@ static int effective_block(const moe_expert_weights_t *w, int M, int k, int b) {
     return (int64_t)M * k >= (int64_t)per_expert * w->E ? kGemmBlock : kGemmNarrow;
 }
 
+// The caller's b, or the library's choice when b == 0; -1 for a negative b.
+static int resolve_block(const moe_expert_weights_t *w, int M, int k, int b) {
+    if (b < 0) return -1;
+    return b == 0 ? library_block(w, M, k) : b;
+}
+
+int moe::block_for(const moe_expert_weights_t *w, int M, int k, int b) {
+    return resolve_block(w, M, k, b);
+}
+
 extern "C" int moe_library_block_size(const moe_expert_weights_t *w, int M, int k, int b) {
-    if (!w || M < 0 || k <= 0 || check_block(b) != MOE_OK) return 0;
-    return effective_block(w, M, k, b);
+    if (!w || M < 0 || k <= 0) return 0;
+    b = resolve_block(w, M, k, b);
+    return check_block(b) == MOE_OK ? b : 0;
 }
 
 size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, int b) {
@@ -354,19 +370,65 @@ size_t moe::workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, i
 }
 
 extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b) {
-    // enough for the caller's b (a caller-supplied alignment) and for the block size the
-    // library picks when it aligns itself (either tile width, so that the size does not
-    // depend on the device the choice is made on)
-    const size_t a = workspace_bytes_fixed(w, M, k, b);
+    if (!w || b < 0) return 0;
+    if (b > 0) return workspace_bytes_fixed(w, M, k, b);
+    // b == 0: enough for either block size the library may pick, so that the size does not
+    // depend on the device the choice is made on
+    const size_t a = workspace_bytes_fixed(w, M, k, library_block(w, M, k));
     if (a == 0) return 0;
-    size_t need = a;
-    const int picks[3] = {effective_block(w, M, k, b), kGemmNarrow, kGemmBlock};
-    const int npicks = effective_block(w, M, k, b) != b ? 3 : 1;
-    for (int i = 0; i < npicks; ++i) {
-        const size_t e = workspace_bytes_fixed(w, M, k, picks[i]);
-        if (e > need) need = e;
-    }
-    return need;
+    const bool tiles = w->kind == MOE_W_DENSE_BF16 || (w->kind == MOE_W_VQ_GATEUP && w->vq_form == 2);
+    if (!tiles) return a;
+    const size_t n = workspace_bytes_fixed(w, M, k, kGemmNarrow);
+    const size_t wide = workspace_bytes_fixed(w, M, k, kGemmBlock);
+    return a > n ? (a > wide ? a : wide) : (n > wide ? n : wide);
+}
+
+// Kernels one moe_decode_block call launches for these dimensions.
+static int block_launches(const moe_expert_weights_t *w, const Dims &d) {
+    if (d.gemm && !d.vq_tc && small_fits(d.M, d.k, d.E, d.H, d.b)) return 1;
+    const bool fused = router_can_align(d.M, d.k);
+    int n = 1 + (fused ? 0 : 1);                                   // router, alignment
+    n += (d.gemm && !fused && d.R > kAlignGatherRoutes) ? 1 : 0;   // row gather
+    if (w->kind == MOE_W_DENSE_BF16) n += 1;                        // gate/up and down, one grid
+    else n += 2 + (d.ttable ? 1 : 0);
+    return n + 1;                                                   // combine
+}
+
+extern "C" int moe_workspace_layout(const moe_expert_weights_t *w, int M, int k, int b,
+                                    moe_workspace_layout_t *out) {
+    if (!w || !out || M < 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    b = resolve_block(w, M, k, b);
+    int rc = check_block(b);
+    if (rc != MOE_OK) return rc;
+    if (workspace_bytes_fixed(w, M, k, b) == 0) return MOE_ERR_UNSUPPORTED;
+    const Dims d = dims_for(w, M, k, b);
+    const WsLayout L = ws_layout(d);
+    memset(out, 0, sizeof *out);
+    out->b = b;
+    out->kn = d.gemm ? d.kn : 0;
+    out->tpb = d.gemm ? d.tpb : 0;
+    out->cap = d.cap;
+    out->status = L.status;
+    out->sorted_route_ids = L.sorted;
+    out->expert_block_ids = L.blocks;
+    out->num_padded = L.npad;
+    out->y = L.y;
+    out->p_tiles = L.p_tiles;
+    out->zero_bytes = (int32_t)(L.ctl + (size_t)kSmallCtlInts * 4);
+    out->launches = block_launches(w, d);
+    out->p_rows = out->launches == 1 ? L.p_rows : 0;
+    return MOE_OK;
+}
+
+// Where the kernel that writes the x tiles puts them, and the ready counts it zeroes.
+static RowTiles row_tiles(const Dims &d, unsigned char *ws, const WsLayout &L) {
+    RowTiles rows;
+    rows.x_tiles = reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles);
+    rows.kn = d.kn;
+    rows.tpb = d.tpb;
+    rows.ready = reinterpret_cast<int32_t *>(ws + L.ready);
+    rows.nready = (d.cap / d.b) * d.tpb + 1;  // the tiles' counts and the unit counter
+    return rows;
 }
 
 // Runs gate/up and down for aligned routes (alignment pointers already resolved).
@@ -431,16 +493,25 @@ static int run_gemm(const void *h, const moe_expert_weights_t *w, const Dims &d,
     g.cb_up = d.vq_tc ? static_cast<const __nv_bfloat16 *>(w->cb_up) : nullptr;
     g.R = d.R;
     g.cap = d.cap;
+    g.ready = reinterpret_cast<int32_t *>(ws + L.ready);
+    g.nready = (d.cap / d.b) * d.tpb + 1;  // the tiles' counts, then the unit counter
     cudaError_t err = rows_ready ? cudaSuccess : launch_gather_rows(g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (!rows_ready) trace(2, stream);  // the row gather counts with the alignment
-    err = d.vq_tc ? launch_gemm_gateup_vq(tm_gate, tm_up, g, w->d, stream)
-                  : launch_gemm_gateup(tm_gate, tm_up, g, stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
-    trace(3, stream);
-    err = launch_gemm_down(tm_down, g, stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
-    trace(4, stream);
+    if (d.vq_tc) {
+        err = launch_gemm_gateup_vq(tm_gate, tm_up, g, w->d, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        trace(3, stream);
+        err = launch_gemm_down(tm_down, g, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        trace(4, stream);
+    } else {
+        // gate/up and down in one grid: both trace points after it
+        err = launch_gemm_fused(tm_gate, tm_up, tm_down, g, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        trace(3, stream);
+        trace(4, stream);
+    }
     GemvArgs c;
     memset(&c, 0, sizeof c);
     c.topk_ids = topk_ids;
@@ -563,7 +634,7 @@ static int check_ffn_common(const void *h, const moe_expert_weights_t *w, int M,
     if (!aligned(h, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
         (residual && !aligned(residual, 16)))
         return MOE_ERR_INVALID_ARG;
-    if (ws_bytes < moe_workspace_bytes(w, M, k, b)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < workspace_bytes_fixed(w, M, k, b)) return MOE_ERR_WORKSPACE;
     return MOE_OK;
 }
 
@@ -572,6 +643,9 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
                               const int32_t *sorted_route_ids, const int32_t *expert_block_ids,
                               const int32_t *num_padded, int b, const void *residual, void *out,
                               void *workspace, size_t ws_bytes, void *stream) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    const int b_in = b;
+    b = resolve_block(w, M, k, b);
     int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace, ws_bytes);
     if (rc != MOE_OK || M == 0) return rc;
     if (!topk_ids || !topk_weights || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
@@ -579,7 +653,7 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
     const int given = (sorted_route_ids != nullptr) + (expert_block_ids != nullptr) +
                       (num_padded != nullptr);
     if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
-    if (given == 0) b = effective_block(w, M, k, b);
+    if (given == 3 && b_in == 0) return MOE_ERR_INVALID_ARG;  // an alignment has its own b
     Dims d = dims_for(w, M, k, b);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -595,7 +669,7 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
         int32_t *ws_sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
         int32_t *ws_blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
         if (d.gemm && (int64_t)M * k <= kAlignGatherRoutes) {
-            const RowTiles rows{reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles), d.kn, d.tpb};
+            const RowTiles rows = row_tiles(d, ws, L);
             err = launch_align_gather(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
                                       status, static_cast<const __nv_bfloat16 *>(h), w->H, rows, s);
             rows_ready = true;
@@ -627,22 +701,62 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
                        rows_ready);
 }
 
+// The whole block for a few tokens in one grid (decode_small.cu).
+static int run_small(const void *h, const void *w_router, const float *bias,
+                     const moe_expert_weights_t *w, const Dims &d, const void *residual, void *out,
+                     int32_t *topk_ids, float *topk_weights, unsigned char *ws, const WsLayout &L,
+                     cudaStream_t s) {
+    CUtensorMap tm_gate, tm_up, tm_down;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_tmap_2d(&tm_gate, w->w_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                      (uint64_t)d.E * d.H, 64, kGemmStageK, sw) ||
+        !make_tmap_2d(&tm_up, w->w_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.I,
+                      (uint64_t)d.E * d.H, 64, kGemmStageK, sw) ||
+        !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
+                      (uint64_t)d.E * d.I, 64, kGemmStageK, sw))
+        return MOE_ERR_CUDA;
+    SmallArgs a;
+    a.h = static_cast<const __nv_bfloat16 *>(h);
+    a.w_router = static_cast<const __nv_bfloat16 *>(w_router);
+    a.residual = static_cast<const __nv_bfloat16 *>(residual);
+    a.bias = bias;
+    a.M = d.M;
+    a.k = d.k;
+    a.E = d.E;
+    a.H = d.H;
+    a.I = d.I;
+    a.b = d.b;
+    a.cap = d.cap;
+    a.topk_ids = topk_ids;
+    a.topk_wts = topk_weights;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.partials = reinterpret_cast<float *>(ws + L.partials);
+    a.ctl = reinterpret_cast<int32_t *>(ws + L.ctl);
+    a.sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    a.blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
+    a.npad = reinterpret_cast<int32_t *>(ws + L.npad);
+    a.p_rows = reinterpret_cast<__nv_bfloat16 *>(ws + L.p_rows);
+    a.y = reinterpret_cast<float *>(ws + L.y);
+    a.status = reinterpret_cast<int32_t *>(ws + L.status);
+    a.ntiles_cap = (int)(d.cap / d.b);
+    if (launch_decode_small(tm_gate, tm_up, tm_down, a, s) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int i = 1; i < kTracePoints; ++i) trace(i, s);  // one kernel: every stage ends here
+    return MOE_OK;
+}
+
 int moe::decode_block(const void *h, const void *w_router, const float *bias,
                       const moe_expert_weights_t *w, int M, int k, int b, const void *residual,
                       void *out, int32_t *topk_ids, float *topk_weights, void *workspace,
-                      size_t ws_bytes, void *stream, bool pick_regime) {
-    // with a fixed b the workspace only needs that b's layout
-    int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace,
-                              pick_regime ? ws_bytes : (size_t)-1);
-    if (rc == MOE_OK && !pick_regime && ws_bytes < workspace_bytes_fixed(w, M, k, b))
-        rc = MOE_ERR_WORKSPACE;
+                      size_t ws_bytes, void *stream) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    b = resolve_block(w, M, k, b);
+    int rc = check_ffn_common(h, w, M, k, b, residual, out, workspace, ws_bytes);
     if (rc != MOE_OK) return rc;
     rc = check_router_shape(M, w->H, w->E, k);
     if (rc != MOE_OK || M == 0) return rc;
     if (!w_router || !topk_ids || !topk_weights || !aligned(w_router, 16) ||
         !aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
-    if (pick_regime) b = effective_block(w, M, k, b);
     Dims d = dims_for(w, M, k, b);
     const WsLayout L = ws_layout(d);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -653,14 +767,16 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
     int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
     SubBlock *ws_sbt = reinterpret_cast<SubBlock *>(ws + L.sbt);
     int32_t *ws_status = reinterpret_cast<int32_t *>(ws + L.status);
+    if (d.gemm && !d.vq_tc && small_fits(M, k, w->E, w->H, b))
+        return run_small(h, w_router, bias, w, d, residual, out, topk_ids, topk_weights, ws, L, s);
     LowRankProj lr_store;
     const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store);  // rides in the router launch
     cudaError_t err;
     const bool fused = router_can_align(M, k);
     bool rows_ready = fused && d.gemm;  // x tiles written before the expert kernels
     if (fused) {  // one launch routes, aligns and (dense weights) writes the x tiles
-        RowTiles rows{nullptr, d.kn, d.tpb};
-        if (d.gemm) rows.x_tiles = reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles);
+        RowTiles rows{nullptr, d.kn, d.tpb, nullptr, 0};
+        if (d.gemm) rows = row_tiles(d, ws, L);
         err = launch_router_align(static_cast<const __nv_bfloat16 *>(h),
                                   static_cast<const __nv_bfloat16 *>(w_router), bias, M, w->H, w->E,
                                   k, 1, topk_ids, topk_weights, b, d.rsub, ws_sorted, ws_blocks,
@@ -674,7 +790,7 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         trace(1, s);
         if (d.gemm && (int64_t)M * k <= kAlignGatherRoutes) {
-            const RowTiles rows{reinterpret_cast<__nv_bfloat16 *>(ws + L.x_tiles), d.kn, d.tpb};
+            const RowTiles rows = row_tiles(d, ws, L);
             err = launch_align_gather(topk_ids, M, k, w->E, b, ws_sorted, ws_blocks, ws_npad, d.cap,
                                       ws_status, static_cast<const __nv_bfloat16 *>(h), w->H, rows,
                                       s);
@@ -696,7 +812,7 @@ extern "C" int moe_decode_block(const void *h, const void *w_router, const float
                                 float *topk_weights, void *workspace, size_t ws_bytes,
                                 void *stream) {
     return decode_block(h, w_router, bias, w, M, k, b, residual, out, topk_ids, topk_weights,
-                        workspace, ws_bytes, stream, true);
+                        workspace, ws_bytes, stream);
 }
 
 extern "C" int moe_decode_block_host(const void *h_host, const void *residual_host,
@@ -709,7 +825,8 @@ extern "C" int moe_decode_block_host(const void *h_host, const void *residual_ho
     if (M > 0 && (!h_host || !out_host || !h_dev || !out_dev)) return MOE_ERR_INVALID_ARG;
     if ((residual_host != nullptr) != (residual_dev != nullptr)) return MOE_ERR_INVALID_ARG;
     // Validate everything before the first copy, so an error leaves nothing enqueued.
-    int rc = check_ffn_common(h_dev, w, M, k, b, residual_dev, out_dev, workspace, ws_bytes);
+    int rc = check_ffn_common(h_dev, w, M, k, resolve_block(w, M, k, b), residual_dev, out_dev,
+                              workspace, ws_bytes);
     if (rc != MOE_OK) return rc;
     rc = check_router_shape(M, w->H, w->E, k);
     if (rc != MOE_OK || M == 0) return rc;

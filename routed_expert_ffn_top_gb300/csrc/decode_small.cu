@@ -1,0 +1,608 @@
+// decode_small.cu -- the whole decode block for a few tokens in one persistent grid: router,
+// alignment, gate/up + SiLU, down and the affinity-weighted combine.
+//
+// The block is the one of "A Multi-Engine Dataflow for MoE Decoding on Scratchpad-Based
+// Tensor Accelerators" (MoE block background; stage-3 activation; Section 4.3) with the
+// alignment of "Route-Block Membership Selects Packed-AWQ Arithmetic" (Sections 2.1, 5.3).
+// At one to four tokens the expert weights are the only real traffic (75 MB per layer at
+// one token), and every step of a chain of kernels costs a launch boundary on the critical
+// path before the weight stream starts and after it ends.  So one grid does it all:
+//
+//  1. Routing.  CTAs 0..7 each hold one eighth of the rows of W_r (copied before the wait
+//     for the previous grid) and reduce it against h to partial logits, with exactly the
+//     arithmetic of the router kernel's CTA of the same rank (the same row groups and
+//     orders, so the logits and the selection are bitwise those of the multi-kernel path).
+//     They publish the partials with a release count; every CTA acquires them, and runs the
+//     router's own finalisation (logits in slice order, top-k as ranks, softmax) and the
+//     alignment (align_small) itself, in shared memory: no CTA waits for another's result.
+//  2. Experts.  Units as in the fused grid (gemm_tc05.cu): gate/up units (tile, 64 channels
+//     of I) first, then down units (tile, 128 channels of H), CTA c taking units c, c + G ...
+//     The weight boxes come by TMA (warp 0); the tile's few token rows (gate/up: h; down:
+//     p) are copied into the stage's swizzled B slot by warp 6 with cp.async, which then
+//     fences the generic writes for the tensor cores' async proxy and arrives on the stage's
+//     barrier.  A down unit's weight boxes stream at once; its p rows wait for the tile's
+//     ready count (release by each gate/up unit once its p rows are stored).  Each output
+//     element is one K-ordered MMA chain, as in the multi-kernel path.
+//  3. Combine.  A down unit stores y for its routes and counts them, per token and 128-channel
+//     tile of H; the unit whose count completes a token's valid routes forms that token's
+//     output for its channels: out = bf16(residual + sum_j a_j y_j), slots in order, the
+//     combine kernel's arithmetic.
+//
+// The counters live in a control region of the workspace that is zero between calls: the
+// last CTA to finish (an exit count) restores it.  Every wait is bounded; a wait that gives
+// up sets MOE_DEV_WAIT_TIMEOUT and the grid drains and exits.
+#include "align_core.cuh"
+#include "gemm_core.cuh"
+#include "route_core.cuh"
+
+namespace moe {
+
+using GS = GTile<16>;
+constexpr int kSThreads = 224;  // producer, MMA, 4 epilogue warps, row loader
+constexpr int kSLoaderWarp = 6;
+static_assert(kSThreads % 32 == 0 && kSThreads >= kSmallMaxRoutes, "one thread per route");
+
+struct SmallState {
+    int32_t ids[kSmallMaxRoutes];
+    float wts[kSmallMaxRoutes];
+    int32_t tile_e[kSmallMaxRoutes];                     // expert of each tile (block)
+    int32_t tile_n[kSmallMaxRoutes];                     // rows holding a route (the first ones)
+    int32_t tile_r[kSmallMaxRoutes][kSmallMaxTokens];    // their routes
+    int32_t nvalid[kSmallMaxTokens];                     // valid routes of each token
+    int32_t comb[kSmallMaxTokens];                       // per row of the down unit: token to combine, or -1
+    int32_t ntiles;
+};
+
+// Shared-memory bytes the routing phase carves out of the ring (before any stage is used).
+__host__ __device__ constexpr size_t small_routing_bytes(int M, int H, int E) {
+    return (size_t)(H / kRouterCluster) * E * 2 +              // W_r slice
+           (size_t)M * (H / kRouterCluster) * 2 +              // h slices
+           (size_t)(kRouterThreads / (E / 2)) * M * E * 4 +    // row-group sums
+           (size_t)M * kRouterCluster * E * 4 +                // the 8 partials of every token
+           (size_t)M * E * 8 + (size_t)M * 32 * 8 +            // keys and values, slots
+           (size_t)(align_small_smem_ints(kSThreads) + kSmallMaxRoutes) * 4 + 1024;
+}
+
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t *p, int32_t v) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Bounded wait until *p >= need (acquire, GPU scope), polling every few tens of ns.
+__device__ __forceinline__ bool count_wait(const int32_t *p, int need, GCtl &ctl) {
+    if (ld_acquire_gpu(p) >= need) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(p) >= need) return true;
+        if (ctl.abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            ctl.abort = 1;
+            return false;
+        }
+    }
+}
+
+struct SmallUnits {
+    int64_t Tgu, T;
+    int n_gu, n_dn, nks_gu, nks_dn;
+    __device__ __forceinline__ void at(int64_t u, bool &gu, int &tile, int &ct, int &nks) const {
+        gu = u < Tgu;
+        const int64_t v = gu ? u : u - Tgu;
+        const int n = gu ? n_gu : n_dn;
+        tile = (int)(v / n);
+        ct = (int)(v % n);
+        nks = gu ? nks_gu : nks_dn;
+    }
+};
+
+// Partial logits of this CTA's slice q of H, with the router kernel's arithmetic for a CTA of
+// rank q: row group g of the slice is rows [g*HS/RG, (g+1)*HS/RG) (RG = 512 / (E/2), the
+// router's split for its 512 threads), each (token, expert) summed over its group's rows in
+// ascending order with one fused multiply-add per row, then the groups added in order.
+template <int TM>
+__device__ void small_router_dots(const SmallArgs &a, const __nv_bfloat16 *w_s,
+                                  const __nv_bfloat16 *x_s, float *red, int HS) {
+    const int E = a.E, npairs = E / 2, RG = kRouterThreads / npairs;
+    const uint32_t *x32 = reinterpret_cast<const uint32_t *>(x_s);
+    for (int item = threadIdx.x; item < npairs * RG; item += blockDim.x) {
+        const int pair = item % npairs, rg = item / npairs;
+        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(w_s) + pair;
+        const int r0 = rg * HS / RG, r1 = (rg + 1) * HS / RG;
+        // one chain per (token, expert), rows ascending; the tokens' chains interleave so that
+        // one weight load serves them all, and one load of h serves two rows
+        float acc0[TM], acc1[TM];
+#pragma unroll
+        for (int t = 0; t < TM; ++t) acc0[t] = acc1[t] = 0.0f;
+        int r = r0;
+        // eight rows per step: their weights and h pairs are all loaded before the first
+        // multiply-add, which then run in row order as before
+        for (; r + 7 < r1 && (r & 1) == 0; r += 8) {
+            uint32_t w8[8], x4[TM][4];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) w8[u] = wrow[(size_t)(r + u) * npairs];
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) x4[t][u] = x32[((size_t)t * HS + r + 2 * u) >> 1];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int t = 0; t < TM; ++t) {
+                    acc0[t] = fma_bf16<0, 0>(x4[t][u], w8[2 * u], acc0[t]);
+                    acc1[t] = fma_bf16<0, 1>(x4[t][u], w8[2 * u], acc1[t]);
+                    acc0[t] = fma_bf16<1, 0>(x4[t][u], w8[2 * u + 1], acc0[t]);
+                    acc1[t] = fma_bf16<1, 1>(x4[t][u], w8[2 * u + 1], acc1[t]);
+                }
+        }
+        for (; r + 1 < r1 && (r & 1) == 0; r += 2) {
+            const uint32_t wa = wrow[(size_t)r * npairs];
+            const uint32_t wb = wrow[(size_t)(r + 1) * npairs];
+#pragma unroll
+            for (int t = 0; t < TM; ++t) {
+                const uint32_t xv = x32[((size_t)t * HS + r) >> 1];
+                acc0[t] = fma_bf16<0, 0>(xv, wa, acc0[t]);
+                acc1[t] = fma_bf16<0, 1>(xv, wa, acc1[t]);
+                acc0[t] = fma_bf16<1, 0>(xv, wb, acc0[t]);
+                acc1[t] = fma_bf16<1, 1>(xv, wb, acc1[t]);
+            }
+        }
+        for (; r < r1; ++r) {  // an odd row at either end of a group
+            const uint32_t wa = wrow[(size_t)r * npairs];
+#pragma unroll
+            for (int t = 0; t < TM; ++t) {
+                const uint32_t xv = x32[((size_t)t * HS + r) >> 1];
+                if (r & 1) {
+                    acc0[t] = fma_bf16<1, 0>(xv, wa, acc0[t]);
+                    acc1[t] = fma_bf16<1, 1>(xv, wa, acc1[t]);
+                } else {
+                    acc0[t] = fma_bf16<0, 0>(xv, wa, acc0[t]);
+                    acc1[t] = fma_bf16<0, 1>(xv, wa, acc1[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TM; ++t) {
+            red[((size_t)rg * TM + t) * E + 2 * pair] = acc0[t];
+            red[((size_t)rg * TM + t) * E + 2 * pair + 1] = acc1[t];
+        }
+    }
+}
+
+__device__ void small_router_slice(const SmallArgs &a, const __nv_bfloat16 *w_s,
+                                   const __nv_bfloat16 *x_s, float *red, int HS) {
+    const int E = a.E, M = a.M, RG = kRouterThreads / (E / 2);
+    switch (M) {
+        case 1: small_router_dots<1>(a, w_s, x_s, red, HS); break;
+        case 2: small_router_dots<2>(a, w_s, x_s, red, HS); break;
+        case 3: small_router_dots<3>(a, w_s, x_s, red, HS); break;
+        default: small_router_dots<4>(a, w_s, x_s, red, HS); break;
+    }
+    __syncthreads();
+    // the row groups in order, published as this slice's partials
+    const int q = blockIdx.x;
+    for (int idx = threadIdx.x; idx < M * E; idx += blockDim.x) {
+        float s = red[idx];
+        for (int g = 1; g < RG; ++g) s += red[(size_t)g * M * E + idx];
+        a.partials[(size_t)q * M * E + idx] = s;
+    }
+}
+
+// Copy issuer (one thread): the weight boxes of every stage.
+__device__ void small_producer(const SmallArgs &a, GCtl &ctl, unsigned char *stages,
+                               const SmallState &st, const SmallUnits &f,
+                               const CUtensorMap *tm_gate, const CUtensorMap *tm_up,
+                               const CUtensorMap *tm_down) {
+    const uint64_t pol = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, parity_bits = 0;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < f.T && !stop && !ctl.abort; u += gridDim.x) {
+        bool gu;
+        int tile, ct, nks;
+        f.at(u, gu, tile, ct, nks);
+        const int e = st.tile_e[tile];
+        for (int s = 0; s < nks; ++s) {
+            if (!gwait(&ctl.empty[stage], phase ^ 1u, ctl)) {
+                stop = true;
+                break;
+            }
+            uint64_t *bar = &ctl.full[stage];
+            unsigned char *dst = stages + stage * GS::kStageBytes;
+            mbar_arrive_expect_tx(bar, GS::kABytes);
+            if (gu) {
+                const int32_t y = e * a.H + s * GS::kK;
+                tma_load_2d(dst, tm_gate, ct * 64, y, bar, pol);
+                tma_load_2d(dst + GS::kHalfBytes, tm_up, ct * 64, y, bar, pol);
+            } else {
+                const int32_t y = e * a.I + s * GS::kK;
+                tma_load_2d(dst, tm_down, ct * kGM, y, bar, pol);
+                tma_load_2d(dst + GS::kHalfBytes, tm_down, ct * kGM + 64, y, bar, pol);
+            }
+            issued |= 1u << stage;
+            parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+            gadvance<GS>(stage, phase);
+        }
+    }
+    for (int s = 0; s < GS::kStages; ++s)
+        if ((issued >> s) & 1u)
+            if (!mbar_wait_bounded(&ctl.full[s], (parity_bits >> s) & 1u)) ctl.abort = 1;
+}
+
+// Row loader (one warp): per stage, the 256-deep K slice of every row of the tile that holds a
+// route -- h of the route's token (gate/up) or p of the route (down) -- into the stage's B slot
+// in the K-major 128-byte-swizzle layout (row n at n * 128 bytes of each 64-wide chunk, 16-byte
+// piece j at (j ^ n % 8) * 16), one 16-byte piece per lane.  Rows without a route keep
+// whatever the slot held: their columns of the MMA are dropped.  Two stages' copies are in
+// flight at a time: a stage is released (proxy fence, arrival) once its copies have landed,
+// after the next stage's are issued.  Before a down unit waits for its tile's p, every
+// stage still held is released, so that no wait depends on this warp's own arrivals.
+__device__ void small_loader(const SmallArgs &a, GCtl &ctl, unsigned char *stages,
+                             const SmallState &st, const SmallUnits &f) {
+    const int lane = threadIdx.x & 31;
+    int stage = 0;
+    uint32_t phase = 0;
+    int held[2];
+    int nheld = 0;
+    auto release_oldest = [&](bool all) {
+        if (all)
+            cp_async_wait_group<0>();
+        else
+            cp_async_wait_group<1>();
+        fence_proxy_async_smem();  // generic writes, read next by the tensor cores
+        __syncwarp();
+        const int n = all ? nheld : 1;
+        if (lane == 0)
+            for (int i = 0; i < n; ++i) mbar_arrive(&ctl.full[held[i]]);
+        if (!all) held[0] = held[1];
+        nheld -= n;
+    };
+    for (int64_t u = blockIdx.x; u < f.T && !ctl.abort; u += gridDim.x) {
+        bool gu;
+        int tile, ct, nks;
+        f.at(u, gu, tile, ct, nks);
+        const int nrow = st.tile_n[tile];
+        if (!gu) {  // p of the tile's routes: stored by all I/64 gate/up units of the tile
+            if (nheld > 0) release_oldest(true);
+            bool ok = true;
+            if (lane == 0) ok = count_wait(a.ctl + kSmallCtlReady + tile, f.n_gu, ctl);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
+        }
+        for (int s = 0; s < nks; ++s) {
+            if (!__all_sync(0xffffffffu, gwait(&ctl.empty[stage], phase ^ 1u, ctl))) return;
+            unsigned char *bslot = stages + stage * GS::kStageBytes + GS::kBOff;
+            for (int n = 0; n < nrow; ++n) {
+                const int r = st.tile_r[tile][n];
+                const __nv_bfloat16 *src = gu ? a.h + (size_t)(r / a.k) * a.H + (size_t)s * GS::kK
+                                              : a.p_rows + (size_t)r * a.I + (size_t)s * GS::kK;
+                cp_async_16(bslot + (lane >> 3) * GS::kChunkBytes + tile_offset(n, lane & 7),
+                            src + lane * 8);
+            }
+            cp_async_commit();
+            held[nheld++] = stage;
+            if (nheld == 2) release_oldest(false);
+            gadvance<GS>(stage, phase);
+        }
+    }
+    if (nheld > 0) release_oldest(true);
+}
+
+// MMA issuer (one thread): as in the fused grid.
+__device__ void small_mma(GCtl &ctl, unsigned char *stages, const SmallUnits &f) {
+    constexpr uint32_t idesc = umma_idesc_bf16(kGM, 16, true, false);
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    for (int64_t u = blockIdx.x; u < f.T && !ctl.abort; u += gridDim.x, ++local) {
+        bool gu;
+        int tile, ct, nks;
+        f.at(u, gu, tile, ct, nks);
+        const int buf = local & 1;
+        if (!gwait(&ctl.tempty[buf], ((uint32_t)(local >> 1) & 1u) ^ 1u, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = ctl.tmem + (uint32_t)(buf * 16);
+        bool ok = true;
+        for (int s = 0; s < nks; ++s) {
+            if (!gwait(&ctl.full[stage], phase, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t A = smem_u32(stages + stage * GS::kStageBytes);
+            const uint32_t B = A + GS::kBOff;
+#pragma unroll
+            for (int ks = 0; ks < GS::kK / 16; ++ks) {
+                const uint64_t ad = umma_smem_desc(A + ks * 2048, GS::kHalfBytes, 1024, 2);
+                const uint64_t bd =
+                    umma_smem_desc(B + (ks >> 2) * GS::kChunkBytes + (ks & 3) * 32, 16, 1024, 2);
+                umma_bf16(d, ad, bd, idesc, s > 0 || ks > 0);
+            }
+            umma_commit(&ctl.empty[stage]);
+            gadvance<GS>(stage, phase);
+        }
+        if (!ok) break;
+        umma_commit(&ctl.tfull[buf]);
+    }
+    umma_commit(&ctl.done);
+    if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
+}
+
+__global__ void __launch_bounds__(kSThreads, 1)
+    decode_small_kernel(const __grid_constant__ CUtensorMap tm_gate,
+                        const __grid_constant__ CUtensorMap tm_up,
+                        const __grid_constant__ CUtensorMap tm_down, const SmallArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *stages = base;
+    float *gbuf = reinterpret_cast<float *>(base + GS::kStages * GS::kStageBytes);  // [16][64]
+    GCtl &ctl = *reinterpret_cast<GCtl *>(base + GS::kStages * GS::kStageBytes + 16 * 64 * 4);
+    SmallState &st = *reinterpret_cast<SmallState *>(reinterpret_cast<unsigned char *>(&ctl) +
+                                                     ((sizeof(GCtl) + 15) & ~size_t(15)));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = a.M, E = a.E, H = a.H, HS = H / kRouterCluster, R = M * a.k;
+    const bool router = blockIdx.x < kRouterCluster;
+
+    // routing scratch inside the ring (no stage is in use yet)
+    unsigned char *p = stages;
+    __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(p);
+    p += (size_t)HS * E * 2;
+    __nv_bfloat16 *x_s = reinterpret_cast<__nv_bfloat16 *>(p);
+    p += (size_t)M * HS * 2;
+    float *red = reinterpret_cast<float *>(p);
+    p += (size_t)(kRouterThreads / (E / 2)) * M * E * 4;
+    float *part_s = reinterpret_cast<float *>(p);
+    p += (size_t)M * kRouterCluster * E * 4;
+    uint32_t *key_s = reinterpret_cast<uint32_t *>(p);
+    p += (size_t)M * E * 4;
+    float *val_s = reinterpret_cast<float *>(p);
+    p += (size_t)M * E * 4;
+    int32_t *slot_e = reinterpret_cast<int32_t *>(p);
+    p += (size_t)M * 32 * 4;
+    float *slot_v = reinterpret_cast<float *>(p);
+    p += (size_t)M * 32 * 4;
+    int32_t *align_sm = reinterpret_cast<int32_t *>(p);
+    p += (size_t)align_small_smem_ints(kSThreads) * 4;
+    int32_t *pos_s = reinterpret_cast<int32_t *>(p);
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_gate);
+        prefetch_tensormap(&tm_up);
+        prefetch_tensormap(&tm_down);
+    }
+    // full barriers: the producer's expect_tx arrival and the row loader's arrival; bfull[0]
+    // (unused by this kernel's ring) tracks the router slice's copy
+    if (threadIdx.x == 0) mbar_init(&ctl.bfull[0], 1);
+    gemm_init<GS>(ctl, warp, 0, 2);
+    // the router slice never depends on the previous grid: its copy starts before the wait
+    const uint32_t w_bytes = (uint32_t)HS * E * 2;
+    if (router && threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&ctl.bfull[0], w_bytes);
+        bulk_load(w_s, a.w_router + (size_t)blockIdx.x * HS * E, w_bytes, &ctl.bfull[0]);
+    }
+    pdl_wait();  // h, and the control region, come after the previous grid
+    pdl_launch_dependents();
+
+    // ---------------------------------------------------------------- 1. routing
+    if (router) {
+        for (int idx = threadIdx.x; idx < M * (HS / 8); idx += blockDim.x) {
+            const int t = idx / (HS / 8), pc = idx - t * (HS / 8);
+            *reinterpret_cast<uint4 *>(x_s + (size_t)t * HS + pc * 8) =
+                *reinterpret_cast<const uint4 *>(a.h + (size_t)t * H + (size_t)blockIdx.x * HS + pc * 8);
+        }
+        if (!mbar_wait_bounded(&ctl.bfull[0], 0)) ctl.abort = 1;
+        __syncthreads();
+        small_router_slice(a, w_s, x_s, red, HS);
+        __syncthreads();
+        if (threadIdx.x == 0) red_release_gpu_add(a.ctl + kSmallCtlRouted, 1);
+    }
+    if (threadIdx.x == 0 && !count_wait(a.ctl + kSmallCtlRouted, kRouterCluster, ctl))
+        atomicOr(a.status, MOE_DEV_WAIT_TIMEOUT);
+    __syncthreads();
+    // the 8 slices' partials of every token, four experts per load, every load of a thread in
+    // flight before the first store
+    {
+        const int n4 = M * kRouterCluster * E / 4, e4n = E / 4;
+        constexpr int kBatch = 8;
+        for (int base = threadIdx.x; base < n4; base += kBatch * blockDim.x) {
+            float4 v[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int idx = base + i * blockDim.x;
+                if (idx < n4) {
+                    const int qt = idx / e4n, e4 = idx - qt * e4n;  // qt = q * M + t
+                    v[i] = __ldcg(reinterpret_cast<const float4 *>(a.partials + (size_t)qt * E) + e4);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int idx = base + i * blockDim.x;
+                if (idx < n4) {
+                    const int qt = idx / e4n, e4 = idx - qt * e4n;
+                    const int q = qt / M, t = qt - q * M;
+                    reinterpret_cast<float4 *>(part_s + ((size_t)t * kRouterCluster + q) * E)[e4] = v[i];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    route_finalize(part_s, M, E, a.k, a.bias, !ctl.abort, 1, key_s, val_s, slot_e, slot_v,
+                   [&](int i, int j, int id, float wt) {
+                       st.ids[i * a.k + j] = id;
+                       st.wts[i * a.k + j] = wt;
+                       if (blockIdx.x == 0) {
+                           a.topk_ids[(size_t)i * a.k + j] = id;
+                           a.topk_wts[(size_t)i * a.k + j] = wt;
+                       }
+                   });
+    __syncthreads();
+    // the alignment, in shared memory (CTA 0 also leaves it in the workspace)
+    int32_t *sorted_s = pos_s + kSmallMaxRoutes;
+    int32_t *blocks_s = sorted_s + a.cap;
+    int32_t *npad_s = blocks_s + a.cap / a.b;
+    align_small(st.ids, R, a.k, E, a.b, a.b, sorted_s, blocks_s, npad_s, a.cap, nullptr,
+                blockIdx.x == 0 ? a.status : nullptr, align_sm, pos_s);
+    __syncthreads();
+    const int ntiles = npad_s[0] / a.b;
+    for (int t = threadIdx.x; t < ntiles; t += blockDim.x) {
+        st.tile_e[t] = blocks_s[t];
+        int n = 0;
+        for (int row = 0; row < a.b && n < kSmallMaxTokens; ++row) {
+            const int r = sorted_s[(size_t)t * a.b + row];
+            if (r < 0 || r >= R) break;  // the routes of a block come first
+            st.tile_r[t][n++] = r;
+        }
+        st.tile_n[t] = n;
+    }
+    if (threadIdx.x < M) {
+        int n = 0;
+        for (int j = 0; j < a.k; ++j) {
+            const int e = st.ids[threadIdx.x * a.k + j];
+            n += (e >= 0 && e < E) ? 1 : 0;
+        }
+        st.nvalid[threadIdx.x] = n;
+    }
+    if (threadIdx.x == 0) st.ntiles = ntiles;
+    if (blockIdx.x == 0) {
+        for (int64_t i = threadIdx.x; i < a.cap; i += blockDim.x) a.sorted[i] = sorted_s[i];
+        for (int64_t i = threadIdx.x; i < a.cap / a.b; i += blockDim.x) a.blocks[i] = blocks_s[i];
+        if (threadIdx.x == 0) a.npad[0] = npad_s[0];
+    }
+    __syncthreads();
+    // a token without a valid route: its output is the residual (or zero)
+    if (blockIdx.x == 0)
+        for (int t = 0; t < M; ++t)
+            if (st.nvalid[t] == 0)
+                for (int n = threadIdx.x; n < H; n += blockDim.x)
+                    a.out[(size_t)t * H + n] =
+                        a.residual ? a.residual[(size_t)t * H + n] : __float2bfloat16(0.0f);
+
+    // ---------------------------------------------------------------- 2. experts
+    SmallUnits f;
+    f.n_gu = a.I / 64;
+    f.n_dn = H / kGM;
+    f.nks_gu = H / GS::kK;
+    f.nks_dn = a.I / GS::kK;
+    f.Tgu = (int64_t)ntiles * f.n_gu;
+    f.T = f.Tgu + (int64_t)ntiles * f.n_dn;
+    if (warp == 0) {
+        if (lane == 0) small_producer(a, ctl, stages, st, f, &tm_gate, &tm_up, &tm_down);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) small_mma(ctl, stages, f);
+        __syncwarp();
+    } else if (warp == kSLoaderWarp) {
+        small_loader(a, ctl, stages, st, f);
+    } else {
+        const int quad = warp & 3;
+        const int row = 32 * quad + lane;  // accumulator row: channel of the unit
+        int32_t *done = a.ctl + kSmallCtlReady + a.ntiles_cap;
+        int local = 0;
+        for (int64_t u = blockIdx.x; u < f.T; u += gridDim.x, ++local) {
+            bool gu;
+            int tile, ct, nks;
+            f.at(u, gu, tile, ct, nks);
+            const int buf = local & 1;
+            const int nrow = st.tile_n[tile];
+            const bool ok_u = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
+            if (named_bar_or(1, 128, !ok_u)) break;
+            float v[16];
+            drain_accumulator<16>(ctl, quad, buf, v);
+            if (gu) {
+                if (quad < 2) {
+#pragma unroll
+                    for (int n = 0; n < kSmallMaxTokens; ++n)
+                        if (n < nrow) gbuf[n * 64 + row] = v[n];
+                }
+                named_bar_sync(1, 128);
+                if (quad >= 2) {
+                    const int ch = row - 64;
+#pragma unroll
+                    for (int n = 0; n < kSmallMaxTokens; ++n) {
+                        if (n >= nrow) break;
+                        const float pv = silu_f32(gbuf[n * 64 + ch]) * v[n];
+                        a.p_rows[(size_t)st.tile_r[tile][n] * a.I + ct * 64 + ch] = __float2bfloat16(pv);
+                    }
+                }
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 64) red_release_gpu_add(a.ctl + kSmallCtlReady + tile, 1);
+            } else {
+#pragma unroll
+                for (int n = 0; n < kSmallMaxTokens; ++n)
+                    if (n < nrow) a.y[(size_t)st.tile_r[tile][n] * H + ct * kGM + row] = v[n];
+                named_bar_sync(1, 128);
+                // row n's count is taken by thread 64 + n (the rows' tokens are distinct: a
+                // token routes to an expert once); the one completing its token's valid
+                // routes marks the token for the combine
+                if (threadIdx.x >= 64 && threadIdx.x < 64 + nrow) {
+                    const int n = threadIdx.x - 64;
+                    const int m = st.tile_r[tile][n] / a.k;
+                    const int old = atom_add_acq_rel_gpu(done + m * f.n_dn + ct, 1);
+                    st.comb[n] = old + 1 == st.nvalid[m] ? m : -1;
+                }
+                named_bar_sync(1, 128);
+                // out = bf16(residual + sum_j a_j y_j), valid slots in order (the combine)
+                for (int c = 0; c < nrow; ++c) {
+                    const int m = st.comb[c];
+                    if (m < 0) continue;
+                    const int col = ct * kGM + row;
+                    float acc = 0.0f;
+                    for (int j = 0; j < a.k; ++j) {
+                        const int e = st.ids[m * a.k + j];
+                        if (e < 0 || e >= E) continue;
+                        acc = fmaf(st.wts[m * a.k + j], __ldcg(a.y + (size_t)(m * a.k + j) * H + col), acc);
+                    }
+                    const float res = a.residual ? __bfloat162float(a.residual[(size_t)m * H + col]) : 0.0f;
+                    a.out[(size_t)m * H + col] = __float2bfloat16_rn(res + acc);
+                }
+            }
+        }
+    }
+    gemm_finish<GS>(ctl, warp, a.status);
+
+    // ---------------------------------------------------------------- exit: restore the region
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int old = atom_add_acq_rel_gpu(a.ctl + kSmallCtlExit, 1);
+        if (old == (int)gridDim.x - 1) {
+            a.ctl[kSmallCtlRouted] = 0;
+            for (int i = 0; i < a.ntiles_cap; ++i) a.ctl[kSmallCtlReady + i] = 0;
+            for (int i = 0; i < M * (H / kGM); ++i) a.ctl[kSmallCtlReady + a.ntiles_cap + i] = 0;
+            a.ctl[kSmallCtlExit] = 0;
+        }
+    }
+}
+
+// Dynamic shared memory: the ring (which also holds the routing scratch), the gate/up
+// exchange buffer, the control block and the routing results.
+static size_t small_smem_bytes() {
+    const size_t ring = (size_t)GS::kStages * GS::kStageBytes;
+    return 1024 + ring + 16 * 64 * 4 + ((sizeof(GCtl) + 15) & ~size_t(15)) + sizeof(SmallState);
+}
+
+bool small_fits(int M, int k, int E, int H, int b) {
+    if (M < 1 || M > kSmallMaxTokens || (int64_t)M * k > kSmallMaxRoutes || b < 1 || b > 16)
+        return false;
+    if ((size_t)(H / kRouterCluster) * E * 2 > 64 * 1024) return false;  // one router pass
+    const int64_t R = (int64_t)M * k;
+    const int64_t cap = R + (R < E ? R : E) * (b - 1);
+    // routing scratch, then the alignment's rows and block vector, inside the ring
+    const size_t scratch = small_routing_bytes(M, H, E) + (size_t)(cap + cap / b + 4) * 4;
+    if (scratch > (size_t)GS::kStages * GS::kStageBytes) return false;
+    return small_smem_bytes() <= 227 * 1024 && (int64_t)M * (H / kGM) <= kSmallCtlDone &&
+           cap / b <= kSmallMaxRoutes;
+}
+
+cudaError_t launch_decode_small(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                                const CUtensorMap &tm_down, const SmallArgs &a,
+                                cudaStream_t stream) {
+    const size_t smem = small_smem_bytes();
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(decode_small_kernel), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kSThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, decode_small_kernel, tm_gate, tm_up, tm_down, a);
+}
+
+}  // namespace moe

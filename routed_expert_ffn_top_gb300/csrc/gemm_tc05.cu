@@ -41,114 +41,9 @@
 // depend on the other columns of B, on N or on its row of the tile (checked bitwise on this
 // GPU for N = 16..64, column shifts and row rotations), so a route's bits do not depend on
 // the grid, on M, on the other routes of its tile, on its block position or on kN.
-#include "moe_internal.cuh"
-#include "ptx.cuh"
+#include "gemm_core.cuh"
 
 namespace moe {
-
-constexpr int kGM = 128;                             // output channels per MMA
-constexpr int kGThreads = 192;                       // 6 warps
-constexpr int kGMaxStages = 8;
-
-// The shapes of one tile width kN (the MMA's N: 16 or 64 aligned rows).  A stage is the two
-// 32 KB weight boxes (64 columns x 256 rows of K, one per 64-wide M half) and the tile's
-// 256-deep slice of rows; narrow tiles keep three stages in flight, wide ones two.  (Stages
-// of 128 rows, six in flight, were slower for narrow tiles at 1 to 8 tokens.)
-template <int kN>
-struct GTile {
-    static_assert(kN == 16 || kN == 64, "tile widths: 16 or 64 rows");
-    static constexpr int kK = kGemmStageK;                    // K per stage
-    static constexpr int kHalfBytes = 64 * kK * 2;            // one M half: 32 KB
-    static constexpr int kABytes = 2 * kHalfBytes;            // 64 KB
-    static constexpr int kBBytes = kN * kK * 2;               // 8 KB or 32 KB
-    static constexpr int kStageBytes = kABytes + kBBytes;     // 72 KB or 96 KB
-    static constexpr int kStages = kN == 16 ? 3 : 2;
-    static constexpr int kChunkBytes = kN * 64 * 2;         // one 64-wide K chunk: 2 or 8 KB
-    static constexpr uint32_t kTmemCols = 2 * kN < 32 ? 32 : 2 * kN;  // two accumulators
-    static constexpr int kBOff = kABytes;                   // the row slice after the weights
-    static constexpr int kTxBytes = kStageBytes;            // bytes the stage's copies bring
-    static constexpr int kTileN = kN;
-    static constexpr int kDefer = kStages;  // row-slice copies held back until griddepcontrol
-    static constexpr bool kSplitB = false;  // one barrier for the weights and the row slice
-};
-
-// The VQ gate/up kernel (tiles of kN = 16 or 64 rows, code words of kD).  A unit is a tile and
-// 128 output channels of both projections: two M = 128 MMAs per K step, into a gate and an
-// up accumulator.  Its copy ring holds, per 256-deep stage, the gate and up index boxes
-// (256 / kD index rows x 128 columns of uint8 each, by TMA: 128-byte rows) and the tile's row
-// slice (behind a barrier of its own, so that decoding starts as soon as the index boxes
-// land).  The weight operand is decoded into tensor memory: slots of 64 K rows (32 columns
-// per projection) after the accumulators, six in flight with 16-row tiles and three with
-// 64-row ones (whose accumulators take 256 columns).  The code books sit in shared memory
-// with each entry repeated kReps times across the banks, so that the lanes of one wavefront,
-// each reading its own repeat, never share a bank.
-template <int kD, int kN>
-struct GTileVQ {
-    static_assert(kD == 4 || kD == 8, "code words of 4 or 8");
-    static_assert(kN == 16 || kN == 64, "tile widths: 16 or 64 rows");
-    static constexpr int kK = kGemmStageK;
-    static constexpr int kCT = 128;                         // channels per unit and projection
-    static constexpr int kJRows = kK / kD;
-    static constexpr int kJBytes = kJRows * kCT;            // one projection's index box
-    static constexpr int kBOff = 2 * kJBytes;
-    static constexpr int kBBytes = kN * kK * 2;
-    static constexpr int kStageBytes = kBOff + kBBytes;     // 24/16 KB (16 rows), 48/40 KB (64)
-    static constexpr int kTxBytes = kStageBytes;
-    static constexpr int kStages = kN == 16 ? (kD == 4 ? 6 : 8) : 3;
-    static constexpr int kChunkBytes = kN * 64 * 2;
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kTileN = kN;
-    static constexpr int kDefer = 2;
-    static constexpr bool kSplitB = true;  // decoders wait for the index boxes only
-    static constexpr int kDecWarps = 8;    // per TMEM lane quadrant one gate and one up warp
-    static constexpr int kSlotK = 64;                       // K rows per tensor-memory slot
-    static constexpr int kSlotsPerStage = kK / kSlotK;
-    static constexpr int kSlots = kN == 16 ? 6 : 3;
-    static constexpr uint32_t kSlotCols = 64;               // gate 32 columns, then up 32
-    static constexpr uint32_t kAccCols = 4 * kN;            // two buffers of gate and up
-    static constexpr uint32_t kSlotCol0 = kAccCols < 64 ? 64 : kAccCols;
-    static constexpr int kReps = kD == 4 ? 16 : 8;          // 8-byte words: 16 lanes a wavefront
-    static constexpr int kEntryBytes = kReps * kD * 2;      // 128
-    static constexpr int kCbBytes = 256 * kEntryBytes;      // one projection's code book
-    static_assert(kStageBytes % 1024 == 0 && kBOff % 1024 == 0, "stage alignment");
-    static_assert(kSlotCol0 + kSlots * kSlotCols <= kTmemCols, "tensor memory");
-    static_assert(kSlots <= kGMaxStages && kStages <= kGMaxStages, "barriers");
-};
-
-struct GCtl {
-    uint64_t full[kGMaxStages];
-    uint64_t empty[kGMaxStages];
-    uint64_t bfull[kGMaxStages];  // VQ: the stage's row slice has landed
-    uint64_t afull[kGMaxStages];   // VQ: a tensor-memory slot of the weight operand is written
-    uint64_t aempty[kGMaxStages];  // VQ: the MMAs reading a slot have completed
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t done;
-    uint32_t tmem;
-    volatile int abort;
-    int route[2][kGemmBlock];  // down epilogue: route of each tile row, per accumulator
-};
-
-__device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, GCtl &ctl) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (ctl.abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            ctl.abort = 1;
-            return false;
-        }
-    }
-}
-
-template <typename L>
-__device__ __forceinline__ void gadvance(int &stage, uint32_t &phase) {
-    if (++stage == L::kStages) {
-        stage = 0;
-        phase ^= 1u;
-    }
-}
 
 // The route of aligned row `pos` of a block of expert e, or -1 for padding and for a row
 // whose route does not belong to e (flagged, then skipped like padding).
@@ -195,6 +90,7 @@ __device__ __forceinline__ int tile_route(const GemmArgs &a, int64_t t, int n, i
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmArgs a) {
     pdl_wait();
     pdl_launch_dependents();
+    if (blockIdx.x == 0) zero_counts(a.ready, a.nready);  // the fused grid's, read after this grid
     const int lane = threadIdx.x & 31;
     const int64_t nrows = gemm_blocks(a) * a.b;
     const int nchunk = a.H / 64;
@@ -344,65 +240,271 @@ __device__ void gemm_mma(GCtl &ctl, unsigned char *stages, int64_t T, int nks) {
     if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
 }
 
-// decoder_warps (VQ): warps that also read each stage (its index boxes) before it is free,
-// and fill the tensor-memory slots of the weight operand.
-template <typename G>
-__device__ __forceinline__ void gemm_init(GCtl &ctl, int warp, int decoder_warps = 0) {
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < G::kStages; ++s) {
-            mbar_init(&ctl.full[s], 1);                   // the producer's expect_tx arrival
-            mbar_init(&ctl.empty[s], 1 + decoder_warps);  // MMA completion (+ decoders)
+// ------------------------------------------------------------- gate/up and down, one grid
+// Dense weights run both projections in one persistent grid.  Units are numbered gate/up
+// first -- (tile, 64-channel tile of I), u < Tgu -- then down -- (tile, 128-channel tile of H),
+// v = u - Tgu -- and CTA c takes units c, c + G, c + 2G ... (G = grid size).  So every CTA
+// runs all its gate/up units before its first down unit, and a down unit only ever waits for
+// gate/up units, which wait for nothing but their own copies: with the CTAs resident (one per
+// SM) no wait can close a cycle, and every wait is bounded in any case.
+//
+// A down unit's weight boxes do not depend on p, so the producer issues them as soon as ring
+// slots free up, while other SMs still run gate/up (the overlap of the down-projection DMA
+// with the gate/up computation in "A Multi-Engine Dataflow for MoE Decoding on
+// Scratchpad-Based Tensor Accelerators", Section 4).  Only the unit's p slices wait: for the
+// tile's ready count, to which every gate/up unit of the tile adds one (release, GPU scope)
+// once its p is stored.  The count is zeroed by the kernel before this one (the one that
+// wrote the x tiles), read with acquire, and followed by a proxy fence before the bulk copies
+// of p, which go through the async proxy.
+//
+// Both unit kinds keep the arithmetic of the separate kernels: one K-ordered MMA chain per
+// output element into its own accumulator column.
+struct FusedShape {
+    int64_t Tgu, T;            // gate/up units; all units
+    int n_gu, n_dn;            // channel tiles per tile: I / 64 (gate/up), H / 128 (down)
+    int nks_gu, nks_dn;        // 256-deep stages per unit
+};
+
+__device__ __forceinline__ FusedShape fused_shape(const GemmArgs &a, int kK) {
+    FusedShape f;
+    const int64_t tiles = gemm_blocks(a) * a.tpb;
+    f.n_gu = a.I / 64;
+    f.n_dn = a.H / kGM;
+    f.nks_gu = a.H / kK;
+    f.nks_dn = a.I / kK;
+    f.Tgu = tiles * f.n_gu;
+    f.T = f.Tgu + tiles * f.n_dn;
+    return f;
+}
+
+struct FusedUnit {
+    bool gu;
+    int64_t tile;
+    int ct, nks;
+};
+
+__device__ __forceinline__ FusedUnit fused_unit(const FusedShape &f, int64_t u) {
+    FusedUnit x;
+    x.gu = u < f.Tgu;
+    const int64_t v = x.gu ? u : u - f.Tgu;
+    const int n = x.gu ? f.n_gu : f.n_dn;
+    x.tile = v / n;
+    x.ct = (int)(v % n);
+    x.nks = x.gu ? f.nks_gu : f.nks_dn;
+    return x;
+}
+
+// Bounded wait until `need` gate/up units of `tile` have stored their p.
+__device__ __forceinline__ bool tile_ready_wait(const int32_t *ready, int64_t tile, int need,
+                                                GCtl &ctl) {
+    if (ld_acquire_gpu(ready + tile) >= need) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (ld_acquire_gpu(ready + tile) >= need) return true;
+        if (ctl.abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            ctl.abort = 1;
+            return false;
         }
-        for (int s = 0; s < kGMaxStages && decoder_warps; ++s) {
-            mbar_init(&ctl.afull[s], decoder_warps);
-            mbar_init(&ctl.aempty[s], 1);
-        }
-        for (int s = 0; s < G::kStages && G::kSplitB; ++s) mbar_init(&ctl.bfull[s], 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl.tfull[b], 1);
-            mbar_init(&ctl.tempty[b], 4);  // the 4 epilogue warps
-        }
-        mbar_init(&ctl.done, 1);
-        ctl.abort = 0;
-        fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&ctl.tmem, G::kTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
 }
 
-template <typename G>
-__device__ __forceinline__ void gemm_finish(GCtl &ctl, int warp, int32_t *status) {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(ctl.tmem, G::kTmemCols);
-    if (threadIdx.x == 0 && ctl.abort) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
-}
+// Unit queue.  A CTA's first unit is unit blockIdx.x; each later one is taken from a grid-wide
+// counter (units are handed out in increasing order, so every CTA runs its gate/up units
+// before its down units and a down unit never waits behind a unit of its own CTA), which keeps
+// the SMs busy to the end when units take different times.  The producer passes each unit to
+// the MMA issuer and the epilogue warps through an 8-slot ring of unit ids in shared memory;
+// -1 ends the sequence.
+constexpr int kUQSlots = 8;
+struct UnitQueue {
+    uint64_t full[kUQSlots];   // the producer wrote the slot
+    uint64_t empty[kUQSlots];  // the MMA thread and the 4 epilogue warps read it
+    int64_t u[kUQSlots];
+};
 
-// Epilogue warp: the kN fp32 columns of its 32 TMEM lanes of accumulator `buf`, then the
-// accumulator is handed back to the MMA issuer.
-template <int kN>
-__device__ __forceinline__ void drain_accumulator(GCtl &ctl, int quad, int buf, float (&v)[kN]) {
-    tc_fence_after();
-#pragma unroll
-    for (int c0 = 0; c0 < kN; c0 += 16) {
-        float t16[16];
-        tmem_ld16(ctl.tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(buf * kN + c0), t16);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[c0 + i] = t16[i];
+__device__ __forceinline__ void uq_init(UnitQueue &q) {
+    for (int s = 0; s < kUQSlots; ++s) {
+        mbar_init(&q.full[s], 1);
+        mbar_init(&q.empty[s], 5);
     }
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.tempty[buf]);
 }
 
-// ---------------------------------------------------------------------------- gate/up
+__device__ __forceinline__ bool uq_push(UnitQueue &q, GCtl &ctl, int i, int64_t u) {
+    const int slot = i % kUQSlots;
+    if (!gwait(&q.empty[slot], ((uint32_t)(i / kUQSlots) & 1u) ^ 1u, ctl)) return false;
+    q.u[slot] = u;
+    mbar_arrive(&q.full[slot]);
+    return true;
+}
+
+// The i-th unit of this CTA, or -1 (the end, or a wait that gave up).
+__device__ __forceinline__ int64_t uq_pop(UnitQueue &q, GCtl &ctl, int i) {
+    const int slot = i % kUQSlots;
+    if (!gwait(&q.full[slot], (uint32_t)(i / kUQSlots) & 1u, ctl)) return -1;
+    return q.u[slot];
+}
+
+// Copy issuer.  Row-slice copies that cannot go yet are held (at most one ring of them):
+// a gate/up unit's x slices until the previous grid is complete (they wait for griddepcontrol
+// only after the first kDefer weight stages are in flight), a down unit's p slices until the
+// tile's ready count is complete (they wait when the ring is full of the unit's stages, or at
+// its last stage).  A gate/up slice never waits behind a down unit's readiness: held x slices
+// are released before a down unit starts.  The next unit is taken from the counter once the
+// previous grid is complete (it zeroes the counter) and while this unit's copies stream.
+template <typename G>
+__device__ void fused_producer(const GemmArgs &a, GCtl &ctl, UnitQueue &q, unsigned char *stages,
+                               const FusedShape &f, int e_first_gu, const CUtensorMap *tm_gate,
+                               const CUtensorMap *tm_up, const CUtensorMap *tm_down) {
+    const uint64_t pol = policy_evict_first();
+    const unsigned char *xt = reinterpret_cast<const unsigned char *>(a.x_tiles);
+    const unsigned char *pt = reinterpret_cast<const unsigned char *>(a.p_tiles);
+    int32_t *sched = a.ready + a.nready - 1;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, parity_bits = 0;
+    bool waited = a.wait_first != 0;
+    int npend = 0;
+    const unsigned char *pend_src[G::kStages];
+    int pend_stage[G::kStages];
+    auto release_held = [&]() {
+        for (int qq = 0; qq < npend; ++qq)
+            bulk_load(stages + pend_stage[qq] * G::kStageBytes + G::kBOff, pend_src[qq], G::kBBytes,
+                      &ctl.full[pend_stage[qq]]);
+        npend = 0;
+    };
+    bool stop = false;
+    int i = 0;
+    int64_t u = blockIdx.x;
+    while (u < f.T && !stop && !ctl.abort) {
+        if (!uq_push(q, ctl, i++, u)) break;
+        const FusedUnit x = fused_unit(f, u);
+        if (!x.gu && npend > 0) {  // x slices of earlier gate/up units still held
+            if (!waited) pdl_wait();
+            waited = true;
+            release_held();
+        }
+        int64_t next = -1;
+        if (waited) next = (int64_t)gridDim.x + atomicAdd(sched, 1);
+        int e = (u == (int64_t)blockIdx.x && x.gu) ? e_first_gu : a.blocks[x.tile / a.tpb];
+        if (e < 0 || e >= a.E) {
+            atomicOr(a.status, MOE_DEV_BAD_ALIGNMENT);
+            e = 0;  // keep the pipeline in step; every row of such a block is dropped
+        }
+        bool ready = x.gu;
+        for (int s = 0; s < x.nks; ++s) {
+            if (!gwait(&ctl.empty[stage], phase ^ 1u, ctl)) {
+                stop = true;
+                break;
+            }
+            uint64_t *bar = &ctl.full[stage];
+            unsigned char *st = stages + stage * G::kStageBytes;
+            mbar_arrive_expect_tx(bar, G::kTxBytes);
+            if (x.gu) {
+                const int32_t y = e * a.H + s * G::kK;
+                tma_load_2d(st, tm_gate, x.ct * 64, y, bar, pol);
+                tma_load_2d(st + G::kHalfBytes, tm_up, x.ct * 64, y, bar, pol);
+            } else {
+                const int32_t y = e * a.I + s * G::kK;
+                tma_load_2d(st, tm_down, x.ct * kGM, y, bar, pol);
+                tma_load_2d(st + G::kHalfBytes, tm_down, x.ct * kGM + 64, y, bar, pol);
+            }
+            const unsigned char *src = (x.gu ? xt : pt) + (x.tile * x.nks + s) * (int64_t)G::kBBytes;
+            issued |= 1u << stage;
+            parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+            if (waited && ready) {
+                bulk_load(st + G::kBOff, src, G::kBBytes, bar);
+            } else {
+                pend_src[npend] = src;
+                pend_stage[npend] = stage;
+                ++npend;
+            }
+            gadvance<G>(stage, phase);
+            const bool go = x.gu ? npend == G::kDefer
+                                 : (npend > 0 && (npend == G::kStages || s == x.nks - 1));
+            if (go) {
+                if (!waited) pdl_wait();
+                waited = true;
+                if (!ready) {
+                    if (!tile_ready_wait(a.ready, x.tile, f.n_gu, ctl)) {
+                        stop = true;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                    ready = true;
+                }
+                release_held();
+            }
+            if (waited && next < 0) next = (int64_t)gridDim.x + atomicAdd(sched, 1);
+        }
+        if (next < 0 && !stop) {
+            if (!waited) pdl_wait();
+            waited = true;
+            release_held();
+            next = (int64_t)gridDim.x + atomicAdd(sched, 1);
+        }
+        u = next;
+    }
+    uq_push(q, ctl, i, -1);  // the end (if this wait gives up, the consumers' own waits do too)
+    // Held slices are copied even after an abort (their contents then no longer matter), so
+    // that every stage's barrier completes and the drain below ends at once.
+    if (npend > 0) {
+        if (!waited) pdl_wait();
+        release_held();
+    }
+    for (int s = 0; s < G::kStages; ++s)
+        if ((issued >> s) & 1u)
+            if (!mbar_wait_bounded(&ctl.full[s], (parity_bits >> s) & 1u)) ctl.abort = 1;
+}
+
+// MMA issuer (one thread): per unit its stages x 16 MMAs of K = 16 into the accumulator
+// buffer of the unit's parity; each stage is released when its MMAs complete.
+template <typename G>
+__device__ void fused_mma(GCtl &ctl, UnitQueue &q, unsigned char *stages, const FusedShape &f) {
+    constexpr int kN = G::kTileN;
+    constexpr uint32_t idesc = umma_idesc_bf16(kGM, kN, true, false);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int local = 0; !ctl.abort; ++local) {
+        const int64_t u = uq_pop(q, ctl, local);
+        mbar_arrive(&q.empty[local % kUQSlots]);
+        if (u < 0) break;
+        const int nks = fused_unit(f, u).nks;
+        const int buf = local & 1;
+        const uint32_t tph = (uint32_t)(local >> 1) & 1u;
+        if (!gwait(&ctl.tempty[buf], tph ^ 1u, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = ctl.tmem + (uint32_t)(buf * kN);
+        bool ok = true;
+        for (int s = 0; s < nks; ++s) {
+            if (!gwait(&ctl.full[stage], phase, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t A = smem_u32(stages + stage * G::kStageBytes);
+            const uint32_t B = A + G::kBOff;
+#pragma unroll
+            for (int ks = 0; ks < G::kK / 16; ++ks) {
+                const uint64_t ad = umma_smem_desc(A + ks * 2048, G::kHalfBytes, 1024, 2);
+                const uint64_t bd =
+                    umma_smem_desc(B + (ks >> 2) * G::kChunkBytes + (ks & 3) * 32, 16, 1024, 2);
+                umma_bf16(d, ad, bd, idesc, s > 0 || ks > 0);
+            }
+            umma_commit(&ctl.empty[stage]);
+            gadvance<G>(stage, phase);
+        }
+        if (!ok) break;
+        umma_commit(&ctl.tfull[buf]);
+    }
+    umma_commit(&ctl.done);
+    if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
+}
+
 template <int kN>
 __global__ void __launch_bounds__(kGThreads, 1)
-    gemm_gateup_kernel(const __grid_constant__ CUtensorMap tm_gate,
-                       const __grid_constant__ CUtensorMap tm_up, const GemmArgs a) {
+    gemm_fused_kernel(const __grid_constant__ CUtensorMap tm_gate,
+                      const __grid_constant__ CUtensorMap tm_up,
+                      const __grid_constant__ CUtensorMap tm_down, const GemmArgs a) {
     using G = GTile<kN>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
@@ -410,70 +512,84 @@ __global__ void __launch_bounds__(kGThreads, 1)
     unsigned char *stages = base;
     float *gbuf = reinterpret_cast<float *>(base + G::kStages * G::kStageBytes);  // [kN][64]
     GCtl &ctl = *reinterpret_cast<GCtl *>(base + G::kStages * G::kStageBytes + kN * 64 * 4);
+    UnitQueue &q = *reinterpret_cast<UnitQueue *>(reinterpret_cast<unsigned char *>(&ctl) +
+                                                  ((sizeof(GCtl) + 15) & ~size_t(15)));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
+        prefetch_tensormap(&tm_down);
+        uq_init(q);  // made visible by gemm_init's fence and barrier
     }
     gemm_init<G>(ctl, warp);
-    // When the router wrote the alignment and the x tiles, this grid may start while it
-    // still runs: wait for it before anything reads them, and only then let the down grid
-    // start (it reads the block vector before its own wait).
+    // When the previous kernel wrote the alignment (and the x tiles), wait for it before
+    // anything reads them.  The next kernel (the combine) may start at once: it waits for
+    // this grid before it reads anything.
     if (a.wait_first) pdl_wait();
     pdl_launch_dependents();
 
-    const int n_ct = a.I / 64;
-    const int nks = a.H / G::kK;
-    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
-    const int64_t T = gemm_blocks(a) * a.tpb * n_ct;
+    // the expert of this CTA's first unit if it is a gate/up unit, read beside the unit count
+    const int n_gu = a.I / 64;
+    const int e_first_gu = threadIdx.x == 0 ? first_unit_expert(a, n_gu) : 0;
+    const FusedShape f = fused_shape(a, G::kK);
 
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            gemm_producer<G>(a, ctl, stages, reinterpret_cast<const unsigned char *>(a.x_tiles),
-                              T, n_ct, nks, a.wait_first != 0, e_first,
-                              [&](unsigned char *st, uint64_t *bar, int e, int ct, int s) {
-                const int32_t y = e * a.H + s * G::kK;
-                tma_load_2d(st, &tm_gate, ct * 64, y, bar, pol);
-                tma_load_2d(st + G::kHalfBytes, &tm_up, ct * 64, y, bar, pol);
-            });
-        }
+        if (lane == 0) fused_producer<G>(a, ctl, q, stages, f, e_first_gu, &tm_gate, &tm_up, &tm_down);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) gemm_mma<G>(ctl, stages, T, nks);
+        if (lane == 0) fused_mma<G>(ctl, q, stages, f);
         __syncwarp();
     } else {
         const int quad = warp & 3;           // TMEM lanes [32 quad, 32 quad + 32)
-        const int row = 32 * quad + lane;    // accumulator row: gate channel (< 64) or up channel
-        int local = 0;
-        for (int64_t u = blockIdx.x; u < T; u += gridDim.x, ++local) {
-            const int64_t tile = u / n_ct;
-            const int ct = (int)(u % n_ct);
+        const int row = 32 * quad + lane;    // accumulator row (gate/up: gate < 64 <= up)
+        // the ready counts were zeroed by the previous grid: add to them only after it is done
+        if (!a.wait_first) pdl_wait();
+        for (int local = 0;; ++local) {
+            const int64_t u = uq_pop(q, ctl, local);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q.empty[local % kUQSlots]);
+            if (named_bar_or(1, 128, u < 0)) break;
+            const FusedUnit x = fused_unit(f, u);
             const int buf = local & 1;
-            // Only rows that hold a route get p: the other columns of the tile are dropped
-            // by the down epilogue, so their p rows may keep whatever they held.
-            if (row < kN) ctl.route[buf][row] = tile_route(a, tile, row, a.blocks[tile / a.tpb], false);
+            // Only rows that hold a route get p (gate/up) or y (down); the other columns of
+            // the tile are dropped.
+            if (row < kN)
+                ctl.route[buf][row] = tile_route(a, x.tile, row, a.blocks[x.tile / a.tpb], false);
             const bool ok = gwait(&ctl.tfull[buf], (uint32_t)(local >> 1) & 1u, ctl);
             if (named_bar_or(1, 128, !ok)) break;
             float v[kN];
             drain_accumulator<kN>(ctl, quad, buf, v);
-            if (quad < 2) {
+            if (x.gu) {
+                if (quad < 2) {
 #pragma unroll
-                for (int n = 0; n < kN; ++n)
-                    if (ctl.route[buf][n] >= 0) gbuf[n * 64 + row] = v[n];
-            }
-            named_bar_sync(1, 128);
-            if (quad >= 2) {
-                // p of each route row straight into the tile's swizzled chunk: a warp's 32
-                // channels are four 16-byte pieces of the row
-                const int ch = row - 64;
-                unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
-                                     (tile * n_ct + ct) * (int64_t)G::kChunkBytes + (ch & 7) * 2;
+                    for (int n = 0; n < kN; ++n)
+                        if (ctl.route[buf][n] >= 0) gbuf[n * 64 + row] = v[n];
+                }
+                named_bar_sync(1, 128);
+                if (quad >= 2) {
+                    // p of each route row straight into the tile's swizzled chunk: a warp's 32
+                    // channels are four 16-byte pieces of the row
+                    const int ch = row - 64;
+                    unsigned char *dst = reinterpret_cast<unsigned char *>(a.p_tiles) +
+                                         (x.tile * f.n_gu + x.ct) * (int64_t)G::kChunkBytes +
+                                         (ch & 7) * 2;
+#pragma unroll
+                    for (int n = 0; n < kN; ++n) {
+                        if (ctl.route[buf][n] < 0) continue;
+                        const float p = silu_f32(gbuf[n * 64 + ch]) * v[n];
+                        *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, ch >> 3)) =
+                            __float2bfloat16(p);
+                    }
+                    fence_proxy_async_global();  // read next through the async proxy
+                }
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 64) red_release_gpu_add(a.ready + x.tile, 1);
+            } else {
+                float *ybase = a.y + x.ct * kGM + row;
 #pragma unroll
                 for (int n = 0; n < kN; ++n) {
-                    if (ctl.route[buf][n] < 0) continue;
-                    const float p = silu_f32(gbuf[n * 64 + ch]) * v[n];
-                    *reinterpret_cast<__nv_bfloat16 *>(dst + tile_offset(n, ch >> 3)) = __float2bfloat16(p);
+                    const int r = ctl.route[buf][n];
+                    if (r >= 0) ybase[(int64_t)r * a.H] = v[n];
                 }
             }
         }
@@ -812,9 +928,10 @@ __global__ void __launch_bounds__(kGThreads, 1) wait_selftest_kernel(int32_t *st
 }
 
 template <int kN>
-static size_t gemm_gateup_smem() {
+static size_t gemm_fused_smem() {
     using G = GTile<kN>;
-    return 1024 + G::kStages * G::kStageBytes + kN * 64 * 4 + sizeof(GCtl);
+    return 1024 + G::kStages * G::kStageBytes + kN * 64 * 4 + ((sizeof(GCtl) + 15) & ~size_t(15)) +
+           sizeof(UnitQueue);
 }
 template <int kN>
 static size_t gemm_down_smem() {
@@ -832,14 +949,15 @@ cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream) {
 }
 
 template <int kN>
-static cudaError_t launch_gateup_tiles(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
-                                       const GemmArgs &a, cudaStream_t stream) {
-    const size_t smem = gemm_gateup_smem<kN>();
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_gateup_kernel<kN>), smem);
+static cudaError_t launch_fused_tiles(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                                      const CUtensorMap &tm_down, const GemmArgs &a,
+                                      cudaStream_t stream) {
+    const size_t smem = gemm_fused_smem<kN>();
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(gemm_fused_kernel<kN>), smem);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attrs[2];
     cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, gemm_gateup_kernel<kN>, tm_gate, tm_up, a);
+    return cudaLaunchKernelEx(&cfg, gemm_fused_kernel<kN>, tm_gate, tm_up, tm_down, a);
 }
 
 template <int kN>
@@ -853,10 +971,10 @@ static cudaError_t launch_down_tiles(const CUtensorMap &tm_down, const GemmArgs 
     return cudaLaunchKernelEx(&cfg, gemm_down_kernel<kN>, tm_down, a);
 }
 
-cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
-                               const GemmArgs &a, cudaStream_t stream) {
-    if (a.kn == 16) return launch_gateup_tiles<16>(tm_gate, tm_up, a, stream);
-    if (a.kn == 64) return launch_gateup_tiles<64>(tm_gate, tm_up, a, stream);
+cudaError_t launch_gemm_fused(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                              const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream) {
+    if (a.kn == 16) return launch_fused_tiles<16>(tm_gate, tm_up, tm_down, a, stream);
+    if (a.kn == 64) return launch_fused_tiles<64>(tm_gate, tm_up, tm_down, a, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -50,6 +50,7 @@ static_assert(sizeof(SubBlock) == 80, "SubBlock layout");
 
 struct WsLayout {
     size_t status;   // int32[16]
+    size_t ctl;      // int32[kSmallCtlInts]  counters of the one-kernel path, zero between calls
     size_t sorted;   // int32[cap]
     size_t blocks;   // int32[cap / b]
     size_t npad;     // int32[4]
@@ -59,6 +60,9 @@ struct WsLayout {
     size_t z;        // float[M * 2r]  low-rank projections z = D^T h (gate, then up)
     size_t x_tiles;  // bf16[tile rows * H]  dense weights: token rows per tile row
     size_t p_tiles;  // bf16[tile rows * I]  dense weights: p per tile row
+    size_t ready;    // int32[tiles]  dense weights: gate/up units of each tile whose p is stored
+    size_t partials; // float[8 * M * E]  one-kernel path: router partials of the 8 slices of H
+    size_t p_rows;   // bf16[R * I]  one-kernel path: p per route
     size_t tt_part;  // float[slices * M*k * 2 * I]  VQ through projected code books
     size_t total;
 };
@@ -91,7 +95,7 @@ struct GemvArgs {
 // Dense weights (and VQ decoded on the tensor cores): grouped GEMMs on tcgen05 over tiles
 // of kn aligned rows of one expert.  An aligned block of b rows is cut into tpb = ceil(b / kn)
 // tiles, kn = 16 for b <= 16, else 64.  The library picks 16- or 64-row blocks by routes per
-// expert (effective_block in api.cu).
+// expert when the caller passes b = 0 (library_block in api.cu).
 constexpr int kGemmBlock = 64;
 constexpr int kGemmNarrow = 16;
 
@@ -108,10 +112,20 @@ __host__ __device__ constexpr uint32_t tile_offset(int n, int j) {
 }
 
 // Where row tiles of h are written by the router when it also aligns (NULL x_tiles: not).
+// The kernel that writes them also zeroes the per-tile ready counts of the grouped GEMM that
+// reads them (`ready`, `nready` entries; NULL: none).
 struct RowTiles {
     __nv_bfloat16 *x_tiles;
     int kn, tpb;
+    int32_t *ready;
+    int64_t nready;
 };
+
+// Zeroes n counts with the threads of one CTA.
+__device__ __forceinline__ void zero_counts(int32_t *p, int64_t n) {
+    if (p)
+        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0;
+}
 
 struct GemmArgs {
     const __nv_bfloat16 *x;   // h [M,H] (read by the row gather)
@@ -128,11 +142,49 @@ struct GemmArgs {
     int wait_first;           // the previous kernel wrote the x tiles (and the alignment)
     const __nv_bfloat16 *cb_gate, *cb_up;  // VQ on the tensor cores: the code books
     int64_t R, cap;
+    int32_t *ready;           // [tiles] gate/up units done per tile, then the fused grid's unit
+    int64_t nready;           // counter: nready = tiles + 1 ints, zeroed by the previous kernel
 };
 
+// The whole block for a few tokens in one persistent grid (decode_small.cu): router,
+// alignment, gate/up, down and combine.  Its counters live in the workspace's control region
+// (zero between calls; the grid's last CTA restores it).
+constexpr int kSmallMaxTokens = 4;
+constexpr int kSmallMaxRoutes = 64;
+constexpr int kSmallCtlRouted = 0;  // router slices published
+constexpr int kSmallCtlExit = 1;    // CTAs finished
+constexpr int kSmallCtlReady = 32;  // ready[tiles], then done[M][H / 128]
+constexpr int kSmallCtlInts = 512;
+constexpr int kSmallCtlDone = kSmallCtlInts - kSmallCtlReady - kSmallMaxRoutes;
+
+struct SmallArgs {
+    const __nv_bfloat16 *h, *w_router, *residual;
+    const float *bias;
+    int M, k, E, H, I, b;
+    int64_t cap;
+    int32_t *topk_ids;
+    float *topk_wts;
+    __nv_bfloat16 *out;
+    float *partials;                  // [8][M][E]
+    int32_t *ctl;                     // the control region
+    int32_t *sorted, *blocks, *npad;  // the alignment, left in the workspace
+    __nv_bfloat16 *p_rows;            // [M*k][I]
+    float *y;                         // [M*k][H]
+    int32_t *status;
+    int ntiles_cap;                   // cap / b
+};
+// Whether the one-kernel path takes (M, k, E, H, b): dense weights, 1 <= M <= 4, M*k <= 64,
+// b <= 16, one router pass per slice of H.
+bool small_fits(int M, int k, int E, int H, int b);
+cudaError_t launch_decode_small(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                                const CUtensorMap &tm_down, const SmallArgs &a,
+                                cudaStream_t stream);
+
 cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream);
-cudaError_t launch_gemm_gateup(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
-                               const GemmArgs &a, cudaStream_t stream);
+// Gate/up + SiLU and down for dense weights in one persistent grid: a down unit's weights
+// stream while gate/up runs; its p waits on the tile's ready count.
+cudaError_t launch_gemm_fused(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,
+                              const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap &tm_down, const GemmArgs &a, cudaStream_t stream);
 // Blockwise-VQ gate/up on the tensor cores (16-row tiles, d = 4 or 8): index maps by TMA,
 // decoded through the code books into the MMA's A operand.
@@ -283,14 +335,14 @@ cudaError_t launch_down(const CUtensorMap &tm_down, const GemvArgs &a, cudaStrea
 
 cudaError_t launch_combine(const GemvArgs &a, cudaStream_t stream);
 
-// The decode block with the block size fixed to the caller's b (no switch to the grouped-
-// GEMM regime) and the workspace size that needs: the allocation-free entry, whose scratch
-// has a fixed size, runs through these.
+// The decode block (b == 0: the library's block size) and the workspace one resolved b
+// needs: the allocation-free entry, whose scratch has a fixed size, runs through these.
 int decode_block(const void *h, const void *w_router, const float *bias,
                  const moe_expert_weights_t *w, int M, int k, int b, const void *residual,
                  void *out, int32_t *topk_ids, float *topk_weights, void *workspace,
-                 size_t ws_bytes, void *stream, bool pick_regime);
+                 size_t ws_bytes, void *stream);
 size_t workspace_bytes_fixed(const moe_expert_weights_t *w, int M, int k, int b);
+int block_for(const moe_expert_weights_t *w, int M, int k, int b);  // b, or the library's (b == 0)
 
 // Raises `func`'s dynamic shared-memory limit to at least `bytes` on the current device.
 // The attribute is set once per (kernel, device) and remembered: repeating the runtime call

@@ -46,7 +46,7 @@ extern "C" int moe_decode_block_noalloc(const void *h, const void *w_router, con
                                         const void *residual, void *out, int32_t *topk_ids,
                                         float *topk_weights, void *stream) {
     if (w == nullptr || M < 0) return MOE_ERR_INVALID_ARG;
-    const size_t need = moe::workspace_bytes_fixed(w, M, k, b);
+    const size_t need = moe::workspace_bytes_fixed(w, M, k, moe::block_for(w, M, k, b));
     if (need == 0) return MOE_ERR_UNSUPPORTED;
     if (need > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
     if (M == 0) return MOE_OK;
@@ -58,5 +58,5 @@ extern "C" int moe_decode_block_noalloc(const void *h, const void *w_router, con
     if (cudaMemsetAsync(ws, 0, 64, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return moe::decode_block(h, w_router, bias, w, M, k, b, residual, out, topk_ids,
-                             topk_weights, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream, false);
+                             topk_weights, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -23,6 +23,7 @@
 
 #include "align_core.cuh"
 #include "ptx.cuh"
+#include "route_core.cuh"
 
 namespace moe {
 
@@ -58,14 +59,6 @@ __device__ __forceinline__ T *cluster_peer_mut(T *p, uint32_t rank) {
     return reinterpret_cast<T *>(out);
 }
 
-// fp32 -> uint32 with the same order (larger float, larger key; -0 and +0 both map to the
-// key of +0, so they tie as floats do).  Every non-NaN float maps above 0.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    if (v == 0.0f) v = 0.0f;
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // TM tokens per cluster tile; kPerLane experts per lane in the top-k warp (E <= 32 kPerLane).
 template <int TM, int kPerLane>
 __global__ void __launch_bounds__(kRouterThreads)
@@ -96,9 +89,17 @@ __global__ void __launch_bounds__(kRouterThreads)
     const int npass = router_passes(HS, E);
     const int HP = HS / npass;
 
+    // When one cluster aligns every token (routing clusters of the fused launch), every rank
+    // receives every token's partial logits and finalises all of them itself, so that the
+    // aligned rows are known in every rank without a second cluster barrier.  Otherwise
+    // rank t finalises token t of the tile.
+    const bool all_ranks = fa.enabled && !zmode;
+    const int GT = all_ranks ? TM : 1;  // tokens whose partials this CTA gathers
+
     // shared layout: w_s [HP][E] bf16 | x_s [TM][HS] bf16 | red [RG][TM][E] f32 |
-    //                gath [8][E] f32 (this CTA's token: the partial logits of every rank) |
-    //                ids_s [8 * 32] | bar | align scratch | aligned row of every route
+    //                gath [GT][8][E] f32 (the partial logits of every rank) |
+    //                ids_s [8 * 32] | key_s [GT][E] | val_s [GT][E] | slot_e, slot_v [GT][32] |
+    //                bar | align scratch | aligned row of every route
     unsigned char *ptr = smem_raw;
     __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(ptr);
     ptr += (size_t)HP * E * 2;
@@ -107,9 +108,17 @@ __global__ void __launch_bounds__(kRouterThreads)
     float *red = reinterpret_cast<float *>(ptr);
     ptr += (size_t)RG * TM * E * 4;
     float *gath = reinterpret_cast<float *>(ptr);
-    ptr += (size_t)kRouterCluster * E * 4;
-    int32_t *ids_s = reinterpret_cast<int32_t *>(ptr);  // [8 * 32] gathered ids (rank 0)
+    ptr += (size_t)GT * kRouterCluster * E * 4;
+    int32_t *ids_s = reinterpret_cast<int32_t *>(ptr);  // [8 * 32] every token's ids
     ptr += 8 * 32 * 4;
+    uint32_t *key_s = reinterpret_cast<uint32_t *>(ptr);
+    ptr += (size_t)GT * E * 4;
+    float *val_s = reinterpret_cast<float *>(ptr);
+    ptr += (size_t)GT * E * 4;
+    int32_t *slot_e = reinterpret_cast<int32_t *>(ptr);
+    ptr += (size_t)GT * 32 * 4;
+    float *slot_v = reinterpret_cast<float *>(ptr);
+    ptr += (size_t)GT * 32 * 4;
     uint64_t *bar = reinterpret_cast<uint64_t *>(ptr);
     ptr += 16;
     int32_t *align_sm = reinterpret_cast<int32_t *>(ptr);
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(kRouterThreads)
     }
     pdl_wait();  // h may come from the previous kernel in the stream
     pdl_launch_dependents();
+    if (fa.enabled && rank == 0 && blockIdx.y == 0) zero_counts(fa.rows.ready, fa.rows.nready);
 
     // h slices: 16-byte pieces (8 rows) of each token of the tile
     const int pieces = HS / 8;
@@ -194,22 +204,26 @@ __global__ void __launch_bounds__(kRouterThreads)
         }
     }
     __syncthreads();
-    // Row groups summed in order, then pushed to the CTA that finalises the token: rank t
-    // receives every rank's partial logits of token t in its own shared memory, so after the
-    // cluster barrier all reads are local.
+    // Row groups summed in order, then pushed to the CTAs that finalise the token (rank t, or
+    // every rank), into their own shared memory, so that after the cluster barrier all reads
+    // are local and no CTA touches another's shared memory.
     for (int idx = tid; idx < TM * E; idx += kRouterThreads) {
         float s = red[idx];
         for (int g = 1; g < RG; ++g) s += red[(size_t)g * TM * E + idx];
         const int t = idx / E, e = idx - t * E;
-        if (tile * TM + t < M) cluster_peer_mut(gath, (uint32_t)t)[(size_t)rank * E + e] = s;
+        if (tile * TM + t >= M) continue;
+        if (all_ranks) {
+            for (uint32_t q = 0; q < (uint32_t)kRouterCluster; ++q)
+                cluster_peer_mut(gath, q)[((size_t)t * kRouterCluster + rank) * E + e] = s;
+        } else {
+            cluster_peer_mut(gath, (uint32_t)t)[(size_t)rank * E + e] = s;
+        }
     }
     cluster_sync();
 
-    // Finalise: CTA of rank t handles token t of the tile (TM <= 8 = cluster size).
-    const int warp = tid >> 5, lane = tid & 31;
-    const int t = (int)rank;
-    const int m = tile * TM + t;
     if (zmode) {  // the projection: the 8 partials summed in rank order
+        const int t = (int)rank;
+        const int m = tile * TM + t;
         if (t < TM && m < M)
             for (int c = tid; c < E; c += kRouterThreads) {
                 float v = 0.0f;
@@ -217,91 +231,24 @@ __global__ void __launch_bounds__(kRouterThreads)
                 for (int q = 0; q < kRouterCluster; ++q) v += gath[(size_t)q * E + c];
                 lr.z[(size_t)m * 2 * lr.r + (size_t)proj * lr.r + c] = ok ? v : 0.0f;
             }
-        return;  // no CTA touches another's shared memory after the cluster barrier
+        return;
     }
-    if (warp == 0 && t < TM && m < M) {
-        float vals[kPerLane];
-        uint32_t key[kPerLane];
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int e = lane + 32 * i;
-            float v = -FLT_MAX;
-            key[i] = 0u;  // no candidate
-            if (e < E) {
-                v = 0.0f;
-#pragma unroll
-                for (int q = 0; q < kRouterCluster; ++q) v += gath[(size_t)q * E + e];
-                if (bias) v += bias[e];
-                if (!ok) v = -FLT_MAX;
-                key[i] = order_key(v);
-            }
-            vals[i] = v;
-        }
-        // k rounds of a warp arg-max: the largest key, ties to the lower expert id (each lane
-        // scans its experts in ascending id, then the lowest id among the lanes at the max)
-        int my_e = -1;
-        float my_v = -FLT_MAX;
-        for (int j = 0; j < k; ++j) {
-            uint32_t bk = 0u;
-            int bi = -1;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i)
-                if (key[i] > bk) {
-                    bk = key[i];
-                    bi = i;
-                }
-            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-            const uint32_t cand = (bi >= 0 && bk == mk) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
-            const uint32_t be = __reduce_min_sync(0xffffffffu, cand);
-            float bv = -FLT_MAX;
-            if (be != 0xffffffffu && (int)(be & 31) == lane) {
-                const int i = (int)(be >> 5);
-#pragma unroll
-                for (int q = 0; q < kPerLane; ++q)
-                    if (q == i) {
-                        bv = vals[q];
-                        key[q] = 0u;  // taken
-                    }
-            }
-            bv = __shfl_sync(0xffffffffu, bv, (int)(be & 31));
-            if (lane == j) {
-                my_e = be == 0xffffffffu ? -1 : (int)be;
-                my_v = bv;
-            }
-        }
-        const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
-        float denom;
-        float ex = 0.0f;
-        if (renorm) {
-            ex = (lane < k) ? expf(my_v - l0) : 0.0f;
-            denom = ex;
-        } else {
-            float s = 0.0f;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i)
-                if (lane + 32 * i < E) s += expf(vals[i] - l0);
-            denom = s;
-            ex = (lane < k) ? expf(my_v - l0) : 0.0f;
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
-        if (lane < k) {
-            const int id = ok ? my_e : -1;
-            topk_ids[(size_t)m * k + lane] = id;
-            topk_wts[(size_t)m * k + lane] = ok ? ex / denom : 0.0f;
-            // every token's ids go to rank 0, which aligns them when one cluster holds all
-            // (to every rank when the ranks also write the row tiles)
-            if (fa.enabled) {
-                if (fa.rows.x_tiles)
-                    for (uint32_t q = 0; q < (uint32_t)kRouterCluster; ++q)
-                        cluster_peer_mut(ids_s, q)[t * k + lane] = id;
-                else
-                    cluster_peer_mut(ids_s, 0u)[t * k + lane] = id;
-            }
-        }
-    }
+    // Tokens finalised here: t0 .. t0 + nt - 1 of the tile.
+    const int t0 = all_ranks ? 0 : (int)rank;
+    int nt = all_ranks ? TM : ((int)rank < TM ? 1 : 0);
+    if (tile * TM + t0 + nt > M) nt = M - tile * TM - t0 > 0 ? M - tile * TM - t0 : 0;
+    route_finalize(gath, nt, E, k, bias, ok, renorm, key_s, val_s, slot_e, slot_v,
+                   [&](int i, int j, int id, float wt) {
+                       const int t = t0 + i;
+                       const int m = tile * TM + t;
+                       if (!all_ranks || rank == 0) {
+                           topk_ids[(size_t)m * k + j] = id;
+                           topk_wts[(size_t)m * k + j] = wt;
+                       }
+                       if (all_ranks) ids_s[t * k + j] = id;  // every rank aligns them below
+                   });
     if (fa.enabled) {
-        cluster_sync();
+        __syncthreads();
         int32_t *pos_s = align_sm + align_small_smem_ints(kRouterThreads);  // [M * k]
         const int R = M * k;
         if (rank == 0)
@@ -333,14 +280,16 @@ __global__ void __launch_bounds__(kRouterThreads)
             }
         }
     }
-    // No CTA touches another's shared memory after the last cluster barrier.
+    // No CTA touches another's shared memory after the cluster barrier.
 }
 
 static size_t router_smem(int TM, int H, int E, bool fuse) {
     const int HS = H / kRouterCluster;
     const int RG = kRouterThreads / (E / 2);
+    const int GT = fuse ? TM : 1;
     return (size_t)(HS / router_passes(HS, E)) * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
-           (size_t)kRouterCluster * E * 4 + 8 * 32 * 4 + 16 +
+           (size_t)GT * kRouterCluster * E * 4 + 8 * 32 * 4 + (size_t)GT * E * 8 +
+           (size_t)GT * 32 * 8 + 16 +
            (fuse ? (size_t)(align_small_smem_ints(kRouterThreads) + 8 * 32) * 4 : 0);
 }
 

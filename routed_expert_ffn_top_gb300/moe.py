@@ -39,7 +39,7 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_expert_ffn", "moe_decode_block", "moe_decode_block_host",
     "moe_read_device_status", "moe_set_trace_events", "moe_decode_block_noalloc",
     "moe_selftest_wait_timeout", "moe_reader_build", "moe_reader_workspace_bytes",
-    "moe_reader_ffn", "moe_library_block_size",
+    "moe_reader_ffn", "moe_library_block_size", "moe_workspace_layout",
 )
 
 
@@ -62,6 +62,18 @@ class ExpertWeights(ctypes.Structure):
         ("c_gate", ctypes.c_void_p), ("c_up", ctypes.c_void_p),
         ("r", ctypes.c_int32),
         ("vq_form", ctypes.c_int32),
+    ]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [
+        ("b", ctypes.c_int32), ("kn", ctypes.c_int32), ("cap", ctypes.c_int64),
+        ("status", ctypes.c_size_t), ("sorted_route_ids", ctypes.c_size_t),
+        ("expert_block_ids", ctypes.c_size_t), ("num_padded", ctypes.c_size_t),
+        ("y", ctypes.c_size_t), ("p_tiles", ctypes.c_size_t),
+        ("tpb", ctypes.c_int32), ("zero_bytes", ctypes.c_int32),
+        ("launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("p_rows", ctypes.c_size_t),
     ]
 
 
@@ -109,6 +121,7 @@ def lib():
             L.moe_workspace_bytes.restype = sz
             L.moe_library_block_size.argtypes = [wp, ci, ci, ci]
             L.moe_library_block_size.restype = ci
+            L.moe_workspace_layout.argtypes = [wp, ci, ci, ci, ctypes.POINTER(WorkspaceLayout)]
             L.moe_expert_ffn.argtypes = [vp, wp, ci, ci, vp, vp, vp, vp, vp, ci, vp, vp, vp, sz, vp]
             L.moe_decode_block.argtypes = [vp, vp, vp, wp, ci, ci, ci, vp, vp, vp, vp, vp, sz, vp]
             L.moe_decode_block_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, wp, ci, ci, ci,
@@ -254,6 +267,28 @@ def moe_library_block_size(layer: dict, M, k, b) -> int:
     """The block size moe_decode_block aligns with for these weights and sizes."""
     w = expert_weights(layer)
     return int(lib().moe_library_block_size(ctypes.byref(w), M, k, b))
+
+
+def moe_workspace_layout(layer: dict, M, k, b) -> dict:
+    """Block size, capacity and byte offsets of the alignment inside the workspace of
+    moe_decode_block / moe_expert_ffn (library alignment) for these sizes."""
+    w = expert_weights(layer)
+    out = WorkspaceLayout()
+    _check(lib().moe_workspace_layout(ctypes.byref(w), M, k, b, ctypes.byref(out)),
+           "moe_workspace_layout")
+    return {f: int(getattr(out, f)) for f, _ in WorkspaceLayout._fields_ if f != "reserved"}
+
+
+def workspace_alignment(workspace: torch.Tensor, layout: dict):
+    """Views (sorted_route_ids, expert_block_ids, num_padded) of the alignment a call left in
+    `workspace`, at the offsets of `layout` (moe_workspace_layout)."""
+    cap, b = layout["cap"], layout["b"]
+
+    def view(off, n):
+        return workspace[off:off + 4 * n].view(torch.int32)
+
+    return (view(layout["sorted_route_ids"], cap), view(layout["expert_block_ids"], cap // b),
+            view(layout["num_padded"], 1))
 
 
 def alloc_workspace(layer: dict, M, k, b, device=None) -> torch.Tensor:
@@ -423,16 +458,6 @@ def capture_graph(fn, stream: Optional[torch.cuda.Stream] = None) -> torch.cuda.
 
 
 # ------------------------------------------------------------------------ channel reader
-def reader_basis(w_down: torch.Tensor, rank: int = 32) -> torch.Tensor:
-    """U [H, rank] fp32 for the reader's recovery map: the top left singular vectors of the
-    H x (E I) matrix of down columns, from the eigenvectors of D^T D (an offline build step
-    done once per layer with torch's symmetric eigensolver, not part of the decode path)."""
-    D = w_down.reshape(-1, w_down.shape[-1]).to(torch.float64)
-    evals, evecs = torch.linalg.eigh((D.T @ D).cpu())  # H x H, solved on the host
-    order = torch.argsort(evals, descending=True, stable=True)[:rank]
-    return evecs[:, order].to(device=w_down.device, dtype=torch.float32).contiguous()
-
-
 def _reader_struct(rd: dict) -> ReaderStruct:
     s = ReaderStruct()
     s.H, s.I, s.E, s.rank = rd["H"], rd["I"], rd["E"], rd["rank"]

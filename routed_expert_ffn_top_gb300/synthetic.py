@@ -158,37 +158,3 @@ def bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype != torch.bfloat16:
         raise TypeError("expected a bf16 tensor")
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-
-
-def oracle_weights(layer: dict, experts=None) -> dict:
-    """Host copies of a layer's expert weights in the oracle's dict form.
-
-    ``experts`` (optional, sorted list of expert ids) restricts the copy to those experts
-    and renumbers them 0..len-1; the caller must renumber routes the same way.
-    """
-    def sel(t):
-        if t is None:
-            return None
-        if experts is not None:
-            t = t[torch.as_tensor(experts, device=t.device, dtype=torch.long)]
-        return t
-
-    w = {"kind": layer["kind"], "H": layer["H"], "I": layer["I"],
-         "E": layer["E"] if experts is None else len(experts),
-         "d": layer.get("d", 0), "K": layer.get("K", 0)}
-    if layer["kind"] == W_DENSE:
-        w["w_gate"] = bits(sel(layer["w_gate"]))
-        w["w_up"] = bits(sel(layer["w_up"]))
-    else:
-        w["j_gate"] = sel(layer["j_gate"]).cpu().numpy()
-        w["j_up"] = sel(layer["j_up"]).cpu().numpy()
-        w["cb_gate"] = bits(layer["cb_gate"])
-        w["cb_up"] = bits(layer["cb_up"])
-    if layer["kind"] == W_VQLR:
-        w["r"] = layer["r"]
-        w["d_gate"] = bits(layer["d_gate"])
-        w["d_up"] = bits(layer["d_up"])
-        w["c_gate"] = bits(sel(layer["c_gate"]))
-        w["c_up"] = bits(sel(layer["c_up"]))
-    w["w_down"] = bits(sel(layer["w_down"]))
-    return w

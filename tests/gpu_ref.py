@@ -6,8 +6,9 @@ Tolerances (the bars the parity tests enforce):
 * affinities: |gpu - oracle| <= 1e-4 * oracle + 1e-6 (fp32 softmax of fp32 logits);
 * block output (bf16): relative L2 error <= 3e-3 and max-abs error <= 2e-2 * RMS(oracle).
 A token whose oracle margin between the k-th and (k+1)-th logit is below NEAR_TIE may
-legitimately select differently in fp32; such a token is accepted when the GPU's set is a
-valid top-k within NEAR_TIE, and its output is then checked with the GPU's ids.
+legitimately select differently in fp32, and two selected experts whose logits lie within
+NEAR_TIE may legitimately swap slots; only such tokens are excused (check_routing), at most
+max(1, M // 50) of them, and their output is then checked with the GPU's ids.
 """
 from __future__ import annotations
 
@@ -53,33 +54,63 @@ def oracle_routing(layer, h, k, renormalize=True):
     return ids, wts, gap, logits
 
 
-def check_routing(gpu_ids, gpu_wts, o_ids, o_wts, logits, k, renormalize=True):
-    """Bit-exact ids except documented near-ties; returns (ids, weights) to use downstream
-    and the number of near-tie tokens."""
+def check_routing(gpu_ids, gpu_wts, o_ids, o_wts, logits, k, renormalize=True, max_near=None):
+    """Routing ids bit-exact against the oracle, except at documented near-ties.
+
+    A token whose GPU ids differ from the oracle's is excused only when the difference is one
+    that fp32 rounding of a near-tie can cause:
+      * a different expert SET only when the oracle's own margin between its k-th and
+        (k+1)-th logit (the gap it reports) is below NEAR_TIE, and every GPU expert's logit
+        is at least the oracle's k-th minus NEAR_TIE;
+      * a different SLOT ORDER only between experts whose logits lie within NEAR_TIE: the GPU
+        slots must descend in the oracle's logits up to NEAR_TIE.
+    At most `max_near` tokens (default max(1, M // 50)) may be excused.  The affinities are
+    checked against the fp64 softmax of the ids actually used.  Returns (ids, weights) to
+    use downstream and the number of excused tokens."""
     gpu_ids = np.asarray(gpu_ids)
     gpu_wts = np.asarray(gpu_wts, np.float64)
+    M = o_ids.shape[0]
+    if max_near is None:
+        max_near = max(1, M // 50)
+    _, _, gap = oracle.topk_softmax(logits, k, renormalize)
     ids = o_ids.copy()
     wts = o_wts.copy()
     near = 0
-    for m in range(o_ids.shape[0]):
+    for m in range(M):
         if np.array_equal(gpu_ids[m], o_ids[m]):
             continue
         l = logits[m]
-        kth = np.sort(l)[::-1][k - 1]
-        assert np.all(l[gpu_ids[m]] >= kth - NEAR_TIE), "token %d: GPU ids %s not a top-%d" % (
-            m, gpu_ids[m], k)
-        assert len(set(gpu_ids[m].tolist())) == k
+        g = gpu_ids[m]
+        assert len(set(g.tolist())) == k and np.all((g >= 0) & (g < l.size)), \
+            "token %d: GPU ids %s are not k distinct experts" % (m, g)
+        if set(g.tolist()) != set(o_ids[m].tolist()):
+            assert gap[m] < NEAR_TIE, "token %d: GPU set %s, oracle %s, oracle gap %.3e" % (
+                m, g, o_ids[m], gap[m])
+            kth = l[o_ids[m][k - 1]]
+            assert np.all(l[g] >= kth - NEAR_TIE), "token %d: GPU ids %s not a top-%d" % (m, g, k)
+        for j in range(k - 1):
+            assert l[g[j]] >= l[g[j + 1]] - NEAR_TIE, \
+                "token %d: GPU slot %d (expert %d) below slot %d (expert %d)" % (
+                    m, j, g[j], j + 1, g[j + 1])
         near += 1
-        ids[m] = gpu_ids[m]
-        sel = l[gpu_ids[m]]
+        ids[m] = g
+        sel = l[g]
         if renormalize:
             ex = np.exp(sel - sel.max())
             wts[m] = ex / ex.sum()
         else:
             ex = np.exp(l - l.max())
             wts[m] = np.exp(sel - l.max()) / ex.sum()
+    assert near <= max_near, "%d near-tie tokens excused, at most %d allowed" % (near, max_near)
     assert np.allclose(gpu_wts, wts, rtol=1e-4, atol=1e-6), np.abs(gpu_wts - wts).max()
     return ids, wts, near
+
+
+def near_tie_count(logits, k):
+    """Tokens whose oracle margin between the k-th and (k+1)-th logit is below NEAR_TIE (the
+    ones whose selection fp32 rounding could legitimately change)."""
+    _, _, gap = oracle.topk_softmax(logits, k)
+    return int((gap < NEAR_TIE).sum())
 
 
 def oracle_ffn(layer, h, ids, wts, residual=None, tokens=None):
@@ -96,7 +127,7 @@ def oracle_ffn(layer, h, ids, wts, residual=None, tokens=None):
     local = np.array([[remap.get(int(e), -1) for e in row] for row in sub_ids], np.int32)
     if not used:  # no valid route at all: the block output is the residual (or zero)
         used = [0]
-    w = syn.oracle_weights(layer, used)
+    w = oracle.host_weights(layer, used)
     hs = h[torch.as_tensor(tokens, device=h.device, dtype=torch.long)]
     res = None
     if residual is not None:

@@ -328,7 +328,7 @@ def pin_single_expert_textbook_swiglu():
     x = f64(syn.bits(h))
     res = syn.make_hidden(wl, seed=9, device="cpu", tag="res")
     ids = np.zeros((wl.M, 1), np.int32)
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, np.ones((wl.M, 1)),
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, np.ones((wl.M, 1)),
                             residual=syn.bits(res))
     ref = f64(syn.bits(res)) + (silu(x @ wg[0]) * (x @ wu[0])) @ wd[0]
     assert np.allclose(out, ref, rtol=1e-11, atol=1e-13), np.abs(out - ref).max()
@@ -357,7 +357,7 @@ def pin_dense_all_experts_reference():
     rng = np.random.default_rng(0)
     ids = np.stack([rng.permutation(wl.E)[:wl.k] for _ in range(wl.M)]).astype(np.int32)
     a = rng.random((wl.M, wl.k))
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     ref = _all_experts_reference(layer, h, ids, a)
     assert np.allclose(out, ref, rtol=1e-10, atol=1e-12), np.abs(out - ref).max()
 
@@ -375,7 +375,7 @@ def pin_channel_view():
     act = np.einsum("mh,mjhc->mjc", x, wg[ids])
     act = silu(act) * np.einsum("mh,mjhc->mjc", x, wu[ids])
     ref = np.einsum("mj,mjc,mjch->mh", a, act, wd[ids])
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
 
 
@@ -385,7 +385,7 @@ def pin_zero_cases():
     res = syn.make_hidden(wl, seed=8, device="cpu", tag="res")
     ids = np.array([[0, 1], [2, 3], [1, 2]], np.int32)
     a = np.full((3, 2), 0.5)
-    w = syn.oracle_weights(layer)
+    w = oracle.host_weights(layer)
     # h = 0  =>  out = residual
     out = oracle.expert_ffn(np.zeros_like(syn.bits(h)), w, ids, a, residual=syn.bits(res))
     assert np.array_equal(out, f64(syn.bits(res)))
@@ -401,7 +401,7 @@ def pin_zero_cases():
 def pin_invalid_routes_contribute_nothing():
     wl = small_workload(E=4, k=3, M=3, H=32, I=16)
     layer, h = small_layer(wl, seed=10)
-    w = syn.oracle_weights(layer)
+    w = oracle.host_weights(layer)
     ids = np.array([[0, -1, 2], [4, 1, 3], [2, 3, 9]], np.int32)
     a = np.array([[0.2, 0.3, 0.5], [0.6, 0.3, 0.1], [0.4, 0.4, 0.2]])
     out = oracle.expert_ffn(syn.bits(h), w, ids, a)
@@ -424,7 +424,7 @@ def pin_vq_equals_decoded_dense():
              "w_gate": bf16_bits(wg), "w_up": bf16_bits(wu), "w_down": syn.bits(layer["w_down"])}
     ids = np.array([[0, 4], [3, 1], [2, 0]], np.int32)
     a = np.array([[0.6, 0.4], [0.5, 0.5], [0.25, 0.75]])
-    out_vq = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out_vq = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     out_dense = oracle.expert_ffn(syn.bits(h), dense, ids, a)
     assert np.array_equal(out_vq, out_dense)
 
@@ -438,7 +438,7 @@ def pin_vq_d8_equals_decoded_dense():
              "w_gate": bf16_bits(wg), "w_up": bf16_bits(wu), "w_down": syn.bits(layer["w_down"])}
     ids = np.array([[1, 3], [4, 0], [2, 2]], np.int32)
     a = np.array([[0.7, 0.3], [0.5, 0.5], [0.4, 0.6]])
-    out_vq = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out_vq = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     out_dense = oracle.expert_ffn(syn.bits(h), dense, ids, a)
     assert np.array_equal(out_vq, out_dense)
 
@@ -465,7 +465,7 @@ def pin_vq_projection_codebook():
             g = Tg[np.arange(Q)[:, None], jg[e]].sum(axis=0)
             u = Tu[np.arange(Q)[:, None], ju[e]].sum(axis=0)
             ref[m] += a[m, j] * ((silu(g) * u) @ wd[e])
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     assert np.allclose(out, ref, rtol=1e-11, atol=1e-13)
 
 
@@ -482,7 +482,7 @@ def pin_vq_constant_index_is_dense():
     x = f64(syn.bits(h))
     wd = f64(syn.bits(layer["w_down"]))
     ids = np.array([[1], [0]], np.int32)
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, np.ones((2, 1)))
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, np.ones((2, 1)))
     ref = np.stack([(silu(x[m] @ wg[ids[m, 0]]) * (x[m] @ wu[ids[m, 0]])) @ wd[ids[m, 0]]
                     for m in range(2)])
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
@@ -510,7 +510,7 @@ def pin_vqlr_equals_materialised_dense():
         for j in range(wl.k):
             e = ids[m, j]
             ref[m] += a[m, j] * ((silu(x[m] @ wg[e]) * (x[m] @ wu[e])) @ wd[e])
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     assert np.allclose(out, ref, rtol=1e-11, atol=1e-13)
 
 
@@ -525,8 +525,8 @@ def pin_vqlr_zero_coefficients_is_vq():
     vq["kind"] = syn.W_VQ
     ids = np.array([[2, 0], [1, 2]], np.int32)
     a = np.array([[0.3, 0.7], [0.8, 0.2]])
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
-    out_vq = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(vq), ids, a)
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
+    out_vq = oracle.expert_ffn(syn.bits(h), oracle.host_weights(vq), ids, a)
     assert np.array_equal(out, out_vq)
 
 
@@ -543,7 +543,7 @@ def pin_vqlr_zero_codebook_is_low_rank_swiglu():
     cg, cu = f64(syn.bits(layer["c_gate"])), f64(syn.bits(layer["c_up"]))
     wd = f64(syn.bits(layer["w_down"]))
     ids = np.array([[1], [0]], np.int32)
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, np.ones((2, 1)))
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, np.ones((2, 1)))
     ref = np.stack([(silu((x[m] @ dg) @ cg[ids[m, 0]]) * ((x[m] @ du) @ cu[ids[m, 0]]))
                     @ wd[ids[m, 0]] for m in range(2)])
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
@@ -563,7 +563,7 @@ def pin_vqlr_projections_are_separate():
     x = f64(syn.bits(h))
     ids = np.array([[1]], np.int32)
     g = x[0] @ wg[1]
-    out = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, np.ones((1, 1)))
+    out = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, np.ones((1, 1)))
     assert np.allclose(out[0], (silu(g) * g) @ wd[1], rtol=1e-12, atol=1e-14)
 
 
@@ -571,7 +571,7 @@ def pin_vqlr_projections_are_separate():
 def pin_decode_block_composition():
     wl = small_workload(E=8, k=3, M=4, H=64, I=16, router_bias=True)
     layer, h = small_layer(wl, seed=15)
-    w = syn.oracle_weights(layer)
+    w = oracle.host_weights(layer)
     bias = layer["bias"].numpy()
     ids, wts, gap, out = oracle.decode_block(syn.bits(h), syn.bits(layer["w_router"]), bias,
                                              w, wl.k)
@@ -581,6 +581,30 @@ def pin_decode_block_composition():
     ref = _all_experts_reference(layer, h, ids, wts)
     assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
     assert np.allclose(wts.sum(axis=1), 1.0, atol=1e-15)
+
+
+def pin_threads_do_not_change_results():
+    """The expert loop on several threads (whole tokens each) gives the single-threaded
+    results bit for bit, with the intermediates, and the all-experts reference still holds."""
+    wl = small_workload(E=8, k=3, M=13, H=64, I=32)
+    layer, h = small_layer(wl, seed=21)
+    rng = np.random.default_rng(21)
+    ids = np.stack([rng.permutation(wl.E)[:wl.k] for _ in range(wl.M)]).astype(np.int32)
+    ids[3, 1] = -1  # an invalid route among them
+    a = rng.random((wl.M, wl.k))
+    w = oracle.host_weights(layer)
+    before = oracle.set_threads(0)
+    try:
+        oracle.set_threads(1)
+        one = oracle.expert_ffn(syn.bits(h), w, ids, a, want_intermediates=True)
+        oracle.set_threads(4)
+        many = oracle.expert_ffn(syn.bits(h), w, ids, a, want_intermediates=True)
+    finally:
+        oracle.set_threads(before)
+    for x, y in zip(one, many):
+        assert np.array_equal(x, y)
+    ref = _all_experts_reference(layer, h, ids, a)
+    assert np.allclose(many[0], ref, rtol=1e-10, atol=1e-12)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -185,24 +185,49 @@ def test_reader_validation_without_gpu(lib):
 
 
 def test_library_block_size_without_gpu(lib):
-    """The alignment block size the library picks: the caller's b for VQ forms 0 and 1; for
-    dense weights and VQ form 2 a tile width (16 at one token; 64 for VQ form 2 from 16
-    routes per expert); 0 on invalid arguments."""
+    """The alignment block size of the decode block: the caller's b when b > 0; for b = 0 the
+    library's pick -- 8 for VQ forms 0 and 1, for dense weights and VQ form 2 a tile width
+    (16 at one token; 64 for VQ form 2 from 16 routes per expert); 0 on invalid arguments."""
     L = moe.lib()
     d = _weights()
-    assert L.moe_library_block_size(ctypes.byref(d), 1, 8, 8) == 16
-    assert L.moe_library_block_size(ctypes.byref(d), 4096, 8, 8) == 64
+    assert L.moe_library_block_size(ctypes.byref(d), 1, 8, 8) == 8  # binding
+    assert L.moe_library_block_size(ctypes.byref(d), 4096, 8, 8) == 8
+    assert L.moe_library_block_size(ctypes.byref(d), 1, 8, 0) == 16  # the library's pick
+    assert L.moe_library_block_size(ctypes.byref(d), 4096, 8, 0) == 64
     assert L.moe_library_block_size(ctypes.byref(d), 1, 8, 12) == 0  # invalid b
+    assert L.moe_library_block_size(ctypes.byref(d), 1, 8, -8) == 0
     assert L.moe_library_block_size(None, 1, 8, 8) == 0
     v = _weights(kind=moe.MOE_W_VQ_GATEUP)
-    assert L.moe_library_block_size(ctypes.byref(v), 21, 8, 8) == 8
+    assert L.moe_library_block_size(ctypes.byref(v), 21, 8, 3) == 3
+    assert L.moe_library_block_size(ctypes.byref(v), 21, 8, 0) == 8
     v.vq_form = 2
-    assert L.moe_library_block_size(ctypes.byref(v), 255, 8, 8) == 16  # 15.9 routes per expert
-    assert L.moe_library_block_size(ctypes.byref(v), 256, 8, 8) == 64
-    # the workspace covers either tile width
-    assert L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 8) >= max(
+    assert L.moe_library_block_size(ctypes.byref(v), 255, 8, 0) == 16  # 15.9 routes per expert
+    assert L.moe_library_block_size(ctypes.byref(v), 256, 8, 0) == 64
+    # b = 0: the workspace covers either tile width; b > 0: exactly that b's layout
+    assert L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 0) >= max(
         L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 16),
         L.moe_workspace_bytes(ctypes.byref(d), 64, 8, 64))
+    assert L.moe_workspace_bytes(ctypes.byref(d), 64, 8, -1) == 0
+
+
+def test_workspace_layout_without_gpu(lib):
+    """moe_workspace_layout: the alignment's place in the workspace, for the resolved b."""
+    L = moe.lib()
+    d = _weights()
+    out = moe.WorkspaceLayout()
+    for M, b, want_b in ((1, 8, 8), (21, 0, 16), (4096, 0, 64), (3, 1, 1)):
+        assert L.moe_workspace_layout(ctypes.byref(d), M, 8, b, ctypes.byref(out)) == moe.MOE_OK
+        assert out.b == want_b
+        assert out.cap == L.moe_align_capacity(M, 8, d.E, want_b)
+        # 256-byte aligned regions after the status word, each large enough, inside the size
+        assert out.status == 0
+        assert out.sorted_route_ids % 256 == 0 and out.sorted_route_ids >= 64
+        assert out.expert_block_ids >= out.sorted_route_ids + 4 * out.cap
+        assert out.num_padded >= out.expert_block_ids + 4 * (out.cap // want_b)
+        assert out.num_padded + 4 <= L.moe_workspace_bytes(ctypes.byref(d), M, 8, b)
+    assert L.moe_workspace_layout(ctypes.byref(d), 1, 8, 12, ctypes.byref(out)) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_workspace_layout(None, 1, 8, 8, ctypes.byref(out)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_workspace_layout(ctypes.byref(d), 1, 8, 8, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_vq_form_validation_without_gpu(lib):

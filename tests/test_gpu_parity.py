@@ -1,4 +1,6 @@
 """CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -131,17 +133,20 @@ def test_expert_ffn_small(M, k, E, H, I, b):
     res = syn.make_hidden(wl, seed=5, device=DEV, tag="res")
     t_ids = torch.as_tensor(ids, device=DEV)
     t_a = torch.as_tensor(a, device=DEV)
-    ws = moe.alloc_workspace(layer, M, k, b)
-    out = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, residual=res, workspace=ws)
+    ws = moe.alloc_workspace(layer, M, k, 0)
+    out = moe.moe_expert_ffn(h, layer, t_ids, t_a, 0, residual=res, workspace=ws)
     assert moe.moe_read_device_status(ws) == 0
     ref = G.oracle_ffn(layer, h, ids, a, residual=res)
     G.assert_close_block(G.to_f64(out), ref, "expert_ffn %s" % (SMALL,))
-    # the same call with the caller's own b-row alignment (the library aligned in 16- or
-    # 64-row blocks of its own): a route's bits do not depend on its block
+    # the same routes aligned by the library in b-row blocks, and in the caller's own b-row
+    # alignment (the first call aligned in 16- or 64-row blocks of the library's choice): a
+    # route's bits do not depend on its block
+    ws_b = moe.alloc_workspace(layer, M, k, b)
+    out_b = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, residual=res, workspace=ws_b)
     srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
     out2 = moe.moe_expert_ffn(h, layer, t_ids, t_a, b, alignment=(srt, blk, npad), residual=res,
-                              workspace=ws)
-    assert torch.equal(out, out2)
+                              workspace=ws_b)
+    assert torch.equal(out, out_b) and torch.equal(out, out2)
 
 
 def test_expert_ffn_invalid_ids_and_status():
@@ -285,6 +290,36 @@ def test_layer_m21_alignment_and_20_run_determinism():
     for run in range(20):
         out2, ids2, wts2 = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
         assert torch.equal(out2, out) and torch.equal(ids2, ids) and torch.equal(wts2, wts), run
+
+
+@pytest.mark.parametrize("name,M,b", [
+    ("layer_m21", 1, 0), ("layer_m21", 1, 8), ("layer_m21", 2, 8), ("layer_m21", 2, 16),
+    ("layer_m21", 3, 8), ("layer_m21", 8, 16), ("layer_m21", 16, 8), ("layer_m21", 16, 0),
+    ("layer_m21", 21, 8), ("layer_m21", 40, 0), ("vq_d4", 1, 8), ("vq_d4", 2, 3),
+    ("vq_d4", 9, 8)])
+def test_decode_block_alignment_bit_exact(name, M, b):
+    """The alignment the decode block itself builds -- in the router's launch for up to 2
+    tokens, in one launch with the row tiles up to 128 routes, in the stand-alone kernel
+    above -- equals the oracle's alignment of the call's own ids element by element: the
+    sorted route ids with the sentinel tail, the block vector with its -1 tail, the row
+    count.  The workspace starts dirty, so every entry must have been written."""
+    wl = syn.workload(name, M=M)
+    layer = _workload_layer(name)
+    h = syn.make_hidden(wl, M=M, seed=40 + M, device=DEV)
+    ws = moe.alloc_workspace(layer, M, wl.k, b)
+    lay = moe.moe_workspace_layout(layer, M, wl.k, b)
+    ws.fill_(0xFF)
+    ws[:lay["zero_bytes"]] = 0  # the status word and counters start at zero, as required
+    out, ids, wts = moe.moe_decode_block(h, layer, wl.k, b, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    assert lay["b"] == (b if b else moe.moe_library_block_size(layer, M, wl.k, 0))
+    srt, blk, npad = moe.workspace_alignment(ws, lay)
+    o_srt, o_blk, o_np = oracle.align(ids.cpu().numpy(), wl.E, lay["b"])
+    assert int(npad.item()) == o_np
+    assert np.array_equal(srt.cpu().numpy(), o_srt)
+    assert np.array_equal(blk.cpu().numpy(), o_blk)
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+    G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts, logits, wl.k)
 
 
 def test_batch_invariance_bitwise():
@@ -456,8 +491,8 @@ def test_vq_tensor_core_bits_same_in_both_tile_widths():
     ids = _random_ids(rng, M, k, E)
     a = _random_affinities(rng, M, k)
     t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
-    assert moe.moe_library_block_size(layer, M, k, 8) == 64
-    wide = moe.moe_expert_ffn(h, layer, t_ids, t_a, 8)  # library: 64-row blocks
+    assert moe.moe_library_block_size(layer, M, k, 0) == 64
+    wide = moe.moe_expert_ffn(h, layer, t_ids, t_a, 0)  # library: 64-row blocks
     G.assert_close_block(G.to_f64(wide), G.oracle_ffn(layer, h, ids, a), "vq 64-row tiles")
     for b in (1, 8, 16, 24, 64, 128):
         srt, blk, npad = moe.moe_align_block_size(t_ids, E, b)
@@ -466,7 +501,7 @@ def test_vq_tensor_core_bits_same_in_both_tile_widths():
     for sub in ([7], [0, 39], list(range(3, 9))):
         sel = torch.as_tensor(sub, device=DEV)
         o = moe.moe_expert_ffn(h[sel].contiguous(), layer, t_ids[sel].contiguous(),
-                               t_a[sel].contiguous(), 8)  # library: 16-row blocks
+                               t_a[sel].contiguous(), 0)  # library: 16-row blocks
         assert torch.equal(o, wide[sel]), sub
 
 
@@ -483,7 +518,7 @@ def test_vq_tensor_core_block_every_m_and_invariance():
         ws = moe.alloc_workspace(layer, M, wl.k, wl.b)
         if M in (1, 7, 12):
             ws.fill_(0xFF)
-            ws[:64] = 0
+            ws[:moe.moe_workspace_layout(layer, M, wl.k, wl.b)["zero_bytes"]] = 0
         out, ids, wts = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
         assert moe.moe_read_device_status(ws) == 0
         assert torch.equal(ids, ids16[:M]) and torch.equal(out, out16[:M]), M
@@ -500,9 +535,9 @@ def test_vq_tensor_core_block_every_m_and_invariance():
     assert all(torch.equal(r, out16) for r in runs)
     # 256 tokens (16 routes per expert) run 64-row tiles: the 16 shared tokens keep their
     # bits; sampled parity
-    assert moe.moe_library_block_size(layer, 256, wl.k, wl.b) == 64
+    assert moe.moe_library_block_size(layer, 256, wl.k, 0) == 64
     h256 = torch.cat([h16, syn.make_hidden(wl, M=240, seed=10, device=DEV)])
-    out256, ids256, wts256 = moe.moe_decode_block(h256, layer, wl.k, wl.b)
+    out256, ids256, wts256 = moe.moe_decode_block(h256, layer, wl.k, 0)
     assert torch.equal(ids256[:16], ids16) and torch.equal(out256[:16], out16)
     o_ids, o_wts, _, logits = G.oracle_routing(layer, h256, wl.k)
     use_ids, use_wts, _ = G.check_routing(ids256.cpu().numpy(), wts256.cpu().numpy(), o_ids,
@@ -575,25 +610,34 @@ def test_vqlr_block_every_m_1_to_16(name):
 
 
 def test_large_m256_sampled_tokens():
-    layer, h, ws, out, ids, wts = _check_block("large_m256",
-                                               tokens=np.array([0, 1, 77, 128, 200, 254, 255]))
+    """The large-batch layer (H=4096, I=1536, b=64, biased router): 64 of its 256 tokens (every
+    fourth, plus the last) against the oracle, which runs its routes on all host cores."""
+    tokens = np.unique(np.concatenate([np.arange(0, 256, 4), [255]]))
+    before = oracle.set_threads(0)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        layer, h, ws, out, ids, wts = _check_block("large_m256", tokens=tokens)
+    finally:
+        oracle.set_threads(before)
     wl = syn.WORKLOADS["large_m256"]
     out2, _, _ = moe.moe_decode_block(h, layer, wl.k, wl.b, workspace=ws)
     assert torch.equal(out, out2)
 
 
 def test_decode_block_picks_the_gemm_regime_for_large_batches():
-    """From 24 routes per expert on the default layer (one wave of 16-row units' weights fits
-    in L2 there) the library aligns in 64-row blocks (64-row tiles) whatever b is, below
-    that in 16-row blocks; the bits are the same either way."""
+    """Left to the library (b = 0), the default layer aligns in 64-row blocks (64-row tiles)
+    from 24 routes per expert (one wave of 16-row units' weights fits in L2 there), below that
+    in 16-row blocks; the caller's b = 8 or 64 is kept; the bits are the same every way."""
     wl = syn.workload("layer_m21", M=384)
     layer = _workload_layer("layer_m21")
-    assert moe.moe_library_block_size(layer, 384, wl.k, 8) == 64
-    assert moe.moe_library_block_size(layer, 64, wl.k, 8) == 16
+    assert moe.moe_library_block_size(layer, 384, wl.k, 0) == 64
+    assert moe.moe_library_block_size(layer, 64, wl.k, 0) == 16
+    assert moe.moe_library_block_size(layer, 384, wl.k, 8) == 8
     h = syn.make_hidden(wl, M=384, seed=64, device=DEV)
     out8, ids, wts = moe.moe_decode_block(h, layer, wl.k, 8)
     out64, _, _ = moe.moe_decode_block(h, layer, wl.k, 64)
-    assert torch.equal(out8, out64)  # the same regime, the same bits
+    out0, _, _ = moe.moe_decode_block(h, layer, wl.k, 0)
+    assert torch.equal(out8, out64) and torch.equal(out8, out0)
     assert torch.equal(moe.moe_expert_ffn(h, layer, ids, wts, 8), out8)
     tokens = np.array([0, 170, 383])
     o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
@@ -642,8 +686,8 @@ def test_route_bits_independent_of_batch_block_and_tile_width():
     ids = _random_ids(rng, M, k, E)
     a = _random_affinities(rng, M, k)
     t_ids, t_a = torch.as_tensor(ids, device=DEV), torch.as_tensor(a, device=DEV)
-    assert moe.moe_library_block_size(layer, M, k, 8) == 64
-    base = moe.moe_expert_ffn(h, layer, t_ids, t_a, 8)  # library: 64-row blocks
+    assert moe.moe_library_block_size(layer, M, k, 0) == 64
+    base = moe.moe_expert_ffn(h, layer, t_ids, t_a, 0)  # library: 64-row blocks
     ref = G.oracle_ffn(layer, h, ids, a)
     G.assert_close_block(G.to_f64(base), ref, "cross-regime base")
     for b in (1, 8, 16, 24, 64, 128):
@@ -653,7 +697,7 @@ def test_route_bits_independent_of_batch_block_and_tile_width():
     for sub in ([3], [0, 71], list(range(10, 17)), list(range(71, -1, -5))):
         sel = torch.as_tensor(sub, device=DEV)
         o = moe.moe_expert_ffn(h[sel].contiguous(), layer, t_ids[sel].contiguous(),
-                               t_a[sel].contiguous(), 8)  # library: 16-row blocks
+                               t_a[sel].contiguous(), 0)  # library: 16-row blocks
         assert torch.equal(o, base[sel]), sub
 
 
@@ -668,11 +712,14 @@ def test_decode_block_on_a_dirty_workspace(M, b):
     res = syn.make_hidden(wl, M=M, seed=32, device=DEV, tag="res")
     ws = moe.alloc_workspace(layer, M, wl.k, b)
     dirty = torch.full_like(ws, 0xFF)
-    dirty[:64] = 0  # the status word starts clear, as the entry points require
+    # the status word and the counters start clear, as the entry points require
+    dirty[:moe.moe_workspace_layout(layer, M, wl.k, b)["zero_bytes"]] = 0
     out_d, ids_d, _ = moe.moe_decode_block(h, layer, wl.k, b, residual=res, workspace=dirty)
     out_z, ids_z, wts_z = moe.moe_decode_block(h, layer, wl.k, b, residual=res, workspace=ws)
     assert moe.moe_read_device_status(dirty) == 0
     assert torch.equal(ids_d, ids_z) and torch.equal(out_d, out_z)
+    zb = moe.moe_workspace_layout(layer, M, wl.k, b)["zero_bytes"]
+    assert int(dirty[:zb].count_nonzero().item()) == 0  # every call leaves them zero
     o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
     use_ids, use_wts, _ = G.check_routing(ids_z.cpu().numpy(), wts_z.cpu().numpy(), o_ids, o_wts,
                                           logits, wl.k)

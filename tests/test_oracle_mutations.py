@@ -26,7 +26,10 @@ MUTANTS = [
                            "o[n] = 0.0;")]),
     ("down_columns_reversed", [("y[n] += p[i] * bf16_bits_to_double(drow[n]);",
                                 "y[n] += p[i] * bf16_bits_to_double(drow[H - 1 - n]);")]),
-    ("affinity_of_slot0", [("o[n] += a[r] * y[n];", "o[n] += a[(size_t)m * k] * y[n];")]),
+    ("affinity_of_slot0", [("o[n] += a[r] * yall[r * H + n];",
+                            "o[n] += a[(size_t)m * k] * yall[r * H + n];")]),
+    ("combine_slots_reversed", [("const size_t r = (size_t)m * k + j;\n            const int e = topk_ids[r];",
+                                 "const size_t r = (size_t)m * k + (k - 1 - j);\n            const int e = topk_ids[(size_t)m * k + j];")]),
     ("tie_to_higher_id", [("if (best < 0 || v > bestv)", "if (best < 0 || v >= bestv)")]),
     ("select_in_fp64", [("float bestv = 0.0f;", "double bestv = 0.0;"),
                         ("float v = to_f32(l[e]);", "double v = l[e];")]),

@@ -108,7 +108,7 @@ def test_full_budget_reader_is_the_exact_block():
     rd = R.build(wg, wu, wd, s, rank=16)
     ids = np.array([[0, 3, 5, 7], [1, 2, 3, 4], [6, -1, 0, 2]], np.int32)
     a = np.array([[0.4, 0.3, 0.2, 0.1], [0.25] * 4, [0.5, 0.0, 0.3, 0.2]])
-    ref = oracle.expert_ffn(syn.bits(h), syn.oracle_weights(layer), ids, a)
+    ref = oracle.expert_ffn(syn.bits(h), oracle.host_weights(layer), ids, a)
     x = h.to(torch.float64).numpy()
     for m in range(3):
         out, sel, _, _ = R.reader_token(x[m], ids[m], a[m], wg, wu, wd, rd, s,
