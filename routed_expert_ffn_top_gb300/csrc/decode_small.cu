@@ -4,17 +4,17 @@
 // The block is the one of "A Multi-Engine Dataflow for MoE Decoding on Scratchpad-Based
 // Tensor Accelerators" (MoE block background; stage-3 activation; Section 4.3) with the
 // alignment of "Route-Block Membership Selects Packed-AWQ Arithmetic" (Sections 2.1, 5.3).
-// At one to four tokens the expert weights are the only real traffic (75 MB per layer at
-// one token), and every step of a chain of kernels costs a launch boundary on the critical
-// path before the weight stream starts and after it ends.  So one grid does it all:
+// At one or two tokens the expert weights are the only real traffic (75 MB per layer at one
+// token), and every step of a chain of kernels costs a launch boundary on the critical path
+// before the weight stream starts and after it ends.  So one grid does it all:
 //
 //  1. Routing.  CTAs 0..7 each hold one eighth of the rows of W_r (copied before the wait
 //     for the previous grid) and reduce it against h to partial logits, with exactly the
 //     arithmetic of the router kernel's CTA of the same rank (the same row groups and
 //     orders, so the logits and the selection are bitwise those of the multi-kernel path).
 //     They publish the partials with a release count; every CTA acquires them, and runs the
-//     router's own finalisation (logits in slice order, top-k as ranks, softmax) and the
-//     alignment (align_small) itself, in shared memory: no CTA waits for another's result.
+//     router's own finalisation (logits in slice order, the warp arg-max top-k, softmax)
+//     and the alignment itself (one warp, at most 32 routes): no CTA waits for another's result.
 //  2. Experts.  Units as in the fused grid (gemm_tc05.cu): gate/up units (tile, 64 channels
 //     of I) first, then down units (tile, 128 channels of H), CTA c taking units c, c + G ...
 //     The weight boxes come by TMA (warp 0); the tile's few token rows (gate/up: h; down:
@@ -38,9 +38,12 @@
 namespace moe {
 
 using GS = GTile<16>;
-constexpr int kSThreads = 224;  // producer, MMA, 4 epilogue warps, row loader
+// producer, MMA, 4 epilogue warps, row loader; 9 more warps that only help with the routing
+// (512 threads, so that the router's dot products run one row group and expert pair per
+// thread, as in the router kernel)
+constexpr int kSThreads = kRouterThreads;
 constexpr int kSLoaderWarp = 6;
-static_assert(kSThreads % 32 == 0 && kSThreads >= kSmallMaxRoutes, "one thread per route");
+static_assert(kSmallMaxRoutes <= 32, "the alignment runs in one warp");
 
 struct SmallState {
     int32_t ids[kSmallMaxRoutes];
@@ -58,9 +61,7 @@ __host__ __device__ constexpr size_t small_routing_bytes(int M, int H, int E) {
     return (size_t)(H / kRouterCluster) * E * 2 +              // W_r slice
            (size_t)M * (H / kRouterCluster) * 2 +              // h slices
            (size_t)(kRouterThreads / (E / 2)) * M * E * 4 +    // row-group sums
-           (size_t)M * kRouterCluster * E * 4 +                // the 8 partials of every token
-           (size_t)M * E * 8 + (size_t)M * 32 * 8 +            // keys and values, slots
-           (size_t)(align_small_smem_ints(kSThreads) + kSmallMaxRoutes) * 4 + 1024;
+           (size_t)M * kRouterCluster * E * 4 + 1024;          // the 8 partials of every token
 }
 
 __device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t *p, int32_t v) {
@@ -353,18 +354,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
     float *red = reinterpret_cast<float *>(p);
     p += (size_t)(kRouterThreads / (E / 2)) * M * E * 4;
     float *part_s = reinterpret_cast<float *>(p);
-    p += (size_t)M * kRouterCluster * E * 4;
-    uint32_t *key_s = reinterpret_cast<uint32_t *>(p);
-    p += (size_t)M * E * 4;
-    float *val_s = reinterpret_cast<float *>(p);
-    p += (size_t)M * E * 4;
-    int32_t *slot_e = reinterpret_cast<int32_t *>(p);
-    p += (size_t)M * 32 * 4;
-    float *slot_v = reinterpret_cast<float *>(p);
-    p += (size_t)M * 32 * 4;
-    int32_t *align_sm = reinterpret_cast<int32_t *>(p);
-    p += (size_t)align_small_smem_ints(kSThreads) * 4;
-    int32_t *pos_s = reinterpret_cast<int32_t *>(p);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_gate);
@@ -427,33 +416,58 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
     }
     __syncthreads();
-    route_finalize(part_s, M, E, a.k, a.bias, !ctl.abort, 1, key_s, val_s, slot_e, slot_v,
-                   [&](int i, int j, int id, float wt) {
-                       st.ids[i * a.k + j] = id;
-                       st.wts[i * a.k + j] = wt;
-                       if (blockIdx.x == 0) {
-                           a.topk_ids[(size_t)i * a.k + j] = id;
-                           a.topk_wts[(size_t)i * a.k + j] = wt;
-                       }
-                   });
+    route_finalize_any(part_s, M, E, a.k, a.bias, !ctl.abort, 1,
+                       [&](int i, int j, int id, float wt) {
+                           st.ids[i * a.k + j] = id;
+                           st.wts[i * a.k + j] = wt;
+                           if (blockIdx.x == 0) {
+                               a.topk_ids[(size_t)i * a.k + j] = id;
+                               a.topk_wts[(size_t)i * a.k + j] = wt;
+                           }
+                       });
     __syncthreads();
-    // the alignment, in shared memory (CTA 0 also leaves it in the workspace)
-    int32_t *sorted_s = pos_s + kSmallMaxRoutes;
-    int32_t *blocks_s = sorted_s + a.cap;
-    int32_t *npad_s = blocks_s + a.cap / a.b;
-    align_small(st.ids, R, a.k, E, a.b, a.b, sorted_s, blocks_s, npad_s, a.cap, nullptr,
-                blockIdx.x == 0 ? a.status : nullptr, align_sm, pos_s);
-    __syncthreads();
-    const int ntiles = npad_s[0] / a.b;
-    for (int t = threadIdx.x; t < ntiles; t += blockDim.x) {
-        st.tile_e[t] = blocks_s[t];
-        int n = 0;
-        for (int row = 0; row < a.b && n < kSmallMaxTokens; ++row) {
-            const int r = sorted_s[(size_t)t * a.b + row];
-            if (r < 0 || r >= R) break;  // the routes of a block come first
-            st.tile_r[t][n++] = r;
+    // The alignment of the (at most 32) routes in one warp, lane r holding route r: the lanes
+    // of one expert find each other (match), a route's row is the padded rows of the experts
+    // below its own plus the routes of its expert before it -- the order of align_core: experts
+    // ascending, routes ascending, each expert padded to a multiple of b with sentinels.
+    if (warp == 0) {
+        const int b = a.b;
+        const int e = lane < R ? st.ids[lane] : -1;
+        const bool valid = lane < R && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int lower = __popc(peers & ((1u << lane) - 1u));
+        const int n = __popc(peers);
+        const bool leader = valid && lower == 0;
+        const int padded = leader ? (n + b - 1) / b * b : 0;
+        int off = 0, total = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const int eq = __shfl_sync(0xffffffffu, e, q);
+            const int pq = __shfl_sync(0xffffffffu, padded, q);
+            total += pq;
+            if (pq != 0 && eq < e) off += pq;
         }
-        st.tile_n[t] = n;
+        const int pos = valid ? off + lower : -1;
+        if (valid) st.tile_r[pos / b][pos % b] = lane;  // pos % b = lower % b < M
+        if (leader)
+            for (int q = 0; q < padded / b; ++q) {
+                st.tile_e[off / b + q] = e;
+                st.tile_n[off / b + q] = min(b, n - q * b);
+            }
+        if (lane == 0) st.ntiles = total / b;
+        if (blockIdx.x == 0) {  // the alignment as moe_align_block_size gives it
+            const bool any_invalid = __any_sync(0xffffffffu, lane < R && !valid);
+            for (int64_t i = lane; i < a.cap; i += 32) a.sorted[i] = R;
+            __syncwarp();
+            if (valid) a.sorted[pos] = lane;
+            if (leader)
+                for (int q = 0; q < padded / b; ++q) a.blocks[off / b + q] = e;
+            for (int64_t q = total / b + lane; q < a.cap / b; q += 32) a.blocks[q] = -1;
+            if (lane == 0) {
+                a.npad[0] = total;
+                if (any_invalid) atomicOr(a.status, MOE_DEV_INVALID_EXPERT);
+            }
+        }
     }
     if (threadIdx.x < M) {
         int n = 0;
@@ -463,13 +477,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         st.nvalid[threadIdx.x] = n;
     }
-    if (threadIdx.x == 0) st.ntiles = ntiles;
-    if (blockIdx.x == 0) {
-        for (int64_t i = threadIdx.x; i < a.cap; i += blockDim.x) a.sorted[i] = sorted_s[i];
-        for (int64_t i = threadIdx.x; i < a.cap / a.b; i += blockDim.x) a.blocks[i] = blocks_s[i];
-        if (threadIdx.x == 0) a.npad[0] = npad_s[0];
-    }
     __syncthreads();
+    const int ntiles = st.ntiles;
     // a token without a valid route: its output is the residual (or zero)
     if (blockIdx.x == 0)
         for (int t = 0; t < M; ++t)
@@ -494,7 +503,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         __syncwarp();
     } else if (warp == kSLoaderWarp) {
         small_loader(a, ctl, stages, st, f);
-    } else {
+    } else if (warp >= 2 && warp < 6) {  // the epilogue warps (warps 7.. only helped to route)
         const int quad = warp & 3;
         const int row = 32 * quad + lane;  // accumulator row: channel of the unit
         int32_t *done = a.ctl + kSmallCtlReady + a.ntiles_cap;
@@ -587,9 +596,7 @@ bool small_fits(int M, int k, int E, int H, int b) {
     if ((size_t)(H / kRouterCluster) * E * 2 > 64 * 1024) return false;  // one router pass
     const int64_t R = (int64_t)M * k;
     const int64_t cap = R + (R < E ? R : E) * (b - 1);
-    // routing scratch, then the alignment's rows and block vector, inside the ring
-    const size_t scratch = small_routing_bytes(M, H, E) + (size_t)(cap + cap / b + 4) * 4;
-    if (scratch > (size_t)GS::kStages * GS::kStageBytes) return false;
+    if (small_routing_bytes(M, H, E) > (size_t)GS::kStages * GS::kStageBytes) return false;
     return small_smem_bytes() <= 227 * 1024 && (int64_t)M * (H / kGM) <= kSmallCtlDone &&
            cap / b <= kSmallMaxRoutes;
 }

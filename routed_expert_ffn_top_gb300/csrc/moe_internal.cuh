@@ -149,8 +149,12 @@ struct GemmArgs {
 // The whole block for a few tokens in one persistent grid (decode_small.cu): router,
 // alignment, gate/up, down and combine.  Its counters live in the workspace's control region
 // (zero between calls; the grid's last CTA restores it).
-constexpr int kSmallMaxTokens = 4;
-constexpr int kSmallMaxRoutes = 64;
+// Up to 2 tokens (same-box A/B on GB300, H=2048, I=768, E=128, k=8, us per layer, one grid
+// against router + fused expert grid + combine: M=1 28.6 / 29.8, M=2 40.5 / 40.8, M=3
+// 49.2 / 47.9, M=4 58.8 / 56.9: from three tokens the routing every CTA repeats costs more
+// than the launches it saves).
+constexpr int kSmallMaxTokens = 2;
+constexpr int kSmallMaxRoutes = 32;
 constexpr int kSmallCtlRouted = 0;  // router slices published
 constexpr int kSmallCtlExit = 1;    // CTAs finished
 constexpr int kSmallCtlReady = 32;  // ready[tiles], then done[M][H / 128]
@@ -173,7 +177,7 @@ struct SmallArgs {
     int32_t *status;
     int ntiles_cap;                   // cap / b
 };
-// Whether the one-kernel path takes (M, k, E, H, b): dense weights, 1 <= M <= 4, M*k <= 64,
+// Whether the one-kernel path takes (M, k, E, H, b): dense weights, 1 <= M <= 2, M*k <= 32,
 // b <= 16, one router pass per slice of H.
 bool small_fits(int M, int k, int E, int H, int b);
 cudaError_t launch_decode_small(const CUtensorMap &tm_gate, const CUtensorMap &tm_up,

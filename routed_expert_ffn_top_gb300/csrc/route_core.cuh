@@ -19,84 +19,98 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Finalises nt tokens.  part[(i * kRouterCluster + q) * E + e] (shared memory) holds the
-// partial logit of token i and expert e over slice q of H; the logit is the 8 partials
-// summed in slice order from zero, plus the bias (NULL: none), or -FLT_MAX for every expert
-// when !ok.  The top-k are ranks: expert e's slot is the number of experts before it in the
-// order (larger key first, ties to the lower id); the k with a slot below k are the
-// selection, already in slot order.  Four threads count a quarter of the experts each (those
-// congruent to their part modulo 4: neighbouring words, no bank conflicts) and add by
-// shuffles; they are neighbouring lanes, and E % 8 == 0 with blockDim.x % 32 == 0 keeps whole
-// warps in or out of the loop.  Then warp i takes token i (lane j holds slot j): renorm != 0
-// gives exp(l_j - l_0) / sum_{j'<k} exp(l_j' - l_0), renorm == 0 the softmax over all E at
-// the selected experts.  emit(i, j, id, weight) runs on lane j < k of warp i.  Every thread
-// of the CTA must call it; scratch key_s, val_s [nt * E] and slot_e, slot_v [nt * 32].
-template <typename Emit>
+// Finalises nt tokens, one warp per token (warp i: token i; at least nt warps).
+// part[(i * kRouterCluster + q) * E + e] (shared memory) holds the partial logit of token i and
+// expert e over slice q of H; lane l owns experts l, l + 32, ... (kPerLane of them,
+// E <= 32 * kPerLane).  The logit is the 8 partials summed in slice order from zero, plus the
+// bias (NULL: none), or -FLT_MAX for every expert when !ok.  Top-k in k rounds of a warp
+// arg-max over order-preserving keys: the largest key, ties to the lower expert id (each lane
+// scans its experts in ascending id, then the lowest id among the lanes at the maximum), so
+// slot j holds the j-th largest logit.  Then renorm != 0 gives exp(l_j - l_0) /
+// sum_{j'<k} exp(l_j' - l_0), renorm == 0 the softmax over all E at the selected experts.
+// emit(i, j, id, weight) runs on lane j < k of warp i.
+template <int kPerLane, typename Emit>
 __device__ void route_finalize(const float *part, int nt, int E, int k, const float *bias,
-                               bool ok, int renorm, uint32_t *key_s, float *val_s,
-                               int32_t *slot_e, float *slot_v, Emit emit) {
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    for (int idx = tid; idx < nt * E; idx += nthr) {
-        const int i = idx / E, e = idx - i * E;
-        float v = 0.0f;
+                               bool ok, int renorm, Emit emit) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= nt) return;
+    const int i = warp;
+    float vals[kPerLane];
+    uint32_t key[kPerLane];
 #pragma unroll
-        for (int q = 0; q < kRouterCluster; ++q) v += part[((size_t)i * kRouterCluster + q) * E + e];
-        if (bias) v += bias[e];
-        if (!ok) v = -FLT_MAX;
-        val_s[idx] = v;
-        key_s[idx] = order_key(v);
+    for (int q = 0; q < kPerLane; ++q) {
+        const int e = lane + 32 * q;
+        float v = -FLT_MAX;
+        key[q] = 0u;  // no candidate
+        if (e < E) {
+            v = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kRouterCluster; ++s) v += part[((size_t)i * kRouterCluster + s) * E + e];
+            if (bias) v += bias[e];
+            if (!ok) v = -FLT_MAX;
+            key[q] = order_key(v);
+        }
+        vals[q] = v;
     }
-    for (int idx = tid; idx < nt * 32; idx += nthr) {
-        slot_e[idx] = -1;  // no candidate (only when fewer than k logits are numbers)
-        slot_v[idx] = -FLT_MAX;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nt * E * 4; idx += nthr) {
-        const int part_q = idx & 3, ie = idx >> 2;
-        const int i = ie / E, e = ie - i * E;
-        const uint32_t *keys = key_s + (size_t)i * E;
-        const uint32_t ke = keys[e];
-        int cnt = 0;
-        // eight keys per step, all loaded before any is compared (E % 8 == 0)
-        for (int f0 = part_q; f0 < E; f0 += 32) {
-            uint32_t kk[8];
+    int my_e = -1;
+    float my_v = -FLT_MAX;
+    for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0u;
+        int bi = -1;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) kk[u] = f0 + 4 * u < E ? keys[f0 + 4 * u] : 0u;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int f = f0 + 4 * u;
-                cnt += (f < E && (kk[u] > ke || (kk[u] == ke && f < e))) ? 1 : 0;
+        for (int q = 0; q < kPerLane; ++q)
+            if (key[q] > bk) {
+                bk = key[q];
+                bi = q;
             }
-        }
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-        if (part_q == 0 && ke != 0u && cnt < k) {  // key 0: not a candidate
-            slot_e[i * 32 + cnt] = e;
-            slot_v[i * 32 + cnt] = val_s[ie];
-        }
-    }
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31;
-    if (warp < nt) {
-        const int i = warp;
-        const int my_e = lane < k ? slot_e[i * 32 + lane] : -1;
-        const float my_v = lane < k ? slot_v[i * 32 + lane] : -FLT_MAX;
-        const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
-        float denom;
-        float ex = 0.0f;
-        if (renorm) {
-            ex = (lane < k) ? expf(my_v - l0) : 0.0f;
-            denom = ex;
-        } else {
-            float s = 0.0f;
-            for (int e = lane; e < E; e += 32) s += expf(val_s[(size_t)i * E + e] - l0);
-            denom = s;
-            ex = (lane < k) ? expf(my_v - l0) : 0.0f;
-        }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t cand = (bi >= 0 && bk == mk) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+        const uint32_t be = __reduce_min_sync(0xffffffffu, cand);
+        float bv = -FLT_MAX;
+        if (be != 0xffffffffu && (int)(be & 31) == lane) {
+            const int qi = (int)(be >> 5);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
-        if (lane < k) emit(i, lane, ok ? my_e : -1, ok ? ex / denom : 0.0f);
+            for (int q = 0; q < kPerLane; ++q)
+                if (q == qi) {
+                    bv = vals[q];
+                    key[q] = 0u;  // taken
+                }
+        }
+        bv = __shfl_sync(0xffffffffu, bv, (int)(be & 31));
+        if (lane == j) {
+            my_e = be == 0xffffffffu ? -1 : (int)be;
+            my_v = bv;
+        }
     }
+    const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
+    float denom;
+    float ex = 0.0f;
+    if (renorm) {
+        ex = (lane < k) ? expf(my_v - l0) : 0.0f;
+        denom = ex;
+    } else {
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kPerLane; ++q)
+            if (lane + 32 * q < E) sum += expf(vals[q] - l0);
+        denom = sum;
+        ex = (lane < k) ? expf(my_v - l0) : 0.0f;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
+    if (lane < k) emit(i, lane, ok ? my_e : -1, ok ? ex / denom : 0.0f);
+}
+
+// route_finalize for any supported E (8 <= E <= 512): experts per lane by E.
+template <typename Emit>
+__device__ void route_finalize_any(const float *part, int nt, int E, int k, const float *bias,
+                                   bool ok, int renorm, Emit emit) {
+    if (E <= 128)
+        route_finalize<4>(part, nt, E, k, bias, ok, renorm, emit);
+    else if (E <= 256)
+        route_finalize<8>(part, nt, E, k, bias, ok, renorm, emit);
+    else
+        route_finalize<16>(part, nt, E, k, bias, ok, renorm, emit);
 }
 
 }  // namespace moe

@@ -98,8 +98,7 @@ __global__ void __launch_bounds__(kRouterThreads)
 
     // shared layout: w_s [HP][E] bf16 | x_s [TM][HS] bf16 | red [RG][TM][E] f32 |
     //                gath [GT][8][E] f32 (the partial logits of every rank) |
-    //                ids_s [8 * 32] | key_s [GT][E] | val_s [GT][E] | slot_e, slot_v [GT][32] |
-    //                bar | align scratch | aligned row of every route
+    //                ids_s [8 * 32] | bar | align scratch | aligned row of every route
     unsigned char *ptr = smem_raw;
     __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(ptr);
     ptr += (size_t)HP * E * 2;
@@ -111,14 +110,6 @@ __global__ void __launch_bounds__(kRouterThreads)
     ptr += (size_t)GT * kRouterCluster * E * 4;
     int32_t *ids_s = reinterpret_cast<int32_t *>(ptr);  // [8 * 32] every token's ids
     ptr += 8 * 32 * 4;
-    uint32_t *key_s = reinterpret_cast<uint32_t *>(ptr);
-    ptr += (size_t)GT * E * 4;
-    float *val_s = reinterpret_cast<float *>(ptr);
-    ptr += (size_t)GT * E * 4;
-    int32_t *slot_e = reinterpret_cast<int32_t *>(ptr);
-    ptr += (size_t)GT * 32 * 4;
-    float *slot_v = reinterpret_cast<float *>(ptr);
-    ptr += (size_t)GT * 32 * 4;
     uint64_t *bar = reinterpret_cast<uint64_t *>(ptr);
     ptr += 16;
     int32_t *align_sm = reinterpret_cast<int32_t *>(ptr);
@@ -237,7 +228,7 @@ __global__ void __launch_bounds__(kRouterThreads)
     const int t0 = all_ranks ? 0 : (int)rank;
     int nt = all_ranks ? TM : ((int)rank < TM ? 1 : 0);
     if (tile * TM + t0 + nt > M) nt = M - tile * TM - t0 > 0 ? M - tile * TM - t0 : 0;
-    route_finalize(gath, nt, E, k, bias, ok, renorm, key_s, val_s, slot_e, slot_v,
+    route_finalize<kPerLane>(gath, nt, E, k, bias, ok, renorm,
                    [&](int i, int j, int id, float wt) {
                        const int t = t0 + i;
                        const int m = tile * TM + t;
@@ -288,8 +279,7 @@ static size_t router_smem(int TM, int H, int E, bool fuse) {
     const int RG = kRouterThreads / (E / 2);
     const int GT = fuse ? TM : 1;
     return (size_t)(HS / router_passes(HS, E)) * E * 2 + (size_t)TM * HS * 2 + (size_t)RG * TM * E * 4 +
-           (size_t)GT * kRouterCluster * E * 4 + 8 * 32 * 4 + (size_t)GT * E * 8 +
-           (size_t)GT * 32 * 8 + 16 +
+           (size_t)GT * kRouterCluster * E * 4 + 8 * 32 * 4 + 16 +
            (fuse ? (size_t)(align_small_smem_ints(kRouterThreads) + 8 * 32) * 4 : 0);
 }
 
