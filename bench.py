@@ -264,16 +264,16 @@ def shared_bytes(wl):
     return b
 
 
-def surface_hashes(moe, layer, wl, M, h, ws, ids, out):
-    """SHA-256 of the block's surfaces after one call (the route-block page's exact-trajectory
-    record): the activation p = SiLU(g) * u (bf16) and the routed down outputs y (fp32) of the
-    valid routes in ascending route order, and the final output (bf16).  The gate/up GEMM's
-    own output (g, u) is never stored on this path: SiLU and the product are applied to the
-    accumulators."""
-    lay = moe.moe_workspace_layout(layer, M, wl.k, wl.b)
-    R, I, H = M * wl.k, wl.I, wl.H
+def surface_tensors(moe, layer, M, k, b, ws, ids):
+    """The block's intermediate surfaces as one call left them in its workspace (dense
+    weights): (valid route ids ascending, p = SiLU(g) * u [bf16, one row per valid route],
+    y = p W_down [fp32, one row per valid route]).  p is read from the one-grid path's
+    p rows, or de-swizzled from the p tiles the down GEMM reads."""
+    lay = moe.moe_workspace_layout(layer, M, k, b)
+    I, H = layer["I"], layer["H"]
+    R = M * k
     idl = ids.flatten().long()
-    valid = torch.nonzero((idl >= 0) & (idl < wl.E)).flatten()
+    valid = torch.nonzero((idl >= 0) & (idl < layer["E"])).flatten()
     y = ws[lay["y"]:lay["y"] + R * H * 4].view(torch.float32).view(R, H)[valid]
     if lay["p_rows"]:
         p = ws[lay["p_rows"]:lay["p_rows"] + R * I * 2].view(torch.bfloat16).view(R, I)[valid]
@@ -294,7 +294,20 @@ def surface_hashes(moe, layer, wl, M, h, ws, ids, out):
         pieces = ws[lay["p_tiles"]:].view(-1)
         byte_idx = (off[..., None] + torch.arange(16, device=ws.device)).reshape(len(pv), -1)
         p = pieces[byte_idx].contiguous().view(torch.bfloat16).view(len(pv), I)
-    digest = lambda t: hashlib.sha256(t.contiguous().cpu().numpy().tobytes()).hexdigest()  # noqa: E731
+    return valid, p, y
+
+
+def surface_hashes(moe, layer, wl, M, h, ws, ids, out):
+    """SHA-256 of the block's surfaces after one call (the route-block page's exact-trajectory
+    record): the activation p = SiLU(g) * u (bf16) and the routed down outputs y (fp32) of the
+    valid routes in ascending route order, and the final output (bf16), each hashed as its
+    raw bytes.  The gate/up GEMM's own output (g, u) is never stored on this path: SiLU and
+    the product are applied to the accumulators."""
+    _, p, y = surface_tensors(moe, layer, M, wl.k, wl.b, ws, ids)
+
+    def digest(t):
+        raw = t.contiguous().view(-1).view(torch.uint8)
+        return hashlib.sha256(raw.cpu().numpy().tobytes()).hexdigest()
     return {"w13": "not stored (SiLU(g) * u formed in the gate/up epilogue)",
             "activation": digest(p), "routed_w2": digest(y), "final": digest(out)}
 
@@ -430,9 +443,11 @@ def per_config_entries(dev, local, min_seconds=0.4, near_inputs=None):
              "gpu_launches": block_launches(layers[0], wl, M) * layers_per_step * steps,
              "clocks": clk.summary()}
         if gemm_regime(wl):
-            npad = statistics.mean(npad_rows)
-            gu_flop = 2.0 * npad * (2 * wl.H * wl.I if wl.kind == syn.W_DENSE else 0)
-            flops = gu_flop + 2.0 * npad * wl.I * wl.H
+            # the MMAs' N side: every block of b rows is tpb tiles of kn columns
+            lay = moe.moe_workspace_layout(layers[0], M, wl.k, wl.b)
+            cols = statistics.mean(npad_rows) / b_used * lay["tpb"] * lay["kn"]
+            gu_flop = 2.0 * cols * (2 * wl.H * wl.I if wl.kind == syn.W_DENSE else 0)
+            flops = gu_flop + 2.0 * cols * wl.I * wl.H
             e["tensor_tflops_issued"] = round(flops / (us_layer * 1e-6) / 1e12, 2)
             e["tensor_frac_measured"] = round(flops / (us_layer * 1e-6) / 1e12 / tpeak, 4)
         entries["%s_M%d" % (name, M)] = e
@@ -690,6 +705,13 @@ def run_ours(args, world, rank, local):
         k_ms = mean_ms["gateup"]
     achieved = alg / (k_ms * 1e-3) / 1e9
     traffic = recorded_traffic(kernel, wl.name, u_mean)
+    if one_kernel:  # every trace point follows the one grid
+        traced = {kernel: k_ms}
+    elif wl.kind == syn.W_DENSE:  # the row gather counts with the alignment interval
+        traced = {"router": mean_ms["router"], "align": mean_ms["align"], kernel: k_ms,
+                  "combine": mean_ms["combine"]}
+    else:
+        traced = mean_ms
     result["roofline"] = {
         "kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
         "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -697,17 +719,19 @@ def run_ours(args, world, rank, local):
         "traffic": None if traffic is None else int(traffic),
         "algorithmic_bytes_per_launch": int(alg),
         "kernel_ms": round(k_ms, 5),
-        "kernel_ms_traced": {k: round(v, 5) for k, v in mean_ms.items()},
+        "kernel_ms_traced": {k: round(v, 5) for k, v in traced.items()},
     }
     if not one_kernel and wl.kind != syn.W_DENSE:
         dn_alg = u_mean * dn_b + M * wl.k * (wl.I * p_bytes + wl.H * 4)
         result["down_kernel_gbs"] = round(dn_alg / (mean_ms["down"] * 1e-3) / 1e9, 1)
     if gemm:
-        # tensor work actually issued: every aligned row, valid or padding, x 2 flops per MAC
-        npad = float(sum(padded_rows) / len(padded_rows))
-        flops = 2 * npad * (2 * wl.H * wl.I if wl.kind == syn.W_DENSE else 0)
+        # tensor work actually issued: every MMA column (tpb tiles of kn per block of b rows,
+        # valid or padding) x 2 flops per MAC
+        lay = moe.moe_workspace_layout(layers[0], M, wl.k, wl.b)
+        cols = float(sum(padded_rows) / len(padded_rows)) / lay["b"] * lay["tpb"] * lay["kn"]
+        flops = 2 * cols * (2 * wl.H * wl.I if wl.kind == syn.W_DENSE else 0)
         if wl.kind == syn.W_DENSE:
-            flops += 2 * npad * wl.I * wl.H
+            flops += 2 * cols * wl.I * wl.H
         result["roofline"]["tensor_tflops_issued"] = round(flops / (k_ms * 1e-3) / 1e12, 1)
 
     # --- e2e: host h in, host out back, copies inside the timed region

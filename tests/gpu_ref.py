@@ -133,3 +133,17 @@ def oracle_ffn(layer, h, ids, wts, residual=None, tokens=None):
     if residual is not None:
         res = syn.bits(residual[torch.as_tensor(tokens, device=residual.device, dtype=torch.long)])
     return oracle.expert_ffn(syn.bits(hs), w, local, np.asarray(wts, np.float64)[tokens], res)
+
+
+def oracle_intermediates(layer, h, ids, wts):
+    """Oracle (p [M*k, I], y [M*k, H]) per route r = m*k + j for the given routing, copying to
+    the host only the experts it uses; rows of invalid routes are zero."""
+    ids = np.asarray(ids)
+    E = layer["E"]
+    used = sorted({int(e) for e in ids.reshape(-1) if 0 <= e < E}) or [0]
+    remap = {e: i for i, e in enumerate(used)}
+    local = np.array([[remap.get(int(e), -1) for e in row] for row in ids], np.int32)
+    w = oracle.host_weights(layer, used)
+    _, p, y = oracle.expert_ffn(syn.bits(h), w, local, np.asarray(wts, np.float64),
+                                want_intermediates=True)
+    return p, y

@@ -322,6 +322,27 @@ def test_decode_block_alignment_bit_exact(name, M, b):
     G.check_routing(ids.cpu().numpy(), wts.cpu().numpy(), o_ids, o_wts, logits, wl.k)
 
 
+@pytest.mark.parametrize("M,b", [(1, 0), (2, 8), (21, 8), (40, 64)])
+def test_block_surfaces_match_oracle_intermediates(M, b):
+    """The intermediate surfaces one decode block leaves in its workspace -- p = SiLU(g) * u
+    (bf16: the p rows of the one-grid path up to 2 tokens, else the swizzled 16- or 64-row p
+    tiles) and y = p W_down (fp32) -- read back the way the bench hashes them, against the
+    oracle's p and y of the same routes."""
+    import bench
+    wl = syn.workload("layer_m21", M=M)
+    layer = _workload_layer("layer_m21")
+    h = syn.make_hidden(wl, M=M, seed=70 + M, device=DEV)
+    ws = moe.alloc_workspace(layer, M, wl.k, b)
+    out, ids, wts = moe.moe_decode_block(h, layer, wl.k, b, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    valid, p, y = bench.surface_tensors(moe, layer, M, wl.k, b, ws, ids)
+    assert valid.numel() == M * wl.k
+    o_p, o_y = G.oracle_intermediates(layer, h, ids.cpu().numpy(), wts.cpu().numpy())
+    rows = valid.cpu().numpy()
+    assert G.rel_l2(G.to_f64(p), o_p[rows]) <= 4e-3  # p is rounded to bf16 (2^-9 relative)
+    G.assert_close_block(G.to_f64(y), o_y[rows], "y")
+
+
 def test_batch_invariance_bitwise():
     wl = syn.WORKLOADS["layer_m21"]
     layer = _workload_layer("layer_m21")
