@@ -8,13 +8,15 @@
 // token), and every step of a chain of kernels costs a launch boundary on the critical path
 // before the weight stream starts and after it ends.  So one grid does it all:
 //
-//  1. Routing.  CTAs 0..7 each hold one eighth of the rows of W_r (copied before the wait
-//     for the previous grid) and reduce it against h to partial logits, with exactly the
-//     arithmetic of the router kernel's CTA of the same rank (the same row groups and
-//     orders, so the logits and the selection are bitwise those of the multi-kernel path).
-//     They publish the partials with a release count; every CTA acquires them, and runs the
-//     router's own finalisation (logits in slice order, the warp arg-max top-k, softmax)
-//     and the alignment itself (one warp, at most 32 routes): no CTA waits for another's result.
+//  1. Routing.  The router kernel's 8 slices of W_r's rows, each cut into row groups with one
+//     chain per (token, expert) (the same groups, rows and orders, so the logits and the
+//     selection are bitwise those of the multi-kernel path), are spread over 64 CTAs at
+//     E = 128: CTA (slice q, chunk c) holds the slice's rows of 16 experts, copied before
+//     the wait for the previous grid, and runs one group and expert pair per thread.  It adds
+//     its groups in order and publishes the slice's partial logits of its experts with a
+//     release count.  Every CTA acquires them and runs the router's own finalisation (logits
+//     in slice order, the warp arg-max top-k, softmax) and the alignment itself (one warp,
+//     at most 32 routes): no CTA waits for another's result.
 //  2. Experts.  Units as in the fused grid (gemm_tc05.cu): gate/up units (tile, 64 channels
 //     of I) first, then down units (tile, 128 channels of H), CTA c taking units c, c + G ...
 //     The weight boxes come by TMA (warp 0); the tile's few token rows (gate/up: h; down:
@@ -56,12 +58,14 @@ struct SmallState {
     int32_t ntiles;
 };
 
-// Shared-memory bytes the routing phase carves out of the ring (before any stage is used).
+// Shared-memory bytes the routing phase carves out of the ring (before any stage is used):
+// the CTA's block of W_r (a slice's rows, one padding row per row group, at most all E
+// columns), the slice's h rows, the row-group sums, and the 8 partials of every token.
 __host__ __device__ constexpr size_t small_routing_bytes(int M, int H, int E) {
-    return (size_t)(H / kRouterCluster) * E * 2 +              // W_r slice
-           (size_t)M * (H / kRouterCluster) * 2 +              // h slices
-           (size_t)(kRouterThreads / (E / 2)) * M * E * 4 +    // row-group sums
-           (size_t)M * kRouterCluster * E * 4 + 1024;          // the 8 partials of every token
+    return (size_t)(H / kRouterCluster + router_row_groups(E)) * E * 2 + 16 +  // W_r block
+           (size_t)M * (H / kRouterCluster) * 2 + 16 +                           // h rows
+           (size_t)router_row_groups(E) * M * E * 4 + 16 +                       // group sums
+           (size_t)M * kRouterCluster * E * 4 + 16;                              // partials
 }
 
 __device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t *p, int32_t v) {
@@ -98,35 +102,85 @@ struct SmallUnits {
     }
 };
 
-// Partial logits of this CTA's slice q of H, with the router kernel's arithmetic for a CTA of
-// rank q: row group g of the slice is rows [g*HS/RG, (g+1)*HS/RG) (RG = 512 / (E/2), the
-// router's split for its 512 threads), each (token, expert) summed over its group's rows in
-// ascending order with one fused multiply-add per row, then the groups added in order.
+// The router kernel's split of W_r: CTA q of its cluster holds slice q (HS = H/8 rows), cuts
+// it into RG = 512 / (E/2) row groups (rows [rg*HS/RG, (rg+1)*HS/RG) of the slice) with one
+// chain per (token, expert) and group, rows ascending, and adds the groups in order.  Here
+// each slice is cut further by experts into C chunks of expert pairs, one CTA per (slice,
+// chunk): every thread runs one (group, pair) chain of the router kernel, and the CTA adds
+// the groups of its experts in the same order.  A CTA reads only its own block of W_r, and
+// every CTA gathers 8 partials per token and expert, as after the router kernel.
+struct RouterSplit {
+    int HS, RG, npairs, C, NR;  // NR = 8 * C CTAs hold the router
+    int q, p0, PC;              // this CTA's slice and pairs [p0, p0 + PC)
+};
+__device__ __forceinline__ RouterSplit router_split(int H, int E) {
+    RouterSplit r;
+    r.HS = H / kRouterCluster;
+    r.npairs = E / 2;
+    r.RG = router_row_groups(E);
+    r.C = min(min(8, r.npairs), (int)gridDim.x / kRouterCluster);
+    r.NR = kRouterCluster * r.C;
+    const int c = (int)blockIdx.x % r.C;
+    r.q = (int)blockIdx.x / r.C;
+    r.p0 = c * r.npairs / r.C;
+    r.PC = (c + 1) * r.npairs / r.C - r.p0;
+    return r;
+}
+
+// Row group of slice row r (rows [g*HS/RG, (g+1)*HS/RG) form group g).
+__device__ __forceinline__ int router_group_of(int r, int HS, int RG) {
+    return ((r + 1) * RG + HS - 1) / HS - 1;
+}
+
+// Copies this CTA's block of W_r (the slice's HS rows, pairs [p0, p0 + PC)) into w_s as rows
+// of PC bf16 pairs, one empty row after each row group: the threads of a warp read the same
+// row of up to four groups at a time, and the shift puts them in different banks.
+__device__ void small_router_copy(const SmallArgs &a, const RouterSplit &sp, uint32_t *w_s) {
+    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(a.w_router) +
+                          (size_t)sp.q * sp.HS * sp.npairs + sp.p0;
+    if (sp.PC % 4 == 0 && sp.p0 % 4 == 0) {  // 16-byte pieces
+        const int per_row = sp.PC / 4;
+        for (int i = threadIdx.x; i < sp.HS * per_row; i += blockDim.x) {
+            const int r = i / per_row, j = i - r * per_row;
+            cp_async_16(w_s + (size_t)(r + router_group_of(r, sp.HS, sp.RG)) * sp.PC + 4 * j,
+                        w32 + (size_t)r * sp.npairs + 4 * j);
+        }
+    } else {
+        for (int i = threadIdx.x; i < sp.HS * sp.PC; i += blockDim.x) {
+            const int r = i / sp.PC, j = i - r * sp.PC;
+            cp_async_4(w_s + (size_t)(r + router_group_of(r, sp.HS, sp.RG)) * sp.PC + j,
+                       w32 + (size_t)r * sp.npairs + j);
+        }
+    }
+}
+
+// This CTA's partial logits: thread (group rg, pair pl) chains over the group's rows (one
+// fused multiply-add per row) into red[(rg * TM + t) * 2PC + 2 pl (+1)]; then the groups of
+// each (token, expert) added in order into a.partials[(q * M + t) * E + e].
 template <int TM>
-__device__ void small_router_dots(const SmallArgs &a, const __nv_bfloat16 *w_s,
-                                  const __nv_bfloat16 *x_s, float *red, int HS) {
-    const int E = a.E, npairs = E / 2, RG = kRouterThreads / npairs;
+__device__ void small_router_chunk(const SmallArgs &a, const RouterSplit &sp,
+                                   const uint32_t *w_s, const __nv_bfloat16 *x_s, float *red) {
+    const int PC = sp.PC, HS = sp.HS, RG = sp.RG;
     const uint32_t *x32 = reinterpret_cast<const uint32_t *>(x_s);
-    for (int item = threadIdx.x; item < npairs * RG; item += blockDim.x) {
-        const int pair = item % npairs, rg = item / npairs;
-        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(w_s) + pair;
+    const int item = threadIdx.x;
+    if (item < RG * PC) {
+        const int rg = item / PC, pl = item - rg * PC;
+        const uint32_t *wrow = w_s + (size_t)rg * PC + pl;  // row r at wrow[r * PC]
         const int r0 = rg * HS / RG, r1 = (rg + 1) * HS / RG;
-        // one chain per (token, expert), rows ascending; the tokens' chains interleave so that
-        // one weight load serves them all, and one load of h serves two rows
         float acc0[TM], acc1[TM];
 #pragma unroll
         for (int t = 0; t < TM; ++t) acc0[t] = acc1[t] = 0.0f;
         int r = r0;
         // eight rows per step: their weights and h pairs are all loaded before the first
-        // multiply-add, which then run in row order as before
+        // multiply-add, which then run in row order
         for (; r + 7 < r1 && (r & 1) == 0; r += 8) {
             uint32_t w8[8], x4[TM][4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) w8[u] = wrow[(size_t)(r + u) * npairs];
+            for (int u = 0; u < 8; ++u) w8[u] = wrow[(r + u) * PC];
 #pragma unroll
             for (int t = 0; t < TM; ++t)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) x4[t][u] = x32[((size_t)t * HS + r + 2 * u) >> 1];
+                for (int u = 0; u < 4; ++u) x4[t][u] = x32[(t * HS + r + 2 * u) >> 1];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -138,11 +192,11 @@ __device__ void small_router_dots(const SmallArgs &a, const __nv_bfloat16 *w_s,
                 }
         }
         for (; r + 1 < r1 && (r & 1) == 0; r += 2) {
-            const uint32_t wa = wrow[(size_t)r * npairs];
-            const uint32_t wb = wrow[(size_t)(r + 1) * npairs];
+            const uint32_t wa = wrow[r * PC];
+            const uint32_t wb = wrow[(r + 1) * PC];
 #pragma unroll
             for (int t = 0; t < TM; ++t) {
-                const uint32_t xv = x32[((size_t)t * HS + r) >> 1];
+                const uint32_t xv = x32[(t * HS + r) >> 1];
                 acc0[t] = fma_bf16<0, 0>(xv, wa, acc0[t]);
                 acc1[t] = fma_bf16<0, 1>(xv, wa, acc1[t]);
                 acc0[t] = fma_bf16<1, 0>(xv, wb, acc0[t]);
@@ -150,10 +204,10 @@ __device__ void small_router_dots(const SmallArgs &a, const __nv_bfloat16 *w_s,
             }
         }
         for (; r < r1; ++r) {  // an odd row at either end of a group
-            const uint32_t wa = wrow[(size_t)r * npairs];
+            const uint32_t wa = wrow[r * PC];
 #pragma unroll
             for (int t = 0; t < TM; ++t) {
-                const uint32_t xv = x32[((size_t)t * HS + r) >> 1];
+                const uint32_t xv = x32[(t * HS + r) >> 1];
                 if (r & 1) {
                     acc0[t] = fma_bf16<1, 0>(xv, wa, acc0[t]);
                     acc1[t] = fma_bf16<1, 1>(xv, wa, acc1[t]);
@@ -165,28 +219,16 @@ __device__ void small_router_dots(const SmallArgs &a, const __nv_bfloat16 *w_s,
         }
 #pragma unroll
         for (int t = 0; t < TM; ++t) {
-            red[((size_t)rg * TM + t) * E + 2 * pair] = acc0[t];
-            red[((size_t)rg * TM + t) * E + 2 * pair + 1] = acc1[t];
+            red[((size_t)rg * TM + t) * 2 * PC + 2 * pl] = acc0[t];
+            red[((size_t)rg * TM + t) * 2 * PC + 2 * pl + 1] = acc1[t];
         }
     }
-}
-
-__device__ void small_router_slice(const SmallArgs &a, const __nv_bfloat16 *w_s,
-                                   const __nv_bfloat16 *x_s, float *red, int HS) {
-    const int E = a.E, M = a.M, RG = kRouterThreads / (E / 2);
-    switch (M) {
-        case 1: small_router_dots<1>(a, w_s, x_s, red, HS); break;
-        case 2: small_router_dots<2>(a, w_s, x_s, red, HS); break;
-        case 3: small_router_dots<3>(a, w_s, x_s, red, HS); break;
-        default: small_router_dots<4>(a, w_s, x_s, red, HS); break;
-    }
     __syncthreads();
-    // the row groups in order, published as this slice's partials
-    const int q = blockIdx.x;
-    for (int idx = threadIdx.x; idx < M * E; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < TM * 2 * PC; idx += blockDim.x) {
         float s = red[idx];
-        for (int g = 1; g < RG; ++g) s += red[(size_t)g * M * E + idx];
-        a.partials[(size_t)q * M * E + idx] = s;
+        for (int g = 1; g < RG; ++g) s += red[(size_t)g * TM * 2 * PC + idx];
+        const int t = idx / (2 * PC), el = idx - t * 2 * PC;
+        a.partials[((size_t)sp.q * TM + t) * a.E + 2 * sp.p0 + el] = s;
     }
 }
 
@@ -343,16 +385,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                                      ((sizeof(GCtl) + 15) & ~size_t(15)));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = a.M, E = a.E, H = a.H, HS = H / kRouterCluster, R = M * a.k;
-    const bool router = blockIdx.x < kRouterCluster;
+    const RouterSplit sp = router_split(H, E);
+    const bool router = (int)blockIdx.x < sp.NR;
 
     // routing scratch inside the ring (no stage is in use yet)
     unsigned char *p = stages;
-    __nv_bfloat16 *w_s = reinterpret_cast<__nv_bfloat16 *>(p);
-    p += (size_t)HS * E * 2;
+    uint32_t *w_s = reinterpret_cast<uint32_t *>(p);
+    p += ((size_t)(HS + sp.RG) * E * 2 + 15) & ~size_t(15);
     __nv_bfloat16 *x_s = reinterpret_cast<__nv_bfloat16 *>(p);
-    p += (size_t)M * HS * 2;
+    p += ((size_t)M * HS * 2 + 15) & ~size_t(15);
     float *red = reinterpret_cast<float *>(p);
-    p += (size_t)(kRouterThreads / (E / 2)) * M * E * 4;
+    p += ((size_t)sp.RG * M * E * 4 + 15) & ~size_t(15);
     float *part_s = reinterpret_cast<float *>(p);
 
     if (threadIdx.x == 0) {
@@ -360,16 +403,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         prefetch_tensormap(&tm_up);
         prefetch_tensormap(&tm_down);
     }
-    // full barriers: the producer's expect_tx arrival and the row loader's arrival; bfull[0]
-    // (unused by this kernel's ring) tracks the router slice's copy
-    if (threadIdx.x == 0) mbar_init(&ctl.bfull[0], 1);
+    // full barriers: the producer's expect_tx arrival and the row loader's arrival
     gemm_init<GS>(ctl, warp, 0, 2);
-    // the router slice never depends on the previous grid: its copy starts before the wait
-    const uint32_t w_bytes = (uint32_t)HS * E * 2;
-    if (router && threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&ctl.bfull[0], w_bytes);
-        bulk_load(w_s, a.w_router + (size_t)blockIdx.x * HS * E, w_bytes, &ctl.bfull[0]);
-    }
+    // W_r never depends on the previous grid: the CTA's block is copied before the wait
+    if (router) small_router_copy(a, sp, w_s);
     pdl_wait();  // h, and the control region, come after the previous grid
     pdl_launch_dependents();
 
@@ -378,15 +415,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
         for (int idx = threadIdx.x; idx < M * (HS / 8); idx += blockDim.x) {
             const int t = idx / (HS / 8), pc = idx - t * (HS / 8);
             *reinterpret_cast<uint4 *>(x_s + (size_t)t * HS + pc * 8) =
-                *reinterpret_cast<const uint4 *>(a.h + (size_t)t * H + (size_t)blockIdx.x * HS + pc * 8);
+                *reinterpret_cast<const uint4 *>(a.h + (size_t)t * H + (size_t)sp.q * HS + pc * 8);
         }
-        if (!mbar_wait_bounded(&ctl.bfull[0], 0)) ctl.abort = 1;
+        cp_async_wait_all();
         __syncthreads();
-        small_router_slice(a, w_s, x_s, red, HS);
+        if (M == 1)
+            small_router_chunk<1>(a, sp, w_s, x_s, red);
+        else
+            small_router_chunk<2>(a, sp, w_s, x_s, red);
         __syncthreads();
         if (threadIdx.x == 0) red_release_gpu_add(a.ctl + kSmallCtlRouted, 1);
     }
-    if (threadIdx.x == 0 && !count_wait(a.ctl + kSmallCtlRouted, kRouterCluster, ctl))
+    if (threadIdx.x == 0 && !count_wait(a.ctl + kSmallCtlRouted, sp.NR, ctl))
         atomicOr(a.status, MOE_DEV_WAIT_TIMEOUT);
     __syncthreads();
     // the 8 slices' partials of every token, four experts per load, every load of a thread in
@@ -594,6 +634,7 @@ bool small_fits(int M, int k, int E, int H, int b) {
     if (M < 1 || M > kSmallMaxTokens || (int64_t)M * k > kSmallMaxRoutes || b < 1 || b > 16)
         return false;
     if ((size_t)(H / kRouterCluster) * E * 2 > 64 * 1024) return false;  // one router pass
+    if (num_sms() < kRouterCluster) return false;  // at least one CTA per slice
     const int64_t R = (int64_t)M * k;
     const int64_t cap = R + (R < E ? R : E) * (b - 1);
     if (small_routing_bytes(M, H, E) > (size_t)GS::kStages * GS::kStageBytes) return false;

@@ -60,11 +60,29 @@ __device__ __forceinline__ int gemm_route(const GemmArgs &a, int64_t pos, int e,
 // The block vector entry of this CTA's first unit (unit blockIdx.x), read before the unit
 // count is known so that the two loads overlap; the index is clamped into the array and
 // the value is used only when the unit exists.
-__device__ __forceinline__ int first_unit_expert(const GemmArgs &a, int n_ct) {
+// The expert of block blk, and whether the expert spans more than one tile (several tiles
+// per block, or a neighbouring block of the same expert): then other units read the same
+// weight boxes at about the same time, and the boxes stay in L2 at normal priority for them;
+// weights read by one tile only are marked first to evict.
+struct UnitExpert {
+    int e;
+    bool shared;
+};
+// With at most b tokens and distinct experts per token no expert fills two blocks, and the
+// neighbours are not read.
+__device__ __forceinline__ UnitExpert unit_expert(const GemmArgs &a, int64_t blk) {
     const int64_t nblk = a.cap / a.b;
-    int64_t blk = ((int64_t)blockIdx.x / n_ct) / a.tpb;
     if (blk >= nblk) blk = nblk - 1;
-    return a.blocks[blk];
+    const int e = a.blocks[blk];
+    if (a.tpb > 1) return {e, true};
+    if (a.M <= a.b) return {e, false};
+    const int before = blk > 0 ? a.blocks[blk - 1] : -1;
+    const int after = blk + 1 < nblk ? a.blocks[blk + 1] : -1;
+    return {e, before == e || after == e};
+}
+
+__device__ __forceinline__ UnitExpert first_unit_expert(const GemmArgs &a, int n_ct) {
+    return unit_expert(a, ((int64_t)blockIdx.x / n_ct) / a.tpb);
 }
 
 __device__ __forceinline__ int64_t gemm_blocks(const GemmArgs &a) {
@@ -353,9 +371,12 @@ __device__ __forceinline__ int64_t uq_pop(UnitQueue &q, GCtl &ctl, int i) {
 // previous grid is complete (it zeroes the counter) and while this unit's copies stream.
 template <typename G>
 __device__ void fused_producer(const GemmArgs &a, GCtl &ctl, UnitQueue &q, unsigned char *stages,
-                               const FusedShape &f, int e_first_gu, const CUtensorMap *tm_gate,
-                               const CUtensorMap *tm_up, const CUtensorMap *tm_down) {
-    const uint64_t pol = policy_evict_first();
+                               const FusedShape &f, UnitExpert first_gu,
+                               const CUtensorMap *tm_gate, const CUtensorMap *tm_up,
+                               const CUtensorMap *tm_down) {
+    const uint64_t pol_once = policy_evict_first(), pol_shared = policy_evict_normal();
+    // the row slices are read by every channel tile of their tile: kept before the weights
+    const uint64_t pol_rows = policy_evict_last();
     const unsigned char *xt = reinterpret_cast<const unsigned char *>(a.x_tiles);
     const unsigned char *pt = reinterpret_cast<const unsigned char *>(a.p_tiles);
     int32_t *sched = a.ready + a.nready - 1;
@@ -368,8 +389,8 @@ __device__ void fused_producer(const GemmArgs &a, GCtl &ctl, UnitQueue &q, unsig
     int pend_stage[G::kStages];
     auto release_held = [&]() {
         for (int qq = 0; qq < npend; ++qq)
-            bulk_load(stages + pend_stage[qq] * G::kStageBytes + G::kBOff, pend_src[qq], G::kBBytes,
-                      &ctl.full[pend_stage[qq]]);
+            bulk_load_hint(stages + pend_stage[qq] * G::kStageBytes + G::kBOff, pend_src[qq],
+                           G::kBBytes, &ctl.full[pend_stage[qq]], pol_rows);
         npend = 0;
     };
     bool stop = false;
@@ -385,7 +406,10 @@ __device__ void fused_producer(const GemmArgs &a, GCtl &ctl, UnitQueue &q, unsig
         }
         int64_t next = -1;
         if (waited) next = (int64_t)gridDim.x + atomicAdd(sched, 1);
-        int e = (u == (int64_t)blockIdx.x && x.gu) ? e_first_gu : a.blocks[x.tile / a.tpb];
+        const UnitExpert ue =
+            (u == (int64_t)blockIdx.x && x.gu) ? first_gu : unit_expert(a, x.tile / a.tpb);
+        int e = ue.e;
+        const uint64_t pol = ue.shared ? pol_shared : pol_once;
         if (e < 0 || e >= a.E) {
             atomicOr(a.status, MOE_DEV_BAD_ALIGNMENT);
             e = 0;  // keep the pipeline in step; every row of such a block is dropped
@@ -412,7 +436,7 @@ __device__ void fused_producer(const GemmArgs &a, GCtl &ctl, UnitQueue &q, unsig
             issued |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
             if (waited && ready) {
-                bulk_load(st + G::kBOff, src, G::kBBytes, bar);
+                bulk_load_hint(st + G::kBOff, src, G::kBBytes, bar, pol_rows);
             } else {
                 pend_src[npend] = src;
                 pend_stage[npend] = stage;
@@ -530,11 +554,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     // the expert of this CTA's first unit if it is a gate/up unit, read beside the unit count
     const int n_gu = a.I / 64;
-    const int e_first_gu = threadIdx.x == 0 ? first_unit_expert(a, n_gu) : 0;
+    const UnitExpert first_gu = threadIdx.x == 0 ? first_unit_expert(a, n_gu) : UnitExpert{0, false};
     const FusedShape f = fused_shape(a, G::kK);
 
     if (warp == 0) {
-        if (lane == 0) fused_producer<G>(a, ctl, q, stages, f, e_first_gu, &tm_gate, &tm_up, &tm_down);
+        if (lane == 0) fused_producer<G>(a, ctl, q, stages, f, first_gu, &tm_gate, &tm_up, &tm_down);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) fused_mma<G>(ctl, q, stages, f);
@@ -793,7 +817,7 @@ __global__ void __launch_bounds__(kGVQThreads, 1)
     const int n_ct = a.I / G::kCT;
     const int nks = a.H / G::kK;
     const int nrows = a.H / kD;
-    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
+    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct).e : 0;
     const int64_t T = gemm_blocks(a) * a.tpb * n_ct;
 
     if (warp == 0) {
@@ -869,7 +893,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     const int n_ct = a.H / kGM;
     const int nks = a.I / G::kK;
-    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct) : 0;
+    const int e_first = threadIdx.x == 0 ? first_unit_expert(a, n_ct).e : 0;
     const int64_t T = gemm_blocks(a) * a.tpb * n_ct;
 
     if (warp == 0) {

@@ -20,6 +20,9 @@ constexpr int kConsumerWarps = 8;
 constexpr int kGemvThreads = 32 * (2 + kConsumerWarps);  // producer, loader, consumers
 constexpr int kRouterCluster = 8;  // CTAs per router cluster (split of H)
 constexpr int kRouterThreads = 512;
+// Row groups per slice of the router's split of H: RG = 512 / (E/2) (every thread of a
+// router CTA one group and expert pair).
+__host__ __device__ constexpr int router_row_groups(int E) { return kRouterThreads / (E / 2); }
 
 struct Dims {
     int M, k, E, H, I, b;
