@@ -154,8 +154,9 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int k, int E, int b,
  * (b == 0: enough for any block size the library may pick).  The workspace holds the
  * alignment (when the library computes it), the per-route intermediates (dense weights:
  * tiles of token rows and of p in bf16, per-tile counters; VQ weights: p [M*k, I] fp32),
- * the expert outputs y [M*k, H] fp32, and the device status word (its first 4 bytes),
- * which must be zero before the first call (allocate it zero-filled).  Calls that share a
+ * the expert outputs y [M*k, H] fp32, the device status word (its first 4 bytes) and
+ * counters, which must be zero before the first call (allocate it zero-filled, or zero the
+ * first zero_bytes of moe_workspace_layout) and which every call leaves zero.  Calls that share a
  * workspace must be ordered on one stream.  Returns 0 on unsupported arguments.
  */
 size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int k, int b);
@@ -197,8 +198,9 @@ typedef struct moe_workspace_layout {
     size_t y;
     size_t p_tiles;
     int32_t tpb;              /* p tiles per aligned block */
-    int32_t zero_bytes;       /* the first zero_bytes bytes (status word and counters) must be
-                                 zero before the first call; every call leaves them zero */
+    int32_t zero_bytes;       /* the first zero_bytes bytes (status word, counters, the
+                                 one-grid path's routing exchange) must be zero before the
+                                 first call; every call leaves them zero */
     int32_t launches;         /* kernels one moe_decode_block call launches (1: the whole
                                  block in one grid) */
     int32_t reserved;

@@ -44,6 +44,7 @@ WsLayout ws_layout(const Dims &d) {
     };
     L.status = take(64);
     L.ctl = take((size_t)kSmallCtlInts * 4);  // every layout keeps it (no other path writes it)
+    L.partials = take((size_t)kSmallPartialInts * 4);  // likewise
     L.sorted = take((size_t)d.cap * 4);
     L.blocks = take((size_t)(d.cap / d.b) * 4);
     L.npad = take(16);
@@ -57,7 +58,6 @@ WsLayout ws_layout(const Dims &d) {
     L.p_tiles = take(tile_rows * d.I * 2);
     L.ready = take(d.gemm ? ((size_t)(d.cap / d.b) * d.tpb + 1) * 4 : 0);  // + the unit counter
     const bool small = d.gemm && !d.vq_tc && small_fits(d.M, d.k, d.E, d.H, d.b);
-    L.partials = take(small ? (size_t)kRouterCluster * d.M * d.E * 4 : 0);
     L.p_rows = take(small ? (size_t)d.R * d.I * 2 : 0);
     L.tt_part = take(d.ttable ? (size_t)vq_ttable_slices(d.H, d.vqd) * d.R * 2 * d.I * 4 : 0);
     L.total = off;
@@ -414,7 +414,7 @@ extern "C" int moe_workspace_layout(const moe_expert_weights_t *w, int M, int k,
     out->num_padded = L.npad;
     out->y = L.y;
     out->p_tiles = L.p_tiles;
-    out->zero_bytes = (int32_t)(L.ctl + (size_t)kSmallCtlInts * 4);
+    out->zero_bytes = (int32_t)(L.partials + (size_t)kSmallPartialInts * 4);
     out->launches = block_launches(w, d);
     out->p_rows = out->launches == 1 ? L.p_rows : 0;
     return MOE_OK;

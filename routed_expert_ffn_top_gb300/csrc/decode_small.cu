@@ -56,6 +56,7 @@ struct SmallState {
     int32_t nvalid[kSmallMaxTokens];                     // valid routes of each token
     int32_t comb[kSmallMaxTokens];                       // per row of the down unit: token to combine, or -1
     int32_t ntiles;
+    int32_t last;  // this CTA took the last exit ticket
 };
 
 // Shared-memory bytes the routing phase carves out of the ring (before any stage is used):
@@ -224,11 +225,14 @@ __device__ void small_router_chunk(const SmallArgs &a, const RouterSplit &sp,
         }
     }
     __syncthreads();
+    // stored complemented: arithmetic never produces the all-ones NaN (NaN results are the
+    // canonical 0x7fffffff), so a zero word means "not written yet" to the readers
+    uint32_t *dst = reinterpret_cast<uint32_t *>(a.partials);
     for (int idx = threadIdx.x; idx < TM * 2 * PC; idx += blockDim.x) {
         float s = red[idx];
         for (int g = 1; g < RG; ++g) s += red[(size_t)g * TM * 2 * PC + idx];
         const int t = idx / (2 * PC), el = idx - t * 2 * PC;
-        a.partials[((size_t)sp.q * TM + t) * a.E + 2 * sp.p0 + el] = s;
+        dst[((size_t)sp.q * TM + t) * a.E + 2 * sp.p0 + el] = ~__float_as_uint(s);
     }
 }
 
@@ -371,6 +375,29 @@ __device__ void small_mma(GCtl &ctl, unsigned char *stages, const SmallUnits &f)
     if (!mbar_wait_bounded(&ctl.done, 0)) ctl.abort = 1;
 }
 
+// CTA 0, one warp, while the expert phase runs: the alignment as moe_align_block_size gives
+// it (rows of tile t: its routes, then sentinels; the block vector; the row count), the
+// status bit for invalid routes, and out = residual (or zero) for a token with no valid route.
+__device__ void small_write_alignment(const SmallArgs &a, const SmallState &st, int R) {
+    const int lane = threadIdx.x & 31, b = a.b, ntiles = st.ntiles;
+    for (int64_t i = lane; i < a.cap; i += 32) {
+        const int t = (int)(i / b), n = (int)(i - (int64_t)t * b);
+        a.sorted[i] = (t < ntiles && n < st.tile_n[t]) ? st.tile_r[t][n] : R;
+    }
+    for (int64_t q = lane; q < a.cap / b; q += 32) a.blocks[q] = q < ntiles ? st.tile_e[q] : -1;
+    int nv = 0;
+    for (int t = 0; t < a.M; ++t) nv += st.nvalid[t];
+    if (lane == 0) {
+        a.npad[0] = ntiles * b;
+        if (nv < R) atomicOr(a.status, MOE_DEV_INVALID_EXPERT);
+    }
+    for (int t = 0; t < a.M; ++t)
+        if (st.nvalid[t] == 0)
+            for (int n = lane; n < a.H; n += 32)
+                a.out[(size_t)t * a.H + n] =
+                    a.residual ? a.residual[(size_t)t * a.H + n] : __float2bfloat16(0.0f);
+}
+
 __global__ void __launch_bounds__(kSThreads, 1)
     decode_small_kernel(const __grid_constant__ CUtensorMap tm_gate,
                         const __grid_constant__ CUtensorMap tm_up,
@@ -423,39 +450,55 @@ __global__ void __launch_bounds__(kSThreads, 1)
             small_router_chunk<1>(a, sp, w_s, x_s, red);
         else
             small_router_chunk<2>(a, sp, w_s, x_s, red);
-        __syncthreads();
-        if (threadIdx.x == 0) red_release_gpu_add(a.ctl + kSmallCtlRouted, 1);
     }
-    if (threadIdx.x == 0 && !count_wait(a.ctl + kSmallCtlRouted, sp.NR, ctl))
-        atomicOr(a.status, MOE_DEV_WAIT_TIMEOUT);
-    __syncthreads();
-    // the 8 slices' partials of every token, four experts per load, every load of a thread in
-    // flight before the first store
+    // The 8 slices' partials of every token, polled where they lie: every load of a thread in
+    // flight at once, reloaded until no word of it is zero (not written yet).
     {
-        const int n4 = M * kRouterCluster * E / 4, e4n = E / 4;
+        const int n4 = M * kRouterCluster * E / 4, e4n = E / 4;  // at most 4096 = 8 x 512
         constexpr int kBatch = 8;
-        for (int base = threadIdx.x; base < n4; base += kBatch * blockDim.x) {
-            float4 v[kBatch];
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.partials);
+        uint4 v[kBatch];
+        unsigned pending = 0;
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int idx = base + i * blockDim.x;
-                if (idx < n4) {
-                    const int qt = idx / e4n, e4 = idx - qt * e4n;  // qt = q * M + t
-                    v[i] = __ldcg(reinterpret_cast<const float4 *>(a.partials + (size_t)qt * E) + e4);
-                }
+        for (int i = 0; i < kBatch; ++i) {
+            const int idx = (int)threadIdx.x + i * (int)blockDim.x;
+            if (idx < n4) {
+                v[i] = __ldcg(src + idx);
+                pending |= 1u << i;
             }
+        }
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int idx = base + i * blockDim.x;
-                if (idx < n4) {
-                    const int qt = idx / e4n, e4 = idx - qt * e4n;
-                    const int q = qt / M, t = qt - q * M;
-                    reinterpret_cast<float4 *>(part_s + ((size_t)t * kRouterCluster + q) * E)[e4] = v[i];
-                }
+            for (int i = 0; i < kBatch; ++i)
+                if ((pending >> i) & 1u)
+                    if (v[i].x != 0u && v[i].y != 0u && v[i].z != 0u && v[i].w != 0u)
+                        pending &= ~(1u << i);
+            if (pending == 0u || ctl.abort) break;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                ctl.abort = 1;
+                atomicOr(a.status, MOE_DEV_WAIT_TIMEOUT);
+                break;
+            }
+            __nanosleep(32);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if ((pending >> i) & 1u) v[i] = __ldcg(src + (int)threadIdx.x + i * (int)blockDim.x);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int idx = (int)threadIdx.x + i * (int)blockDim.x;
+            if (idx < n4) {
+                const int qt = idx / e4n, e4 = idx - qt * e4n;  // qt = q * M + t
+                const int q = qt / M, t = qt - q * M;
+                reinterpret_cast<float4 *>(part_s + ((size_t)t * kRouterCluster + q) * E)[e4] =
+                    make_float4(__uint_as_float(~v[i].x), __uint_as_float(~v[i].y),
+                                __uint_as_float(~v[i].z), __uint_as_float(~v[i].w));
             }
         }
     }
     __syncthreads();
+    int my_id = -1;  // lane j of warp t: the expert of token t's slot j
     route_finalize_any(part_s, M, E, a.k, a.bias, !ctl.abort, 1,
                        [&](int i, int j, int id, float wt) {
                            st.ids[i * a.k + j] = id;
@@ -464,68 +507,72 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                a.topk_ids[(size_t)i * a.k + j] = id;
                                a.topk_wts[(size_t)i * a.k + j] = wt;
                            }
+                           my_id = id;
                        });
-    __syncthreads();
-    // The alignment of the (at most 32) routes in one warp, lane r holding route r: the lanes
-    // of one expert find each other (match), a route's row is the padded rows of the experts
-    // below its own plus the routes of its expert before it -- the order of align_core: experts
-    // ascending, routes ascending, each expert padded to a multiple of b with sentinels.
-    if (warp == 0) {
-        const int b = a.b;
-        const int e = lane < R ? st.ids[lane] : -1;
-        const bool valid = lane < R && e >= 0 && e < E;
-        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-        const int lower = __popc(peers & ((1u << lane) - 1u));
-        const int n = __popc(peers);
-        const bool leader = valid && lower == 0;
-        const int padded = leader ? (n + b - 1) / b * b : 0;
-        int off = 0, total = 0;
+    // The alignment of the (at most 32) routes -- the order of align_core: experts ascending,
+    // routes ascending, each expert padded to a multiple of b with sentinels -- as the tile
+    // plan the expert phase reads (CTA 0 writes it out as the workspace's alignment later).
+    if (M == 1) {
+        // One token: its valid experts are distinct, one route each padded to b rows, so slot
+        // j's tile is the rank of its expert among the token's valid experts, taken from the
+        // ids warp 0 still holds (lane j: slot j).
+        if (warp == 0) {
+            const bool valid = lane < a.k && my_id >= 0 && my_id < E;
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            int rank = 0;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int eq = __shfl_sync(0xffffffffu, e, q);
-            const int pq = __shfl_sync(0xffffffffu, padded, q);
-            total += pq;
-            if (pq != 0 && eq < e) off += pq;
-        }
-        const int pos = valid ? off + lower : -1;
-        if (valid) st.tile_r[pos / b][pos % b] = lane;  // pos % b = lower % b < M
-        if (leader)
-            for (int q = 0; q < padded / b; ++q) {
-                st.tile_e[off / b + q] = e;
-                st.tile_n[off / b + q] = min(b, n - q * b);
+            for (int q = 0; q < 32; ++q) {
+                const int eq = __shfl_sync(0xffffffffu, my_id, q);
+                rank += ((vmask >> q) & 1u) && eq < my_id ? 1 : 0;
             }
-        if (lane == 0) st.ntiles = total / b;
-        if (blockIdx.x == 0) {  // the alignment as moe_align_block_size gives it
-            const bool any_invalid = __any_sync(0xffffffffu, lane < R && !valid);
-            for (int64_t i = lane; i < a.cap; i += 32) a.sorted[i] = R;
-            __syncwarp();
-            if (valid) a.sorted[pos] = lane;
+            if (valid) {
+                st.tile_e[rank] = my_id;
+                st.tile_n[rank] = 1;
+                st.tile_r[rank][0] = lane;
+            }
+            if (lane == 0) st.ntiles = st.nvalid[0] = __popc(vmask);
+        }
+    } else {
+        __syncthreads();
+        // In one warp, lane r holding route r: the lanes of one expert find each other
+        // (match), and a route's row is the padded rows of the experts below its own plus the
+        // routes of its expert before it.
+        if (warp == 0) {
+            const int b = a.b;
+            const int e = lane < R ? st.ids[lane] : -1;
+            const bool valid = lane < R && e >= 0 && e < E;
+            const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+            const int lower = __popc(peers & ((1u << lane) - 1u));
+            const int n = __popc(peers);
+            const bool leader = valid && lower == 0;
+            const int ntile = leader ? (n + b - 1) / b : 0;  // tiles of this lane's expert
+            int tile_off = 0, total = 0;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int eq = __shfl_sync(0xffffffffu, e, q);
+                const int tq = __shfl_sync(0xffffffffu, ntile, q);
+                total += tq;
+                if (tq != 0 && eq < e) tile_off += tq;
+            }
+            if (valid) st.tile_r[tile_off + lower / b][lower % b] = lane;  // lower % b < M
             if (leader)
-                for (int q = 0; q < padded / b; ++q) a.blocks[off / b + q] = e;
-            for (int64_t q = total / b + lane; q < a.cap / b; q += 32) a.blocks[q] = -1;
-            if (lane == 0) {
-                a.npad[0] = total;
-                if (any_invalid) atomicOr(a.status, MOE_DEV_INVALID_EXPERT);
+                for (int q = 0; q < ntile; ++q) {
+                    st.tile_e[tile_off + q] = e;
+                    st.tile_n[tile_off + q] = min(b, n - q * b);
+                }
+            if (lane == 0) st.ntiles = total;
+        }
+        if (threadIdx.x < M) {
+            int n = 0;
+            for (int j = 0; j < a.k; ++j) {
+                const int e = st.ids[threadIdx.x * a.k + j];
+                n += (e >= 0 && e < E) ? 1 : 0;
             }
+            st.nvalid[threadIdx.x] = n;
         }
-    }
-    if (threadIdx.x < M) {
-        int n = 0;
-        for (int j = 0; j < a.k; ++j) {
-            const int e = st.ids[threadIdx.x * a.k + j];
-            n += (e >= 0 && e < E) ? 1 : 0;
-        }
-        st.nvalid[threadIdx.x] = n;
     }
     __syncthreads();
     const int ntiles = st.ntiles;
-    // a token without a valid route: its output is the residual (or zero)
-    if (blockIdx.x == 0)
-        for (int t = 0; t < M; ++t)
-            if (st.nvalid[t] == 0)
-                for (int n = threadIdx.x; n < H; n += blockDim.x)
-                    a.out[(size_t)t * H + n] =
-                        a.residual ? a.residual[(size_t)t * H + n] : __float2bfloat16(0.0f);
 
     // ---------------------------------------------------------------- 2. experts
     SmallUnits f;
@@ -543,6 +590,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         __syncwarp();
     } else if (warp == kSLoaderWarp) {
         small_loader(a, ctl, stages, st, f);
+    } else if (warp == kSLoaderWarp + 1) {
+        if (blockIdx.x == 0) small_write_alignment(a, st, R);
     } else if (warp >= 2 && warp < 6) {  // the epilogue warps (warps 7.. only helped to route)
         const int quad = warp & 3;
         const int row = 32 * quad + lane;  // accumulator row: channel of the unit
@@ -612,14 +661,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
     // ---------------------------------------------------------------- exit: restore the region
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const int old = atom_add_acq_rel_gpu(a.ctl + kSmallCtlExit, 1);
-        if (old == (int)gridDim.x - 1) {
-            a.ctl[kSmallCtlRouted] = 0;
-            for (int i = 0; i < a.ntiles_cap; ++i) a.ctl[kSmallCtlReady + i] = 0;
-            for (int i = 0; i < M * (H / kGM); ++i) a.ctl[kSmallCtlReady + a.ntiles_cap + i] = 0;
-            a.ctl[kSmallCtlExit] = 0;
-        }
+    if (threadIdx.x == 0) st.last = atom_add_acq_rel_gpu(a.ctl + kSmallCtlExit, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (st.last) {  // every CTA is done with the counters and the partials
+        for (int i = threadIdx.x; i < a.ntiles_cap; i += blockDim.x) a.ctl[kSmallCtlReady + i] = 0;
+        for (int i = threadIdx.x; i < M * (H / kGM); i += blockDim.x)
+            a.ctl[kSmallCtlReady + a.ntiles_cap + i] = 0;
+        for (int i = threadIdx.x; i < M * kRouterCluster * E / 4; i += blockDim.x)
+            reinterpret_cast<uint4 *>(a.partials)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (threadIdx.x == 0) a.ctl[kSmallCtlExit] = 0;
     }
 }
 

@@ -64,7 +64,7 @@ struct WsLayout {
     size_t x_tiles;  // bf16[tile rows * H]  dense weights: token rows per tile row
     size_t p_tiles;  // bf16[tile rows * I]  dense weights: p per tile row
     size_t ready;    // int32[tiles]  dense weights: gate/up units of each tile whose p is stored
-    size_t partials; // float[8 * M * E]  one-kernel path: router partials of the 8 slices of H
+    size_t partials; // uint32[kSmallPartialInts]  one-kernel path: the router's partials, zero between calls
     size_t p_rows;   // bf16[R * I]  one-kernel path: p per route
     size_t tt_part;  // float[slices * M*k * 2 * I]  VQ through projected code books
     size_t total;
@@ -158,10 +158,13 @@ struct GemmArgs {
 // than the launches it saves).
 constexpr int kSmallMaxTokens = 2;
 constexpr int kSmallMaxRoutes = 32;
-constexpr int kSmallCtlRouted = 0;  // router slices published
 constexpr int kSmallCtlExit = 1;    // CTAs finished
 constexpr int kSmallCtlReady = 32;  // ready[tiles], then done[M][H / 128]
 constexpr int kSmallCtlInts = 512;
+// The one-grid path's routing exchange: the partial logits [8][M][E] of the router's slices,
+// stored complemented (a zero word: not written yet), in a region of fixed size right after
+// the control region in every workspace layout, zero between calls like it.
+constexpr int kSmallPartialInts = kRouterCluster * kSmallMaxTokens * 512;
 constexpr int kSmallCtlDone = kSmallCtlInts - kSmallCtlReady - kSmallMaxRoutes;
 
 struct SmallArgs {
@@ -172,7 +175,7 @@ struct SmallArgs {
     int32_t *topk_ids;
     float *topk_wts;
     __nv_bfloat16 *out;
-    float *partials;                  // [8][M][E]
+    float *partials;                  // [8][M][E], complemented bits, zero between calls
     int32_t *ctl;                     // the control region
     int32_t *sorted, *blocks, *npad;  // the alignment, left in the workspace
     __nv_bfloat16 *p_rows;            // [M*k][I]

@@ -53,8 +53,10 @@ extern "C" int moe_decode_block_noalloc(const void *h, const void *w_router, con
     void *ws = nullptr;
     int rc = scratch_on_current_device(&ws);
     if (rc != MOE_OK) return rc;
-    // The array keeps whatever the previous call left in it.  Only the status word must
-    // start at zero; everything else is written before it is read.
+    // The array keeps whatever the previous call left in it.  The status word is cleared
+    // here; the counters and the one-grid path's routing exchange, which must also start at
+    // zero, are zero in the fresh array and every call leaves them zero (no other path writes
+    // them); everything else is written before it is read.
     if (cudaMemsetAsync(ws, 0, 64, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return moe::decode_block(h, w_router, bias, w, M, k, b, residual, out, topk_ids,

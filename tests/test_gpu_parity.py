@@ -53,6 +53,41 @@ def test_route_topk(E, k, H, M, bias, renorm):
     assert near <= max(1, M // 50)
 
 
+@pytest.mark.parametrize("pattern", ["period16", "zeros"])
+@pytest.mark.parametrize("M", [1, 2, 3, 21])
+def test_routing_exact_ties_go_to_the_lower_expert(pattern, M):
+    """Logits that tie exactly: W_r's columns repeat with period 16 (each expert's logit is
+    computed from the same column values in the same order, so experts e, e+16, e+32 ... tie
+    bit for bit -- within one lane's experts and across lanes), or W_r is zero (every logit
+    ties).  Ties go to the lower expert id, so the selection equals the oracle's exactly,
+    through the router kernel, the one-grid block (M <= 2) and the multi-kernel block."""
+    wl = syn.workload("layer_m21", M=M)
+    layer = dict(_workload_layer("layer_m21"))
+    g = torch.Generator(device=DEV).manual_seed(90 + M)
+    if pattern == "zeros":
+        wr = torch.zeros(wl.H, wl.E, dtype=torch.bfloat16, device=DEV)
+    else:
+        base = (torch.randn(wl.H, 16, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+        wr = base.repeat(1, wl.E // 16).contiguous()
+    layer["w_router"] = wr
+    h = syn.make_hidden(wl, M=M, seed=90 + M, device=DEV)
+    o_ids, o_wts, _, logits = G.oracle_routing(layer, h, wl.k)
+    ids, wts = moe.moe_route_topk(h, wr, None, wl.k)
+    assert np.array_equal(ids.cpu().numpy(), o_ids)
+    assert np.allclose(wts.cpu().numpy(), o_wts, rtol=1e-4, atol=1e-6)
+    ws = moe.alloc_workspace(layer, M, wl.k, 0)
+    out, ids2, wts2 = moe.moe_decode_block(h, layer, wl.k, 0, workspace=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    assert np.array_equal(ids2.cpu().numpy(), o_ids)
+    assert torch.equal(wts2, wts)
+    if pattern == "period16":  # the top group: one column's 8 experts, ascending
+        top = int(o_ids[0, 0])
+        assert o_ids[0].tolist() == [top + 16 * j for j in range(wl.k)]
+    else:
+        assert o_ids.tolist() == [list(range(wl.k))] * M
+    G.assert_close_block(G.to_f64(out), G.oracle_ffn(layer, h, o_ids, o_wts), "ties")
+
+
 # --------------------------------------------------------------------------- alignment
 def _gpu_align(ids_np, E, b):
     ids = torch.as_tensor(ids_np, dtype=torch.int32, device=DEV).reshape(ids_np.shape)
