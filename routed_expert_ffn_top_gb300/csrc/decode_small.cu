@@ -95,10 +95,11 @@ struct SmallUnits {
     int n_gu, n_dn, nks_gu, nks_dn;
     __device__ __forceinline__ void at(int64_t u, bool &gu, int &tile, int &ct, int &nks) const {
         gu = u < Tgu;
-        const int64_t v = gu ? u : u - Tgu;
-        const int n = gu ? n_gu : n_dn;
-        tile = (int)(v / n);
-        ct = (int)(v % n);
+        const uint32_t v = (uint32_t)(gu ? u : u - Tgu);  // units fit 32 bits (few tiles here)
+        const uint32_t n = (uint32_t)(gu ? n_gu : n_dn);
+        const uint32_t t = v / n;
+        tile = (int)t;
+        ct = (int)(v - t * n);
         nks = gu ? nks_gu : nks_dn;
     }
 };
