@@ -52,8 +52,9 @@ def build(force: bool = False) -> str:
     tmp = _LIB_PATH + ".tmp%d" % os.getpid()
     # -ffp-contract=off: no fused multiply-add contraction, so the rounding of every
     # product and sum is the one written in the source on every host architecture.
-    # -fopenmp: the expert loop may take whole tokens on several threads (each token's
-    # arithmetic unchanged); without an OpenMP runtime the same source builds serial.
+    # -fopenmp: the expert loop may take routes on several threads (each route's arithmetic
+    # unchanged; the combine runs afterwards in slot order), so the results do not depend on
+    # the thread count; without an OpenMP runtime the same source builds serial.
     base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp]
     if subprocess.run(base + ["-fopenmp", "-lm"], capture_output=True).returncode != 0:
         subprocess.run(base + ["-lm"], check=True)
