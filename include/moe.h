@@ -296,7 +296,7 @@ int moe_decode_block_noalloc(const void *h, const void *w_router, const float *b
  * down kernel, events[5] after the combine kernel (stages a call does not run are not
  * recorded; n must be 6).  moe_reader_ffn records events[0] before its first kernel, then
  * events[1..5] after its scan and sketch scores, selection, exact reads, recovery and final
- * sum.  An
+ * sum (for one token, whose stages run in one kernel, all five after it).  An
  * event between two kernels removes the launch overlap the
  * kernels otherwise get, so traced calls run slightly slower.  Pass NULL (n = 0) to stop.
  */
@@ -380,7 +380,11 @@ size_t moe_reader_workspace_bytes(const moe_reader_t *rd, int M, int k, int K);
  * bf16.  Optional outputs for inspection: selected [M,K] int32, the kept channels of each
  * token (slot * I + channel, ascending, -1 past the token's count), and xr [M,H] fp32, Rx
  * with the unscanned coordinates set to zero.  workspace: ws_bytes >=
- * moe_reader_workspace_bytes(rd, M, k, K), 256-byte aligned.
+ * moe_reader_workspace_bytes(rd, M, k, K), 256-byte aligned; its first 128 bytes (the
+ * status word and the counters of the one-token path) must be zero before the first call
+ * (allocate it zero-filled), and every call leaves them zero.  One token runs as one grid
+ * (the stages in one persistent kernel, bitwise the same results); several tokens run the
+ * stages as five kernels.
  */
 int moe_reader_ffn(const void *h, const moe_reader_t *rd, int M, int k, const int32_t *topk_ids,
                    const float *topk_weights, int K, int nscan, const void *residual, void *out,

@@ -230,7 +230,7 @@ struct ReaderArgs {
     const __nv_bfloat16 *coef;              // [E][I][rank]
 };
 struct ReaderWs {
-    size_t status, xr, ahat, score, keep, sel, nsel, partial, zpart, total;
+    size_t status, ctl, xr, ahat, score, keep, sel, nsel, partial, zpart, total;
     int nchunk;
 };
 ReaderWs reader_ws_layout(const ReaderArgs &r, int M, int k, int K);

@@ -27,6 +27,7 @@
 // Every sum has an order fixed by indices (never by the grid or by M): a token's output
 // is bitwise reproducible and independent of the other tokens.
 #include <algorithm>
+#include <type_traits>
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
@@ -258,31 +259,23 @@ __device__ __forceinline__ void scan_block(const __nv_bfloat16 *hm, char4 sg, in
 // Grid (G, M), 32 warps (one CTA per SM and token, so the scan and the table are built once
 // per SM); shared memory: the table, (H/4) x 17 floats (one pad float per group spreads
 // the lanes' reads over the banks) and xr (H floats).
-template <int kMaxPass>
-__global__ void __launch_bounds__(kSketchWarps * 32)
-    reader_sketch_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h, int nscan,
-                         float *__restrict__ xr_out, const int32_t *__restrict__ ids,
-                         const float *__restrict__ wts, int k, float *__restrict__ ahat,
-                         float *__restrict__ score) {
-    extern __shared__ __align__(16) float T[];  // nibble table (nib_index), xr [H], xp [H/32][33]
-    // the rotation signs of this warp's first block are weights: load them before the wait
-    const int nb0 = r.H / kRB;
-    char4 sg0 = make_char4(0, 0, 0, 0);
-    if ((int)(threadIdx.x >> 5) < nb0)
-        sg0 = *reinterpret_cast<const char4 *>(r.signs + (threadIdx.x >> 5) * kRB + 4 * (threadIdx.x & 31));
-    pdl_wait();
-    pdl_launch_dependents();
-    const int m = blockIdx.y, H = r.H, I = r.I, nb = H / kRB;
-    const int N = k * I;
+// Stage 1a in one CTA for token row hm: x rotated and scanned into xr (warp w of W takes
+// blocks w, w + W, ...; sg0 is the signs of warp w's first block, loaded early), then the
+// nibble table T (see nib_index) from a copy of xr padded to 33 floats per 32-coordinate word.
+// T: the shared-memory table, xr at T + nib_table_floats(H), the padded copy after xr.
+// xr_out (may be NULL): where the scanned xr is also stored.
+__device__ void sketch_prepare(const ReaderArgs &r, const __nv_bfloat16 *hm, int nscan, char4 sg0,
+                               float *T, float *xr_out) {
+    const int H = r.H, nb = H / kRB;
     float *xr = T + nib_table_floats(H);
-    for (int b = threadIdx.x >> 5; b < nb; b += kSketchWarps) {
+    for (int b = threadIdx.x >> 5; b < nb; b += (int)(blockDim.x >> 5)) {
         const char4 sg = b == (int)(threadIdx.x >> 5) ? sg0 : *reinterpret_cast<const char4 *>(
                                                                r.signs + b * kRB + 4 * (threadIdx.x & 31));
-        scan_block(h + (size_t)m * H, sg, b, nscan, xr + b * kRB, threadIdx.x & 31);
+        scan_block(hm, sg, b, nscan, xr + b * kRB, threadIdx.x & 31);
     }
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int c = threadIdx.x; c < H; c += blockDim.x) xr_out[(size_t)m * H + c] = xr[c];
+    if (xr_out)
+        for (int c = threadIdx.x; c < H; c += blockDim.x) xr_out[c] = xr[c];
     // The table from a copy of xr padded to 33 floats per 32-coordinate word: the thread of
     // (word w, group q) reads its 4 coordinates and writes its 16 sums, both bank-distinct
     // across the warp's consecutive words.
@@ -304,11 +297,31 @@ __global__ void __launch_bounds__(kSketchWarps * 32)
         }
     }
     __syncthreads();
+}
+
+// The signs of this thread's warp's first rotation block (weights: read before the wait).
+__device__ __forceinline__ char4 first_block_signs(const ReaderArgs &r) {
+    char4 sg0 = make_char4(0, 0, 0, 0);
+    if ((int)(threadIdx.x >> 5) < r.H / kRB)
+        sg0 = *reinterpret_cast<const char4 *>(r.signs + (threadIdx.x >> 5) * kRB + 4 * (threadIdx.x & 31));
+    return sg0;
+}
+
+// Stage 1b and the score of Stage 2 for token m's candidate channels f = f0, f0 + fstep, ...
+// (this warp's), against the table T: a code word pair (nonzero, negative masks of 32
+// coordinates) dots with xr in 16 table reads, the positive nibbles' sums minus the negative
+// nibbles' sums; lanes take the 32-coordinate words of a block four at a time, and the
+// blocks are summed with their scales in block order.
+template <int kMaxPass>
+__device__ void sketch_channels(const ReaderArgs &r, const float *T, int m, int f0, int fstep,
+                                const int32_t *__restrict__ ids, const float *__restrict__ wts,
+                                int k, float *__restrict__ ahat, float *__restrict__ score) {
+    const int I = r.I, nb = r.H / kRB;
+    const int N = k * I;
     const int lane = threadIdx.x & 31;
-    const int nwarps = gridDim.x * kSketchWarps;
     const int nwords = 4 * nb;              // 32-coordinate words per row
     const int npass = (nwords + 31) / 32;   // words per lane and row, at most kMaxPass
-    for (int f = blockIdx.x * kSketchWarps + (threadIdx.x >> 5); f < N; f += nwarps) {
+    for (int f = f0; f < N; f += fstep) {
         const int j = f / I, i = f - j * I;
         const int e = ids[(size_t)m * k + j];
         const size_t o = (size_t)m * N + f;
@@ -373,9 +386,32 @@ __global__ void __launch_bounds__(kSketchWarps * 32)
     }
 }
 
-// Inclusive scan over the 1024 threads of a block (values in thread order).
-__device__ __forceinline__ int block_scan_1024(int v, int *warp_tot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Stage 1 and the score of Stage 2.  Every CTA of token m rotates and scans the token's x and
+// builds the table (CTA 0 also stores xr for inspection); then one warp per candidate channel
+// at a time (warps stride over the token's channels).  Grid (G, M), 32 warps (one CTA per SM
+// and token, so the scan and the table are built once per SM); shared memory: the table, xr
+// (H floats) and its padded copy ((H/32) x 33 floats).
+template <int kMaxPass>
+__global__ void __launch_bounds__(kSketchWarps * 32)
+    reader_sketch_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h, int nscan,
+                         float *__restrict__ xr_out, const int32_t *__restrict__ ids,
+                         const float *__restrict__ wts, int k, float *__restrict__ ahat,
+                         float *__restrict__ score) {
+    extern __shared__ __align__(16) float T[];
+    // the rotation signs of this warp's first block are weights: load them before the wait
+    const char4 sg0 = first_block_signs(r);
+    pdl_wait();
+    pdl_launch_dependents();
+    const int m = blockIdx.y;
+    sketch_prepare(r, h + (size_t)m * r.H, nscan, sg0, T,
+                   blockIdx.x == 0 ? xr_out + (size_t)m * r.H : nullptr);
+    sketch_channels<kMaxPass>(r, T, m, blockIdx.x * kSketchWarps + (threadIdx.x >> 5),
+                              gridDim.x * kSketchWarps, ids, wts, k, ahat, score);
+}
+
+// Inclusive scan over the threads of a block of at most 1024 (values in thread order).
+__device__ __forceinline__ int block_scan(int v, int *warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -384,7 +420,7 @@ __device__ __forceinline__ int block_scan_1024(int v, int *warp_tot) {
     if (lane == 31) warp_tot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        int t = warp_tot[lane];
+        int t = lane < nwarps ? warp_tot[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int u = __shfl_up_sync(0xffffffffu, t, o);
@@ -398,33 +434,30 @@ __device__ __forceinline__ int block_scan_1024(int v, int *warp_tot) {
     return v + add;
 }
 
-// Stage 2 selection: the K largest scores of token m (ties: lower channel index), by a
+// Stage 2 selection: the K largest of a token's N scores (ties: lower channel index), by a
 // most-significant-digit radix select on order-preserving keys (integer counts commute, so
 // the result does not depend on arrival order), then the kept flags and the kept channels
-// in ascending index.  One 1024-thread CTA per token; keys in shared memory.
-__global__ void __launch_bounds__(kSelectThreads)
-    reader_select_kernel(const float *__restrict__ score, int N, int K,
-                         uint8_t *__restrict__ keep, int32_t *__restrict__ sel,
-                         int32_t *__restrict__ nsel) {
-    extern __shared__ uint32_t keys[];  // [N], then two sets of 32 warp histograms of 256 bins
-    int *whist = reinterpret_cast<int *>(keys + N);
+// in ascending index.  One CTA of 256 to 1024 threads (the result does not depend on the
+// count); keys [N] and two sets of 32 warp histograms of 256 bins in shared memory.  On return keys[f] is 1 for a kept channel, else 0 (read after
+// a barrier).  Outputs: keep (may be NULL) one byte per channel, sel [K] the kept channels
+// then -1, nsel the count.
+__device__ void select_token(const float *__restrict__ score, int N, int K, uint32_t *keys,
+                             int *whist, uint8_t *keep, int32_t *sel, int32_t *nsel) {
     __shared__ int warp_tot[32];
     __shared__ int s_nvalid, s_digit, s_remaining, s_count;
     __shared__ uint32_t s_and, s_or;
-    pdl_wait();
-    pdl_launch_dependents();
-    const int m = blockIdx.x, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     if (tid == 0) {
         s_nvalid = 0;
         s_and = ~0u;
         s_or = 0u;
     }
-    for (int d = tid; d < 32 * 256; d += kSelectThreads) whist[d] = 0;
+    for (int d = tid; d < 32 * 256; d += (int)blockDim.x) whist[d] = 0;
     __syncthreads();
     int nv = 0;
     uint32_t k_and = ~0u, k_or = 0u;  // over the valid keys: their common leading bits
-    for (int f = tid; f < N; f += kSelectThreads) {
-        const float s = score[(size_t)m * N + f];
+    for (int f = tid; f < N; f += (int)blockDim.x) {
+        const float s = __ldcg(score + f);
         const uint32_t key = s >= 0.0f ? __float_as_uint(s) + 1u : 0u;  // invalid / NaN: 0
         keys[f] = key;
         nv += key != 0u;
@@ -467,16 +500,16 @@ __global__ void __launch_bounds__(kSelectThreads)
             const int wbase = (tid >> 5) * 256;
             // each warp counts into its own histogram (integer adds commute); the other set
             // is cleared for the next pass meanwhile
-            for (int f = tid; f < N; f += kSelectThreads)
+            for (int f = tid; f < N; f += (int)blockDim.x)
                 if ((keys[f] & mask) == prefix) atomicAdd(&hist[wbase + ((keys[f] >> lo) & dmask)], 1);
-            for (int d = tid; d < 32 * 256; d += kSelectThreads) next[d] = 0;
+            for (int d = tid; d < 32 * 256; d += (int)blockDim.x) next[d] = 0;
             __syncthreads();
             // thread t < nb owns digit nb - 1 - t: its count over the warps, then a scan in
             // descending digit order finds the digit where the count reaches `remaining`
             int c = 0;
             if (tid < nb)
                 for (int w = 0; w < 32; ++w) c += hist[w * 256 + (nb - 1 - tid)];
-            const int incl = block_scan_1024(c, warp_tot);
+            const int incl = block_scan(c, warp_tot);
             if (tid < nb && c > 0 && incl >= remaining && incl - c < remaining) {
                 s_digit = nb - 1 - tid;
                 s_remaining = remaining - (incl - c);
@@ -495,11 +528,11 @@ __global__ void __launch_bounds__(kSelectThreads)
     // keys above the prefix are kept, and the first `remaining` keys under it in index order;
     // each thread owns a contiguous run of channels
     const uint32_t T = prefix;
-    const int per = (N + kSelectThreads - 1) / kSelectThreads;
+    const int per = (N + (int)blockDim.x - 1) / (int)blockDim.x;
     const int f0 = tid * per, f1 = min(N, f0 + per);
     int eq = 0;
     for (int f = f0; f < f1; ++f) eq += (Keff > 0 && (keys[f] & mask) == T);
-    int eq_before = block_scan_1024(eq, warp_tot) - eq;
+    int eq_before = block_scan(eq, warp_tot) - eq;
     int kc = 0;
     for (int f = f0; f < f1; ++f) {
         const uint32_t key = keys[f] & mask;
@@ -508,50 +541,59 @@ __global__ void __launch_bounds__(kSelectThreads)
             if (key > T) kp = true;
             else if (key == T) kp = eq_before++ < remaining;
         }
-        keep[(size_t)m * N + f] = kp ? 1 : 0;
+        if (keep) keep[f] = kp ? 1 : 0;
         keys[f] = kp ? 1u : 0u;  // reused as the kept flag
         kc += kp;
     }
     __syncthreads();
-    int pos = block_scan_1024(kc, warp_tot) - kc;
+    int pos = block_scan(kc, warp_tot) - kc;
     for (int f = f0; f < f1; ++f)
-        if (keys[f]) sel[(size_t)m * K + pos++] = f;
-    for (int q = Keff + tid; q < K; q += kSelectThreads) sel[(size_t)m * K + q] = -1;
-    if (tid == 0) nsel[m] = Keff;
+        if (keys[f]) sel[pos++] = f;
+    for (int q = Keff + tid; q < K; q += (int)blockDim.x) sel[q] = -1;
+    if (tid == 0) *nsel = Keff;
 }
 
-// Stage 2 exact reads: chunk c of token m's kept channels (positions 8c .. 8c+7 of the
-// ascending list), one warp per channel for a = SiLU(g . x) (v . x), then the chunk's
-// sum of w a d in channel order into its own partial row.  Grid (nchunk, M), 256 threads.
-template <int kDPass>
-__global__ void __launch_bounds__(256)
-    reader_exact_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h,
-                        const int32_t *__restrict__ ids, const float *__restrict__ wts, int k,
-                        int K, const int32_t *__restrict__ sel, const int32_t *__restrict__ nsel,
-                        int nchunk, float *__restrict__ partial) {
-    extern __shared__ __align__(16) unsigned char xraw[];  // token row, bf16 [H]
-    __shared__ float wa[kExactChunk];
-    __shared__ int64_t chs[kExactChunk];
+// The selection of token m = blockIdx.x, into the workspace.  One 1024-thread CTA per token.
+__global__ void __launch_bounds__(kSelectThreads)
+    reader_select_kernel(const float *__restrict__ score, int N, int K,
+                         uint8_t *__restrict__ keep, int32_t *__restrict__ sel,
+                         int32_t *__restrict__ nsel) {
+    extern __shared__ uint32_t keys[];  // [N], then two sets of 32 warp histograms of 256 bins
     pdl_wait();
     pdl_launch_dependents();
-    const int m = blockIdx.y, c = blockIdx.x, H = r.H, I = r.I;
+    const int m = blockIdx.x;
+    select_token(score + (size_t)m * N, N, K, keys, reinterpret_cast<int *>(keys + N),
+                 keep + (size_t)m * N, sel + (size_t)m * K, nsel + m);
+}
+
+// Stage 2 exact reads: chunk c of a token's kept channels (positions 8c .. 8c+7 of the
+// ascending list sel, nsel of them), one warp per channel for a = SiLU(g . x) (v . x), then
+// the chunk's sum of w a d in channel order into its own partial row out [H].  The work runs
+// on the CTA's first 256 threads; every thread of the CTA must call it (it has barriers).
+// Shared memory: xs4 the token row (H bf16), wa [8], chs [8].
+template <int kDPass>
+__device__ void exact_chunk(const ReaderArgs &r, const __nv_bfloat16 *__restrict__ hm,
+                            const int32_t *__restrict__ ids_m, const float *__restrict__ wts_m,
+                            const int32_t *sel, int nsel, int c, float *__restrict__ out,
+                            uint4 *xs4, float *wa, int64_t *chs) {
+    const int H = r.H, I = r.I;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint4 *hx = reinterpret_cast<const uint4 *>(h + (size_t)m * H);
-    uint4 *xs4 = reinterpret_cast<uint4 *>(xraw);
+    const bool act = threadIdx.x < 256;
+    const uint4 *hx = reinterpret_cast<const uint4 *>(hm);
     for (int q = threadIdx.x; q < H / 8; q += blockDim.x) xs4[q] = hx[q];
     __syncthreads();
     // the chunk's channels first (one per warp), so that every load below can be issued at once
     const int s = c * kExactChunk + warp;
-    if (lane == 0) {
+    if (warp < kExactChunk && lane == 0) {
         int64_t ch = -1;
         float w = 0.0f;
-        if (s < nsel[m]) {
-            const int f = sel[(size_t)m * K + s];
+        if (s < nsel) {
+            const int f = sel[s];
             const int j = f / I, i = f - j * I;
-            const int e = ids[(size_t)m * k + j];
+            const int e = ids_m[j];
             if (e >= 0 && e < r.E) {
                 ch = (int64_t)e * I + i;
-                w = wts[(size_t)m * k + j];
+                w = wts_m[j];
             }
         }
         chs[warp] = ch;
@@ -561,13 +603,15 @@ __global__ void __launch_bounds__(256)
     // this thread's pieces of the chunk's down rows are in flight while the warps form a
     const int c0 = threadIdx.x * 8;  // 2048 columns per pass: kDPass = ceil(H / 2048)
     uint4 dv[kDPass][kExactChunk];
+    if (act) {
 #pragma unroll
-    for (int ps = 0; ps < kDPass; ++ps)
+        for (int ps = 0; ps < kDPass; ++ps)
 #pragma unroll
-        for (int q = 0; q < kExactChunk; ++q)
-            if (c0 + ps * 2048 < H && chs[q] >= 0)
-                dv[ps][q] = *reinterpret_cast<const uint4 *>(r.w_down + chs[q] * H + c0 + ps * 2048);
-    const int64_t ch = chs[warp];
+            for (int q = 0; q < kExactChunk; ++q)
+                if (c0 + ps * 2048 < H && chs[q] >= 0)
+                    dv[ps][q] = *reinterpret_cast<const uint4 *>(r.w_down + chs[q] * H + c0 + ps * 2048);
+    }
+    const int64_t ch = warp < kExactChunk ? chs[warp] : -1;
     if (ch >= 0) {
         const uint4 *g = reinterpret_cast<const uint4 *>(r.g_rows + ch * H);
         const uint4 *v = reinterpret_cast<const uint4 *>(r.v_rows + ch * H);
@@ -606,56 +650,76 @@ __global__ void __launch_bounds__(256)
         if (lane == 0) wa[warp] = wa[warp] * (silu_f32(gx) * vx);
     }
     __syncthreads();
-    float *out = partial + ((size_t)m * nchunk + c) * H;
+    if (act) {
 #pragma unroll
-    for (int ps = 0; ps < kDPass; ++ps) {
-        const int cc = c0 + ps * 2048;
-        if (cc >= H) break;
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int ps = 0; ps < kDPass; ++ps) {
+            const int cc = c0 + ps * 2048;
+            if (cc >= H) break;
+            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int q = 0; q < kExactChunk; ++q) {
-            if (chs[q] < 0) continue;
-            const uint32_t dw[4] = {dv[ps][q].x, dv[ps][q].y, dv[ps][q].z, dv[ps][q].w};
-            const float a = wa[q];
+            for (int q = 0; q < kExactChunk; ++q) {
+                if (chs[q] < 0) continue;
+                const uint32_t dw[4] = {dv[ps][q].x, dv[ps][q].y, dv[ps][q].z, dv[ps][q].w};
+                const float a = wa[q];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                acc[2 * t] = fmaf(a, bf16_lo(dw[t]), acc[2 * t]);
-                acc[2 * t + 1] = fmaf(a, bf16_hi(dw[t]), acc[2 * t + 1]);
+                for (int t = 0; t < 4; ++t) {
+                    acc[2 * t] = fmaf(a, bf16_lo(dw[t]), acc[2 * t]);
+                    acc[2 * t + 1] = fmaf(a, bf16_hi(dw[t]), acc[2 * t + 1]);
+                }
             }
+            *reinterpret_cast<float4 *>(out + cc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4 *>(out + cc + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
-        *reinterpret_cast<float4 *>(out + cc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(out + cc + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
+    __syncthreads();  // the shared arrays may be reused by the caller's next chunk
+}
+
+// The exact reads of chunk blockIdx.x of token blockIdx.y.  Grid (nchunk, M), 256 threads.
+template <int kDPass>
+__global__ void __launch_bounds__(256)
+    reader_exact_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h,
+                        const int32_t *__restrict__ ids, const float *__restrict__ wts, int k,
+                        int K, const int32_t *__restrict__ sel, const int32_t *__restrict__ nsel,
+                        int nchunk, float *__restrict__ partial) {
+    extern __shared__ __align__(16) unsigned char xraw[];  // token row, bf16 [H]
+    __shared__ float wa[kExactChunk];
+    __shared__ int64_t chs[kExactChunk];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int m = blockIdx.y, c = blockIdx.x;
+    exact_chunk<kDPass>(r, h + (size_t)m * r.H, ids + (size_t)m * k, wts + (size_t)m * k,
+                        sel + (size_t)m * K, nsel[m], c, partial + ((size_t)m * nchunk + c) * r.H,
+                        reinterpret_cast<uint4 *>(xraw), wa, chs);
 }
 
 // Stage 3: z_j = sum over the discarded channels i of slot j (ascending within a thread,
 // then the lanes by a fixed xor tree, then the warps in order) of w_j ahat b_{e,i}.
-// It needs only the selection, which was complete before the exact-read grid that precedes
-// it could start, so it runs beside that grid (reading the selection from L2) and waits for
-// it only before finishing: the final grid, which waits for this one, then sees both.
-// Part p of slot j takes channels [p I/4, (p+1) I/4).  Grid (4 k, M), 256 threads.
+// Part p of slot j takes channels [p I/4, (p+1) I/4) of a token; its z goes to zpart.  The
+// work runs on the CTA's first 256 threads; every thread must call it (it has a barrier).
+// keep: the token's kept flags (global bytes, or the selection's shared-memory flags).
 constexpr int kRecParts = 4;
-__global__ void __launch_bounds__(256)
-    reader_recover_kernel(ReaderArgs r, const int32_t *__restrict__ ids,
-                          const float *__restrict__ wts, int k, const float *__restrict__ ahat,
-                          const uint8_t *__restrict__ keep, float *__restrict__ zpart) {
-    __shared__ float red[8][kReaderMaxRank];
-    pdl_launch_dependents();
-    const int j = blockIdx.x / kRecParts, part = blockIdx.x % kRecParts, m = blockIdx.y;
+__device__ __forceinline__ bool kept_flag(const uint8_t *keep, size_t f) { return __ldcg(keep + f) != 0; }
+__device__ __forceinline__ bool kept_flag(const uint32_t *keep, size_t f) { return keep[f] != 0u; }
+
+template <typename KeepT>
+__device__ void recover_part(const ReaderArgs &r, const int32_t *__restrict__ ids_m,
+                             const float *__restrict__ wts_m, int k, const float *ahat_m,
+                             const KeepT *keep_m, int j, int part, float *__restrict__ zout,
+                             float (*red)[kReaderMaxRank]) {
     const int I = r.I, rank = r.rank, tid = threadIdx.x;
-    const int N = k * I;
+    const bool act = tid < 256;
     const int per = (I + kRecParts - 1) / kRecParts;
     const int i0 = part * per, i1 = min(I, i0 + per);
-    const int e = ids[(size_t)m * k + j];
+    const int e = ids_m[j];
     float acc[kReaderMaxRank];
 #pragma unroll
     for (int q = 0; q < kReaderMaxRank; ++q) acc[q] = 0.0f;
-    if (e >= 0 && e < r.E) {
-        const float w = wts[(size_t)m * k + j];
+    if (act && e >= 0 && e < r.E) {
+        const float w = wts_m[j];
         for (int i = i0 + tid; i < i1; i += 256) {
-            const size_t f = (size_t)m * N + (size_t)j * I + i;
-            if (__ldcg(keep + f)) continue;
-            const float cw = w * __ldcg(ahat + f);
+            const size_t f = (size_t)j * I + i;
+            if (kept_flag(keep_m, f)) continue;
+            const float cw = w * __ldcg(ahat_m + f);
             const __nv_bfloat16 *b = r.coef + ((int64_t)e * I + i) * rank;
             if ((rank & 7) == 0) {  // whole 16-byte pieces of 8 coefficients
 #pragma unroll
@@ -676,75 +740,237 @@ __global__ void __launch_bounds__(256)
             }
         }
     }
+    if (act) {
 #pragma unroll
-    for (int q = 0; q < kReaderMaxRank; ++q) {
-        const float v = warp_sum(acc[q]);
-        if ((tid & 31) == 0) red[tid >> 5][q] = v;
+        for (int q = 0; q < kReaderMaxRank; ++q) {
+            const float v = warp_sum(acc[q]);
+            if ((tid & 31) == 0) red[tid >> 5][q] = v;
+        }
     }
     __syncthreads();
     if (tid < rank) {
         float z = 0.0f;
         for (int w = 0; w < 8; ++w) z += red[w][tid];
-        zpart[(((size_t)m * k + j) * kRecParts + part) * rank + tid] = z;
+        zout[tid] = z;
     }
+    __syncthreads();  // red may be reused by the caller's next part
+}
+
+// It needs only the selection, which was complete before the exact-read grid that precedes
+// it could start, so it runs beside that grid (reading the selection from L2) and waits for
+// it only before finishing: the final grid, which waits for this one, then sees both.
+// Grid (4 k, M), 256 threads.
+__global__ void __launch_bounds__(256)
+    reader_recover_kernel(ReaderArgs r, const int32_t *__restrict__ ids,
+                          const float *__restrict__ wts, int k, const float *__restrict__ ahat,
+                          const uint8_t *__restrict__ keep, float *__restrict__ zpart) {
+    __shared__ float red[8][kReaderMaxRank];
+    pdl_launch_dependents();
+    const int j = blockIdx.x / kRecParts, part = blockIdx.x % kRecParts, m = blockIdx.y;
+    const size_t N = (size_t)k * r.I;
+    recover_part(r, ids + (size_t)m * k, wts + (size_t)m * k, k, ahat + (size_t)m * N,
+                 keep + (size_t)m * N, j, part,
+                 zpart + (((size_t)m * k + j) * kRecParts + part) * r.rank, red);
     pdl_wait();  // the exact-read grid has finished before this one does
 }
 
-// out[m][n] = bf16(residual + (ex + sum_r U[n][r] z[r])), z = sum over slots in order, ex the
-// chunk partials: warp w of the CTA sums chunks w, w + 8, ... in order for 32 columns, then
-// the 8 warps' sums are added in warp order.  Grid (ceil(H / 32), M), 256 threads.
+// out[n] = bf16(residual + (ex + sum_r U[n][r] z[r])) for the 32 columns of block bx of a
+// token: z = sum over slots in order of zpart, ex the chunk partials -- warp w sums chunks
+// w, w + 8, ... in order for 32 columns, then the 8 warps' sums are added in warp order.  The
+// work runs on the CTA's first 256 threads; every thread must call it (it has barriers).
+__device__ void final_block(const ReaderArgs &r, int k, int nchunk, const float *partial_m,
+                            const float *zpart_m, const __nv_bfloat16 *res_m,
+                            __nv_bfloat16 *out_m, int bx, float *z, float (*red)[32],
+                            float *recs) {
+    const int H = r.H, rank = r.rank, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const bool act = tid < 256;
+    if (tid < rank) {
+        float s = 0.0f;
+        for (int q = 0; q < k * kRecParts; ++q) s += __ldcg(zpart_m + (size_t)q * rank + tid);
+        z[tid] = s;
+    }
+    const int n = bx * 32 + lane;
+    if (act) {
+        float ex = 0.0f;
+        if (n < H) {
+            const float *pp = partial_m + n;
+            int c = warp;
+            for (; c + 8 * 7 < nchunk; c += 8 * 8) {  // 8 of the warp's chunks in flight
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldcg(pp + (size_t)(c + 8 * u) * H);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) ex += v[u];
+            }
+            for (; c < nchunk; c += 8) ex += __ldcg(pp + (size_t)c * H);
+        }
+        red[warp][lane] = ex;
+    }
+    __syncthreads();
+    // U z for the block's 32 columns: warp w takes columns 4w .. 4w+3, lane q the q-th
+    // coefficient of a column's U row (one coalesced row read), then a fixed xor tree
+    if (act) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int col = bx * 32 + 4 * warp + u;
+            float t = 0.0f;
+            if (col < H && lane < rank) t = r.U[(size_t)col * rank + lane] * z[lane];
+            t = warp_sum(t);
+            if (lane == 0) recs[4 * warp + u] = t;
+        }
+    }
+    __syncthreads();
+    if (warp == 0 && n < H) {
+        float acc = 0.0f;
+        for (int w = 0; w < 8; ++w) acc += red[w][lane];
+        acc += recs[lane];
+        const float res = res_m ? __bfloat162float(res_m[n]) : 0.0f;
+        out_m[n] = __float2bfloat16_rn(res + acc);
+    }
+    __syncthreads();  // the shared arrays may be reused by the caller's next block
+}
+
+// The final sum of column block blockIdx.x of token blockIdx.y.  Grid (ceil(H / 32), M), 256
+// threads.
 __global__ void __launch_bounds__(256)
     reader_final_kernel(ReaderArgs r, int k, int nchunk, const float *__restrict__ partial,
                         const float *__restrict__ zpart, const __nv_bfloat16 *__restrict__ residual,
                         __nv_bfloat16 *__restrict__ out) {
     __shared__ float z[kReaderMaxRank];
     __shared__ float red[8][32];
+    __shared__ float recs[32];
     pdl_wait();
     pdl_launch_dependents();
-    const int m = blockIdx.y, H = r.H, rank = r.rank, tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    if (tid < rank) {
-        float s = 0.0f;
-        for (int q = 0; q < k * kRecParts; ++q) s += __ldcg(zpart + ((size_t)m * k * kRecParts + q) * rank + tid);
-        z[tid] = s;
-    }
-    const int n = blockIdx.x * 32 + lane;
-    float ex = 0.0f;
-    if (n < H) {
-        const float *pp = partial + (size_t)m * nchunk * H + n;
-        int c = warp;
-        for (; c + 8 * 7 < nchunk; c += 8 * 8) {  // 8 of the warp's chunks in flight
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(pp + (size_t)(c + 8 * u) * H);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ex += v[u];
-        }
-        for (; c < nchunk; c += 8) ex += __ldcg(pp + (size_t)c * H);
-    }
-    red[warp][lane] = ex;
-    __syncthreads();
-    // U z for the CTA's 32 columns: warp w takes columns 4w .. 4w+3, lane q the q-th
-    // coefficient of a column's U row (one coalesced row read), then a fixed xor tree
-    __shared__ float recs[32];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int col = blockIdx.x * 32 + 4 * warp + u;
-        float t = 0.0f;
-        if (col < H && lane < rank) t = r.U[(size_t)col * rank + lane] * z[lane];
-        t = warp_sum(t);
-        if (lane == 0) recs[4 * warp + u] = t;
-    }
-    __syncthreads();
-    if (warp != 0 || n >= H) return;
-    float acc = 0.0f;
-    for (int w = 0; w < 8; ++w) acc += red[w][lane];
-    acc += recs[lane];
-    const float res = residual ? __bfloat162float(residual[(size_t)m * H + n]) : 0.0f;
-    out[(size_t)m * H + n] = __float2bfloat16_rn(res + acc);
+    const int m = blockIdx.y, H = r.H;
+    final_block(r, k, nchunk, partial + (size_t)m * nchunk * H,
+                zpart + (size_t)m * k * kRecParts * r.rank,
+                residual ? residual + (size_t)m * H : nullptr, out + (size_t)m * H, blockIdx.x, z,
+                red, recs);
 }
 
-// Workspace of one reader call: xr, ahat, score, keep, sel, nsel, partial, zpart.
+// ------------------------------------------------------------- one token, one grid
+// For one token the five stages above run as one persistent grid of 512-thread CTAs, one
+// per SM: every stage is the same device function with the same arithmetic, so the output
+// is bitwise the multi-kernel path's.  Between the stages:
+//   scores   -> every CTA, after a release count of all CTAs: the selection, run by every
+//               CTA on its own (the same result everywhere; CTA 0 stores it);
+//   items    -> exact chunks c and recovery parts, CTA i taking items i, i + G, ...;
+//   partials -> the CTAs of the column blocks, after a second count: the final sum.
+// The counters live in the workspace (zero between calls: the last CTA to leave, found with
+// an exit ticket, restores them); every wait is bounded and a wait that gives up sets
+// MOE_DEV_WAIT_TIMEOUT.
+constexpr int kReaderCtlScores = 0, kReaderCtlItems = 1, kReaderCtlExit = 2;
+// 512 threads: the exact reads' 122 registers per thread fit.  (1024 threads cap them at 64:
+// with the exact reads' loads batched 4 instead of 8 it still spilled, and measured slower,
+// 36.5 against 33.1 us per router + reader step.)
+constexpr int kOneThreads = 512;
+
+// Bounded wait until *p >= need (acquire, GPU scope).
+__device__ __forceinline__ bool reader_count_wait(const int32_t *p, int need) {
+    if (ld_acquire_gpu(p) >= need) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= need) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Shared-memory floats of the one-grid kernel: the largest of the stages' carves.
+__host__ __device__ inline size_t reader_one_smem_floats(int H, int N, int K) {
+    const size_t sketch = (size_t)nib_table_floats(H) + H + (size_t)(H / 32) * 33;
+    const size_t later = (size_t)N + 2 * 32 * 256 + (((size_t)(K > 0 ? K : 1) + 3) & ~size_t(3)) + H / 2;
+    return sketch > later ? sketch : later;
+}
+
+template <int kMaxPass, int kDPass>
+__global__ void __launch_bounds__(kOneThreads, 1)
+    reader_one_kernel(ReaderArgs r, const __nv_bfloat16 *__restrict__ h, int nscan,
+                      float *__restrict__ xr_out, const int32_t *__restrict__ ids,
+                      const float *__restrict__ wts, int k, int K, float *__restrict__ ahat,
+                      float *__restrict__ score, int32_t *__restrict__ sel,
+                      int32_t *__restrict__ nsel, int nchunk, float *__restrict__ partial,
+                      float *__restrict__ zpart, const __nv_bfloat16 *__restrict__ residual,
+                      __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ ctl,
+                      int32_t *__restrict__ status) {
+    extern __shared__ __align__(16) float smem[];
+    __shared__ float wa[kExactChunk];
+    __shared__ int64_t chs[kExactChunk];
+    __shared__ float red_r[8][kReaderMaxRank];
+    __shared__ float zf[kReaderMaxRank], redf[8][32], recs[32];
+    __shared__ int32_t nsel_s;
+    __shared__ int last_s;
+    const int tid = threadIdx.x, G = gridDim.x, H = r.H;
+    const int N = k * r.I;
+    const char4 sg0 = first_block_signs(r);  // weights: before the wait
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // Stage 1: scan, table, and the scores of this CTA's share of the channels
+    sketch_prepare(r, h, nscan, sg0, smem, blockIdx.x == 0 ? xr_out : nullptr);
+    sketch_channels<kMaxPass>(r, smem, 0, blockIdx.x * (kOneThreads / 32) + (tid >> 5),
+                              G * (kOneThreads / 32), ids, wts, k, ahat, score);
+    __syncthreads();
+    if (tid == 0) {
+        red_release_gpu_add(ctl + kReaderCtlScores, 1);
+        if (!reader_count_wait(ctl + kReaderCtlScores, G)) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+    }
+    __syncthreads();
+
+    // Stage 2 selection, in every CTA
+    uint32_t *keys = reinterpret_cast<uint32_t *>(smem);
+    int *whist = reinterpret_cast<int *>(keys + N);
+    int32_t *sel_s = whist + 2 * 32 * 256;
+    uint4 *xs4 = reinterpret_cast<uint4 *>(sel_s + (((K > 0 ? K : 1) + 3) & ~3));
+    select_token(score, N, K, keys, whist, nullptr, sel_s, &nsel_s);
+    __syncthreads();
+    const int nsl = nsel_s;
+    if (blockIdx.x == 0) {
+        for (int q = tid; q < K; q += blockDim.x) sel[q] = sel_s[q];
+        if (tid == 0) nsel[0] = nsl;
+    }
+
+    // Stage 2 exact reads and Stage 3 recovery: items i, i + G, ...
+    const int nitems = nchunk + k * kRecParts;
+    for (int it = blockIdx.x; it < nitems; it += G) {
+        if (it < nchunk) {
+            exact_chunk<kDPass>(r, h, ids, wts, sel_s, nsl, it, partial + (size_t)it * H, xs4, wa, chs);
+        } else {
+            const int q = it - nchunk, j = q / kRecParts, part = q % kRecParts;
+            recover_part(r, ids, wts, k, ahat, keys, j, part,
+                         zpart + ((size_t)j * kRecParts + part) * r.rank, red_r);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) red_release_gpu_add(ctl + kReaderCtlItems, 1);
+
+    // the final sum, by the CTAs of the column blocks
+    const int nbx = (H + 31) / 32;
+    if ((int)blockIdx.x < nbx) {
+        if (tid == 0 && !reader_count_wait(ctl + kReaderCtlItems, G))
+            atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+        __syncthreads();
+        for (int bx = blockIdx.x; bx < nbx; bx += G)
+            final_block(r, k, nchunk, partial, zpart, residual, out, bx, zf, redf, recs);
+    }
+
+    // exit: the last CTA restores the counters
+    __syncthreads();
+    if (tid == 0) {
+        int32_t old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ctl + kReaderCtlExit) : "memory");
+        last_s = old == G - 1;
+        if (last_s) {
+            ctl[kReaderCtlScores] = 0;
+            ctl[kReaderCtlItems] = 0;
+            ctl[kReaderCtlExit] = 0;
+        }
+    }
+}
+
+// Workspace of one reader call: status, counters, xr, ahat, score, keep, sel, nsel, partial,
+// zpart.
 ReaderWs reader_ws_layout(const ReaderArgs &r, int M, int k, int K) {
     ReaderWs L;
     size_t off = 0;
@@ -756,6 +982,7 @@ ReaderWs reader_ws_layout(const ReaderArgs &r, int M, int k, int K) {
     const size_t N = (size_t)k * r.I;
     L.nchunk = (K + kExactChunk - 1) / kExactChunk;
     L.status = take(64);
+    L.ctl = take(64);  // the one-grid path's counters: zero between calls
     L.xr = take((size_t)M * r.H * 4);
     L.ahat = take((size_t)M * N * 4);
     L.score = take((size_t)M * N * 4);
@@ -786,7 +1013,32 @@ cudaError_t launch_reader_decode(const ReaderArgs &r, const __nv_bfloat16 *h, in
     cudaError_t err;
     // trace points: 0 before the first kernel, 1 after the scan and sketch scores, 2 after
     // the selection, 3 after the exact reads, 4 after the recovery, 5 after the final sum
+    // (one token: every point after the one grid)
     trace_point(0, stream);
+    const size_t one_smem = reader_one_smem_floats(r.H, N, K) * 4;
+    if (M == 1 && one_smem <= 200 * 1024) {
+        const int npass = (r.H / 32 + 31) / 32;
+        const int dp = (r.H + 2047) / 2048;
+        auto pick = [&](auto mp) {
+            constexpr int kMP = decltype(mp)::value;
+            return dp <= 1 ? reader_one_kernel<kMP, 1> : dp <= 2 ? reader_one_kernel<kMP, 2>
+                                                                 : reader_one_kernel<kMP, 4>;
+        };
+        auto kern = npass <= 1 ? pick(std::integral_constant<int, 1>())
+                  : npass <= 2 ? pick(std::integral_constant<int, 2>())
+                  : npass <= 4 ? pick(std::integral_constant<int, 4>())
+                               : pick(std::integral_constant<int, 8>());
+        err = ensure_smem(reinterpret_cast<const void *>(kern), one_smem);
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg =
+            launch_config(dim3(num_sms()), dim3(kOneThreads), one_smem, stream, attrs, 0);
+        err = cudaLaunchKernelEx(&cfg, kern, r, h, nscan, xr, ids, wts, k, K, ahat, score, sel, nsel,
+                                 L.nchunk, partial, zpart, residual, out,
+                                 reinterpret_cast<int32_t *>(ws + L.ctl),
+                                 reinterpret_cast<int32_t *>(ws + L.status));
+        for (int i = 1; i <= 5; ++i) trace_point(i, stream);
+        return err;
+    }
     {
         // the nibble table and xr
         const size_t smem = ((size_t)nib_table_floats(r.H) + r.H + (size_t)(r.H / 32) * 33) * 4;
