@@ -458,7 +458,70 @@ def per_config_entries(dev, local, min_seconds=0.4, near_inputs=None):
         del ws, out, h0
     cache.clear()
     torch.cuda.empty_cache()
+    entries["reader_m1_M1"] = reader_config_entry(dev, local, min_seconds)
+    torch.cuda.empty_cache()
     return entries
+
+
+def reader_config_entry(dev, local, min_seconds=0.4):
+    """The channel reader at one token (router + reader per layer, 8 rotating weight sets), in
+    its own timed region with clock samples, beside the exact block on the same weights."""
+    from routed_expert_ffn_top_gb300 import moe
+
+    wl = syn.WORKLOADS["reader_m1"]
+    M, K, nscan = wl.M, wl.reader_K, wl.reader_nscan
+    layers, readers = [], []
+    for li in range(8):
+        layer = syn.make_layer(wl, layer=li, seed=1, device=dev)
+        signs = syn.make_rotation_signs(wl.H, seed=li, device=dev)
+        readers.append(moe.reader_build(layer, signs, reader_basis(layer["w_down"], wl.reader_rank)))
+        layers.append(layer)
+    h0 = syn.make_hidden(wl, seed=1, device=dev)
+    out = torch.empty_like(h0)
+    ids = torch.empty((M, wl.k), dtype=torch.int32, device=dev)
+    wts = torch.empty((M, wl.k), dtype=torch.float32, device=dev)
+    ws = moe.reader_workspace(readers[0], M, wl.k, K)
+    ws_exact = moe.alloc_workspace(layers[0], M, wl.k, wl.b, dev)
+
+    def reader_step(i):
+        li = i % len(layers)
+        moe.moe_route_topk(h0, layers[li]["w_router"], layers[li]["bias"], wl.k, topk_ids=ids,
+                           topk_weights=wts)
+        moe.moe_reader_ffn(h0, readers[li], ids, wts, K, nscan, out=out, workspace=ws)
+
+    def exact_step(i):
+        moe.moe_decode_block(h0, layers[i % len(layers)], wl.k, wl.b, out=out, topk_ids=ids,
+                             topk_weights=wts, workspace=ws_exact)
+
+    def timed(step, clocks=False):
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step(0)
+        torch.cuda.synchronize()
+        steps = int(max(10, min(20000, min_seconds / max(time.perf_counter() - t0, 1e-6))))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            torch.cuda.synchronize()
+            ev0.record()
+            for i in range(steps):
+                step(i)
+            ev1.record()
+            torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) * 1e3 / steps, steps, clk.summary()
+
+    us, steps, clocks = timed(reader_step)
+    exact_us, _, _ = timed(exact_step)
+    nvalid = M * wl.k * wl.I
+    kept = M * min(K, wl.k * wl.I)
+    sk_b, ex_b, rc_b = reader_bytes(wl, nvalid, kept)
+    full = M * wl.k * (2 * wl.H * wl.I * 2 + wl.I * wl.H * 2)
+    return {"workload": "reader_m1", "M": M, "reader_K": K, "reader_nscan": nscan,
+            "steps": steps, "us_per_layer": round(us, 3), "tokens_per_s": round(M / (us * 1e-6), 2),
+            "exact_block_us_per_layer": round(exact_us, 3),
+            "bytes_read_fraction_of_routed": round((sk_b + ex_b + rc_b) / full, 4),
+            "gpu_launches": 2 * steps, "clocks": clocks}
 
 
 # ------------------------------------------------------------------------------ ours
