@@ -767,7 +767,8 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
     int32_t *ws_npad = reinterpret_cast<int32_t *>(ws + L.npad);
     SubBlock *ws_sbt = reinterpret_cast<SubBlock *>(ws + L.sbt);
     int32_t *ws_status = reinterpret_cast<int32_t *>(ws + L.status);
-    if (d.gemm && !d.vq_tc && small_fits(M, k, w->E, w->H, b))
+    // (the one grid puts a router CTA on every slice of H: at least 8 SMs)
+    if (d.gemm && !d.vq_tc && small_fits(M, k, w->E, w->H, b) && num_sms() >= kRouterCluster)
         return run_small(h, w_router, bias, w, d, residual, out, topk_ids, topk_weights, ws, L, s);
     LowRankProj lr_store;
     const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store);  // rides in the router launch

@@ -685,7 +685,6 @@ bool small_fits(int M, int k, int E, int H, int b) {
     if (M < 1 || M > kSmallMaxTokens || (int64_t)M * k > kSmallMaxRoutes || b < 1 || b > 16)
         return false;
     if ((size_t)(H / kRouterCluster) * E * 2 > 64 * 1024) return false;  // one router pass
-    if (num_sms() < kRouterCluster) return false;  // at least one CTA per slice
     const int64_t R = (int64_t)M * k;
     const int64_t cap = R + (R < E ? R : E) * (b - 1);
     if (small_routing_bytes(M, H, E) > (size_t)GS::kStages * GS::kStageBytes) return false;
