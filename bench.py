@@ -826,16 +826,20 @@ def run_ours(args, world, rank, local):
     result["e2e"] = {"value": round(M * args.steps * world / t_e2e, 3), "unit": UNIT,
                      "h2d_bytes_per_step": M * wl.H * 2, "d2h_bytes_per_step": M * wl.H * 2}
 
-    # --- the exact-trajectory record: surface hashes of two calls on the same inputs
-    hashes = []
-    for _ in range(2):
-        ws.zero_()
-        o = torch.empty_like(h0)
-        moe.moe_decode_block(h0, layers[0], wl.k, wl.b, out=o, topk_ids=ids, topk_weights=wts,
-                             workspace=ws)
-        torch.cuda.synchronize()
-        hashes.append(surface_hashes(moe, layers[0], wl, M, h0, ws, ids, o))
-    result["surface_hashes"] = dict(hashes[0], repeat_identical=hashes[0] == hashes[1])
+    # --- the exact-trajectory record: surface hashes of two calls on the same inputs (dense
+    # weights: their p is in the tiles or rows the workspace layout names)
+    if wl.kind == syn.W_DENSE:
+        hashes = []
+        for _ in range(2):
+            ws.zero_()
+            o = torch.empty_like(h0)
+            moe.moe_decode_block(h0, layers[0], wl.k, wl.b, out=o, topk_ids=ids,
+                                 topk_weights=wts, workspace=ws)
+            torch.cuda.synchronize()
+            hashes.append(surface_hashes(moe, layers[0], wl, M, h0, ws, ids, o))
+        result["surface_hashes"] = dict(hashes[0], repeat_identical=hashes[0] == hashes[1])
+    else:
+        result["surface_hashes"] = "recorded for dense weights only"
     result["config"]["b_effective"] = moe.moe_library_block_size(layers[0], M, wl.k, wl.b)
     result["config"]["launches_per_layer"] = launches_per_block
 
