@@ -384,8 +384,14 @@ extern "C" size_t moe_workspace_bytes(const moe_expert_weights_t *w, int M, int 
 }
 
 // Kernels one moe_decode_block call launches for these dimensions.
+static bool vq_small_path(const moe_expert_weights_t *w, const Dims &d) {
+    return w->kind == MOE_W_VQ_GATEUP && w->vq_form == 0 && !d.gemm &&
+           vq_small_fits(d.M, d.k, d.E, d.H, d.I, d.b, w->d);
+}
+
 static int block_launches(const moe_expert_weights_t *w, const Dims &d) {
     if (d.gemm && !d.vq_tc && small_fits(d.M, d.k, d.E, d.H, d.b)) return 1;
+    if (vq_small_path(w, d)) return 1;
     const bool fused = router_can_align(d.M, d.k);
     int n = 1 + (fused ? 0 : 1);                                   // router, alignment
     n += (d.gemm && !fused && d.R > kAlignGatherRoutes) ? 1 : 0;   // row gather
@@ -702,6 +708,65 @@ extern "C" int moe_expert_ffn(const void *h, const moe_expert_weights_t *w, int 
 }
 
 // The whole block for a few tokens in one grid (decode_small.cu).
+static int run_vq_small(const void *h, const void *w_router, const float *bias,
+                        const moe_expert_weights_t *w, const Dims &d, const void *residual,
+                        void *out, int32_t *topk_ids, float *topk_weights, unsigned char *ws,
+                        const WsLayout &L, cudaStream_t s) {
+    CUtensorMap tm_gate, tm_up, tm_down;
+    // index maps [E * H/d rows][I] uint8, boxes of 1024/d rows x 64 columns; W_down boxes of
+    // 64 columns x 256 rows
+    if (!make_tmap_2d(&tm_gate, w->j_gate, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                      (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d) ||
+        !make_tmap_2d(&tm_up, w->j_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d.I,
+                      (uint64_t)d.E * (d.H / w->d), kTI, 1024 / w->d) ||
+        !make_tmap_2d(&tm_down, w->w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.H,
+                      (uint64_t)d.E * d.I, kTN, kBoxRows))
+        return MOE_ERR_CUDA;
+    VQSmallArgs a;
+    GemvArgs &g = a.g;
+    g = GemvArgs{};
+    g.h = static_cast<const __nv_bfloat16 *>(h);
+    g.topk_ids = topk_ids;
+    g.topk_wts = topk_weights;
+    g.sbt = reinterpret_cast<const SubBlock *>(ws + L.sbt);
+    g.npad = reinterpret_cast<const int32_t *>(ws + L.npad);
+    g.residual = static_cast<const __nv_bfloat16 *>(residual);
+    g.out = static_cast<__nv_bfloat16 *>(out);
+    g.p = reinterpret_cast<float *>(ws + L.p);
+    g.y = reinterpret_cast<float *>(ws + L.y);
+    g.status = reinterpret_cast<int32_t *>(ws + L.status);
+    g.w_down = static_cast<const unsigned char *>(w->w_down);
+    g.cb_gate = static_cast<const uint2 *>(w->cb_gate);
+    g.cb_up = static_cast<const uint2 *>(w->cb_up);
+    g.M = d.M;
+    g.k = d.k;
+    g.E = d.E;
+    g.H = d.H;
+    g.I = d.I;
+    g.b = d.b;
+    g.rsub = d.rsub;
+    g.n_it = d.n_it;
+    g.n_hb = d.n_hb;
+    g.n_ht = d.n_ht;
+    g.n_ib = d.n_ib;
+    g.n_qb = d.H / (4 * kBoxRows);
+    g.max_sub = d.max_sub;
+    a.w_router = static_cast<const __nv_bfloat16 *>(w_router);
+    a.bias = bias;
+    a.topk_ids = topk_ids;
+    a.topk_wts = topk_weights;
+    a.partials = reinterpret_cast<float *>(ws + L.partials);
+    a.ctl = reinterpret_cast<int32_t *>(ws + L.ctl);
+    a.sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    a.blocks = reinterpret_cast<int32_t *>(ws + L.blocks);
+    a.npad = reinterpret_cast<int32_t *>(ws + L.npad);
+    a.sbt_ws = reinterpret_cast<SubBlock *>(ws + L.sbt);
+    a.cap = d.cap;
+    if (launch_decode_vq_small(tm_gate, tm_up, tm_down, a, s) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int i = 1; i < kTracePoints; ++i) trace(i, s);  // one kernel: every stage ends here
+    return MOE_OK;
+}
+
 static int run_small(const void *h, const void *w_router, const float *bias,
                      const moe_expert_weights_t *w, const Dims &d, const void *residual, void *out,
                      int32_t *topk_ids, float *topk_weights, unsigned char *ws, const WsLayout &L,
@@ -770,6 +835,8 @@ int moe::decode_block(const void *h, const void *w_router, const float *bias,
     // (the one grid puts a router CTA on every slice of H: at least 8 SMs)
     if (d.gemm && !d.vq_tc && small_fits(M, k, w->E, w->H, b) && num_sms() >= kRouterCluster)
         return run_small(h, w_router, bias, w, d, residual, out, topk_ids, topk_weights, ws, L, s);
+    if (vq_small_path(w, d) && num_sms() >= kRouterCluster)
+        return run_vq_small(h, w_router, bias, w, d, residual, out, topk_ids, topk_weights, ws, L, s);
     LowRankProj lr_store;
     const LowRankProj *lr = lowrank_proj(w, d, ws, L, &lr_store);  // rides in the router launch
     cudaError_t err;

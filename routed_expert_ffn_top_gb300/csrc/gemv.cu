@@ -43,6 +43,8 @@
 // depend on M.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "route_core.cuh"
+#include "small_route.cuh"
 
 namespace moe {
 
@@ -346,11 +348,12 @@ __device__ __forceinline__ void stage_partials(float *red, const Lane &ln, float
 // Stages: a gate and an up index box for every 1024 rows of H; with kLR, then a C_gate and
 // a C_up box for every 256 rows of r, multiplied by z = D^T h into the same accumulators
 // ([MED]'s joint accumulation of the VQ and low-rank terms).
-template <int NT, bool kLR, int kD>
+template <int NT, bool kLR, int kD, int kStride = 0>
 __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                             const uint2 *cbs, const Lane &ln, int it, int r0, int r1, int &stage,
                             uint32_t &phase) {
-    constexpr int kSt = kLR ? kStageBytesLR : vq_stage_bytes(kD);
+    // stage stride: the gate/up kernel's own (kStride 0), or a ring shared with down tiles
+    constexpr int kSt = kStride ? kStride : (kLR ? kStageBytesLR : vq_stage_bytes(kD));
     float ag[NT][4], au[NT][4];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
@@ -766,6 +769,405 @@ cudaError_t launch_combine(const GemvArgs &a, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = launch_config(grid, dim3(kCombineThreads), 0, stream, attrs, 0);
     return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)a.y, a.topk_ids, a.topk_wts,
                               a.residual, a.out, a.M, a.k, a.E, a.H);
+}
+
+// ------------------------------------------------------ VQ weights, one or two tokens
+// The whole block for VQ-only gate/up weights (code words of 4) in one persistent grid: the
+// one-grid routing (small_route.cuh, route_core.cuh), the alignment into sub-blocks in every
+// CTA, then units in one ring -- gate/up tiles (sub-block, 64 columns of I) first, then down
+// tiles (sub-block, 64 columns of H) -- with the tile bodies of the two kernels above, so the
+// arithmetic and the bits are those of the multi-kernel path.  A down tile's W_down boxes
+// stream at once; its p slices wait for the sub-block's ready count (each gate/up tile
+// releases it once its p columns are stored).  The down tile that completes a token's routes
+// for its 64 columns forms out = bf16(residual + sum_j a_j y_j), slots in order: the
+// combine kernel's arithmetic.  Counters in the workspace's control region, zero between
+// calls (the last CTA to leave restores them and the routing exchange).
+constexpr int kVQSmallStage = kStageBytesDN;  // one stride for both kinds of stage
+constexpr int kVQSmallMaxSub = 32;            // sub-blocks (cap / rsub) the plan holds
+constexpr int kVQCtlExit = 1, kVQCtlReady = 32;
+static_assert(vq_stage_bytes(4) <= kVQSmallStage, "a gate/up stage fits a down stage");
+
+struct VQSmallState {
+    SubBlock sbt[kVQSmallMaxSub];
+    int32_t ids[kSmallMaxRoutes];
+    float wts[kSmallMaxRoutes];
+    int32_t nvalid[kSmallMaxTokens];
+    int32_t nsub;
+    int32_t comb[kNT];  // per route of the down tile: the token to combine, or -1
+    int32_t last;
+};
+
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu_vq(int32_t *p, int32_t v) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Bounded wait until *p >= need (acquire, GPU scope).
+__device__ __forceinline__ bool vq_count_wait(const int32_t *p, int need, Ctl &ctl) {
+    if (ld_acquire_gpu(p) >= need) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(p) >= need) return true;
+        if (ctl.abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            ctl.abort = 1;
+            return false;
+        }
+    }
+}
+
+struct VQUnit {
+    bool gu;
+    int sub, ct, nst;
+};
+__device__ __forceinline__ VQUnit vq_unit(const GemvArgs &g, int nsub, int u) {
+    VQUnit x;
+    const int Tgu = nsub * g.n_it;
+    x.gu = u < Tgu;
+    const int v = x.gu ? u : u - Tgu;
+    const int n = x.gu ? g.n_it : g.n_ht;
+    x.sub = v / n;
+    x.ct = v - x.sub * n;
+    x.nst = x.gu ? 2 * g.n_qb : g.n_ib;
+    return x;
+}
+
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    decode_vq_small_kernel(const __grid_constant__ CUtensorMap tm_jgate,
+                           const __grid_constant__ CUtensorMap tm_jup,
+                           const __grid_constant__ CUtensorMap tm_down, const VQSmallArgs a) {
+    constexpr int kD = 4;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *stages = base;
+    float *red = reinterpret_cast<float *>(base + kStages * kVQSmallStage);
+    uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kVQSmallStage + kRedBytesGU);
+    Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kVQSmallStage + kRedBytesGU +
+                                        2 * vq_codebook_bytes(kD));
+    VQSmallState &st = *reinterpret_cast<VQSmallState *>(reinterpret_cast<unsigned char *>(&ctl) +
+                                                         ((sizeof(Ctl) + 15) & ~size_t(15)));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const GemvArgs &g0 = a.g;
+    const int M = g0.M, E = g0.E, H = g0.H, k = g0.k, R = M * k;
+
+    const SmallRouteScratch sc = small_route_scratch(stages, M, H, E);
+    const RouterSplit sp = router_split(H, E);
+    const bool router = (int)blockIdx.x < sp.NR;
+    if (threadIdx.x == 0) {
+        init_ring(ctl);
+        prefetch_tensormap(&tm_jgate);
+        prefetch_tensormap(&tm_jup);
+        prefetch_tensormap(&tm_down);
+    }
+    // weights, before the dependency wait: the code books and this CTA's block of W_r
+    constexpr int kCbWords = vq_codebook_bytes(kD) / 8;
+    for (int i = threadIdx.x; i < 2 * kCbWords; i += blockDim.x)
+        cbs[i] = i < kCbWords ? g0.cb_gate[i] : g0.cb_up[i - kCbWords];
+    if (router) small_router_copy(a.w_router, sp, sc.w_s);
+    __syncthreads();
+    pdl_wait();  // h, and the control region, come after the previous grid
+    pdl_launch_dependents();
+
+    // ---------------------------------------------------------------- routing
+    if (router) small_route_dots(g0.h, M, H, E, a.partials, sp, sc);
+    small_route_gather(a.partials, M, E, sc.part_s, &ctl.abort, g0.status);
+    route_finalize_any(sc.part_s, M, E, k, a.bias, !ctl.abort, 1,
+                       [&](int i, int j, int id, float wt) {
+                           st.ids[i * k + j] = id;
+                           st.wts[i * k + j] = wt;
+                           if (blockIdx.x == 0) {
+                               a.topk_ids[(size_t)i * k + j] = id;
+                               a.topk_wts[(size_t)i * k + j] = wt;
+                           }
+                       });
+    __syncthreads();
+    // The alignment as sub-blocks (align_core's order: experts ascending, routes ascending,
+    // each expert padded to a multiple of b; rsub consecutive rows per sub-block), in one
+    // warp with lane r holding route r.
+    if (warp == 0) {
+        const int b = g0.b, rsub = g0.rsub;
+        const int e = lane < R ? st.ids[lane] : -1;
+        const bool valid = lane < R && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int lower = __popc(peers & ((1u << lane) - 1u));
+        const int n = __popc(peers);
+        const bool leader = valid && lower == 0;
+        const int padded = leader ? (n + b - 1) / b * b : 0;
+        int off = 0, total = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const int eq = __shfl_sync(0xffffffffu, e, q);
+            const int pq = __shfl_sync(0xffffffffu, padded, q);
+            total += pq;
+            if (pq != 0 && eq < e) off += pq;
+        }
+        if (leader)
+            for (int sb = off / rsub; sb < (off + padded) / rsub; ++sb) {
+                const int first = sb * rsub - off;
+                SubBlock &rec = st.sbt[sb];
+                rec.e = e;
+                rec.ntok = max(0, min(rsub, n - first));
+                for (int q = rec.ntok; q < kNT; ++q) rec.routes[q] = rec.tokens[q] = -1;
+            }
+        __syncwarp();
+        if (valid) {
+            const int pos = off + lower;
+            st.sbt[pos / rsub].routes[pos % rsub] = lane;
+            st.sbt[pos / rsub].tokens[pos % rsub] = lane / k;
+        }
+        if (lane == 0) st.nsub = total / rsub;
+        if (lane < M) {
+            int nv = 0;
+            for (int j = 0; j < k; ++j) {
+                const int ej = st.ids[lane * k + j];
+                nv += (ej >= 0 && ej < E) ? 1 : 0;
+            }
+            st.nvalid[lane] = nv;
+        }
+    }
+    __syncthreads();
+    const int nsub = st.nsub;
+    // CTA 0 leaves the alignment and the sub-block table in the workspace (as
+    // moe_align_block_size gives them), and out = residual (or zero) for a token with no route
+    if (blockIdx.x == 0) {
+        const int rsub = g0.rsub;
+        for (int64_t i = threadIdx.x; i < a.cap; i += blockDim.x) {
+            const int sb = (int)(i / rsub), q = (int)(i - (int64_t)sb * rsub);
+            a.sorted[i] = (sb < nsub && q < st.sbt[sb].ntok) ? st.sbt[sb].routes[q] : R;
+        }
+        for (int64_t q = threadIdx.x; q < a.cap / g0.b; q += blockDim.x)
+            a.blocks[q] = q * g0.b < (int64_t)nsub * rsub ? st.sbt[q * g0.b / rsub].e : -1;
+        for (int i = threadIdx.x; i < nsub * (int)(sizeof(SubBlock) / 4); i += blockDim.x)
+            reinterpret_cast<int32_t *>(a.sbt_ws)[i] = reinterpret_cast<const int32_t *>(st.sbt)[i];
+        if (threadIdx.x == 0) {
+            a.npad[0] = nsub * rsub;
+            int nv = 0;
+            for (int t = 0; t < M; ++t) nv += st.nvalid[t];
+            if (nv < R) atomicOr(g0.status, MOE_DEV_INVALID_EXPERT);
+        }
+        for (int t = 0; t < M; ++t)
+            if (st.nvalid[t] == 0)
+                for (int c = threadIdx.x; c < H; c += blockDim.x)
+                    g0.out[(size_t)t * H + c] =
+                        g0.residual ? g0.residual[(size_t)t * H + c] : __float2bfloat16(0.0f);
+    }
+    GemvArgs ga = g0;
+    ga.sbt = st.sbt;
+    const int T = nsub * (ga.n_it + ga.n_ht);
+    int32_t *ready = a.ctl + kVQCtlReady;
+    int32_t *done = ready + kVQSmallMaxSub;
+
+    // ---------------------------------------------------------------- experts
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, parity_bits = 0;
+            bool stop = false;
+            for (int u = blockIdx.x; u < T && !stop && !ctl.abort; u += gridDim.x) {
+                const VQUnit x = vq_unit(ga, nsub, u);
+                const SubBlock &rec = st.sbt[x.sub];
+                const int nst = rec.ntok > 0 ? x.nst : 1;
+                for (int j = 0; j < nst; ++j) {
+                    if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) {
+                        stop = true;
+                        break;
+                    }
+                    ctl.meta[stage] = rec;
+                    uint64_t *bar = &ctl.full[stage];
+                    unsigned char *dst = stages + stage * kVQSmallStage;
+                    if (rec.ntok == 0) {
+                        mbar_arrive(bar);
+                    } else if (x.gu) {
+                        mbar_arrive_expect_tx(bar, vq_box_bytes(kD));
+                        tma_load_2d(dst, (j & 1) ? (const void *)&tm_jup : (const void *)&tm_jgate,
+                                    x.ct * kTI, rec.e * (H / kD) + (j >> 1) * vq_rows(kD), bar, pol_w);
+                    } else {
+                        mbar_arrive_expect_tx(bar, kBoxBytes);
+                        tma_load_2d(dst, &tm_down, x.ct * kTN, rec.e * ga.I + j * kBoxRows, bar, pol_w);
+                    }
+                    issued |= 1u << stage;
+                    parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+                    advance(stage, phase);
+                }
+            }
+            for (int s2 = 0; s2 < kStages; ++s2)
+                if ((issued >> s2) & 1u)
+                    if (!mbar_wait_bounded(&ctl.full[s2], (parity_bits >> s2) & 1u)) ctl.abort = 1;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool stop = false;
+        for (int u = blockIdx.x; u < T && !stop && !ctl.abort; u += gridDim.x) {
+            const VQUnit x = vq_unit(ga, nsub, u);
+            const SubBlock &rec = st.sbt[x.sub];
+            const int ntok = rec.ntok;
+            const int nst = ntok > 0 ? x.nst : 1;
+            if (!x.gu && ntok > 0) {  // p of the sub-block: stored by all its gate/up tiles
+                bool ok = true;
+                if (lane == 0) ok = vq_count_wait(ready + x.sub, ga.n_it, ctl);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            }
+            for (int j = 0; j < nst; ++j) {
+                if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl)) {
+                    stop = true;
+                    break;
+                }
+                if (ntok > 0) {
+                    unsigned char *dst = stages + stage * kVQSmallStage;
+                    for (int q = 0; q < ntok; ++q) {
+                        const int route = rec.routes[q], token = rec.tokens[q];
+                        if (x.gu) {  // h rows [1024 (j/2), +1024): four 16-byte pieces per lane
+                            for (int c = 0; c < 4; ++c) {
+                                const int piece = lane * 4 + c;
+                                cp_async_16(dst + vq_box_bytes(kD) + q * kVQHRows * 2 + piece * 16,
+                                            reinterpret_cast<const unsigned char *>(ga.h) +
+                                                ((size_t)token * H + (size_t)(j >> 1) * kVQHRows) * 2 +
+                                                piece * 16);
+                            }
+                        } else {  // p rows [256 j, +256) of the route: two pieces per lane
+                            for (int c = 0; c < 2; ++c) {
+                                const int piece = lane * 2 + c;
+                                cp_async_16(dst + kBoxBytes + q * kBoxRows * 4 + piece * 16,
+                                            reinterpret_cast<const unsigned char *>(ga.p) +
+                                                ((size_t)route * ga.I + (size_t)j * kBoxRows) * 4 +
+                                                piece * 16);
+                            }
+                        }
+                    }
+                    cp_async_mbar_arrive(&ctl.full[stage]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.full[stage]);
+                advance(stage, phase);
+            }
+        }
+        cp_async_wait_all();
+    } else {
+        Lane ln;
+        ln.ctid = threadIdx.x - 32 * kFirstConsumerWarp;
+        ln.cw = warp - kFirstConsumerWarp;
+        ln.lane = lane;
+        ln.half = lane >> 4;
+        ln.c4 = (lane & 15) * 4;
+        ln.rbase = ln.cw * kRowsPerWarp + ln.half * kRowsPerThread;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = blockIdx.x; u < T; u += gridDim.x) {
+            const VQUnit x = vq_unit(ga, nsub, u);
+            if (!wait_or_abort(&ctl.full[stage], phase, ctl)) {
+                named_bar_or(1, kConsumerThreads, true);
+                break;
+            }
+            const SubBlock &mt = ctl.meta[stage];
+            const int ntok = mt.ntok;
+            const int cols = x.gu ? kTI : kTN;
+            const int q0 = ln.ctid / cols, q1 = (ln.ctid + kConsumerThreads) / cols;
+            const int r0 = (q0 < ntok) ? mt.routes[q0] : -1;
+            const int r1 = (q1 < ntok) ? mt.routes[q1] : -1;
+            // the record's slot is reused once the tile's stages are released: keep what the
+            // combine needs (thread q < ntok: the token of route q)
+            const int my_token = ln.ctid < ntok ? mt.tokens[ln.ctid] : -1;
+            bool go = true;
+#define MOE_VQS_TILE(N)                                                                      \
+    case N:                                                                                  \
+        go = x.gu ? gateup_tile<N, false, kD, kVQSmallStage>(ga, ctl, stages, red, cbs, ln,  \
+                                                             x.ct, r0, r1, stage, phase)     \
+                  : down_tile<N>(ga, ctl, stages, red, ln, x.ct, r0, r1, stage, phase);     \
+        break;
+            switch (ntok) {
+                MOE_VQS_TILE(1)
+                MOE_VQS_TILE(2)
+                MOE_VQS_TILE(3)
+                MOE_VQS_TILE(4)
+                MOE_VQS_TILE(5)
+                MOE_VQS_TILE(6)
+                MOE_VQS_TILE(7)
+                MOE_VQS_TILE(8)
+                default:  // an empty sub-block is announced by a single stage
+                    release_stage(ctl, ln, stage, phase);
+                    go = !named_bar_or(1, kConsumerThreads, false);
+            }
+#undef MOE_VQS_TILE
+            if (!go) break;
+            if (ntok == 0) continue;
+            if (x.gu) {
+                // the tile's p columns are stored (the tile body ends with a barrier)
+                if (ln.ctid == 0) red_release_gpu_add(ready + x.sub, 1);
+            } else {
+                // y of the tile's routes is stored: count them per token and 64-column tile;
+                // the route completing its token's valid routes marks the token for the combine
+                if (ln.ctid < ntok) {
+                    const int m = my_token;
+                    const int old = atom_add_acq_rel_gpu_vq(done + m * ga.n_ht + x.ct, 1);
+                    st.comb[ln.ctid] = old + 1 == st.nvalid[m] ? m : -1;
+                }
+                named_bar_sync(1, kConsumerThreads);
+                // out = bf16(residual + sum_j a_j y_j), valid slots in order (the combine)
+                for (int q = 0; q < ntok; ++q) {
+                    const int m = st.comb[q];
+                    if (m < 0 || ln.ctid >= kTN) continue;
+                    const int col = x.ct * kTN + ln.ctid;
+                    float acc = 0.0f;
+                    for (int j = 0; j < k; ++j) {
+                        const int ej = st.ids[m * k + j];
+                        if (ej < 0 || ej >= E) continue;
+                        acc = fmaf(st.wts[m * k + j], __ldcg(ga.y + ((size_t)m * k + j) * H + col), acc);
+                    }
+                    const float res = ga.residual ? __bfloat162float(ga.residual[(size_t)m * H + col]) : 0.0f;
+                    ga.out[(size_t)m * H + col] = __float2bfloat16_rn(res + acc);
+                }
+                named_bar_sync(1, kConsumerThreads);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- exit: restore the region
+    __syncthreads();
+    if (ctl.abort) atomicOr(g0.status, MOE_DEV_WAIT_TIMEOUT);
+    if (threadIdx.x == 0) st.last = atom_add_acq_rel_gpu_vq(a.ctl + kVQCtlExit, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (st.last) {  // every CTA is done with the counters and the partials
+        for (int i = threadIdx.x; i < kVQSmallMaxSub; i += blockDim.x) ready[i] = 0;
+        for (int i = threadIdx.x; i < M * ga.n_ht; i += blockDim.x) done[i] = 0;
+        for (int i = threadIdx.x; i < M * kRouterCluster * E / 4; i += blockDim.x)
+            reinterpret_cast<uint4 *>(a.partials)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (threadIdx.x == 0) a.ctl[kVQCtlExit] = 0;
+    }
+}
+
+static size_t vq_small_smem() {
+    return 1024 + (size_t)kStages * kVQSmallStage + kRedBytesGU + 2 * vq_codebook_bytes(4) +
+           ((sizeof(Ctl) + 15) & ~size_t(15)) + sizeof(VQSmallState);
+}
+
+bool vq_small_fits(int M, int k, int E, int H, int I, int b, int d) {
+    if (d != 4 || M < 1 || M > kSmallMaxTokens || (int64_t)M * k > kSmallMaxRoutes || b < 1 || b > 64)
+        return false;
+    if ((size_t)(H / kRouterCluster) * E * 2 > 64 * 1024) return false;  // one router pass
+    if (small_routing_bytes(M, H, E) > (size_t)kStages * kVQSmallStage) return false;
+    const int64_t R = (int64_t)M * k;
+    const int64_t cap = R + (R < E ? R : E) * (b - 1);
+    const int rsub = b <= kNT ? b : kNT;
+    if (cap / rsub > kVQSmallMaxSub) return false;
+    if (kVQCtlReady + kVQSmallMaxSub + (int64_t)M * (H / kTN) > kSmallCtlInts) return false;
+    return vq_small_smem() <= 227 * 1024;
+}
+
+cudaError_t launch_decode_vq_small(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                                   const CUtensorMap &tm_down, const VQSmallArgs &a,
+                                   cudaStream_t stream) {
+    const size_t smem = vq_small_smem();
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(decode_vq_small_kernel), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(num_sms()), dim3(kGemvThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, decode_vq_small_kernel, tm_jgate, tm_jup, tm_down, a);
 }
 
 }  // namespace moe

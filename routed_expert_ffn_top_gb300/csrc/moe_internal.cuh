@@ -190,6 +190,26 @@ cudaError_t launch_decode_small(const CUtensorMap &tm_gate, const CUtensorMap &t
                                 const CUtensorMap &tm_down, const SmallArgs &a,
                                 cudaStream_t stream);
 
+// The whole block for VQ-only gate/up weights (code words of 4) and one or two tokens in one
+// persistent grid (gemv.cu).
+struct VQSmallArgs {
+    GemvArgs g;  // sbt, p, y, status: the workspace's (sbt is replaced by each CTA's own plan)
+    const __nv_bfloat16 *w_router;
+    const float *bias;
+    int32_t *topk_ids;
+    float *topk_wts;
+    float *partials;  // the routing exchange
+    int32_t *ctl;     // [kVQCtlExit], ready [kVQCtlReady + s], then done [M][H / 64]
+    int32_t *sorted, *blocks, *npad;
+    SubBlock *sbt_ws;  // the workspace's sub-block table (CTA 0 writes the plan there)
+    int64_t cap;
+};
+
+bool vq_small_fits(int M, int k, int E, int H, int I, int b, int d);
+cudaError_t launch_decode_vq_small(const CUtensorMap &tm_jgate, const CUtensorMap &tm_jup,
+                                   const CUtensorMap &tm_down, const VQSmallArgs &a,
+                                   cudaStream_t stream);
+
 cudaError_t launch_gather_rows(const GemmArgs &a, cudaStream_t stream);
 // Gate/up + SiLU and down for dense weights in one persistent grid: a down unit's weights
 // stream while gate/up runs; its p waits on the tile's ready count.
