@@ -291,9 +291,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
     // ---------------------------------------------------------------- 1. routing
     if (router) small_route_dots(a.h, M, H, E, a.partials, sp, sc);
-    small_route_gather(a.partials, M, E, sc.part_s, &ctl.abort, a.status);
+    small_route_gather(a.partials, M, E, a.bias, sc.part_s, &ctl.abort, a.status);
     int my_id = -1;  // lane j of warp t: the expert of token t's slot j
-    route_finalize_any(sc.part_s, M, E, a.k, a.bias, !ctl.abort, 1,
+    route_finalize_any<true>(sc.part_s, M, E, a.k, nullptr, !ctl.abort, 1,
                        [&](int i, int j, int id, float wt) {
                            st.ids[i * a.k + j] = id;
                            st.wts[i * a.k + j] = wt;

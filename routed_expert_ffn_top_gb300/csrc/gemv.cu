@@ -873,8 +873,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
     // ---------------------------------------------------------------- routing
     if (router) small_route_dots(g0.h, M, H, E, a.partials, sp, sc);
-    small_route_gather(a.partials, M, E, sc.part_s, &ctl.abort, g0.status);
-    route_finalize_any(sc.part_s, M, E, k, a.bias, !ctl.abort, 1,
+    small_route_gather(a.partials, M, E, a.bias, sc.part_s, &ctl.abort, g0.status);
+    route_finalize_any<true>(sc.part_s, M, E, k, nullptr, !ctl.abort, 1,
                        [&](int i, int j, int id, float wt) {
                            st.ids[i * k + j] = id;
                            st.wts[i * k + j] = wt;

@@ -29,7 +29,9 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 // slot j holds the j-th largest logit.  Then renorm != 0 gives exp(l_j - l_0) /
 // sum_{j'<k} exp(l_j' - l_0), renorm == 0 the softmax over all E at the selected experts.
 // emit(i, j, id, weight) runs on lane j < k of warp i.
-template <int kPerLane, typename Emit>
+// kLogits: part holds the finished logits [nt][E] (the 8 partials already summed in slice
+// order and the bias added), else the partials as above.
+template <int kPerLane, bool kLogits = false, typename Emit>
 __device__ void route_finalize(const float *part, int nt, int E, int k, const float *bias,
                                bool ok, int renorm, Emit emit) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -43,10 +45,14 @@ __device__ void route_finalize(const float *part, int nt, int E, int k, const fl
         float v = -FLT_MAX;
         key[q] = 0u;  // no candidate
         if (e < E) {
-            v = 0.0f;
+            if (kLogits) {
+                v = part[(size_t)i * E + e];
+            } else {
+                v = 0.0f;
 #pragma unroll
-            for (int s = 0; s < kRouterCluster; ++s) v += part[((size_t)i * kRouterCluster + s) * E + e];
-            if (bias) v += bias[e];
+                for (int s = 0; s < kRouterCluster; ++s) v += part[((size_t)i * kRouterCluster + s) * E + e];
+                if (bias) v += bias[e];
+            }
             if (!ok) v = -FLT_MAX;
             key[q] = order_key(v);
         }
@@ -102,15 +108,15 @@ __device__ void route_finalize(const float *part, int nt, int E, int k, const fl
 }
 
 // route_finalize for any supported E (8 <= E <= 512): experts per lane by E.
-template <typename Emit>
+template <bool kLogits = false, typename Emit>
 __device__ void route_finalize_any(const float *part, int nt, int E, int k, const float *bias,
                                    bool ok, int renorm, Emit emit) {
     if (E <= 128)
-        route_finalize<4>(part, nt, E, k, bias, ok, renorm, emit);
+        route_finalize<4, kLogits>(part, nt, E, k, bias, ok, renorm, emit);
     else if (E <= 256)
-        route_finalize<8>(part, nt, E, k, bias, ok, renorm, emit);
+        route_finalize<8, kLogits>(part, nt, E, k, bias, ok, renorm, emit);
     else
-        route_finalize<16>(part, nt, E, k, bias, ok, renorm, emit);
+        route_finalize<16, kLogits>(part, nt, E, k, bias, ok, renorm, emit);
 }
 
 }  // namespace moe

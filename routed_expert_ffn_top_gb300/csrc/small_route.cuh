@@ -159,7 +159,7 @@ __host__ __device__ constexpr size_t small_routing_bytes(int M, int H, int E) {
 struct SmallRouteScratch {
     uint32_t *w_s;
     __nv_bfloat16 *x_s;
-    float *red, *part_s;  // part_s [M][8][E]: the gathered partials
+    float *red, *part_s;  // part_s [M][E]: the gathered logits (room for [M][8][E])
 };
 __device__ __forceinline__ SmallRouteScratch small_route_scratch(unsigned char *p, int M, int H,
                                                                  int E) {
@@ -194,52 +194,56 @@ __device__ inline void small_route_dots(const __nv_bfloat16 *h, int M, int H, in
         small_router_chunk<2>(partials, E, sp, sc.w_s, sc.x_s, sc.red);
 }
 
-// Every CTA: the 8 slices' partials of every token, polled where they lie -- every load of a
-// thread in flight at once, reloaded until no word of it is zero (not written yet) -- into
-// part_s.  A wait past the limit sets *abort and MOE_DEV_WAIT_TIMEOUT.  Ends with a barrier.
-__device__ inline void small_route_gather(const float *partials, int M, int E, float *part_s,
-                                   volatile int *abort, int32_t *status) {
-    const int n4 = M * kRouterCluster * E / 4, e4n = E / 4;  // at most 4096 = 8 x 512
-    constexpr int kBatch = 8;
-    const uint4 *src = reinterpret_cast<const uint4 *>(partials);
-    uint4 v[kBatch];
-    unsigned pending = 0;
+// Every CTA: the logits of every token from the 8 slices' partials, polled where they lie.
+// Thread t < M * E/4 takes token t / (E/4) and experts 4 (t % (E/4)) .. +3: its 8 slices'
+// loads all in flight at once, reloaded until no word is zero (not written yet), then each
+// logit summed in slice order from zero and the bias added -- the router kernel's order --
+// into logits [M][E].  A wait past the limit sets *abort and MOE_DEV_WAIT_TIMEOUT.  Ends
+// with a barrier.
+__device__ inline void small_route_gather(const float *partials, int M, int E, const float *bias,
+                                          float *logits, volatile int *abort, int32_t *status) {
+    const int e4n = E / 4;
+    const int t = threadIdx.x;
+    if (t < M * e4n) {
+        const int m = t / e4n, e4 = t - m * e4n;
+        const uint4 *src = reinterpret_cast<const uint4 *>(partials);
+        uint4 v[kRouterCluster];
+        unsigned pending = 0;
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-        const int idx = (int)threadIdx.x + i * (int)blockDim.x;
-        if (idx < n4) {
-            v[i] = __ldcg(src + idx);
-            pending |= 1u << i;
+        for (int q = 0; q < kRouterCluster; ++q) {
+            v[q] = __ldcg(src + ((size_t)q * M + m) * e4n + e4);
+            pending |= 1u << q;
         }
-    }
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-            if ((pending >> i) & 1u)
-                if (v[i].x != 0u && v[i].y != 0u && v[i].z != 0u && v[i].w != 0u)
-                    pending &= ~(1u << i);
-        if (pending == 0u || *abort) break;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
-            break;
+            for (int q = 0; q < kRouterCluster; ++q)
+                if ((pending >> q) & 1u)
+                    if (v[q].x != 0u && v[q].y != 0u && v[q].z != 0u && v[q].w != 0u)
+                        pending &= ~(1u << q);
+            if (pending == 0u || *abort) break;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+                break;
+            }
+            __nanosleep(32);
+#pragma unroll
+            for (int q = 0; q < kRouterCluster; ++q)
+                if ((pending >> q) & 1u) v[q] = __ldcg(src + ((size_t)q * M + m) * e4n + e4);
         }
-        __nanosleep(32);
+        float l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-            if ((pending >> i) & 1u) v[i] = __ldcg(src + (int)threadIdx.x + i * (int)blockDim.x);
-    }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-        const int idx = (int)threadIdx.x + i * (int)blockDim.x;
-        if (idx < n4) {
-            const int qt = idx / e4n, e4 = idx - qt * e4n;  // qt = q * M + t
-            const int q = qt / M, t = qt - q * M;
-            reinterpret_cast<float4 *>(part_s + ((size_t)t * kRouterCluster + q) * E)[e4] =
-                make_float4(__uint_as_float(~v[i].x), __uint_as_float(~v[i].y),
-                            __uint_as_float(~v[i].z), __uint_as_float(~v[i].w));
+        for (int q = 0; q < kRouterCluster; ++q) {
+            l[0] += __uint_as_float(~v[q].x);
+            l[1] += __uint_as_float(~v[q].y);
+            l[2] += __uint_as_float(~v[q].z);
+            l[3] += __uint_as_float(~v[q].w);
         }
+        if (bias)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) l[c] += bias[4 * e4 + c];
+        *reinterpret_cast<float4 *>(logits + (size_t)m * E + 4 * e4) = make_float4(l[0], l[1], l[2], l[3]);
     }
     __syncthreads();
 }
