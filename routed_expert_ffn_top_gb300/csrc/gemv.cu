@@ -67,6 +67,11 @@ __host__ __device__ constexpr int vq_rows(int d) { return kVQHRows / d; }
 __host__ __device__ constexpr int vq_box_bytes(int d) { return vq_rows(d) * kTI; }
 __host__ __device__ constexpr int vq_stage_bytes(int d) { return vq_box_bytes(d) + kNT * kVQHRows * 2; }
 __host__ __device__ constexpr int vq_codebook_bytes(int d) { return 256 * d * 2; }  // one projection
+// The VQ-only gate/up kernel keeps kCbReps copies of each code book, entry-major (the copies
+// of an entry side by side), and lane l reads copy l % kCbReps: the 32 lanes' random entries
+// then meet in at most 4 lanes per bank set instead of up to 8 or more (on this GPU a box's
+// decoding was bound by those lookups' bank conflicts).  Same values, same order: same bits.
+constexpr int kCbReps = 8;
 constexpr int kStageBytesVQ = vq_stage_bytes(4);
 // VQ + low-rank gate/up: the ring also carries C boxes (256 rows of r x 64 columns, bf16)
 // with fp32 z slices, the shape of a down stage.
@@ -262,19 +267,20 @@ __device__ __forceinline__ void accumulate_f32_box(const unsigned char *st, cons
 // (bf16 x bf16 -> fp32, H rows ascending).  `cb` is the code book in shared memory, one
 // kD-element code word per 8 (d = 4) or 16 (d = 8) bytes.  A warp owns 1/8 of the box's
 // index rows, a lane half 1/16 of them.
-template <int NT, int kD>
+template <int NT, int kD, int kReps = 1>
 __device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const void *cb,
                                                   const Lane &ln, float (&acc)[NT][4]) {
     constexpr int kRows = vq_rows(kD) / 16;  // index rows per thread: 16 (d = 4), 8 (d = 8)
     const int rb = ln.cw * (2 * kRows) + ln.half * kRows;
     const unsigned char *xs = st + vq_box_bytes(kD) + rb * kD * 2;
+    const int rep = ln.lane % kReps;  // this lane's copy of the code book
 #pragma unroll(kD == 4 ? 2 : 1)  // (deeper unrolling spills registers)
     for (int i = 0; i < kRows; ++i) {
         const uint32_t jw = *reinterpret_cast<const uint32_t *>(st + (rb + i) * kTI + ln.c4);
         if constexpr (kD == 4) {
             uint2 cw[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) cw[c] = static_cast<const uint2 *>(cb)[(jw >> (8 * c)) & 0xffu];
+            for (int c = 0; c < 4; ++c) cw[c] = static_cast<const uint2 *>(cb)[((jw >> (8 * c)) & 0xffu) * kReps + rep];
 #pragma unroll
             for (int q = 0; q < NT; ++q) {
                 const uint2 xv = *reinterpret_cast<const uint2 *>(xs + q * kVQHRows * 2 + i * 8);
@@ -291,7 +297,7 @@ __device__ __forceinline__ void accumulate_vq_box(const unsigned char *st, const
         } else {
             uint4 cw[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) cw[c] = static_cast<const uint4 *>(cb)[(jw >> (8 * c)) & 0xffu];
+            for (int c = 0; c < 4; ++c) cw[c] = static_cast<const uint4 *>(cb)[((jw >> (8 * c)) & 0xffu) * kReps + rep];
 #pragma unroll
             for (int q = 0; q < NT; ++q) {
                 const uint4 xv = *reinterpret_cast<const uint4 *>(xs + q * kVQHRows * 2 + i * 16);
@@ -348,7 +354,7 @@ __device__ __forceinline__ void stage_partials(float *red, const Lane &ln, float
 // Stages: a gate and an up index box for every 1024 rows of H; with kLR, then a C_gate and
 // a C_up box for every 256 rows of r, multiplied by z = D^T h into the same accumulators
 // ([MED]'s joint accumulation of the VQ and low-rank terms).
-template <int NT, bool kLR, int kD, int kStride = 0>
+template <int NT, bool kLR, int kD, int kStride = 0, int kReps = 1>
 __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                             const uint2 *cbs, const Lane &ln, int it, int r0, int r1, int &stage,
                             uint32_t &phase) {
@@ -376,9 +382,9 @@ __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, 
         } else {
             const unsigned char *cb = reinterpret_cast<const unsigned char *>(cbs);
             if (j & 1)
-                accumulate_vq_box<NT, kD>(st, cb + vq_codebook_bytes(kD), ln, au);
+                accumulate_vq_box<NT, kD, kReps>(st, cb + vq_codebook_bytes(kD) * kReps, ln, au);
             else
-                accumulate_vq_box<NT, kD>(st, cb, ln, ag);
+                accumulate_vq_box<NT, kD, kReps>(st, cb, ln, ag);
         }
         release_stage(ctl, ln, stage, phase);
     }
@@ -408,7 +414,7 @@ __device__ bool gateup_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, 
 }
 
 // One down tile with NT routes (first stage already waited for); see gateup_tile.
-template <int NT>
+template <int NT, int kStride = kStageBytesDN>
 __device__ bool down_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, float *red,
                           const Lane &ln, int ht, int r0, int r1, int &stage, uint32_t &phase) {
     float acc[NT][4];
@@ -422,7 +428,7 @@ __device__ bool down_tile(const GemvArgs &a, Ctl &ctl, unsigned char *stages, fl
             failed = true;
             break;
         }
-        accumulate_f32_box<NT>(stages + stage * kStageBytesDN, ln, acc);
+        accumulate_f32_box<NT>(stages + stage * kStride, ln, acc);
         release_stage(ctl, ln, stage, phase);
     }
     if (named_bar_or(1, kConsumerThreads, failed)) return false;
@@ -484,7 +490,7 @@ __device__ void consume_tiles(const GemvArgs &a, Ctl &ctl, unsigned char *stages
         if constexpr (kKind == kDown)                                                        \
             go = down_tile<N>(a, ctl, stages, red, ln, ct, r0, r1, stage, phase);            \
         else                                                                                 \
-            go = gateup_tile<N, kKind == kVQLRGateUp, kD>(                                    \
+            go = gateup_tile<N, kKind == kVQLRGateUp, kD, 0, kKind == kVQGateUp ? kCbReps : 1>( \
                 a, ctl, stages, red, cbs, ln, ct, r0, r1, stage, phase);                     \
         break;
         switch (ntok) {
@@ -545,8 +551,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     unsigned char *stages = base;
     float *red = reinterpret_cast<float *>(base + kStages * kSt);
     uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kSt + kRedBytesGU);
+    constexpr int kReps = kLR ? 1 : kCbReps;
     Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kSt + kRedBytesGU +
-                                        2 * vq_codebook_bytes(kD));
+                                        2 * vq_codebook_bytes(kD) * kReps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -559,10 +566,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         }
     }
     // the layer-shared code books (weights, not produced by an earlier kernel), 8 bytes at
-    // a time: gate's K d-element words, then up's
-    constexpr int kCbWords = vq_codebook_bytes(kD) / 8;
-    for (int i = threadIdx.x; i < 2 * kCbWords; i += blockDim.x)
-        cbs[i] = i < kCbWords ? a.cb_gate[i] : a.cb_up[i - kCbWords];
+    // a time: gate's K d-element words, then up's, kReps copies of each entry side by side
+    constexpr int kCbWords = vq_codebook_bytes(kD) / 8;  // 8-byte words per book
+    constexpr int kEntWords = kD / 4;                     // 8-byte words per entry
+    for (int i = threadIdx.x; i < 2 * kCbWords * kReps; i += blockDim.x) {
+        const int book = i / (kCbWords * kReps), r = i - book * kCbWords * kReps;
+        const int ent = r / (kEntWords * kReps), w = r % kEntWords;
+        const uint2 *src = book ? a.cb_up : a.cb_gate;
+        cbs[i] = src[ent * kEntWords + w];
+    }
     __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
@@ -726,7 +738,7 @@ static size_t down_smem() { return 1024 + kStages * kStageBytesDN + kRedBytesDN 
 
 static size_t gateup_vq_smem(bool lr, int d) {
     return 1024 + kStages * (lr ? kStageBytesLR : vq_stage_bytes(d)) + kRedBytesGU +
-           2 * vq_codebook_bytes(d) + sizeof(Ctl);
+           2 * vq_codebook_bytes(d) * (lr ? 1 : kCbReps) + sizeof(Ctl);
 }
 
 template <bool kLR, int kD>
@@ -782,10 +794,16 @@ cudaError_t launch_combine(const GemvArgs &a, cudaStream_t stream) {
 // for its 64 columns forms out = bf16(residual + sum_j a_j y_j), slots in order: the
 // combine kernel's arithmetic.  Counters in the workspace's control region, zero between
 // calls (the last CTA to leave restores them and the routing exchange).
-constexpr int kVQSmallStage = kStageBytesDN;  // one stride for both kinds of stage
+// One stride for both kinds of stage, sized for at most kSmallMaxTokens routes per sub-block
+// (a sub-block holds one expert, and a token routes to an expert once): a W_down box and two
+// p slices, or an index box and two h slices.  The room left holds kCbReps copies of the
+// code books, as in the gate/up kernel.
+constexpr int kVQSmallStage = 34 * 1024;
 constexpr int kVQSmallMaxSub = 32;            // sub-blocks (cap / rsub) the plan holds
 constexpr int kVQCtlExit = 1, kVQCtlReady = 32;
-static_assert(vq_stage_bytes(4) <= kVQSmallStage, "a gate/up stage fits a down stage");
+static_assert(kBoxBytes + kSmallMaxTokens * kBoxRows * 4 <= kVQSmallStage, "down stage");
+static_assert(vq_box_bytes(4) + kSmallMaxTokens * kVQHRows * 2 <= kVQSmallStage, "gate/up stage");
+static_assert(kSmallMaxTokens <= 2, "the tile bodies below are instantiated for 1 and 2 routes");
 
 struct VQSmallState {
     SubBlock sbt[kVQSmallMaxSub];
@@ -846,7 +864,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     float *red = reinterpret_cast<float *>(base + kStages * kVQSmallStage);
     uint2 *cbs = reinterpret_cast<uint2 *>(base + kStages * kVQSmallStage + kRedBytesGU);
     Ctl &ctl = *reinterpret_cast<Ctl *>(base + kStages * kVQSmallStage + kRedBytesGU +
-                                        2 * vq_codebook_bytes(kD));
+                                        2 * vq_codebook_bytes(kD) * kCbReps);
     VQSmallState &st = *reinterpret_cast<VQSmallState *>(reinterpret_cast<unsigned char *>(&ctl) +
                                                          ((sizeof(Ctl) + 15) & ~size_t(15)));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -862,10 +880,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         prefetch_tensormap(&tm_jup);
         prefetch_tensormap(&tm_down);
     }
-    // weights, before the dependency wait: the code books and this CTA's block of W_r
-    constexpr int kCbWords = vq_codebook_bytes(kD) / 8;
-    for (int i = threadIdx.x; i < 2 * kCbWords; i += blockDim.x)
-        cbs[i] = i < kCbWords ? g0.cb_gate[i] : g0.cb_up[i - kCbWords];
+    // weights, before the dependency wait: the code books (kCbReps copies of each entry side
+    // by side) and this CTA's block of W_r
+    constexpr int kCbWords = vq_codebook_bytes(kD) / 8;  // 8-byte words per book
+    constexpr int kEntWords = kD / 4;                     // 8-byte words per entry
+    for (int i = threadIdx.x; i < 2 * kCbWords * kCbReps; i += blockDim.x) {
+        const int book = i / (kCbWords * kCbReps), r = i - book * kCbWords * kCbReps;
+        const int ent = r / (kEntWords * kCbReps), w = r % kEntWords;
+        cbs[i] = (book ? g0.cb_up : g0.cb_gate)[ent * kEntWords + w];
+    }
     if (router) small_router_copy(a.w_router, sp, sc.w_s);
     __syncthreads();
     pdl_wait();  // h, and the control region, come after the previous grid
@@ -1076,19 +1099,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             bool go = true;
 #define MOE_VQS_TILE(N)                                                                      \
     case N:                                                                                  \
-        go = x.gu ? gateup_tile<N, false, kD, kVQSmallStage>(ga, ctl, stages, red, cbs, ln,  \
-                                                             x.ct, r0, r1, stage, phase)     \
-                  : down_tile<N>(ga, ctl, stages, red, ln, x.ct, r0, r1, stage, phase);     \
+        go = x.gu ? gateup_tile<N, false, kD, kVQSmallStage, kCbReps>(                       \
+                        ga, ctl, stages, red, cbs, ln, x.ct, r0, r1, stage, phase)           \
+                  : down_tile<N, kVQSmallStage>(ga, ctl, stages, red, ln, x.ct, r0, r1,      \
+                                                stage, phase);                               \
         break;
-            switch (ntok) {
+            switch (ntok) {  // (at most kSmallMaxTokens routes per sub-block)
                 MOE_VQS_TILE(1)
                 MOE_VQS_TILE(2)
-                MOE_VQS_TILE(3)
-                MOE_VQS_TILE(4)
-                MOE_VQS_TILE(5)
-                MOE_VQS_TILE(6)
-                MOE_VQS_TILE(7)
-                MOE_VQS_TILE(8)
                 default:  // an empty sub-block is announced by a single stage
                     release_stage(ctl, ln, stage, phase);
                     go = !named_bar_or(1, kConsumerThreads, false);
@@ -1142,7 +1160,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 }
 
 static size_t vq_small_smem() {
-    return 1024 + (size_t)kStages * kVQSmallStage + kRedBytesGU + 2 * vq_codebook_bytes(4) +
+    return 1024 + (size_t)kStages * kVQSmallStage + kRedBytesGU + 2 * vq_codebook_bytes(4) * kCbReps +
            ((sizeof(Ctl) + 15) & ~size_t(15)) + sizeof(VQSmallState);
 }
 
