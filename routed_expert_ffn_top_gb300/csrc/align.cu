@@ -11,15 +11,17 @@
 
 namespace moe {
 
-// Shared-memory ints the alignment kernel uses for (E, R, cap, b): align_core's tables, the
-// staged ids, and the aligned rows and block vector built in shared memory.  Returns 0 when
-// they do not fit (then ids and rows stay in global memory).
+// Shared-memory ints the alignment kernel of kThreads threads uses for (E, R, cap, b):
+// align_core's tables, the staged ids, and the aligned rows and block vector built in shared
+// memory.  Returns 0 when they do not fit (then ids and rows stay in global memory).
+template <int kThreads>
 static int64_t align_kernel_ints(int E, int64_t R, int64_t cap, int b) {
-    const int64_t n = align_smem_ints(E) + R + cap + cap / b + 4;
+    const int64_t n = align_smem_ints<kThreads>(E) + R + cap + cap / b + 4;
     return (R <= kAlignStagedRoutes && n * 4 <= kAlignSmemBytes) ? n : 0;
 }
 
-__global__ void __launch_bounds__(kAlignThreads)
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads)
     align_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int b,
                  int32_t *__restrict__ sorted, int32_t *__restrict__ blocks,
                  int32_t *__restrict__ npad, int64_t cap, SubBlock *sbt, int rsub,
@@ -29,29 +31,45 @@ __global__ void __launch_bounds__(kAlignThreads)
     pdl_launch_dependents();
     const int64_t R = (int64_t)M * k;
     if (!staged) {
-        align_core(ids, R, k, E, b, rsub, sorted, blocks, npad, cap, sbt, status, sm);
+        align_core<kThreads>(ids, R, k, E, b, rsub, sorted, blocks, npad, cap, sbt, status, sm);
         return;
     }
     // Everything in shared memory: the ids are read once with all loads in flight, the rows
     // and the block vector are built there, then leave with coalesced stores; the sub-block
     // records are formed one per thread from the finished rows.
-    int32_t *ids_s = sm + align_smem_ints(E);
+    int32_t *ids_s = sm + align_smem_ints<kThreads>(E);
     int32_t *rows_s = ids_s + R;
     int32_t *blocks_s = rows_s + cap;
 #pragma unroll 8
-    for (int64_t r = threadIdx.x; r < R; r += kAlignThreads) ids_s[r] = ids[r];
+    for (int64_t r = threadIdx.x; r < R; r += kThreads) ids_s[r] = ids[r];
     __syncthreads();
-    align_core(ids_s, R, k, E, b, rsub, rows_s, blocks_s, npad, cap, nullptr, status, sm);
+    align_core<kThreads>(ids_s, R, k, E, b, rsub, rows_s, blocks_s, npad, cap, nullptr, status, sm);
     __syncthreads();
     if (sorted)
-        for (int64_t i = threadIdx.x; i < cap; i += kAlignThreads) sorted[i] = rows_s[i];
+        for (int64_t i = threadIdx.x; i < cap; i += kThreads) sorted[i] = rows_s[i];
     if (blocks)
-        for (int64_t i = threadIdx.x; i < cap / b; i += kAlignThreads) blocks[i] = blocks_s[i];
+        for (int64_t i = threadIdx.x; i < cap / b; i += kThreads) blocks[i] = blocks_s[i];
     if (sbt) {
-        const int64_t total = sm[(3 + kAlignWarps) * E];  // align_core's padded row count
-        for (int64_t sb = threadIdx.x; sb < total / rsub; sb += kAlignThreads)
+        const int64_t total = sm[(3 + kThreads / 32) * E];  // align_core's padded row count
+        for (int64_t sb = threadIdx.x; sb < total / rsub; sb += kThreads)
             build_subblock(rows_s, blocks_s, ids_s, sb, rsub, b, E, R, k, false, status, sbt + sb);
     }
+}
+
+template <int kThreads>
+static cudaError_t launch_align_t(const int32_t *topk_ids, int M, int k, int E, int b,
+                                  int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
+                                  SubBlock *sbt, int rsub, int32_t *status, cudaStream_t stream) {
+    const int64_t R = (int64_t)M * k;
+    const int64_t staged_ints = align_kernel_ints<kThreads>(E, R, cap, b);
+    const size_t smem =
+        (size_t)(staged_ints ? staged_ints : align_smem_ints<kThreads>(E)) * sizeof(int32_t);
+    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(align_kernel<kThreads>), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kThreads), smem, stream, attrs, 0);
+    return cudaLaunchKernelEx(&cfg, align_kernel<kThreads>, topk_ids, M, k, E, b, sorted, blocks,
+                              npad, cap, sbt, rsub, status, staged_ints ? 1 : 0);
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
@@ -71,18 +89,18 @@ __global__ void __launch_bounds__(kAlignThreads)
         build_subblock(sorted, blocks, ids, sb, rsub, b, E, R, k, true, status, sbt + sb);
 }
 
+// One CTA of 256 threads, or of 1024 from kAlignWideRoutes routes (the positions are the
+// same; more threads shorten the passes over the routes and rows).
+constexpr int64_t kAlignWideRoutes = 512;
+
 cudaError_t launch_align(const int32_t *topk_ids, int M, int k, int E, int b, int32_t *sorted,
                          int32_t *blocks, int32_t *npad, int64_t cap, SubBlock *sbt, int rsub,
                          int32_t *status, cudaStream_t stream) {
-    const int64_t R = (int64_t)M * k;
-    const int64_t staged_ints = align_kernel_ints(E, R, cap, b);
-    const size_t smem = (size_t)(staged_ints ? staged_ints : align_smem_ints(E)) * sizeof(int32_t);
-    cudaError_t err = ensure_smem(reinterpret_cast<const void *>(align_kernel), smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attrs[2];
-    cudaLaunchConfig_t cfg = launch_config(dim3(1), dim3(kAlignThreads), smem, stream, attrs, 0);
-    return cudaLaunchKernelEx(&cfg, align_kernel, topk_ids, M, k, E, b, sorted, blocks, npad,
-                              cap, sbt, rsub, status, staged_ints ? 1 : 0);
+    if ((int64_t)M * k >= kAlignWideRoutes)
+        return launch_align_t<1024>(topk_ids, M, k, E, b, sorted, blocks, npad, cap, sbt, rsub,
+                                    status, stream);
+    return launch_align_t<kAlignThreads>(topk_ids, M, k, E, b, sorted, blocks, npad, cap, sbt,
+                                         rsub, status, stream);
 }
 
 // Alignment and row tiles in one launch, for up to kAlignGatherRoutes routes (the tcgen05

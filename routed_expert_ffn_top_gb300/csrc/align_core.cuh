@@ -27,34 +27,39 @@ constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kAlignStagedRoutes = 32768;
 constexpr int kAlignSmemBytes = 200 * 1024;
 
-// Shared-memory ints align_core needs for E experts.
-__host__ __device__ constexpr int align_smem_ints(int E) { return (3 + kAlignWarps) * E + 4; }
+// Shared-memory ints align_core needs for E experts, in a CTA of kThreads threads.
+template <int kThreads = kAlignThreads>
+__host__ __device__ constexpr int align_smem_ints(int E) { return (3 + kThreads / 32) * E + 4; }
 
 // ids: M*k expert ids (global or shared memory); outputs may be NULL except npad.
-// Requires blockDim.x == kAlignThreads and every thread of the CTA to call it.
+// Requires blockDim.x == kThreads and every thread of the CTA to call it.  The positions do
+// not depend on kThreads (a route's rank counts the routes of its expert before it, however
+// the chunks are cut).
 // n rounded up to a multiple of b (mask arithmetic when b is a power of two).
 __device__ __forceinline__ int pad_to(int n, int b) {
     return (b & (b - 1)) == 0 ? (n + b - 1) & ~(b - 1) : (n + b - 1) / b * b;
 }
 
+template <int kThreads = kAlignThreads>
 __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, int b, int rsub,
                                   int32_t *sorted, int32_t *blocks, int32_t *npad, int64_t cap,
                                   SubBlock *sbt, int32_t *status, int32_t *sm) {
+    constexpr int kWarps = kThreads / 32;
     int32_t *cnt = sm;                          // [E]
     int32_t *off = cnt + E;                     // [E] padded row offsets
     int32_t *running = off + E;                 // [E]
-    int32_t *warp_cnt = running + E;            // [kAlignWarps][E]
-    int32_t *misc = warp_cnt + kAlignWarps * E;  // [0] total, [1] invalid flag
+    int32_t *warp_cnt = running + E;            // [kWarps][E]
+    int32_t *misc = warp_cnt + kWarps * E;      // [0] total, [1] invalid flag
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t sentinel = (int32_t)R;
 
-    for (int i = tid; i < (3 + kAlignWarps) * E; i += kAlignThreads) sm[i] = 0;
+    for (int i = tid; i < (3 + kWarps) * E; i += kThreads) sm[i] = 0;
     if (tid == 0) misc[1] = 0;
     __syncthreads();
 
     // (1) counts
     int local_invalid = 0;
-    for (int64_t r = tid; r < R; r += kAlignThreads) {
+    for (int64_t r = tid; r < R; r += kThreads) {
         const int e = ids[r];
         if (e >= 0 && e < E)
             atomicAdd(&cnt[e], 1);
@@ -88,13 +93,13 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
     // Every row starts as a sentinel (coalesced, all threads); the scatter below overwrites
     // the rows of valid routes, so the padding rows and the tail need no per-expert loops.
     if (sorted) {
-        for (int64_t pos = tid; pos < cap; pos += kAlignThreads) sorted[pos] = sentinel;
+        for (int64_t pos = tid; pos < cap; pos += kThreads) sorted[pos] = sentinel;
         __syncthreads();
     }
 
     // (3) stable scatter in ascending route id
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int64_t base = 0; base < R; base += kAlignThreads) {
+    for (int64_t base = 0; base < R; base += kThreads) {
         const int64_t r = base + tid;
         const int e = (r < R) ? ids[r] : -1;
         const bool valid = (e >= 0 && e < E);
@@ -106,7 +111,11 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
         __syncthreads();
         if (valid) {
             int rank = running[e] + lower;
-            for (int w = 0; w < warp; ++w) rank += warp_cnt[w * E + e];
+            int w = 0;
+            for (; w + 4 <= warp; w += 4)  // four counts loaded before they are added
+                rank += warp_cnt[w * E + e] + warp_cnt[(w + 1) * E + e] +
+                        warp_cnt[(w + 2) * E + e] + warp_cnt[(w + 3) * E + e];
+            for (; w < warp; ++w) rank += warp_cnt[w * E + e];
             const int64_t pos = (int64_t)off[e] + rank;
             if (pos < cap) {
                 if (sorted) sorted[pos] = (int32_t)r;
@@ -127,7 +136,7 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
     }
 
     // (4) block vector, sub-block records, tail of the block vector
-    for (int e = tid; e < E; e += kAlignThreads) {
+    for (int e = tid; e < E; e += kThreads) {
         const int n = cnt[e];
         if (n == 0) continue;
         const int padded = pad_to(n, b);
@@ -144,7 +153,7 @@ __device__ inline void align_core(const int32_t *ids, int64_t R, int k, int E, i
             }
     }
     if (blocks)
-        for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += kAlignThreads) blocks[q] = -1;
+        for (int64_t q = (int64_t)total / b + tid; q < cap / b; q += kThreads) blocks[q] = -1;
     if (tid == 0) {
         npad[0] = total;
         if (status && misc[1]) atomicOr(status, MOE_DEV_INVALID_EXPERT);
