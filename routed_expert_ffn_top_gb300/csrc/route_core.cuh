@@ -24,9 +24,9 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 // expert e over slice q of H; lane l owns experts l, l + 32, ... (kPerLane of them,
 // E <= 32 * kPerLane).  The logit is the 8 partials summed in slice order from zero, plus the
 // bias (NULL: none), or -FLT_MAX for every expert when !ok.  Top-k in k rounds of a warp
-// arg-max over order-preserving keys: the largest key, ties to the lower expert id (each lane
-// scans its experts in ascending id, then the lowest id among the lanes at the maximum), so
-// slot j holds the j-th largest logit.  Then renorm != 0 gives exp(l_j - l_0) /
+// arg-max over order-preserving keys: the largest key, ties to the lower expert id (the
+// lowest id among the lanes' candidates at the maximum), so slot j holds the j-th largest
+// logit.  Then renorm != 0 gives exp(l_j - l_0) /
 // sum_{j'<k} exp(l_j' - l_0), renorm == 0 the softmax over all E at the selected experts.
 // emit(i, j, id, weight) runs on lane j < k of warp i.
 // kLogits: part holds the finished logits [nt][E] (the 8 partials already summed in slice
@@ -58,35 +58,52 @@ __device__ void route_finalize(const float *part, int nt, int E, int k, const fl
         }
         vals[q] = v;
     }
-    int my_e = -1;
-    float my_v = -FLT_MAX;
-    for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0u;
-        int bi = -1;
+    // This lane's candidates sorted once, largest key first and the lower expert id first
+    // among equal keys; a round then looks only at each lane's head.  The lowest id at the
+    // warp's largest key is some lane's head (a lane's other experts at that key come after
+    // its head), so the selection is the arg-max described above.
+    uint32_t sk[kPerLane];
+    int sq[kPerLane];
 #pragma unroll
-        for (int q = 0; q < kPerLane; ++q)
-            if (key[q] > bk) {
-                bk = key[q];
-                bi = q;
+    for (int q = 0; q < kPerLane; ++q) {
+        sk[q] = key[q];
+        sq[q] = q;
+    }
+#pragma unroll
+    for (int a = 0; a < kPerLane - 1; ++a)
+#pragma unroll
+        for (int c = 0; c < kPerLane - 1 - a; ++c)
+            if (sk[c] < sk[c + 1] || (sk[c] == sk[c + 1] && sq[c] > sq[c + 1])) {
+                const uint32_t tk = sk[c];
+                sk[c] = sk[c + 1];
+                sk[c + 1] = tk;
+                const int tq = sq[c];
+                sq[c] = sq[c + 1];
+                sq[c + 1] = tq;
             }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t cand = (bi >= 0 && bk == mk) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    int my_e = -1;
+    for (int j = 0; j < k; ++j) {
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, sk[0]);
+        const uint32_t cand =
+            (sk[0] != 0u && sk[0] == mk) ? (uint32_t)(lane + 32 * sq[0]) : 0xffffffffu;
         const uint32_t be = __reduce_min_sync(0xffffffffu, cand);
-        float bv = -FLT_MAX;
-        if (be != 0xffffffffu && (int)(be & 31) == lane) {
-            const int qi = (int)(be >> 5);
+        if (lane == j) my_e = be == 0xffffffffu ? -1 : (int)be;
+        if (be != 0xffffffffu && (int)(be & 31) == lane) {  // taken: the next one moves up
 #pragma unroll
-            for (int q = 0; q < kPerLane; ++q)
-                if (q == qi) {
-                    bv = vals[q];
-                    key[q] = 0u;  // taken
-                }
+            for (int q = 0; q < kPerLane - 1; ++q) {
+                sk[q] = sk[q + 1];
+                sq[q] = sq[q + 1];
+            }
+            sk[kPerLane - 1] = 0u;
         }
-        bv = __shfl_sync(0xffffffffu, bv, (int)(be & 31));
-        if (lane == j) {
-            my_e = be == 0xffffffffu ? -1 : (int)be;
-            my_v = bv;
-        }
+    }
+    // the selected logits, from the lanes that own them
+    float my_v = -FLT_MAX;
+    const int src = my_e >= 0 ? (my_e & 31) : 0;
+#pragma unroll
+    for (int q = 0; q < kPerLane; ++q) {
+        const float t = __shfl_sync(0xffffffffu, vals[q], src);
+        if (my_e >= 0 && (my_e >> 5) == q) my_v = t;
     }
     const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
     float denom;

@@ -129,6 +129,28 @@ def test_align_page_fixture():
     assert np.array_equal(g_srt, o_srt) and np.array_equal(g_blk, o_blk)
 
 
+@pytest.mark.parametrize("M,k", [(63, 8), (64, 8), (171, 3), (256, 8), (300, 6)])
+def test_align_both_cta_sizes_bit_exact(M, k):
+    """The stand-alone alignment runs one CTA of 256 threads below 512 routes and of 1024 from
+    512 on; the positions are the same function of the ids on both sides of the switch, with
+    distinct and repeated experts, invalid ids, and block sizes that do and do not divide
+    the expert counts ([RBM] Section 2.1)."""
+    rng = np.random.default_rng(500 + M * k)
+    for E in (8, 128, 300):
+        for b in (1, 3, 16, 64):
+            for distinct in (True, False):
+                ids = _random_ids(rng, M, k, E, distinct=distinct and k <= E).reshape(M, k)
+                if not distinct:
+                    mask = rng.random(ids.shape) < 0.1
+                    ids[mask] = rng.choice([-1, E, E + 3], size=int(mask.sum()))
+                o_srt, o_blk, o_np = oracle.align(ids, E, b)
+                g_srt, g_blk, g_np = _gpu_align(ids, E, b)
+                case = (M, k, E, b, distinct)
+                assert g_np == o_np, case
+                assert np.array_equal(g_srt, o_srt), case
+                assert np.array_equal(g_blk[:o_blk.size], o_blk), case
+
+
 def test_align_large_and_deterministic():
     rng = np.random.default_rng(7)
     ids = _random_ids(rng, 1024, 8, 256)
