@@ -209,7 +209,8 @@ def gateup_kernel_name(wl) -> str:
 
 
 KERNEL_SOURCES = {
-    "decode_small_kernel": ("decode_small.cu", "gemm_core.cuh", "route_core.cuh", "align_core.cuh"),
+    "decode_small_kernel": ("decode_small.cu", "gemm_core.cuh", "route_core.cuh", "align_core.cuh",
+                            "small_route.cuh"),
     "gemm_fused_kernel": ("gemm_tc05.cu", "gemm_core.cuh"),
     "gemm_gateup_vq_kernel": ("gemm_tc05.cu", "gemm_core.cuh"),
 }
