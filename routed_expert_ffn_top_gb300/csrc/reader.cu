@@ -452,7 +452,8 @@ __device__ void select_token(const float *__restrict__ score, int N, int K, uint
         s_and = ~0u;
         s_or = 0u;
     }
-    for (int d = tid; d < 32 * 256; d += (int)blockDim.x) whist[d] = 0;
+    const int nwh = (int)blockDim.x >> 5;  // one histogram per warp
+    for (int d = tid; d < nwh * 256; d += (int)blockDim.x) whist[d] = 0;
     __syncthreads();
     int nv = 0;
     uint32_t k_and = ~0u, k_or = 0u;  // over the valid keys: their common leading bits
@@ -496,19 +497,19 @@ __device__ void select_token(const float *__restrict__ score, int N, int K, uint
             const int nb = 1 << (hi - lo + 1);  // bins of this pass's digit
             const uint32_t dmask = (uint32_t)nb - 1u;
             int *hist = whist + buf * 32 * 256;
-            int *next = whist + (buf ^ 1) * 32 * 256;
+            int *next = whist + (buf ^ 1) * 32 * 256;  // (sets spaced for 32 warps)
             const int wbase = (tid >> 5) * 256;
             // each warp counts into its own histogram (integer adds commute); the other set
             // is cleared for the next pass meanwhile
             for (int f = tid; f < N; f += (int)blockDim.x)
                 if ((keys[f] & mask) == prefix) atomicAdd(&hist[wbase + ((keys[f] >> lo) & dmask)], 1);
-            for (int d = tid; d < 32 * 256; d += (int)blockDim.x) next[d] = 0;
+            for (int d = tid; d < nwh * 256; d += (int)blockDim.x) next[d] = 0;
             __syncthreads();
             // thread t < nb owns digit nb - 1 - t: its count over the warps, then a scan in
             // descending digit order finds the digit where the count reaches `remaining`
             int c = 0;
             if (tid < nb)
-                for (int w = 0; w < 32; ++w) c += hist[w * 256 + (nb - 1 - tid)];
+                for (int w = 0; w < nwh; ++w) c += hist[w * 256 + (nb - 1 - tid)];
             const int incl = block_scan(c, warp_tot);
             if (tid < nb && c > 0 && incl >= remaining && incl - c < remaining) {
                 s_digit = nb - 1 - tid;
