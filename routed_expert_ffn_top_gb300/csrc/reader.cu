@@ -457,14 +457,23 @@ __device__ void select_token(const float *__restrict__ score, int N, int K, uint
     __syncthreads();
     int nv = 0;
     uint32_t k_and = ~0u, k_or = 0u;  // over the valid keys: their common leading bits
-    for (int f = tid; f < N; f += (int)blockDim.x) {
-        const float s = __ldcg(score + f);
-        const uint32_t key = s >= 0.0f ? __float_as_uint(s) + 1u : 0u;  // invalid / NaN: 0
-        keys[f] = key;
-        nv += key != 0u;
-        if (key != 0u) {
-            k_and &= key;
-            k_or |= key;
+    const int nthr = (int)blockDim.x;
+    for (int f0 = tid; f0 < N; f0 += 8 * nthr) {  // 8 scores' loads in flight at once
+        float sv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sv[u] = f0 + u * nthr < N ? __ldcg(score + f0 + u * nthr) : -1.0f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int f = f0 + u * nthr;
+            if (f >= N) break;
+            const float s = sv[u];
+            const uint32_t key = s >= 0.0f ? __float_as_uint(s) + 1u : 0u;  // invalid / NaN: 0
+            keys[f] = key;
+            nv += key != 0u;
+            if (key != 0u) {
+                k_and &= key;
+                k_or |= key;
+            }
         }
     }
     atomicAdd(&s_nvalid, nv);
