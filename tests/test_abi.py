@@ -230,6 +230,31 @@ def test_workspace_layout_without_gpu(lib):
     assert L.moe_workspace_layout(ctypes.byref(d), 1, 8, 8, None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_kernel_counts_per_path_without_gpu(lib):
+    """moe_workspace_layout's `launches`: the kernels one moe_decode_block call launches, which
+    the bench multiplies into its launch count.  Expected per path: dense weights at one or two
+    tokens, blocks of at most 16 rows: the whole block in one grid; up to 128 routes: router,
+    alignment with the row tiles, the fused expert grid, combine; above: router, alignment,
+    row gather, fused grid, combine; one token with 32-row blocks: the router aligns and writes
+    the rows itself.  VQ weights with code words of 4 at one or two tokens: one grid; else
+    router (aligning at one or two tokens), alignment, gate/up, down, combine."""
+    L = moe.lib()
+    out = moe.WorkspaceLayout()
+    d = _weights()
+    for M, b, want in ((1, 8, 1), (2, 16, 1), (3, 16, 4), (16, 16, 4), (21, 8, 5), (256, 64, 5),
+                       (1, 32, 3)):
+        assert L.moe_workspace_layout(ctypes.byref(d), M, 8, b, ctypes.byref(out)) == moe.MOE_OK
+        assert out.launches == want, (M, b, out.launches)
+        assert (out.p_rows > 0) == (want == 1), (M, b)  # p rows: the one-grid path's only
+    v = _weights(kind=moe.MOE_W_VQ_GATEUP)
+    for M, want in ((1, 1), (2, 1), (4, 5), (16, 5)):
+        assert L.moe_workspace_layout(ctypes.byref(v), M, 8, 8, ctypes.byref(out)) == moe.MOE_OK
+        assert out.launches == want, (M, out.launches)
+    v.d = 8  # no one-grid path for code words of 8
+    assert L.moe_workspace_layout(ctypes.byref(v), 1, 8, 8, ctypes.byref(out)) == moe.MOE_OK
+    assert out.launches == 4
+
+
 def test_vq_form_validation_without_gpu(lib):
     L = moe.lib()
     w = _weights(kind=moe.MOE_W_VQ_GATEUP)
